@@ -1,0 +1,435 @@
+"""CPU oracle for asymmetric low-bit KV-cache quantization and decode attention.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this module.  It shares no code with the
+CUDA path and imports nothing from it.
+
+Everything here is the plain definition, written for a reader to check against
+the pages by eye:
+
+* Uniform asymmetric integer quantization per group (ihal.it article,
+  paragraph 3): a group's range [min, max] is divided into the 2^b levels of a
+  b-bit code, with a scale factor and a zero point per group.
+* Grouping axes (same article, paragraphs 1, 4-6): keys are grouped per
+  channel (one channel over 32 consecutive tokens), values per token (32
+  consecutive channels of one token), group size 32.
+* Recent tokens kept in full precision (same article, paragraph 8): tokens that
+  do not yet fill a 32-token key group stay in an fp16 tail and are quantized
+  in groups once enough have arrived.
+* Decode attention (same article, paragraphs 2 and 6): the output is a
+  softmax-weighted sum of value vectors over every cached token, computed here
+  in float64 over the dequantized cache.
+* The mixed-width packed layout (RDKV summary, gist.science 2605.08317,
+  sections 2.1-2.2 and "2.2 TriZone"): widths {0,2,4,8,16} per V token, width
+  0 = evicted, 16 = kept in fp16; K channels at {2,4,8} bits for kept tokens
+  only; rows grouped by width; fresh tokens fp16.
+
+Readings taken where the pages are silent (all of them are listed in the
+design notes of the repository):
+
+* scale = fp16( fp32(max - min) / (2^b - 1) ), zero = fp16(min); both -0 -> +0.
+* code = clamp( rint_half_even( (fp32(x) - fp32(zero_h)) / fp32(scale_h) ),
+  0, 2^b - 1 ) with every fp32 operation rounded to nearest even, computed
+  against the STORED fp16 scale and zero; a zero stored scale gives code 0.
+* dequantized value = fp64(zero_h) + fp64(scale_h) * code (exact in fp64).
+* An empty context (no cached token) gives an all-zero output.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+
+GROUP = 32
+F16 = np.float16
+F32 = np.float32
+F64 = np.float64
+
+
+# ---------------------------------------------------------------------------
+# Quantizer (ihal.it article, paragraph 3: range split into 2^b levels with a
+# scale factor and zero point per group).
+# ---------------------------------------------------------------------------
+def quantize_groups(x16: np.ndarray, bits: int):
+    """Quantize groups along the last axis.
+
+    x16: float16 [..., n] (n = 32 for full groups; fewer for a partial group).
+    Returns (codes uint8 [..., n], scale float16 [...], zero float16 [...]).
+    """
+    if bits not in (2, 4, 8):
+        raise ValueError(f"bits must be 2, 4 or 8, got {bits}")
+    x16 = np.asarray(x16, dtype=F16)
+    x = x16.astype(F32)
+    if not np.all(np.isfinite(x)):
+        raise ValueError("inputs must be finite")
+    # 1. group min / max, as fp32 values (exact for fp16 inputs)
+    mn = x.min(axis=-1)
+    mx = x.max(axis=-1)
+    # 2. range and scale in IEEE fp32, round to nearest even
+    rng = (mx - mn).astype(F32)
+    scale32 = (rng / F32(2 ** bits - 1)).astype(F32)
+    # 3. stored fp16 scale and zero point, -0 canonicalised to +0
+    scale_h = scale32.astype(F16)
+    zero_h = mn.astype(F16)
+    scale_h = np.where(scale_h == 0, F16(0.0), scale_h).astype(F16)
+    zero_h = np.where(zero_h == 0, F16(0.0), zero_h).astype(F16)
+    # 4. codes against the stored scale and zero, fp32 subtract and divide,
+    #    round half to even, clamp to [0, 2^b - 1]; zero scale -> code 0
+    s = scale_h.astype(F32)[..., None]
+    z = zero_h.astype(F32)[..., None]
+    diff = (x - z).astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quot = (diff / s).astype(F32)
+    code = np.rint(quot)
+    code = np.clip(code, 0, 2 ** bits - 1)
+    code = np.where(s == 0, 0.0, code)
+    return code.astype(np.uint8), scale_h, zero_h
+
+
+def dequantize(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """x_hat = zero + scale * code, in float64 (exact).  scale/zero broadcast
+    against codes' last axis the way quantize_groups produced them."""
+    return zero.astype(F64)[..., None] + scale.astype(F64)[..., None] * codes.astype(F64)
+
+
+def quantize_keys(k16: np.ndarray, bits: int):
+    """Keys, per channel over 32-token spans (article, paragraph 4).
+
+    k16: float16 [..., n, D] with n a multiple of 32.
+    Returns codes uint8 [..., n, D], scale/zero float16 [..., n/32, D].
+    """
+    *lead, n, d = k16.shape
+    if n % GROUP:
+        raise ValueError("key groups need whole 32-token spans")
+    x = k16.reshape(*lead, n // GROUP, GROUP, d)
+    x = np.swapaxes(x, -1, -2)  # [..., G, D, 32]: one channel over 32 tokens
+    c, s, z = quantize_groups(x, bits)
+    c = np.swapaxes(c, -1, -2).reshape(*lead, n, d)
+    return c, s, z
+
+
+def dequantize_keys(codes, scale, zero) -> np.ndarray:
+    """Inverse view of quantize_keys, float64 [..., n, D]."""
+    *lead, n, d = codes.shape
+    c = np.swapaxes(codes.reshape(*lead, n // GROUP, GROUP, d), -1, -2)
+    x = dequantize(c, scale, zero)  # [..., G, D, 32]
+    return np.swapaxes(x, -1, -2).reshape(*lead, n, d)
+
+
+def quantize_values(v16: np.ndarray, bits: int):
+    """Values, per token over 32-channel spans (article, paragraphs 5-6).
+
+    v16: float16 [..., n, D] with D a multiple of 32.
+    Returns codes uint8 [..., n, D], scale/zero float16 [..., n, D/32].
+    """
+    *lead, n, d = v16.shape
+    x = v16.reshape(*lead, n, d // GROUP, GROUP)
+    c, s, z = quantize_groups(x, bits)
+    return c.reshape(*lead, n, d), s, z
+
+
+def dequantize_values(codes, scale, zero) -> np.ndarray:
+    *lead, n, d = codes.shape
+    x = dequantize(codes.reshape(*lead, n, d // GROUP, GROUP), scale, zero)
+    return x.reshape(*lead, n, d)
+
+
+# ---------------------------------------------------------------------------
+# Decode attention (article, paragraphs 2 and 6): one query per head attends to
+# every cached token; output = softmax-weighted sum of value vectors.
+# ---------------------------------------------------------------------------
+def decode_attention(q16: np.ndarray, keys: np.ndarray, values: np.ndarray,
+                     sm_scale: float) -> np.ndarray:
+    """q16: float16 [Hq, D]; keys/values: float64 [Hkv, N, D].  Query head h reads
+    KV head h // (Hq / Hkv).  Returns float64 [Hq, D]."""
+    hq, d = q16.shape
+    hkv = keys.shape[0]
+    group = hq // hkv
+    out = np.zeros((hq, d), dtype=F64)
+    if keys.shape[1] == 0:
+        return out
+    for h in range(hq):
+        kh = h // group
+        logits = sm_scale * (keys[kh] @ q16[h].astype(F64))
+        p = np.exp(logits - logits.max())
+        p /= p.sum()
+        out[h] = p @ values[kh]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Uniform cache state: tokens [0, n_quant) quantized in 32-token groups, tokens
+# [n_quant, n_quant + n_tail) kept fp16 (article, paragraph 8).
+# ---------------------------------------------------------------------------
+def split_sequence(seq_len: int, n_tail: int):
+    n_quant = seq_len - n_tail
+    if n_quant < 0 or n_quant % GROUP:
+        raise ValueError("quantized region must be a whole number of 32-token groups")
+    return n_quant
+
+
+def quantize_sequence(k16: np.ndarray, v16: np.ndarray, seq_len: int, n_tail: int,
+                      bits: int) -> dict:
+    """One sequence.  k16/v16: float16 [T, Hkv, D] (T >= seq_len).
+    Returns per-head arrays (leading axis Hkv)."""
+    n_quant = split_sequence(seq_len, n_tail)
+    k = np.ascontiguousarray(np.swapaxes(k16[:seq_len], 0, 1))  # [Hkv, T, D]
+    v = np.ascontiguousarray(np.swapaxes(v16[:seq_len], 0, 1))
+    kc, ks, kz = quantize_keys(k[:, :n_quant], bits)
+    vc, vs, vz = quantize_values(v[:, :n_quant], bits)
+    return {
+        "bits": bits, "n_quant": n_quant, "n_tail": n_tail,
+        "k_codes": kc, "k_scale": ks, "k_zero": kz,
+        "v_codes": vc, "v_scale": vs, "v_zero": vz,
+        "k_tail": k[:, n_quant:seq_len], "v_tail": v[:, n_quant:seq_len],
+    }
+
+
+def sequence_kv(state: dict):
+    """Dequantized keys and values of a sequence, float64 [Hkv, n, D]: the
+    quantized region followed by the fp16 tail (exact in float64)."""
+    kq = dequantize_keys(state["k_codes"], state["k_scale"], state["k_zero"])
+    vq = dequantize_values(state["v_codes"], state["v_scale"], state["v_zero"])
+    keys = np.concatenate([kq, state["k_tail"].astype(F64)], axis=1)
+    values = np.concatenate([vq, state["v_tail"].astype(F64)], axis=1)
+    return keys, values
+
+
+def sequence_attention(q16: np.ndarray, state: dict, sm_scale: float) -> np.ndarray:
+    keys, values = sequence_kv(state)
+    return decode_attention(q16, keys, values, sm_scale)
+
+
+def append_lengths(n_quant: int, n_tail: int, tail_cap: int):
+    """Lengths after appending one token (article, paragraph 8): when the tail
+    is full, its oldest 32 tokens become the next quantized group first."""
+    flushed = n_tail == tail_cap
+    if flushed:
+        n_quant += GROUP
+        n_tail -= GROUP
+    return n_quant, n_tail + 1, flushed
+
+
+# ---------------------------------------------------------------------------
+# Packed byte layout of the uniform cache.  The pages fix no bit layout; this is
+# the library's own, written out from its specification:
+#
+# A tile holds the codes of 32 consecutive tokens x D channels at b bits.  It is
+# cut into 32 lanes (gid = lane // 4, tig = lane % 4).  Each lane owns D/2 code
+# PAIRS, enumerated in this order:
+#   K tile: for kt in [0, D/16), mt in [0, 2), i in [0, 4):
+#             token t = 16*mt + gid + 8*(i % 2), channel d = 16*kt + 2*tig + 8*(i // 2)
+#             pair = (code[t][d], code[t][d + 1])
+#   V tile: for mt in [0, D/16), kt in [0, 2), i in [0, 4):
+#             channel d = 16*mt + gid + 8*(i % 2), token t = 16*kt + 2*tig + 8*(i // 2)
+#             pair = (code[t][d], code[t + 1][d])
+# Pair P of a lane goes to the lane's word P // (16/b), slot k = P % (16/b): the
+# first code at bits [b*k, b*k + b), the second at bits [16 + b*k, 16 + b*k + b).
+# A lane's word w sits at byte ((w // 4) * 32 + lane) * 16 + (w % 4) * 4 of the
+# tile, little-endian.  Tile bytes: 32 * D * b / 8.
+#
+# Metadata: K, per group, float16 [2][D] = (scale[channel], zero[channel]);
+# V, per 32-token tile, float16 [2][D/32][32] = (scale[j][t], zero[j][t]) for
+# channel group j and token t of the tile.
+# ---------------------------------------------------------------------------
+@functools.lru_cache(maxsize=None)
+def tile_code_positions(kind: str, d: int, bits: int):
+    """Word index and bit offset of every code of a 32 x D tile.
+    Returns (word int64 [32, D], bit int64 [32, D])."""
+    if kind not in ("K", "V"):
+        raise ValueError(kind)
+    per_word = 16 // bits
+    word = np.full((GROUP, d), -1, dtype=np.int64)
+    bit = np.full((GROUP, d), -1, dtype=np.int64)
+    for lane in range(32):
+        gid, tig = lane // 4, lane % 4
+        pairs = []
+        if kind == "K":
+            for kt in range(d // 16):
+                for mt in range(2):
+                    for i in range(4):
+                        t = 16 * mt + gid + 8 * (i % 2)
+                        c = 16 * kt + 2 * tig + 8 * (i // 2)
+                        pairs.append(((t, c), (t, c + 1)))
+        else:
+            for mt in range(d // 16):
+                for kt in range(2):
+                    for i in range(4):
+                        c = 16 * mt + gid + 8 * (i % 2)
+                        t = 16 * kt + 2 * tig + 8 * (i // 2)
+                        pairs.append(((t, c), (t + 1, c)))
+        for p, (first, second) in enumerate(pairs):
+            w, k = p // per_word, p % per_word
+            gword = ((w // 4) * 32 + lane) * 4 + (w % 4)
+            for (t, c), off in ((first, bits * k), (second, 16 + bits * k)):
+                assert word[t, c] == -1, "layout must place each code once"
+                word[t, c] = gword
+                bit[t, c] = off
+    assert (word >= 0).all()
+    word.setflags(write=False)
+    bit.setflags(write=False)
+    return word, bit
+
+
+def tile_bytes(d: int, bits: int) -> int:
+    return GROUP * d * bits // 8
+
+
+def pack_tiles(codes: np.ndarray, kind: str, bits: int) -> np.ndarray:
+    """codes uint8 [..., 32, D] (token, channel) -> packed uint8 [..., 32*D*b/8]."""
+    *lead, n, d = codes.shape
+    assert n == GROUP
+    word, bit = tile_code_positions(kind, d, bits)
+    n_words = GROUP * d * bits // 32
+    flat = codes.reshape(*lead, GROUP * d).astype(np.uint32)
+    w_flat, b_flat = word.ravel(), bit.ravel()
+    # every code ORs into its own bit field of its word (fields never overlap)
+    order = np.argsort(w_flat, kind="stable")
+    per = 32 // bits
+    gathered = flat[..., order].reshape(*lead, n_words, per)
+    shifts = b_flat[order].reshape(n_words, per).astype(np.uint32)
+    out = np.ascontiguousarray(np.bitwise_or.reduce(gathered << shifts, axis=-1), dtype="<u4")
+    return out.view(np.uint8).reshape(*lead, n_words * 4)
+
+
+def unpack_tiles(packed: np.ndarray, kind: str, d: int, bits: int) -> np.ndarray:
+    """Inverse of pack_tiles: packed uint8 [..., 32*D*b/8] -> codes uint8 [..., 32, D]."""
+    *lead, nb = packed.shape
+    words = np.ascontiguousarray(packed).view("<u4").astype(np.uint32)
+    word, bit = tile_code_positions(kind, d, bits)
+    vals = (words[..., word] >> bit.astype(np.uint32)) & np.uint32(2 ** bits - 1)
+    return vals.astype(np.uint8)
+
+
+def uniform_buffers(states: list, n_groups_cap: int, tail_cap: int) -> dict:
+    """Expected device buffers for a batch of sequence states (quantize_sequence
+    output), in the library's uniform layout.  Unused groups / tail slots are 0;
+    tests compare only the valid region.  Tail tokens sit at ring slots
+    0 .. n_tail-1 (ring head 0), as prefill leaves them."""
+    b = len(states)
+    hkv, _, d = states[0]["k_codes"].shape
+    bits = states[0]["bits"]
+    tb = tile_bytes(d, bits)
+    out = {
+        "k_codes": np.zeros((b, hkv, n_groups_cap, tb), np.uint8),
+        "v_codes": np.zeros((b, hkv, n_groups_cap, tb), np.uint8),
+        "k_meta": np.zeros((b, hkv, n_groups_cap, 2, d), F16),
+        "v_meta": np.zeros((b, hkv, n_groups_cap, 2, d // GROUP, GROUP), F16),
+        "k_tail": np.zeros((b, hkv, tail_cap, d), F16),
+        "v_tail": np.zeros((b, hkv, tail_cap, d), F16),
+        "n_quant": np.zeros((b,), np.int32),
+        "n_tail": np.zeros((b,), np.int32),
+    }
+    for i, st in enumerate(states):
+        g = st["n_quant"] // GROUP
+        nt = st["n_tail"]
+        out["n_quant"][i] = st["n_quant"]
+        out["n_tail"][i] = nt
+        if g:
+            kc = st["k_codes"].reshape(hkv, g, GROUP, d)
+            vc = st["v_codes"].reshape(hkv, g, GROUP, d)
+            out["k_codes"][i, :, :g] = pack_tiles(kc, "K", bits)
+            out["v_codes"][i, :, :g] = pack_tiles(vc, "V", bits)
+            out["k_meta"][i, :, :g, 0] = st["k_scale"]
+            out["k_meta"][i, :, :g, 1] = st["k_zero"]
+            vs = st["v_scale"].reshape(hkv, g, GROUP, d // GROUP)
+            vz = st["v_zero"].reshape(hkv, g, GROUP, d // GROUP)
+            out["v_meta"][i, :, :g, 0] = np.swapaxes(vs, -1, -2)
+            out["v_meta"][i, :, :g, 1] = np.swapaxes(vz, -1, -2)
+        out["k_tail"][i, :, :nt] = st["k_tail"]
+        out["v_tail"][i, :, :nt] = st["v_tail"]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Mixed-width cache (RDKV summary, sections 2.1-2.2 and "2.2 TriZone").
+#
+# Per (sequence, KV head): every old token t has a V width in {0,2,4,8,16}
+# (0 = evicted, 16 = fp16) and every channel d a K width in {2,4,8}; K is kept
+# only for kept tokens.  Kept tokens are grouped by V width (stable, widths in
+# ascending order), and each width class is cut into consecutive 32-token
+# blocks (the last block of a class may be partial), so every block has one V
+# width.  A block's V rows are quantized per token over 32-channel spans at the
+# block's width (width 16: fp16 rows).  A block's K is quantized per channel
+# over the block's tokens at that channel's width.  Fresh tokens stay fp16.
+# ---------------------------------------------------------------------------
+TRIZONE_V_WIDTHS = (2, 4, 8, 16)
+TRIZONE_K_WIDTHS = (2, 4, 8)
+
+
+def trizone_blocks(v_width: np.ndarray):
+    """Stream order of the kept old tokens: list of (width, token indices)."""
+    blocks = []
+    for w in TRIZONE_V_WIDTHS:
+        toks = np.nonzero(v_width == w)[0]
+        for i in range(0, len(toks), GROUP):
+            blocks.append((w, toks[i:i + GROUP]))
+    return blocks
+
+
+def trizone_quantize(k16: np.ndarray, v16: np.ndarray, v_width: np.ndarray,
+                     k_width: np.ndarray) -> dict:
+    """One (sequence, KV head).  k16/v16: float16 [T, D]; the first len(v_width)
+    tokens are old, the rest fresh."""
+    t_old = len(v_width)
+    d = k16.shape[1]
+    out_blocks = []
+    for w, toks in trizone_blocks(v_width):
+        kb = k16[toks]  # [n, D]
+        blk = {"width": int(w), "tokens": toks,
+               "k_codes": np.zeros((len(toks), d), np.uint8),
+               "k_scale": np.zeros((d,), F16), "k_zero": np.zeros((d,), F16)}
+        for kw in TRIZONE_K_WIDTHS:
+            ch = np.nonzero(k_width == kw)[0]
+            if len(ch) == 0:
+                continue
+            c, s, z = quantize_groups(kb[:, ch].T, kw)  # one group per channel
+            blk["k_codes"][:, ch] = c.T
+            blk["k_scale"][ch] = s
+            blk["k_zero"][ch] = z
+        if w == 16:
+            blk["v_fp16"] = v16[toks]
+        else:
+            c, s, z = quantize_values(v16[toks], w)
+            blk.update(v_codes=c, v_scale=s, v_zero=z)
+        out_blocks.append(blk)
+    return {"blocks": out_blocks, "fresh_k": k16[t_old:], "fresh_v": v16[t_old:],
+            "k_width": k_width, "t_old": t_old}
+
+
+def trizone_kv(tz: dict):
+    """Dequantized keys/values float64 [n, D] of the kept old tokens in ORIGINAL
+    token order, followed by the fresh tokens."""
+    d = tz["fresh_k"].shape[1]
+    kept, keys, values = [], [], []
+    for blk in tz["blocks"]:
+        khat = (blk["k_zero"].astype(F64)[None, :]
+                + blk["k_scale"].astype(F64)[None, :] * blk["k_codes"].astype(F64))
+        if blk["width"] == 16:
+            vhat = blk["v_fp16"].astype(F64)
+        else:
+            vhat = dequantize_values(blk["v_codes"], blk["v_scale"], blk["v_zero"])
+        kept.append(blk["tokens"])
+        keys.append(khat)
+        values.append(vhat)
+    if kept:
+        order = np.argsort(np.concatenate(kept), kind="stable")
+        keys = np.concatenate(keys)[order]
+        values = np.concatenate(values)[order]
+    else:
+        keys = np.zeros((0, d))
+        values = np.zeros((0, d))
+    keys = np.concatenate([keys, tz["fresh_k"].astype(F64)])
+    values = np.concatenate([values, tz["fresh_v"].astype(F64)])
+    return keys, values
+
+
+def trizone_attention(q16: np.ndarray, tz_heads: list, sm_scale: float) -> np.ndarray:
+    """q16 float16 [Hq, D]; tz_heads: trizone_quantize output per KV head."""
+    kv = [trizone_kv(tz) for tz in tz_heads]
+    out = np.zeros(q16.shape, dtype=F64)
+    group = q16.shape[0] // len(tz_heads)
+    for kh, (keys, values) in enumerate(kv):
+        sl = slice(kh * group, (kh + 1) * group)
+        out[sl] = decode_attention(q16[sl], keys[None], values[None], sm_scale)
+    return out

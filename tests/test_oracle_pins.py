@@ -1,0 +1,427 @@
+"""Pins for the CPU oracle against facts other than its own formula.
+
+Every check here comes from outside the oracle's code: exact rational brute
+force, hand-derived closed forms, invariants the definition implies, a library
+routine (torch scaled_dot_product_attention in float64) on the special cases
+that reduce to it, and bit positions derived by hand from the PTX ISA's
+m16n8k16 fragment tables.  A dropped term, a wrong rounding rule, the fp32
+scale in place of the stored fp16 one, a missing clamp or a transposed operand
+each fail at least one test below.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvq_oracle as O
+from quantized_kv_cache_11_gb300 import synthetic as S
+
+F16 = np.float16
+
+
+def _fr(x) -> Fraction:
+    return Fraction(float(x))
+
+
+# ---------------------------------------------------------------- closed forms
+def test_closed_form_exact_grid_2bit():
+    # min 0, max 1.5, 2-bit: scale = 1.5 / 3 = 0.5 exactly, zero = 0, code = x / 0.5
+    x = np.array([0.0, 0.5, 1.0, 1.5] * 8, dtype=F16)
+    c, s, z = O.quantize_groups(x, 2)
+    assert float(s) == 0.5 and float(z) == 0.0
+    assert c.tolist() == [0, 1, 2, 3] * 8
+
+
+def test_closed_form_integers_4bit_and_8bit():
+    x = np.array(list(range(16)) + list(range(15, -1, -1)), dtype=F16) - F16(3)
+    c, s, z = O.quantize_groups(x, 4)
+    assert float(s) == 1.0 and float(z) == -3.0
+    assert c.tolist() == list(range(16)) + list(range(15, -1, -1))
+    x8 = np.array([0, 255] + list(range(7, 37)), dtype=F16)
+    c, s, z = O.quantize_groups(x8, 8)
+    assert float(s) == 1.0 and float(z) == 0.0
+    assert c.tolist() == [0, 255] + list(range(7, 37))
+
+
+def test_ties_round_half_to_even():
+    # min -1, max 2, 2-bit: scale 1, zero -1; (x - zero) = 1.5, 0.5, 2.5 are exact
+    # ties -> 2, 0, 2 under half-to-even (half-up would give 2, 1, 3).
+    x = np.array([-1.0, 2.0, 0.5, -0.5, 1.5, 0.0, 1.0] + [0.0] * 25, dtype=F16)
+    c, s, z = O.quantize_groups(x, 2)
+    assert float(s) == 1.0 and float(z) == -1.0
+    assert c[:7].tolist() == [0, 3, 2, 0, 2, 1, 2]
+
+
+def test_scale_is_rounded_to_fp16_and_codes_use_it():
+    # min 0, max 1, 4-bit: exact scale 1/15 = 0.0666..., whose nearest fp16 value
+    # is 1092 * 2^-14 = 0.06665039.  Codes divide by that stored value:
+    # 1 / 0.06665039 = 15.0037 -> 15; 0.5 / 0.06665039 = 7.5018 -> 8;
+    # 0.25 / 0.06665039 = 3.7509 -> 4.
+    x = np.array([0.0, 1.0, 0.5] + [0.25] * 29, dtype=F16)
+    c, s, z = O.quantize_groups(x, 4)
+    assert s == F16(1092 * 2.0 ** -14)
+    assert c[:3].tolist() == [0, 15, 8]
+    assert c[3] == 4  # 0.25 / 0.0666504 = 3.7509 -> 4
+
+
+def test_constant_group_reconstructs_exactly():
+    for val in (3.25, -7.0, 0.0, -0.0, 60000.0):
+        x = np.full(32, val, dtype=F16)
+        for b in (2, 4, 8):
+            c, s, z = O.quantize_groups(x, b)
+            assert (c == 0).all()
+            assert float(s) == 0.0 and not np.signbit(s)
+            assert float(z) == abs(val) if val == 0 else float(z) == val
+            assert not np.signbit(z) or val < 0
+            xh = O.dequantize(c, s, z)
+            assert (xh == x.astype(np.float64)).all()
+
+
+def test_negative_zero_canonicalised():
+    x = np.array([-0.0] + [1.0] * 31, dtype=F16)
+    c, s, z = O.quantize_groups(x, 2)
+    assert float(z) == 0.0 and not np.signbit(z)
+
+
+# ------------------------------------------------------------- brute force
+def _brute_force_check(x, bits):
+    """Exact rational check of one group's scale, zero and codes."""
+    c, s, z = O.quantize_groups(x, bits)
+    xs = [_fr(v) for v in x]
+    mn, mx = min(xs), max(xs)
+    assert _fr(z) == mn  # zero point = group minimum, exactly
+    exact_scale = (mx - mn) / (2 ** bits - 1)
+    sf = _fr(s)
+    # stored scale is one of the two fp16 neighbours of the exact scale, the
+    # nearer one unless fp32 rounding first made the choice a near-tie
+    if exact_scale == 0:
+        assert sf == 0
+    else:
+        lo = _fr(np.float16(float(exact_scale)))
+        err = abs(sf - exact_scale)
+        best = abs(lo - exact_scale)
+        assert err <= best * (1 + Fraction(1, 2 ** 10)) + Fraction(1, 2 ** 40)
+    levels = range(2 ** bits)
+    for xi, ci in zip(xs, c.tolist()):
+        assert 0 <= ci < 2 ** bits
+        if sf == 0:
+            assert ci == 0
+            continue
+        d = {k: abs(xi - (mn + sf * k)) for k in levels}
+        best = min(d.values())
+        if d[ci] == best:
+            continue
+        # only a near-tie may go either way: exact quotient within 2^-20 of k + 1/2
+        q = (xi - mn) / sf
+        frac = q - int(q)
+        assert abs(frac - Fraction(1, 2)) < Fraction(1, 2 ** 20) * (1 + abs(q)), (xi, ci, q)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("dist,scale", [("normal", 1.0), ("normal", 30.0),
+                                        ("uniform", 1e-3), ("lognormal", 1.0),
+                                        ("normal", 1e-6)])
+def test_brute_force_random_groups(bits, dist, scale):
+    x = S.random_groups(seed=bits * 100 + int(scale * 7) % 97, n=24, dist=dist, scale=scale)
+    for row in x:
+        _brute_force_check(row, bits)
+
+
+def test_brute_force_subnormal_scale():
+    # fp16 subnormal scale: range 3 * 2^-24 at 2-bit -> scale 2^-24
+    x = np.array([0, 2.0 ** -24, 2 * 2.0 ** -24, 3 * 2.0 ** -24] * 8, dtype=F16)
+    c, s, z = O.quantize_groups(x, 2)
+    assert float(s) == 2.0 ** -24
+    assert c.tolist() == [0, 1, 2, 3] * 8
+    _brute_force_check(x, 2)
+
+
+# ------------------------------------------------------------- invariants
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_invariants_range_min_max_error(bits):
+    x = S.random_groups(seed=7 + bits, n=256, dist="normal", scale=3.0)
+    c, s, z = O.quantize_groups(x, bits)
+    assert c.max() <= 2 ** bits - 1
+    for row, cr, sr in zip(x, c, s):
+        assert cr[np.argmin(row)] == 0
+        assert cr[np.argmax(row)] == 2 ** bits - 1
+    xh = O.dequantize(c, s, z)
+    err = np.abs(xh - x.astype(np.float64))
+    # |x - x_hat| <= scale_h / 2 (normal fp16 scales; fp32 rounding slack 2^-9)
+    assert (err <= s.astype(np.float64)[:, None] * 0.5 * (1 + 2.0 ** -9)).all()
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_power_of_two_scaling_invariance(bits):
+    x = S.random_groups(seed=11, n=64, dist="normal", scale=1.0)
+    c0, s0, z0 = O.quantize_groups(x, bits)
+    for k in (-3, 2, 5):
+        xk = (x.astype(np.float32) * 2.0 ** k).astype(F16)
+        assert (xk.astype(np.float32) == x.astype(np.float32) * 2.0 ** k).all()
+        ck, sk, zk = O.quantize_groups(xk, bits)
+        assert (ck == c0).all()
+        assert (sk.astype(np.float64) == s0.astype(np.float64) * 2.0 ** k).all()
+        assert (zk.astype(np.float64) == z0.astype(np.float64) * 2.0 ** k).all()
+
+
+def test_permutation_within_group():
+    x = S.random_groups(seed=3, n=16, dist="normal")
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(32)
+    c, s, z = O.quantize_groups(x, 4)
+    cp, sp, zp = O.quantize_groups(x[:, perm], 4)
+    assert (cp == c[:, perm]).all() and (sp == s).all() and (zp == z).all()
+
+
+def test_key_groups_are_per_channel_over_tokens():
+    # An outlier at (token 7, channel 5) widens exactly one key group: channel 5 of
+    # tokens 0..31.  Per-token grouping, or a transposed reshape, would widen others.
+    rng = np.random.default_rng(1)
+    k = rng.standard_normal((64, 64)).astype(F16)
+    _, s0, z0 = O.quantize_keys(k, 2)
+    k2 = k.copy()
+    k2[7, 5] = F16(500)
+    c2, s2, z2 = O.quantize_keys(k2, 2)
+    changed = np.argwhere(s2 != s0)
+    assert changed.tolist() == [[0, 5]]
+    assert s2.shape == (2, 64)
+
+
+def test_value_groups_are_per_token_over_channels():
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((64, 128)).astype(F16)
+    _, s0, _ = O.quantize_values(v, 2)
+    v2 = v.copy()
+    v2[7, 70] = F16(500)  # channel group 70 // 32 = 2 of token 7
+    _, s2, _ = O.quantize_values(v2, 2)
+    assert np.argwhere(s2 != s0).tolist() == [[7, 2]]
+    assert s2.shape == (64, 4)
+
+
+def test_key_grouping_axis_matters_on_outlier_channels():
+    # The article (paragraph 4): per-channel key groups isolate outlier channels.
+    # On the outlier recipe, per-channel reconstruction error is far below
+    # per-token grouping of the same keys.
+    w = S.LLAMA2_13B.scaled(batch=1, n_q_heads=2, n_kv_heads=2, context=256)
+    inp = S.generate(w)
+    k = np.swapaxes(inp["K"][0], 0, 1)  # [H, T, D]
+    c, s, z = O.quantize_keys(k, 2)
+    err_ch = np.abs(O.dequantize_keys(c, s, z) - k.astype(np.float64)).mean()
+    c2, s2, z2 = O.quantize_values(k, 2)  # per-token groups of the keys
+    err_tok = np.abs(O.dequantize_values(c2, s2, z2) - k.astype(np.float64)).mean()
+    assert err_ch < 0.5 * err_tok
+
+
+# ------------------------------------------------------------- attention
+def _sdpa64(q, k, v, scale):
+    qt = torch.from_numpy(q.astype(np.float64))[:, None, :]  # [H, 1, D]
+    kt = torch.from_numpy(k.astype(np.float64))
+    vt = torch.from_numpy(v.astype(np.float64))
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+    return o[:, 0, :].numpy()
+
+
+def test_all_tail_equals_sdpa_float64():
+    # n_quant = 0: every token is fp16 in the tail; the oracle must equal exact
+    # attention (north_star: "with no quantization the result matches exact attention").
+    w = S.LLAMA31_8B_128K.scaled(context=96, n_tail=96, tail_cap=96)
+    inp = S.generate(w)
+    st = O.quantize_sequence(inp["K"][0], inp["V"][0], 96, 96, 2)
+    out = O.sequence_attention(inp["q"][0], st, w.sm_scale)
+    k = np.swapaxes(inp["K"][0], 0, 1)
+    v = np.swapaxes(inp["V"][0], 0, 1)
+    kk = np.repeat(k, w.gqa, axis=0)
+    vv = np.repeat(v, w.gqa, axis=0)
+    ref = _sdpa64(inp["q"][0], kk, vv, w.sm_scale)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_dequantized_cache_equals_sdpa_on_dequantized_inputs():
+    w = S.TINY
+    inp = S.generate(w)
+    st = O.quantize_sequence(inp["K"][0], inp["V"][0], 256, 0, 2)
+    keys, values = O.sequence_kv(st)
+    out = O.sequence_attention(inp["q"][0], st, w.sm_scale)
+    ref = _sdpa64(inp["q"][0], keys, values, w.sm_scale)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(5)
+    d, n = 64, 40
+    keys = rng.standard_normal((1, n, d))
+    row = rng.standard_normal(d)
+    q = rng.standard_normal((1, d)).astype(F16)
+    # all V rows equal -> output is that row
+    out = O.decode_attention(q, keys, np.tile(row, (1, n, 1)), 0.125)
+    np.testing.assert_allclose(out[0], row, atol=1e-13)
+    # q = 0 -> uniform weights -> mean of V
+    values = rng.standard_normal((1, n, d))
+    out = O.decode_attention(np.zeros((1, d), F16), keys, values, 0.125)
+    np.testing.assert_allclose(out[0], values[0].mean(0), atol=1e-13)
+    # a single token -> its V row
+    out = O.decode_attention(q, keys[:, :1], values[:, :1], 0.125)
+    np.testing.assert_allclose(out[0], values[0, 0], atol=1e-13)
+    # two tokens, hand softmax: weights e^{l0}/(e^{l0}+e^{l1})
+    l0 = 0.125 * keys[0, 0] @ q[0].astype(np.float64)
+    l1 = 0.125 * keys[0, 1] @ q[0].astype(np.float64)
+    p0 = 1.0 / (1.0 + np.exp(l1 - l0))
+    out = O.decode_attention(q, keys[:, :2], values[:, :2], 0.125)
+    np.testing.assert_allclose(out[0], p0 * values[0, 0] + (1 - p0) * values[0, 1], atol=1e-12)
+    # empty context -> zeros
+    assert (O.decode_attention(q, keys[:, :0], values[:, :0], 0.125) == 0).all()
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    rng = np.random.default_rng(6)
+    keys = rng.standard_normal((2, 33, 32))
+    values = rng.standard_normal((2, 33, 32))
+    q = rng.standard_normal((8, 32)).astype(F16)
+    gqa = O.decode_attention(q, keys, values, 0.2)
+    mha = O.decode_attention(q, np.repeat(keys, 4, 0), np.repeat(values, 4, 0), 0.2)
+    np.testing.assert_allclose(gqa, mha, atol=1e-14)
+    # query head 5 reads KV head 1 (contiguous groups of 4)
+    one = O.decode_attention(q[5:6], keys[1:2], values[1:2], 0.2)
+    np.testing.assert_allclose(gqa[5], one[0], atol=1e-14)
+
+
+def test_attention_token_permutation_invariance():
+    rng = np.random.default_rng(7)
+    keys = rng.standard_normal((1, 50, 16))
+    values = rng.standard_normal((1, 50, 16))
+    q = rng.standard_normal((1, 16)).astype(F16)
+    perm = rng.permutation(50)
+    a = O.decode_attention(q, keys, values, 0.25)
+    b = O.decode_attention(q, keys[:, perm], values[:, perm], 0.25)
+    np.testing.assert_allclose(a, b, atol=1e-14)
+
+
+# ------------------------------------------------------------- tail / append
+def test_append_flushes_only_when_tail_full():
+    assert O.append_lengths(64, 31, 32) == (64, 32, False)
+    assert O.append_lengths(64, 32, 32) == (96, 1, True)
+    assert O.append_lengths(0, 64, 64) == (32, 33, True)
+    assert O.append_lengths(0, 0, 32) == (0, 1, False)
+
+
+def test_flushed_group_equals_prefill_quantization():
+    # Appending tokens one by one (flush of the oldest 32 when the tail is full)
+    # leaves the same quantized region as quantizing the whole prefix at once,
+    # because key groups are aligned 32-token spans from token 0.
+    w = S.TINY.scaled(context=160)
+    inp = S.generate(w)
+    k, v = inp["K"][0], inp["V"][0]
+    nq, nt = 0, 0
+    for _ in range(160):
+        nq, nt, _ = O.append_lengths(nq, nt, 32)
+    assert nq + nt == 160 and nq == 128 and nt == 32
+    st = O.quantize_sequence(k, v, 160, nt, 2)
+    ref = O.quantize_sequence(k[:128], v[:128], 128, 0, 2)
+    assert (st["k_codes"] == ref["k_codes"]).all() and (st["k_scale"] == ref["k_scale"]).all()
+
+
+# ------------------------------------------------------------- layout pins
+# Positions derived by hand from the PTX ISA's mma.m16n8k16 .f16 A-fragment
+# table (a0: row gid, cols 2*tig..+1; a1: row gid+8; a2: cols +8; a3: both) and
+# the tile rules: lane = 4*gid + tig; pair P -> word P // (16/b), slot P % (16/b);
+# first code at bits [b*slot, +b), second at [16 + b*slot, +b); lane word w at
+# byte ((w // 4) * 32 + lane) * 16 + (w % 4) * 4.
+KPOS_2BIT_D128 = [
+    # (token, channel) -> (byte offset of the 32-bit word, bit offset)
+    ((0, 0), (0, 0)), ((0, 1), (0, 16)), ((8, 0), (0, 2)), ((0, 8), (0, 4)),
+    ((8, 9), (0, 22)), ((16, 0), (0, 8)), ((24, 8), (0, 14)), ((1, 0), (64, 0)),
+    ((0, 2), (16, 0)), ((0, 16), (4, 0)), ((0, 64), (512, 0)), ((31, 127), (512 + 31 * 16 + 12, 30)),
+]
+KPOS_4BIT_D128 = [((0, 0), (0, 0)), ((16, 0), (4, 0)), ((8, 1), (0, 20)), ((0, 16), (8, 0)),
+                  ((0, 32), (512, 0))]
+VPOS_2BIT_D128 = [
+    ((0, 0), (0, 0)), ((1, 0), (0, 16)), ((0, 8), (0, 2)), ((8, 0), (0, 4)),
+    ((16, 0), (0, 8)), ((2, 0), (16, 0)), ((0, 1), (64, 0)), ((0, 16), (4, 0)),
+]
+
+
+@pytest.mark.parametrize("kind,bits,table", [("K", 2, KPOS_2BIT_D128), ("K", 4, KPOS_4BIT_D128),
+                                             ("V", 2, VPOS_2BIT_D128)])
+def test_tile_layout_hand_positions(kind, bits, table):
+    codes = np.zeros((32, 128), np.uint8)
+    for (t, d), (byte, bit) in table:
+        codes[:] = 0
+        codes[t, d] = 2 ** bits - 1
+        packed = O.pack_tiles(codes, kind, bits)
+        words = packed.view("<u4")
+        nz = np.nonzero(words)[0]
+        assert nz.tolist() == [byte // 4], (t, d)
+        assert int(words[byte // 4]) == (2 ** bits - 1) << bit, (t, d)
+
+
+@pytest.mark.parametrize("kind", ["K", "V"])
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_tile_layout_is_a_bijection(kind, bits, d):
+    word, bit = O.tile_code_positions(kind, d, bits)
+    fields = set(zip((word * 32 + bit).ravel().tolist()))
+    assert len(fields) == 32 * d
+    assert word.max() + 1 == 32 * d * bits // 32
+    rng = np.random.default_rng(bits + d)
+    codes = rng.integers(0, 2 ** bits, (2, 32, d), dtype=np.uint8)
+    assert (O.unpack_tiles(O.pack_tiles(codes, kind, bits), kind, d, bits) == codes).all()
+
+
+# ------------------------------------------------------------- mixed width
+def _small_trizone(seed=4, t_old=200, fresh=8, d=64, probs=None):
+    w = S.TRIZONE.scaled(batch=1, n_q_heads=4, n_kv_heads=1, head_dim=d,
+                         context=t_old + fresh, trizone_fresh=fresh, seed=seed,
+                         **({"v_width_probs": probs} if probs else {}))
+    inp = S.generate(w)
+    return w, inp
+
+
+def test_trizone_all_fp16_equals_exact_attention():
+    # every old token at width 16 (no V quantization) and K at 8 bits: the V side
+    # is exact; with the K codes dequantized first, the result equals SDPA.
+    w, inp = _small_trizone(probs=(0, 0, 0, 0, 1.0))
+    k, v = inp["K"][0, :, 0], inp["V"][0, :, 0]
+    tz = O.trizone_quantize(k, v, inp["v_width"][0, 0], np.full(64, 8, np.uint8))
+    keys, values = O.trizone_kv(tz)
+    assert (values == v.astype(np.float64)).all()
+    out = O.trizone_attention(inp["q"][0], [tz], w.sm_scale)
+    ref = _sdpa64(inp["q"][0], np.repeat(keys[None], 4, 0), np.repeat(values[None], 4, 0), w.sm_scale)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+
+
+def test_trizone_all_evicted_leaves_fresh_tokens():
+    w, inp = _small_trizone(probs=(1.0, 0, 0, 0, 0))
+    k, v = inp["K"][0, :, 0], inp["V"][0, :, 0]
+    tz = O.trizone_quantize(k, v, inp["v_width"][0, 0], inp["k_width"][0, 0])
+    assert tz["blocks"] == []
+    out = O.trizone_attention(inp["q"][0], [tz], w.sm_scale)
+    ref = _sdpa64(inp["q"][0], np.repeat(k[200:][None], 4, 0), np.repeat(v[200:][None], 4, 0),
+                  w.sm_scale)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+
+
+def test_trizone_blocks_are_width_uniform_and_cover_kept_tokens():
+    w, inp = _small_trizone()
+    vw = inp["v_width"][0, 0]
+    blocks = O.trizone_blocks(vw)
+    seen = np.concatenate([t for _, t in blocks])
+    assert sorted(seen.tolist()) == np.nonzero(vw)[0].tolist()
+    for width, toks in blocks:
+        assert (vw[toks] == width).all() and 1 <= len(toks) <= 32
+    widths = [wd for wd, _ in blocks]
+    assert widths == sorted(widths)
+
+
+def test_trizone_matches_uniform_when_widths_are_uniform():
+    # all V widths 4, all K widths 4, 192 old tokens: blocks are the uniform
+    # cache's 32-token groups, so codes and attention coincide.
+    w, inp = _small_trizone(t_old=192, probs=(0, 0, 1.0, 0, 0))
+    k, v = inp["K"][0, :, 0], inp["V"][0, :, 0]
+    tz = O.trizone_quantize(k, v, inp["v_width"][0, 0], np.full(64, 4, np.uint8))
+    st = O.quantize_sequence(k[:, None], v[:, None], 200, 8, 4)
+    kc = np.concatenate([b["k_codes"] for b in tz["blocks"]])
+    assert (kc == st["k_codes"][0]).all()
+    a = O.trizone_attention(inp["q"][0], [tz], w.sm_scale)
+    b = O.sequence_attention(inp["q"][0], st, w.sm_scale)
+    np.testing.assert_allclose(a, b, atol=1e-13)
