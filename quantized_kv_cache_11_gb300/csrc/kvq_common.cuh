@@ -1,0 +1,248 @@
+// Shared device code of the kvq library: the group quantizer, the packed tile
+// layout and thin PTX wrappers.  sm_103a only.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kGroup = KVQ_GROUP;
+
+// ---------------------------------------------------------------------------
+// Group quantizer ("KV-cache quantization axes", ihal.it, paragraph 3: the
+// group's range is divided into the 2^b levels of the code, one scale and one
+// zero point per group).  Every fp32 operation is an explicit round-to-nearest
+// intrinsic so the result is bit-identical to an IEEE fp32 evaluation.
+// ---------------------------------------------------------------------------
+struct GroupParams {
+  __half scale_h;
+  __half zero_h;
+  float scale;  // fp32 value of the stored fp16 scale
+  float zero;   // fp32 value of the stored fp16 zero point
+};
+
+template <int BITS>
+__device__ __forceinline__ GroupParams group_params(float mn, float mx) {
+  const float rng = __fsub_rn(mx, mn);
+  const float sc = __fdiv_rn(rng, (float)((1 << BITS) - 1));
+  GroupParams p;
+  p.scale_h = __float2half_rn(sc);
+  p.zero_h = __float2half_rn(mn);  // exact: mn is an fp16 value
+  p.scale = __half2float(p.scale_h);
+  p.zero = __half2float(p.zero_h);
+  if (p.scale == 0.f) { p.scale_h = __float2half_rn(0.f); p.scale = 0.f; }  // -0 -> +0
+  if (p.zero == 0.f) { p.zero_h = __float2half_rn(0.f); p.zero = 0.f; }
+  return p;
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t quant_code(float x, const GroupParams& p) {
+  if (p.scale == 0.f) return 0u;
+  const float q = __fdiv_rn(__fsub_rn(x, p.zero), p.scale);
+  int c = __float2int_rn(q);  // round half to even
+  c = c < 0 ? 0 : c;
+  c = c > (1 << BITS) - 1 ? (1 << BITS) - 1 : c;
+  return (uint32_t)c;
+}
+
+// ---------------------------------------------------------------------------
+// Packed tile layout (see kvq.h).  Lane L (gid = L/4, tig = L%4) owns D/2 code
+// pairs; pair P lives in the lane's word P/(16/BITS), slot P%(16/BITS).
+// ---------------------------------------------------------------------------
+template <int D, int BITS>
+struct Tile {
+  static constexpr int kBytes = kGroup * D * BITS / 8;   // bytes per tile
+  static constexpr int kWordsPerLane = D * BITS / 32;     // >= 4
+  static constexpr int kChunksPerLane = kWordsPerLane / 4;  // 16-byte chunks
+  static constexpr int kPairsPerWord = 16 / BITS;
+  static_assert(kWordsPerLane % 4 == 0, "a lane owns whole 16-byte chunks");
+};
+
+// (token, channel) of the FIRST code of key pair P of a lane; the second code is
+// at channel + 1.
+__device__ __forceinline__ void key_pair_pos(int P, int gid, int tig, int& t, int& c) {
+  const int kt = P >> 3, mt = (P >> 2) & 1, i = P & 3;
+  t = 16 * mt + gid + 8 * (i & 1);
+  c = 16 * kt + 2 * tig + 8 * (i >> 1);
+}
+
+// (token, channel) of the FIRST code of value pair P; the second is at token + 1.
+__device__ __forceinline__ void value_pair_pos(int P, int gid, int tig, int& t, int& c) {
+  const int mt = P >> 3, kt = (P >> 2) & 1, i = P & 3;
+  c = 16 * mt + gid + 8 * (i & 1);
+  t = 16 * kt + 2 * tig + 8 * (i >> 1);
+}
+
+// Pack a 32 x D tile of codes held in shared memory (ct[t * D + c]) and store it
+// to global memory with one 16-byte store per lane per chunk (coalesced).
+template <int D, int BITS, bool IS_KEY>
+__device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst, int lane) {
+  using T = Tile<D, BITS>;
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t w[T::kWordsPerLane];
+#pragma unroll
+  for (int i = 0; i < T::kWordsPerLane; ++i) w[i] = 0u;
+#pragma unroll
+  for (int P = 0; P < D / 2; ++P) {
+    int t, c;
+    uint32_t first, second;
+    if (IS_KEY) {
+      key_pair_pos(P, gid, tig, t, c);
+      first = ct[t * D + c];
+      second = ct[t * D + c + 1];
+    } else {
+      value_pair_pos(P, gid, tig, t, c);
+      first = ct[t * D + c];
+      second = ct[(t + 1) * D + c];
+    }
+    const int wi = P / T::kPairsPerWord, k = P % T::kPairsPerWord;
+    w[wi] |= (first << (BITS * k)) | (second << (16 + BITS * k));
+  }
+#pragma unroll
+  for (int ch = 0; ch < T::kChunksPerLane; ++ch) {
+    uint4 v = make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+    *reinterpret_cast<uint4*>(dst + (size_t)(ch * 32 + lane) * 16) = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One warp quantizes one 32-token tile of keys and of values.
+//   ksrc/vsrc: token 0 of the tile for this head; rows tstride elements apart,
+//   channels contiguous.  Writes packed codes and metadata of the tile.
+//   ct: shared scratch of 32 * D bytes for this warp; vm: shared 2 * D halves.
+// Keys: one group per channel over the 32 tokens (lane-local min/max, each lane
+// owns D/32 channels).  Values: one group per 32 channels of a token (min/max
+// reduced over the lanes that share a group with shuffles).
+// ---------------------------------------------------------------------------
+template <int D>
+struct LaneRow;  // D/32 consecutive halves of a row held by one lane
+template <>
+struct LaneRow<128> {
+  static constexpr int kN = 4;
+  uint2 raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ float get(int i) const {
+    const uint32_t w = (i < 2) ? raw.x : raw.y;
+    const uint16_t hbits = (i & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xffffu);
+    return __half2float(__ushort_as_half(hbits));
+  }
+};
+template <>
+struct LaneRow<64> {
+  static constexpr int kN = 2;
+  uint32_t raw;
+  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ __forceinline__ float get(int i) const {
+    const uint16_t hbits = i ? (uint16_t)(raw >> 16) : (uint16_t)(raw & 0xffffu);
+    return __half2float(__ushort_as_half(hbits));
+  }
+};
+
+template <int D, int BITS>
+__device__ __forceinline__ void quantize_tile_warp(const __half* ksrc, const __half* vsrc,
+                                                   int64_t tstride, uint8_t* kcodes_dst,
+                                                   __half* kmeta_dst, uint8_t* vcodes_dst,
+                                                   __half* vmeta_dst, uint8_t* ct, __half* vm,
+                                                   int lane) {
+  constexpr int CPL = D / 32;  // channels per lane
+  const int c0 = lane * CPL;
+  // ---- keys: per channel over 32 tokens
+  {
+    LaneRow<D> rows[kGroup];
+#pragma unroll
+    for (int t = 0; t < kGroup; ++t) rows[t].load(ksrc + (int64_t)t * tstride + c0);
+    __half sc[CPL], ze[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      float mn = rows[0].get(j), mx = mn;
+#pragma unroll
+      for (int t = 1; t < kGroup; ++t) {
+        const float x = rows[t].get(j);
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+      const GroupParams p = group_params<BITS>(mn, mx);
+      sc[j] = p.scale_h;
+      ze[j] = p.zero_h;
+#pragma unroll
+      for (int t = 0; t < kGroup; ++t) ct[t * D + c0 + j] = (uint8_t)quant_code<BITS>(rows[t].get(j), p);
+    }
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      kmeta_dst[c0 + j] = sc[j];
+      kmeta_dst[D + c0 + j] = ze[j];
+    }
+  }
+  __syncwarp();
+  pack_store_tile<D, BITS, true>(ct, kcodes_dst, lane);
+  __syncwarp();
+  // ---- values: per token over 32-channel spans
+  {
+    constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
+    const int j = c0 / kGroup;     // this lane's channel group
+#pragma unroll 4
+    for (int t = 0; t < kGroup; ++t) {
+      LaneRow<D> r;
+      r.load(vsrc + (int64_t)t * tstride + c0);
+      float mn = r.get(0), mx = mn;
+#pragma unroll
+      for (int i = 1; i < CPL; ++i) {
+        mn = fminf(mn, r.get(i));
+        mx = fmaxf(mx, r.get(i));
+      }
+#pragma unroll
+      for (int off = 1; off < LPG; off <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      }
+      const GroupParams p = group_params<BITS>(mn, mx);
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) ct[t * D + c0 + i] = (uint8_t)quant_code<BITS>(r.get(i), p);
+      if ((lane % LPG) == 0) {
+        vm[j * kGroup + t] = p.scale_h;
+        vm[D + j * kGroup + t] = p.zero_h;
+      }
+    }
+  }
+  __syncwarp();
+  pack_store_tile<D, BITS, false>(ct, vcodes_dst, lane);
+  // metadata planes: 2 * D halves = 4 * D bytes, D / 8 bytes per lane
+  if (D == 128) {
+    reinterpret_cast<uint4*>(vmeta_dst)[lane] = reinterpret_cast<const uint4*>(vm)[lane];
+  } else {
+    reinterpret_cast<uint2*>(vmeta_dst)[lane] = reinterpret_cast<const uint2*>(vm)[lane];
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers.
+// ---------------------------------------------------------------------------
+// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col); fragment layouts per
+// the PTX ISA's mma.m16n8k16 tables.
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+}  // namespace kvq

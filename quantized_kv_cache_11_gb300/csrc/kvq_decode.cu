@@ -1,0 +1,794 @@
+// Fused-dequant split-K decode attention over the uniform packed cache.
+//
+// What it computes ("KV-cache quantization axes", ihal.it, paragraphs 2 and 6;
+// VQKV summary, section 2 "decoding phase"): for every sequence b and query head
+// hq (KV head h = hq / G), out = softmax(sm_scale * q . K_hat^T) . V_hat over the
+// quantized tokens (K_hat = zero + scale * code, dequantized inside the
+// products, never written out) and the fp16 tail tokens.
+//
+// How:
+// * Work partition (stream-K): the quantized 32-token groups of every
+//   (sequence, KV head) are laid end to end and the list is cut into equal
+//   contiguous ranges, one per resident CTA, so ragged batches stay balanced.
+//   Inside a CTA each warp streams its own sub-range through a private
+//   multi-stage cp.async ring in shared memory.  The fp16 tail of each
+//   (sequence, KV head) is handled by one extra "tail warp".
+// * Per 32-token group (one warp, the whole GQA group of G query heads):
+//   Q.K^T on tensor cores (mma.m16n8k16, fp16 in, fp32 accumulate) with
+//   A = 2^b + code (one logic op per pair of codes gives exact fp16 values) and
+//   B = q * scale split into two fp16 halves (hi + lo, exact), so the per
+//   channel scale folds into q once per group; the zero point and the 2^b
+//   offset fold into one per-group constant computed by a small extra MMA.
+//   Online softmax in fp32; P.V on tensor cores with B = p * scale (hi + lo)
+//   per 32-channel value group, the value zero point again in a small MMA.
+// * Splits are merged by log-sum-exp; the last CTA to finish a (sequence, KV
+//   head) merges and writes the output, then resets its counter.  No spin-wait.
+#include <cmath>
+
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+template <int D, int BITS, int G>
+struct DecodeCfg {
+  using T = Tile<D, BITS>;
+  static constexpr int TB = T::kBytes;
+  static constexpr int KMETA = 4 * D;  // [2][D] halves
+  static constexpr int VMETA = 4 * D;  // [2][D/32][32] halves
+  static constexpr int STAGE = 2 * TB + KMETA + VMETA;
+  static constexpr int NT = (2 * G + 7) / 8;  // 8-column n-tiles: column 2g = hi, 2g+1 = lo
+  static constexpr int KT = D / 16;
+  static constexpr int NWL = T::kWordsPerLane;
+  static constexpr int PPW = T::kPairsPerWord;
+  static constexpr int WARPS = BITS == 8 ? 4 : 8;
+  static constexpr int NSTAGE = BITS == 2 ? 4 : (BITS == 4 ? 2 : 3);
+  static constexpr float OFF = (float)(1 << BITS);
+  static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
+  static constexpr int RING = WARPS * NSTAGE * STAGE;
+  static constexpr int PS = WARPS * G * kGroup * 2;  // p~ exchange, halves
+  static constexpr int PREFIX = 2 * (KVQ_MAX_BATCH + 1) * 4;
+  static constexpr int SMEM = RING + PS + PREFIX;
+  static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
+  static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
+};
+
+struct DecodeParams {
+  const uint8_t* k_codes;
+  const uint8_t* v_codes;
+  const __half* k_meta;
+  const __half* v_meta;
+  const __half* k_tail;
+  const __half* v_tail;
+  const int32_t* n_quant;
+  const int32_t* n_tail;
+  const int32_t* tail_head;
+  int32_t* error_flags;
+  const __half* q;
+  float* out;
+  int32_t* counters;
+  float* tail_part;
+  float* part;
+  float scale_log2;
+  int32_t batch, hkv, max_groups, tail_cap;
+  int32_t n_tail_ctas;
+  int32_t n_stream;
+};
+
+// Lengths as the decode sees them; an inconsistent sequence counts as empty.
+struct SeqLen {
+  int nq, nt, th;
+};
+__device__ __forceinline__ SeqLen read_lengths(const DecodeParams& p, int b, bool report) {
+  SeqLen s{p.n_quant[b], p.n_tail[b], p.tail_head[b]};
+  const bool ok = s.nq >= 0 && s.nq % kGroup == 0 && s.nq / kGroup <= p.max_groups && s.nt >= 0 &&
+                  s.nt <= p.tail_cap && s.th >= 0 && s.th < p.tail_cap;
+  if (!ok) {
+    if (report && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_BAD_LENGTHS);
+    s = SeqLen{0, 0, 0};
+  }
+  return s;
+}
+
+// s_pref[b] = quantized groups of sequences < b; s_ne[b] = nonempty sequences < b.
+__device__ void build_prefix(const DecodeParams& p, int* s_pref, int* s_ne) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int run = 0, run_ne = 0;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int g = 0;
+    if (b < p.batch) g = read_lengths(p, b, blockIdx.x == 0).nq / kGroup;
+    int ne = g > 0 ? 1 : 0;
+    // inclusive warp scan
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, g, off);
+      const int c = __shfl_up_sync(0xffffffffu, ne, off);
+      if (lane >= off) { g += a; ne += c; }
+    }
+    if (b < p.batch) { s_pref[b + 1] = run + g; s_ne[b + 1] = run_ne + ne; }
+    run += __shfl_sync(0xffffffffu, g, 31);
+    run_ne += __shfl_sync(0xffffffffu, ne, 31);
+  }
+  if (lane == 0) { s_pref[0] = 0; s_ne[0] = 0; }
+}
+
+// The stream-K CTA that owns global group index x (ranges [x*T/N, ...)).
+__device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
+  return ((x + 1) * n - 1) / total;
+}
+
+template <int D, int BITS, int G>
+struct Decoder {
+  using C = DecodeCfg<D, BITS, G>;
+  static constexpr int NT = C::NT, KT = C::KT;
+
+  // Per-warp running state of the online softmax for the G heads.
+  float m[NT], l[NT];
+  float o[KT][NT][4];
+  float zc[NT][4];
+  uint32_t qf[NT][KT][2];  // q pairs of column 8nt+gid (head 4nt + gid/2), 0 beyond G
+  int lane, gid, tig, hl;
+
+  __device__ __forceinline__ void init(const DecodeParams& p, int b, int h) {
+    lane = threadIdx.x & 31;
+    gid = lane >> 2;
+    tig = lane & 3;
+    hl = gid & 1;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt] = -INFINITY;
+      l[nt] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) zc[nt][i] = 0.f;
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[kt][nt][i] = 0.f;
+      const int g = 4 * nt + (gid >> 1);
+      const __half* qh = p.q + ((size_t)b * p.hkv * G + (size_t)h * G + g) * D;
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          qf[nt][kt][r] = (g < G) ? *reinterpret_cast<const uint32_t*>(qh + 16 * kt + 2 * tig + 8 * r) : 0u;
+    }
+  }
+
+  // fp16 pair (2^b + c_first, 2^b + c_second) of pair P of the lane's packed words;
+  // P must be a compile-time constant after unrolling.
+  static __device__ __forceinline__ uint32_t unpack(const uint32_t* w, int P) {
+    const int k = P % C::PPW;
+    const int sh = BITS * k - (10 - BITS);
+    constexpr uint32_t M = (uint32_t)((1 << BITS) - 1) << (10 - BITS);
+    constexpr uint32_t MASK = M | (M << 16);
+    constexpr uint32_t EXPO = (uint32_t)((15 + BITS) << 10) * 0x10001u;
+    const uint32_t word = w[P / C::PPW];
+    const uint32_t x = sh >= 0 ? (word >> sh) : (word << -sh);
+    return (x & MASK) | EXPO;
+  }
+  // A fragment (4 registers) of pairs P0 .. P0+3.
+  static __device__ __forceinline__ void frag(const uint32_t* w, int P0, uint32_t (&a)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = unpack(w, P0 + i);
+  }
+
+  static __device__ __forceinline__ uint32_t split_mul(uint32_t a, uint32_t b, int lo) {
+    const __half2 x = u32_as_h2(a), y = u32_as_h2(b);
+    const __half2 hi = __hmul2_rn(x, y);
+    const __half2 rem = __hfma2(x, y, __hneg2(hi));  // exact remainder (fp16 product has <= 22 bits)
+    return lo ? h2_as_u32(rem) : h2_as_u32(hi);
+  }
+
+  // Online softmax over one 32-token chunk.  lg[nt][mt][r] are log2-domain logits of
+  // token 16mt + gid + 8r for head 4nt + tig.  Writes p~ (fp16) to ps.
+  __device__ __forceinline__ void softmax(float (&lg)[NT][2][2], __half* ps) {
+    bool need = false;
+    float mloc[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float mx = fmaxf(fmaxf(lg[nt][0][0], lg[nt][0][1]), fmaxf(lg[nt][1][0], lg[nt][1][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      mloc[nt] = mx;
+      need |= mx > m[nt];
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float mnew = fmaxf(m[nt], mloc[nt]);
+        const float alpha = (mnew == m[nt]) ? 1.f : exp2f(m[nt] - mnew);
+        m[nt] = mnew;
+        l[nt] *= alpha;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) zc[nt][i] *= alpha;
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[kt][nt][i] *= alpha;
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = 4 * nt + tig;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float pv = exp2f(lg[nt][mt][r] - m[nt]);
+          const __half ph = __float2half_rn(pv);
+          l[nt] += __half2float(ph);
+          if (g < G) ps[g * kGroup + 16 * mt + gid + 8 * r] = ph;
+        }
+    }
+    __syncwarp();
+  }
+
+  // p~ pairs for the V-side B fragments: column 8nt+gid (head 4nt + gid/2), tokens
+  // 16kt + 2tig + 8r and +1.
+  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = 4 * nt + (gid >> 1);
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          pp[nt][kt][r] = (g < G) ? *reinterpret_cast<const uint32_t*>(ps + g * kGroup + 16 * kt + 2 * tig + 8 * r) : 0u;
+    }
+  }
+
+  // One quantized 32-token group staged in shared memory.
+  __device__ __forceinline__ void quant_group(const uint8_t* stage, __half* ps, float scale_log2) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(stage);
+    uint32_t kw[C::NWL];
+#pragma unroll
+    for (int ch = 0; ch < C::NWL / 4; ++ch) {
+      const uint4 v = s4[ch * 32 + lane];
+      kw[4 * ch] = v.x; kw[4 * ch + 1] = v.y; kw[4 * ch + 2] = v.z; kw[4 * ch + 3] = v.w;
+    }
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);  // scale pairs, then zero pairs
+    float sacc[2][NT][4];
+    float cacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { sacc[0][nt][i] = 0.f; sacc[1][nt][i] = 0.f; cacc[nt][i] = 0.f; }
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      const uint32_t sp0 = km[8 * kt + tig], sp1 = km[8 * kt + 4 + tig];
+      const uint32_t zp0 = km[D / 2 + 8 * kt + tig], zp1 = km[D / 2 + 8 * kt + 4 + tig];
+      uint32_t a0[4], a1[4];
+      frag(kw, (kt * 2 + 0) * 4, a0);  // pairs of (kt, mt = 0)
+      frag(kw, (kt * 2 + 1) * 4, a1);  // pairs of (kt, mt = 1)
+      const uint32_t ac[4] = {gid == 0 ? zp0 : (gid == 1 ? sp0 : 0u), 0u,
+                              gid == 0 ? zp1 : (gid == 1 ? sp1 : 0u), 0u};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t b0 = split_mul(qf[nt][kt][0], sp0, hl);
+        const uint32_t b1 = split_mul(qf[nt][kt][1], sp1, hl);
+        mma_16816(sacc[0][nt], a0, b0, b1);
+        mma_16816(sacc[1][nt], a1, b0, b1);
+        mma_16816(cacc[nt], ac, hl ? 0u : qf[nt][kt][0], hl ? 0u : qf[nt][kt][1]);
+      }
+    }
+    float lg[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float zq = __shfl_sync(0xffffffffu, cacc[nt][0], tig);
+      const float sq = __shfl_sync(0xffffffffu, cacc[nt][0], 4 + tig);
+      const float kc = zq - C::OFF * sq;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          lg[nt][mt][r] = (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1] + kc) * scale_log2;
+    }
+    softmax(lg, ps);
+    uint32_t pp[NT][2][2];
+    load_pp(ps, pp);
+    // ---- P.V
+    uint32_t vw[C::NWL];
+#pragma unroll
+    for (int ch = 0; ch < C::NWL / 4; ++ch) {
+      const uint4 v = s4[(C::TB / 16) + ch * 32 + lane];
+      vw[4 * ch] = v.x; vw[4 * ch + 1] = v.y; vw[4 * ch + 2] = v.z; vw[4 * ch + 3] = v.w;
+    }
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB + C::KMETA);
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        const uint32_t vs0 = vm[16 * j + 8 * kt + tig], vs1 = vm[16 * j + 8 * kt + 4 + tig];
+        uint32_t b[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          b[nt][0] = split_mul(pp[nt][kt][0], vs0, hl);
+          b[nt][1] = split_mul(pp[nt][kt][1], vs1, hl);
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+          const int mt = 2 * j + mi;
+          uint32_t a[4];
+          frag(vw, (mt * 2 + kt) * 4, a);  // pairs of (mt, kt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, b[nt][0], b[nt][1]);
+        }
+      }
+    }
+    // value zero points and the 2^b offset: rows j = sum_t p~ z[j][t], rows 4+j = sum_t p~ s[j][t]
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+      const int row = gid;
+      uint32_t x0 = 0u, x1 = 0u;
+      if (row < D / 32) {
+        x0 = vm[D / 2 + 16 * row + 8 * kt + tig];
+        x1 = vm[D / 2 + 16 * row + 8 * kt + 4 + tig];
+      } else if (row >= 4 && row - 4 < D / 32) {
+        x0 = vm[16 * (row - 4) + 8 * kt + tig];
+        x1 = vm[16 * (row - 4) + 8 * kt + 4 + tig];
+      }
+      const uint32_t ac[4] = {x0, 0u, x1, 0u};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_16816(zc[nt], ac, hl ? 0u : pp[nt][kt][0], hl ? 0u : pp[nt][kt][1]);
+    }
+    __syncwarp();
+  }
+
+  // One chunk of up to 32 fp16 tail tokens, read from the ring in global memory.
+  __device__ __forceinline__ void tail_chunk(const __half* kt_base, const __half* vt_base, int first,
+                                             int count, int th, int R, __half* ps, float scale_log2) {
+    auto slot = [&](int t) { return (th + first + t) % R; };
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { sacc[0][nt][i] = 0.f; sacc[1][nt][i] = 0.f; }
+    int rowoff[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int t = 16 * mt + gid + 8 * r;
+        rowoff[mt][r] = t < count ? slot(t) * D : -1;
+      }
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ro = rowoff[mt][i & 1];
+          const int c = 16 * kt + 2 * tig + 8 * (i >> 1);
+          a[mt][i] = ro >= 0 ? __ldg(reinterpret_cast<const unsigned int*>(kt_base + ro + c)) : 0u;
+        }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t b0 = hl ? 0u : qf[nt][kt][0], b1 = hl ? 0u : qf[nt][kt][1];
+        mma_16816(sacc[0][nt], a[0], b0, b1);
+        mma_16816(sacc[1][nt], a[1], b0, b1);
+      }
+    }
+    float lg[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          lg[nt][mt][r] = rowoff[mt][r] >= 0
+                              ? (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1]) * scale_log2
+                              : -INFINITY;
+    softmax(lg, ps);
+    uint32_t pp[NT][2][2];
+    load_pp(ps, pp);
+    const unsigned short* vt = reinterpret_cast<const unsigned short*>(vt_base);
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+      int tok[2][2];  // [i>>1][e] -> ring row offset or -1
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = 16 * kt + 2 * tig + 8 * hh + e;
+          tok[hh][e] = t < count ? slot(t) * D : -1;
+        }
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        uint32_t a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = 16 * mt + gid + 8 * (i & 1);
+          const int r0 = tok[i >> 1][0], r1 = tok[i >> 1][1];
+          const uint32_t lo = r0 >= 0 ? (uint32_t)__ldg(vt + r0 + c) : 0u;
+          const uint32_t hi = r1 >= 0 ? (uint32_t)__ldg(vt + r1 + c) : 0u;
+          a[i] = lo | (hi << 16);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_16816(o[mt][nt], a, hl ? 0u : pp[nt][kt][0], hl ? 0u : pp[nt][kt][1]);
+      }
+    }
+    __syncwarp();
+  }
+
+  // Write this warp's partial (m, l, unnormalised o) for its G heads.
+  __device__ __forceinline__ void write_partial(float* dst) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = 4 * nt + tig;
+      float lt = l[nt];
+      lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+      float vc[D / 32];
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        const float zs = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);
+        const float ss = __shfl_sync(0xffffffffu, zc[nt][0], 4 * (4 + j) + tig);
+        vc[j] = zs - C::OFF * ss;
+      }
+      if (g < G) {
+        float* d = dst + g * C::PSTRIDE;
+        if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          d[4 + 16 * mt + gid] = o[mt][nt][0] + o[mt][nt][1] + vc[mt / 2];
+          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + o[mt][nt][3] + vc[mt / 2];
+        }
+      }
+    }
+  }
+};
+
+// Log-sum-exp merge of a segment's partials -- its tail partial plus nparts
+// consecutive stream-K partials -- into the normalised output [G][D].  Partials
+// come from other CTAs, so they are read through L2.
+template <int D, int G>
+__device__ void final_merge(const float* tail, const float* parts, int nparts, float* out, int tid,
+                            int nthreads) {
+  constexpr int PS = D + 4;
+  for (int e = tid; e < G * D; e += nthreads) {
+    const int g = e / D, d = e % D;
+    float mx = __ldcg(tail + g * PS);
+    for (int i = 0; i < nparts; ++i) mx = fmaxf(mx, __ldcg(parts + (size_t)i * G * PS + g * PS));
+    float lsum = 0.f, osum = 0.f;
+    if (mx != -INFINITY) {
+      const float wt = exp2f(__ldcg(tail + g * PS) - mx);
+      lsum = wt * __ldcg(tail + g * PS + 1);
+      osum = wt * __ldcg(tail + g * PS + 4 + d);
+      for (int i = 0; i < nparts; ++i) {
+        const float* src = parts + (size_t)i * G * PS + g * PS;
+        const float w = exp2f(__ldcg(src) - mx);
+        lsum += w * __ldcg(src + 1);
+        osum += w * __ldcg(src + 4 + d);
+      }
+    }
+    out[g * D + d] = lsum > 0.f ? osum / lsum : 0.f;
+  }
+}
+
+template <int D, int BITS, int G>
+__global__ void __launch_bounds__(DecodeCfg<D, BITS, G>::WARPS * 32)
+decode_kernel(const DecodeParams p) {
+  using C = DecodeCfg<D, BITS, G>;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_last;
+  uint8_t* ring = smem;
+  __half* ps_all = reinterpret_cast<__half*>(smem + C::RING);
+  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS);
+  int* s_ne = s_pref + (KVQ_MAX_BATCH + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __half* ps = ps_all + warp * G * kGroup;
+  uint8_t* wring = ring + warp * C::NSTAGE * C::STAGE;
+
+  build_prefix(p, s_pref, s_ne);
+  __syncthreads();
+  const int64_t total = (int64_t)p.hkv * s_pref[p.batch];
+  const int64_t nstream = total < p.n_stream ? total : p.n_stream;
+  const int R = p.tail_cap;
+  const int nseg = p.batch * p.hkv;
+
+  // Participants of segment (b, h): its tail warp and the stream-K CTAs
+  // [c0, c1] whose ranges meet it; CTA c keeps its partial in slot c + k with k
+  // the segment's index among nonempty segments (distinct for every pair).
+  struct SegInfo {
+    int target;
+    int64_t c0, k;
+    int nparts;
+  };
+  auto seg_info = [&](int b, int h) -> SegInfo {
+    SegInfo si{1, 0, 0, 0};
+    const int items = s_pref[b + 1] - s_pref[b];
+    if (items > 0) {
+      const int64_t A = (int64_t)p.hkv * s_pref[b] + (int64_t)h * items;
+      si.c0 = cta_of(A, total, nstream);
+      si.nparts = (int)(cta_of(A + items - 1, total, nstream) - si.c0 + 1);
+      si.k = (int64_t)p.hkv * s_ne[b] + h;
+      si.target = 1 + si.nparts;
+    }
+    return si;
+  };
+  auto out_ptr = [&](int b, int h) { return p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D; };
+  auto part_ptr = [&](int64_t slot) { return p.part + (size_t)slot * G * C::PSTRIDE; };
+
+  if ((int)blockIdx.x < p.n_tail_ctas) {
+    // ---------------- tail warps: one per (sequence, KV head)
+    const int seg = blockIdx.x * C::WARPS + warp;
+    if (seg >= nseg) return;
+    const int b = seg / p.hkv, h = seg % p.hkv;
+    const SeqLen L = read_lengths(p, b, false);
+    Decoder<D, BITS, G> dec;
+    dec.init(p, b, h);
+    const __half* kt = p.k_tail + (size_t)seg * R * D;
+    const __half* vt = p.v_tail + (size_t)seg * R * D;
+    for (int first = 0; first < L.nt; first += kGroup)
+      dec.tail_chunk(kt, vt, first, min(kGroup, L.nt - first), L.th, R, ps, p.scale_log2);
+    float* mine = p.tail_part + (size_t)seg * G * C::PSTRIDE;
+    dec.write_partial(mine);
+    __threadfence();
+    __syncwarp();
+    const SegInfo si = seg_info(b, h);
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&p.counters[seg], 1) == si.target - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      final_merge<D, G>(mine, part_ptr(si.c0 + si.k), si.nparts, out_ptr(b, h), lane, 32);
+      if (lane == 0) p.counters[seg] = 0;
+    }
+    return;
+  }
+
+  // ---------------- stream-K CTAs over the quantized groups
+  const int64_t c = (int64_t)blockIdx.x - p.n_tail_ctas;
+  if (c >= nstream) return;
+  const int64_t r0 = c * total / nstream, r1 = (c + 1) * total / nstream;
+  for (int64_t x = r0; x < r1;) {
+    // segment containing x: the largest b with hkv * pref[b] <= x
+    int lo = 0, hi = p.batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)p.hkv * s_pref[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int items = s_pref[b + 1] - s_pref[b];
+    const int64_t off = x - (int64_t)p.hkv * s_pref[b];
+    const int h = (int)(off / items);
+    const int g0 = (int)(off % items);
+    const int64_t xe = min(r1, x + (items - g0));
+    const int n = (int)(xe - x);
+    const int seg = b * p.hkv + h;
+    // this warp's contiguous share of groups [g0, g0 + n)
+    const int per = (n + C::WARPS - 1) / C::WARPS;
+    const int ga = g0 + min(n, warp * per), cnt = min(n, (warp + 1) * per) - min(n, warp * per);
+    Decoder<D, BITS, G> dec;
+    dec.init(p, b, h);
+    {
+      const size_t gbase = (size_t)seg * p.max_groups + ga;
+      auto issue = [&](int idx, int slotn) {
+        const size_t g = gbase + idx;
+        uint8_t* dst = wring + slotn * C::STAGE;
+        const uint8_t* kc = p.k_codes + g * C::TB;
+        const uint8_t* vc = p.v_codes + g * C::TB;
+        const uint8_t* km = reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA;
+        const uint8_t* vm = reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA;
+#pragma unroll
+        for (int o = lane * 16; o < C::TB; o += 512) cp_async_16(dst + o, kc + o);
+#pragma unroll
+        for (int o = lane * 16; o < C::TB; o += 512) cp_async_16(dst + C::TB + o, vc + o);
+#pragma unroll
+        for (int o = lane * 16; o < C::KMETA; o += 512) cp_async_16(dst + 2 * C::TB + o, km + o);
+#pragma unroll
+        for (int o = lane * 16; o < C::VMETA; o += 512)
+          cp_async_16(dst + 2 * C::TB + C::KMETA + o, vm + o);
+      };
+#pragma unroll
+      for (int s = 0; s < C::NSTAGE - 1; ++s) {
+        if (s < cnt) issue(s, s);
+        cp_async_commit();
+      }
+      for (int i = 0; i < cnt; ++i) {
+        if (i + C::NSTAGE - 1 < cnt) issue(i + C::NSTAGE - 1, (i + C::NSTAGE - 1) % C::NSTAGE);
+        cp_async_commit();
+        cp_async_wait<C::NSTAGE - 1>();
+        __syncwarp();
+        dec.quant_group(wring + (i % C::NSTAGE) * C::STAGE, ps, p.scale_log2);
+      }
+      cp_async_wait<0>();
+      __syncwarp();
+    }
+    // warp partial into the warp's (now idle) ring slice
+    dec.write_partial(reinterpret_cast<float*>(wring));
+    __syncthreads();
+    const SegInfo si = seg_info(b, h);
+    float* slot = part_ptr(c + si.k);
+    for (int e2 = threadIdx.x; e2 < G * D; e2 += blockDim.x) {
+      const int g = e2 / D, d = e2 % D;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::WARPS; ++w)
+        mx = fmaxf(mx, reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE)[g * C::PSTRIDE]);
+      float lsum = 0.f, osum = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < C::WARPS; ++w) {
+          const float* src = reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE) + g * C::PSTRIDE;
+          const float wt = exp2f(src[0] - mx);
+          lsum += wt * src[1];
+          osum += wt * src[4 + d];
+        }
+      }
+      slot[g * C::PSTRIDE + 4 + d] = osum;
+      if (d == 0) { slot[g * C::PSTRIDE] = mx; slot[g * C::PSTRIDE + 1] = lsum; }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&p.counters[seg], 1) == si.target - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      final_merge<D, G>(p.tail_part + (size_t)seg * G * C::PSTRIDE, part_ptr(si.c0 + si.k), si.nparts,
+                        out_ptr(b, h), threadIdx.x, blockDim.x);
+      if (threadIdx.x == 0) p.counters[seg] = 0;
+    }
+    __syncthreads();
+    x = xe;
+  }
+}
+
+struct DecodeLayout {
+  size_t counters, tail_part, part, total;
+};
+
+inline int decode_warps(int bits) { return bits == 8 ? 4 : 8; }
+
+inline DecodeLayout decode_layout(const kvq_cache* c, int G, int n_stream) {
+  DecodeLayout L;
+  const size_t seg = (size_t)c->batch * c->n_kv_heads;
+  const size_t pstride = (size_t)(c->head_dim + 4) * 4 * G;
+  L.counters = 0;
+  L.tail_part = ((seg * 4 + 255) / 256) * 256;
+  L.part = L.tail_part + seg * pstride;
+  L.total = L.part + ((size_t)n_stream + seg) * pstride;
+  return L;
+}
+
+template <int D, int BITS, int G>
+struct DecodeLaunch {
+  static int slots(int* err) {
+    // resident CTAs on the whole GPU (one wave), computed once per instantiation
+    static int cached = -1;
+    if (cached < 0) {
+      using C = DecodeCfg<D, BITS, G>;
+      int dev = 0, sms = 0, per = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaFuncSetAttribute(decode_kernel<D, BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<D, BITS, G>, C::WARPS * 32,
+                                                        C::SMEM) != cudaSuccess || per < 1) {
+        *err = 1;
+        return 0;
+      }
+      cached = sms * per;
+    }
+    return cached;
+  }
+  static kvq_status run(DecodeParams p, int batch, int hkv, cudaStream_t s) {
+    using C = DecodeCfg<D, BITS, G>;
+    int err = 0;
+    const int n = slots(&err);
+    if (err) return KVQ_ERR_CUDA;
+    p.n_stream = n;
+    p.n_tail_ctas = (batch * hkv + C::WARPS - 1) / C::WARPS;
+    dim3 grid(p.n_tail_ctas + p.n_stream);
+    decode_kernel<D, BITS, G><<<grid, C::WARPS * 32, C::SMEM, s>>>(p);
+    return launch_status();
+  }
+};
+
+template <int D, int BITS>
+kvq_status decode_dispatch_g(int G, const DecodeParams& p, int batch, int hkv, cudaStream_t s) {
+  switch (G) {
+    case 1: return DecodeLaunch<D, BITS, 1>::run(p, batch, hkv, s);
+    case 2: return DecodeLaunch<D, BITS, 2>::run(p, batch, hkv, s);
+    case 4: return DecodeLaunch<D, BITS, 4>::run(p, batch, hkv, s);
+    case 8: return DecodeLaunch<D, BITS, 8>::run(p, batch, hkv, s);
+    default: return KVQ_ERR_UNSUPPORTED;
+  }
+}
+
+inline int decode_slots(const kvq_cache* c, int G, int* err) {
+#define KVQ_SLOTS(D_, B_, G_) \
+  if (c->head_dim == D_ && c->bits == B_ && G == G_) return DecodeLaunch<D_, B_, G_>::slots(err);
+#define KVQ_SLOTS_G(D_, B_) KVQ_SLOTS(D_, B_, 1) KVQ_SLOTS(D_, B_, 2) KVQ_SLOTS(D_, B_, 4) KVQ_SLOTS(D_, B_, 8)
+  KVQ_SLOTS_G(128, 2) KVQ_SLOTS_G(128, 4) KVQ_SLOTS_G(128, 8)
+  KVQ_SLOTS_G(64, 2) KVQ_SLOTS_G(64, 4) KVQ_SLOTS_G(64, 8)
+#undef KVQ_SLOTS_G
+#undef KVQ_SLOTS
+  *err = 2;
+  return 0;
+}
+
+inline kvq_status validate_decode(const kvq_cache* c, int32_t n_q_heads, int* G) {
+  kvq_status s = validate_cache(c);
+  if (s != KVQ_OK) return s;
+  if (c->batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
+  if (n_q_heads < c->n_kv_heads || n_q_heads % c->n_kv_heads) return KVQ_ERR_INVALID;
+  const int g = n_q_heads / c->n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return KVQ_ERR_UNSUPPORTED;
+  *G = g;
+  return KVQ_OK;
+}
+
+}  // namespace kvq
+
+extern "C" kvq_status kvq_decode_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, size_t* bytes) {
+  using namespace kvq;
+  int G = 0;
+  kvq_status s = validate_geometry(c);
+  if (s != KVQ_OK) return s;
+  if (bytes == nullptr) return KVQ_ERR_INVALID;
+  if (c->batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
+  if (n_q_heads < c->n_kv_heads || n_q_heads % c->n_kv_heads) return KVQ_ERR_INVALID;
+  G = n_q_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ_ERR_UNSUPPORTED;
+  int err = 0;
+  const int n = decode_slots(c, G, &err);
+  if (err) return KVQ_ERR_CUDA;
+  *bytes = decode_layout(c, G, n).total;
+  return KVQ_OK;
+}
+
+extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, const void* q, float* out,
+                                      float sm_scale, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  using namespace kvq;
+  int G = 0;
+  kvq_status s = validate_decode(c, n_q_heads, &G);
+  if (s != KVQ_OK) return s;
+  if (q == nullptr || out == nullptr || workspace == nullptr) return KVQ_ERR_INVALID;
+  if (!aligned(q, 4) || !aligned(out, 4) || !aligned(workspace, 16)) return KVQ_ERR_INVALID;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID;
+  int err = 0;
+  const int n = decode_slots(c, G, &err);
+  if (err) return KVQ_ERR_CUDA;
+  const DecodeLayout L = decode_layout(c, G, n);
+  if (workspace_bytes < L.total) return KVQ_ERR_INVALID;
+  DecodeParams p{};
+  p.k_codes = static_cast<const uint8_t*>(c->k_codes);
+  p.v_codes = static_cast<const uint8_t*>(c->v_codes);
+  p.k_meta = static_cast<const __half*>(c->k_meta);
+  p.v_meta = static_cast<const __half*>(c->v_meta);
+  p.k_tail = static_cast<const __half*>(c->k_tail);
+  p.v_tail = static_cast<const __half*>(c->v_tail);
+  p.n_quant = c->n_quant;
+  p.n_tail = c->n_tail;
+  p.tail_head = c->tail_head;
+  p.error_flags = c->error_flags;
+  p.q = static_cast<const __half*>(q);
+  p.out = out;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
+  p.tail_part = reinterpret_cast<float*>(ws + L.tail_part);
+  p.part = reinterpret_cast<float*>(ws + L.part);
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.batch = c->batch;
+  p.hkv = c->n_kv_heads;
+  p.max_groups = c->max_groups;
+  p.tail_cap = c->tail_cap;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->head_dim == 128) {
+    if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, c->batch, c->n_kv_heads, st);
+    if (c->bits == 4) return decode_dispatch_g<128, 4>(G, p, c->batch, c->n_kv_heads, st);
+    return decode_dispatch_g<128, 8>(G, p, c->batch, c->n_kv_heads, st);
+  }
+  if (c->bits == 2) return decode_dispatch_g<64, 2>(G, p, c->batch, c->n_kv_heads, st);
+  if (c->bits == 4) return decode_dispatch_g<64, 4>(G, p, c->batch, c->n_kv_heads, st);
+  return decode_dispatch_g<64, 8>(G, p, c->batch, c->n_kv_heads, st);
+}

@@ -1,0 +1,250 @@
+// Prefill quantization and per-token append (with the 32-token flush) of the
+// uniform cache.  One warp quantizes one 32-token tile of keys (per channel)
+// and values (per token) and writes packed codes and fp16 metadata in one
+// coalesced pass.
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr int kPrefillWarps = 4;
+constexpr int kAppendWarps = 8;
+
+struct PrefillParams {
+  const __half* k;
+  const __half* v;
+  int64_t sb, st, sh;
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  __half* k_meta;
+  __half* v_meta;
+  __half* k_tail;
+  __half* v_tail;
+  int32_t* n_quant;
+  int32_t* n_tail;
+  int32_t* tail_head;
+  int32_t hkv, max_groups, tail_cap;
+  int32_t seq_len[KVQ_MAX_BATCH];
+  int32_t ntail[KVQ_MAX_BATCH];
+};
+
+// grid (work items / warps, Hkv, B); a work item is a 32-token tile to quantize
+// or a chunk of up to 32 tail tokens to copy.
+template <int D, int BITS>
+__global__ void __launch_bounds__(kPrefillWarps * 32)
+prefill_kernel(const __grid_constant__ PrefillParams p) {
+  __shared__ __align__(16) uint8_t s_ct[kPrefillWarps][kGroup * D];
+  __shared__ __align__(16) __half s_vm[kPrefillWarps][2 * D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int item = blockIdx.x * kPrefillWarps + warp;
+  const int seq = p.seq_len[b], nt = p.ntail[b];
+  const int nq = seq - nt, ng = nq / kGroup;
+  if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
+    p.n_quant[b] = nq;
+    p.n_tail[b] = nt;
+    p.tail_head[b] = 0;
+  }
+  const size_t bh = (size_t)b * p.hkv + h;
+  const __half* kseq = p.k + (int64_t)b * p.sb + (int64_t)h * p.sh;
+  const __half* vseq = p.v + (int64_t)b * p.sb + (int64_t)h * p.sh;
+  if (item < ng) {
+    using T = Tile<D, BITS>;
+    const size_t gi = bh * p.max_groups + item;
+    quantize_tile_warp<D, BITS>(kseq + (int64_t)item * kGroup * p.st,
+                                vseq + (int64_t)item * kGroup * p.st, p.st,
+                                p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
+                                p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D, s_ct[warp],
+                                s_vm[warp], lane);
+  } else if (item < ng + (nt + kGroup - 1) / kGroup) {
+    // copy tail tokens [nq + 32c, nq + 32c + 32) to ring slots 32c.. (ring head 0)
+    const int c = item - ng;
+    constexpr int CPL = D / 32;
+    for (int i = 32 * c; i < min(nt, 32 * c + 32); ++i) {
+      const int64_t src = (int64_t)(nq + i) * p.st + lane * CPL;
+      const size_t dst = (bh * p.tail_cap + i) * D + lane * CPL;
+      if (CPL == 4) {
+        *reinterpret_cast<uint2*>(p.k_tail + dst) = *reinterpret_cast<const uint2*>(kseq + src);
+        *reinterpret_cast<uint2*>(p.v_tail + dst) = *reinterpret_cast<const uint2*>(vseq + src);
+      } else {
+        *reinterpret_cast<uint32_t*>(p.k_tail + dst) = *reinterpret_cast<const uint32_t*>(kseq + src);
+        *reinterpret_cast<uint32_t*>(p.v_tail + dst) = *reinterpret_cast<const uint32_t*>(vseq + src);
+      }
+    }
+  }
+}
+
+struct AppendParams {
+  const __half* k_new;
+  const __half* v_new;
+  uint8_t* k_codes;
+  uint8_t* v_codes;
+  __half* k_meta;
+  __half* v_meta;
+  __half* k_tail;
+  __half* v_tail;
+  int32_t* n_quant;
+  int32_t* n_tail;
+  int32_t* tail_head;
+  int32_t* error_flags;
+  int32_t hkv, max_groups, tail_cap;
+};
+
+// grid (B); each block owns one sequence so the length update is race-free.
+template <int D, int BITS>
+__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p) {
+  __shared__ __align__(16) uint8_t s_ct[kAppendWarps][kGroup * D];
+  __shared__ __align__(16) __half s_vm[kAppendWarps][2 * D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x;
+  const int R = p.tail_cap;
+  const int nq = p.n_quant[b], nt = p.n_tail[b], hd = p.tail_head[b];
+  const bool sane = nq >= 0 && nq % kGroup == 0 && nq / kGroup <= p.max_groups && nt >= 0 &&
+                    nt <= R && hd >= 0 && hd < R && hd % kGroup == 0;
+  const bool flush = sane && nt == R;
+  const bool fits = !flush || nq / kGroup < p.max_groups;
+  if (!sane || !fits) {
+    if (threadIdx.x == 0 && p.error_flags != nullptr)
+      atomicOr(p.error_flags, sane ? KVQ_DEVERR_APPEND_CAPACITY : KVQ_DEVERR_BAD_LENGTHS);
+    return;
+  }
+  const int hd2 = flush ? (hd + kGroup) % R : hd;
+  const int nt2 = flush ? nt - kGroup : nt;
+  const int slot = (hd2 + nt2) % R;
+  constexpr int CPL = D / 32;
+  for (int h = warp; h < p.hkv; h += kAppendWarps) {
+    const size_t bh = (size_t)b * p.hkv + h;
+    __half* kt = p.k_tail + bh * R * D;
+    __half* vt = p.v_tail + bh * R * D;
+    if (flush) {
+      using T = Tile<D, BITS>;
+      const size_t gi = bh * p.max_groups + nq / kGroup;
+      quantize_tile_warp<D, BITS>(kt + (size_t)hd * D, vt + (size_t)hd * D, D,
+                                  p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
+                                  p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D, s_ct[warp],
+                                  s_vm[warp], lane);
+    }
+    const size_t src = bh * D + lane * CPL;
+    const size_t dst = (size_t)slot * D + lane * CPL;
+    if (CPL == 4) {
+      *reinterpret_cast<uint2*>(kt + dst) = *reinterpret_cast<const uint2*>(p.k_new + src);
+      *reinterpret_cast<uint2*>(vt + dst) = *reinterpret_cast<const uint2*>(p.v_new + src);
+    } else {
+      *reinterpret_cast<uint32_t*>(kt + dst) = *reinterpret_cast<const uint32_t*>(p.k_new + src);
+      *reinterpret_cast<uint32_t*>(vt + dst) = *reinterpret_cast<const uint32_t*>(p.v_new + src);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    p.n_quant[b] = nq + (flush ? kGroup : 0);
+    p.n_tail[b] = nt2 + 1;
+    p.tail_head[b] = hd2;
+  }
+}
+
+template <template <int, int> class F, typename... A>
+kvq_status dispatch_db(int d, int bits, A&&... args) {
+  if (d == 128) {
+    if (bits == 2) return F<128, 2>::run(args...);
+    if (bits == 4) return F<128, 4>::run(args...);
+    if (bits == 8) return F<128, 8>::run(args...);
+  } else if (d == 64) {
+    if (bits == 2) return F<64, 2>::run(args...);
+    if (bits == 4) return F<64, 4>::run(args...);
+    if (bits == 8) return F<64, 8>::run(args...);
+  }
+  return KVQ_ERR_UNSUPPORTED;
+}
+
+template <int D, int BITS>
+struct PrefillLaunch {
+  static kvq_status run(const PrefillParams& p, int batch, int max_items, cudaStream_t s) {
+    dim3 grid((max_items + kPrefillWarps - 1) / kPrefillWarps, p.hkv, batch);
+    prefill_kernel<D, BITS><<<grid, kPrefillWarps * 32, 0, s>>>(p);
+    return launch_status();
+  }
+};
+
+template <int D, int BITS>
+struct AppendLaunch {
+  static kvq_status run(const AppendParams& p, int batch, cudaStream_t s) {
+    append_kernel<D, BITS><<<batch, kAppendWarps * 32, 0, s>>>(p);
+    return launch_status();
+  }
+};
+
+}  // namespace kvq
+
+extern "C" kvq_status kvq_quantize_prefill(const kvq_cache* c, const void* k, const void* v,
+                                           int64_t stride_b, int64_t stride_t, int64_t stride_h,
+                                           const int32_t* seq_len, const int32_t* n_tail,
+                                           void* stream) {
+  using namespace kvq;
+  kvq_status s = validate_cache(c);
+  if (s != KVQ_OK) return s;
+  if (c->batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
+  if (k == nullptr || v == nullptr || seq_len == nullptr || n_tail == nullptr) return KVQ_ERR_INVALID;
+  if (!aligned(k, 8) || !aligned(v, 8)) return KVQ_ERR_INVALID;
+  if (stride_b % 4 || stride_t % 4 || stride_h % 4) return KVQ_ERR_INVALID;
+  if (stride_b < 0 || stride_t < 0 || stride_h < 0) return KVQ_ERR_INVALID;
+  PrefillParams p{};
+  int max_items = 0;
+  for (int b = 0; b < c->batch; ++b) {
+    const int L = seq_len[b], nt = n_tail[b];
+    if (L < 0 || nt < 0 || nt > L || nt > c->tail_cap) return KVQ_ERR_INVALID;
+    if ((L - nt) % KVQ_GROUP) return KVQ_ERR_INVALID;
+    if ((L - nt) / KVQ_GROUP > c->max_groups) return KVQ_ERR_CAPACITY;
+    p.seq_len[b] = L;
+    p.ntail[b] = nt;
+    const int items = (L - nt) / KVQ_GROUP + (nt + KVQ_GROUP - 1) / KVQ_GROUP;
+    max_items = items > max_items ? items : max_items;
+  }
+  p.k = static_cast<const __half*>(k);
+  p.v = static_cast<const __half*>(v);
+  p.sb = stride_b;
+  p.st = stride_t;
+  p.sh = stride_h;
+  p.k_codes = static_cast<uint8_t*>(c->k_codes);
+  p.v_codes = static_cast<uint8_t*>(c->v_codes);
+  p.k_meta = static_cast<__half*>(c->k_meta);
+  p.v_meta = static_cast<__half*>(c->v_meta);
+  p.k_tail = static_cast<__half*>(c->k_tail);
+  p.v_tail = static_cast<__half*>(c->v_tail);
+  p.n_quant = c->n_quant;
+  p.n_tail = c->n_tail;
+  p.tail_head = c->tail_head;
+  p.hkv = c->n_kv_heads;
+  p.max_groups = c->max_groups;
+  p.tail_cap = c->tail_cap;
+  if (max_items == 0) max_items = 1;  // still write the lengths
+  if (c->n_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+  return dispatch_db<PrefillLaunch>(c->head_dim, c->bits, p, c->batch, max_items,
+                                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kvq_status kvq_append_token(const kvq_cache* c, const void* k_new, const void* v_new,
+                                       void* stream) {
+  using namespace kvq;
+  kvq_status s = validate_cache(c);
+  if (s != KVQ_OK) return s;
+  if (k_new == nullptr || v_new == nullptr || !aligned(k_new, 8) || !aligned(v_new, 8))
+    return KVQ_ERR_INVALID;
+  AppendParams p{};
+  p.k_new = static_cast<const __half*>(k_new);
+  p.v_new = static_cast<const __half*>(v_new);
+  p.k_codes = static_cast<uint8_t*>(c->k_codes);
+  p.v_codes = static_cast<uint8_t*>(c->v_codes);
+  p.k_meta = static_cast<__half*>(c->k_meta);
+  p.v_meta = static_cast<__half*>(c->v_meta);
+  p.k_tail = static_cast<__half*>(c->k_tail);
+  p.v_tail = static_cast<__half*>(c->v_tail);
+  p.n_quant = c->n_quant;
+  p.n_tail = c->n_tail;
+  p.tail_head = c->tail_head;
+  p.error_flags = c->error_flags;
+  p.hkv = c->n_kv_heads;
+  p.max_groups = c->max_groups;
+  p.tail_cap = c->tail_cap;
+  return dispatch_db<AppendLaunch>(c->head_dim, c->bits, p, c->batch,
+                                   static_cast<cudaStream_t>(stream));
+}

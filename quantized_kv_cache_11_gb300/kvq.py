@@ -1,0 +1,261 @@
+"""Thin Python binding of libkvq.so (the C ABI declared in include/kvq.h).
+
+Argument marshalling only: every step of the quantizer and of the decode runs
+in the library's CUDA kernels.  Tensors are PyTorch CUDA tensors; PyTorch is
+used for device memory and streams only.  There is no CPU fallback: if the
+shared library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+KVQ_OK = 0
+KVQ_ERR_INVALID = -1
+KVQ_ERR_UNSUPPORTED = -2
+KVQ_ERR_CAPACITY = -3
+KVQ_ERR_CUDA = -4
+KVQ_DEVERR_APPEND_CAPACITY = 1
+KVQ_DEVERR_BAD_LENGTHS = 2
+KVQ_GROUP = 32
+KVQ_MAX_BATCH = 512
+KVQ_NBUF = 7
+(KVQ_BUF_K_CODES, KVQ_BUF_V_CODES, KVQ_BUF_K_META, KVQ_BUF_V_META, KVQ_BUF_K_TAIL,
+ KVQ_BUF_V_TAIL, KVQ_BUF_LENGTHS) = range(7)
+
+# Every entry point of include/kvq.h.
+EXPORTS = ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
+           "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_status_string",
+           "kvq_version")
+
+
+class kvq_cache(ctypes.Structure):
+    """Mirror of ``struct kvq_cache``."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("bits", ctypes.c_int32),
+        ("max_groups", ctypes.c_int32),
+        ("tail_cap", ctypes.c_int32),
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_meta", ctypes.c_void_p),
+        ("v_meta", ctypes.c_void_p),
+        ("k_tail", ctypes.c_void_p),
+        ("v_tail", ctypes.c_void_p),
+        ("n_quant", ctypes.c_void_p),
+        ("n_tail", ctypes.c_void_p),
+        ("tail_head", ctypes.c_void_p),
+        ("error_flags", ctypes.c_void_p),
+    ]
+
+
+class KVQError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libkvq.so (built in-tree).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m quantized_kv_cache_11_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    c_int, c_i64, c_f, c_vp, c_sz = (ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                     ctypes.c_void_p, ctypes.c_size_t)
+    cache_p = P(kvq_cache)
+    lib.kvq_cache_bytes.argtypes = [cache_p, P(c_sz)]
+    lib.kvq_quantize_prefill.argtypes = [cache_p, c_vp, c_vp, c_i64, c_i64, c_i64,
+                                         P(ctypes.c_int32), P(ctypes.c_int32), c_vp]
+    lib.kvq_append_token.argtypes = [cache_p, c_vp, c_vp, c_vp]
+    lib.kvq_decode_workspace_bytes.argtypes = [cache_p, ctypes.c_int32, P(c_sz)]
+    lib.kvq_decode_attn.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_sz, c_vp]
+    lib.kvq_status_string.argtypes = [c_int]
+    lib.kvq_status_string.restype = ctypes.c_char_p
+    lib.kvq_version.argtypes = []
+    lib.kvq_version.restype = ctypes.c_char_p
+    for name in ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
+                 "kvq_decode_workspace_bytes", "kvq_decode_attn"):
+        getattr(lib, name).restype = c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().kvq_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != KVQ_OK:
+        raise KVQError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def kvq_cache_bytes(desc: kvq_cache) -> list:
+    sizes = (ctypes.c_size_t * KVQ_NBUF)()
+    _check("kvq_cache_bytes", load_library().kvq_cache_bytes(ctypes.byref(desc), sizes))
+    return list(sizes)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def kvq_quantize_prefill(cache: "QuantizedKVCache", k: torch.Tensor, v: torch.Tensor,
+                         seq_len: Sequence[int], n_tail: Sequence[int], stream=None) -> None:
+    """k, v: fp16 CUDA tensors [B, T, Hkv, D] (same strides, D contiguous)."""
+    _need(k, torch.float16, "k")
+    _need(v, torch.float16, "v")
+    if k.shape != v.shape or k.stride() != v.stride() or k.stride(3) != 1:
+        raise ValueError("k and v need equal shapes and strides with a contiguous last dim")
+    B = cache.batch
+    sl = (ctypes.c_int32 * B)(*[int(x) for x in seq_len])
+    nt = (ctypes.c_int32 * B)(*[int(x) for x in n_tail])
+    st = load_library().kvq_quantize_prefill(
+        ctypes.byref(cache.desc), _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2),
+        sl, nt, _stream(stream))
+    _check("kvq_quantize_prefill", st)
+
+
+def kvq_append_token(cache: "QuantizedKVCache", k_new: torch.Tensor, v_new: torch.Tensor,
+                     stream=None) -> None:
+    """k_new, v_new: fp16 CUDA tensors [B, Hkv, D], contiguous."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.float16, n)
+        if not t.is_contiguous() or t.shape != (cache.batch, cache.n_kv_heads, cache.head_dim):
+            raise ValueError(f"{n} must be a contiguous [B, Hkv, D] tensor")
+    st = load_library().kvq_append_token(ctypes.byref(cache.desc), _ptr(k_new), _ptr(v_new),
+                                         _stream(stream))
+    _check("kvq_append_token", st)
+
+
+def kvq_decode_workspace_bytes(cache: "QuantizedKVCache", n_q_heads: int) -> int:
+    out = ctypes.c_size_t()
+    _check("kvq_decode_workspace_bytes", load_library().kvq_decode_workspace_bytes(
+        ctypes.byref(cache.desc), int(n_q_heads), ctypes.byref(out)))
+    return out.value
+
+
+def kvq_decode_attn(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.Tensor,
+                    sm_scale: float, workspace: torch.Tensor, stream=None) -> None:
+    """q: fp16 [B, Hq, D] contiguous; out: fp32 [B, Hq, D] contiguous;
+    workspace: uint8 CUDA tensor, zero-filled before first use."""
+    _need(q, torch.float16, "q")
+    _need(out, torch.float32, "out")
+    _need(workspace, torch.uint8, "workspace")
+    if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    st = load_library().kvq_decode_attn(ctypes.byref(cache.desc), q.shape[1], _ptr(q), _ptr(out),
+                                        float(sm_scale), _ptr(workspace), workspace.numel(),
+                                        _stream(stream))
+    _check("kvq_decode_attn", st)
+
+
+class QuantizedKVCache:
+    """Owns the device buffers of a uniform cache (allocated with PyTorch)."""
+
+    def __init__(self, batch: int, n_kv_heads: int, head_dim: int, bits: int, max_tokens: int,
+                 tail_cap: int = 32, device="cuda"):
+        self.batch, self.n_kv_heads, self.head_dim, self.bits = batch, n_kv_heads, head_dim, bits
+        self.tail_cap = tail_cap
+        self.max_groups = math.ceil(max_tokens / KVQ_GROUP)
+        d = kvq_cache(batch, n_kv_heads, head_dim, bits, self.max_groups, tail_cap)
+        sizes = kvq_cache_bytes(d)
+        dev = torch.device(device)
+
+        def buf(n, dtype=torch.uint8):
+            return torch.zeros(max(n, 16) // torch.empty((), dtype=dtype).element_size(),
+                               dtype=dtype, device=dev)
+
+        self.k_codes = buf(sizes[KVQ_BUF_K_CODES])
+        self.v_codes = buf(sizes[KVQ_BUF_V_CODES])
+        self.k_meta = buf(sizes[KVQ_BUF_K_META], torch.float16)
+        self.v_meta = buf(sizes[KVQ_BUF_V_META], torch.float16)
+        self.k_tail = buf(sizes[KVQ_BUF_K_TAIL], torch.float16)
+        self.v_tail = buf(sizes[KVQ_BUF_V_TAIL], torch.float16)
+        lens = torch.zeros(4, (batch + 3) // 4 * 4, dtype=torch.int32, device=dev)
+        self._lens = lens
+        self.n_quant, self.n_tail, self.tail_head = lens[0, :batch], lens[1, :batch], lens[2, :batch]
+        self.error_flags = lens[3, :1]
+        for f, t in (("k_codes", self.k_codes), ("v_codes", self.v_codes),
+                     ("k_meta", self.k_meta), ("v_meta", self.v_meta),
+                     ("k_tail", self.k_tail), ("v_tail", self.v_tail),
+                     ("n_quant", self.n_quant), ("n_tail", self.n_tail),
+                     ("tail_head", self.tail_head), ("error_flags", self.error_flags)):
+            setattr(d, f, t.data_ptr())
+        self.desc = d
+        self._workspaces = {}
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.k_codes, self.v_codes, self.k_meta, self.v_meta, self.k_tail, self.v_tail))
+
+    def views(self) -> dict:
+        """The buffers shaped as in include/kvq.h (no copies)."""
+        B, H, D, G, R = self.batch, self.n_kv_heads, self.head_dim, self.max_groups, self.tail_cap
+        tb = KVQ_GROUP * D * self.bits // 8
+        return {
+            "k_codes": self.k_codes[:B * H * G * tb].view(B, H, G, tb),
+            "v_codes": self.v_codes[:B * H * G * tb].view(B, H, G, tb),
+            "k_meta": self.k_meta[:B * H * G * 2 * D].view(B, H, G, 2, D),
+            "v_meta": self.v_meta[:B * H * G * 2 * D].view(B, H, G, 2, D // 32, 32),
+            "k_tail": self.k_tail[:B * H * R * D].view(B, H, R, D),
+            "v_tail": self.v_tail[:B * H * R * D].view(B, H, R, D),
+            "n_quant": self.n_quant, "n_tail": self.n_tail, "tail_head": self.tail_head,
+        }
+
+    def workspace(self, n_q_heads: int) -> torch.Tensor:
+        ws = self._workspaces.get(n_q_heads)
+        if ws is None:
+            ws = torch.zeros(kvq_decode_workspace_bytes(self, n_q_heads), dtype=torch.uint8,
+                             device=self.k_codes.device)
+            self._workspaces[n_q_heads] = ws
+        return ws
+
+    def prefill(self, k, v, seq_len, n_tail, stream=None):
+        kvq_quantize_prefill(self, k, v, seq_len, n_tail, stream)
+
+    def append(self, k_new, v_new, stream=None):
+        kvq_append_token(self, k_new, v_new, stream)
+
+    def decode(self, q, sm_scale: Optional[float] = None, out=None, stream=None):
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.head_dim)
+        kvq_decode_attn(self, q, out, sm_scale, self.workspace(q.shape[1]), stream)
+        return out
+
+    def device_errors(self) -> int:
+        """Read (with a sync) the device error bits."""
+        return int(self.error_flags.item())

@@ -1,0 +1,113 @@
+"""The C-ABI library loads, exports every entry point of include/kvq.h, and its
+host-side validation rejects bad arguments before any CUDA call (CPU-only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_kv_cache_11_gb300 import build, kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kvq.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert names == sorted(kvq.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert kvq.status_string(0) == "ok"
+    assert kvq.status_string(-1) == "invalid argument"
+    assert kvq.status_string(12345) == "unknown status"
+    assert lib.kvq_version().decode().count(".") == 2
+
+
+def test_cache_bytes_matches_layout(lib):
+    d = kvq.kvq_cache(2, 8, 128, 2, 4096 // 32, 64)
+    sizes = kvq.kvq_cache_bytes(d)
+    groups = 2 * 8 * 128
+    assert sizes[kvq.KVQ_BUF_K_CODES] == groups * 32 * 128 * 2 // 8
+    assert sizes[kvq.KVQ_BUF_V_CODES] == sizes[kvq.KVQ_BUF_K_CODES]
+    assert sizes[kvq.KVQ_BUF_K_META] == groups * 2 * 128 * 2
+    assert sizes[kvq.KVQ_BUF_V_META] == groups * 2 * 128 * 2
+    assert sizes[kvq.KVQ_BUF_K_TAIL] == 2 * 8 * 64 * 128 * 2
+    assert sizes[kvq.KVQ_BUF_LENGTHS] == 2 * 4
+    # Llama-3.1-8B 128k, 2-bit: codes + metadata per sequence = 100,663,296 bytes
+    d = kvq.kvq_cache(1, 8, 128, 2, 131072 // 32, 64)
+    s = kvq.kvq_cache_bytes(d)
+    assert sum(s[:4]) == 8 * 4096 * (1024 + 1024 + 512 + 512)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 96, kvq.KVQ_ERR_UNSUPPORTED), ("bits", 3, kvq.KVQ_ERR_UNSUPPORTED),
+    ("tail_cap", 40, kvq.KVQ_ERR_INVALID), ("tail_cap", 0, kvq.KVQ_ERR_INVALID),
+    ("batch", 0, kvq.KVQ_ERR_INVALID), ("max_groups", -1, kvq.KVQ_ERR_INVALID),
+])
+def test_cache_bytes_rejects_bad_geometry(lib, field, value, status):
+    d = kvq.kvq_cache(1, 8, 128, 2, 16, 32)
+    setattr(d, field, value)
+    sizes = (ctypes.c_size_t * kvq.KVQ_NBUF)()
+    assert lib.kvq_cache_bytes(ctypes.byref(d), sizes) == status
+
+
+def _fake_cache(**kw):
+    # Host-side validation only: pointers are never dereferenced when a check
+    # fails, so aligned fake addresses are enough.
+    d = kvq.kvq_cache(2, 4, 128, 2, 8, 32)
+    for i, f in enumerate(("k_codes", "v_codes", "k_meta", "v_meta", "k_tail", "v_tail",
+                           "n_quant", "n_tail", "tail_head")):
+        setattr(d, f, 0x10000 * (i + 1))
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_prefill_validation_fails_before_launch(lib):
+    i32 = ctypes.c_int32 * 2
+    d = _fake_cache()
+    call = lambda d, k=0x100000, sl=(64, 64), nt=(0, 0), st=(1 << 14, 512, 128): \
+        lib.kvq_quantize_prefill(ctypes.byref(d), k, k + 0x1000, *st, i32(*sl), i32(*nt), None)
+    assert call(_fake_cache(k_codes=None)) == kvq.KVQ_ERR_INVALID
+    assert call(_fake_cache(k_meta=0x10008)) == kvq.KVQ_ERR_INVALID  # misaligned
+    assert call(d, k=0) == kvq.KVQ_ERR_INVALID
+    assert call(d, sl=(65, 64)) == kvq.KVQ_ERR_INVALID  # 65 - 0 not a multiple of 32
+    assert call(d, sl=(64, 64), nt=(33, 0)) == kvq.KVQ_ERR_INVALID  # n_tail > R
+    assert call(d, sl=(320, 64)) == kvq.KVQ_ERR_CAPACITY  # 10 groups > 8
+    assert call(d, st=(1 << 14, 514, 128)) == kvq.KVQ_ERR_INVALID  # stride not multiple of 4
+    assert call(d, k=0x100002) == kvq.KVQ_ERR_INVALID  # k not 8-byte aligned
+    assert call(_fake_cache(head_dim=80)) == kvq.KVQ_ERR_UNSUPPORTED
+
+
+def test_decode_and_append_validation_fails_before_launch(lib):
+    d = _fake_cache()
+    ws = ctypes.c_size_t()
+    assert lib.kvq_decode_workspace_bytes(ctypes.byref(d), 6, ctypes.byref(ws)) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_decode_workspace_bytes(ctypes.byref(d), 12, ctypes.byref(ws)) == kvq.KVQ_ERR_UNSUPPORTED
+    dec = lambda d, hq=16, q=0x200000, out=0x300000, scale=0.088, w=0x400000, wb=1 << 30: \
+        lib.kvq_decode_attn(ctypes.byref(d), hq, q, out, scale, w, wb, None)
+    assert dec(d, hq=6) == kvq.KVQ_ERR_INVALID
+    assert dec(d, hq=48) == kvq.KVQ_ERR_UNSUPPORTED  # G = 12
+    assert dec(d, q=0) == kvq.KVQ_ERR_INVALID
+    assert dec(d, w=0) == kvq.KVQ_ERR_INVALID
+    assert dec(d, scale=0.0) == kvq.KVQ_ERR_INVALID
+    assert dec(d, scale=float("nan")) == kvq.KVQ_ERR_INVALID
+    assert dec(_fake_cache(n_tail=None)) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_append_token(ctypes.byref(d), 0, 0x1000, None) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_append_token(ctypes.byref(d), 0x1004, 0x1000, None) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_append_token(ctypes.byref(_fake_cache(bits=5)), 0x1000, 0x2000, None) == \
+        kvq.KVQ_ERR_UNSUPPORTED
