@@ -53,7 +53,7 @@ def algorithmic_bytes(w, n_quant, n_tail) -> int:
     """Bytes one decode step must move: packed K/V codes, fp16 scale + zero of
     every group, the fp16 tail, q in and the fp32 output."""
     D, H, b = w.head_dim, w.n_kv_heads, w.bits
-    per_tok = 2 * D * b // 8 + 2 * (2 * D // 32) * 2  # codes K+V, V meta (scale, zero per 32 ch)
+    per_tok = 2 * D * b // 8 + (2 * D // 32) * 2  # codes K+V, V meta (fp16 scale + zero per 32 ch)
     k_meta = (n_quant // 32) * 2 * D * 2  # per key group: scale + zero per channel
     tail = n_tail * D * 2 * 2
     return w.batch * H * (n_quant * per_tok + k_meta + tail) + w.batch * w.n_q_heads * D * (2 + 4)
