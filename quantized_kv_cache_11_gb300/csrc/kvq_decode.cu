@@ -7,20 +7,23 @@
 // products, never written out) and the fp16 tail tokens.
 //
 // How:
-// * Work partition (stream-K): the quantized 32-token groups of every
-//   (sequence, KV head) are laid end to end and the list is cut into equal
+// * Work partition (stream-K): the work items of every (sequence, KV head) --
+//   its quantized 32-token groups, then its fp16 tail chunks (each weighted as
+//   kTailWeight items) -- are laid end to end, and the list is cut into equal
 //   contiguous ranges, one per resident CTA, so ragged batches stay balanced.
-//   Inside a CTA each warp streams its own sub-range through a private
-//   multi-stage cp.async ring in shared memory.  The fp16 tail of each
-//   (sequence, KV head) is handled by one extra "tail warp".
+//   Inside a CTA each warp streams its own sub-range of groups through a private
+//   multi-stage cp.async ring in shared memory.
 // * Per 32-token group (one warp, the whole GQA group of G query heads):
-//   Q.K^T on tensor cores (mma.m16n8k16, fp16 in, fp32 accumulate) with
-//   A = 2^b + code (one logic op per pair of codes gives exact fp16 values) and
-//   B = q * scale split into two fp16 halves (hi + lo, exact), so the per
-//   channel scale folds into q once per group; the zero point and the 2^b
-//   offset fold into one per-group constant computed by a small extra MMA.
-//   Online softmax in fp32; P.V on tensor cores with B = p * scale (hi + lo)
-//   per 32-channel value group, the value zero point again in a small MMA.
+//   Q.K^T on tensor cores (mma.m16n8k16, fp16 in, fp32 accumulate).  The A
+//   operand is the codes as exact fp16 integers: one logic op ORs a code pair
+//   into the mantissas of 2^e (e chosen by the codes' bit position) and one
+//   fp16 subtraction removes 2^e.  B = q * scale, split into two fp16 halves
+//   (hi = fp16(q*s), lo = q*s - hi, exact), in separate columns, so the
+//   per-channel scale is applied to q once per group.  The zero points enter
+//   through one more small MMA (rows = zero points).  Online softmax in fp32;
+//   P.V likewise with B = p * scale (hi + lo) per 32-channel value group, the
+//   value zero points and the softmax denominator (a row of ones) from one
+//   small MMA.
 // * Splits are merged by log-sum-exp; the last CTA to finish a (sequence, KV
 //   head) merges and writes the output, then resets its counter.  No spin-wait.
 #include <cmath>
@@ -29,6 +32,8 @@
 #include "kvq_internal.h"
 
 namespace kvq {
+
+constexpr int kTailWeight = 3;  // a 32-token fp16 tail chunk counts as this many groups
 
 template <int D, int BITS, int G>
 struct DecodeCfg {
@@ -43,14 +48,15 @@ struct DecodeCfg {
   static constexpr int PPW = T::kPairsPerWord;
   static constexpr int WARPS = BITS == 8 ? 4 : 8;
   static constexpr int NSTAGE = BITS == 2 ? 4 : (BITS == 4 ? 2 : 3);
-  static constexpr float OFF = (float)(1 << BITS);
   static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
   static constexpr int RING = WARPS * NSTAGE * STAGE;
-  static constexpr int PS = WARPS * G * kGroup * 2;  // p~ exchange, halves
-  static constexpr int PREFIX = 2 * (KVQ_MAX_BATCH + 1) * 4;
-  static constexpr int SMEM = RING + PS + PREFIX;
+  static constexpr int PS = WARPS * G * kGroup * 2;  // p~ exchange (halves), bytes
+  static constexpr int ZERO = 4 * D;                 // zero row for lanes without a metadata row
+  static constexpr int PREFIX = (KVQ_MAX_BATCH + 1) * 4;
+  static constexpr int SMEM = RING + PS + ZERO + PREFIX;
   static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
   static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
+  static_assert(PS % 16 == 0 && RING % 16 == 0, "aligned shared regions");
 };
 
 struct DecodeParams {
@@ -67,11 +73,9 @@ struct DecodeParams {
   const __half* q;
   float* out;
   int32_t* counters;
-  float* tail_part;
   float* part;
   float scale_log2;
   int32_t batch, hkv, max_groups, tail_cap;
-  int32_t n_tail_ctas;
   int32_t n_stream;
 };
 
@@ -82,7 +86,7 @@ struct SeqLen {
 __device__ __forceinline__ SeqLen read_lengths(const DecodeParams& p, int b, bool report) {
   SeqLen s{p.n_quant[b], p.n_tail[b], p.tail_head[b]};
   const bool ok = s.nq >= 0 && s.nq % kGroup == 0 && s.nq / kGroup <= p.max_groups && s.nt >= 0 &&
-                  s.nt <= p.tail_cap && s.th >= 0 && s.th < p.tail_cap;
+                  s.nt <= p.tail_cap && s.th >= 0 && s.th < p.tail_cap && s.th % kGroup == 0;
   if (!ok) {
     if (report && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_BAD_LENGTHS);
     s = SeqLen{0, 0, 0};
@@ -90,45 +94,61 @@ __device__ __forceinline__ SeqLen read_lengths(const DecodeParams& p, int b, boo
   return s;
 }
 
-// s_pref[b] = quantized groups of sequences < b; s_ne[b] = nonempty sequences < b.
-__device__ void build_prefix(const DecodeParams& p, int* s_pref, int* s_ne) {
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  int run = 0, run_ne = 0;
-  for (int b0 = 0; b0 < p.batch; b0 += 32) {
-    const int b = b0 + lane;
-    int g = 0;
-    if (b < p.batch) g = read_lengths(p, b, blockIdx.x == 0).nq / kGroup;
-    int ne = g > 0 ? 1 : 0;
-    // inclusive warp scan
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, g, off);
-      const int c = __shfl_up_sync(0xffffffffu, ne, off);
-      if (lane >= off) { g += a; ne += c; }
-    }
-    if (b < p.batch) { s_pref[b + 1] = run + g; s_ne[b + 1] = run_ne + ne; }
-    run += __shfl_sync(0xffffffffu, g, 31);
-    run_ne += __shfl_sync(0xffffffffu, ne, 31);
-  }
-  if (lane == 0) { s_pref[0] = 0; s_ne[0] = 0; }
+// Work items of one (sequence, KV head): its groups, kTailWeight per tail chunk,
+// and at least one (an empty sequence still needs its zero output written).
+__device__ __forceinline__ int seq_items(const SeqLen& s) {
+  const int n = s.nq / kGroup + kTailWeight * ((s.nt + kGroup - 1) / kGroup);
+  return n > 0 ? n : 1;
 }
 
-// The stream-K CTA that owns global group index x (ranges [x*T/N, ...)).
+// s_pref[b] = work items of the sequences before b (per KV head).
+__device__ void build_prefix(const DecodeParams& p, int* s_pref) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int run = 0;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int v = (b < p.batch) ? seq_items(read_lengths(p, b, blockIdx.x == 0)) : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += a;
+    }
+    if (b < p.batch) s_pref[b + 1] = run + v;
+    run += __shfl_sync(0xffffffffu, v, 31);
+  }
+  if (lane == 0) s_pref[0] = 0;
+}
+
+// The stream-K CTA that owns global item x (CTA c owns [c*T/N, (c+1)*T/N)).
 __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
   return ((x + 1) * n - 1) / total;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int D, int BITS, int G>
 struct Decoder {
   using C = DecodeCfg<D, BITS, G>;
   static constexpr int NT = C::NT, KT = C::KT;
+  // Highest bit position (within a 16-bit half) a code can take inside the fp16
+  // mantissa; codes above it are read from the word shifted right by kShift.
+  static constexpr int kLim = 10 - BITS;
+  static constexpr int kShift = BITS == 2 ? 6 : 8;
+  static constexpr uint32_t kOnes = 0x3C003C00u;  // half2(1, 1)
 
   // Per-warp running state of the online softmax for the G heads.
-  float m[NT], l[NT];
-  float o[KT][NT][4];
-  float zc[NT][4];
+  float m[NT];
+  float o[KT][NT][4];  // P.V accumulators: rows = channels, columns (head, hi|lo)
+  float zc[NT][4];     // rows j < D/32: sum p~ * zero_j; row 8: sum p~ (the denominator)
   uint32_t qf[NT][KT][2];  // q pairs of column 8nt+gid (head 4nt + gid/2), 0 beyond G
+  uint32_t nhl;            // half2(-hl): 0 for the hi column, -1 for the lo column
+  uint32_t hi_only;        // half2(1 - hl)
+  uint32_t ones_a;         // the ones row of the value-constant MMA (lanes of row 8)
   int lane, gid, tig, hl;
 
   __device__ __forceinline__ void init(const DecodeParams& p, int b, int h) {
@@ -136,10 +156,12 @@ struct Decoder {
     gid = lane >> 2;
     tig = lane & 3;
     hl = gid & 1;
+    nhl = hl ? 0xBC00BC00u : 0u;
+    hi_only = hl ? 0u : kOnes;
+    ones_a = gid == 0 ? kOnes : 0u;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt] = -INFINITY;
-      l[nt] = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) zc[nt][i] = 0.f;
 #pragma unroll
@@ -156,33 +178,35 @@ struct Decoder {
     }
   }
 
-  // fp16 pair (2^b + c_first, 2^b + c_second) of pair P of the lane's packed words;
-  // P must be a compile-time constant after unrolling.
-  static __device__ __forceinline__ uint32_t unpack(const uint32_t* w, int P) {
-    const int k = P % C::PPW;
-    const int sh = BITS * k - (10 - BITS);
-    constexpr uint32_t M = (uint32_t)((1 << BITS) - 1) << (10 - BITS);
-    constexpr uint32_t MASK = M | (M << 16);
-    constexpr uint32_t EXPO = (uint32_t)((15 + BITS) << 10) * 0x10001u;
-    const uint32_t word = w[P / C::PPW];
-    const uint32_t x = sh >= 0 ? (word >> sh) : (word << -sh);
-    return (x & MASK) | EXPO;
+  // Exact fp16 pair (c_first, c_second) of pair P of the lane's packed words (w;
+  // ws = the words shifted right by kShift).  P is a compile-time constant after
+  // unrolling.  The code bits land in the mantissa of 2^(10-pos) (pos = their
+  // bit position), giving 2^(10-pos) + c exactly; the subtraction leaves c.
+  static __device__ __forceinline__ uint32_t unpack(const uint32_t* w, const uint32_t* ws, int P) {
+    const int pos0 = BITS * (P % C::PPW);
+    const bool direct = pos0 <= kLim;
+    const int pos = direct ? pos0 : pos0 - kShift;
+    const uint32_t word = direct ? w[P / C::PPW] : ws[P / C::PPW];
+    const uint32_t mask = ((uint32_t)((1 << BITS) - 1) << pos) * 0x10001u;
+    const uint32_t expo = (uint32_t)((25 - pos) << 10) * 0x10001u;  // half2(2^(10-pos))
+    const uint32_t raw = (word & mask) | expo;
+    return h2_as_u32(__hsub2(u32_as_h2(raw), u32_as_h2(expo)));
   }
-  // A fragment (4 registers) of pairs P0 .. P0+3.
-  static __device__ __forceinline__ void frag(const uint32_t* w, int P0, uint32_t (&a)[4]) {
+  static __device__ __forceinline__ void frag(const uint32_t* w, const uint32_t* ws, int P0,
+                                              uint32_t (&a)[4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = unpack(w, P0 + i);
+    for (int i = 0; i < 4; ++i) a[i] = unpack(w, ws, P0 + i);
   }
 
-  static __device__ __forceinline__ uint32_t split_mul(uint32_t a, uint32_t b, int lo) {
+  // hi column: fp16(x*y); lo column: x*y - fp16(x*y) (exact: x*y has <= 22 bits).
+  __device__ __forceinline__ uint32_t split_mul(uint32_t a, uint32_t b) const {
     const __half2 x = u32_as_h2(a), y = u32_as_h2(b);
     const __half2 hi = __hmul2_rn(x, y);
-    const __half2 rem = __hfma2(x, y, __hneg2(hi));  // exact remainder (fp16 product has <= 22 bits)
-    return lo ? h2_as_u32(rem) : h2_as_u32(hi);
+    return h2_as_u32(__hfma2(x, y, __hmul2_rn(hi, u32_as_h2(nhl))));
   }
 
-  // Online softmax over one 32-token chunk.  lg[nt][mt][r] are log2-domain logits of
-  // token 16mt + gid + 8r for head 4nt + tig.  Writes p~ (fp16) to ps.
+  // Online softmax over one 32-token chunk.  lg[nt][mt][r]: log2-domain logits of
+  // token 16mt + gid + 8r for head 4nt + tig.  Writes p~ (fp16) to ps[g][t].
   __device__ __forceinline__ void softmax(float (&lg)[NT][2][2], __half* ps) {
     bool need = false;
     float mloc[NT];
@@ -199,9 +223,8 @@ struct Decoder {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const float mnew = fmaxf(m[nt], mloc[nt]);
-        const float alpha = (mnew == m[nt]) ? 1.f : exp2f(m[nt] - mnew);
+        const float alpha = (mnew == m[nt]) ? 1.f : fast_exp2(m[nt] - mnew);
         m[nt] = mnew;
-        l[nt] *= alpha;
 #pragma unroll
         for (int i = 0; i < 4; ++i) zc[nt][i] *= alpha;
 #pragma unroll
@@ -214,21 +237,21 @@ struct Decoder {
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float pv = exp2f(lg[nt][mt][r] - m[nt]);
-          const __half ph = __float2half_rn(pv);
-          l[nt] += __half2float(ph);
-          if (g < G) ps[g * kGroup + 16 * mt + gid + 8 * r] = ph;
+      for (int mt = 0; mt < 2; ++mt) {
+        const __half2 ph = __floats2half2_rn(fast_exp2(lg[nt][mt][0] - m[nt]),
+                                             fast_exp2(lg[nt][mt][1] - m[nt]));
+        if (g < G) {
+          ps[g * kGroup + 16 * mt + gid] = __low2half(ph);
+          ps[g * kGroup + 16 * mt + gid + 8] = __high2half(ph);
         }
+      }
     }
     __syncwarp();
   }
 
   // p~ pairs for the V-side B fragments: column 8nt+gid (head 4nt + gid/2), tokens
   // 16kt + 2tig + 8r and +1.
-  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) {
+  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + (gid >> 1);
@@ -240,16 +263,22 @@ struct Decoder {
     }
   }
 
-  // One quantized 32-token group staged in shared memory.
-  __device__ __forceinline__ void quant_group(const uint8_t* stage, __half* ps, float scale_log2) {
+  // One quantized 32-token group staged in shared memory.  zrow: a zero row of
+  // at least D/2 words in shared memory.
+  __device__ __forceinline__ void quant_group(const uint8_t* stage, __half* ps, const uint32_t* zrow,
+                                              float scale_log2) {
     const uint4* s4 = reinterpret_cast<const uint4*>(stage);
-    uint32_t kw[C::NWL];
+    uint32_t kw[C::NWL], kws[C::NWL];
 #pragma unroll
     for (int ch = 0; ch < C::NWL / 4; ++ch) {
       const uint4 v = s4[ch * 32 + lane];
       kw[4 * ch] = v.x; kw[4 * ch + 1] = v.y; kw[4 * ch + 2] = v.z; kw[4 * ch + 3] = v.w;
     }
-    const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);  // scale pairs, then zero pairs
+#pragma unroll
+    for (int i = 0; i < C::NWL; ++i) kws[i] = kw[i] >> kShift;
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);  // scale pairs, zero pairs
+    // K-constant MMA rows: row 0 = zero points (lanes gid 0), other rows 0
+    const uint32_t* krow = gid == 0 ? km + D / 2 : zrow;
     float sacc[2][NT][4];
     float cacc[NT][4];
 #pragma unroll
@@ -259,43 +288,41 @@ struct Decoder {
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt) {
       const uint32_t sp0 = km[8 * kt + tig], sp1 = km[8 * kt + 4 + tig];
-      const uint32_t zp0 = km[D / 2 + 8 * kt + tig], zp1 = km[D / 2 + 8 * kt + 4 + tig];
       uint32_t a0[4], a1[4];
-      frag(kw, (kt * 2 + 0) * 4, a0);  // pairs of (kt, mt = 0)
-      frag(kw, (kt * 2 + 1) * 4, a1);  // pairs of (kt, mt = 1)
-      const uint32_t ac[4] = {gid == 0 ? zp0 : (gid == 1 ? sp0 : 0u), 0u,
-                              gid == 0 ? zp1 : (gid == 1 ? sp1 : 0u), 0u};
+      frag(kw, kws, (kt * 2 + 0) * 4, a0);  // pairs of (kt, mt = 0)
+      frag(kw, kws, (kt * 2 + 1) * 4, a1);  // pairs of (kt, mt = 1)
+      const uint32_t ac[4] = {krow[8 * kt + tig], 0u, krow[8 * kt + 4 + tig], 0u};
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t b0 = split_mul(qf[nt][kt][0], sp0, hl);
-        const uint32_t b1 = split_mul(qf[nt][kt][1], sp1, hl);
+        const uint32_t b0 = split_mul(qf[nt][kt][0], sp0);
+        const uint32_t b1 = split_mul(qf[nt][kt][1], sp1);
         mma_16816(sacc[0][nt], a0, b0, b1);
         mma_16816(sacc[1][nt], a1, b0, b1);
-        mma_16816(cacc[nt], ac, hl ? 0u : qf[nt][kt][0], hl ? 0u : qf[nt][kt][1]);
+        mma_16816(cacc[nt], ac, qf[nt][kt][0], qf[nt][kt][1]);
       }
     }
     float lg[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float zq = __shfl_sync(0xffffffffu, cacc[nt][0], tig);
-      const float sq = __shfl_sync(0xffffffffu, cacc[nt][0], 4 + tig);
-      const float kc = zq - C::OFF * sq;
+      const float zq = __shfl_sync(0xffffffffu, cacc[nt][0], tig);  // sum_d q z of head 4nt+tig
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          lg[nt][mt][r] = (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1] + kc) * scale_log2;
+          lg[nt][mt][r] = (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1] + zq) * scale_log2;
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
     load_pp(ps, pp);
     // ---- P.V
-    uint32_t vw[C::NWL];
+    uint32_t vw[C::NWL], vws[C::NWL];
 #pragma unroll
     for (int ch = 0; ch < C::NWL / 4; ++ch) {
       const uint4 v = s4[(C::TB / 16) + ch * 32 + lane];
       vw[4 * ch] = v.x; vw[4 * ch + 1] = v.y; vw[4 * ch + 2] = v.z; vw[4 * ch + 3] = v.w;
     }
+#pragma unroll
+    for (int i = 0; i < C::NWL; ++i) vws[i] = vw[i] >> kShift;
     const uint32_t* vm = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB + C::KMETA);
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
@@ -305,35 +332,26 @@ struct Decoder {
         uint32_t b[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          b[nt][0] = split_mul(pp[nt][kt][0], vs0, hl);
-          b[nt][1] = split_mul(pp[nt][kt][1], vs1, hl);
+          b[nt][0] = split_mul(pp[nt][kt][0], vs0);
+          b[nt][1] = split_mul(pp[nt][kt][1], vs1);
         }
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
           const int mt = 2 * j + mi;
           uint32_t a[4];
-          frag(vw, (mt * 2 + kt) * 4, a);  // pairs of (mt, kt)
+          frag(vw, vws, (mt * 2 + kt) * 4, a);  // pairs of (mt, kt)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, b[nt][0], b[nt][1]);
         }
       }
     }
-    // value zero points and the 2^b offset: rows j = sum_t p~ z[j][t], rows 4+j = sum_t p~ s[j][t]
+    // value zero points (rows j < D/32) and the softmax denominator (row 8)
+    const uint32_t* vrow = gid < D / 32 ? vm + D / 2 + 16 * gid : zrow;
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
-      const int row = gid;
-      uint32_t x0 = 0u, x1 = 0u;
-      if (row < D / 32) {
-        x0 = vm[D / 2 + 16 * row + 8 * kt + tig];
-        x1 = vm[D / 2 + 16 * row + 8 * kt + 4 + tig];
-      } else if (row >= 4 && row - 4 < D / 32) {
-        x0 = vm[16 * (row - 4) + 8 * kt + tig];
-        x1 = vm[16 * (row - 4) + 8 * kt + 4 + tig];
-      }
-      const uint32_t ac[4] = {x0, 0u, x1, 0u};
+      const uint32_t ac[4] = {vrow[8 * kt + tig], ones_a, vrow[8 * kt + 4 + tig], ones_a};
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        mma_16816(zc[nt], ac, hl ? 0u : pp[nt][kt][0], hl ? 0u : pp[nt][kt][1]);
+      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
     }
     __syncwarp();
   }
@@ -341,7 +359,6 @@ struct Decoder {
   // One chunk of up to 32 fp16 tail tokens, read from the ring in global memory.
   __device__ __forceinline__ void tail_chunk(const __half* kt_base, const __half* vt_base, int first,
                                              int count, int th, int R, __half* ps, float scale_log2) {
-    auto slot = [&](int t) { return (th + first + t) % R; };
     float sacc[2][NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -353,7 +370,7 @@ struct Decoder {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int t = 16 * mt + gid + 8 * r;
-        rowoff[mt][r] = t < count ? slot(t) * D : -1;
+        rowoff[mt][r] = t < count ? ((th + first + t) % R) * D : -1;
       }
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt) {
@@ -368,21 +385,18 @@ struct Decoder {
         }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t b0 = hl ? 0u : qf[nt][kt][0], b1 = hl ? 0u : qf[nt][kt][1];
-        mma_16816(sacc[0][nt], a[0], b0, b1);
-        mma_16816(sacc[1][nt], a[1], b0, b1);
+        mma_16816(sacc[0][nt], a[0], qf[nt][kt][0], qf[nt][kt][1]);
+        mma_16816(sacc[1][nt], a[1], qf[nt][kt][0], qf[nt][kt][1]);
       }
     }
-    float lg[NT][2][2];
+    float lg[NT][2][2];  // B = q in both columns of a head: use one of them
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          lg[nt][mt][r] = rowoff[mt][r] >= 0
-                              ? (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1]) * scale_log2
-                              : -INFINITY;
+          lg[nt][mt][r] = rowoff[mt][r] >= 0 ? sacc[mt][nt][2 * r] * scale_log2 : -INFINITY;
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
     load_pp(ps, pp);
@@ -395,8 +409,14 @@ struct Decoder {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int t = 16 * kt + 2 * tig + 8 * hh + e;
-          tok[hh][e] = t < count ? slot(t) * D : -1;
+          tok[hh][e] = t < count ? ((th + first + t) % R) * D : -1;
         }
+      uint32_t bh[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        bh[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pp[nt][kt][0]), u32_as_h2(hi_only)));
+        bh[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pp[nt][kt][1]), u32_as_h2(hi_only)));
+      }
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
         uint32_t a[4];
@@ -409,29 +429,24 @@ struct Decoder {
           a[i] = lo | (hi << 16);
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_16816(o[mt][nt], a, hl ? 0u : pp[nt][kt][0], hl ? 0u : pp[nt][kt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, bh[nt][0], bh[nt][1]);
       }
+      const uint32_t ac[4] = {0u, ones_a, 0u, ones_a};  // denominator row only
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
     }
     __syncwarp();
   }
 
   // Write this warp's partial (m, l, unnormalised o) for its G heads.
-  __device__ __forceinline__ void write_partial(float* dst) {
+  __device__ __forceinline__ void write_partial(float* dst) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
-      float lt = l[nt];
-      lt += __shfl_xor_sync(0xffffffffu, lt, 4);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 8);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+      const float lt = __shfl_sync(0xffffffffu, zc[nt][2], tig);  // row 8 lives in lanes gid 0
       float vc[D / 32];
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        const float zs = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);
-        const float ss = __shfl_sync(0xffffffffu, zc[nt][0], 4 * (4 + j) + tig);
-        vc[j] = zs - C::OFF * ss;
-      }
+      for (int j = 0; j < D / 32; ++j) vc[j] = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);
       if (g < G) {
         float* d = dst + g * C::PSTRIDE;
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
@@ -445,22 +460,17 @@ struct Decoder {
   }
 };
 
-// Log-sum-exp merge of a segment's partials -- its tail partial plus nparts
-// consecutive stream-K partials -- into the normalised output [G][D].  Partials
-// come from other CTAs, so they are read through L2.
+// Log-sum-exp merge of a segment's nparts consecutive partials into the
+// normalised output [G][D].  Partials come from other CTAs: read through L2.
 template <int D, int G>
-__device__ void final_merge(const float* tail, const float* parts, int nparts, float* out, int tid,
-                            int nthreads) {
+__device__ void final_merge(const float* parts, int nparts, float* out, int tid, int nthreads) {
   constexpr int PS = D + 4;
   for (int e = tid; e < G * D; e += nthreads) {
     const int g = e / D, d = e % D;
-    float mx = __ldcg(tail + g * PS);
+    float mx = -INFINITY;
     for (int i = 0; i < nparts; ++i) mx = fmaxf(mx, __ldcg(parts + (size_t)i * G * PS + g * PS));
     float lsum = 0.f, osum = 0.f;
     if (mx != -INFINITY) {
-      const float wt = exp2f(__ldcg(tail + g * PS) - mx);
-      lsum = wt * __ldcg(tail + g * PS + 1);
-      osum = wt * __ldcg(tail + g * PS + 4 + d);
       for (int i = 0; i < nparts; ++i) {
         const float* src = parts + (size_t)i * G * PS + g * PS;
         const float w = exp2f(__ldcg(src) - mx);
@@ -480,73 +490,20 @@ decode_kernel(const DecodeParams p) {
   __shared__ int s_last;
   uint8_t* ring = smem;
   __half* ps_all = reinterpret_cast<__half*>(smem + C::RING);
-  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS);
-  int* s_ne = s_pref + (KVQ_MAX_BATCH + 1);
+  uint32_t* zrow = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS);
+  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS + C::ZERO);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __half* ps = ps_all + warp * G * kGroup;
   uint8_t* wring = ring + warp * C::NSTAGE * C::STAGE;
 
-  build_prefix(p, s_pref, s_ne);
+  for (int i = threadIdx.x; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
+  build_prefix(p, s_pref);
   __syncthreads();
   const int64_t total = (int64_t)p.hkv * s_pref[p.batch];
   const int64_t nstream = total < p.n_stream ? total : p.n_stream;
-  const int R = p.tail_cap;
-  const int nseg = p.batch * p.hkv;
-
-  // Participants of segment (b, h): its tail warp and the stream-K CTAs
-  // [c0, c1] whose ranges meet it; CTA c keeps its partial in slot c + k with k
-  // the segment's index among nonempty segments (distinct for every pair).
-  struct SegInfo {
-    int target;
-    int64_t c0, k;
-    int nparts;
-  };
-  auto seg_info = [&](int b, int h) -> SegInfo {
-    SegInfo si{1, 0, 0, 0};
-    const int items = s_pref[b + 1] - s_pref[b];
-    if (items > 0) {
-      const int64_t A = (int64_t)p.hkv * s_pref[b] + (int64_t)h * items;
-      si.c0 = cta_of(A, total, nstream);
-      si.nparts = (int)(cta_of(A + items - 1, total, nstream) - si.c0 + 1);
-      si.k = (int64_t)p.hkv * s_ne[b] + h;
-      si.target = 1 + si.nparts;
-    }
-    return si;
-  };
-  auto out_ptr = [&](int b, int h) { return p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D; };
-  auto part_ptr = [&](int64_t slot) { return p.part + (size_t)slot * G * C::PSTRIDE; };
-
-  if ((int)blockIdx.x < p.n_tail_ctas) {
-    // ---------------- tail warps: one per (sequence, KV head)
-    const int seg = blockIdx.x * C::WARPS + warp;
-    if (seg >= nseg) return;
-    const int b = seg / p.hkv, h = seg % p.hkv;
-    const SeqLen L = read_lengths(p, b, false);
-    Decoder<D, BITS, G> dec;
-    dec.init(p, b, h);
-    const __half* kt = p.k_tail + (size_t)seg * R * D;
-    const __half* vt = p.v_tail + (size_t)seg * R * D;
-    for (int first = 0; first < L.nt; first += kGroup)
-      dec.tail_chunk(kt, vt, first, min(kGroup, L.nt - first), L.th, R, ps, p.scale_log2);
-    float* mine = p.tail_part + (size_t)seg * G * C::PSTRIDE;
-    dec.write_partial(mine);
-    __threadfence();
-    __syncwarp();
-    const SegInfo si = seg_info(b, h);
-    int last = 0;
-    if (lane == 0) last = atomicAdd(&p.counters[seg], 1) == si.target - 1;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence();
-      final_merge<D, G>(mine, part_ptr(si.c0 + si.k), si.nparts, out_ptr(b, h), lane, 32);
-      if (lane == 0) p.counters[seg] = 0;
-    }
-    return;
-  }
-
-  // ---------------- stream-K CTAs over the quantized groups
-  const int64_t c = (int64_t)blockIdx.x - p.n_tail_ctas;
+  const int64_t c = blockIdx.x;
   if (c >= nstream) return;
+  const int R = p.tail_cap;
   const int64_t r0 = c * total / nstream, r1 = (c + 1) * total / nstream;
   for (int64_t x = r0; x < r1;) {
     // segment containing x: the largest b with hkv * pref[b] <= x
@@ -557,18 +514,21 @@ decode_kernel(const DecodeParams p) {
     }
     const int b = lo;
     const int items = s_pref[b + 1] - s_pref[b];
-    const int64_t off = x - (int64_t)p.hkv * s_pref[b];
-    const int h = (int)(off / items);
-    const int g0 = (int)(off % items);
-    const int64_t xe = min(r1, x + (items - g0));
+    const int64_t seg_first = (int64_t)p.hkv * s_pref[b];
+    const int h = (int)((x - seg_first) / items);
+    const int i0 = (int)((x - seg_first) % items);
+    const int64_t xe = min(r1, x + (items - i0));
     const int n = (int)(xe - x);
     const int seg = b * p.hkv + h;
-    // this warp's contiguous share of groups [g0, g0 + n)
+    const SeqLen L = read_lengths(p, b, false);
+    const int ng = L.nq / kGroup;
+    // this warp's contiguous share of items [i0, i0 + n)
     const int per = (n + C::WARPS - 1) / C::WARPS;
-    const int ga = g0 + min(n, warp * per), cnt = min(n, (warp + 1) * per) - min(n, warp * per);
+    const int ia = i0 + min(n, warp * per), ie = i0 + min(n, (warp + 1) * per);
     Decoder<D, BITS, G> dec;
     dec.init(p, b, h);
     {
+      const int ga = ia, cnt = max(0, min(ie, ng) - ia);
       const size_t gbase = (size_t)seg * p.max_groups + ga;
       auto issue = [&](int idx, int slotn) {
         const size_t g = gbase + idx;
@@ -597,16 +557,24 @@ decode_kernel(const DecodeParams p) {
         cp_async_commit();
         cp_async_wait<C::NSTAGE - 1>();
         __syncwarp();
-        dec.quant_group(wring + (i % C::NSTAGE) * C::STAGE, ps, p.scale_log2);
+        dec.quant_group(wring + (i % C::NSTAGE) * C::STAGE, ps, zrow, p.scale_log2);
       }
       cp_async_wait<0>();
       __syncwarp();
     }
-    // warp partial into the warp's (now idle) ring slice
+    // tail chunks whose first weighted item falls in this warp's range
+    for (int t = max(ia, ng); t < ie; ++t) {
+      const int u = t - ng;
+      if (u % kTailWeight != 0) continue;
+      const int first = (u / kTailWeight) * kGroup;
+      if (first >= L.nt) continue;
+      dec.tail_chunk(p.k_tail + (size_t)seg * R * D, p.v_tail + (size_t)seg * R * D, first,
+                     min(kGroup, L.nt - first), L.th, R, ps, p.scale_log2);
+    }
+    // warp partial into the warp's (now idle) ring slice, then the CTA merge
     dec.write_partial(reinterpret_cast<float*>(wring));
     __syncthreads();
-    const SegInfo si = seg_info(b, h);
-    float* slot = part_ptr(c + si.k);
+    float* slot = p.part + (size_t)(c + seg) * G * C::PSTRIDE;
     for (int e2 = threadIdx.x; e2 < G * D; e2 += blockDim.x) {
       const int g = e2 / D, d = e2 % D;
       float mx = -INFINITY;
@@ -628,12 +596,14 @@ decode_kernel(const DecodeParams p) {
     }
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&p.counters[seg], 1) == si.target - 1;
+    const int64_t c0 = cta_of(seg_first + (int64_t)h * items, total, nstream);
+    const int nparts = (int)(cta_of(seg_first + (int64_t)(h + 1) * items - 1, total, nstream) - c0 + 1);
+    if (threadIdx.x == 0) s_last = atomicAdd(&p.counters[seg], 1) == nparts - 1;
     __syncthreads();
     if (s_last) {
       __threadfence();
-      final_merge<D, G>(p.tail_part + (size_t)seg * G * C::PSTRIDE, part_ptr(si.c0 + si.k), si.nparts,
-                        out_ptr(b, h), threadIdx.x, blockDim.x);
+      final_merge<D, G>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
+                        p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D, threadIdx.x, blockDim.x);
       if (threadIdx.x == 0) p.counters[seg] = 0;
     }
     __syncthreads();
@@ -642,26 +612,24 @@ decode_kernel(const DecodeParams p) {
 }
 
 struct DecodeLayout {
-  size_t counters, tail_part, part, total;
+  size_t counters, part, total;
 };
-
-inline int decode_warps(int bits) { return bits == 8 ? 4 : 8; }
 
 inline DecodeLayout decode_layout(const kvq_cache* c, int G, int n_stream) {
   DecodeLayout L;
   const size_t seg = (size_t)c->batch * c->n_kv_heads;
   const size_t pstride = (size_t)(c->head_dim + 4) * 4 * G;
   L.counters = 0;
-  L.tail_part = ((seg * 4 + 255) / 256) * 256;
-  L.part = L.tail_part + seg * pstride;
+  L.part = ((seg * 4 + 255) / 256) * 256;
+  // CTA c writes its partial of segment s to slot c + s (distinct for every pair)
   L.total = L.part + ((size_t)n_stream + seg) * pstride;
   return L;
 }
 
 template <int D, int BITS, int G>
 struct DecodeLaunch {
+  // resident CTAs on the whole GPU (one wave), computed once per instantiation
   static int slots(int* err) {
-    // resident CTAs on the whole GPU (one wave), computed once per instantiation
     static int cached = -1;
     if (cached < 0) {
       using C = DecodeCfg<D, BITS, G>;
@@ -679,26 +647,24 @@ struct DecodeLaunch {
     }
     return cached;
   }
-  static kvq_status run(DecodeParams p, int batch, int hkv, cudaStream_t s) {
+  static kvq_status run(DecodeParams p, cudaStream_t s) {
     using C = DecodeCfg<D, BITS, G>;
     int err = 0;
     const int n = slots(&err);
     if (err) return KVQ_ERR_CUDA;
     p.n_stream = n;
-    p.n_tail_ctas = (batch * hkv + C::WARPS - 1) / C::WARPS;
-    dim3 grid(p.n_tail_ctas + p.n_stream);
-    decode_kernel<D, BITS, G><<<grid, C::WARPS * 32, C::SMEM, s>>>(p);
+    decode_kernel<D, BITS, G><<<n, C::WARPS * 32, C::SMEM, s>>>(p);
     return launch_status();
   }
 };
 
 template <int D, int BITS>
-kvq_status decode_dispatch_g(int G, const DecodeParams& p, int batch, int hkv, cudaStream_t s) {
+kvq_status decode_dispatch_g(int G, const DecodeParams& p, cudaStream_t s) {
   switch (G) {
-    case 1: return DecodeLaunch<D, BITS, 1>::run(p, batch, hkv, s);
-    case 2: return DecodeLaunch<D, BITS, 2>::run(p, batch, hkv, s);
-    case 4: return DecodeLaunch<D, BITS, 4>::run(p, batch, hkv, s);
-    case 8: return DecodeLaunch<D, BITS, 8>::run(p, batch, hkv, s);
+    case 1: return DecodeLaunch<D, BITS, 1>::run(p, s);
+    case 2: return DecodeLaunch<D, BITS, 2>::run(p, s);
+    case 4: return DecodeLaunch<D, BITS, 4>::run(p, s);
+    case 8: return DecodeLaunch<D, BITS, 8>::run(p, s);
     default: return KVQ_ERR_UNSUPPORTED;
   }
 }
@@ -715,9 +681,7 @@ inline int decode_slots(const kvq_cache* c, int G, int* err) {
   return 0;
 }
 
-inline kvq_status validate_decode(const kvq_cache* c, int32_t n_q_heads, int* G) {
-  kvq_status s = validate_cache(c);
-  if (s != KVQ_OK) return s;
+inline kvq_status validate_q_heads(const kvq_cache* c, int32_t n_q_heads, int* G) {
   if (c->batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
   if (n_q_heads < c->n_kv_heads || n_q_heads % c->n_kv_heads) return KVQ_ERR_INVALID;
   const int g = n_q_heads / c->n_kv_heads;
@@ -730,14 +694,12 @@ inline kvq_status validate_decode(const kvq_cache* c, int32_t n_q_heads, int* G)
 
 extern "C" kvq_status kvq_decode_workspace_bytes(const kvq_cache* c, int32_t n_q_heads, size_t* bytes) {
   using namespace kvq;
-  int G = 0;
   kvq_status s = validate_geometry(c);
   if (s != KVQ_OK) return s;
   if (bytes == nullptr) return KVQ_ERR_INVALID;
-  if (c->batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
-  if (n_q_heads < c->n_kv_heads || n_q_heads % c->n_kv_heads) return KVQ_ERR_INVALID;
-  G = n_q_heads / c->n_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return KVQ_ERR_UNSUPPORTED;
+  int G = 0;
+  s = validate_q_heads(c, n_q_heads, &G);
+  if (s != KVQ_OK) return s;
   int err = 0;
   const int n = decode_slots(c, G, &err);
   if (err) return KVQ_ERR_CUDA;
@@ -749,8 +711,10 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, con
                                       float sm_scale, void* workspace, size_t workspace_bytes,
                                       void* stream) {
   using namespace kvq;
+  kvq_status s = validate_cache(c);
+  if (s != KVQ_OK) return s;
   int G = 0;
-  kvq_status s = validate_decode(c, n_q_heads, &G);
+  s = validate_q_heads(c, n_q_heads, &G);
   if (s != KVQ_OK) return s;
   if (q == nullptr || out == nullptr || workspace == nullptr) return KVQ_ERR_INVALID;
   if (!aligned(q, 4) || !aligned(out, 4) || !aligned(workspace, 16)) return KVQ_ERR_INVALID;
@@ -775,7 +739,6 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, con
   p.out = out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
-  p.tail_part = reinterpret_cast<float*>(ws + L.tail_part);
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.batch = c->batch;
@@ -784,11 +747,11 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, con
   p.tail_cap = c->tail_cap;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->head_dim == 128) {
-    if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, c->batch, c->n_kv_heads, st);
-    if (c->bits == 4) return decode_dispatch_g<128, 4>(G, p, c->batch, c->n_kv_heads, st);
-    return decode_dispatch_g<128, 8>(G, p, c->batch, c->n_kv_heads, st);
+    if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, st);
+    if (c->bits == 4) return decode_dispatch_g<128, 4>(G, p, st);
+    return decode_dispatch_g<128, 8>(G, p, st);
   }
-  if (c->bits == 2) return decode_dispatch_g<64, 2>(G, p, c->batch, c->n_kv_heads, st);
-  if (c->bits == 4) return decode_dispatch_g<64, 4>(G, p, c->batch, c->n_kv_heads, st);
-  return decode_dispatch_g<64, 8>(G, p, c->batch, c->n_kv_heads, st);
+  if (c->bits == 2) return decode_dispatch_g<64, 2>(G, p, st);
+  if (c->bits == 4) return decode_dispatch_g<64, 4>(G, p, st);
+  return decode_dispatch_g<64, 8>(G, p, st);
 }
