@@ -224,14 +224,22 @@ def append_lengths(n_quant: int, n_tail: int, tail_cap: int):
 #             channel d = 16*mt + gid + 8*(i % 2), token t = 16*kt + 2*tig + 8*(i // 2)
 #             pair = (code[t][d], code[t + 1][d])
 # Pair P of a lane goes to the lane's word P // (16/b), slot k = P % (16/b): the
-# first code at bits [b*k, b*k + b), the second at bits [16 + b*k, 16 + b*k + b).
-# A lane's word w sits at byte ((w // 4) * 32 + lane) * 16 + (w % 4) * 4 of the
-# tile, little-endian.  Tile bytes: 32 * D * b / 8.
+# first code at bits [p, p + b), the second at bits [16 + p, 16 + p + b), with
+# p = SLOT_BITPOS[b][k].  A lane's word w sits at byte ((w // 4) * 32 + lane) * 16
+# + (w % 4) * 4 of the tile, little-endian.  Tile bytes: 32 * D * b / 8.
 #
-# Metadata: K, per group, float16 [2][D] = (scale[channel], zero[channel]);
-# V, per 32-token tile, float16 [2][D/32][32] = (scale[j][t], zero[j][t]) for
-# channel group j and token t of the tile.
+# Metadata, stored as pairs of fp16 values (32-bit words), each block holding a
+# scale plane then a zero-point plane of D/2 pairs:
+#   K, per group:        pair index tig*(D/8) + 2*kt + r   (tig < 4, kt < D/16, r < 2)
+#                        = (x[c], x[c + 1]) for channel c = 16*kt + 2*tig + 8*r
+#   V, per 32-token tile: pair index tig*(D/8) + 4*j + 2*kt + r
+#                        (tig < 4, j < D/32, kt < 2, r < 2)
+#                        = (x[j][t], x[j][t + 1]) for channel group j and token
+#                        t = 16*kt + 2*tig + 8*r of the tile
 # ---------------------------------------------------------------------------
+SLOT_BITPOS = {2: (2, 6, 0, 4, 10, 14, 8, 12), 4: (0, 4, 8, 12), 8: (0, 8)}
+
+
 @functools.lru_cache(maxsize=None)
 def tile_code_positions(kind: str, d: int, bits: int):
     """Word index and bit offset of every code of a 32 x D tile.
@@ -261,7 +269,8 @@ def tile_code_positions(kind: str, d: int, bits: int):
         for p, (first, second) in enumerate(pairs):
             w, k = p // per_word, p % per_word
             gword = ((w // 4) * 32 + lane) * 4 + (w % 4)
-            for (t, c), off in ((first, bits * k), (second, 16 + bits * k)):
+            pos = SLOT_BITPOS[bits][k]
+            for (t, c), off in ((first, pos), (second, 16 + pos)):
                 assert word[t, c] == -1, "layout must place each code once"
                 word[t, c] = gword
                 bit[t, c] = off
@@ -301,44 +310,52 @@ def unpack_tiles(packed: np.ndarray, kind: str, d: int, bits: int) -> np.ndarray
     return vals.astype(np.uint8)
 
 
-def uniform_buffers(states: list, n_groups_cap: int, tail_cap: int) -> dict:
-    """Expected device buffers for a batch of sequence states (quantize_sequence
-    output), in the library's uniform layout.  Unused groups / tail slots are 0;
-    tests compare only the valid region.  Tail tokens sit at ring slots
-    0 .. n_tail-1 (ring head 0), as prefill leaves them."""
-    b = len(states)
-    hkv, _, d = states[0]["k_codes"].shape
-    bits = states[0]["bits"]
-    tb = tile_bytes(d, bits)
-    out = {
-        "k_codes": np.zeros((b, hkv, n_groups_cap, tb), np.uint8),
-        "v_codes": np.zeros((b, hkv, n_groups_cap, tb), np.uint8),
-        "k_meta": np.zeros((b, hkv, n_groups_cap, 2, d), F16),
-        "v_meta": np.zeros((b, hkv, n_groups_cap, 2, d // GROUP, GROUP), F16),
-        "k_tail": np.zeros((b, hkv, tail_cap, d), F16),
-        "v_tail": np.zeros((b, hkv, tail_cap, d), F16),
-        "n_quant": np.zeros((b,), np.int32),
-        "n_tail": np.zeros((b,), np.int32),
-    }
-    for i, st in enumerate(states):
-        g = st["n_quant"] // GROUP
-        nt = st["n_tail"]
-        out["n_quant"][i] = st["n_quant"]
-        out["n_tail"][i] = nt
-        if g:
-            kc = st["k_codes"].reshape(hkv, g, GROUP, d)
-            vc = st["v_codes"].reshape(hkv, g, GROUP, d)
-            out["k_codes"][i, :, :g] = pack_tiles(kc, "K", bits)
-            out["v_codes"][i, :, :g] = pack_tiles(vc, "V", bits)
-            out["k_meta"][i, :, :g, 0] = st["k_scale"]
-            out["k_meta"][i, :, :g, 1] = st["k_zero"]
-            vs = st["v_scale"].reshape(hkv, g, GROUP, d // GROUP)
-            vz = st["v_zero"].reshape(hkv, g, GROUP, d // GROUP)
-            out["v_meta"][i, :, :g, 0] = np.swapaxes(vs, -1, -2)
-            out["v_meta"][i, :, :g, 1] = np.swapaxes(vz, -1, -2)
-        out["k_tail"][i, :, :nt] = st["k_tail"]
-        out["v_tail"][i, :, :nt] = st["v_tail"]
-    return out
+@functools.lru_cache(maxsize=None)
+def key_meta_order(d: int) -> np.ndarray:
+    """Channel of every fp16 slot of a key metadata plane (length D)."""
+    order = np.full(d, -1, dtype=np.int64)
+    for tig in range(4):
+        for kt in range(d // 16):
+            for r in range(2):
+                pair = tig * (d // 8) + 2 * kt + r
+                c = 16 * kt + 2 * tig + 8 * r
+                order[2 * pair], order[2 * pair + 1] = c, c + 1
+    assert sorted(order.tolist()) == list(range(d))
+    order.setflags(write=False)
+    return order
+
+
+@functools.lru_cache(maxsize=None)
+def value_meta_order(d: int) -> np.ndarray:
+    """(channel group j) * 32 + token t of every fp16 slot of a value metadata
+    plane (length D)."""
+    order = np.full(d, -1, dtype=np.int64)
+    for tig in range(4):
+        for j in range(d // GROUP):
+            for kt in range(2):
+                for r in range(2):
+                    pair = tig * (d // 8) + 4 * j + 2 * kt + r
+                    t = 16 * kt + 2 * tig + 8 * r
+                    order[2 * pair], order[2 * pair + 1] = j * GROUP + t, j * GROUP + t + 1
+    assert sorted(order.tolist()) == list(range(d))
+    order.setflags(write=False)
+    return order
+
+
+def pack_key_meta(scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """scale/zero float16 [..., D] of key groups -> float16 [..., 2, D] block."""
+    order = key_meta_order(scale.shape[-1])
+    return np.stack([scale[..., order], zero[..., order]], axis=-2)
+
+
+def pack_value_meta(scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """scale/zero float16 [..., 32, D/32] (token, channel group) of one value tile
+    -> float16 [..., 2, D] block."""
+    d = scale.shape[-1] * GROUP
+    order = value_meta_order(d)
+    flat_s = np.swapaxes(scale, -1, -2).reshape(*scale.shape[:-2], d)  # j * 32 + t
+    flat_z = np.swapaxes(zero, -1, -2).reshape(*zero.shape[:-2], d)
+    return np.stack([flat_s[..., order], flat_z[..., order]], axis=-2)
 
 
 # ---------------------------------------------------------------------------

@@ -66,13 +66,13 @@ def assert_buffers_equal(cache: kvq.QuantizedKVCache, states: list, batches=None
             assert (O.unpack_tiles(vc, "V", D, bits) == ev).all(), "value codes differ"
             assert (kc == O.pack_tiles(ek, "K", bits)).all(), "packed key bytes differ"
             assert (vc == O.pack_tiles(ev, "V", bits)).all(), "packed value bytes differ"
-            ks, kz = st["k_scale"][:, gs], st["k_zero"][:, gs]
-            assert (km[:, :, 0].view(np.uint16) == ks.view(np.uint16)).all(), "key scales differ"
-            assert (km[:, :, 1].view(np.uint16) == kz.view(np.uint16)).all(), "key zeros differ"
-            vs = st["v_scale"].reshape(len(hs), ng, 32, D // 32)[:, gs].swapaxes(-1, -2)
-            vz = st["v_zero"].reshape(len(hs), ng, 32, D // 32)[:, gs].swapaxes(-1, -2)
-            assert (vm[:, :, 0].view(np.uint16) == vs.view(np.uint16)).all(), "value scales differ"
-            assert (vm[:, :, 1].view(np.uint16) == vz.view(np.uint16)).all(), "value zeros differ"
+            ekm = O.pack_key_meta(st["k_scale"][:, gs], st["k_zero"][:, gs])
+            assert (km.view(np.uint16) == ekm.view(np.uint16)).all(), "key scales/zeros differ"
+            vs = st["v_scale"].reshape(len(hs), ng, 32, D // 32)[:, gs]
+            vz = st["v_zero"].reshape(len(hs), ng, 32, D // 32)[:, gs]
+            evm = O.pack_value_meta(vs, vz)
+            assert (vm.reshape(evm.shape).view(np.uint16) == evm.view(np.uint16)).all(), \
+                "value scales/zeros differ"
         # tail in logical order through the ring
         R = cache.tail_cap
         slots = (th[b] + np.arange(st["n_tail"])) % R

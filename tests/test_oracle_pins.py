@@ -328,16 +328,17 @@ def test_flushed_group_equals_prefill_quantization():
 # first code at bits [b*slot, +b), second at [16 + b*slot, +b); lane word w at
 # byte ((w // 4) * 32 + lane) * 16 + (w % 4) * 4.
 KPOS_2BIT_D128 = [
-    # (token, channel) -> (byte offset of the 32-bit word, bit offset)
-    ((0, 0), (0, 0)), ((0, 1), (0, 16)), ((8, 0), (0, 2)), ((0, 8), (0, 4)),
-    ((8, 9), (0, 22)), ((16, 0), (0, 8)), ((24, 8), (0, 14)), ((1, 0), (64, 0)),
-    ((0, 2), (16, 0)), ((0, 16), (4, 0)), ((0, 64), (512, 0)), ((31, 127), (512 + 31 * 16 + 12, 30)),
+    # (token, channel) -> (byte offset of the 32-bit word, bit offset); 2-bit slot
+    # bit positions (2, 6, 0, 4, 10, 14, 8, 12)
+    ((0, 0), (0, 2)), ((0, 1), (0, 18)), ((8, 0), (0, 6)), ((0, 8), (0, 0)),
+    ((8, 9), (0, 20)), ((16, 0), (0, 10)), ((24, 8), (0, 12)), ((1, 0), (64, 2)),
+    ((0, 2), (16, 2)), ((0, 16), (4, 2)), ((0, 64), (512, 2)), ((31, 127), (1020, 28)),
 ]
 KPOS_4BIT_D128 = [((0, 0), (0, 0)), ((16, 0), (4, 0)), ((8, 1), (0, 20)), ((0, 16), (8, 0)),
                   ((0, 32), (512, 0))]
 VPOS_2BIT_D128 = [
-    ((0, 0), (0, 0)), ((1, 0), (0, 16)), ((0, 8), (0, 2)), ((8, 0), (0, 4)),
-    ((16, 0), (0, 8)), ((2, 0), (16, 0)), ((0, 1), (64, 0)), ((0, 16), (4, 0)),
+    ((0, 0), (0, 2)), ((1, 0), (0, 18)), ((0, 8), (0, 6)), ((8, 0), (0, 0)),
+    ((16, 0), (0, 10)), ((2, 0), (16, 2)), ((0, 1), (64, 2)), ((0, 16), (4, 2)),
 ]
 
 
@@ -353,6 +354,27 @@ def test_tile_layout_hand_positions(kind, bits, table):
         nz = np.nonzero(words)[0]
         assert nz.tolist() == [byte // 4], (t, d)
         assert int(words[byte // 4]) == (2 ** bits - 1) << bit, (t, d)
+
+
+def test_metadata_order_hand_positions():
+    # key plane slot -> channel; pair (tig, kt, r) at tig*(D/8) + 2kt + r holds
+    # channels 16kt + 2tig + 8r and +1
+    ko = O.key_meta_order(128)
+    assert ko[:6].tolist() == [0, 1, 8, 9, 16, 17]
+    assert ko[32:34].tolist() == [2, 3]  # pair 16 = (tig 1, kt 0, r 0)
+    assert ko[126:128].tolist() == [126, 127]  # pair 63 = (tig 3, kt 7, r 1)
+    # value plane slot -> j*32 + token; pair (tig, j, kt, r) at tig*(D/8) + 4j + 2kt + r
+    vo = O.value_meta_order(128)
+    assert vo[:8].tolist() == [0, 1, 8, 9, 16, 17, 24, 25]
+    assert vo[8:10].tolist() == [32, 33]  # pair 4 = (tig 0, j 1, kt 0, r 0)
+    assert vo[32:34].tolist() == [2, 3]  # pair 16 = (tig 1, j 0, kt 0, r 0)
+    # packing places a planted value where the order says
+    sc = np.zeros(128, np.float16)
+    sc[17] = 5
+    assert np.nonzero(O.pack_key_meta(sc, np.zeros_like(sc))[0])[0].tolist() == [5]
+    vs = np.zeros((32, 4), np.float16)
+    vs[16, 1] = 7  # token 16 of channel group 1 -> pair (tig 0, j 1, kt 1, r 0) = 6 -> slot 12
+    assert np.nonzero(O.pack_value_meta(vs, np.zeros_like(vs))[0])[0].tolist() == [12]
 
 
 @pytest.mark.parametrize("kind", ["K", "V"])
