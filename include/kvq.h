@@ -80,9 +80,9 @@ typedef enum {
  * s, KV head h, group g (tile = 32 tokens, TB = 32 * D * b / 8 bytes):
  *   k_codes   uint8 [B][Hkv][max_groups][TB]   packed key codes of group g
  *   v_codes   uint8 [B][Hkv][max_groups][TB]   packed value codes of tokens 32g..32g+31
- *   k_meta    fp16  [B][Hkv][max_groups][2][D]          (scale[d], zero[d]) of key group (g, d)
- *   v_meta    fp16  [B][Hkv][max_groups][2][D/32][32]   (scale[j][t], zero[j][t]) of value
- *                                                       group j of token 32g + t
+ *   k_meta    fp16  [B][Hkv][max_groups][2][D]   scale plane, zero plane of key group g
+ *   v_meta    fp16  [B][Hkv][max_groups][2][D]   scale plane, zero plane of the value
+ *                                                groups of tokens 32g..32g+31
  *   k_tail    fp16  [B][Hkv][R][D]   ring of fp16 keys; logical tail token i sits
  *   v_tail    fp16  [B][Hkv][R][D]   at slot (tail_head[s] + i) mod R
  *   n_quant   int32 [B]  tokens in the quantized region (multiple of 32)
@@ -100,11 +100,18 @@ typedef enum {
  *   values: for mt < D/16, kt < 2, i < 4: channel c = 16mt + gid + 8(i%2),
  *           token t = 16kt + 2tig + 8(i/2); pair = (code[t][c], code[t+1][c])
  * Pair P of a lane goes to the lane's 32-bit word P/(16/b), slot k = P%(16/b): the
- * first code at bits [b*k, b*k+b), the second at bits [16+b*k, 16+b*k+b).  The
- * lane's word w is stored little-endian at byte ((w/4)*32 + lane)*16 + (w%4)*4 of
- * the tile.  (The pairs are the operand fragments of a 16x8x16 tensor-core
- * product, so a warp turns each word into fp16 operands with one logic op per
- * pair.)
+ * first code at bits [p, p+b), the second at bits [16+p, 16+p+b), where p is
+ * 2,6,0,4,10,14,8,12 for k = 0..7 at b = 2 and p = b*k at b = 4, 8.  The lane's
+ * word w is stored little-endian at byte ((w/4)*32 + lane)*16 + (w%4)*4 of the
+ * tile.  (The pairs are the operand fragments of a 16x8x16 tensor-core product,
+ * so a warp turns each word into fp16 operands with one logic op per pair.)
+ *
+ * Metadata planes are stored as fp16 pairs (32-bit words) in lane order, D/2
+ * pairs per plane:
+ *   key plane, pair 16(kt/2) + 4tig + 2(kt%2) + r (tig<4, kt<D/16, r<2):
+ *       (x[c], x[c+1]) for channel c = 16kt + 2tig + 8r
+ *   value plane, pair 16j + 4tig + 2kt + r (tig<4, j<D/32, kt<2, r<2):
+ *       (x[j][t], x[j][t+1]) for channel group j, token t = 16kt + 2tig + 8r
  */
 typedef struct kvq_cache {
   int32_t batch;

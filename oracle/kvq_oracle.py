@@ -230,9 +230,10 @@ def append_lengths(n_quant: int, n_tail: int, tail_cap: int):
 #
 # Metadata, stored as pairs of fp16 values (32-bit words), each block holding a
 # scale plane then a zero-point plane of D/2 pairs:
-#   K, per group:        pair index tig*(D/8) + 2*kt + r   (tig < 4, kt < D/16, r < 2)
+#   K, per group:        pair index 16*(kt // 2) + 4*tig + 2*(kt % 2) + r
+#                        (tig < 4, kt < D/16, r < 2)
 #                        = (x[c], x[c + 1]) for channel c = 16*kt + 2*tig + 8*r
-#   V, per 32-token tile: pair index tig*(D/8) + 4*j + 2*kt + r
+#   V, per 32-token tile: pair index 16*j + 4*tig + 2*kt + r
 #                        (tig < 4, j < D/32, kt < 2, r < 2)
 #                        = (x[j][t], x[j][t + 1]) for channel group j and token
 #                        t = 16*kt + 2*tig + 8*r of the tile
@@ -317,7 +318,7 @@ def key_meta_order(d: int) -> np.ndarray:
     for tig in range(4):
         for kt in range(d // 16):
             for r in range(2):
-                pair = tig * (d // 8) + 2 * kt + r
+                pair = 16 * (kt // 2) + 4 * tig + 2 * (kt % 2) + r
                 c = 16 * kt + 2 * tig + 8 * r
                 order[2 * pair], order[2 * pair + 1] = c, c + 1
     assert sorted(order.tolist()) == list(range(d))
@@ -334,7 +335,7 @@ def value_meta_order(d: int) -> np.ndarray:
         for j in range(d // GROUP):
             for kt in range(2):
                 for r in range(2):
-                    pair = tig * (d // 8) + 4 * j + 2 * kt + r
+                    pair = 16 * j + 4 * tig + 2 * kt + r
                     t = 16 * kt + 2 * tig + 8 * r
                     order[2 * pair], order[2 * pair + 1] = j * GROUP + t, j * GROUP + t + 1
     assert sorted(order.tolist()) == list(range(d))

@@ -61,6 +61,15 @@ struct Tile {
   static_assert(kWordsPerLane % 4 == 0, "a lane owns whole 16-byte chunks");
 };
 
+// Bit position (within each 16-bit half of a word) of the codes in slot k.  For
+// 2-bit codes the slots of one shifted word pair up: slots {0,1,4,5} sit 2 bits
+// above slots {2,3,6,7}, so one shift aligns a code of each to the top two
+// mantissa fields of an fp16 value.
+template <int BITS>
+__host__ __device__ constexpr int slot_bitpos(int k) {
+  return BITS == 2 ? ((k & 4) ? 8 : 0) + ((k & 1) ? 4 : 0) + ((k & 2) ? 0 : 2) : BITS * k;
+}
+
 // (token, channel) of the FIRST code of key pair P of a lane; the second code is
 // at channel + 1.
 __device__ __forceinline__ void key_pair_pos(int P, int gid, int tig, int& t, int& c) {
@@ -99,12 +108,38 @@ __device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst,
       second = ct[(t + 1) * D + c];
     }
     const int wi = P / T::kPairsPerWord, k = P % T::kPairsPerWord;
-    w[wi] |= (first << (BITS * k)) | (second << (16 + BITS * k));
+    w[wi] |= (first << slot_bitpos<BITS>(k)) | (second << (16 + slot_bitpos<BITS>(k)));
   }
 #pragma unroll
   for (int ch = 0; ch < T::kChunksPerLane; ++ch) {
     uint4 v = make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
     *reinterpret_cast<uint4*>(dst + (size_t)(ch * 32 + lane) * 16) = v;
+  }
+}
+
+// Metadata blocks are stored as fp16 pairs in "lane order" (see kvq.h): pair p
+// of a key plane holds channels 16kt + 2tig + 8r (+1) with kt = 2(p/16) +
+// (p%4)/2, tig = p%16/4, r = p%2; pair p of a value plane holds tokens
+// 16kt + 2tig + 8r (+1) of channel group j = p/16 with tig = p%16/4,
+// kt = (p%4)/2, r = p%2.  The natural-order planes are staged in shared memory
+// (nat[2][D]) and written out permuted.
+template <int D, bool IS_KEY>
+__device__ __forceinline__ void store_meta_lane_order(const __half* nat, __half* dst, int lane) {
+  constexpr int PAIRS = D / 2, PER_LANE = PAIRS / 32;
+  const uint16_t* n16 = reinterpret_cast<const uint16_t*>(nat);
+  uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+  for (int plane = 0; plane < 2; ++plane) {
+#pragma unroll
+    for (int e = 0; e < PER_LANE; ++e) {
+      const int p = lane * PER_LANE + e;
+      const int tig = (p % 16) / 4, w = p % 4, r = w % 2;
+      int idx;
+      if (IS_KEY) idx = 16 * (2 * (p / 16) + w / 2) + 2 * tig + 8 * r;
+      else idx = kGroup * (p / 16) + 16 * (w / 2) + 2 * tig + 8 * r;
+      const uint32_t lo = n16[plane * D + idx], hi = n16[plane * D + idx + 1];
+      d32[plane * PAIRS + p] = lo | (hi << 16);
+    }
   }
 }
 
@@ -172,12 +207,13 @@ __device__ __forceinline__ void quantize_tile_warp(const __half* ksrc, const __h
     }
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
-      kmeta_dst[c0 + j] = sc[j];
-      kmeta_dst[D + c0 + j] = ze[j];
+      vm[c0 + j] = sc[j];
+      vm[D + c0 + j] = ze[j];
     }
   }
   __syncwarp();
   pack_store_tile<D, BITS, true>(ct, kcodes_dst, lane);
+  store_meta_lane_order<D, true>(vm, kmeta_dst, lane);
   __syncwarp();
   // ---- values: per token over 32-channel spans
   {
@@ -209,12 +245,7 @@ __device__ __forceinline__ void quantize_tile_warp(const __half* ksrc, const __h
   }
   __syncwarp();
   pack_store_tile<D, BITS, false>(ct, vcodes_dst, lane);
-  // metadata planes: 2 * D halves = 4 * D bytes, D / 8 bytes per lane
-  if (D == 128) {
-    reinterpret_cast<uint4*>(vmeta_dst)[lane] = reinterpret_cast<const uint4*>(vm)[lane];
-  } else {
-    reinterpret_cast<uint2*>(vmeta_dst)[lane] = reinterpret_cast<const uint2*>(vm)[lane];
-  }
+  store_meta_lane_order<D, false>(vm, vmeta_dst, lane);
   __syncwarp();
 }
 
@@ -235,6 +266,23 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
 __device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+// 16-byte copy that reads src_bytes (0 or 16) bytes and zero-fills the rest.
+__device__ __forceinline__ void cp_async_16_zfill(void* smem, const void* gmem, int src_bytes) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
+               : "memory");
+}
+// Four 8x8 b16 matrices; lane i supplies the row address of row i%8 of matrix i/8.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem_row);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(s));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* smem_row) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem_row);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(s));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>

@@ -35,6 +35,12 @@ namespace kvq {
 
 constexpr int kTailWeight = 3;  // a 32-token fp16 tail chunk counts as this many groups
 
+// half2(4), half2(16), half2(256): OR-ing a code into the top 2, 4 or 8 mantissa
+// bits of these gives 4 + c, 16 + c or 256 + c exactly.  Kept in constant memory so
+// the unpack's single logic op takes one operand from there and the mask as an
+// immediate.
+__constant__ uint32_t c_expo[3] = {0x44004400u, 0x4C004C00u, 0x5C005C00u};
+
 template <int D, int BITS, int G>
 struct DecodeCfg {
   using T = Tile<D, BITS>;
@@ -50,13 +56,16 @@ struct DecodeCfg {
   static constexpr int NSTAGE = BITS == 2 ? 4 : (BITS == 4 ? 2 : 3);
   static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
   static constexpr int RING = WARPS * NSTAGE * STAGE;
-  static constexpr int PS = WARPS * G * kGroup * 2;  // p~ exchange (halves), bytes
+  static constexpr int PSROW = 48;                   // halves per head row of the p~ exchange
+  static constexpr int PS = WARPS * G * PSROW * 2;   // p~ exchange, bytes
   static constexpr int ZERO = 4 * D;                 // zero row for lanes without a metadata row
+  static constexpr int ONES = 64;                    // half2(1,1) x 16: the denominator row
   static constexpr int PREFIX = (KVQ_MAX_BATCH + 1) * 4;
-  static constexpr int SMEM = RING + PS + ZERO + PREFIX;
+  static constexpr int SMEM = RING + PS + ZERO + ONES + PREFIX;
   static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
   static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
   static_assert(PS % 16 == 0 && RING % 16 == 0, "aligned shared regions");
+  static_assert(NSTAGE * STAGE >= kGroup * (2 * D + 16), "a staged tail chunk fits a warp's ring");
 };
 
 struct DecodeParams {
@@ -135,20 +144,20 @@ template <int D, int BITS, int G>
 struct Decoder {
   using C = DecodeCfg<D, BITS, G>;
   static constexpr int NT = C::NT, KT = C::KT;
-  // Highest bit position (within a 16-bit half) a code can take inside the fp16
-  // mantissa; codes above it are read from the word shifted right by kShift.
-  static constexpr int kLim = 10 - BITS;
-  static constexpr int kShift = BITS == 2 ? 6 : 8;
+  // fp16 offsets carried by the unpacked codes: slots whose pair index i%4 < 2
+  // (first half of a fragment's k range) carry kOff0, the others kOff1.
+  static constexpr float kOff0 = BITS == 2 ? 4.f : (BITS == 4 ? 16.f : 256.f);
+  static constexpr float kOff1 = BITS == 2 ? 16.f : (BITS == 4 ? 16.f : 256.f);
   static constexpr uint32_t kOnes = 0x3C003C00u;  // half2(1, 1)
 
   // Per-warp running state of the online softmax for the G heads.
   float m[NT];
   float o[KT][NT][4];  // P.V accumulators: rows = channels, columns (head, hi|lo)
-  float zc[NT][4];     // rows j < D/32: sum p~ * zero_j; row 8: sum p~ (the denominator)
+  float zc[NT][4];     // value-constant MMA: zero points, scale sums, row 12 = sum p~
   uint32_t qf[NT][KT][2];  // q pairs of column 8nt+gid (head 4nt + gid/2), 0 beyond G
   uint32_t nhl;            // half2(-hl): 0 for the hi column, -1 for the lo column
   uint32_t hi_only;        // half2(1 - hl)
-  uint32_t ones_a;         // the ones row of the value-constant MMA (lanes of row 8)
+  uint32_t ones_a;         // the ones row (row 12) of the value-constant MMA: lanes gid 4
   int lane, gid, tig, hl;
 
   __device__ __forceinline__ void init(const DecodeParams& p, int b, int h) {
@@ -158,7 +167,7 @@ struct Decoder {
     hl = gid & 1;
     nhl = hl ? 0xBC00BC00u : 0u;
     hi_only = hl ? 0u : kOnes;
-    ones_a = gid == 0 ? kOnes : 0u;
+    ones_a = gid == 4 ? kOnes : 0u;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt] = -INFINITY;
@@ -178,24 +187,39 @@ struct Decoder {
     }
   }
 
-  // Exact fp16 pair (c_first, c_second) of pair P of the lane's packed words (w;
-  // ws = the words shifted right by kShift).  P is a compile-time constant after
-  // unrolling.  The code bits land in the mantissa of 2^(10-pos) (pos = their
-  // bit position), giving 2^(10-pos) + c exactly; the subtraction leaves c.
-  static __device__ __forceinline__ uint32_t unpack(const uint32_t* w, const uint32_t* ws, int P) {
-    const int pos0 = BITS * (P % C::PPW);
-    const bool direct = pos0 <= kLim;
-    const int pos = direct ? pos0 : pos0 - kShift;
-    const uint32_t word = direct ? w[P / C::PPW] : ws[P / C::PPW];
-    const uint32_t mask = ((uint32_t)((1 << BITS) - 1) << pos) * 0x10001u;
-    const uint32_t expo = (uint32_t)((25 - pos) << 10) * 0x10001u;  // half2(2^(10-pos))
-    const uint32_t raw = (word & mask) | expo;
-    return h2_as_u32(__hsub2(u32_as_h2(raw), u32_as_h2(expo)));
-  }
-  static __device__ __forceinline__ void frag(const uint32_t* w, const uint32_t* ws, int P0,
-                                              uint32_t (&a)[4]) {
+  // fp16 pairs (off + c_first, off + c_second) of pairs P0 .. P0+7 of the lane's
+  // words (P0 a multiple of 8): one shift and one logic op per pair at most.
+  // 2-bit: a word's slots (0,2), (1,3), (4,6), (5,7) sit at bit positions
+  // (2,0), (6,4), (10,8), (14,12); shifting by 6, 2, -2, -6 puts the first of each
+  // at mantissa bits [8,10) (offset 4) and the second at [6,8) (offset 16).
+  static __device__ __forceinline__ void unpack8(const uint32_t* w, int P0, uint32_t (&a)[8]) {
+    if (BITS == 2) {
+      const uint32_t x = w[P0 / 8];
+      const uint32_t s0 = x << 6, s1 = x << 2, s2 = x >> 2, s3 = x >> 6;
+      const uint32_t e4 = c_expo[0], e16 = c_expo[1];
+      a[0] = (s0 & 0x03000300u) | e4;  a[2] = (s0 & 0x00C000C0u) | e16;
+      a[1] = (s1 & 0x03000300u) | e4;  a[3] = (s1 & 0x00C000C0u) | e16;
+      a[4] = (s2 & 0x03000300u) | e4;  a[6] = (s2 & 0x00C000C0u) | e16;
+      a[5] = (s3 & 0x03000300u) | e4;  a[7] = (s3 & 0x00C000C0u) | e16;
+    } else if (BITS == 4) {
+      const uint32_t e16 = c_expo[1];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = unpack(w, ws, P0 + i);
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t x = w[P0 / 4 + h];
+        a[4 * h + 0] = ((x << 6) & 0x03C003C0u) | e16;
+        a[4 * h + 1] = ((x << 2) & 0x03C003C0u) | e16;
+        a[4 * h + 2] = ((x >> 2) & 0x03C003C0u) | e16;
+        a[4 * h + 3] = ((x >> 6) & 0x03C003C0u) | e16;
+      }
+    } else {
+      const uint32_t e256 = c_expo[2];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t x = w[P0 / 2 + h];
+        a[2 * h + 0] = ((x << 2) & 0x03FC03FCu) | e256;
+        a[2 * h + 1] = ((x >> 6) & 0x03FC03FCu) | e256;
+      }
+    }
   }
 
   // hi column: fp16(x*y); lo column: x*y - fp16(x*y) (exact: x*y has <= 22 bits).
@@ -241,8 +265,8 @@ struct Decoder {
         const __half2 ph = __floats2half2_rn(fast_exp2(lg[nt][mt][0] - m[nt]),
                                              fast_exp2(lg[nt][mt][1] - m[nt]));
         if (g < G) {
-          ps[g * kGroup + 16 * mt + gid] = __low2half(ph);
-          ps[g * kGroup + 16 * mt + gid + 8] = __high2half(ph);
+          ps[g * C::PSROW + 16 * mt + gid] = __low2half(ph);
+          ps[g * C::PSROW + 16 * mt + gid + 8] = __high2half(ph);
         }
       }
     }
@@ -259,26 +283,29 @@ struct Decoder {
       for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          pp[nt][kt][r] = (g < G) ? *reinterpret_cast<const uint32_t*>(ps + g * kGroup + 16 * kt + 2 * tig + 8 * r) : 0u;
+          pp[nt][kt][r] = (g < G) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r) : 0u;
     }
   }
 
   // One quantized 32-token group staged in shared memory.  zrow: a zero row of
   // at least D/2 words in shared memory.
   __device__ __forceinline__ void quant_group(const uint8_t* stage, __half* ps, const uint32_t* zrow,
-                                              float scale_log2) {
+                                              const uint32_t* orow, float scale_log2) {
     const uint4* s4 = reinterpret_cast<const uint4*>(stage);
-    uint32_t kw[C::NWL], kws[C::NWL];
+    uint32_t kw[C::NWL];
 #pragma unroll
     for (int ch = 0; ch < C::NWL / 4; ++ch) {
       const uint4 v = s4[ch * 32 + lane];
       kw[4 * ch] = v.x; kw[4 * ch + 1] = v.y; kw[4 * ch + 2] = v.z; kw[4 * ch + 3] = v.w;
     }
-#pragma unroll
-    for (int i = 0; i < C::NWL; ++i) kws[i] = kw[i] >> kShift;
-    const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);  // scale pairs, zero pairs
-    // K-constant MMA rows: row 0 = zero points (lanes gid 0), other rows 0
-    const uint32_t* krow = gid == 0 ? km + D / 2 : zrow;
+    // key metadata, lane order: pair (kt, r) of this lane at 16(kt/2) + 4tig + 2(kt%2) + r
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);
+    const uint32_t* ks = km + 4 * tig;           // scale pairs
+    const uint32_t* kz = km + D / 2 + 4 * tig;   // zero-point pairs
+    // constant-MMA rows: 0 = zero points, 1 = scales of channels 16kt+[0,8),
+    // 2 = scales of channels 16kt+[8,16); a0 reads (kt, r=0) words, a2 (kt, r=1)
+    const uint32_t* rowA = gid == 0 ? kz : (gid == 1 ? ks : zrow);
+    const uint32_t* rowB = gid == 0 ? kz : (gid == 2 ? ks : zrow);
     float sacc[2][NT][4];
     float cacc[NT][4];
 #pragma unroll
@@ -286,49 +313,63 @@ struct Decoder {
 #pragma unroll
       for (int i = 0; i < 4; ++i) { sacc[0][nt][i] = 0.f; sacc[1][nt][i] = 0.f; cacc[nt][i] = 0.f; }
 #pragma unroll
-    for (int kt = 0; kt < KT; ++kt) {
-      const uint32_t sp0 = km[8 * kt + tig], sp1 = km[8 * kt + 4 + tig];
-      uint32_t a0[4], a1[4];
-      frag(kw, kws, (kt * 2 + 0) * 4, a0);  // pairs of (kt, mt = 0)
-      frag(kw, kws, (kt * 2 + 1) * 4, a1);  // pairs of (kt, mt = 1)
-      const uint32_t ac[4] = {krow[8 * kt + tig], 0u, krow[8 * kt + 4 + tig], 0u};
+    for (int kt2 = 0; kt2 < KT; kt2 += 2) {
+      const uint4 sv = *reinterpret_cast<const uint4*>(ks + 8 * kt2);
+      const uint4 av = *reinterpret_cast<const uint4*>(rowA + 8 * kt2);
+      const uint4 bv = *reinterpret_cast<const uint4*>(rowB + 8 * kt2);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t b0 = split_mul(qf[nt][kt][0], sp0);
-        const uint32_t b1 = split_mul(qf[nt][kt][1], sp1);
-        mma_16816(sacc[0][nt], a0, b0, b1);
-        mma_16816(sacc[1][nt], a1, b0, b1);
-        mma_16816(cacc[nt], ac, qf[nt][kt][0], qf[nt][kt][1]);
+      for (int h = 0; h < 2; ++h) {
+        const int kt = kt2 + h;
+        const uint32_t sp0 = h ? sv.z : sv.x, sp1 = h ? sv.w : sv.y;
+        uint32_t a[8];
+        unpack8(kw, kt * 8, a);  // pairs of (kt, mt = 0) then (kt, mt = 1)
+        const uint32_t a0[4] = {a[0], a[1], a[2], a[3]};
+        const uint32_t a1[4] = {a[4], a[5], a[6], a[7]};
+        const uint32_t ac[4] = {h ? av.z : av.x, 0u, h ? bv.w : bv.y, 0u};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t b0 = split_mul(qf[nt][kt][0], sp0);
+          const uint32_t b1 = split_mul(qf[nt][kt][1], sp1);
+          mma_16816(sacc[0][nt], a0, b0, b1);
+          mma_16816(sacc[1][nt], a1, b0, b1);
+          mma_16816(cacc[nt], ac, qf[nt][kt][0], qf[nt][kt][1]);
+        }
       }
     }
     float lg[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float zq = __shfl_sync(0xffffffffu, cacc[nt][0], tig);  // sum_d q z of head 4nt+tig
+      // sum_d q z - off0 * sum_{first halves} q s - off1 * sum_{second halves} q s, head 4nt+tig
+      const float zq = __shfl_sync(0xffffffffu, cacc[nt][0], tig);
+      const float s0 = __shfl_sync(0xffffffffu, cacc[nt][0], 4 + tig);
+      const float s1 = __shfl_sync(0xffffffffu, cacc[nt][0], 8 + tig);
+      const float kc = zq - kOff0 * s0 - kOff1 * s1;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          lg[nt][mt][r] = (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1] + zq) * scale_log2;
+          lg[nt][mt][r] = (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1] + kc) * scale_log2;
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
     load_pp(ps, pp);
     // ---- P.V
-    uint32_t vw[C::NWL], vws[C::NWL];
+    uint32_t vw[C::NWL];
 #pragma unroll
     for (int ch = 0; ch < C::NWL / 4; ++ch) {
       const uint4 v = s4[(C::TB / 16) + ch * 32 + lane];
       vw[4 * ch] = v.x; vw[4 * ch + 1] = v.y; vw[4 * ch + 2] = v.z; vw[4 * ch + 3] = v.w;
     }
-#pragma unroll
-    for (int i = 0; i < C::NWL; ++i) vws[i] = vw[i] >> kShift;
+    // value metadata, lane order: pair (j, kt, r) of this lane at 16j + 4tig + 2kt + r
     const uint32_t* vm = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB + C::KMETA);
+    const uint32_t* vsl = vm + 4 * tig;          // scale pairs
+    const uint32_t* vzl = vm + D / 2 + 4 * tig;  // zero pairs
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
+      const uint4 sv = *reinterpret_cast<const uint4*>(vsl + 16 * j);
 #pragma unroll
       for (int kt = 0; kt < 2; ++kt) {
-        const uint32_t vs0 = vm[16 * j + 8 * kt + tig], vs1 = vm[16 * j + 8 * kt + 4 + tig];
+        const uint32_t vs0 = kt ? sv.z : sv.x, vs1 = kt ? sv.w : sv.y;
         uint32_t b[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -338,57 +379,77 @@ struct Decoder {
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
           const int mt = 2 * j + mi;
-          uint32_t a[4];
-          frag(vw, vws, (mt * 2 + kt) * 4, a);  // pairs of (mt, kt)
+          uint32_t a8[8];
+          unpack8(vw, mt * 8, a8);  // pairs of (mt, kt = 0) then (mt, kt = 1)
+          const uint32_t a[4] = {a8[4 * kt], a8[4 * kt + 1], a8[4 * kt + 2], a8[4 * kt + 3]};
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, b[nt][0], b[nt][1]);
         }
       }
     }
-    // value zero points (rows j < D/32) and the softmax denominator (row 8)
-    const uint32_t* vrow = gid < D / 32 ? vm + D / 2 + 16 * gid : zrow;
+    // constant-MMA rows (tokens 16kt + 2tig (+8r)): 0..D/32-1 = zero points of group
+    // j; 4+j = scales of group j, first token halves (a0 only); 8+j (a3) = scales,
+    // second token halves; 12 = ones (the softmax denominator)
+    const uint32_t* r0 = gid < D / 32 ? vzl + 16 * gid : (gid >= 4 && gid < 4 + D / 32 ? vsl + 16 * (gid - 4) : zrow);
+    const uint32_t* r2 = gid < D / 32 ? vzl + 16 * gid : zrow;
+    const uint32_t* r3 = gid < D / 32 ? vsl + 16 * gid : (gid == 4 ? orow + 4 * tig : zrow);
+    const uint4 v0 = *reinterpret_cast<const uint4*>(r0);
+    const uint4 v2 = *reinterpret_cast<const uint4*>(r2);
+    const uint4 v3 = *reinterpret_cast<const uint4*>(r3);
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
-      const uint32_t ac[4] = {vrow[8 * kt + tig], ones_a, vrow[8 * kt + 4 + tig], ones_a};
+      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v2.w : v2.y, kt ? v3.w : v3.y};
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
     }
     __syncwarp();
   }
 
-  // One chunk of up to 32 fp16 tail tokens, read from the ring in global memory.
-  __device__ __forceinline__ void tail_chunk(const __half* kt_base, const __half* vt_base, int first,
-                                             int count, int th, int R, __half* ps, float scale_log2) {
+  // One chunk of up to 32 fp16 tail tokens.  The rows are staged through the
+  // warp's (idle) stage ring: keys first, then values, each as 32 rows of D
+  // halves at a padded pitch (conflict-free fragment loads), missing tokens
+  // zero-filled.  Fragments come from ldmatrix (keys) and ldmatrix.trans
+  // (values, the transposed operand of P.V).
+  static constexpr int kPitch = 2 * D + 16;  // bytes per staged row
+  __device__ __forceinline__ void stage_rows(uint8_t* buf, const __half* base, int first, int count,
+                                             int th, int R) const {
+    constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
+#pragma unroll 4
+    for (int e = lane; e < kGroup * CPR; e += 32) {
+      const int t = e / CPR, ch = e % CPR;
+      const bool ok = t < count;
+      const __half* src = base + (size_t)(ok ? (th + first + t) % R : 0) * D + ch * 8;
+      cp_async_16_zfill(buf + t * kPitch + ch * 16, src, ok ? 16 : 0);
+    }
+    cp_async_commit();
+  }
+  __device__ __forceinline__ void tail_chunk(uint8_t* buf, const __half* kt_base, const __half* vt_base,
+                                             int first, int count, int th, int R, __half* ps,
+                                             float scale_log2) {
+    stage_rows(buf, kt_base, first, count, th, R);
+    cp_async_wait<0>();
+    __syncwarp();
     float sacc[2][NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) { sacc[0][nt][i] = 0.f; sacc[1][nt][i] = 0.f; }
-    int rowoff[2][2];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = 16 * mt + gid + 8 * r;
-        rowoff[mt][r] = t < count ? ((th + first + t) % R) * D : -1;
-      }
+    // lane's ldmatrix row: matrix lane/8 -> (+8 rows if bit 0, +8 columns if bit 1)
+    const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lcol = 8 * (lane >> 4);
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt) {
       uint32_t a[2][4];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int ro = rowoff[mt][i & 1];
-          const int c = 16 * kt + 2 * tig + 8 * (i >> 1);
-          a[mt][i] = ro >= 0 ? __ldg(reinterpret_cast<const unsigned int*>(kt_base + ro + c)) : 0u;
-        }
+        ldmatrix_x4(a[mt], buf + (16 * mt + lrow) * kPitch + (16 * kt + lcol) * 2);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         mma_16816(sacc[0][nt], a[0], qf[nt][kt][0], qf[nt][kt][1]);
         mma_16816(sacc[1][nt], a[1], qf[nt][kt][0], qf[nt][kt][1]);
       }
     }
+    __syncwarp();
+    stage_rows(buf, vt_base, first, count, th, R);  // overlaps the softmax below
     float lg[NT][2][2];  // B = q in both columns of a head: use one of them
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -396,21 +457,16 @@ struct Decoder {
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          lg[nt][mt][r] = rowoff[mt][r] >= 0 ? sacc[mt][nt][2 * r] * scale_log2 : -INFINITY;
+          lg[nt][mt][r] = (16 * mt + gid + 8 * r) < count ? sacc[mt][nt][2 * r] * scale_log2 : -INFINITY;
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
     load_pp(ps, pp);
-    const unsigned short* vt = reinterpret_cast<const unsigned short*>(vt_base);
+    cp_async_wait<0>();
+    __syncwarp();
+    // value rows: A[d][t] = v[t][d]; matrix lane/8 -> (+8 channels if bit 0, +8 tokens if bit 1)
+    const int vtok = (lane & 7) + 8 * (lane >> 4), vch = 8 * ((lane >> 3) & 1);
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
-      int tok[2][2];  // [i>>1][e] -> ring row offset or -1
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = 16 * kt + 2 * tig + 8 * hh + e;
-          tok[hh][e] = t < count ? ((th + first + t) % R) * D : -1;
-        }
       uint32_t bh[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -420,14 +476,7 @@ struct Decoder {
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
         uint32_t a[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = 16 * mt + gid + 8 * (i & 1);
-          const int r0 = tok[i >> 1][0], r1 = tok[i >> 1][1];
-          const uint32_t lo = r0 >= 0 ? (uint32_t)__ldg(vt + r0 + c) : 0u;
-          const uint32_t hi = r1 >= 0 ? (uint32_t)__ldg(vt + r1 + c) : 0u;
-          a[i] = lo | (hi << 16);
-        }
+        ldmatrix_x4_trans(a, buf + (16 * kt + vtok) * kPitch + (16 * mt + vch) * 2);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, bh[nt][0], bh[nt][1]);
       }
@@ -443,10 +492,15 @@ struct Decoder {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
-      const float lt = __shfl_sync(0xffffffffu, zc[nt][2], tig);  // row 8 lives in lanes gid 0
+      const float lt = __shfl_sync(0xffffffffu, zc[nt][2], 16 + tig);  // row 12: lanes gid 4
       float vc[D / 32];
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) vc[j] = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);
+      for (int j = 0; j < D / 32; ++j) {
+        const float zs = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);         // row j
+        const float s0 = __shfl_sync(0xffffffffu, zc[nt][0], 4 * (4 + j) + tig);   // row 4+j
+        const float s1 = __shfl_sync(0xffffffffu, zc[nt][2], 4 * j + tig);         // row 8+j
+        vc[j] = zs - kOff0 * s0 - kOff1 * s1;
+      }
       if (g < G) {
         float* d = dst + g * C::PSTRIDE;
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
@@ -461,23 +515,57 @@ struct Decoder {
 };
 
 // Log-sum-exp merge of a segment's nparts consecutive partials into the
-// normalised output [G][D].  Partials come from other CTAs: read through L2.
+// normalised output [G][D], by the whole CTA.  Partials come from other CTAs and
+// are read through L2; each phase issues all its loads before using any, so a
+// phase costs about one L2 round trip.  s_w: shared scratch of at least
+// 2 * G * nparts + G floats.
 template <int D, int G>
-__device__ void final_merge(const float* parts, int nparts, float* out, int tid, int nthreads) {
+__device__ void final_merge(const float* parts, int nparts, float* out, float* s_w) {
   constexpr int PS = D + 4;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  float* s_m = s_w;                  // [nparts][G] m, then the weights
+  float* s_l = s_w + nparts * G;     // [nparts][G] l
+  float* s_lt = s_w + 2 * nparts * G;  // [G] total l
+  for (int e = tid; e < nparts * G; e += nthreads) {
+    const float* src = parts + (size_t)(e / G) * G * PS + (e % G) * PS;
+    const float mv = __ldcg(src), lv = __ldcg(src + 1);
+    s_m[e] = mv;
+    s_l[e] = lv;
+  }
+  __syncthreads();
+  // one warp per head: max, weights 2^(m_i - M), total l
+  for (int g = warp; g < G; g += nthreads / 32) {
+    float mx = -INFINITY;
+    for (int i = lane; i < nparts; i += 32) mx = fmaxf(mx, s_m[i * G + g]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float lsum = 0.f;
+    for (int i = lane; i < nparts; i += 32) {
+      const float w = mx == -INFINITY ? 0.f : exp2f(s_m[i * G + g] - mx);
+      s_m[i * G + g] = w;
+      lsum += w * s_l[i * G + g];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if (lane == 0) s_lt[g] = lsum;
+  }
+  __syncthreads();
+  // o = sum_i w_i o_i / l: 16 independent loads in flight per output
+  constexpr int U = 16;
   for (int e = tid; e < G * D; e += nthreads) {
     const int g = e / D, d = e % D;
-    float mx = -INFINITY;
-    for (int i = 0; i < nparts; ++i) mx = fmaxf(mx, __ldcg(parts + (size_t)i * G * PS + g * PS));
-    float lsum = 0.f, osum = 0.f;
-    if (mx != -INFINITY) {
-      for (int i = 0; i < nparts; ++i) {
-        const float* src = parts + (size_t)i * G * PS + g * PS;
-        const float w = exp2f(__ldcg(src) - mx);
-        lsum += w * __ldcg(src + 1);
-        osum += w * __ldcg(src + 4 + d);
-      }
+    const float* src = parts + g * PS + 4 + d;
+    float osum = 0.f;
+    for (int i0 = 0; i0 < nparts; i0 += U) {
+      float v[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) v[k] = (i0 + k < nparts) ? __ldcg(src + (size_t)(i0 + k) * G * PS) : 0.f;
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+        if (i0 + k < nparts) osum += s_m[(i0 + k) * G + g] * v[k];
     }
+    const float lsum = s_lt[g];
     out[g * D + d] = lsum > 0.f ? osum / lsum : 0.f;
   }
 }
@@ -491,12 +579,14 @@ decode_kernel(const DecodeParams p) {
   uint8_t* ring = smem;
   __half* ps_all = reinterpret_cast<__half*>(smem + C::RING);
   uint32_t* zrow = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS);
-  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS + C::ZERO);
+  uint32_t* orow = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS + C::ZERO);
+  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS + C::ZERO + C::ONES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __half* ps = ps_all + warp * G * kGroup;
+  __half* ps = ps_all + warp * G * C::PSROW;
   uint8_t* wring = ring + warp * C::NSTAGE * C::STAGE;
 
   for (int i = threadIdx.x; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
+  if (threadIdx.x < C::ONES / 4) orow[threadIdx.x] = 0x3C003C00u;
   build_prefix(p, s_pref);
   __syncthreads();
   const int64_t total = (int64_t)p.hkv * s_pref[p.batch];
@@ -530,22 +620,28 @@ decode_kernel(const DecodeParams p) {
     {
       const int ga = ia, cnt = max(0, min(ie, ng) - ia);
       const size_t gbase = (size_t)seg * p.max_groups + ga;
+      // this lane's first 16 bytes of each array for group ga; group idx adds idx * size
+      const uint8_t* kc0 = p.k_codes + gbase * C::TB + lane * 16;
+      const uint8_t* vc0 = p.v_codes + gbase * C::TB + lane * 16;
+      const uint8_t* km0 = reinterpret_cast<const uint8_t*>(p.k_meta) + gbase * C::KMETA + lane * 16;
+      const uint8_t* vm0 = reinterpret_cast<const uint8_t*>(p.v_meta) + gbase * C::VMETA + lane * 16;
+      uint8_t* dst0 = wring + lane * 16;
       auto issue = [&](int idx, int slotn) {
-        const size_t g = gbase + idx;
-        uint8_t* dst = wring + slotn * C::STAGE;
-        const uint8_t* kc = p.k_codes + g * C::TB;
-        const uint8_t* vc = p.v_codes + g * C::TB;
-        const uint8_t* km = reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA;
-        const uint8_t* vm = reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA;
+        uint8_t* dst = dst0 + slotn * C::STAGE;
+        const uint8_t* kc = kc0 + (size_t)idx * C::TB;
+        const uint8_t* vc = vc0 + (size_t)idx * C::TB;
+        const uint8_t* km = km0 + (size_t)idx * C::KMETA;
+        const uint8_t* vm = vm0 + (size_t)idx * C::VMETA;
 #pragma unroll
-        for (int o = lane * 16; o < C::TB; o += 512) cp_async_16(dst + o, kc + o);
+        for (int o = 0; o < C::TB; o += 512) cp_async_16(dst + o, kc + o);
 #pragma unroll
-        for (int o = lane * 16; o < C::TB; o += 512) cp_async_16(dst + C::TB + o, vc + o);
+        for (int o = 0; o < C::TB; o += 512) cp_async_16(dst + C::TB + o, vc + o);
 #pragma unroll
-        for (int o = lane * 16; o < C::KMETA; o += 512) cp_async_16(dst + 2 * C::TB + o, km + o);
+        for (int o = 0; o < C::KMETA; o += 512)
+          if (o + lane * 16 < C::KMETA) cp_async_16(dst + 2 * C::TB + o, km + o);
 #pragma unroll
-        for (int o = lane * 16; o < C::VMETA; o += 512)
-          cp_async_16(dst + 2 * C::TB + C::KMETA + o, vm + o);
+        for (int o = 0; o < C::VMETA; o += 512)
+          if (o + lane * 16 < C::VMETA) cp_async_16(dst + 2 * C::TB + C::KMETA + o, vm + o);
       };
 #pragma unroll
       for (int s = 0; s < C::NSTAGE - 1; ++s) {
@@ -557,7 +653,7 @@ decode_kernel(const DecodeParams p) {
         cp_async_commit();
         cp_async_wait<C::NSTAGE - 1>();
         __syncwarp();
-        dec.quant_group(wring + (i % C::NSTAGE) * C::STAGE, ps, zrow, p.scale_log2);
+        dec.quant_group(wring + (i % C::NSTAGE) * C::STAGE, ps, zrow, orow, p.scale_log2);
       }
       cp_async_wait<0>();
       __syncwarp();
@@ -568,7 +664,7 @@ decode_kernel(const DecodeParams p) {
       if (u % kTailWeight != 0) continue;
       const int first = (u / kTailWeight) * kGroup;
       if (first >= L.nt) continue;
-      dec.tail_chunk(p.k_tail + (size_t)seg * R * D, p.v_tail + (size_t)seg * R * D, first,
+      dec.tail_chunk(wring, p.k_tail + (size_t)seg * R * D, p.v_tail + (size_t)seg * R * D, first,
                      min(kGroup, L.nt - first), L.th, R, ps, p.scale_log2);
     }
     // warp partial into the warp's (now idle) ring slice, then the CTA merge
@@ -602,8 +698,10 @@ decode_kernel(const DecodeParams p) {
     __syncthreads();
     if (s_last) {
       __threadfence();
+      // the stage ring is idle here: its first bytes hold the merge weights
       final_merge<D, G>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
-                        p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D, threadIdx.x, blockDim.x);
+                        p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D,
+                        reinterpret_cast<float*>(ring));
       if (threadIdx.x == 0) p.counters[seg] = 0;
     }
     __syncthreads();
@@ -644,13 +742,15 @@ struct DecodeLaunch {
         return 0;
       }
       cached = sms * per;
+      // the final merge keeps two floats per (partial, head) in the stage ring
+      if (cached > C::RING / (8 * G) - 1) cached = C::RING / (8 * G) - 1;
     }
     return cached;
   }
   static kvq_status run(DecodeParams p, cudaStream_t s) {
     using C = DecodeCfg<D, BITS, G>;
     int err = 0;
-    const int n = slots(&err);
+    const int n = slots(&err);  // <= RING / (8 G): the final merge keeps 2 floats per partial
     if (err) return KVQ_ERR_CUDA;
     p.n_stream = n;
     decode_kernel<D, BITS, G><<<n, C::WARPS * 32, C::SMEM, s>>>(p);
