@@ -60,6 +60,7 @@ typedef enum {
 /* Bits OR-ed into *error_flags by device code. */
 #define KVQ_DEVERR_APPEND_CAPACITY 1 /* append needed a flush but the quantized region was full */
 #define KVQ_DEVERR_BAD_LENGTHS 2     /* decode saw n_tail > tail_cap or n_quant beyond capacity */
+#define KVQ_DEVERR_TIMEOUT 4         /* a bounded wait for staged data gave up; output invalid */
 
 #define KVQ_GROUP 32
 #define KVQ_MAX_BATCH 512 /* sequences per prefill call */
@@ -209,7 +210,8 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t n_q_heads,
  *
  *   q         fp16 device [batch][Hq][D], contiguous; query head hq reads KV
  *             head hq / (Hq/Hkv)
- *   out       fp32 device [batch][Hq][D]: softmax(sm_scale * q.K_hat^T) . V_hat over
+ *   out       fp32 device [batch][Hq][D], 16-byte aligned:
+ *             softmax(sm_scale * q.K_hat^T) . V_hat over
  *             the n_quant quantized tokens and the n_tail fp16 tail tokens of
  *             each sequence (all zeros for an empty sequence)
  *   sm_scale  softmax scale, typically 1/sqrt(D)

@@ -34,6 +34,9 @@
 namespace kvq {
 
 constexpr int kTailWeight = 3;  // a 32-token fp16 tail chunk counts as this many groups
+// Polls of an mbarrier before a wait gives up (each poll may suspend the thread
+// briefly): far longer than any copy takes, short enough to end a stuck kernel.
+constexpr uint32_t kMaxPolls = 1u << 22;
 
 // half2(4), half2(16), half2(256): OR-ing a code into the top 2, 4 or 8 mantissa
 // bits of these gives 4 + c, 16 + c or 256 + c exactly.  Kept in constant memory so
@@ -52,19 +55,29 @@ struct DecodeCfg {
   static constexpr int KT = D / 16;
   static constexpr int NWL = T::kWordsPerLane;
   static constexpr int PPW = T::kPairsPerWord;
+  // 2 CTAs per SM (16 warps) for 2- and 4-bit codes
   static constexpr int WARPS = BITS == 8 ? 4 : 8;
   static constexpr int NSTAGE = BITS == 2 ? 4 : (BITS == 4 ? 2 : 3);
+  static constexpr int MIN_CTAS = BITS == 8 ? 1 : 2;
   static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
   static constexpr int RING = WARPS * NSTAGE * STAGE;
   static constexpr int PSROW = 48;                   // halves per head row of the p~ exchange
   static constexpr int PS = WARPS * G * PSROW * 2;   // p~ exchange, bytes
   static constexpr int ZERO = 4 * D;                 // zero row for lanes without a metadata row
   static constexpr int ONES = 64;                    // half2(1,1) x 16: the denominator row
-  static constexpr int PREFIX = (KVQ_MAX_BATCH + 1) * 4;
-  static constexpr int SMEM = RING + PS + ZERO + ONES + PREFIX;
+  static constexpr int PREFIX = ((KVQ_MAX_BATCH + 1) * 4 + 15) / 16 * 16;
+  static constexpr int QS = NT * 4 * (D / 2) * 4;     // q pairs of the segment's heads, lane order
+  static constexpr int MBAR = (WARPS * NSTAGE + 1) * 8;  // one mbarrier per stage + the merge's
+  static constexpr int SMEM = RING + PS + ZERO + ONES + PREFIX + QS + MBAR;
+  // partials staged per merge batch: they fit the ring, their weights the p~ area
+  static constexpr int MERGE_BATCH = RING / (G * PSTRIDE * 4) < PS / (4 * G) ? RING / (G * PSTRIDE * 4)
+                                                                              : PS / (4 * G);
+  static_assert(MERGE_BATCH >= 1, "a merge batch holds at least one partial");
   static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
   static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
-  static_assert(PS % 16 == 0 && RING % 16 == 0, "aligned shared regions");
+  static_assert(PS % 16 == 0 && RING % 16 == 0 && ZERO % 16 == 0 && ONES % 16 == 0 && PREFIX % 16 == 0 &&
+                    QS % 16 == 0,
+                "aligned shared regions (the mbarriers need 8 bytes, the copies 16)");
   static_assert(NSTAGE * STAGE >= kGroup * (2 * D + 16), "a staged tail chunk fits a warp's ring");
 };
 
@@ -154,13 +167,14 @@ struct Decoder {
   float m[NT];
   float o[KT][NT][4];  // P.V accumulators: rows = channels, columns (head, hi|lo)
   float zc[NT][4];     // value-constant MMA: zero points, scale sums, row 12 = sum p~
-  uint32_t qf[NT][KT][2];  // q pairs of column 8nt+gid (head 4nt + gid/2), 0 beyond G
+  const uint32_t* qs;      // q pairs of column 8nt+gid (head 4nt + gid/2) in shared memory
   uint32_t nhl;            // half2(-hl): 0 for the hi column, -1 for the lo column
   uint32_t hi_only;        // half2(1 - hl)
   uint32_t ones_a;         // the ones row (row 12) of the value-constant MMA: lanes gid 4
   int lane, gid, tig, hl;
 
-  __device__ __forceinline__ void init(const DecodeParams& p, int b, int h) {
+  // q_smem: the segment's q pairs in lane order ([4 NT heads][D/2] words)
+  __device__ __forceinline__ void init(const uint32_t* q_smem) {
     lane = threadIdx.x & 31;
     gid = lane >> 2;
     tig = lane & 3;
@@ -168,6 +182,7 @@ struct Decoder {
     nhl = hl ? 0xBC00BC00u : 0u;
     hi_only = hl ? 0u : kOnes;
     ones_a = gid == 4 ? kOnes : 0u;
+    qs = q_smem + (gid >> 1) * (D / 2) + 4 * tig;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt] = -INFINITY;
@@ -177,14 +192,11 @@ struct Decoder {
       for (int kt = 0; kt < KT; ++kt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[kt][nt][i] = 0.f;
-      const int g = 4 * nt + (gid >> 1);
-      const __half* qh = p.q + ((size_t)b * p.hkv * G + (size_t)h * G + g) * D;
-#pragma unroll
-      for (int kt = 0; kt < KT; ++kt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-          qf[nt][kt][r] = (g < G) ? *reinterpret_cast<const uint32_t*>(qh + 16 * kt + 2 * tig + 8 * r) : 0u;
     }
+  }
+  // q pairs (kt, r) and (kt + 1, r) of this lane's column in n-tile nt (kt even)
+  __device__ __forceinline__ uint4 qpairs(int nt, int kt) const {
+    return *reinterpret_cast<const uint4*>(qs + nt * 4 * (D / 2) + 8 * kt);
   }
 
   // fp16 pairs (off + c_first, off + c_second) of pairs P0 .. P0+7 of the lane's
@@ -306,14 +318,21 @@ struct Decoder {
     // 2 = scales of channels 16kt+[8,16); a0 reads (kt, r=0) words, a2 (kt, r=1)
     const uint32_t* rowA = gid == 0 ? kz : (gid == 1 ? ks : zrow);
     const uint32_t* rowB = gid == 0 ? kz : (gid == 2 ? ks : zrow);
-    float sacc[2][NT][4];
-    float cacc[NT][4];
+    constexpr int CH = 2;  // two independent accumulation chains over kt (shorter MMA dependency)
+    float sacc[CH][2][NT][4];
+    float cacc[CH][NT][4];
+#pragma unroll
+    for (int ch = 0; ch < CH; ++ch)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { sacc[0][nt][i] = 0.f; sacc[1][nt][i] = 0.f; cacc[nt][i] = 0.f; }
+      for (int i = 0; i < 4; ++i) { sacc[ch][0][nt][i] = 0.f; sacc[ch][1][nt][i] = 0.f; cacc[ch][nt][i] = 0.f; }
 #pragma unroll
     for (int kt2 = 0; kt2 < KT; kt2 += 2) {
+      const int ch = (kt2 / 2) % CH;
+      uint4 qv[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) qv[nt] = qpairs(nt, kt2);
       const uint4 sv = *reinterpret_cast<const uint4*>(ks + 8 * kt2);
       const uint4 av = *reinterpret_cast<const uint4*>(rowA + 8 * kt2);
       const uint4 bv = *reinterpret_cast<const uint4*>(rowB + 8 * kt2);
@@ -328,27 +347,38 @@ struct Decoder {
         const uint32_t ac[4] = {h ? av.z : av.x, 0u, h ? bv.w : bv.y, 0u};
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const uint32_t b0 = split_mul(qf[nt][kt][0], sp0);
-          const uint32_t b1 = split_mul(qf[nt][kt][1], sp1);
-          mma_16816(sacc[0][nt], a0, b0, b1);
-          mma_16816(sacc[1][nt], a1, b0, b1);
-          mma_16816(cacc[nt], ac, qf[nt][kt][0], qf[nt][kt][1]);
+          const uint32_t q0 = h ? qv[nt].z : qv[nt].x, q1 = h ? qv[nt].w : qv[nt].y;
+          const uint32_t b0 = split_mul(q0, sp0);
+          const uint32_t b1 = split_mul(q1, sp1);
+          mma_16816(sacc[ch][0][nt], a0, b0, b1);
+          mma_16816(sacc[ch][1][nt], a1, b0, b1);
+          mma_16816(cacc[ch][nt], ac, q0, q1);
         }
       }
     }
+#pragma unroll
+    for (int c2 = 1; c2 < CH; ++c2)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          sacc[0][0][nt][i] += sacc[c2][0][nt][i];
+          sacc[0][1][nt][i] += sacc[c2][1][nt][i];
+          cacc[0][nt][i] += cacc[c2][nt][i];
+        }
     float lg[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       // sum_d q z - off0 * sum_{first halves} q s - off1 * sum_{second halves} q s, head 4nt+tig
-      const float zq = __shfl_sync(0xffffffffu, cacc[nt][0], tig);
-      const float s0 = __shfl_sync(0xffffffffu, cacc[nt][0], 4 + tig);
-      const float s1 = __shfl_sync(0xffffffffu, cacc[nt][0], 8 + tig);
+      const float zq = __shfl_sync(0xffffffffu, cacc[0][nt][0], tig);
+      const float s0 = __shfl_sync(0xffffffffu, cacc[0][nt][0], 4 + tig);
+      const float s1 = __shfl_sync(0xffffffffu, cacc[0][nt][0], 8 + tig);
       const float kc = zq - kOff0 * s0 - kOff1 * s1;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          lg[nt][mt][r] = (sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1] + kc) * scale_log2;
+          lg[nt][mt][r] = (sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + kc) * scale_log2;
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
@@ -444,8 +474,10 @@ struct Decoder {
         ldmatrix_x4(a[mt], buf + (16 * mt + lrow) * kPitch + (16 * kt + lcol) * 2);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        mma_16816(sacc[0][nt], a[0], qf[nt][kt][0], qf[nt][kt][1]);
-        mma_16816(sacc[1][nt], a[1], qf[nt][kt][0], qf[nt][kt][1]);
+        const uint4 qv = qpairs(nt, kt & ~1);
+        const uint32_t q0 = (kt & 1) ? qv.z : qv.x, q1 = (kt & 1) ? qv.w : qv.y;
+        mma_16816(sacc[0][nt], a[0], q0, q1);
+        mma_16816(sacc[1][nt], a[1], q0, q1);
       }
     }
     __syncwarp();
@@ -515,65 +547,84 @@ struct Decoder {
 };
 
 // Log-sum-exp merge of a segment's nparts consecutive partials into the
-// normalised output [G][D], by the whole CTA.  Partials come from other CTAs and
-// are read through L2; each phase issues all its loads before using any, so a
-// phase costs about one L2 round trip.  s_w: shared scratch of at least
-// 2 * G * nparts + G floats.
-template <int D, int G>
-__device__ void final_merge(const float* parts, int nparts, float* out, float* s_w) {
-  constexpr int PS = D + 4;
+// normalised output [G][D], by the whole CTA.  The partials come from other CTAs:
+// one thread bulk-copies them, MERGE_BATCH at a time, into the (idle) stage ring,
+// so a batch costs one memory round trip; the arithmetic then runs out of shared
+// memory.  Returns false if a bounded wait gave up.
+template <int D, int BITS, int G>
+__device__ bool final_merge(const float* parts, int nparts, float* out, uint8_t* ring, float* s_w,
+                            uint64_t* bar, uint32_t& parity) {
+  using C = DecodeCfg<D, BITS, G>;
+  constexpr int PS = C::PSTRIDE;
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
-  float* s_m = s_w;                  // [nparts][G] m, then the weights
-  float* s_l = s_w + nparts * G;     // [nparts][G] l
-  float* s_lt = s_w + 2 * nparts * G;  // [G] total l
-  for (int e = tid; e < nparts * G; e += nthreads) {
-    const float* src = parts + (size_t)(e / G) * G * PS + (e % G) * PS;
-    const float mv = __ldcg(src), lv = __ldcg(src + 1);
-    s_m[e] = mv;
-    s_l[e] = lv;
-  }
-  __syncthreads();
-  // one warp per head: max, weights 2^(m_i - M), total l
-  for (int g = warp; g < G; g += nthreads / 32) {
-    float mx = -INFINITY;
-    for (int i = lane; i < nparts; i += 32) mx = fmaxf(mx, s_m[i * G + g]);
+  __shared__ float s_M[G], s_L[G], s_scale[G];
+  constexpr int PER = (G * D + C::WARPS * 32 - 1) / (C::WARPS * 32);  // outputs per thread
+  float acc[PER];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float lsum = 0.f;
-    for (int i = lane; i < nparts; i += 32) {
-      const float w = mx == -INFINITY ? 0.f : exp2f(s_m[i * G + g] - mx);
-      s_m[i * G + g] = w;
-      lsum += w * s_l[i * G + g];
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  if (tid < G) { s_M[tid] = -INFINITY; s_L[tid] = 0.f; }
+  bool ok = true;
+  const float* stage = reinterpret_cast<const float*>(ring);
+  for (int first = 0; first < nparts; first += C::MERGE_BATCH) {
+    const int nb = min(C::MERGE_BATCH, nparts - first);
+    __syncthreads();  // the ring (and s_w) are free
+    if (tid == 0) {
+      const uint32_t bytes = (uint32_t)(nb * G * PS * 4);
+      fence_proxy_async();
+      mbar_arrive_expect_tx(bar, bytes);
+      tma_load_1d(ring, parts + (size_t)first * G * PS, bytes, bar);
     }
+    ok = mbar_wait(bar, parity, kMaxPolls) && ok;
+    parity ^= 1u;
+    // per head (one warp each): batch max, new running max, weights, l
+    for (int g = warp; g < G; g += nthreads / 32) {
+      float mx = -INFINITY;
+      for (int i = lane; i < nb; i += 32) mx = fmaxf(mx, stage[(i * G + g) * PS]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    if (lane == 0) s_lt[g] = lsum;
-  }
-  __syncthreads();
-  // o = sum_i w_i o_i / l: 16 independent loads in flight per output
-  constexpr int U = 16;
-  for (int e = tid; e < G * D; e += nthreads) {
-    const int g = e / D, d = e % D;
-    const float* src = parts + g * PS + 4 + d;
-    float osum = 0.f;
-    for (int i0 = 0; i0 < nparts; i0 += U) {
-      float v[U];
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mold = s_M[g], mnew = fmaxf(mold, mx);
+      const float sc = (mnew == -INFINITY || mold == mnew) ? 1.f : exp2f(mold - mnew);
+      float lsum = 0.f;
+      for (int i = lane; i < nb; i += 32) {
+        const float mi = stage[(i * G + g) * PS];
+        const float w = mnew == -INFINITY ? 0.f : exp2f(mi - mnew);
+        s_w[i * G + g] = w;
+        lsum += w * stage[(i * G + g) * PS + 1];
+      }
 #pragma unroll
-      for (int k = 0; k < U; ++k) v[k] = (i0 + k < nparts) ? __ldcg(src + (size_t)(i0 + k) * G * PS) : 0.f;
-#pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (i0 + k < nparts) osum += s_m[(i0 + k) * G + g] * v[k];
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      __syncwarp();
+      if (lane == 0) { s_M[g] = mnew; s_L[g] = s_L[g] * sc + lsum; s_scale[g] = sc; }
     }
-    const float lsum = s_lt[g];
-    out[g * D + d] = lsum > 0.f ? osum / lsum : 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = tid + k * nthreads;
+      if (e < G * D) {
+        const int g = e / D, d = e % D;
+        float o = acc[k] * s_scale[g];
+        for (int i = 0; i < nb; ++i) o += s_w[i * G + g] * stage[(i * G + g) * PS + 4 + d];
+        acc[k] = o;
+      }
+    }
   }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int e = tid + k * nthreads;
+    if (e < G * D) {
+      const float l = s_L[e / D];
+      out[e] = l > 0.f ? acc[k] / l : 0.f;
+    }
+  }
+  return ok;
 }
 
 template <int D, int BITS, int G>
-__global__ void __launch_bounds__(DecodeCfg<D, BITS, G>::WARPS * 32)
+__global__ void __launch_bounds__(DecodeCfg<D, BITS, G>::WARPS * 32, DecodeCfg<D, BITS, G>::MIN_CTAS)
 decode_kernel(const DecodeParams p) {
   using C = DecodeCfg<D, BITS, G>;
+  constexpr int NTILES = C::NT;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
   uint8_t* ring = smem;
@@ -582,11 +633,24 @@ decode_kernel(const DecodeParams p) {
   uint32_t* orow = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS + C::ZERO);
   int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS + C::ZERO + C::ONES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* q_smem = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS + C::ZERO + C::ONES + C::PREFIX);
+  uint64_t* bars_all =
+      reinterpret_cast<uint64_t*>(smem + C::RING + C::PS + C::ZERO + C::ONES + C::PREFIX + C::QS);
+  uint64_t* bars = bars_all + warp * C::NSTAGE;
+  uint64_t* merge_bar = bars_all + C::WARPS * C::NSTAGE;
   __half* ps = ps_all + warp * G * C::PSROW;
   uint8_t* wring = ring + warp * C::NSTAGE * C::STAGE;
 
   for (int i = threadIdx.x; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
   if (threadIdx.x < C::ONES / 4) orow[threadIdx.x] = 0x3C003C00u;
+  if (lane == 0) {
+    for (int st = 0; st < C::NSTAGE; ++st) mbar_init(bars + st, 1);
+    if (warp == 0) mbar_init(merge_bar, 1);
+    mbar_fence_init();
+  }
+  uint32_t parity = 0;  // bit st: parity of the next phase of stage st's mbarrier
+  uint32_t merge_parity = 0;
+  bool failed = false;  // a bounded wait gave up: stop using staged data
   build_prefix(p, s_pref);
   __syncthreads();
   const int64_t total = (int64_t)p.hkv * s_pref[p.batch];
@@ -616,50 +680,60 @@ decode_kernel(const DecodeParams p) {
     const int per = (n + C::WARPS - 1) / C::WARPS;
     const int ia = i0 + min(n, warp * per), ie = i0 + min(n, (warp + 1) * per);
     Decoder<D, BITS, G> dec;
-    dec.init(p, b, h);
     {
-      const int ga = ia, cnt = max(0, min(ie, ng) - ia);
-      const size_t gbase = (size_t)seg * p.max_groups + ga;
-      // this lane's first 16 bytes of each array for group ga; group idx adds idx * size
-      const uint8_t* kc0 = p.k_codes + gbase * C::TB + lane * 16;
-      const uint8_t* vc0 = p.v_codes + gbase * C::TB + lane * 16;
-      const uint8_t* km0 = reinterpret_cast<const uint8_t*>(p.k_meta) + gbase * C::KMETA + lane * 16;
-      const uint8_t* vm0 = reinterpret_cast<const uint8_t*>(p.v_meta) + gbase * C::VMETA + lane * 16;
-      uint8_t* dst0 = wring + lane * 16;
+      const int ga = ia, cnt = failed ? 0 : max(0, min(ie, ng) - ia);
+      const size_t g0 = (size_t)seg * p.max_groups + ga;
+      // one lane issues four bulk copies per group, completing on the stage's mbarrier
       auto issue = [&](int idx, int slotn) {
-        uint8_t* dst = dst0 + slotn * C::STAGE;
-        const uint8_t* kc = kc0 + (size_t)idx * C::TB;
-        const uint8_t* vc = vc0 + (size_t)idx * C::TB;
-        const uint8_t* km = km0 + (size_t)idx * C::KMETA;
-        const uint8_t* vm = vm0 + (size_t)idx * C::VMETA;
-#pragma unroll
-        for (int o = 0; o < C::TB; o += 512) cp_async_16(dst + o, kc + o);
-#pragma unroll
-        for (int o = 0; o < C::TB; o += 512) cp_async_16(dst + C::TB + o, vc + o);
-#pragma unroll
-        for (int o = 0; o < C::KMETA; o += 512)
-          if (o + lane * 16 < C::KMETA) cp_async_16(dst + 2 * C::TB + o, km + o);
-#pragma unroll
-        for (int o = 0; o < C::VMETA; o += 512)
-          if (o + lane * 16 < C::VMETA) cp_async_16(dst + 2 * C::TB + C::KMETA + o, vm + o);
+        if (lane == 0) {
+          const size_t g = g0 + idx;
+          uint8_t* dst = wring + slotn * C::STAGE;
+          fence_proxy_async();
+          mbar_arrive_expect_tx(bars + slotn, C::STAGE);
+          tma_load_1d(dst, p.k_codes + g * C::TB, C::TB, bars + slotn);
+          tma_load_1d(dst + C::TB, p.v_codes + g * C::TB, C::TB, bars + slotn);
+          tma_load_1d(dst + 2 * C::TB, reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA, C::KMETA,
+                      bars + slotn);
+          tma_load_1d(dst + 2 * C::TB + C::KMETA, reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA,
+                      C::VMETA, bars + slotn);
+        }
       };
+      // start the first copies, then stage this segment's q (lane order) while they fly
+      int issued = 0, waited = 0;
 #pragma unroll
-      for (int s = 0; s < C::NSTAGE - 1; ++s) {
-        if (s < cnt) issue(s, s);
-        cp_async_commit();
+      for (int st = 0; st < C::NSTAGE - 1; ++st)
+        if (st < cnt) { issue(st, st); ++issued; }
+      {
+        const __half* qh = p.q + ((size_t)b * p.hkv + h) * G * D;
+        for (int e = threadIdx.x; e < NTILES * 4 * (D / 2); e += blockDim.x) {
+          const int g = e / (D / 2), pr = e % (D / 2);
+          const int kt = 2 * (pr / 16) + (pr % 4) / 2, tg = (pr % 16) / 4, r = pr % 2;
+          const int c = 16 * kt + 2 * tg + 8 * r;
+          q_smem[e] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * D + c) : 0u;
+        }
       }
+      __syncthreads();
+      dec.init(q_smem);
       for (int i = 0; i < cnt; ++i) {
-        if (i + C::NSTAGE - 1 < cnt) issue(i + C::NSTAGE - 1, (i + C::NSTAGE - 1) % C::NSTAGE);
-        cp_async_commit();
-        cp_async_wait<C::NSTAGE - 1>();
-        __syncwarp();
-        dec.quant_group(wring + (i % C::NSTAGE) * C::STAGE, ps, zrow, orow, p.scale_log2);
+        if (i + C::NSTAGE - 1 < cnt) { issue(i + C::NSTAGE - 1, (i + C::NSTAGE - 1) % C::NSTAGE); ++issued; }
+        const int slotn = i % C::NSTAGE;
+        const bool ok = mbar_wait(bars + slotn, (parity >> slotn) & 1u, kMaxPolls);
+        parity ^= 1u << slotn;
+        ++waited;
+        if (!ok) { failed = true; break; }
+        dec.quant_group(wring + slotn * C::STAGE, ps, zrow, orow, p.scale_log2);
       }
-      cp_async_wait<0>();
+      // after a timeout, wait (bounded) for this warp's copies still in flight
+      for (; waited < issued; ++waited) {
+        const int slotn = waited % C::NSTAGE;
+        mbar_wait(bars + slotn, (parity >> slotn) & 1u, kMaxPolls);
+        parity ^= 1u << slotn;
+      }
       __syncwarp();
     }
+    if (failed && lane == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
     // tail chunks whose first weighted item falls in this warp's range
-    for (int t = max(ia, ng); t < ie; ++t) {
+    for (int t = max(ia, ng); t < (failed ? 0 : ie); ++t) {
       const int u = t - ng;
       if (u % kTailWeight != 0) continue;
       const int first = (u / kTailWeight) * kGroup;
@@ -698,10 +772,11 @@ decode_kernel(const DecodeParams p) {
     __syncthreads();
     if (s_last) {
       __threadfence();
-      // the stage ring is idle here: its first bytes hold the merge weights
-      final_merge<D, G>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
-                        p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D,
-                        reinterpret_cast<float*>(ring));
+      // the stage ring is idle here; the p~ area holds the merge weights
+      const bool ok = final_merge<D, BITS, G>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
+                                               p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D, ring,
+                                               reinterpret_cast<float*>(ps_all), merge_bar, merge_parity);
+      if (!ok && threadIdx.x == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
       if (threadIdx.x == 0) p.counters[seg] = 0;
     }
     __syncthreads();
@@ -742,8 +817,6 @@ struct DecodeLaunch {
         return 0;
       }
       cached = sms * per;
-      // the final merge keeps two floats per (partial, head) in the stage ring
-      if (cached > C::RING / (8 * G) - 1) cached = C::RING / (8 * G) - 1;
     }
     return cached;
   }
@@ -817,7 +890,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, con
   s = validate_q_heads(c, n_q_heads, &G);
   if (s != KVQ_OK) return s;
   if (q == nullptr || out == nullptr || workspace == nullptr) return KVQ_ERR_INVALID;
-  if (!aligned(q, 4) || !aligned(out, 4) || !aligned(workspace, 16)) return KVQ_ERR_INVALID;
+  if (!aligned(q, 4) || !aligned(out, 16) || !aligned(workspace, 16)) return KVQ_ERR_INVALID;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID;
   int err = 0;
   const int n = decode_slots(c, G, &err);

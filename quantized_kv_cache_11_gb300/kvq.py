@@ -24,6 +24,7 @@ KVQ_ERR_CAPACITY = -3
 KVQ_ERR_CUDA = -4
 KVQ_DEVERR_APPEND_CAPACITY = 1
 KVQ_DEVERR_BAD_LENGTHS = 2
+KVQ_DEVERR_TIMEOUT = 4
 KVQ_GROUP = 32
 KVQ_MAX_BATCH = 512
 KVQ_NBUF = 7

@@ -103,6 +103,7 @@ def test_decode_and_append_validation_fails_before_launch(lib):
     assert dec(d, hq=6) == kvq.KVQ_ERR_INVALID
     assert dec(d, hq=48) == kvq.KVQ_ERR_UNSUPPORTED  # G = 12
     assert dec(d, q=0) == kvq.KVQ_ERR_INVALID
+    assert dec(d, out=0x300004) == kvq.KVQ_ERR_INVALID  # out must be 16-byte aligned
     assert dec(d, w=0) == kvq.KVQ_ERR_INVALID
     assert dec(d, scale=0.0) == kvq.KVQ_ERR_INVALID
     assert dec(d, scale=float("nan")) == kvq.KVQ_ERR_INVALID
