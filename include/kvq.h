@@ -229,6 +229,36 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int32_t n_q_heads, const void
                            float* out, float sm_scale, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* Size of the fixed scratch array behind kvq_decode_attn_static (4 MiB). */
+#define KVQ_STATIC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * kvq_decode_attn_static -- kvq_decode_attn without a workspace argument, for
+ * callers that cannot allocate device memory: an engine whose allocator has
+ * already reserved all device memory for its own pool, a host program that
+ * reaches the GPU only through this C ABI and has no device allocator, or a
+ * decode loop that must not call cudaMalloc because that call can synchronize
+ * the whole device.  There is no counterpart in the pages: this is an interface
+ * convenience, and it computes exactly what kvq_decode_attn computes.
+ *
+ * The split-K partials and merge counters live in one array of
+ * KVQ_STATIC_SCRATCH_BYTES compiled into the library; every GPU that loads the
+ * library keeps it until the process exits.  Nothing is allocated: the call
+ * clears the counters with a memset on `stream` and launches the decode.
+ *   Arguments, layout and results are those of kvq_decode_attn.
+ *   Returns KVQ_ERR_CAPACITY when the geometry needs more scratch than the
+ *   array holds (the need is the kvq_decode_workspace_bytes value), before any
+ *   work is enqueued.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents: calls that can overlap on the GPU (different streams, or
+ * different host threads without ordering) race and corrupt each other's
+ * results, so issue them in order on one stream.
+ */
+kvq_status kvq_decode_attn_static(const kvq_cache* cache, int32_t n_q_heads, const void* q,
+                                  float* out, float sm_scale, void* stream);
+
 /* Human-readable name of a status code.  Never NULL. */
 const char* kvq_status_string(int status);
 

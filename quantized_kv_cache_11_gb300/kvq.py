@@ -33,8 +33,9 @@ KVQ_NBUF = 7
 
 # Every entry point of include/kvq.h.
 EXPORTS = ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
-           "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_status_string",
-           "kvq_version")
+           "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
+           "kvq_status_string", "kvq_version")
+KVQ_STATIC_SCRATCH_BYTES = 4 << 20
 
 
 class kvq_cache(ctypes.Structure):
@@ -88,12 +89,13 @@ def load_library() -> ctypes.CDLL:
     lib.kvq_append_token.argtypes = [cache_p, c_vp, c_vp, c_vp]
     lib.kvq_decode_workspace_bytes.argtypes = [cache_p, ctypes.c_int32, P(c_sz)]
     lib.kvq_decode_attn.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_sz, c_vp]
+    lib.kvq_decode_attn_static.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp]
     lib.kvq_status_string.argtypes = [c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     lib.kvq_version.argtypes = []
     lib.kvq_version.restype = ctypes.c_char_p
     for name in ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
-                 "kvq_decode_workspace_bytes", "kvq_decode_attn"):
+                 "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -179,6 +181,19 @@ def kvq_decode_attn(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.Tenso
                                         float(sm_scale), _ptr(workspace), workspace.numel(),
                                         _stream(stream))
     _check("kvq_decode_attn", st)
+
+
+def kvq_decode_attn_static(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.Tensor,
+                           sm_scale: float, stream=None) -> None:
+    """kvq_decode_attn without a workspace: the library's fixed device array holds
+    the scratch (see include/kvq.h).  Calls on one device must not overlap."""
+    _need(q, torch.float16, "q")
+    _need(out, torch.float32, "out")
+    if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    st = load_library().kvq_decode_attn_static(ctypes.byref(cache.desc), q.shape[1], _ptr(q),
+                                               _ptr(out), float(sm_scale), _stream(stream))
+    _check("kvq_decode_attn_static", st)
 
 
 class QuantizedKVCache:
