@@ -350,12 +350,17 @@ def main():
     nbytes = algorithmic_bytes(w, n_quant, n_tail)
     achieved = nbytes / (us_step * 1e-6) / 1e9
     traffic = None
-    tf = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    tf = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     if os.path.exists(tf):
+        rec = {}
         with open(tf) as f:
-            rec = json.load(f)
+            for ln in f:
+                if ":" in ln and not ln.lstrip().startswith("#"):
+                    k, v = ln.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        # only while the kernel source is the one the counters were taken from
         if rec.get("workload") == w.name and rec.get("kernel_source_sha") == _kernel_sha():
-            traffic = rec.get("dram_bytes_per_launch")
+            traffic = int(rec["dram_bytes_per_launch"])
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
