@@ -238,7 +238,7 @@ def append_lengths(n_quant: int, n_tail: int, tail_cap: int):
 #                        = (x[j][t], x[j][t + 1]) for channel group j and token
 #                        t = 16*kt + 2*tig + 8*r of the tile
 # ---------------------------------------------------------------------------
-SLOT_BITPOS = {2: (2, 6, 0, 4, 10, 14, 8, 12), 4: (0, 4, 8, 12), 8: (0, 8)}
+SLOT_BITPOS = {2: (2, 6, 0, 4, 10, 14, 8, 12), 4: (0, 4, 8, 12), 8: (0, 8), 16: (0,)}
 
 
 @functools.lru_cache(maxsize=None)
@@ -303,12 +303,13 @@ def pack_tiles(codes: np.ndarray, kind: str, bits: int) -> np.ndarray:
 
 
 def unpack_tiles(packed: np.ndarray, kind: str, d: int, bits: int) -> np.ndarray:
-    """Inverse of pack_tiles: packed uint8 [..., 32*D*b/8] -> codes uint8 [..., 32, D]."""
+    """Inverse of pack_tiles: packed uint8 [..., 32*D*b/8] -> codes uint8 [..., 32, D]
+    (uint16 for 16-bit fields)."""
     *lead, nb = packed.shape
     words = np.ascontiguousarray(packed).view("<u4").astype(np.uint32)
     word, bit = tile_code_positions(kind, d, bits)
     vals = (words[..., word] >> bit.astype(np.uint32)) & np.uint32(2 ** bits - 1)
-    return vals.astype(np.uint8)
+    return vals.astype(np.uint16 if bits == 16 else np.uint8)
 
 
 @functools.lru_cache(maxsize=None)
@@ -451,3 +452,200 @@ def trizone_attention(q16: np.ndarray, tz_heads: list, sm_scale: float) -> np.nd
         sl = slice(kh * group, (kh + 1) * group)
         out[sl] = decode_attention(q16[sl], keys[None], values[None], sm_scale)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Packed byte layout of the mixed-width cache (the library's own; the pages
+# describe the zones, not their bytes):
+#
+# Channels of a (sequence, KV head) are permuted by K width class: the 2-bit
+# channels in ascending order, then 4-bit, then 8-bit; each class is padded to
+# whole 16-channel k-tiles with "pad" slots (code 0, scale 0, zero 0).
+#
+# One 32-token block (tokens of one V-width class, in stream order) is one
+# contiguous record:
+#   K codes: for each K class c (2, 4, 8) with kt_c k-tiles: 32 tokens x 16*kt_c
+#     channels at c bits; lane L (gid = L//4, tig = L%4) owns the pairs
+#     (kt < kt_c, mt < 2, i < 4): token 16mt + gid + 8(i%2), class channels
+#     16kt + 2tig + 8(i//2) and +1; pair P -> word P // (16/c), slot P % (16/c)
+#     at bit SLOT_BITPOS[c][slot] (+16 for the second code); lane word w at byte
+#     (w*32 + L)*4 of the sub-tile (64 * kt_c * c bytes).
+#   K metadata: scale plane then zero plane, 16 * KT halves each (KT = sum kt_c,
+#     k-tiles of all classes in order); pair (kt, tig, r) at kt*8 + tig*2 + r holds
+#     permuted slots 16kt + 2tig + 8r and +1.
+#   V: width 2/4/8: the uniform value tile at that width (pack_tiles "V") and its
+#     metadata block (pack_value_meta); width 16: the fp16 values as a 16-bit value
+#     tile (pack_tiles "V" with 16-bit fields: word = half2 of tokens t, t + 1 of
+#     one channel), the A fragments of P.V as they are.
+#   Tokens past the block's count are zero everywhere.
+# Fresh tokens form "fresh blocks" of up to 32 tokens: the fp16 keys as a 16-bit
+# key tile (natural channel order; word = half2 of channels c, c + 1 of one token,
+# the A fragments of Q.K^T) followed by the fp16 values as a 16-bit value tile.
+# A (sequence, KV head) stores its blocks class by class (V width 2, 4, 8, 16),
+# then its fresh blocks; all blocks of one kind have the same size.
+#
+# Index record of a (sequence, KV head), 512 bytes: int32 fields
+#   [0:4] kept tokens per V width (2, 4, 8, 16), [4] fresh tokens,
+#   [5:9] blocks per V width, [9] fresh blocks, [10:13] channels per K width
+#   (2, 4, 8), [13:16] k-tiles per K width, [16:21] bytes of one block of each
+#   kind (widths 2, 4, 8, 16, fresh), [21:26] byte offset of each kind's first
+#   block, [26] total bytes, [27:32] zero;
+# then int16 [160] permuted channel slots (-1 = pad, and past the last k-tile),
+# then 64 zero bytes.
+# ---------------------------------------------------------------------------
+TRIZONE_KT_MAX = 10  # sum of ceil(n_c / 16) over three classes of 128 channels
+
+
+def trizone_channel_order(k_width: np.ndarray):
+    """Permuted channel slots (original channel, or -1 for a pad slot) and the
+    k-tiles per K class."""
+    slots, kts = [], []
+    for c in TRIZONE_K_WIDTHS:
+        ch = [int(d) for d in np.nonzero(k_width == c)[0]]
+        kt = (len(ch) + 15) // 16
+        slots += ch + [-1] * (16 * kt - len(ch))
+        kts.append(kt)
+    return np.asarray(slots, dtype=np.int64), tuple(kts)
+
+
+@functools.lru_cache(maxsize=None)
+def trizone_ksub_positions(kt: int, c: int):
+    """(word, bit) of every code of a K sub-tile [32 tokens, 16*kt channels]."""
+    per_word = 16 // c
+    n = 16 * kt
+    word = np.full((GROUP, n), -1, dtype=np.int64)
+    bit = np.full((GROUP, n), -1, dtype=np.int64)
+    for lane in range(32):
+        gid, tig = lane // 4, lane % 4
+        p = 0
+        for k in range(kt):
+            for mt in range(2):
+                for i in range(4):
+                    t = 16 * mt + gid + 8 * (i % 2)
+                    ch = 16 * k + 2 * tig + 8 * (i // 2)
+                    w, s = p // per_word, p % per_word
+                    pos = SLOT_BITPOS[c][s]
+                    for cc, off in ((ch, pos), (ch + 1, 16 + pos)):
+                        assert word[t, cc] == -1
+                        word[t, cc] = w * 32 + lane
+                        bit[t, cc] = off
+                    p += 1
+    assert (word >= 0).all()
+    word.setflags(write=False)
+    bit.setflags(write=False)
+    return word, bit
+
+
+def _pack_words(codes: np.ndarray, word: np.ndarray, bit: np.ndarray, n_words: int) -> np.ndarray:
+    out = np.zeros(n_words, dtype=np.uint64)
+    np.add.at(out, word.ravel(), codes.ravel().astype(np.uint64) << bit.ravel().astype(np.uint64))
+    return out.astype("<u4").view(np.uint8)
+
+
+TRIZONE_FRESH_BLOCK = 2 * GROUP * 128 * 2  # fp16 key tile + fp16 value tile, D = 128
+TRIZONE_INDEX_BYTES = 512
+
+
+def trizone_block_bytes(kts, width: int, d: int = 128) -> int:
+    kb = sum(64 * kt * c for kt, c in zip(kts, TRIZONE_K_WIDTHS)) + 64 * sum(kts)
+    vb = GROUP * d * 2 if width == 16 else GROUP * d * width // 8 + 4 * d
+    return kb + vb
+
+
+def _fp16_tile(rows16: np.ndarray, kind: str, d: int) -> np.ndarray:
+    """fp16 rows [n <= 32, D] -> 16-bit tile bytes (rows past n are zero)."""
+    bits = np.zeros((GROUP, d), np.uint16)
+    bits[:len(rows16)] = np.asarray(rows16, F16).view(np.uint16)
+    return pack_tiles(bits, kind, 16)
+
+
+def trizone_pack_block(blk: dict, slots: np.ndarray, kts, d: int = 128) -> np.ndarray:
+    """Bytes of one block record (trizone_quantize block -> uint8 array)."""
+    n = len(blk["tokens"])
+    parts = []
+    # K codes per class, channels permuted, tokens padded to 32
+    codes = np.zeros((GROUP, len(slots)), dtype=np.uint8)
+    valid = slots >= 0
+    codes[:n, valid] = blk["k_codes"][:, slots[valid]]
+    base = 0
+    for kt, c in zip(kts, TRIZONE_K_WIDTHS):
+        if kt:
+            word, bit = trizone_ksub_positions(kt, c)
+            parts.append(_pack_words(codes[:, base:base + 16 * kt], word, bit, 16 * kt * c))
+        base += 16 * kt
+    # K metadata, lane order over all k-tiles
+    kt_all = sum(kts)
+    sc = np.zeros(16 * kt_all, np.float16)
+    ze = np.zeros(16 * kt_all, np.float16)
+    sc[valid] = blk["k_scale"][slots[valid]]
+    ze[valid] = blk["k_zero"][slots[valid]]
+    order = np.empty(16 * kt_all, dtype=np.int64)
+    for kt in range(kt_all):
+        for tig in range(4):
+            for r in range(2):
+                pr = kt * 8 + tig * 2 + r
+                s = 16 * kt + 2 * tig + 8 * r
+                order[2 * pr], order[2 * pr + 1] = s, s + 1
+    parts.append(np.stack([sc[order], ze[order]]).view(np.uint8).ravel())
+    # V
+    w = blk["width"]
+    if w == 16:
+        parts.append(_fp16_tile(blk["v_fp16"], "V", d))
+    else:
+        vc = np.zeros((GROUP, d), np.uint8)
+        vc[:n] = blk["v_codes"]
+        vs = np.zeros((GROUP, d // GROUP), np.float16)
+        vz = np.zeros((GROUP, d // GROUP), np.float16)
+        vs[:n], vz[:n] = blk["v_scale"], blk["v_zero"]
+        parts.append(pack_tiles(vc, "V", w))
+        parts.append(pack_value_meta(vs, vz).view(np.uint8).ravel())
+    out = np.concatenate(parts)
+    assert out.size == trizone_block_bytes(kts, w, d)
+    return out
+
+
+def trizone_pack_fresh(k16: np.ndarray, v16: np.ndarray, d: int = 128) -> list:
+    """Fresh tokens -> fresh block records (32 tokens each, the last partial)."""
+    out = []
+    for i in range(0, len(k16), GROUP):
+        out.append(np.concatenate([_fp16_tile(k16[i:i + GROUP], "K", d),
+                                   _fp16_tile(v16[i:i + GROUP], "V", d)]))
+    return out
+
+
+def trizone_pack(tz: dict, d: int = 128) -> dict:
+    """The packed form of one (sequence, KV head): index record, stream order of
+    the kept tokens, and the block bytes back to back."""
+    slots, kts = trizone_channel_order(tz["k_width"])
+    n_tok = [0, 0, 0, 0]
+    n_blk = [0, 0, 0, 0]
+    recs, order = [], []
+    for blk in tz["blocks"]:
+        ci = TRIZONE_V_WIDTHS.index(blk["width"])
+        n_tok[ci] += len(blk["tokens"])
+        n_blk[ci] += 1
+        recs.append(trizone_pack_block(blk, slots, kts, d))
+        order.append(blk["tokens"])
+    fresh = trizone_pack_fresh(tz["fresh_k"], tz["fresh_v"], d)
+    recs += fresh
+    rec_bytes = [trizone_block_bytes(kts, w, d) for w in TRIZONE_V_WIDTHS] + [TRIZONE_FRESH_BLOCK]
+    counts = n_blk + [len(fresh)]
+    offs = np.concatenate([[0], np.cumsum(np.multiply(counts, rec_bytes))]).tolist()
+    hdr = np.zeros(32, np.int32)
+    hdr[0:4] = n_tok
+    hdr[4] = len(tz["fresh_k"])
+    hdr[5:10] = counts
+    hdr[10:13] = [int((tz["k_width"] == c).sum()) for c in TRIZONE_K_WIDTHS]
+    hdr[13:16] = kts
+    hdr[16:21] = rec_bytes
+    hdr[21:26] = offs[:5]
+    hdr[26] = offs[5]
+    sl = np.full(160, -1, np.int16)
+    sl[:len(slots)] = slots
+    index = np.concatenate([hdr.view(np.uint8), sl.view(np.uint8), np.zeros(64, np.uint8)])
+    assert index.size == TRIZONE_INDEX_BYTES
+    data = np.concatenate(recs) if recs else np.zeros(0, np.uint8)
+    assert data.size == offs[5]
+    tokens = np.concatenate(order) if order else np.zeros(0, np.int64)
+    return {"index": index, "tokens": tokens.astype(np.int32), "data": data,
+            "slots": slots, "kts": kts, "header": hdr}

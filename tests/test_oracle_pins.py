@@ -448,3 +448,144 @@ def test_trizone_matches_uniform_when_widths_are_uniform():
     a = O.trizone_attention(inp["q"][0], [tz], w.sm_scale)
     b = O.sequence_attention(inp["q"][0], st, w.sm_scale)
     np.testing.assert_allclose(a, b, atol=1e-13)
+
+
+# ------------------------------------------------------- mixed-width layout
+def test_trizone_channel_order_by_hand():
+    # channels 1 and 3 at 2 bits, channel 0 at 8 bits, the other 125 at 4 bits:
+    # class 2 -> [1, 3] + 14 pads; class 4 -> 2, 4, 5, ..., 127 + 3 pads; class 8 -> [0] + 15 pads
+    kw = np.full(128, 4, np.uint8)
+    kw[[1, 3]] = 2
+    kw[0] = 8
+    slots, kts = O.trizone_channel_order(kw)
+    assert kts == (1, 8, 1)
+    assert slots[:2].tolist() == [1, 3] and (slots[2:16] == -1).all()
+    assert slots[16:19].tolist() == [2, 4, 5] and slots[140] == 127 and (slots[141:144] == -1).all()
+    assert slots[144] == 0 and (slots[145:160] == -1).all()
+    assert len(slots) == 160
+
+
+# (kt, bits) -> {(token, class channel): (lane word index w*32 + lane, bit)}, derived by
+# hand from the fragment layout: lane 4 gid + tig; pair P = 8 kt + 4 mt + i covers
+# token 16 mt + gid + 8 (i % 2), channels 16 kt + 2 tig + 8 (i // 2) and +1.
+KSUB_POS = {
+    (1, 2): {(0, 0): (0, 2), (0, 1): (0, 18), (8, 0): (0, 6), (0, 8): (0, 0), (8, 8): (0, 4),
+             (16, 0): (0, 10), (31, 15): (31, 28), (31, 14): (31, 12)},
+    (3, 4): {(25, 2): (37, 4), (25, 3): (37, 20), (0, 16): (64, 0), (31, 47): (191, 28)},
+    (2, 8): {(9, 1): (4, 24), (0, 0): (0, 0), (16, 16): (192, 0)},
+}
+
+
+@pytest.mark.parametrize("kt,bits", list(KSUB_POS))
+def test_trizone_key_subtile_positions_by_hand(kt, bits):
+    word, bit = O.trizone_ksub_positions(kt, bits)
+    for (t, c), pos in KSUB_POS[(kt, bits)].items():
+        assert (int(word[t, c]), int(bit[t, c])) == pos, (t, c)
+    assert len(set(zip((word * 32 + bit).ravel().tolist()))) == 32 * 16 * kt
+    assert word.max() + 1 == 16 * kt * bits
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_trizone_key_subtile_is_the_uniform_tile_word_interleaved(bits):
+    # with all 128 channels in one class the sub-tile holds the uniform key tile's
+    # lane words, word w of lane L at 4 (32 w + L) instead of 16 (32 (w // 4) + L) + 4 (w % 4)
+    rng = np.random.default_rng(bits)
+    codes = rng.integers(0, 2 ** bits, (32, 128), dtype=np.uint8)
+    uni = O.pack_tiles(codes[None], "K", bits).reshape(-1).view("<u4")
+    word, bit = O.trizone_ksub_positions(8, bits)
+    sub = O._pack_words(codes, word, bit, 16 * 8 * bits).view("<u4")
+    nw = 128 * bits // 32
+    for lane in range(32):
+        for w in range(nw):
+            assert sub[w * 32 + lane] == uni[(w // 4) * 32 * 4 + lane * 4 + w % 4]
+
+
+def test_trizone_block_bytes_closed_form():
+    # K: 64 kt c bytes per class + 64 per k-tile of metadata; V: codes + 512 B meta, or fp16 rows
+    assert O.trizone_block_bytes((5, 3, 1), 2) == 1920 + 576 + 1024 + 512
+    assert O.trizone_block_bytes((5, 3, 1), 4) == 1920 + 576 + 2048 + 512
+    assert O.trizone_block_bytes((5, 3, 1), 8) == 1920 + 576 + 4096 + 512
+    assert O.trizone_block_bytes((5, 3, 1), 16) == 1920 + 576 + 8192
+    assert O.trizone_block_bytes((0, 8, 0), 4) == O.tile_bytes(128, 4) * 2 + 1024
+
+
+def test_trizone_pack_block_fields():
+    # a partial block of 20 tokens: decode every field of the record independently
+    w, inp = _small_trizone(t_old=400, fresh=0, d=128, probs=(0, 1.0, 0, 0, 0))
+    k, v = inp["K"][0, :, 0], inp["V"][0, :, 0]
+    kw = np.array([2, 4, 8, 4] * 32, np.uint8)
+    tz = O.trizone_quantize(k[:20], v[:20], np.full(20, 2, np.uint8), kw)
+    blk = tz["blocks"][0]
+    slots, kts = O.trizone_channel_order(kw)
+    assert kts == (2, 4, 2)
+    rec = O.trizone_pack_block(blk, slots, kts)
+    off = 0
+    for kt, c in zip(kts, (2, 4, 8)):
+        word, bit = O.trizone_ksub_positions(kt, c)
+        sub = rec[off:off + 64 * kt * c].view("<u4")
+        got = (sub[word] >> bit.astype(np.uint32)) & (2 ** c - 1)
+        cls = slots[sum(16 * x for x in kts[:(2, 4, 8).index(c)]):][:16 * kt]
+        for j, ch in enumerate(cls):
+            assert (got[:20, j] == blk["k_codes"][:, ch]).all() and (got[20:, j] == 0).all()
+        off += 64 * kt * c
+    meta = rec[off:off + 64 * 8].view(np.float16).reshape(2, 128)
+    # pair (kt=1, tig=2, r=1) = index 13 holds slots 16 + 4 + 8 = 28 and 29
+    assert meta[0, 26].view(np.uint16) == blk["k_scale"][slots[28]].view(np.uint16)
+    assert meta[1, 27].view(np.uint16) == blk["k_zero"][slots[29]].view(np.uint16)
+    off += 512
+    vcodes = O.unpack_tiles(rec[off:off + 1024][None], "V", 128, 2)[0]
+    assert (vcodes[:20] == blk["v_codes"]).all() and (vcodes[20:] == 0).all()
+    off += 1024
+    vm = rec[off:].view(np.float16)
+    assert vm.size == 256 and (vm.view(np.uint16) != 0).sum() > 0
+    assert off + 512 == rec.size
+
+
+# 16-bit tiles: {(token, channel): (byte offset of the 32-bit word, bit)}, by hand from
+# the fragment layouts (word w of lane L at 16 (32 (w // 4) + L) + 4 (w % 4))
+FP16_POS = {
+    "V": {(0, 0): (0, 0), (1, 0): (0, 16), (2, 0): (16, 0), (8, 0): (8, 0), (0, 8): (4, 0),
+          (16, 0): (512, 0), (0, 16): (1024, 0), (0, 1): (64, 0)},
+    "K": {(0, 0): (0, 0), (0, 1): (0, 16), (8, 0): (4, 0), (0, 8): (8, 0), (16, 0): (512, 0),
+          (0, 16): (1024, 0), (1, 0): (64, 0)},
+}
+
+
+@pytest.mark.parametrize("kind", ["K", "V"])
+def test_fp16_tile_positions_by_hand(kind):
+    rows = np.zeros((32, 128), np.float16)
+    for n, (t, c) in enumerate(FP16_POS[kind]):
+        rows[t, c] = np.float16(n + 1)
+    tile = O._fp16_tile(rows, kind, 128)
+    words = tile.view("<u4")
+    for n, ((t, c), (byte, bit)) in enumerate(FP16_POS[kind].items()):
+        assert (words[byte // 4] >> bit) & 0xFFFF == np.float16(n + 1).view(np.uint16), (t, c)
+    assert (O.unpack_tiles(tile, kind, 128, 16) == rows.view(np.uint16)).all()
+
+
+def test_trizone_pack_index_and_stream():
+    w, inp = _small_trizone(t_old=700, fresh=40, d=128)
+    k, v = inp["K"][0, :, 0], inp["V"][0, :, 0]
+    vw, kw = inp["v_width"][0, 0], inp["k_width"][0, 0]
+    tz = O.trizone_quantize(k, v, vw, kw)
+    pk = O.trizone_pack(tz)
+    hdr = pk["index"][:128].view(np.int32)
+    n_tok = [int((vw == c).sum()) for c in (2, 4, 8, 16)]
+    assert hdr[0:4].tolist() == n_tok and hdr[4] == 40
+    assert hdr[5:9].tolist() == [(n + 31) // 32 for n in n_tok] and hdr[9] == 2
+    assert hdr[10:13].tolist() == [int((kw == c).sum()) for c in (2, 4, 8)]
+    assert hdr[13:16].tolist() == [(int((kw == c).sum()) + 15) // 16 for c in (2, 4, 8)]
+    assert hdr[20] == 16384 and hdr[21] == 0 and (hdr[27:] == 0).all()
+    assert all(hdr[21 + i + 1] == hdr[21 + i] + hdr[5 + i] * hdr[16 + i] for i in range(4))
+    assert hdr[26] == hdr[25] + 2 * 16384 == pk["data"].size
+    # stream order: kept tokens by width class, ascending positions inside a class
+    exp = np.concatenate([np.nonzero(vw == c)[0] for c in (2, 4, 8, 16)])
+    assert (pk["tokens"] == exp).all()
+    sl = pk["index"][128:448].view(np.int16)
+    assert sorted(sl[sl >= 0].tolist()) == list(range(128))
+    # the fresh blocks hold the fresh rows (the second one 8 rows, the rest zero)
+    fb = pk["data"][hdr[25] + 16384:]
+    kt = O.unpack_tiles(fb[:8192], "K", 128, 16)
+    assert (kt[:8] == k[732:740].view(np.uint16)).all() and (kt[8:] == 0).all()
+    vt = O.unpack_tiles(fb[8192:], "V", 128, 16)
+    assert (vt[:8] == v[732:740].view(np.uint16)).all() and (vt[8:] == 0).all()
