@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
+    ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone"],
+                    help="uniform: the 128k-token uniform cache (default); trizone: the "
+                         "mixed-width cache, 4 sequences x 65,408 old + 128 fresh tokens")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -168,6 +171,9 @@ def run_reference(args):
     from oracle import kvq_oracle as O
     from quantized_kv_cache_11_gb300 import synthetic as S
     import torch
+    if args.workload == "trizone":
+        run_reference_trizone(args)
+        return
     w = workload(args.bits)
     inp = S.generate(w)
     n = int(inp["seq_len"][0])
@@ -213,10 +219,119 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_trizone(args):
+    """The oracle on the host cores for the mixed-width cache: each step times
+    dequantize + fp64 attention of one (sequence, KV head) segment (several
+    segments rotate), scaled to all segments."""
+    from oracle import kvq_oracle as O
+    from quantized_kv_cache_11_gb300 import synthetic as S
+    import torch
+    w = S.TRIZONE
+    inp = S.generate(w)
+    tzs = [O.trizone_quantize(inp["K"][b, :, h], inp["V"][b, :, h], inp["v_width"][b, h],
+                              inp["k_width"][b, h]) for b, h in ((0, 0), (1, 3), (3, 7))]
+    times = []
+    for i in range(args.warmup + args.steps):
+        b, h = ((0, 0), (1, 3), (3, 7))[i % 3]
+        t0 = time.perf_counter()
+        O.trizone_attention(inp["q"][b][h * w.gqa:(h + 1) * w.gqa], [tzs[i % 3]], w.sm_scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    segs = w.batch * w.n_kv_heads
+    value = statistics.mean(times) * segs * 1e6
+    sample = f"oracle dequant + fp64 attention of 1 of {segs} segments per step, scaled x{segs}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1000.0,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name},
+        "cpu_baseline": {"kind": "oracle", "cores": torch.get_num_threads(), "sample": sample,
+                         "value": value, "unit": UNIT},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def time_graph(launch, n_rep, steps_wanted, world, local):
+    """Capture launch(i) for i < per_graph in a CUDA graph (rotating the n_rep
+    replicas), replay it until >= steps_wanted launches, and time the replays with
+    CUDA events on the current stream, sampling clocks meanwhile.  Returns
+    (us per launch, launches timed, clock summary); max over ranks."""
+    import torch
+    import torch.distributed as dist
+    per_graph = n_rep * max(1, 256 // n_rep)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(per_graph):
+            launch(i)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, math.ceil(steps_wanted / per_graph))
+    steps = reps * per_graph
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=torch.device("cuda", local))
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return elapsed_ms * 1000.0 / steps, steps, clk.summary()
+
+
+def time_e2e(launch, q_host, q_dev, out_host, outs, n_rep, n):
+    """Public-API loop: pinned host q -> device, decode, fp32 output -> pinned host,
+    every step inside the timed region.  Returns us per step."""
+    import torch
+    for i in range(16):
+        q_dev.copy_(q_host, non_blocking=True)
+        launch(i, q_dev)
+        out_host.copy_(outs[i % n_rep], non_blocking=True)
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record()
+    for i in range(n):
+        q_dev.copy_(q_host, non_blocking=True)
+        launch(i, q_dev)
+        out_host.copy_(outs[i % n_rep], non_blocking=True)
+    x1.record()
+    torch.cuda.synchronize()
+    return x0.elapsed_time(x1) * 1000.0 / n
+
+
+def read_traffic(name, workload_name, sha):
+    """Per-launch DRAM bytes from a committed ncu summary, while the kernel source
+    is the one the counters were taken from (else None)."""
+    tf = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(tf):
+        return None
+    rec = {}
+    with open(tf) as f:
+        for ln in f:
+            if ":" in ln and not ln.lstrip().startswith("#"):
+                k, v = ln.split(":", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("workload") == workload_name and rec.get("kernel_source_sha") == sha:
+        return int(rec["dram_bytes_per_launch"])
+    return None
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload == "trizone":
+        main_trizone(args)
         return
     import torch
     import torch.distributed as dist
@@ -293,54 +408,16 @@ def main():
         ref = O.sequence_attention(inp["q"][0][:w.gqa], st, w.sm_scale)
         got = outs[0][0, :w.gqa].double().cpu().numpy()
         parity = {"kv_heads_checked": 1, "max_abs": float(np.abs(got - ref).max())}
-    per_graph = n_rep * max(1, 256 // n_rep)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for i in range(per_graph):
-            caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep])
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    reps = max(1, math.ceil(args.steps / per_graph))
-    steps = reps * per_graph
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        e0.record()
-        for _ in range(reps):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    us_step = elapsed_ms * 1000.0 / steps
+    us_step, steps, clocks = time_graph(
+        lambda i: caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep]),
+        n_rep, args.steps, world, local)
 
     # ---- end to end through the public API: pinned host q in, fp32 output out
     q_host = torch.from_numpy(inp["q"]).pin_memory()
     out_host = torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(q)
-    n_e2e = min(steps, 4000)
-    for i in range(16):
-        q_dev.copy_(q_host, non_blocking=True)
-        caches[i % n_rep].decode(q_dev, w.sm_scale, out=outs[i % n_rep])
-        out_host.copy_(outs[i % n_rep], non_blocking=True)
-    torch.cuda.synchronize()
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    x0.record()
-    for i in range(n_e2e):
-        q_dev.copy_(q_host, non_blocking=True)
-        caches[i % n_rep].decode(q_dev, w.sm_scale, out=outs[i % n_rep])
-        out_host.copy_(outs[i % n_rep], non_blocking=True)
-    x1.record()
-    torch.cuda.synchronize()
-    e2e_us = x0.elapsed_time(x1) * 1000.0 / n_e2e
+    e2e_us = time_e2e(lambda i, qd: caches[i % n_rep].decode(qd, w.sm_scale, out=outs[i % n_rep]),
+                      q_host, q_dev, out_host, outs, n_rep, min(steps, 4000))
 
     if rank != 0:
         if world > 1:
@@ -349,19 +426,7 @@ def main():
     peak, peak_kind = load_peaks()
     nbytes = algorithmic_bytes(w, n_quant, n_tail)
     achieved = nbytes / (us_step * 1e-6) / 1e9
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "decode_traffic.txt")
-    if os.path.exists(tf):
-        rec = {}
-        with open(tf) as f:
-            for ln in f:
-                if ":" in ln and not ln.lstrip().startswith("#"):
-                    k, v = ln.split(":", 1)
-                    rec[k.strip()] = v.strip()
-        # only while the kernel source is the one the counters were taken from
-        if rec.get("workload") == w.name and rec.get("kernel_source_sha") == _kernel_sha():
-            traffic = int(rec["dram_bytes_per_launch"])
-    clocks = clk.summary()
+    traffic = read_traffic("decode_traffic.txt", w.name, _kernel_sha())
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
@@ -390,10 +455,168 @@ def main():
         dist.destroy_process_group()
 
 
-def _kernel_sha() -> str:
+TZ_FILES = ("kvq_trizone_decode.cu", "kvq_trizone_internal.h", "kvq_common.cuh")
+
+
+def trizone_bytes(w, v_width, k_width, n_fresh) -> dict:
+    """Bytes one decode step of the mixed-width cache must move, from the drawn
+    widths (the pages' layout, no padding): per kept old token the key codes at
+    each channel's width and the value codes at the token's width (+ an fp16
+    scale and zero per 32 channels) or its fp16 row; per 32-token block an fp16
+    scale and zero per channel; the fp16 fresh rows; q in, fp32 out."""
+    D = w.head_dim
+    k_bits = np.zeros(v_width.shape[:2])
+    for c in (2, 4, 8):
+        k_bits += (k_width == c).sum(-1) * c
+    total = 0
+    kept_total = 0
+    for b in range(v_width.shape[0]):
+        for h in range(v_width.shape[1]):
+            n = {c: int((v_width[b, h] == c).sum()) for c in (2, 4, 8, 16)}
+            kept = sum(n.values())
+            blocks = sum(-(-x // 32) for x in n.values())
+            total += kept * int(k_bits[b, h]) // 8 + blocks * D * 4
+            total += sum(n[c] * (D * c // 8 + (D // 32) * 4) for c in (2, 4, 8)) + n[16] * D * 2
+            total += n_fresh * D * 4
+            kept_total += kept
+    total += w.batch * w.n_q_heads * D * (2 + 4)
+    return {"decode": total, "kept": kept_total}
+
+
+def trizone_cpu_baseline(w, inp, budget_s=12.0):
+    """The oracle as it stands: dequantize + fp64 attention of one (sequence, KV
+    head) of the mixed-width cache, repeated for ~budget_s, scaled to a step."""
+    from oracle import kvq_oracle as O
+    import torch
+    t_old = w.context - w.trizone_fresh
+    tz = O.trizone_quantize(inp["K"][0, :, 0], inp["V"][0, :, 0], inp["v_width"][0, 0],
+                            inp["k_width"][0, 0])
+    q = inp["q"][0][:w.gqa]
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while time.perf_counter() < t_end or len(times) < 2:
+        t0 = time.perf_counter()
+        O.trizone_attention(q, [tz], w.sm_scale)
+        times.append(time.perf_counter() - t0)
+    segs = w.batch * w.n_kv_heads
+    return {"value": statistics.median(times) * segs * 1e6, "unit": UNIT, "kind": "oracle",
+            "cores": torch.get_num_threads(),
+            "sample": f"1 of {segs} (sequence, KV head) segments ({w.gqa} query heads, {t_old} old + "
+                      f"{w.trizone_fresh} fresh tokens), median of {len(times)} runs, x{segs}"}
+
+
+def main_trizone(args):
+    """The mixed-width cache: 4 sequences x 8 KV heads x (65,408 old tokens with
+    value widths {0,2,4,8,16} and key widths {2,4,8} drawn per token / channel,
+    + 128 fresh fp16 tokens).  A step is one kvq_trizone_decode_attn call."""
+    import torch
+    import torch.distributed as dist
+    from quantized_kv_cache_11_gb300 import kvq
+    from quantized_kv_cache_11_gb300 import synthetic as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kvq.load_library()
+    w = S.TRIZONE
+    inp = S.generate(w)
+    B, H = w.batch, w.n_kv_heads
+    t_old, nf = w.context - w.trizone_fresh, w.trizone_fresh
+    K = torch.from_numpy(inp["K"]).to(dev)
+    V = torch.from_numpy(inp["V"]).to(dev)
+    vw = torch.from_numpy(inp["v_width"]).to(dev)
+    kw = torch.from_numpy(inp["k_width"]).to(dev)
+    q = torch.from_numpy(inp["q"]).to(dev)
+    nb = trizone_bytes(w, inp["v_width"], inp["k_width"], nf)
+
+    def make():
+        c = kvq.TriZoneCache(B, H, t_old, nf, device=dev)
+        c.build(K, V, vw, kw, [t_old] * B, [nf] * B)
+        return c
+
+    probe = make()
+    used = int(probe.views()["index"][:, :, 104:108].contiguous().view(torch.int32).sum())
+    n_rep = max(4, math.ceil(3 * 128e6 / used) + 1)
+    caches = [probe] + [make() for _ in range(n_rep - 1)]
+    torch.cuda.synchronize()
+    # build timing (first replica, repeated)
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record()
+    for _ in range(5):
+        caches[0].build(K, V, vw, kw, [t_old] * B, [nf] * B)
+    b1.record()
+    torch.cuda.synchronize()
+    build_us = b0.elapsed_time(b1) * 1000 / 5
+    # build moves: the kept and fresh K/V rows in, widths in, the records and the
+    # token order out
+    build_bytes = (nb["kept"] + B * H * nf) * w.head_dim * 2 * 2 + vw.numel() + kw.numel() + \
+        used + nb["kept"] * 4 + B * H * 512
+
+    outs = [torch.empty(B, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev) for _ in caches]
+    for i in range(max(args.warmup, 3)):
+        caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep])
+    torch.cuda.synchronize()
+    parity = None
+    if rank == 0:
+        from oracle import kvq_oracle as O
+        tz = O.trizone_quantize(inp["K"][0, :, 0], inp["V"][0, :, 0], inp["v_width"][0, 0],
+                                inp["k_width"][0, 0])
+        ref = O.trizone_attention(inp["q"][0][:w.gqa], [tz], w.sm_scale)
+        got = outs[0][0, :w.gqa].double().cpu().numpy()
+        parity = {"segments_checked": 1, "max_abs": float(np.abs(got - ref).max())}
+    us_step, steps, clocks = time_graph(
+        lambda i: caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep]),
+        n_rep, args.steps, world, local)
+    q_host = torch.from_numpy(inp["q"]).pin_memory()
+    out_host = torch.empty(B, w.n_q_heads, w.head_dim, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(q)
+    e2e_us = time_e2e(lambda i, qd: caches[i % n_rep].decode(qd, w.sm_scale, out=outs[i % n_rep]),
+                      q_host, q_dev, out_host, outs, n_rep, min(steps, 4000))
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = load_peaks()
+    achieved = nb["decode"] / (us_step * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "n_q_heads": w.n_q_heads, "n_kv_heads": H,
+                   "head_dim": w.head_dim, "old_tokens": t_old, "fresh_tokens": nf,
+                   "kept_tokens_mean": nb["kept"] / (B * H),
+                   "v_width_probs": list(w.v_width_probs), "k_width_probs": list(w.k_width_probs),
+                   "stored_bytes": used,
+                   "l2": f"inputs larger than L2: {n_rep} cache replicas ({n_rep * used / 1e6:.0f} MB "
+                         f"stored) rotated every step",
+                   "launch": "CUDA graph of kvq_trizone_decode_attn calls"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": read_traffic("trizone_decode_traffic.txt", w.name, _kernel_sha(TZ_FILES)),
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": nb["decode"]},
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": out_host.numel() * 4},
+        "gpu_launches": steps,
+        "clocks": clocks,
+        "path": {"decode_us": us_step, "build_us": build_us,
+                 "build_gbs": build_bytes / (build_us * 1e-6) / 1e9},
+        "parity_sample": parity,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = trizone_cpu_baseline(w, inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _kernel_sha(files=("kvq_decode.cu", "kvq_common.cuh")) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("kvq_decode.cu", "kvq_common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "quantized_kv_cache_11_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

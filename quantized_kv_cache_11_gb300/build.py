@@ -17,7 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
-SOURCES = ["kvq_api.cu", "kvq_quantize.cu", "kvq_decode.cu"]
+SOURCES = ["kvq_api.cu", "kvq_quantize.cu", "kvq_decode.cu", "kvq_trizone_build.cu",
+           "kvq_trizone_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE-exact fp32 division and no flush-to-zero: the quantizer must match the
 # oracle bit for bit.  Never --use_fast_math.
@@ -39,8 +40,10 @@ def _sources_newer(target: str) -> bool:
     for f in os.listdir(CSRC):
         if os.path.getmtime(os.path.join(CSRC, f)) > t:
             return True
-    inc = os.path.join(os.path.dirname(HERE), "include", "kvq.h")
-    return os.path.getmtime(inc) > t or os.path.getmtime(__file__) > t
+    inc = os.path.join(os.path.dirname(HERE), "include")
+    if any(os.path.getmtime(os.path.join(inc, f)) > t for f in os.listdir(inc)):
+        return True
+    return os.path.getmtime(__file__) > t
 
 
 def build(force: bool = False, verbose: bool = False, extra: list | None = None) -> str:

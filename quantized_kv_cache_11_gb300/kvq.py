@@ -1,4 +1,5 @@
-"""Thin Python binding of libkvq.so (the C ABI declared in include/kvq.h).
+"""Thin Python binding of libkvq.so (the C ABI declared in include/kvq.h and
+include/kvq_trizone.h).
 
 Argument marshalling only: every step of the quantizer and of the decode runs
 in the library's CUDA kernels.  Tensors are PyTorch CUDA tensors; PyTorch is
@@ -31,10 +32,19 @@ KVQ_NBUF = 7
 (KVQ_BUF_K_CODES, KVQ_BUF_V_CODES, KVQ_BUF_K_META, KVQ_BUF_V_META, KVQ_BUF_K_TAIL,
  KVQ_BUF_V_TAIL, KVQ_BUF_LENGTHS) = range(7)
 
-# Every entry point of include/kvq.h.
+KVQ_DEVERR_BAD_WIDTH = 8
+KVQ_TZ_INDEX_BYTES = 512
+KVQ_TZ_MAX_BLOCK_BYTES = 13312
+KVQ_TZ_FRESH_BLOCK_BYTES = 16384
+KVQ_TZ_MAX_SEGMENTS = 1024
+KVQ_TZ_NBUF = 3
+KVQ_TZ_BUF_INDEX, KVQ_TZ_BUF_TOKENS, KVQ_TZ_BUF_BLOCKS = range(3)
+
+# Every entry point of include/*.h.
 EXPORTS = ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
            "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
-           "kvq_status_string", "kvq_version")
+           "kvq_status_string", "kvq_version", "kvq_trizone_bytes", "kvq_trizone_build",
+           "kvq_trizone_decode_workspace_bytes", "kvq_trizone_decode_attn")
 KVQ_STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -57,6 +67,22 @@ class kvq_cache(ctypes.Structure):
         ("n_quant", ctypes.c_void_p),
         ("n_tail", ctypes.c_void_p),
         ("tail_head", ctypes.c_void_p),
+        ("error_flags", ctypes.c_void_p),
+    ]
+
+
+class kvq_trizone(ctypes.Structure):
+    """Mirror of ``struct kvq_trizone``."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("max_old", ctypes.c_int32),
+        ("max_fresh", ctypes.c_int32),
+        ("index", ctypes.c_void_p),
+        ("tokens", ctypes.c_void_p),
+        ("blocks", ctypes.c_void_p),
         ("error_flags", ctypes.c_void_p),
     ]
 
@@ -90,12 +116,21 @@ def load_library() -> ctypes.CDLL:
     lib.kvq_decode_workspace_bytes.argtypes = [cache_p, ctypes.c_int32, P(c_sz)]
     lib.kvq_decode_attn.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_sz, c_vp]
     lib.kvq_decode_attn_static.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp]
+    tz_p = P(kvq_trizone)
+    lib.kvq_trizone_bytes.argtypes = [tz_p, P(c_sz)]
+    lib.kvq_trizone_build.argtypes = [tz_p, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp,
+                                      P(ctypes.c_int32), P(ctypes.c_int32), c_vp]
+    lib.kvq_trizone_decode_workspace_bytes.argtypes = [tz_p, ctypes.c_int32, P(c_sz)]
+    lib.kvq_trizone_decode_attn.argtypes = [tz_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_sz,
+                                            c_vp]
     lib.kvq_status_string.argtypes = [c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     lib.kvq_version.argtypes = []
     lib.kvq_version.restype = ctypes.c_char_p
     for name in ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
-                 "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static"):
+                 "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
+                 "kvq_trizone_bytes", "kvq_trizone_build", "kvq_trizone_decode_workspace_bytes",
+                 "kvq_trizone_decode_attn"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -275,3 +310,111 @@ class QuantizedKVCache:
     def device_errors(self) -> int:
         """Read (with a sync) the device error bits."""
         return int(self.error_flags.item())
+
+
+# --------------------------------------------------------------- mixed width
+def kvq_trizone_bytes(desc: kvq_trizone) -> list:
+    sizes = (ctypes.c_size_t * KVQ_TZ_NBUF)()
+    _check("kvq_trizone_bytes", load_library().kvq_trizone_bytes(ctypes.byref(desc), sizes))
+    return list(sizes)
+
+
+def kvq_trizone_build(cache: "TriZoneCache", k: torch.Tensor, v: torch.Tensor,
+                      v_width: torch.Tensor, k_width: torch.Tensor, t_old: Sequence[int],
+                      n_fresh: Sequence[int], stream=None) -> None:
+    """k, v: fp16 [B, T, Hkv, D] (same strides, D contiguous); v_width: uint8
+    [B, Hkv, max_old] contiguous; k_width: uint8 [B, Hkv, D] contiguous."""
+    _need(k, torch.float16, "k")
+    _need(v, torch.float16, "v")
+    _need(v_width, torch.uint8, "v_width")
+    _need(k_width, torch.uint8, "k_width")
+    if k.shape != v.shape or k.stride() != v.stride() or k.stride(3) != 1:
+        raise ValueError("k and v need equal shapes and strides with a contiguous last dim")
+    B, H = cache.batch, cache.n_kv_heads
+    if v_width.shape != (B, H, cache.max_old) or not v_width.is_contiguous():
+        raise ValueError("v_width must be a contiguous [B, Hkv, max_old] tensor")
+    if k_width.shape != (B, H, cache.head_dim) or not k_width.is_contiguous():
+        raise ValueError("k_width must be a contiguous [B, Hkv, D] tensor")
+    if len(t_old) != B or len(n_fresh) != B:
+        raise ValueError("t_old and n_fresh need one entry per sequence")
+    if k.shape[0] != B or k.shape[2] != H or k.shape[3] != cache.head_dim or \
+            any(int(a) + int(f) > k.shape[1] for a, f in zip(t_old, n_fresh)):
+        raise ValueError("k/v must be [B, T, Hkv, D] with T >= t_old + n_fresh")
+    to = (ctypes.c_int32 * B)(*[int(x) for x in t_old])
+    nf = (ctypes.c_int32 * B)(*[int(x) for x in n_fresh])
+    st = load_library().kvq_trizone_build(
+        ctypes.byref(cache.desc), _ptr(k), _ptr(v), k.stride(0), k.stride(1), k.stride(2),
+        _ptr(v_width), _ptr(k_width), to, nf, _stream(stream))
+    _check("kvq_trizone_build", st)
+
+
+def kvq_trizone_decode_workspace_bytes(cache: "TriZoneCache", n_q_heads: int) -> int:
+    out = ctypes.c_size_t()
+    _check("kvq_trizone_decode_workspace_bytes", load_library().kvq_trizone_decode_workspace_bytes(
+        ctypes.byref(cache.desc), int(n_q_heads), ctypes.byref(out)))
+    return out.value
+
+
+def kvq_trizone_decode_attn(cache: "TriZoneCache", q: torch.Tensor, out: torch.Tensor,
+                            sm_scale: float, workspace: torch.Tensor, stream=None) -> None:
+    """q: fp16 [B, Hq, D] contiguous; out: fp32 [B, Hq, D] contiguous."""
+    _need(q, torch.float16, "q")
+    _need(out, torch.float32, "out")
+    _need(workspace, torch.uint8, "workspace")
+    if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    st = load_library().kvq_trizone_decode_attn(ctypes.byref(cache.desc), q.shape[1], _ptr(q),
+                                                _ptr(out), float(sm_scale), _ptr(workspace),
+                                                workspace.numel(), _stream(stream))
+    _check("kvq_trizone_decode_attn", st)
+
+
+class TriZoneCache:
+    """Owns the device buffers of a mixed-width cache (allocated with PyTorch)."""
+
+    def __init__(self, batch: int, n_kv_heads: int, max_old: int, max_fresh: int,
+                 head_dim: int = 128, device="cuda"):
+        self.batch, self.n_kv_heads, self.head_dim = batch, n_kv_heads, head_dim
+        self.max_old, self.max_fresh = max_old, max_fresh
+        d = kvq_trizone(batch, n_kv_heads, head_dim, max_old, max_fresh)
+        sizes = kvq_trizone_bytes(d)
+        dev = torch.device(device)
+        self.region = sizes[KVQ_TZ_BUF_BLOCKS] // (batch * n_kv_heads)
+        self.index = torch.zeros(sizes[KVQ_TZ_BUF_INDEX], dtype=torch.uint8, device=dev)
+        self.tokens = torch.zeros(max(sizes[KVQ_TZ_BUF_TOKENS] // 4, 4), dtype=torch.int32,
+                                  device=dev)
+        self.blocks = torch.zeros(sizes[KVQ_TZ_BUF_BLOCKS], dtype=torch.uint8, device=dev)
+        self.error_flags = torch.zeros(4, dtype=torch.int32, device=dev)
+        d.index, d.tokens, d.blocks = (self.index.data_ptr(), self.tokens.data_ptr(),
+                                       self.blocks.data_ptr())
+        d.error_flags = self.error_flags.data_ptr()
+        self.desc = d
+        self._workspaces = {}
+
+    def views(self) -> dict:
+        B, H = self.batch, self.n_kv_heads
+        return {"index": self.index.view(B, H, KVQ_TZ_INDEX_BYTES),
+                "tokens": self.tokens[:B * H * self.max_old].view(B, H, self.max_old),
+                "blocks": self.blocks.view(B, H, self.region)}
+
+    def workspace(self, n_q_heads: int) -> torch.Tensor:
+        ws = self._workspaces.get(n_q_heads)
+        if ws is None:
+            ws = torch.zeros(kvq_trizone_decode_workspace_bytes(self, n_q_heads),
+                             dtype=torch.uint8, device=self.index.device)
+            self._workspaces[n_q_heads] = ws
+        return ws
+
+    def build(self, k, v, v_width, k_width, t_old, n_fresh, stream=None):
+        kvq_trizone_build(self, k, v, v_width, k_width, t_old, n_fresh, stream)
+
+    def decode(self, q, sm_scale: Optional[float] = None, out=None, stream=None):
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.head_dim)
+        kvq_trizone_decode_attn(self, q, out, sm_scale, self.workspace(q.shape[1]), stream)
+        return out
+
+    def device_errors(self) -> int:
+        return int(self.error_flags[0].item())

@@ -1,4 +1,4 @@
-"""The C-ABI library loads, exports every entry point of include/kvq.h, and its
+"""The C-ABI library loads, exports every entry point of include/*.h, and its
 host-side validation rejects bad arguments before any CUDA call (CPU-only)."""
 import ctypes
 import os
@@ -18,7 +18,9 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc))
+                  if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(kvq_[a-z_]+)\s*\(", src)))
 
@@ -112,3 +114,60 @@ def test_decode_and_append_validation_fails_before_launch(lib):
     assert lib.kvq_append_token(ctypes.byref(d), 0x1004, 0x1000, None) == kvq.KVQ_ERR_INVALID
     assert lib.kvq_append_token(ctypes.byref(_fake_cache(bits=5)), 0x1000, 0x2000, None) == \
         kvq.KVQ_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------- mixed width
+def test_trizone_bytes_matches_layout(lib):
+    d = kvq.kvq_trizone(4, 8, 128, 65408, 128)
+    s = kvq.kvq_trizone_bytes(d)
+    assert s[kvq.KVQ_TZ_BUF_INDEX] == 32 * 512
+    assert s[kvq.KVQ_TZ_BUF_TOKENS] == 32 * 65408 * 4
+    # worst case per (sequence, KV head): ceil(65408/32) + 3 records of 13312 bytes
+    # plus 4 fresh blocks of 16384, rounded up to 256
+    region = -(-((2044 + 3) * 13312 + 4 * 16384) // 256) * 256
+    assert s[kvq.KVQ_TZ_BUF_BLOCKS] == 32 * region
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, kvq.KVQ_ERR_UNSUPPORTED), ("batch", 0, kvq.KVQ_ERR_INVALID),
+    ("max_old", -1, kvq.KVQ_ERR_INVALID), ("max_fresh", -5, kvq.KVQ_ERR_INVALID),
+])
+def test_trizone_bytes_rejects_bad_geometry(lib, field, value, status):
+    d = kvq.kvq_trizone(1, 8, 128, 1024, 128)
+    setattr(d, field, value)
+    sizes = (ctypes.c_size_t * kvq.KVQ_TZ_NBUF)()
+    assert lib.kvq_trizone_bytes(ctypes.byref(d), sizes) == status
+
+
+def _fake_tz(**kw):
+    d = kvq.kvq_trizone(2, 4, 128, 1024, 64)
+    d.index, d.tokens, d.blocks = 0x10000, 0x20000, 0x100000
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_trizone_validation_fails_before_launch(lib):
+    i32 = ctypes.c_int32 * 2
+    build = lambda d, k=0x1000000, to=(1000, 1000), nf=(64, 64), st=(1 << 14, 512, 128), vw=0x2000000: \
+        lib.kvq_trizone_build(ctypes.byref(d), k, k + 0x1000, *st, vw, vw + 0x10000, i32(*to), i32(*nf),
+                              None)
+    assert build(_fake_tz(index=None)) == kvq.KVQ_ERR_INVALID
+    assert build(_fake_tz(blocks=0x100008)) == kvq.KVQ_ERR_INVALID  # blocks 16-byte aligned
+    assert build(_fake_tz(), k=0) == kvq.KVQ_ERR_INVALID
+    assert build(_fake_tz(), vw=0) == kvq.KVQ_ERR_INVALID
+    assert build(_fake_tz(), to=(1025, 0)) == kvq.KVQ_ERR_CAPACITY
+    assert build(_fake_tz(), nf=(65, 0)) == kvq.KVQ_ERR_CAPACITY
+    assert build(_fake_tz(), to=(-1, 0)) == kvq.KVQ_ERR_INVALID
+    assert build(_fake_tz(), st=(1 << 14, 514, 128)) == kvq.KVQ_ERR_INVALID
+    assert build(_fake_tz(head_dim=64)) == kvq.KVQ_ERR_UNSUPPORTED
+    dec = lambda d, hq=16, q=0x200000, out=0x300000, scale=0.088, w=0x400000, wb=1 << 30: \
+        lib.kvq_trizone_decode_attn(ctypes.byref(d), hq, q, out, scale, w, wb, None)
+    assert dec(_fake_tz(), hq=6) == kvq.KVQ_ERR_INVALID
+    assert dec(_fake_tz(), hq=48) == kvq.KVQ_ERR_UNSUPPORTED
+    assert dec(_fake_tz(), out=0x300004) == kvq.KVQ_ERR_INVALID
+    assert dec(_fake_tz(), scale=-1.0) == kvq.KVQ_ERR_INVALID
+    assert dec(_fake_tz(batch=256, n_kv_heads=8)) == kvq.KVQ_ERR_UNSUPPORTED  # > 1024 segments
+    ws = ctypes.c_size_t()
+    assert lib.kvq_trizone_decode_workspace_bytes(ctypes.byref(_fake_tz()), 6, ctypes.byref(ws)) == \
+        kvq.KVQ_ERR_INVALID
