@@ -49,8 +49,7 @@
  *   [5:9] blocks per value width  [9] fresh blocks
  *   [10:13] channels per key width (2, 4, 8)  [13:16] k-tiles per key width
  *   [16:21] bytes of one block of each kind  [21:26] byte offset of each kind's
- *   first block in the region  [26] bytes used  [27] work weight of the
- *   region (decode's load balance; not part of the reference layout)  [28:32] 0
+ *   first block in the region  [26] bytes used  [27:32] 0
  * followed by int16 [160] permuted channel slots (channel, or -1 for a pad or
  * past the last k-tile) and 64 zero bytes.
  */

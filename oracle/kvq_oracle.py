@@ -489,8 +489,7 @@ def trizone_attention(q16: np.ndarray, tz_heads: list, sm_scale: float) -> np.nd
 #   [5:9] blocks per V width, [9] fresh blocks, [10:13] channels per K width
 #   (2, 4, 8), [13:16] k-tiles per K width, [16:21] bytes of one block of each
 #   kind (widths 2, 4, 8, 16, fresh), [21:26] byte offset of each kind's first
-#   block, [26] total bytes, [27] work weight = max(1, sum over kinds of blocks x
-#   ceil(block bytes / 256)) (the decode's load-balance unit), [28:32] zero;
+#   block, [26] total bytes, [27:32] zero;
 # then int16 [160] permuted channel slots (-1 = pad, and past the last k-tile),
 # then 64 zero bytes.
 # ---------------------------------------------------------------------------
@@ -641,7 +640,6 @@ def trizone_pack(tz: dict, d: int = 128) -> dict:
     hdr[16:21] = rec_bytes
     hdr[21:26] = offs[:5]
     hdr[26] = offs[5]
-    hdr[27] = max(1, sum(n * -(-b // 256) for n, b in zip(counts, rec_bytes)))
     sl = np.full(160, -1, np.int16)
     sl[:len(slots)] = slots
     index = np.concatenate([hdr.view(np.uint8), sl.view(np.uint8), np.zeros(64, np.uint8)])

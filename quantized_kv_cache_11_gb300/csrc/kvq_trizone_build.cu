@@ -141,21 +141,18 @@ __global__ void __launch_bounds__(kIndexThreads) index_kernel(const __grid_const
       rec[4] = KVQ_TZ_FRESH_BLOCK_BYTES;
       s_hdr[H_NFRESH] = nf;
       int off = 0;
-      int64_t weight = 0;
       for (int i = 0; i < kKinds; ++i) {
         s_hdr[H_NBLK + i] = nblk[i];
         s_hdr[H_REC + i] = rec[i];
         s_hdr[H_OFF + i] = off;
         off += nblk[i] * rec[i];
-        weight += (int64_t)nblk[i] * ((rec[i] + kUnit - 1) / kUnit);
       }
       for (int i = 0; i < 3; ++i) {
         s_hdr[H_NCH + i] = nch[i];
         s_hdr[H_KT + i] = kts[i];
       }
       s_hdr[H_USED] = off;
-      s_hdr[H_WEIGHT] = (int)(weight > 0 ? weight : 1);
-      for (int i = H_WEIGHT + 1; i < 32; ++i) s_hdr[i] = 0;
+      for (int i = H_USED + 1; i < 32; ++i) s_hdr[i] = 0;
     }
   }
   if (bad && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_BAD_WIDTH);

@@ -5,10 +5,11 @@
 // (fp16 values) and zone C (fp16 fresh tokens), so the cache is never expanded.
 //
 // How:
-// * Work partition (stream-K over bytes): every block record of every
-//   (sequence, KV head) weighs ceil(record bytes / 256) units; the units of all
-//   segments are laid end to end and cut into equal ranges, one per resident
-//   CTA.  A CTA owns the blocks whose first unit falls in its range.
+// * Work partition (stream-K): every block of every (sequence, KV head) weighs
+//   a few units by kind (the decode of a block costs about the same for every
+//   value width: the arithmetic, not the record's bytes, sets its time); the
+//   units of all segments are laid end to end and cut into equal ranges, one
+//   per resident CTA.  A CTA owns the blocks whose first unit falls in its range.
 // * Inside a CTA the warps deal the CTA's blocks of the current segment round
 //   robin (blocks are stored by kind, so every warp gets a similar mix of sizes,
 //   and the assignment -- hence the summation order -- is the same on every
@@ -95,27 +96,37 @@ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
   return ((x + 1) * n - 1) / total;
 }
 
-// Work weight of a segment as the partition sees it (clamped so that a
-// corrupt index cannot overflow the prefix).
+// Work units of one block of each kind (value width 2, 4, 8, 16, fresh):
+// measured decode time per block, in steps of about a tenth.
+__constant__ int c_kind_units[kKinds] = {10, 10, 11, 12, 12};
+
+// Work units of a segment as the partition sees it: its blocks by kind (block
+// counts clamped so that a corrupt index cannot overflow the prefix), at least 1.
 __device__ __forceinline__ int64_t seg_weight(const Params& p, int s) {
-  const int w = reinterpret_cast<const int32_t*>(p.index + (size_t)s * KVQ_TZ_INDEX_BYTES)[H_WEIGHT];
-  return w < 1 ? 1 : (w > (1 << 26) ? (1 << 26) : w);
+  const int32_t* hd = reinterpret_cast<const int32_t*>(p.index + (size_t)s * KVQ_TZ_INDEX_BYTES);
+  int64_t w = 0;
+#pragma unroll
+  for (int k = 0; k < kKinds; ++k) {
+    const int n = hd[H_NBLK + k];
+    w += (int64_t)(n < 0 ? 0 : (n > (1 << 24) ? (1 << 24) : n)) * c_kind_units[k];
+  }
+  return w > 0 ? w : 1;
 }
 
 // The index record is what the build wrote: every field consistent.
 __device__ __forceinline__ bool header_ok(const int* hd, int64_t region) {
   const int kt2 = hd[H_KT], kt4 = hd[H_KT + 1], kt8 = hd[H_KT + 2];
   bool ok = kt2 >= 0 && kt4 >= 0 && kt8 >= 0 && kt2 + kt4 + kt8 <= kKtMax;
-  int64_t off = 0, weight = 0;
+  int64_t off = 0;
   for (int k = 0; k < kKinds && ok; ++k) {
     const int n = hd[H_NBLK + k];
     const int cnt = k < 4 ? hd[H_NTOK + k] : hd[H_NFRESH];
     const int rec = k < 4 ? record_bytes(kt2, kt4, kt8, k) : KVQ_TZ_FRESH_BLOCK_BYTES;
-    ok = cnt >= 0 && n == (cnt + kGroup - 1) / kGroup && hd[H_REC + k] == rec && hd[H_OFF + k] == off;
+    ok = cnt >= 0 && n <= (1 << 24) && n == (cnt + kGroup - 1) / kGroup && hd[H_REC + k] == rec &&
+         hd[H_OFF + k] == off;
     off += (int64_t)n * rec;
-    weight += (int64_t)n * ((rec + kUnit - 1) / kUnit);
   }
-  return ok && hd[H_USED] == off && off <= region && hd[H_WEIGHT] == (weight > 0 ? weight : 1);
+  return ok && hd[H_USED] == off && off <= region;
 }
 
 template <int G>
@@ -668,7 +679,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
       int cum = 0;
       for (int k = 0; k < kKinds; ++k) {
         const int n = ok ? s_hdr[H_NBLK + k] : 0;
-        const int wg = (s_hdr[H_REC + k] + kUnit - 1) / kUnit;
+        const int wg = c_kind_units[k];
         const int64_t lo64 = a <= cw ? 0 : (a - cw + wg - 1) / wg;
         const int lo = (int)(lo64 < n ? lo64 : n);
         const int64_t hi64 = e <= cw ? 0 : (e - cw + wg - 1) / wg;

@@ -15,7 +15,6 @@ constexpr int kDim = 128;   // head_dim
 constexpr int kKinds = 5;   // block kinds: value width 2, 4, 8, 16, fresh
 constexpr int kKtMax = 10;  // k-tiles of three key classes over 128 channels, at most
 constexpr int kSlots = 16 * kKtMax;
-constexpr int kUnit = 256;  // bytes per unit of the decode's work weight
 constexpr int kFp16TileBytes = 32 * kDim * 2;  // 32 tokens x 128 channels of fp16
 
 // int32 fields of the index record
@@ -28,7 +27,6 @@ enum {
   H_REC = 16,     // [5] bytes of one block of each kind
   H_OFF = 21,     // [5] byte offset of each kind's first block
   H_USED = 26,    // bytes used in the region
-  H_WEIGHT = 27,  // work weight (units of kUnit bytes)
 };
 
 __host__ __device__ constexpr int key_code_bytes(int kt2, int kt4, int kt8) {

@@ -575,9 +575,7 @@ def test_trizone_pack_index_and_stream():
     assert hdr[5:9].tolist() == [(n + 31) // 32 for n in n_tok] and hdr[9] == 2
     assert hdr[10:13].tolist() == [int((kw == c).sum()) for c in (2, 4, 8)]
     assert hdr[13:16].tolist() == [(int((kw == c).sum()) + 15) // 16 for c in (2, 4, 8)]
-    assert hdr[20] == 16384 and hdr[21] == 0 and (hdr[28:] == 0).all()
-    # weight: blocks x 256-byte units of their records, summed over the kinds
-    assert hdr[27] == sum(int(hdr[5 + i]) * ((int(hdr[16 + i]) + 255) // 256) for i in range(5))
+    assert hdr[20] == 16384 and hdr[21] == 0 and (hdr[27:] == 0).all()
     assert all(hdr[21 + i + 1] == hdr[21 + i] + hdr[5 + i] * hdr[16 + i] for i in range(4))
     assert hdr[26] == hdr[25] + 2 * 16384 == pk["data"].size
     # stream order: kept tokens by width class, ascending positions inside a class
