@@ -280,12 +280,21 @@ def time_graph(launch, n_rep, steps_wanted, world, local):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=torch.device("cuda", local))
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), torch.device("cuda", local))
     return elapsed_ms * 1000.0 / steps, steps, clk.summary()
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest of the ranks' values (every rank gets it); the value itself
+    when there is one rank.  Each rank runs its own replica of the workload, so
+    the job's time per step is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def time_e2e(launch, q_host, q_dev, out_host, outs, n_rep, n):
