@@ -22,6 +22,7 @@ struct GroupParams {
   __half zero_h;
   float scale;  // fp32 value of the stored fp16 scale
   float zero;   // fp32 value of the stored fp16 zero point
+  float inv;    // fp32 reciprocal of scale (round to nearest), 0 when scale is 0
 };
 
 template <int BITS>
@@ -35,17 +36,34 @@ __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
   p.zero = __half2float(p.zero_h);
   if (p.scale == 0.f) { p.scale_h = __float2half_rn(0.f); p.scale = 0.f; }  // -0 -> +0
   if (p.zero == 0.f) { p.zero_h = __float2half_rn(0.f); p.zero = 0.f; }
+  p.inv = p.scale == 0.f ? 0.f : __frcp_rn(p.scale);
   return p;
 }
 
+// code = clamp(rint(fl(d / scale))), d = fl(x - zero), every op round-to-nearest.
+// Fast path: y = fl(d * fl(1/scale)).  With Q = d / scale exact, y and the rounded
+// quotient fl(Q) each lie within 2^-23 |Q| of Q, and 0 <= Q < 2^9 here (d <= max -
+// min and scale is that range over 2^b - 1, up to fp16 rounding of the scale), so
+// |y - fl(Q)| < 2^-13: y rounds to the same integer as fl(Q) unless y is within
+// 2^-13 of a half-integer.  Those rare y (window 2^-11, four times the bound) take
+// the exact IEEE division, so the code is bit-identical to the division.
+// Rounding to an integer, ties to even: for 0 <= y < 2^22, y + 1.5 * 2^23 is
+// rounded to a whole number by the fp32 addition itself (the sum's ulp is 1),
+// and its low mantissa bits are that number.
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
 template <int BITS>
 __device__ __forceinline__ uint32_t quant_code(float x, const GroupParams& p) {
   if (p.scale == 0.f) return 0u;
-  const float q = __fdiv_rn(__fsub_rn(x, p.zero), p.scale);
-  int c = __float2int_rn(q);  // round half to even
-  c = c < 0 ? 0 : c;
-  c = c > (1 << BITS) - 1 ? (1 << BITS) - 1 : c;
-  return (uint32_t)c;
+  const float d = __fsub_rn(x, p.zero);  // >= 0
+  float q = __fmul_rn(d, p.inv);
+  float t = __fadd_rn(q, kRoundMagic);
+  if (fabsf(__fsub_rn(q, __fsub_rn(t, kRoundMagic))) > 0.5f - 0x1p-11f) {
+    q = __fdiv_rn(d, p.scale);  // near a tie: the exact quotient decides
+    t = __fadd_rn(q, kRoundMagic);
+  }
+  const uint32_t c = __float_as_uint(t) - kRoundMagicBits;
+  return c > (1u << BITS) - 1 ? (1u << BITS) - 1 : c;
 }
 
 // ---------------------------------------------------------------------------
@@ -147,7 +165,8 @@ __device__ __forceinline__ void store_meta_lane_order(const __half* nat, __half*
 // One warp quantizes one 32-token tile of keys and of values.
 //   ksrc/vsrc: token 0 of the tile for this head; rows tstride elements apart,
 //   channels contiguous.  Writes packed codes and metadata of the tile.
-//   ct: shared scratch of 32 * D bytes for this warp; vm: shared 2 * D halves.
+//   ct: shared scratch of 32 * D bytes for this warp; vm: shared 2 * D halves;
+//   vinv: shared D floats (the value groups' reciprocal scales).
 // Keys: one group per channel over the 32 tokens (lane-local min/max, each lane
 // owns D/32 channels).  Values: one group per 32 channels of a token (min/max
 // reduced over the lanes that share a group with shuffles).
@@ -181,7 +200,7 @@ __device__ __forceinline__ void quantize_tile_warp(const __half* ksrc, const __h
                                                    int64_t tstride, uint8_t* kcodes_dst,
                                                    __half* kmeta_dst, uint8_t* vcodes_dst,
                                                    __half* vmeta_dst, uint8_t* ct, __half* vm,
-                                                   int lane) {
+                                                   float* vinv, int lane) {
   constexpr int CPL = D / 32;  // channels per lane
   const int c0 = lane * CPL;
   // ---- keys: per channel over 32 tokens
@@ -215,32 +234,44 @@ __device__ __forceinline__ void quantize_tile_warp(const __half* ksrc, const __h
   pack_store_tile<D, BITS, true>(ct, kcodes_dst, lane);
   store_meta_lane_order<D, true>(vm, kmeta_dst, lane);
   __syncwarp();
-  // ---- values: per token over 32-channel spans
+  // ---- values: per token over 32-channel spans.  The lanes of a group reduce
+  // min/max with shuffles; the group's parameters are computed once, by lane
+  // (t % LPG) of the group, and read back from shared memory (vm, inv).
   {
     constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
     const int j = c0 / kGroup;     // this lane's channel group
+    LaneRow<D> vr[kGroup];
+#pragma unroll
+    for (int t = 0; t < kGroup; ++t) vr[t].load(vsrc + (int64_t)t * tstride + c0);
 #pragma unroll 4
     for (int t = 0; t < kGroup; ++t) {
-      LaneRow<D> r;
-      r.load(vsrc + (int64_t)t * tstride + c0);
-      float mn = r.get(0), mx = mn;
+      float mn = vr[t].get(0), mx = mn;
 #pragma unroll
       for (int i = 1; i < CPL; ++i) {
-        mn = fminf(mn, r.get(i));
-        mx = fmaxf(mx, r.get(i));
+        mn = fminf(mn, vr[t].get(i));
+        mx = fmaxf(mx, vr[t].get(i));
       }
 #pragma unroll
       for (int off = 1; off < LPG; off <<= 1) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       }
-      const GroupParams p = group_params<BITS>(mn, mx);
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) ct[t * D + c0 + i] = (uint8_t)quant_code<BITS>(r.get(i), p);
-      if ((lane % LPG) == 0) {
+      if ((lane % LPG) == (t % LPG)) {
+        const GroupParams p = group_params<BITS>(mn, mx);
         vm[j * kGroup + t] = p.scale_h;
         vm[D + j * kGroup + t] = p.zero_h;
+        vinv[j * kGroup + t] = p.inv;
       }
+    }
+    __syncwarp();
+#pragma unroll 4
+    for (int t = 0; t < kGroup; ++t) {
+      GroupParams p;
+      p.scale = __half2float(vm[j * kGroup + t]);
+      p.zero = __half2float(vm[D + j * kGroup + t]);
+      p.inv = vinv[j * kGroup + t];
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) ct[t * D + c0 + i] = (uint8_t)quant_code<BITS>(vr[t].get(i), p);
     }
   }
   __syncwarp();

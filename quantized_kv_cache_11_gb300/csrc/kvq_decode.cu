@@ -55,10 +55,11 @@ struct DecodeCfg {
   static constexpr int KT = D / 16;
   static constexpr int NWL = T::kWordsPerLane;
   static constexpr int PPW = T::kPairsPerWord;
-  // 2 CTAs per SM (16 warps) for 2- and 4-bit codes
-  static constexpr int WARPS = BITS == 8 ? 4 : 8;
+  // one CTA of 16 warps per SM for 2- and 4-bit codes: fewer, larger CTAs leave
+  // fewer split-K partials per (sequence, KV head) for the last CTA to merge
+  static constexpr int WARPS = BITS == 8 ? 4 : 16;
   static constexpr int NSTAGE = BITS == 2 ? 4 : (BITS == 4 ? 2 : 3);
-  static constexpr int MIN_CTAS = BITS == 8 ? 1 : 2;
+  static constexpr int MIN_CTAS = 1;
   static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
   static constexpr int RING = WARPS * NSTAGE * STAGE;
   static constexpr int PSROW = 48;                   // halves per head row of the p~ exchange

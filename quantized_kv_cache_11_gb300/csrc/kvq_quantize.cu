@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32)
 prefill_kernel(const __grid_constant__ PrefillParams p) {
   __shared__ __align__(16) uint8_t s_ct[kPrefillWarps][kGroup * D];
   __shared__ __align__(16) __half s_vm[kPrefillWarps][2 * D];
+  __shared__ __align__(16) float s_vinv[kPrefillWarps][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, h = blockIdx.y;
   const int item = blockIdx.x * kPrefillWarps + warp;
@@ -55,7 +56,7 @@ prefill_kernel(const __grid_constant__ PrefillParams p) {
                                 vseq + (int64_t)item * kGroup * p.st, p.st,
                                 p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
                                 p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D, s_ct[warp],
-                                s_vm[warp], lane);
+                                s_vm[warp], s_vinv[warp], lane);
   } else if (item < ng + (nt + kGroup - 1) / kGroup) {
     // copy tail tokens [nq + 32c, nq + 32c + 32) to ring slots 32c.. (ring head 0)
     const int c = item - ng;
@@ -95,6 +96,7 @@ template <int D, int BITS>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p) {
   __shared__ __align__(16) uint8_t s_ct[kAppendWarps][kGroup * D];
   __shared__ __align__(16) __half s_vm[kAppendWarps][2 * D];
+  __shared__ __align__(16) float s_vinv[kAppendWarps][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x;
   const int R = p.tail_cap;
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
       quantize_tile_warp<D, BITS>(kt + (size_t)hd * D, vt + (size_t)hd * D, D,
                                   p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
                                   p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D, s_ct[warp],
-                                  s_vm[warp], lane);
+                                  s_vm[warp], s_vinv[warp], lane);
     }
     const size_t src = bh * D + lane * CPL;
     const size_t dst = (size_t)slot * D + lane * CPL;

@@ -18,10 +18,10 @@ namespace tz {
 constexpr int kIndexThreads = 256;
 constexpr int kBlockWarps = 4;
 // per-warp scratch of the block kernel: 32 staged fp16 rows, codes by slot,
-// key scale/zero by slot, value metadata
+// key scale/zero by slot, value metadata, value reciprocal scales
 constexpr int kRowsBytes = kGroup * kDim * 2;
 constexpr int kCodeBytes = kGroup * kSlots;
-constexpr int kWarpScratch = kRowsBytes + kCodeBytes + 4 * kSlots + 4 * kDim;
+constexpr int kWarpScratch = kRowsBytes + kCodeBytes + 4 * kSlots + 4 * kDim + 4 * kDim;
 
 struct BuildParams {
   const __half* k;
@@ -244,37 +244,48 @@ __device__ __forceinline__ void store_key_subtile(const uint8_t* ct, int base, i
 }
 
 // Per-token value quantization of the staged rows (32-channel groups) at width C:
-// codes to ct[t][c] (t < n; zero after), metadata planes to vm[2][128] (natural order).
+// codes to ct[t][c] (t < n; zero after), metadata planes to vm[2][128] (natural
+// order).  The 8 lanes of a group reduce min/max with shuffles; the group's
+// parameters are computed once, by lane t % 8 of the group, and read back from
+// shared memory (vm, vinv).
 template <int C>
-__device__ __forceinline__ void quantize_values(const __half* rows, int n, uint8_t* ct, __half* vm, int lane) {
+__device__ __forceinline__ void quantize_values(const __half* rows, int n, uint8_t* ct, __half* vm, float* vinv,
+                                                int lane) {
   const int c0 = 4 * lane, j = lane / 8;
   for (int t = 0; t < kGroup; ++t) {
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + c0);
     const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
-    const float x[4] = {__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi)};
-    float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    float mn = fminf(fminf(__low2float(lo), __high2float(lo)), fminf(__low2float(hi), __high2float(hi)));
+    float mx = fmaxf(fmaxf(__low2float(lo), __high2float(lo)), fmaxf(__low2float(hi), __high2float(hi)));
 #pragma unroll
     for (int off = 1; off < 8; off <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     }
-    if (t < n) {
-      const GroupParams g = group_params<C>(mn, mx);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ct[t * kDim + c0 + i] = (uint8_t)quant_code<C>(x[i], g);
-      if ((lane & 7) == 0) {
+    if ((lane & 7) == (t & 7)) {
+      if (t < n) {
+        const GroupParams g = group_params<C>(mn, mx);
         vm[j * kGroup + t] = g.scale_h;
         vm[kDim + j * kGroup + t] = g.zero_h;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ct[t * kDim + c0 + i] = 0;
-      if ((lane & 7) == 0) {
+        vinv[j * kGroup + t] = g.inv;
+      } else {
         vm[j * kGroup + t] = __float2half_rn(0.f);
         vm[kDim + j * kGroup + t] = __float2half_rn(0.f);
+        vinv[j * kGroup + t] = 0.f;
       }
     }
+  }
+  __syncwarp();
+  for (int t = 0; t < kGroup; ++t) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + c0);
+    const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
+    const float x[4] = {__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi)};
+    GroupParams g;
+    g.scale = __half2float(vm[j * kGroup + t]);
+    g.zero = __half2float(vm[kDim + j * kGroup + t]);
+    g.inv = vinv[j * kGroup + t];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ct[t * kDim + c0 + i] = t < n ? (uint8_t)quant_code<C>(x[i], g) : (uint8_t)0;
   }
   __syncwarp();
 }
@@ -320,6 +331,7 @@ __global__ void __launch_bounds__(kBlockWarps * 32) block_kernel(const __grid_co
   __half* ksc = reinterpret_cast<__half*>(ws + kRowsBytes + kCodeBytes);
   __half* kze = ksc + kSlots;
   __half* vm = kze + kSlots;
+  float* vinv = reinterpret_cast<float*>(vm + 2 * kDim);
 
   int j = blockIdx.x * kBlockWarps + warp, kind = 0;
   while (kind < kKinds && j >= s_hdr[H_NBLK + kind]) j -= s_hdr[H_NBLK + kind++];
@@ -384,15 +396,15 @@ __global__ void __launch_bounds__(kBlockWarps * 32) block_kernel(const __grid_co
     return;
   }
   if (kind == 0) {
-    quantize_values<2>(rows, n, ct, vm, lane);
+    quantize_values<2>(rows, n, ct, vm, vinv, lane);
     pack_store_tile<kDim, 2, false>(ct, vdst, lane);
     store_meta_lane_order<kDim, false>(vm, reinterpret_cast<__half*>(vdst + Tile<kDim, 2>::kBytes), lane);
   } else if (kind == 1) {
-    quantize_values<4>(rows, n, ct, vm, lane);
+    quantize_values<4>(rows, n, ct, vm, vinv, lane);
     pack_store_tile<kDim, 4, false>(ct, vdst, lane);
     store_meta_lane_order<kDim, false>(vm, reinterpret_cast<__half*>(vdst + Tile<kDim, 4>::kBytes), lane);
   } else {
-    quantize_values<8>(rows, n, ct, vm, lane);
+    quantize_values<8>(rows, n, ct, vm, vinv, lane);
     pack_store_tile<kDim, 8, false>(ct, vdst, lane);
     store_meta_lane_order<kDim, false>(vm, reinterpret_cast<__half*>(vdst + Tile<kDim, 8>::kBytes), lane);
   }
