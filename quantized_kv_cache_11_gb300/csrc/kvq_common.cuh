@@ -103,9 +103,9 @@ __device__ __forceinline__ void value_pair_pos(int P, int gid, int tig, int& t, 
   t = 16 * kt + 2 * tig + 8 * (i >> 1);
 }
 
-// Pack a 32 x D tile of codes held in shared memory (ct[t * D + c]) and store it
-// to global memory with one 16-byte store per lane per chunk (coalesced).
-template <int D, int BITS, bool IS_KEY>
+// Pack a 32 x D tile of codes held in shared memory (ct[t * PITCH + c]) and store
+// it to global memory with one 16-byte store per lane per chunk (coalesced).
+template <int D, int BITS, bool IS_KEY, int PITCH = D>
 __device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst, int lane) {
   using T = Tile<D, BITS>;
   const int gid = lane >> 2, tig = lane & 3;
@@ -117,13 +117,14 @@ __device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst,
     int t, c;
     uint32_t first, second;
     if (IS_KEY) {
-      key_pair_pos(P, gid, tig, t, c);
-      first = ct[t * D + c];
-      second = ct[t * D + c + 1];
+      key_pair_pos(P, gid, tig, t, c);  // c even: the pair is one 16-bit word
+      const uint32_t pr = *reinterpret_cast<const uint16_t*>(ct + t * PITCH + c);
+      first = pr & 0xFFu;
+      second = pr >> 8;
     } else {
       value_pair_pos(P, gid, tig, t, c);
-      first = ct[t * D + c];
-      second = ct[(t + 1) * D + c];
+      first = ct[t * PITCH + c];
+      second = ct[(t + 1) * PITCH + c];
     }
     const int wi = P / T::kPairsPerWord, k = P % T::kPairsPerWord;
     w[wi] |= (first << slot_bitpos<BITS>(k)) | (second << (16 + slot_bitpos<BITS>(k)));
@@ -303,6 +304,10 @@ __device__ __forceinline__ void cp_async_16_zfill(void* smem, const void* gmem, 
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
                : "memory");
+}
+__device__ __forceinline__ void cp_async_8(void* smem, const void* gmem) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(s), "l"(gmem) : "memory");
 }
 // Four 8x8 b16 matrices; lane i supplies the row address of row i%8 of matrix i/8.
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {

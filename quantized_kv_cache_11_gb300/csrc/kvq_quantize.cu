@@ -28,14 +28,131 @@ struct PrefillParams {
   int32_t ntail[KVQ_MAX_BATCH];
 };
 
+// One warp quantizes one 32-token tile of keys and values whose rows it first
+// stages in shared memory (cp.async, VEC bytes per copy).  Keys: each lane owns
+// D/32 channels (fp16 min/max over the 32 rows, then the codes); values: lane t
+// owns token t (min/max and parameters of its D/32 groups, then the codes).  The
+// codes go through a staging tile at a padded pitch (no bank conflicts) and are
+// packed into the fragment layout.
+template <int D>
+struct StagedTile {
+  static constexpr int PH = D + 8;   // halves per staged row (16-byte aligned rows)
+  static constexpr int PC = D + 8;   // bytes per row of the code staging tile
+  static constexpr int ROWS = kGroup * PH * 2;
+  static constexpr int BYTES = 2 * ROWS + kGroup * PC + 8 * D;  // K rows, V rows, codes, key + value meta
+};
+
+template <int D, int BITS, int VEC>
+__device__ __forceinline__ void quantize_tile_staged(const __half* ksrc, const __half* vsrc, int64_t tstride,
+                                                     uint8_t* kcodes_dst, __half* kmeta_dst, uint8_t* vcodes_dst,
+                                                     __half* vmeta_dst, uint8_t* ws, int lane) {
+  using S = StagedTile<D>;
+  __half* kr = reinterpret_cast<__half*>(ws);
+  __half* vr = reinterpret_cast<__half*>(ws + S::ROWS);
+  uint8_t* ct = ws + 2 * S::ROWS;
+  __half* km = reinterpret_cast<__half*>(ws + 2 * S::ROWS + kGroup * S::PC);
+  __half* vm = km + 2 * D;
+  // ---- stage the 32 key rows and the 32 value rows
+  constexpr int CPR = 2 * D / VEC;  // copies per row
+#pragma unroll 4
+  for (int e = lane; e < kGroup * CPR; e += 32) {
+    const int t = e / CPR, ch = e % CPR;
+    if (VEC == 16) {
+      cp_async_16(kr + t * S::PH + ch * 8, ksrc + (int64_t)t * tstride + ch * 8);
+      cp_async_16(vr + t * S::PH + ch * 8, vsrc + (int64_t)t * tstride + ch * 8);
+    } else {
+      cp_async_8(kr + t * S::PH + ch * 4, ksrc + (int64_t)t * tstride + ch * 4);
+      cp_async_8(vr + t * S::PH + ch * 4, vsrc + (int64_t)t * tstride + ch * 4);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncwarp();
+  // ---- keys: per channel over the 32 tokens; lane owns channels [c0, c0 + CPL)
+  {
+    constexpr int CPL = D / 32, NH = CPL / 2;  // channels, half2 pairs per lane
+    const int c0 = lane * CPL;
+    __half2 mn[NH], mx[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) mn[j] = mx[j] = *reinterpret_cast<const __half2*>(kr + c0 + 2 * j);
+#pragma unroll 8
+    for (int t = 1; t < kGroup; ++t)
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        const __half2 x = *reinterpret_cast<const __half2*>(kr + t * S::PH + c0 + 2 * j);
+        mn[j] = __hmin2(mn[j], x);
+        mx[j] = __hmax2(mx[j], x);
+      }
+    GroupParams gp[CPL];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      gp[2 * j] = group_params<BITS>(__low2float(mn[j]), __low2float(mx[j]));
+      gp[2 * j + 1] = group_params<BITS>(__high2float(mn[j]), __high2float(mx[j]));
+    }
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      km[c0 + j] = gp[j].scale_h;
+      km[D + c0 + j] = gp[j].zero_h;
+    }
+#pragma unroll 4
+    for (int t = 0; t < kGroup; ++t) {
+      uint32_t w = 0u;
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        const __half2 x = *reinterpret_cast<const __half2*>(kr + t * S::PH + c0 + 2 * j);
+        w |= quant_code<BITS>(__low2float(x), gp[2 * j]) << (16 * j);
+        w |= quant_code<BITS>(__high2float(x), gp[2 * j + 1]) << (16 * j + 8);
+      }
+      if (CPL == 4) *reinterpret_cast<uint32_t*>(ct + t * S::PC + c0) = w;
+      else *reinterpret_cast<uint16_t*>(ct + t * S::PC + c0) = (uint16_t)w;
+    }
+  }
+  __syncwarp();
+  pack_store_tile<D, BITS, true, S::PC>(ct, kcodes_dst, lane);
+  store_meta_lane_order<D, true>(km, kmeta_dst, lane);
+  __syncwarp();
+  // ---- values: per token over 32-channel groups; lane t owns token t
+  {
+    const int t = lane;
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const uint4* row = reinterpret_cast<const uint4*>(vr + t * S::PH + 32 * j);
+      uint4 x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = row[i];
+      const __half2* h = reinterpret_cast<const __half2*>(x);
+      __half2 mn = h[0], mx = h[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) {
+        mn = __hmin2(mn, h[i]);
+        mx = __hmax2(mx, h[i]);
+      }
+      const GroupParams gp = group_params<BITS>(fminf(__low2float(mn), __high2float(mn)),
+                                                fmaxf(__low2float(mx), __high2float(mx)));
+      vm[j * kGroup + t] = gp.scale_h;
+      vm[D + j * kGroup + t] = gp.zero_h;
+#pragma unroll
+      for (int w4 = 0; w4 < 8; ++w4) {
+        const uint32_t c0 = quant_code<BITS>(__low2float(h[2 * w4]), gp);
+        const uint32_t c1 = quant_code<BITS>(__high2float(h[2 * w4]), gp);
+        const uint32_t c2 = quant_code<BITS>(__low2float(h[2 * w4 + 1]), gp);
+        const uint32_t c3 = quant_code<BITS>(__high2float(h[2 * w4 + 1]), gp);
+        *reinterpret_cast<uint32_t*>(ct + t * S::PC + 32 * j + 4 * w4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      }
+    }
+  }
+  __syncwarp();
+  pack_store_tile<D, BITS, false, S::PC>(ct, vcodes_dst, lane);
+  store_meta_lane_order<D, false>(vm, vmeta_dst, lane);
+  __syncwarp();
+}
+
 // grid (work items / warps, Hkv, B); a work item is a 32-token tile to quantize
 // or a chunk of up to 32 tail tokens to copy.
-template <int D, int BITS>
+template <int D, int BITS, int VEC>
 __global__ void __launch_bounds__(kPrefillWarps * 32)
 prefill_kernel(const __grid_constant__ PrefillParams p) {
-  __shared__ __align__(16) uint8_t s_ct[kPrefillWarps][kGroup * D];
-  __shared__ __align__(16) __half s_vm[kPrefillWarps][2 * D];
-  __shared__ __align__(16) float s_vinv[kPrefillWarps][D];
+  extern __shared__ __align__(16) uint8_t s_stage[];  // StagedTile<D>::BYTES per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z, h = blockIdx.y;
   const int item = blockIdx.x * kPrefillWarps + warp;
@@ -52,11 +169,10 @@ prefill_kernel(const __grid_constant__ PrefillParams p) {
   if (item < ng) {
     using T = Tile<D, BITS>;
     const size_t gi = bh * p.max_groups + item;
-    quantize_tile_warp<D, BITS>(kseq + (int64_t)item * kGroup * p.st,
-                                vseq + (int64_t)item * kGroup * p.st, p.st,
-                                p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
-                                p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D, s_ct[warp],
-                                s_vm[warp], s_vinv[warp], lane);
+    quantize_tile_staged<D, BITS, VEC>(kseq + (int64_t)item * kGroup * p.st, vseq + (int64_t)item * kGroup * p.st,
+                                       p.st, p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
+                                       p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D,
+                                       s_stage + warp * StagedTile<D>::BYTES, lane);
   } else if (item < ng + (nt + kGroup - 1) / kGroup) {
     // copy tail tokens [nq + 32c, nq + 32c + 32) to ring slots 32c.. (ring head 0)
     const int c = item - ng;
@@ -160,10 +276,25 @@ kvq_status dispatch_db(int d, int bits, A&&... args) {
 
 template <int D, int BITS>
 struct PrefillLaunch {
+  template <int VEC>
+  static kvq_status launch(const PrefillParams& p, dim3 grid, cudaStream_t s) {
+    constexpr int smem = kPrefillWarps * StagedTile<D>::BYTES;
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(prefill_kernel<D, BITS, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return KVQ_ERR_CUDA;
+      attr = true;
+    }
+    prefill_kernel<D, BITS, VEC><<<grid, kPrefillWarps * 32, smem, s>>>(p);
+    return launch_status();
+  }
   static kvq_status run(const PrefillParams& p, int batch, int max_items, cudaStream_t s) {
     dim3 grid((max_items + kPrefillWarps - 1) / kPrefillWarps, p.hkv, batch);
-    prefill_kernel<D, BITS><<<grid, kPrefillWarps * 32, 0, s>>>(p);
-    return launch_status();
+    // 16-byte copies when every row start is 16-byte aligned, else 8-byte copies
+    const bool a16 = ((uintptr_t)p.k % 16 == 0) && ((uintptr_t)p.v % 16 == 0) && p.sb % 8 == 0 &&
+                     p.st % 8 == 0 && p.sh % 8 == 0;
+    return a16 ? launch<16>(p, grid, s) : launch<8>(p, grid, s);
   }
 };
 

@@ -116,6 +116,24 @@ def test_strided_inputs():
     H.assert_buffers_equal(cache, H.oracle_states(inp, 4))
 
 
+def test_inputs_only_8_byte_aligned():
+    # rows that start on 8-byte but not 16-byte boundaries (a 4-element offset and a
+    # head stride of 132 elements): the prefill stages them with 8-byte copies
+    w = S.LLAMA31_8B_128K.scaled(n_q_heads=8, n_kv_heads=2, context=288, n_tail=32)
+    inp = S.generate(w)
+    flat_k = torch.zeros(288 * 2 * 132 + 8, dtype=torch.float16, device="cuda")
+    flat_v = torch.zeros_like(flat_k)
+    big_k = flat_k[4:4 + 288 * 2 * 132].view(1, 288, 2, 132)
+    big_v = flat_v[4:4 + 288 * 2 * 132].view(1, 288, 2, 132)
+    big_k[..., :128] = torch.from_numpy(inp["K"]).cuda()
+    big_v[..., :128] = torch.from_numpy(inp["V"]).cuda()
+    k, v = big_k[..., :128], big_v[..., :128]
+    assert k.data_ptr() % 16 == 8 and k.stride(2) % 8 == 4
+    cache = H.device_cache(w, inp, 2, k=k, v=v)
+    torch.cuda.synchronize()
+    H.assert_buffers_equal(cache, H.oracle_states(inp, 2))
+
+
 @pytest.mark.parametrize("bits,R", [(2, 32), (4, 64)])
 def test_append_flush_matches_oracle(bits, R):
     # prefill, then append tokens one at a time across several flushes; after
