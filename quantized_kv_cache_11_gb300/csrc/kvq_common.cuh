@@ -25,10 +25,10 @@ struct GroupParams {
   float inv;    // fp32 reciprocal of scale (round to nearest), 0 when scale is 0
 };
 
-template <int BITS>
-__device__ __forceinline__ GroupParams group_params(float mn, float mx) {
+// levels = 2^b - 1 (3, 15 or 255: exact in fp32)
+__device__ __forceinline__ GroupParams group_params_levels(float mn, float mx, float levels) {
   const float rng = __fsub_rn(mx, mn);
-  const float sc = __fdiv_rn(rng, (float)((1 << BITS) - 1));
+  const float sc = __fdiv_rn(rng, levels);
   GroupParams p;
   p.scale_h = __float2half_rn(sc);
   p.zero_h = __float2half_rn(mn);  // exact: mn is an fp16 value
@@ -38,6 +38,11 @@ __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
   if (p.zero == 0.f) { p.zero_h = __float2half_rn(0.f); p.zero = 0.f; }
   p.inv = p.scale == 0.f ? 0.f : __frcp_rn(p.scale);
   return p;
+}
+
+template <int BITS>
+__device__ __forceinline__ GroupParams group_params(float mn, float mx) {
+  return group_params_levels(mn, mx, (float)((1 << BITS) - 1));
 }
 
 // code = clamp(rint(fl(d / scale))), d = fl(x - zero), every op round-to-nearest.
@@ -52,8 +57,8 @@ __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
 // and its low mantissa bits are that number.
 constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
 constexpr uint32_t kRoundMagicBits = 0x4B400000u;
-template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, const GroupParams& p) {
+// The code clamped to [0, cmax] (cmax = 2^b - 1).
+__device__ __forceinline__ uint32_t quant_code_levels(float x, const GroupParams& p, uint32_t cmax) {
   if (p.scale == 0.f) return 0u;
   const float d = __fsub_rn(x, p.zero);  // >= 0
   float q = __fmul_rn(d, p.inv);
@@ -63,7 +68,12 @@ __device__ __forceinline__ uint32_t quant_code(float x, const GroupParams& p) {
     t = __fadd_rn(q, kRoundMagic);
   }
   const uint32_t c = __float_as_uint(t) - kRoundMagicBits;
-  return c > (1u << BITS) - 1 ? (1u << BITS) - 1 : c;
+  return c > cmax ? cmax : c;
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t quant_code(float x, const GroupParams& p) {
+  return quant_code_levels(x, p, (1u << BITS) - 1);
 }
 
 // ---------------------------------------------------------------------------

@@ -28,8 +28,9 @@ struct PrefillParams {
   int32_t ntail[KVQ_MAX_BATCH];
 };
 
-// One warp quantizes one 32-token tile of keys and values whose rows it first
-// stages in shared memory (cp.async, VEC bytes per copy).  Keys: each lane owns
+// One warp quantizes one 32-token tile of keys and values whose rows it stages in
+// shared memory (cp.async, VEC bytes per copy; keys first, then the values in the
+// same buffer, so that twice as many warps fit an SM).  Keys: each lane owns
 // D/32 channels (fp16 min/max over the 32 rows, then the codes); values: lane t
 // owns token t (min/max and parameters of its D/32 groups, then the codes).  The
 // codes go through a staging tile at a padded pitch (no bank conflicts) and are
@@ -39,7 +40,7 @@ struct StagedTile {
   static constexpr int PH = D + 8;   // halves per staged row (16-byte aligned rows)
   static constexpr int PC = D + 8;   // bytes per row of the code staging tile
   static constexpr int ROWS = kGroup * PH * 2;
-  static constexpr int BYTES = 2 * ROWS + kGroup * PC + 8 * D;  // K rows, V rows, codes, key + value meta
+  static constexpr int BYTES = ROWS + kGroup * PC + 8 * D;  // rows (keys, then values), codes, key + value meta
 };
 
 template <int D, int BITS, int VEC>
@@ -48,26 +49,23 @@ __device__ __forceinline__ void quantize_tile_staged(const __half* ksrc, const _
                                                      __half* vmeta_dst, uint8_t* ws, int lane) {
   using S = StagedTile<D>;
   __half* kr = reinterpret_cast<__half*>(ws);
-  __half* vr = reinterpret_cast<__half*>(ws + S::ROWS);
-  uint8_t* ct = ws + 2 * S::ROWS;
-  __half* km = reinterpret_cast<__half*>(ws + 2 * S::ROWS + kGroup * S::PC);
+  __half* vr = kr;  // the value rows replace the key rows
+  uint8_t* ct = ws + S::ROWS;
+  __half* km = reinterpret_cast<__half*>(ws + S::ROWS + kGroup * S::PC);
   __half* vm = km + 2 * D;
-  // ---- stage the 32 key rows and the 32 value rows
   constexpr int CPR = 2 * D / VEC;  // copies per row
+  auto stage = [&](__half* dst, const __half* src) {
 #pragma unroll 4
-  for (int e = lane; e < kGroup * CPR; e += 32) {
-    const int t = e / CPR, ch = e % CPR;
-    if (VEC == 16) {
-      cp_async_16(kr + t * S::PH + ch * 8, ksrc + (int64_t)t * tstride + ch * 8);
-      cp_async_16(vr + t * S::PH + ch * 8, vsrc + (int64_t)t * tstride + ch * 8);
-    } else {
-      cp_async_8(kr + t * S::PH + ch * 4, ksrc + (int64_t)t * tstride + ch * 4);
-      cp_async_8(vr + t * S::PH + ch * 4, vsrc + (int64_t)t * tstride + ch * 4);
+    for (int e = lane; e < kGroup * CPR; e += 32) {
+      const int t = e / CPR, ch = e % CPR;
+      if (VEC == 16) cp_async_16(dst + t * S::PH + ch * 8, src + (int64_t)t * tstride + ch * 8);
+      else cp_async_8(dst + t * S::PH + ch * 4, src + (int64_t)t * tstride + ch * 4);
     }
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncwarp();
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncwarp();
+  };
+  stage(kr, ksrc);  // ---- the 32 key rows
   // ---- keys: per channel over the 32 tokens; lane owns channels [c0, c0 + CPL)
   {
     constexpr int CPL = D / 32, NH = CPL / 2;  // channels, half2 pairs per lane
@@ -111,6 +109,7 @@ __device__ __forceinline__ void quantize_tile_staged(const __half* ksrc, const _
   pack_store_tile<D, BITS, true, S::PC>(ct, kcodes_dst, lane);
   store_meta_lane_order<D, true>(km, kmeta_dst, lane);
   __syncwarp();
+  stage(vr, vsrc);  // ---- the 32 value rows
   // ---- values: per token over 32-channel groups; lane t owns token t
   {
     const int t = lane;

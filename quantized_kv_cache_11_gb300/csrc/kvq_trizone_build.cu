@@ -169,17 +169,19 @@ __global__ void __launch_bounds__(kIndexThreads) index_kernel(const __grid_const
 }
 
 // Stage up to 32 fp16 rows (row t of token tok(t), t < n; zero rows after) into
-// rows[32][128].  Each lane moves 4 channels (8 bytes) of every row.
+// rows[32][128]: every lane issues an 8-byte asynchronous copy of 4 channels of
+// every row, then waits for all of them.
 template <typename TokOf>
 __device__ __forceinline__ void stage_rows(__half* rows, const __half* base, int64_t st, int n, TokOf tok_of,
                                            int lane) {
-#pragma unroll 4
+#pragma unroll 8
   for (int t = 0; t < kGroup; ++t) {
     const int tok = tok_of(t);
-    uint2 x = make_uint2(0u, 0u);
-    if (t < n) x = *reinterpret_cast<const uint2*>(base + (int64_t)tok * st + 4 * lane);
-    *reinterpret_cast<uint2*>(rows + t * kDim + 4 * lane) = x;
+    if (t < n) cp_async_8(rows + t * kDim + 4 * lane, base + (int64_t)tok * st + 4 * lane);
+    else *reinterpret_cast<uint2*>(rows + t * kDim + 4 * lane) = make_uint2(0u, 0u);
   }
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncwarp();
 }
 
@@ -290,19 +292,39 @@ __device__ __forceinline__ void quantize_values(const __half* rows, int n, uint8
   __syncwarp();
 }
 
-template <int C>
-__device__ __forceinline__ void key_channel(const __half* rows, int n, int d, int slot, uint8_t* ct, __half* ksc,
-                                            __half* kze) {
-  float mn = __half2float(rows[d]), mx = mn;
+// The lane's 4 key channels d0..d0+3 over the block's n tokens, each at its own
+// width: fp16 min/max on half2, then the parameters and the codes (to ct at the
+// channels' slots).
+__device__ __forceinline__ void key_channels(const __half* rows, int n, int d0, const uint8_t* slot_of,
+                                             const uint8_t* kw, uint8_t* ct, __half* ksc, __half* kze) {
+  __half2 mn0 = *reinterpret_cast<const __half2*>(rows + d0), mn1 = *reinterpret_cast<const __half2*>(rows + d0 + 2);
+  __half2 mx0 = mn0, mx1 = mn1;
   for (int t = 1; t < n; ++t) {
-    const float x = __half2float(rows[t * kDim + d]);
-    mn = fminf(mn, x);
-    mx = fmaxf(mx, x);
+    const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + d0);
+    const __half2 a = u32_as_h2(raw.x), b = u32_as_h2(raw.y);
+    mn0 = __hmin2(mn0, a); mx0 = __hmax2(mx0, a);
+    mn1 = __hmin2(mn1, b); mx1 = __hmax2(mx1, b);
   }
-  const GroupParams g = group_params<C>(mn, mx);
-  ksc[slot] = g.scale_h;
-  kze[slot] = g.zero_h;
-  for (int t = 0; t < n; ++t) ct[t * kSlots + slot] = (uint8_t)quant_code<C>(__half2float(rows[t * kDim + d]), g);
+  const float mns[4] = {__low2float(mn0), __high2float(mn0), __low2float(mn1), __high2float(mn1)};
+  const float mxs[4] = {__low2float(mx0), __high2float(mx0), __low2float(mx1), __high2float(mx1)};
+  GroupParams g[4];
+  uint32_t cmax[4];
+  int slot[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    cmax[i] = (1u << kw[d0 + i]) - 1u;
+    g[i] = group_params_levels(mns[i], mxs[i], (float)cmax[i]);
+    slot[i] = slot_of[d0 + i];
+    ksc[slot[i]] = g[i].scale_h;
+    kze[slot[i]] = g[i].zero_h;
+  }
+  for (int t = 0; t < n; ++t) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + d0);
+    const float x[4] = {__low2float(u32_as_h2(raw.x)), __high2float(u32_as_h2(raw.x)), __low2float(u32_as_h2(raw.y)),
+                        __high2float(u32_as_h2(raw.y))};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ct[t * kSlots + slot[i]] = (uint8_t)quant_code_levels(x[i], g[i], cmax[i]);
+  }
 }
 
 // grid (ceil(items / kBlockWarps), Hkv, B); one warp per block record.
@@ -364,15 +386,7 @@ __global__ void __launch_bounds__(kBlockWarps * 32) block_kernel(const __grid_co
     kze[i] = __float2half_rn(0.f);
   }
   stage_rows(rows, kseq, p.st, n, tok, lane);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int d = 4 * lane + i, slot = s_slot_of[d];
-    switch (s_kw[d]) {
-      case 2: key_channel<2>(rows, n, d, slot, ct, ksc, kze); break;
-      case 4: key_channel<4>(rows, n, d, slot, ct, ksc, kze); break;
-      default: key_channel<8>(rows, n, d, slot, ct, ksc, kze); break;
-    }
-  }
+  key_channels(rows, n, 4 * lane, s_slot_of, s_kw, ct, ksc, kze);
   __syncwarp();
   const int kt2 = s_hdr[H_KT], kt4 = s_hdr[H_KT + 1], kt8 = s_hdr[H_KT + 2], KT = kt2 + kt4 + kt8;
   store_key_subtile<2>(ct, 0, kt2, dst, lane);
