@@ -161,37 +161,49 @@ def decode_attention(q16: np.ndarray, keys: np.ndarray, values: np.ndarray,
 # Uniform cache state: tokens [0, n_quant) quantized in 32-token groups, tokens
 # [n_quant, n_quant + n_tail) kept fp16 (article, paragraph 8).
 # ---------------------------------------------------------------------------
-def split_sequence(seq_len: int, n_tail: int):
-    n_quant = seq_len - n_tail
+def split_sequence(seq_len: int, n_tail: int, n_sink_cap: int = 0):
+    """(n_sink, n_quant) of a sequence: the first min(n_sink_cap, seq_len) tokens
+    are sinks, the last n_tail tokens the tail, the rest whole 32-token groups."""
+    n_sink = min(n_sink_cap, seq_len)
+    n_quant = seq_len - n_sink - n_tail
     if n_quant < 0 or n_quant % GROUP:
         raise ValueError("quantized region must be a whole number of 32-token groups")
-    return n_quant
+    return n_sink, n_quant
 
 
 def quantize_sequence(k16: np.ndarray, v16: np.ndarray, seq_len: int, n_tail: int,
-                      bits: int) -> dict:
+                      bits: int, n_sink_cap: int = 0) -> dict:
     """One sequence.  k16/v16: float16 [T, Hkv, D] (T >= seq_len).
-    Returns per-head arrays (leading axis Hkv)."""
-    n_quant = split_sequence(seq_len, n_tail)
+    Returns per-head arrays (leading axis Hkv).
+
+    Attention sinks ("KV-cache quantization axes", ihal.it, paragraph 11: high-
+    precision windows for the recent tokens and for the attention sinks): with
+    n_sink_cap > 0 the first min(n_sink_cap, seq_len) tokens stay fp16 and the
+    quantized groups start after them."""
+    n_sink, n_quant = split_sequence(seq_len, n_tail, n_sink_cap)
     k = np.ascontiguousarray(np.swapaxes(k16[:seq_len], 0, 1))  # [Hkv, T, D]
     v = np.ascontiguousarray(np.swapaxes(v16[:seq_len], 0, 1))
-    kc, ks, kz = quantize_keys(k[:, :n_quant], bits)
-    vc, vs, vz = quantize_values(v[:, :n_quant], bits)
+    q0, q1 = n_sink, n_sink + n_quant
+    kc, ks, kz = quantize_keys(k[:, q0:q1], bits)
+    vc, vs, vz = quantize_values(v[:, q0:q1], bits)
     return {
-        "bits": bits, "n_quant": n_quant, "n_tail": n_tail,
+        "bits": bits, "n_quant": n_quant, "n_tail": n_tail, "n_sink": n_sink,
         "k_codes": kc, "k_scale": ks, "k_zero": kz,
         "v_codes": vc, "v_scale": vs, "v_zero": vz,
-        "k_tail": k[:, n_quant:seq_len], "v_tail": v[:, n_quant:seq_len],
+        "k_tail": k[:, q1:seq_len], "v_tail": v[:, q1:seq_len],
+        "k_sink": k[:, :n_sink], "v_sink": v[:, :n_sink],
     }
 
 
 def sequence_kv(state: dict):
-    """Dequantized keys and values of a sequence, float64 [Hkv, n, D]: the
-    quantized region followed by the fp16 tail (exact in float64)."""
+    """Dequantized keys and values of a sequence, float64 [Hkv, n, D]: the fp16
+    sinks, the quantized region, then the fp16 tail (exact in float64)."""
     kq = dequantize_keys(state["k_codes"], state["k_scale"], state["k_zero"])
     vq = dequantize_values(state["v_codes"], state["v_scale"], state["v_zero"])
-    keys = np.concatenate([kq, state["k_tail"].astype(F64)], axis=1)
-    values = np.concatenate([vq, state["v_tail"].astype(F64)], axis=1)
+    ks = state.get("k_sink", kq[:, :0]).astype(F64)
+    vs = state.get("v_sink", vq[:, :0]).astype(F64)
+    keys = np.concatenate([ks, kq, state["k_tail"].astype(F64)], axis=1)
+    values = np.concatenate([vs, vq, state["v_tail"].astype(F64)], axis=1)
     return keys, values
 
 
@@ -208,6 +220,15 @@ def append_lengths(n_quant: int, n_tail: int, tail_cap: int):
         n_quant += GROUP
         n_tail -= GROUP
     return n_quant, n_tail + 1, flushed
+
+
+def append_lengths_sink(n_sink: int, n_quant: int, n_tail: int, sink_cap: int, tail_cap: int):
+    """Lengths after appending one token with a sink window: the token is a sink
+    while fewer than sink_cap tokens have arrived, else as append_lengths."""
+    if n_sink < sink_cap:
+        return n_sink + 1, n_quant, n_tail
+    n_quant, n_tail, _ = append_lengths(n_quant, n_tail, tail_cap)
+    return n_sink, n_quant, n_tail
 
 
 # ---------------------------------------------------------------------------

@@ -589,3 +589,55 @@ def test_trizone_pack_index_and_stream():
     assert (kt[:8] == k[732:740].view(np.uint16)).all() and (kt[8:] == 0).all()
     vt = O.unpack_tiles(fb[8192:], "V", 128, 16)
     assert (vt[:8] == v[732:740].view(np.uint16)).all() and (vt[8:] == 0).all()
+
+
+# ------------------------------------------------------------- attention sinks
+def _sink_inp(T=200, H=2, seed=11):
+    w = S.LLAMA31_8B_128K.scaled(n_q_heads=4 * H, n_kv_heads=H, context=T, seed=seed)
+    return w, S.generate(w)
+
+
+def test_sink_zero_is_the_plain_cache():
+    w, inp = _sink_inp(T=160)
+    a = O.quantize_sequence(inp["K"][0], inp["V"][0], 160, 32, 2)
+    b = O.quantize_sequence(inp["K"][0], inp["V"][0], 160, 32, 2, n_sink_cap=0)
+    assert b["n_sink"] == 0 and (a["k_codes"] == b["k_codes"]).all()
+    np.testing.assert_array_equal(O.sequence_attention(inp["q"][0], a, w.sm_scale),
+                                  O.sequence_attention(inp["q"][0], b, w.sm_scale))
+
+
+def test_sink_rows_are_exact_and_groups_start_after_them():
+    # 4 sinks, 128 quantized tokens, 20 tail tokens: the groups are those of a
+    # plain cache over tokens [4, 152), the sinks the fp16 rows themselves
+    w, inp = _sink_inp(T=152)
+    st = O.quantize_sequence(inp["K"][0], inp["V"][0], 152, 20, 4, n_sink_cap=4)
+    assert (st["n_sink"], st["n_quant"], st["n_tail"]) == (4, 128, 20)
+    plain = O.quantize_sequence(inp["K"][0][4:], inp["V"][0][4:], 148, 20, 4)
+    for f in ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero"):
+        assert (st[f].view(np.uint8) == plain[f].view(np.uint8)).all(), f
+    keys, values = O.sequence_kv(st)
+    k0 = np.swapaxes(inp["K"][0][:4], 0, 1).astype(np.float64)
+    assert (keys[:, :4] == k0).all()
+
+
+def test_all_sink_sequence_is_exact_attention():
+    # fewer tokens than the sink window: everything stays fp16, attention = SDPA
+    w, inp = _sink_inp(T=40)
+    st = O.quantize_sequence(inp["K"][0], inp["V"][0], 24, 0, 2, n_sink_cap=32)
+    assert (st["n_sink"], st["n_quant"], st["n_tail"]) == (24, 0, 0)
+    k = np.swapaxes(inp["K"][0][:24], 0, 1).astype(np.float64)
+    v = np.swapaxes(inp["V"][0][:24], 0, 1).astype(np.float64)
+    ref = _sdpa64(inp["q"][0], np.repeat(k, 4, 0), np.repeat(v, 4, 0), w.sm_scale)
+    np.testing.assert_allclose(O.sequence_attention(inp["q"][0], st, w.sm_scale), ref, atol=1e-12)
+
+
+def test_append_with_sinks_fills_the_window_then_the_tail():
+    # after n tokens: min(n, S) sinks, and the plain append state of the rest
+    S_, R = 5, 32
+    state = (0, 0, 0)
+    plain = (0, 0)
+    for n in range(1, 200):
+        state = O.append_lengths_sink(*state, S_, R)
+        if n > S_:
+            plain = O.append_lengths(*plain, R)[:2]
+        assert state == (min(n, S_),) + plain, n
