@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
+    ap.add_argument("--sink", type=int, default=0,
+                    help="uniform cache: keep the first S tokens fp16 (attention-sink window)")
     ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone"],
                     help="uniform: the 128k-token uniform cache (default); trizone: the "
                          "mixed-width cache, 4 sequences x 65,408 old + 128 fresh tokens")
@@ -52,21 +54,35 @@ def workload(bits):
     return S.LLAMA31_8B_128K if bits == 2 else S.LLAMA31_8B_128K_4BIT
 
 
-def algorithmic_bytes(w, n_quant, n_tail) -> int:
+def algorithmic_bytes(w, n_quant, n_tail, n_sink=0) -> int:
     """Bytes one decode step must move: packed K/V codes, fp16 scale + zero of
-    every group, the fp16 tail, q in and the fp32 output."""
+    every group, the fp16 tail and sink tokens, q in and the fp32 output."""
     D, H, b = w.head_dim, w.n_kv_heads, w.bits
     per_tok = 2 * D * b // 8 + (2 * D // 32) * 2  # codes K+V, V meta (fp16 scale + zero per 32 ch)
     k_meta = (n_quant // 32) * 2 * D * 2  # per key group: scale + zero per channel
-    tail = n_tail * D * 2 * 2
-    return w.batch * H * (n_quant * per_tok + k_meta + tail) + w.batch * w.n_q_heads * D * (2 + 4)
+    fp16 = (n_tail + n_sink) * D * 2 * 2
+    return w.batch * H * (n_quant * per_tok + k_meta + fp16) + w.batch * w.n_q_heads * D * (2 + 4)
 
 
-def prefill_algorithmic_bytes(w, n_quant, n_tail) -> int:
+def with_sink(inp, sink):
+    """The workload's tail shortened so that the tokens after an S-token sink
+    window still end in whole groups (the quantized region keeps its length)."""
+    if sink == 0:
+        return inp
+    L = inp["seq_len"].astype(int)
+    ns = np.minimum(sink, L)
+    nq = np.maximum(0, -(-(L - ns - inp["n_tail"]) // 32) * 32)
+    nt = L - ns - nq
+    if (nt < 0).any():
+        raise ValueError("the sink window does not fit the workload's tail")
+    return dict(inp, n_tail=nt.astype(np.int32))
+
+
+def prefill_algorithmic_bytes(w, n_quant, n_tail, n_sink=0) -> int:
     """Prefill reads the fp16 K and V of every token and writes the packed cache
-    (codes and fp16 metadata) plus the fp16 tail."""
-    read = 2 * w.batch * (n_quant + n_tail) * w.n_kv_heads * w.head_dim * 2
-    write = algorithmic_bytes(w, n_quant, n_tail) - w.batch * w.n_q_heads * w.head_dim * 6
+    (codes and fp16 metadata) plus the fp16 tail and sinks."""
+    read = 2 * w.batch * (n_quant + n_tail + n_sink) * w.n_kv_heads * w.head_dim * 2
+    write = algorithmic_bytes(w, n_quant, n_tail, n_sink) - w.batch * w.n_q_heads * w.head_dim * 6
     return read + write
 
 
@@ -138,14 +154,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, inp, budget_s=12.0):
+def cpu_baseline(w, inp, budget_s=12.0, sink=0):
     """The oracle as it stands on this host: dequantize + fp64 attention for one
     KV head (its 4 query heads) over the whole context, repeated for ~budget_s,
     scaled by the number of KV heads to one full decode step."""
     from oracle import kvq_oracle as O
     import torch
     st = O.quantize_sequence(inp["K"][0][:, :1], inp["V"][0][:, :1], int(inp["seq_len"][0]),
-                             int(inp["n_tail"][0]), w.bits)
+                             int(inp["n_tail"][0]), w.bits, n_sink_cap=sink)
     q = inp["q"][0][:w.gqa]
     times = []
     t_end = time.perf_counter() + budget_s
@@ -357,8 +373,9 @@ def main():
     kvq.load_library()
 
     w = workload(args.bits)
-    inp = S.generate(w)
-    n_quant = int(inp["seq_len"][0] - inp["n_tail"][0])
+    inp = with_sink(S.generate(w), args.sink)
+    n_sink = min(args.sink, int(inp["seq_len"][0]))
+    n_quant = int(inp["seq_len"][0] - inp["n_tail"][0]) - n_sink
     n_tail = int(inp["n_tail"][0])
     K = torch.from_numpy(inp["K"]).to(dev)
     V = torch.from_numpy(inp["V"]).to(dev)
@@ -366,10 +383,11 @@ def main():
 
     # ---- cache replicas: total well above the 129 MB L2
     probe = kvq.QuantizedKVCache(w.batch, w.n_kv_heads, w.head_dim, w.bits, w.context, w.tail_cap,
-                                 device=dev)
+                                 device=dev, sink_cap=args.sink)
     n_rep = max(4, math.ceil(3 * 128e6 / probe.nbytes) + 1)
     caches = [probe] + [kvq.QuantizedKVCache(w.batch, w.n_kv_heads, w.head_dim, w.bits, w.context,
-                                             w.tail_cap, device=dev) for _ in range(n_rep - 1)]
+                                             w.tail_cap, device=dev, sink_cap=args.sink)
+                        for _ in range(n_rep - 1)]
     stream = torch.cuda.current_stream(dev)
     # prefill timing (first replica, repeated), then fill every replica
     pre_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -382,11 +400,11 @@ def main():
     pre_ev[1].record()
     torch.cuda.synchronize()
     prefill_us = pre_ev[0].elapsed_time(pre_ev[1]) * 1000 / 5
-    prefill_bytes = prefill_algorithmic_bytes(w, n_quant, n_tail)
+    prefill_bytes = prefill_algorithmic_bytes(w, n_quant, n_tail, n_sink)
 
     # ---- append timing on a separate cache (keeps the replicas unchanged)
     app = kvq.QuantizedKVCache(w.batch, w.n_kv_heads, w.head_dim, w.bits, w.context + 4096,
-                               w.tail_cap, device=dev)
+                               w.tail_cap, device=dev, sink_cap=args.sink)
     app.prefill(K, V, inp["seq_len"].tolist(), inp["n_tail"].tolist())
     kn = torch.randn(w.batch, w.n_kv_heads, w.head_dim, device=dev).half()
     vn = torch.randn(w.batch, w.n_kv_heads, w.head_dim, device=dev).half()
@@ -413,7 +431,7 @@ def main():
     if rank == 0:
         from oracle import kvq_oracle as O
         st = O.quantize_sequence(inp["K"][0][:, :1], inp["V"][0][:, :1], int(inp["seq_len"][0]),
-                                 n_tail, w.bits)
+                                 n_tail, w.bits, n_sink_cap=args.sink)
         ref = O.sequence_attention(inp["q"][0][:w.gqa], st, w.sm_scale)
         got = outs[0][0, :w.gqa].double().cpu().numpy()
         parity = {"kv_heads_checked": 1, "max_abs": float(np.abs(got - ref).max())}
@@ -433,16 +451,16 @@ def main():
             dist.destroy_process_group()
         return
     peak, peak_kind = load_peaks()
-    nbytes = algorithmic_bytes(w, n_quant, n_tail)
+    nbytes = algorithmic_bytes(w, n_quant, n_tail, n_sink)
     achieved = nbytes / (us_step * 1e-6) / 1e9
-    traffic = read_traffic("decode_traffic.txt", w.name, _kernel_sha())
+    traffic = None if args.sink else read_traffic("decode_traffic.txt", w.name, _kernel_sha())
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.context,
-                   "n_quant": n_quant, "n_tail": n_tail, "bits": w.bits, "group": 32,
+                   "n_quant": n_quant, "n_tail": n_tail, "n_sink": n_sink, "bits": w.bits, "group": 32,
                    "l2": f"inputs larger than L2: {n_rep} cache replicas "
                          f"({n_rep * probe.nbytes / 1e6:.0f} MB) rotated every step",
                    "launch": "CUDA graph of kvq_decode_attn calls"},
@@ -458,7 +476,7 @@ def main():
         "parity_sample": parity,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inp)
+        line["cpu_baseline"] = cpu_baseline(w, inp, sink=args.sink)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

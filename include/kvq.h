@@ -90,9 +90,17 @@ typedef enum {
  *   n_tail    int32 [B]  tokens in the tail, 0..R
  *   tail_head int32 [B]  ring slot of the oldest tail token (multiple of 32)
  *   error_flags int32 [1] or NULL: device error bits (KVQ_DEVERR_*)
- * The n_quant / n_tail / tail_head arrays are written by kvq_quantize_prefill and
- * kvq_append_token and read by kvq_decode_attn, all on the device, so a decode
- * loop needs no host synchronisation.
+ *   sink_cap  S, attention-sink window (same article, paragraph 11: high-precision
+ *             windows for the recent tokens and for the attention sinks): the
+ *             first min(S, length) tokens of a sequence stay fp16 and the
+ *             quantized groups start after them; 0..256, 0 = no window (the sink
+ *             pointers may then be NULL)
+ *   k_sink    fp16  [B][Hkv][S][D]   sink token i of a sequence at row i
+ *   v_sink    fp16  [B][Hkv][S][D]
+ *   n_sink    int32 [B]  sink tokens held, 0..S
+ * The n_quant / n_tail / tail_head / n_sink arrays are written by
+ * kvq_quantize_prefill and kvq_append_token and read by kvq_decode_attn, all on
+ * the device, so a decode loop needs no host synchronisation.
  *
  * Packed tile layout.  A tile's codes are split among 32 "lanes" (gid = lane/4,
  * tig = lane%4), each owning D/2 pairs of codes in this order:
@@ -131,6 +139,10 @@ typedef struct kvq_cache {
   int32_t* n_tail;
   int32_t* tail_head;
   int32_t* error_flags;
+  int32_t sink_cap;
+  void* k_sink;
+  void* v_sink;
+  int32_t* n_sink;
 } kvq_cache;
 
 /* Index of each buffer in the sizes[] array of kvq_cache_bytes. */
@@ -141,7 +153,9 @@ enum {
   KVQ_BUF_V_META,
   KVQ_BUF_K_TAIL,
   KVQ_BUF_V_TAIL,
-  KVQ_BUF_LENGTHS, /* one int32 [B] array (n_quant, n_tail and tail_head each need one) */
+  KVQ_BUF_LENGTHS, /* one int32 [B] array (n_quant, n_tail, tail_head and n_sink each need one) */
+  KVQ_BUF_K_SINK,
+  KVQ_BUF_V_SINK,
   KVQ_NBUF
 };
 
@@ -165,12 +179,14 @@ kvq_status kvq_cache_bytes(const kvq_cache* cache, size_t sizes[KVQ_NBUF]);
  *             and k, v 8-byte aligned.
  *   seq_len   HOST int32 [batch]: tokens of sequence s (0 allowed)
  *   n_tail    HOST int32 [batch]: how many of the newest tokens stay fp16;
- *             seq_len[s] - n_tail[s] must be a multiple of 32, n_tail[s] <= R.
- * Tokens [0, seq_len - n_tail) are quantized (keys per channel over 32-token
- * spans, values per token over 32-channel spans) and tokens
+ *             seq_len[s] - min(S, seq_len[s]) - n_tail[s] must be a multiple of
+ *             32 and >= 0, n_tail[s] <= R.
+ * Tokens [0, min(S, seq_len)) are copied to the sink rows, tokens
+ * [min(S, seq_len), seq_len - n_tail) are quantized (keys per channel over
+ * 32-token spans, values per token over 32-channel spans) and tokens
  * [seq_len - n_tail, seq_len) are copied to tail slots 0.. (tail_head = 0).
- * Sets n_quant / n_tail / tail_head on the device.  batch <= KVQ_MAX_BATCH.
- * KVQ_ERR_CAPACITY if a quantized region exceeds max_groups.
+ * Sets n_quant / n_tail / tail_head / n_sink on the device.  batch <=
+ * KVQ_MAX_BATCH.  KVQ_ERR_CAPACITY if a quantized region exceeds max_groups.
  */
 kvq_status kvq_quantize_prefill(const kvq_cache* cache, const void* k, const void* v,
                                 int64_t stride_b, int64_t stride_t, int64_t stride_h,
@@ -183,11 +199,13 @@ kvq_status kvq_quantize_prefill(const kvq_cache* cache, const void* k, const voi
  * and quantized in groups once enough of them have arrived).
  *
  *   k_new, v_new  fp16 device [batch][Hkv][D], contiguous, 8-byte aligned.
- * For every sequence, if its tail holds R tokens the oldest 32 are first
- * quantized as key group n_quant/32 and value rows n_quant..n_quant+31
- * (n_quant += 32, tail_head advances by 32); then the new token is written
- * to the tail.  If that flush would pass max_groups, the sequence is left
- * unchanged and KVQ_DEVERR_APPEND_CAPACITY is set in *error_flags.
+ * For every sequence: while it holds fewer than S sink tokens, the new token
+ * becomes sink row n_sink (n_sink += 1).  Otherwise, if its tail holds R tokens
+ * the oldest 32 are first quantized as key group n_quant/32 and value rows
+ * n_quant..n_quant+31 (n_quant += 32, tail_head advances by 32); then the new
+ * token is written to the tail.  If that flush would pass max_groups, the
+ * sequence is left unchanged and KVQ_DEVERR_APPEND_CAPACITY is set in
+ * *error_flags.
  */
 kvq_status kvq_append_token(const kvq_cache* cache, const void* k_new, const void* v_new,
                             void* stream);
@@ -211,9 +229,9 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t n_q_heads,
  *   q         fp16 device [batch][Hq][D], contiguous; query head hq reads KV
  *             head hq / (Hq/Hkv)
  *   out       fp32 device [batch][Hq][D], 16-byte aligned:
- *             softmax(sm_scale * q.K_hat^T) . V_hat over
- *             the n_quant quantized tokens and the n_tail fp16 tail tokens of
- *             each sequence (all zeros for an empty sequence)
+ *             softmax(sm_scale * q.K_hat^T) . V_hat over the n_sink fp16
+ *             sink tokens, the n_quant quantized tokens and the n_tail fp16 tail
+ *             tokens of each sequence (all zeros for an empty sequence)
  *   sm_scale  softmax scale, typically 1/sqrt(D)
  *   workspace device scratch of kvq_decode_workspace_bytes bytes, 16-byte
  *             aligned, ZERO-FILLED before its first use; every call leaves it

@@ -14,6 +14,8 @@ extern "C" kvq_status kvq_cache_bytes(const kvq_cache* c, size_t sizes[KVQ_NBUF]
   sizes[KVQ_BUF_K_TAIL] = bh * (size_t)c->tail_cap * (size_t)c->head_dim * 2;
   sizes[KVQ_BUF_V_TAIL] = sizes[KVQ_BUF_K_TAIL];
   sizes[KVQ_BUF_LENGTHS] = (size_t)c->batch * sizeof(int32_t);
+  sizes[KVQ_BUF_K_SINK] = bh * (size_t)c->sink_cap * (size_t)c->head_dim * 2;
+  sizes[KVQ_BUF_V_SINK] = sizes[KVQ_BUF_K_SINK];
   return KVQ_OK;
 }
 

@@ -92,35 +92,40 @@ struct DecodeParams {
   const int32_t* n_quant;
   const int32_t* n_tail;
   const int32_t* tail_head;
+  const __half* k_sink;
+  const __half* v_sink;
+  const int32_t* n_sink;
   int32_t* error_flags;
   const __half* q;
   float* out;
   int32_t* counters;
   float* part;
   float scale_log2;
-  int32_t batch, hkv, max_groups, tail_cap;
+  int32_t batch, hkv, max_groups, tail_cap, sink_cap;
   int32_t n_stream;
 };
 
 // Lengths as the decode sees them; an inconsistent sequence counts as empty.
 struct SeqLen {
-  int nq, nt, th;
+  int nq, nt, th, ns;
 };
 __device__ __forceinline__ SeqLen read_lengths(const DecodeParams& p, int b, bool report) {
-  SeqLen s{p.n_quant[b], p.n_tail[b], p.tail_head[b]};
+  SeqLen s{p.n_quant[b], p.n_tail[b], p.tail_head[b], p.sink_cap > 0 ? p.n_sink[b] : 0};
   const bool ok = s.nq >= 0 && s.nq % kGroup == 0 && s.nq / kGroup <= p.max_groups && s.nt >= 0 &&
-                  s.nt <= p.tail_cap && s.th >= 0 && s.th < p.tail_cap && s.th % kGroup == 0;
+                  s.nt <= p.tail_cap && s.th >= 0 && s.th < p.tail_cap && s.th % kGroup == 0 && s.ns >= 0 &&
+                  s.ns <= p.sink_cap && (s.ns == p.sink_cap || (s.nq == 0 && s.nt == 0));
   if (!ok) {
     if (report && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_BAD_LENGTHS);
-    s = SeqLen{0, 0, 0};
+    s = SeqLen{0, 0, 0, 0};
   }
   return s;
 }
 
-// Work items of one (sequence, KV head): its groups, kTailWeight per tail chunk,
-// and at least one (an empty sequence still needs its zero output written).
+// Work items of one (sequence, KV head): its groups, kTailWeight per fp16 chunk
+// (tail chunks, then sink chunks), and at least one (an empty sequence still
+// needs its zero output written).
 __device__ __forceinline__ int seq_items(const SeqLen& s) {
-  const int n = s.nq / kGroup + kTailWeight * ((s.nt + kGroup - 1) / kGroup);
+  const int n = s.nq / kGroup + kTailWeight * ((s.nt + kGroup - 1) / kGroup + (s.ns + kGroup - 1) / kGroup);
   return n > 0 ? n : 1;
 }
 
@@ -733,14 +738,23 @@ decode_kernel(const DecodeParams p) {
       __syncwarp();
     }
     if (failed && lane == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
-    // tail chunks whose first weighted item falls in this warp's range
+    // fp16 chunks (tail, then sinks) whose first weighted item falls in this warp's range
+    const int ctail = (L.nt + kGroup - 1) / kGroup;
     for (int t = max(ia, ng); t < (failed ? 0 : ie); ++t) {
       const int u = t - ng;
       if (u % kTailWeight != 0) continue;
-      const int first = (u / kTailWeight) * kGroup;
-      if (first >= L.nt) continue;
-      dec.tail_chunk(wring, p.k_tail + (size_t)seg * R * D, p.v_tail + (size_t)seg * R * D, first,
-                     min(kGroup, L.nt - first), L.th, R, ps, p.scale_log2);
+      const int ci = u / kTailWeight;
+      if (ci < ctail) {
+        const int first = ci * kGroup;
+        dec.tail_chunk(wring, p.k_tail + (size_t)seg * R * D, p.v_tail + (size_t)seg * R * D, first,
+                       min(kGroup, L.nt - first), L.th, R, ps, p.scale_log2);
+      } else {
+        const int first = (ci - ctail) * kGroup;
+        if (first >= L.ns) continue;
+        const int S = p.sink_cap;
+        dec.tail_chunk(wring, p.k_sink + (size_t)seg * S * D, p.v_sink + (size_t)seg * S * D, first,
+                       min(kGroup, L.ns - first), 0, S, ps, p.scale_log2);
+      }
     }
     // warp partial into the warp's (now idle) ring slice, then the CTA merge
     dec.write_partial(reinterpret_cast<float*>(wring));
@@ -908,6 +922,9 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, con
   p.n_quant = c->n_quant;
   p.n_tail = c->n_tail;
   p.tail_head = c->tail_head;
+  p.k_sink = static_cast<const __half*>(c->k_sink);
+  p.v_sink = static_cast<const __half*>(c->v_sink);
+  p.n_sink = c->n_sink;
   p.error_flags = c->error_flags;
   p.q = static_cast<const __half*>(q);
   p.out = out;
@@ -919,6 +936,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, con
   p.hkv = c->n_kv_heads;
   p.max_groups = c->max_groups;
   p.tail_cap = c->tail_cap;
+  p.sink_cap = c->sink_cap;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->head_dim == 128) {
     if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, st);
@@ -999,6 +1017,9 @@ extern "C" kvq_status kvq_decode_attn_static(const kvq_cache* c, int32_t n_q_hea
   p.n_quant = c->n_quant;
   p.n_tail = c->n_tail;
   p.tail_head = c->tail_head;
+  p.k_sink = static_cast<const __half*>(c->k_sink);
+  p.v_sink = static_cast<const __half*>(c->v_sink);
+  p.n_sink = c->n_sink;
   p.error_flags = c->error_flags;
   p.q = static_cast<const __half*>(q);
   p.out = out;
@@ -1009,6 +1030,7 @@ extern "C" kvq_status kvq_decode_attn_static(const kvq_cache* c, int32_t n_q_hea
   p.hkv = c->n_kv_heads;
   p.max_groups = c->max_groups;
   p.tail_cap = c->tail_cap;
+  p.sink_cap = c->sink_cap;
   if (c->head_dim == 128) {
     if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, st);
     if (c->bits == 4) return decode_dispatch_g<128, 4>(G, p, st);

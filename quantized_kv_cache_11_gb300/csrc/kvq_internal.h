@@ -25,6 +25,7 @@ inline kvq_status validate_geometry(const kvq_cache* c) {
   // keep every buffer offset inside int64 and every grid dimension in range
   if ((int64_t)c->batch * c->n_kv_heads > (1 << 24)) return KVQ_ERR_UNSUPPORTED;
   if ((int64_t)c->max_groups > (1 << 26)) return KVQ_ERR_UNSUPPORTED;
+  if (c->sink_cap < 0 || c->sink_cap > 256) return KVQ_ERR_INVALID;
   return KVQ_OK;
 }
 
@@ -40,6 +41,11 @@ inline kvq_status validate_cache(const kvq_cache* c) {
   for (const void* p : lens)
     if (p == nullptr || !aligned(p, 4)) return KVQ_ERR_INVALID;
   if (c->error_flags != nullptr && !aligned(c->error_flags, 4)) return KVQ_ERR_INVALID;
+  if (c->sink_cap > 0) {
+    if (c->k_sink == nullptr || c->v_sink == nullptr || !aligned(c->k_sink, 16) || !aligned(c->v_sink, 16))
+      return KVQ_ERR_INVALID;
+    if (c->n_sink == nullptr || !aligned(c->n_sink, 4)) return KVQ_ERR_INVALID;
+  }
   return KVQ_OK;
 }
 

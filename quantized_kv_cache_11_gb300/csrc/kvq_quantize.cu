@@ -23,7 +23,10 @@ struct PrefillParams {
   int32_t* n_quant;
   int32_t* n_tail;
   int32_t* tail_head;
-  int32_t hkv, max_groups, tail_cap;
+  __half* k_sink;
+  __half* v_sink;
+  int32_t* n_sink;
+  int32_t hkv, max_groups, tail_cap, sink_cap;
   int32_t seq_len[KVQ_MAX_BATCH];
   int32_t ntail[KVQ_MAX_BATCH];
 };
@@ -156,11 +159,13 @@ prefill_kernel(const __grid_constant__ PrefillParams p) {
   const int b = blockIdx.z, h = blockIdx.y;
   const int item = blockIdx.x * kPrefillWarps + warp;
   const int seq = p.seq_len[b], nt = p.ntail[b];
-  const int nq = seq - nt, ng = nq / kGroup;
+  const int ns = min(p.sink_cap, seq);  // sink tokens [0, ns)
+  const int nq = seq - ns - nt, ng = nq / kGroup;
   if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
     p.n_quant[b] = nq;
     p.n_tail[b] = nt;
     p.tail_head[b] = 0;
+    if (p.sink_cap > 0) p.n_sink[b] = ns;
   }
   const size_t bh = (size_t)b * p.hkv + h;
   const __half* kseq = p.k + (int64_t)b * p.sb + (int64_t)h * p.sh;
@@ -168,23 +173,33 @@ prefill_kernel(const __grid_constant__ PrefillParams p) {
   if (item < ng) {
     using T = Tile<D, BITS>;
     const size_t gi = bh * p.max_groups + item;
-    quantize_tile_staged<D, BITS, VEC>(kseq + (int64_t)item * kGroup * p.st, vseq + (int64_t)item * kGroup * p.st,
+    quantize_tile_staged<D, BITS, VEC>(kseq + (int64_t)(ns + item * kGroup) * p.st,
+                                       vseq + (int64_t)(ns + item * kGroup) * p.st,
                                        p.st, p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
                                        p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D,
                                        s_stage + warp * StagedTile<D>::BYTES, lane);
-  } else if (item < ng + (nt + kGroup - 1) / kGroup) {
-    // copy tail tokens [nq + 32c, nq + 32c + 32) to ring slots 32c.. (ring head 0)
+  } else {
+    // fp16 row copies: tail tokens [ns + nq + 32c, ...) to ring slots 32c..
+    // (ring head 0), then sink tokens [32c', ...) to sink rows 32c'..
+    const int ct = (nt + kGroup - 1) / kGroup, cs = (ns + kGroup - 1) / kGroup;
     const int c = item - ng;
+    if (c >= ct + cs) return;
+    const bool tail = c < ct;
+    const int first = tail ? 32 * c : 32 * (c - ct), count = tail ? nt : ns;
+    const int src0 = tail ? ns + nq : 0;
+    const int cap = tail ? p.tail_cap : p.sink_cap;
+    __half* kd = tail ? p.k_tail : p.k_sink;
+    __half* vd = tail ? p.v_tail : p.v_sink;
     constexpr int CPL = D / 32;
-    for (int i = 32 * c; i < min(nt, 32 * c + 32); ++i) {
-      const int64_t src = (int64_t)(nq + i) * p.st + lane * CPL;
-      const size_t dst = (bh * p.tail_cap + i) * D + lane * CPL;
+    for (int i = first; i < min(count, first + 32); ++i) {
+      const int64_t src = (int64_t)(src0 + i) * p.st + lane * CPL;
+      const size_t dst = (bh * cap + i) * D + lane * CPL;
       if (CPL == 4) {
-        *reinterpret_cast<uint2*>(p.k_tail + dst) = *reinterpret_cast<const uint2*>(kseq + src);
-        *reinterpret_cast<uint2*>(p.v_tail + dst) = *reinterpret_cast<const uint2*>(vseq + src);
+        *reinterpret_cast<uint2*>(kd + dst) = *reinterpret_cast<const uint2*>(kseq + src);
+        *reinterpret_cast<uint2*>(vd + dst) = *reinterpret_cast<const uint2*>(vseq + src);
       } else {
-        *reinterpret_cast<uint32_t*>(p.k_tail + dst) = *reinterpret_cast<const uint32_t*>(kseq + src);
-        *reinterpret_cast<uint32_t*>(p.v_tail + dst) = *reinterpret_cast<const uint32_t*>(vseq + src);
+        *reinterpret_cast<uint32_t*>(kd + dst) = *reinterpret_cast<const uint32_t*>(kseq + src);
+        *reinterpret_cast<uint32_t*>(vd + dst) = *reinterpret_cast<const uint32_t*>(vseq + src);
       }
     }
   }
@@ -203,7 +218,10 @@ struct AppendParams {
   int32_t* n_tail;
   int32_t* tail_head;
   int32_t* error_flags;
-  int32_t hkv, max_groups, tail_cap;
+  __half* k_sink;
+  __half* v_sink;
+  int32_t* n_sink;
+  int32_t hkv, max_groups, tail_cap, sink_cap;
 };
 
 // grid (B); each block owns one sequence so the length update is race-free.
@@ -216,8 +234,29 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
   const int b = blockIdx.x;
   const int R = p.tail_cap;
   const int nq = p.n_quant[b], nt = p.n_tail[b], hd = p.tail_head[b];
+  const int ns = p.sink_cap > 0 ? p.n_sink[b] : 0;
+  if (p.sink_cap > 0 && ns < p.sink_cap) {
+    // the sink window is not full: the token becomes sink row ns (nothing may
+    // follow the sinks yet)
+    if (ns < 0 || nq != 0 || nt != 0) {
+      if (threadIdx.x == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_BAD_LENGTHS);
+      return;
+    }
+    constexpr int CPL = D / 32;
+    for (int h = warp; h < p.hkv; h += kAppendWarps) {
+      const size_t bh = (size_t)b * p.hkv + h;
+      const size_t src = bh * D + lane * CPL, dst = (bh * p.sink_cap + ns) * D + lane * CPL;
+      for (int i = 0; i < CPL; ++i) {
+        p.k_sink[dst + i] = p.k_new[src + i];
+        p.v_sink[dst + i] = p.v_new[src + i];
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) p.n_sink[b] = ns + 1;
+    return;
+  }
   const bool sane = nq >= 0 && nq % kGroup == 0 && nq / kGroup <= p.max_groups && nt >= 0 &&
-                    nt <= R && hd >= 0 && hd < R && hd % kGroup == 0;
+                    nt <= R && hd >= 0 && hd < R && hd % kGroup == 0 && ns == p.sink_cap;
   const bool flush = sane && nt == R;
   const bool fits = !flush || nq / kGroup < p.max_groups;
   if (!sane || !fits) {
@@ -323,12 +362,13 @@ extern "C" kvq_status kvq_quantize_prefill(const kvq_cache* c, const void* k, co
   int max_items = 0;
   for (int b = 0; b < c->batch; ++b) {
     const int L = seq_len[b], nt = n_tail[b];
-    if (L < 0 || nt < 0 || nt > L || nt > c->tail_cap) return KVQ_ERR_INVALID;
-    if ((L - nt) % KVQ_GROUP) return KVQ_ERR_INVALID;
-    if ((L - nt) / KVQ_GROUP > c->max_groups) return KVQ_ERR_CAPACITY;
+    const int ns = L < c->sink_cap ? L : c->sink_cap;
+    if (L < 0 || nt < 0 || nt > L - ns || nt > c->tail_cap) return KVQ_ERR_INVALID;
+    if ((L - ns - nt) % KVQ_GROUP) return KVQ_ERR_INVALID;
+    if ((L - ns - nt) / KVQ_GROUP > c->max_groups) return KVQ_ERR_CAPACITY;
     p.seq_len[b] = L;
     p.ntail[b] = nt;
-    const int items = (L - nt) / KVQ_GROUP + (nt + KVQ_GROUP - 1) / KVQ_GROUP;
+    const int items = (L - ns - nt) / KVQ_GROUP + (nt + KVQ_GROUP - 1) / KVQ_GROUP + (ns + KVQ_GROUP - 1) / KVQ_GROUP;
     max_items = items > max_items ? items : max_items;
   }
   p.k = static_cast<const __half*>(k);
@@ -345,9 +385,13 @@ extern "C" kvq_status kvq_quantize_prefill(const kvq_cache* c, const void* k, co
   p.n_quant = c->n_quant;
   p.n_tail = c->n_tail;
   p.tail_head = c->tail_head;
+  p.k_sink = static_cast<__half*>(c->k_sink);
+  p.v_sink = static_cast<__half*>(c->v_sink);
+  p.n_sink = c->n_sink;
   p.hkv = c->n_kv_heads;
   p.max_groups = c->max_groups;
   p.tail_cap = c->tail_cap;
+  p.sink_cap = c->sink_cap;
   if (max_items == 0) max_items = 1;  // still write the lengths
   if (c->n_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
   return dispatch_db<PrefillLaunch>(c->head_dim, c->bits, p, c->batch, max_items,
@@ -374,9 +418,13 @@ extern "C" kvq_status kvq_append_token(const kvq_cache* c, const void* k_new, co
   p.n_tail = c->n_tail;
   p.tail_head = c->tail_head;
   p.error_flags = c->error_flags;
+  p.k_sink = static_cast<__half*>(c->k_sink);
+  p.v_sink = static_cast<__half*>(c->v_sink);
+  p.n_sink = c->n_sink;
   p.hkv = c->n_kv_heads;
   p.max_groups = c->max_groups;
   p.tail_cap = c->tail_cap;
+  p.sink_cap = c->sink_cap;
   return dispatch_db<AppendLaunch>(c->head_dim, c->bits, p, c->batch,
                                    static_cast<cudaStream_t>(stream));
 }

@@ -28,9 +28,9 @@ KVQ_DEVERR_BAD_LENGTHS = 2
 KVQ_DEVERR_TIMEOUT = 4
 KVQ_GROUP = 32
 KVQ_MAX_BATCH = 512
-KVQ_NBUF = 7
+KVQ_NBUF = 9
 (KVQ_BUF_K_CODES, KVQ_BUF_V_CODES, KVQ_BUF_K_META, KVQ_BUF_V_META, KVQ_BUF_K_TAIL,
- KVQ_BUF_V_TAIL, KVQ_BUF_LENGTHS) = range(7)
+ KVQ_BUF_V_TAIL, KVQ_BUF_LENGTHS, KVQ_BUF_K_SINK, KVQ_BUF_V_SINK) = range(9)
 
 KVQ_DEVERR_BAD_WIDTH = 8
 KVQ_TZ_INDEX_BYTES = 512
@@ -68,6 +68,10 @@ class kvq_cache(ctypes.Structure):
         ("n_tail", ctypes.c_void_p),
         ("tail_head", ctypes.c_void_p),
         ("error_flags", ctypes.c_void_p),
+        ("sink_cap", ctypes.c_int32),
+        ("k_sink", ctypes.c_void_p),
+        ("v_sink", ctypes.c_void_p),
+        ("n_sink", ctypes.c_void_p),
     ]
 
 
@@ -235,11 +239,12 @@ class QuantizedKVCache:
     """Owns the device buffers of a uniform cache (allocated with PyTorch)."""
 
     def __init__(self, batch: int, n_kv_heads: int, head_dim: int, bits: int, max_tokens: int,
-                 tail_cap: int = 32, device="cuda"):
+                 tail_cap: int = 32, device="cuda", sink_cap: int = 0):
         self.batch, self.n_kv_heads, self.head_dim, self.bits = batch, n_kv_heads, head_dim, bits
-        self.tail_cap = tail_cap
+        self.tail_cap, self.sink_cap = tail_cap, sink_cap
         self.max_groups = math.ceil(max_tokens / KVQ_GROUP)
         d = kvq_cache(batch, n_kv_heads, head_dim, bits, self.max_groups, tail_cap)
+        d.sink_cap = sink_cap
         sizes = kvq_cache_bytes(d)
         dev = torch.device(device)
 
@@ -253,15 +258,19 @@ class QuantizedKVCache:
         self.v_meta = buf(sizes[KVQ_BUF_V_META], torch.float16)
         self.k_tail = buf(sizes[KVQ_BUF_K_TAIL], torch.float16)
         self.v_tail = buf(sizes[KVQ_BUF_V_TAIL], torch.float16)
-        lens = torch.zeros(4, (batch + 3) // 4 * 4, dtype=torch.int32, device=dev)
+        self.k_sink = buf(sizes[KVQ_BUF_K_SINK], torch.float16)
+        self.v_sink = buf(sizes[KVQ_BUF_V_SINK], torch.float16)
+        lens = torch.zeros(5, (batch + 3) // 4 * 4, dtype=torch.int32, device=dev)
         self._lens = lens
         self.n_quant, self.n_tail, self.tail_head = lens[0, :batch], lens[1, :batch], lens[2, :batch]
         self.error_flags = lens[3, :1]
+        self.n_sink = lens[4, :batch]
         for f, t in (("k_codes", self.k_codes), ("v_codes", self.v_codes),
                      ("k_meta", self.k_meta), ("v_meta", self.v_meta),
                      ("k_tail", self.k_tail), ("v_tail", self.v_tail),
                      ("n_quant", self.n_quant), ("n_tail", self.n_tail),
-                     ("tail_head", self.tail_head), ("error_flags", self.error_flags)):
+                     ("tail_head", self.tail_head), ("error_flags", self.error_flags),
+                     ("k_sink", self.k_sink), ("v_sink", self.v_sink), ("n_sink", self.n_sink)):
             setattr(d, f, t.data_ptr())
         self.desc = d
         self._workspaces = {}
@@ -282,7 +291,10 @@ class QuantizedKVCache:
             "v_meta": self.v_meta[:B * H * G * 2 * D].view(B, H, G, 2, D // 32, 32),
             "k_tail": self.k_tail[:B * H * R * D].view(B, H, R, D),
             "v_tail": self.v_tail[:B * H * R * D].view(B, H, R, D),
+            "k_sink": self.k_sink[:B * H * self.sink_cap * D].view(B, H, self.sink_cap, D),
+            "v_sink": self.v_sink[:B * H * self.sink_cap * D].view(B, H, self.sink_cap, D),
             "n_quant": self.n_quant, "n_tail": self.n_tail, "tail_head": self.tail_head,
+            "n_sink": self.n_sink,
         }
 
     def workspace(self, n_q_heads: int) -> torch.Tensor:

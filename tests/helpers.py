@@ -15,11 +15,11 @@ ATOL_MEAN = 1e-3
 
 
 def device_cache(w: S.Workload, inp: dict, bits: int, max_tokens: int | None = None,
-                 tail_cap: int | None = None, k=None, v=None) -> kvq.QuantizedKVCache:
+                 tail_cap: int | None = None, k=None, v=None, sink_cap: int = 0) -> kvq.QuantizedKVCache:
     """Allocate a cache and run kvq_quantize_prefill on the workload's K/V."""
     cap = max_tokens if max_tokens is not None else w.context
     cache = kvq.QuantizedKVCache(w.batch, w.n_kv_heads, w.head_dim, bits, cap,
-                                 tail_cap or w.tail_cap)
+                                 tail_cap or w.tail_cap, sink_cap=sink_cap)
     if k is None:
         k = torch.from_numpy(inp["K"]).cuda()
         v = torch.from_numpy(inp["V"]).cuda()
@@ -27,14 +27,15 @@ def device_cache(w: S.Workload, inp: dict, bits: int, max_tokens: int | None = N
     return cache
 
 
-def oracle_states(inp: dict, bits: int, heads=None, batches=None) -> list:
+def oracle_states(inp: dict, bits: int, heads=None, batches=None, sink_cap: int = 0) -> list:
     out = []
     bs = range(inp["K"].shape[0]) if batches is None else batches
     for b in bs:
         k, v = inp["K"][b], inp["V"][b]
         if heads is not None:
             k, v = k[:, heads], v[:, heads]
-        out.append(O.quantize_sequence(k, v, int(inp["seq_len"][b]), int(inp["n_tail"][b]), bits))
+        out.append(O.quantize_sequence(k, v, int(inp["seq_len"][b]), int(inp["n_tail"][b]), bits,
+                                       n_sink_cap=sink_cap))
     return out
 
 
@@ -80,6 +81,13 @@ def assert_buffers_equal(cache: kvq.QuantizedKVCache, states: list, batches=None
         vt = views["v_tail"][b][torch.tensor(hs)].cpu().numpy()[:, slots]
         assert (kt.view(np.uint16) == st["k_tail"].view(np.uint16)).all(), "key tail differs"
         assert (vt.view(np.uint16) == st["v_tail"].view(np.uint16)).all(), "value tail differs"
+        if cache.sink_cap > 0:
+            ns = int(views["n_sink"][b])
+            assert ns == st["n_sink"], (b, ns, st["n_sink"])
+            ks = views["k_sink"][b][torch.tensor(hs)].cpu().numpy()[:, :ns]
+            vs = views["v_sink"][b][torch.tensor(hs)].cpu().numpy()[:, :ns]
+            assert (ks.view(np.uint16) == st["k_sink"].view(np.uint16)).all(), "key sinks differ"
+            assert (vs.view(np.uint16) == st["v_sink"].view(np.uint16)).all(), "value sinks differ"
 
 
 def oracle_decode(q: np.ndarray, states: list, sm_scale: float, heads=None) -> np.ndarray:

@@ -171,3 +171,25 @@ def test_trizone_validation_fails_before_launch(lib):
     ws = ctypes.c_size_t()
     assert lib.kvq_trizone_decode_workspace_bytes(ctypes.byref(_fake_tz()), 6, ctypes.byref(ws)) == \
         kvq.KVQ_ERR_INVALID
+
+
+def test_sink_window_bytes_and_validation(lib):
+    d = kvq.kvq_cache(2, 8, 128, 2, 16, 32)
+    d.sink_cap = 4
+    s = kvq.kvq_cache_bytes(d)
+    assert s[kvq.KVQ_BUF_K_SINK] == s[kvq.KVQ_BUF_V_SINK] == 2 * 8 * 4 * 128 * 2
+    sizes = (ctypes.c_size_t * kvq.KVQ_NBUF)()
+    for bad in (-1, 257):
+        d.sink_cap = bad
+        assert lib.kvq_cache_bytes(ctypes.byref(d), sizes) == kvq.KVQ_ERR_INVALID
+    # a window without its buffers is rejected before any launch
+    f = _fake_cache(sink_cap=4)
+    i32 = ctypes.c_int32 * 2
+    st = lib.kvq_quantize_prefill(ctypes.byref(f), 0x100000, 0x101000, 1 << 14, 512, 128,
+                                  i32(68, 68), i32(0, 0), None)
+    assert st == kvq.KVQ_ERR_INVALID
+    f = _fake_cache(sink_cap=4, k_sink=0x900000, v_sink=0x910000, n_sink=0x920000)
+    # 68 tokens with a 4-token window: 64 quantized tokens = 2 groups; 67 is ragged
+    st = lib.kvq_quantize_prefill(ctypes.byref(f), 0x100000, 0x101000, 1 << 14, 512, 128,
+                                  i32(67, 68), i32(0, 0), None)
+    assert st == kvq.KVQ_ERR_INVALID
