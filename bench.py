@@ -42,9 +42,11 @@ def parse():
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
     ap.add_argument("--sink", type=int, default=0,
                     help="uniform cache: keep the first S tokens fp16 (attention-sink window)")
-    ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone"],
+    ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone", "serving"],
                     help="uniform: the 128k-token uniform cache (default); trizone: the "
-                         "mixed-width cache, 4 sequences x 65,408 old + 128 fresh tokens")
+                         "mixed-width cache, 4 sequences x 65,408 old + 128 fresh tokens; "
+                         "serving: 16 ragged sequences of 8k-32k tokens, 4-bit, one "
+                         "append + decode per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -402,6 +404,9 @@ def main():
     if args.workload == "trizone":
         main_trizone(args)
         return
+    if args.workload == "serving":
+        main_serving(args)
+        return
     import torch
     import torch.distributed as dist
     from quantized_kv_cache_11_gb300 import kvq
@@ -679,6 +684,125 @@ def main_trizone(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = trizone_cpu_baseline(w, inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main_serving(args):
+    """Serving: 16 sequences (32 query heads over 8 KV heads, head_dim 128, 4-bit)
+    with lengths L ~ U[8192, 32768].  Reports the prefill of 16 full 32,768-token
+    chunks (rate and time), and times steps of one kvq_append_token (with its
+    flushes) + one kvq_decode_attn over the ragged caches; the decode alone is
+    timed too for the roofline."""
+    import torch
+    import torch.distributed as dist
+    from quantized_kv_cache_11_gb300 import kvq
+    from quantized_kv_cache_11_gb300 import synthetic as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kvq.load_library()
+    w = S.SERVING
+    inp = S.generate(w)
+    B, H, D, T = w.batch, w.n_kv_heads, w.head_dim, w.context
+    K = torch.from_numpy(inp["K"]).to(dev)
+    V = torch.from_numpy(inp["V"]).to(dev)
+    q = torch.from_numpy(inp["q"]).to(dev)
+    # (i) prefill of the full chunks
+    full = kvq.QuantizedKVCache(B, H, D, w.bits, T, w.tail_cap, device=dev)
+    full.prefill(K, V, [T] * B, [0] * B)
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record()
+    for _ in range(5):
+        full.prefill(K, V, [T] * B, [0] * B)
+    p1.record()
+    torch.cuda.synchronize()
+    prefill_us = p0.elapsed_time(p1) * 1000 / 5
+    prefill_bytes = prefill_algorithmic_bytes(w, T, 0) * 1  # all 16 sequences of T tokens
+    del full
+    torch.cuda.empty_cache()
+    # (ii) the ragged caches, then append + decode steps
+    seq, nt = inp["seq_len"].astype(int), inp["n_tail"].astype(int)
+    cache = kvq.QuantizedKVCache(B, H, D, w.bits, T + 8192, w.tail_cap, device=dev)
+    cache.prefill(K, V, seq.tolist(), nt.tolist())
+    kn = torch.randn(B, H, D, device=dev).half()
+    vn = torch.randn(B, H, D, device=dev).half()
+    out = torch.empty(B, w.n_q_heads, D, dtype=torch.float32, device=dev)
+
+    def step():
+        cache.append(kn, vn)
+        cache.decode(q, w.sm_scale, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    per_graph = 64
+    steps_wanted = min(args.steps, 4096)  # the caches hold 8192 more tokens per sequence
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            step()
+    reps = max(1, math.ceil(steps_wanted / per_graph))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    steps = reps * per_graph
+    step_us = max_over_ranks(e0.elapsed_time(e1), dev) * 1000.0 / steps
+    # the decode alone over the caches as they now are
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd):
+        for _ in range(per_graph):
+            cache.decode(q, w.sm_scale, out=out)
+    gd.replay()
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record()
+    for _ in range(8):
+        gd.replay()
+    d1.record()
+    torch.cuda.synchronize()
+    decode_us = max_over_ranks(d0.elapsed_time(d1), dev) * 1000.0 / (8 * per_graph)
+    assert cache.device_errors() == 0
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    nq = cache.n_quant.cpu().numpy().astype(int)
+    ntl = cache.n_tail.cpu().numpy().astype(int)
+    dbytes = sum(algorithmic_bytes(w.scaled(batch=1), int(a), int(b)) for a, b in zip(nq, ntl))
+    dbytes -= (B - 1) * w.n_q_heads * D * 6  # q and out counted once per batch above
+    peak, peak_kind = load_peaks()
+    achieved = dbytes / (decode_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": step_us, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": step_us / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "n_q_heads": w.n_q_heads, "n_kv_heads": H,
+                   "head_dim": D, "bits": w.bits, "lengths": f"U[{w.ragged[0]}, {w.ragged[1]}]",
+                   "mean_tokens": float((nq + ntl).mean()), "step": "one append + one decode",
+                   "l2": f"inputs larger than L2: {dbytes / 1e6:.0f} MB read per decode",
+                   "launch": "CUDA graph of kvq_append_token + kvq_decode_attn"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "decode_kernel<128,4,4>",
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": dbytes},
+        "gpu_launches": 2 * steps,
+        "clocks": clk.summary(),
+        "path": {"step_us": step_us, "decode_us": decode_us, "append_us": step_us - decode_us,
+                 "prefill_us": prefill_us, "prefill_gbs": prefill_bytes / (prefill_us * 1e-6) / 1e9,
+                 "prefill_bytes": prefill_bytes},
+    }
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
