@@ -173,125 +173,6 @@ __device__ __forceinline__ void store_meta_lane_order(const __half* nat, __half*
 }
 
 // ---------------------------------------------------------------------------
-// One warp quantizes one 32-token tile of keys and of values.
-//   ksrc/vsrc: token 0 of the tile for this head; rows tstride elements apart,
-//   channels contiguous.  Writes packed codes and metadata of the tile.
-//   ct: shared scratch of 32 * D bytes for this warp; vm: shared 2 * D halves;
-//   vinv: shared D floats (the value groups' reciprocal scales).
-// Keys: one group per channel over the 32 tokens (lane-local min/max, each lane
-// owns D/32 channels).  Values: one group per 32 channels of a token (min/max
-// reduced over the lanes that share a group with shuffles).
-// ---------------------------------------------------------------------------
-template <int D>
-struct LaneRow;  // D/32 consecutive halves of a row held by one lane
-template <>
-struct LaneRow<128> {
-  static constexpr int kN = 4;
-  uint2 raw;
-  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint2*>(p); }
-  __device__ __forceinline__ float get(int i) const {
-    const uint32_t w = (i < 2) ? raw.x : raw.y;
-    const uint16_t hbits = (i & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xffffu);
-    return __half2float(__ushort_as_half(hbits));
-  }
-};
-template <>
-struct LaneRow<64> {
-  static constexpr int kN = 2;
-  uint32_t raw;
-  __device__ __forceinline__ void load(const __half* p) { raw = *reinterpret_cast<const uint32_t*>(p); }
-  __device__ __forceinline__ float get(int i) const {
-    const uint16_t hbits = i ? (uint16_t)(raw >> 16) : (uint16_t)(raw & 0xffffu);
-    return __half2float(__ushort_as_half(hbits));
-  }
-};
-
-template <int D, int BITS>
-__device__ __forceinline__ void quantize_tile_warp(const __half* ksrc, const __half* vsrc,
-                                                   int64_t tstride, uint8_t* kcodes_dst,
-                                                   __half* kmeta_dst, uint8_t* vcodes_dst,
-                                                   __half* vmeta_dst, uint8_t* ct, __half* vm,
-                                                   float* vinv, int lane) {
-  constexpr int CPL = D / 32;  // channels per lane
-  const int c0 = lane * CPL;
-  // ---- keys: per channel over 32 tokens
-  {
-    LaneRow<D> rows[kGroup];
-#pragma unroll
-    for (int t = 0; t < kGroup; ++t) rows[t].load(ksrc + (int64_t)t * tstride + c0);
-    __half sc[CPL], ze[CPL];
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      float mn = rows[0].get(j), mx = mn;
-#pragma unroll
-      for (int t = 1; t < kGroup; ++t) {
-        const float x = rows[t].get(j);
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
-      }
-      const GroupParams p = group_params<BITS>(mn, mx);
-      sc[j] = p.scale_h;
-      ze[j] = p.zero_h;
-#pragma unroll
-      for (int t = 0; t < kGroup; ++t) ct[t * D + c0 + j] = (uint8_t)quant_code<BITS>(rows[t].get(j), p);
-    }
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      vm[c0 + j] = sc[j];
-      vm[D + c0 + j] = ze[j];
-    }
-  }
-  __syncwarp();
-  pack_store_tile<D, BITS, true>(ct, kcodes_dst, lane);
-  store_meta_lane_order<D, true>(vm, kmeta_dst, lane);
-  __syncwarp();
-  // ---- values: per token over 32-channel spans.  The lanes of a group reduce
-  // min/max with shuffles; the group's parameters are computed once, by lane
-  // (t % LPG) of the group, and read back from shared memory (vm, inv).
-  {
-    constexpr int LPG = 32 / CPL;  // lanes per 32-channel group
-    const int j = c0 / kGroup;     // this lane's channel group
-    LaneRow<D> vr[kGroup];
-#pragma unroll
-    for (int t = 0; t < kGroup; ++t) vr[t].load(vsrc + (int64_t)t * tstride + c0);
-#pragma unroll 4
-    for (int t = 0; t < kGroup; ++t) {
-      float mn = vr[t].get(0), mx = mn;
-#pragma unroll
-      for (int i = 1; i < CPL; ++i) {
-        mn = fminf(mn, vr[t].get(i));
-        mx = fmaxf(mx, vr[t].get(i));
-      }
-#pragma unroll
-      for (int off = 1; off < LPG; off <<= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      }
-      if ((lane % LPG) == (t % LPG)) {
-        const GroupParams p = group_params<BITS>(mn, mx);
-        vm[j * kGroup + t] = p.scale_h;
-        vm[D + j * kGroup + t] = p.zero_h;
-        vinv[j * kGroup + t] = p.inv;
-      }
-    }
-    __syncwarp();
-#pragma unroll 4
-    for (int t = 0; t < kGroup; ++t) {
-      GroupParams p;
-      p.scale = __half2float(vm[j * kGroup + t]);
-      p.zero = __half2float(vm[D + j * kGroup + t]);
-      p.inv = vinv[j * kGroup + t];
-#pragma unroll
-      for (int i = 0; i < CPL; ++i) ct[t * D + c0 + i] = (uint8_t)quant_code<BITS>(vr[t].get(i), p);
-    }
-  }
-  __syncwarp();
-  pack_store_tile<D, BITS, false>(ct, vcodes_dst, lane);
-  store_meta_lane_order<D, false>(vm, vmeta_dst, lane);
-  __syncwarp();
-}
-
-// ---------------------------------------------------------------------------
 // PTX wrappers.
 // ---------------------------------------------------------------------------
 // D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col); fragment layouts per

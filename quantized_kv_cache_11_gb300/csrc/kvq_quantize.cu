@@ -227,9 +227,7 @@ struct AppendParams {
 // grid (B); each block owns one sequence so the length update is race-free.
 template <int D, int BITS>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p) {
-  __shared__ __align__(16) uint8_t s_ct[kAppendWarps][kGroup * D];
-  __shared__ __align__(16) __half s_vm[kAppendWarps][2 * D];
-  __shared__ __align__(16) float s_vinv[kAppendWarps][D];
+  extern __shared__ __align__(16) uint8_t s_stage[];  // StagedTile<D>::BYTES per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x;
   const int R = p.tail_cap;
@@ -273,12 +271,13 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
     __half* kt = p.k_tail + bh * R * D;
     __half* vt = p.v_tail + bh * R * D;
     if (flush) {
+      // the oldest 32 tail tokens sit in ring slots hd .. hd + 31 (hd and R are
+      // multiples of 32): contiguous, 16-byte aligned rows
       using T = Tile<D, BITS>;
       const size_t gi = bh * p.max_groups + nq / kGroup;
-      quantize_tile_warp<D, BITS>(kt + (size_t)hd * D, vt + (size_t)hd * D, D,
-                                  p.k_codes + gi * T::kBytes, p.k_meta + gi * 2 * D,
-                                  p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D, s_ct[warp],
-                                  s_vm[warp], s_vinv[warp], lane);
+      quantize_tile_staged<D, BITS, 16>(kt + (size_t)hd * D, vt + (size_t)hd * D, D, p.k_codes + gi * T::kBytes,
+                                        p.k_meta + gi * 2 * D, p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D,
+                                        s_stage + warp * StagedTile<D>::BYTES, lane);
     }
     const size_t src = bh * D + lane * CPL;
     const size_t dst = (size_t)slot * D + lane * CPL;
@@ -339,7 +338,15 @@ struct PrefillLaunch {
 template <int D, int BITS>
 struct AppendLaunch {
   static kvq_status run(const AppendParams& p, int batch, cudaStream_t s) {
-    append_kernel<D, BITS><<<batch, kAppendWarps * 32, 0, s>>>(p);
+    constexpr int smem = kAppendWarps * StagedTile<D>::BYTES;
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(append_kernel<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return KVQ_ERR_CUDA;
+      attr = true;
+    }
+    append_kernel<D, BITS><<<batch, kAppendWarps * 32, smem, s>>>(p);
     return launch_status();
   }
 };
