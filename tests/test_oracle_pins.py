@@ -329,15 +329,15 @@ def test_flushed_group_equals_prefill_quantization():
 # byte ((w // 4) * 32 + lane) * 16 + (w % 4) * 4.
 KPOS_2BIT_D128 = [
     # (token, channel) -> (byte offset of the 32-bit word, bit offset); 2-bit slot
-    # bit positions (2, 6, 0, 4, 10, 14, 8, 12)
-    ((0, 0), (0, 2)), ((0, 1), (0, 18)), ((8, 0), (0, 6)), ((0, 8), (0, 0)),
-    ((8, 9), (0, 20)), ((16, 0), (0, 10)), ((24, 8), (0, 12)), ((1, 0), (64, 2)),
-    ((0, 2), (16, 2)), ((0, 16), (4, 2)), ((0, 64), (512, 2)), ((31, 127), (1020, 28)),
+    # bit positions (2, 4, 6, 8, 10, 12, 14, 0)
+    ((0, 0), (0, 2)), ((0, 1), (0, 18)), ((8, 0), (0, 4)), ((0, 8), (0, 6)),
+    ((8, 9), (0, 24)), ((16, 0), (0, 10)), ((24, 8), (0, 0)), ((1, 0), (64, 2)),
+    ((0, 2), (16, 2)), ((0, 16), (4, 2)), ((0, 64), (512, 2)), ((31, 127), (1020, 16)),
 ]
 KPOS_4BIT_D128 = [((0, 0), (0, 0)), ((16, 0), (4, 0)), ((8, 1), (0, 20)), ((0, 16), (8, 0)),
                   ((0, 32), (512, 0))]
 VPOS_2BIT_D128 = [
-    ((0, 0), (0, 2)), ((1, 0), (0, 18)), ((0, 8), (0, 6)), ((8, 0), (0, 0)),
+    ((0, 0), (0, 2)), ((1, 0), (0, 18)), ((0, 8), (0, 4)), ((8, 0), (0, 6)),
     ((16, 0), (0, 10)), ((2, 0), (16, 2)), ((0, 1), (64, 2)), ((0, 16), (4, 2)),
 ]
 
@@ -469,8 +469,8 @@ def test_trizone_channel_order_by_hand():
 # hand from the fragment layout: lane 4 gid + tig; pair P = 8 kt + 4 mt + i covers
 # token 16 mt + gid + 8 (i % 2), channels 16 kt + 2 tig + 8 (i // 2) and +1.
 KSUB_POS = {
-    (1, 2): {(0, 0): (0, 2), (0, 1): (0, 18), (8, 0): (0, 6), (0, 8): (0, 0), (8, 8): (0, 4),
-             (16, 0): (0, 10), (31, 15): (31, 28), (31, 14): (31, 12)},
+    (1, 2): {(0, 0): (0, 2), (0, 1): (0, 18), (8, 0): (0, 4), (0, 8): (0, 6), (8, 8): (0, 8),
+             (16, 0): (0, 10), (31, 15): (31, 16), (31, 14): (31, 0)},
     (3, 4): {(25, 2): (37, 4), (25, 3): (37, 20), (0, 16): (64, 0), (31, 47): (191, 28)},
     (2, 8): {(9, 1): (4, 24), (0, 0): (0, 0), (16, 16): (192, 0)},
 }
