@@ -90,12 +90,12 @@ struct Tile {
 };
 
 // Bit position (within each 16-bit half of a word) of the codes in slot k.  For
-// 2-bit codes the slots of one shifted word pair up: slots {0,1,4,5} sit 2 bits
-// above slots {2,3,6,7}, so one shift aligns a code of each to the top two
-// mantissa fields of an fp16 value.
+// 2-bit codes slots 0..7 sit at 2,4,6,8,10,12,14,0: slots 0-3 lie in the fp16
+// mantissa field as stored, slots 4-6 after a shift right by 8, slot 7 after a
+// shift left by 8.
 template <int BITS>
 __host__ __device__ constexpr int slot_bitpos(int k) {
-  return BITS == 2 ? ((k & 4) ? 8 : 0) + ((k & 1) ? 4 : 0) + ((k & 2) ? 0 : 2) : BITS * k;
+  return BITS == 2 ? ((k + 1) & 7) * 2 : BITS * k;
 }
 
 // (token, channel) of the FIRST code of key pair P of a lane; the second code is

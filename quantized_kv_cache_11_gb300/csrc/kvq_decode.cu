@@ -38,11 +38,11 @@ constexpr int kTailWeight = 3;  // a 32-token fp16 tail chunk counts as this man
 // briefly): far longer than any copy takes, short enough to end a stuck kernel.
 constexpr uint32_t kMaxPolls = 1u << 22;
 
-// half2(4), half2(16), half2(256): OR-ing a code into the top 2, 4 or 8 mantissa
-// bits of these gives 4 + c, 16 + c or 256 + c exactly.  Kept in constant memory so
-// the unpack's single logic op takes one operand from there and the mask as an
-// immediate.
-__constant__ uint32_t c_expo[3] = {0x44004400u, 0x4C004C00u, 0x5C005C00u};
+// half2(4), half2(16), half2(256), half2(64): OR-ing a code into the mantissa bits
+// whose unit is 1 (bits 8-9, 6-9, 2-9 and 4-5) gives 4 + c, 16 + c, 256 + c, 64 + c
+// exactly.  Kept in constant memory so the unpack's single logic op takes one
+// operand from there and the mask as an immediate.
+__constant__ uint32_t c_expo[4] = {0x44004400u, 0x4C004C00u, 0x5C005C00u, 0x54005400u};
 
 template <int D, int BITS, int G>
 struct DecodeCfg {
@@ -163,10 +163,12 @@ template <int D, int BITS, int G>
 struct Decoder {
   using C = DecodeCfg<D, BITS, G>;
   static constexpr int NT = C::NT, KT = C::KT;
-  // fp16 offsets carried by the unpacked codes: slots whose pair index i%4 < 2
-  // (first half of a fragment's k range) carry kOff0, the others kOff1.
-  static constexpr float kOff0 = BITS == 2 ? 4.f : (BITS == 4 ? 16.f : 256.f);
-  static constexpr float kOff1 = BITS == 2 ? 16.f : (BITS == 4 ? 16.f : 256.f);
+  // fp16 offset carried by an unpacked code, by its register i = 0..3 in an mma
+  // A fragment (rows gid / gid+8 for i even / odd, first / second half of the k
+  // range for i < 2 / i >= 2): 2-bit codes 256, 64, 16, 4; wider codes one offset.
+  static __host__ __device__ constexpr float off(int i) {
+    return BITS == 2 ? (i == 0 ? 256.f : (i == 1 ? 64.f : (i == 2 ? 16.f : 4.f))) : (BITS == 4 ? 16.f : 256.f);
+  }
   static constexpr uint32_t kOnes = 0x3C003C00u;  // half2(1, 1)
 
   // Per-warp running state of the online softmax for the G heads.
@@ -206,19 +208,19 @@ struct Decoder {
   }
 
   // fp16 pairs (off + c_first, off + c_second) of pairs P0 .. P0+7 of the lane's
-  // words (P0 a multiple of 8): one shift and one logic op per pair at most.
-  // 2-bit: a word's slots (0,2), (1,3), (4,6), (5,7) sit at bit positions
-  // (2,0), (6,4), (10,8), (14,12); shifting by 6, 2, -2, -6 puts the first of each
-  // at mantissa bits [8,10) (offset 4) and the second at [6,8) (offset 16).
+  // words (P0 a multiple of 8): one logic op per pair, plus two shifts per word at
+  // 2 bits.  2-bit slots 0-3 sit at bits 2, 4, 6, 8 (mantissa fields with offsets
+  // 256, 64, 16, 4 as stored), slots 4-6 at 10, 12, 14 (the same fields after a
+  // shift right by 8), slot 7 at 0 (bits 8-9 after a shift left by 8).
   static __device__ __forceinline__ void unpack8(const uint32_t* w, int P0, uint32_t (&a)[8]) {
     if (BITS == 2) {
       const uint32_t x = w[P0 / 8];
-      const uint32_t s0 = x << 6, s1 = x << 2, s2 = x >> 2, s3 = x >> 6;
-      const uint32_t e4 = c_expo[0], e16 = c_expo[1];
-      a[0] = (s0 & 0x03000300u) | e4;  a[2] = (s0 & 0x00C000C0u) | e16;
-      a[1] = (s1 & 0x03000300u) | e4;  a[3] = (s1 & 0x00C000C0u) | e16;
-      a[4] = (s2 & 0x03000300u) | e4;  a[6] = (s2 & 0x00C000C0u) | e16;
-      a[5] = (s3 & 0x03000300u) | e4;  a[7] = (s3 & 0x00C000C0u) | e16;
+      const uint32_t y = x >> 8, z = x << 8;
+      const uint32_t e4 = c_expo[0], e16 = c_expo[1], e256 = c_expo[2], e64 = c_expo[3];
+      a[0] = (x & 0x000C000Cu) | e256;  a[4] = (y & 0x000C000Cu) | e256;
+      a[1] = (x & 0x00300030u) | e64;   a[5] = (y & 0x00300030u) | e64;
+      a[2] = (x & 0x00C000C0u) | e16;   a[6] = (y & 0x00C000C0u) | e16;
+      a[3] = (x & 0x03000300u) | e4;    a[7] = (z & 0x03000300u) | e4;
     } else if (BITS == 4) {
       const uint32_t e16 = c_expo[1];
 #pragma unroll
@@ -375,16 +377,17 @@ struct Decoder {
     float lg[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      // sum_d q z - off0 * sum_{first halves} q s - off1 * sum_{second halves} q s, head 4nt+tig
+      // sum_d q z - sum over the halves of the k range of off * sum q s, head 4nt+tig;
+      // the offsets of token rows gid (r = 0) and gid + 8 (r = 1) differ at 2 bits
       const float zq = __shfl_sync(0xffffffffu, cacc[0][nt][0], tig);
       const float s0 = __shfl_sync(0xffffffffu, cacc[0][nt][0], 4 + tig);
       const float s1 = __shfl_sync(0xffffffffu, cacc[0][nt][0], 8 + tig);
-      const float kc = zq - kOff0 * s0 - kOff1 * s1;
+      const float kc[2] = {zq - off(0) * s0 - off(2) * s1, zq - off(1) * s0 - off(3) * s1};
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          lg[nt][mt][r] = (sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + kc) * scale_log2;
+          lg[nt][mt][r] = (sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + kc[r]) * scale_log2;
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
@@ -531,21 +534,22 @@ struct Decoder {
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
       const float lt = __shfl_sync(0xffffffffu, zc[nt][2], 16 + tig);  // row 12: lanes gid 4
-      float vc[D / 32];
+      float vc[2][D / 32];  // output channel rows gid / gid + 8 of each 32-channel group
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         const float zs = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);         // row j
         const float s0 = __shfl_sync(0xffffffffu, zc[nt][0], 4 * (4 + j) + tig);   // row 4+j
         const float s1 = __shfl_sync(0xffffffffu, zc[nt][2], 4 * j + tig);         // row 8+j
-        vc[j] = zs - kOff0 * s0 - kOff1 * s1;
+        vc[0][j] = zs - off(0) * s0 - off(2) * s1;
+        vc[1][j] = zs - off(1) * s0 - off(3) * s1;
       }
       if (g < G) {
         float* d = dst + g * C::PSTRIDE;
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
-          d[4 + 16 * mt + gid] = o[mt][nt][0] + o[mt][nt][1] + vc[mt / 2];
-          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + o[mt][nt][3] + vc[mt / 2];
+          d[4 + 16 * mt + gid] = o[mt][nt][0] + o[mt][nt][1] + vc[0][mt / 2];
+          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + o[mt][nt][3] + vc[1][mt / 2];
         }
       }
     }

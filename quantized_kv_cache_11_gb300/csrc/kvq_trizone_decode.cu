@@ -37,9 +37,12 @@ namespace kvq {
 namespace tz {
 
 constexpr uint32_t kMaxPolls = 1u << 22;
-// half2(4), half2(16), half2(256): a code OR-ed into their top mantissa bits
-// gives 4 + c, 16 + c, 256 + c exactly
-__constant__ uint32_t c_tz_expo[3] = {0x44004400u, 0x4C004C00u, 0x5C005C00u};
+// half2(4), half2(16), half2(256), half2(64): a code OR-ed into the mantissa bits
+// whose unit is 1 gives 4 + c, 16 + c, 256 + c, 64 + c exactly
+__constant__ uint32_t c_tz_expo[4] = {0x44004400u, 0x4C004C00u, 0x5C005C00u, 0x54005400u};
+// offset of a 2-bit code by its register i = 0..3 in an mma A fragment (2-bit slots
+// 0..7 sit at bits 2,4,6,8,10,12,14,0)
+__host__ __device__ constexpr float off2(int i) { return i == 0 ? 256.f : (i == 1 ? 64.f : (i == 2 ? 16.f : 4.f)); }
 
 template <int G>
 struct Cfg {
@@ -177,12 +180,12 @@ struct Decoder {
   static __device__ __forceinline__ void unpack8(const uint32_t* w, uint32_t (&a)[8]) {
     if (BITS == 2) {
       const uint32_t x = w[0];
-      const uint32_t s0 = x << 6, s1 = x << 2, s2 = x >> 2, s3 = x >> 6;
-      const uint32_t e4 = c_tz_expo[0], e16 = c_tz_expo[1];
-      a[0] = (s0 & 0x03000300u) | e4;  a[2] = (s0 & 0x00C000C0u) | e16;
-      a[1] = (s1 & 0x03000300u) | e4;  a[3] = (s1 & 0x00C000C0u) | e16;
-      a[4] = (s2 & 0x03000300u) | e4;  a[6] = (s2 & 0x00C000C0u) | e16;
-      a[5] = (s3 & 0x03000300u) | e4;  a[7] = (s3 & 0x00C000C0u) | e16;
+      const uint32_t y = x >> 8, z = x << 8;
+      const uint32_t e4 = c_tz_expo[0], e16 = c_tz_expo[1], e256 = c_tz_expo[2], e64 = c_tz_expo[3];
+      a[0] = (x & 0x000C000Cu) | e256;  a[4] = (y & 0x000C000Cu) | e256;
+      a[1] = (x & 0x00300030u) | e64;   a[5] = (y & 0x00300030u) | e64;
+      a[2] = (x & 0x00C000C0u) | e16;   a[6] = (y & 0x00C000C0u) | e16;
+      a[3] = (x & 0x03000300u) | e4;    a[7] = (z & 0x03000300u) | e4;
     } else if (BITS == 4) {
       const uint32_t e16 = c_tz_expo[1];
 #pragma unroll
@@ -399,8 +402,8 @@ struct Decoder {
 #pragma unroll
         for (int i = 0; i < 4; ++i) { sacc[c][0][nt][i] = 0.f; sacc[c][1][nt][i] = 0.f; cc[nt][i] = 0.f; }
     // constant-product rows: 0 = zero points; 1, 2 = scales of the 2-bit class
-    // (first / second half of a k-tile: offsets 4 / 16); 3 = 4-bit scales (16);
-    // 4 = 8-bit scales (256)
+    // (first / second half of a k-tile; the offsets depend on the token row too:
+    // off2); 3 = 4-bit scales (16); 4 = 8-bit scales (256)
     const uint32_t mz = gid == 0 ? ~0u : 0u;
     int kt = 0;
     key_class<2>(st, kt2, kt, ksc, kze, mz, gid == 1 ? ~0u : 0u, gid == 2 ? ~0u : 0u, sacc, cc);
@@ -415,13 +418,14 @@ struct Decoder {
       const float s2 = __shfl_sync(0xffffffffu, cc[nt][0], 8 + tig);
       const float s3 = __shfl_sync(0xffffffffu, cc[nt][0], 12 + tig);
       const float s4 = __shfl_sync(0xffffffffu, cc[nt][0], 16 + tig);
-      const float kc = zq - 4.f * s1 - 16.f * s2 - 16.f * s3 - 256.f * s4;
+      const float kc48 = zq - 16.f * s3 - 256.f * s4;
+      const float kc[2] = {kc48 - off2(0) * s1 - off2(2) * s2, kc48 - off2(1) * s1 - off2(3) * s2};
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const float x = sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + sacc[1][mt][nt][2 * r] +
-                          sacc[1][mt][nt][2 * r + 1] + kc;
+                          sacc[1][mt][nt][2 * r + 1] + kc[r];
           lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? x * scale_log2 : -INFINITY;
         }
     }
@@ -477,13 +481,16 @@ struct Decoder {
 
   // This warp's partial (m, l, unnormalised o) for its G heads.
   __device__ __forceinline__ void write_partial(float* dst) const {
-    constexpr float off0[3] = {4.f, 16.f, 256.f}, off1[3] = {16.f, 16.f, 256.f};
+    // offsets of the value classes' codes by A-fragment register i: 2-bit off2(i),
+    // 4-bit 16, 8-bit 256; output rows gid take registers 0 and 2, rows gid + 8
+    // registers 1 and 3
+    constexpr float off[3][4] = {{256.f, 64.f, 16.f, 4.f}, {16.f, 16.f, 16.f, 16.f}, {256.f, 256.f, 256.f, 256.f}};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
-      float lt = 0.f, vc[kDim / 32];
+      float lt = 0.f, vc[2][kDim / 32];
 #pragma unroll
-      for (int j = 0; j < kDim / 32; ++j) vc[j] = 0.f;
+      for (int j = 0; j < kDim / 32; ++j) { vc[0][j] = 0.f; vc[1][j] = 0.f; }
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
         lt += __shfl_sync(0xffffffffu, zc[c][nt][2], 16 + tig);  // row 12
@@ -492,7 +499,8 @@ struct Decoder {
           const float zs = __shfl_sync(0xffffffffu, zc[c][nt][0], 4 * j + tig);        // row j
           const float s0 = __shfl_sync(0xffffffffu, zc[c][nt][0], 4 * (4 + j) + tig);  // row 4+j
           const float s1 = __shfl_sync(0xffffffffu, zc[c][nt][2], 4 * j + tig);        // row 8+j
-          vc[j] += zs - off0[c] * s0 - off1[c] * s1;
+          vc[0][j] += zs - off[c][0] * s0 - off[c][2] * s1;
+          vc[1][j] += zs - off[c][1] * s0 - off[c][3] * s1;
         }
       }
       if (g < G) {
@@ -500,8 +508,8 @@ struct Decoder {
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          d[4 + 16 * mt + gid] = o[mt][nt][0] + o[mt][nt][1] + vc[mt / 2];
-          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + o[mt][nt][3] + vc[mt / 2];
+          d[4 + 16 * mt + gid] = o[mt][nt][0] + o[mt][nt][1] + vc[0][mt / 2];
+          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + o[mt][nt][3] + vc[1][mt / 2];
         }
       }
     }
