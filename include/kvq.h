@@ -110,10 +110,12 @@ typedef enum {
  *           token t = 16kt + 2tig + 8(i/2); pair = (code[t][c], code[t+1][c])
  * Pair P of a lane goes to the lane's 32-bit word P/(16/b), slot k = P%(16/b): the
  * first code at bits [p, p+b), the second at bits [16+p, 16+p+b), where p is
- * 2,4,6,8,10,12,14,0 for k = 0..7 at b = 2 and p = b*k at b = 4, 8.  The lane's
+ * 0,2,8,10,4,6,12,14 for k = 0..7 at b = 2 and p = b*k at b = 4, 8.  The lane's
  * word w is stored little-endian at byte ((w/4)*32 + lane)*16 + (w%4)*4 of the
- * tile.  (The pairs are the operand fragments of a 16x8x16 tensor-core product,
- * so a warp turns each word into fp16 operands with one logic op per pair.)
+ * tile.  (The pairs are the operand fragments of a 16x8x16 tensor-core product:
+ * a warp turns each word into fp16 operands with one mask per pair, the codes
+ * read as fp16 subnormals, and the two k-halves of a fragment row always share
+ * a bit position.)
  *
  * Metadata planes are stored as fp16 pairs (32-bit words) in lane order, D/2
  * pairs per plane:

@@ -259,7 +259,7 @@ def append_lengths_sink(n_sink: int, n_quant: int, n_tail: int, sink_cap: int, t
 #                        = (x[j][t], x[j][t + 1]) for channel group j and token
 #                        t = 16*kt + 2*tig + 8*r of the tile
 # ---------------------------------------------------------------------------
-SLOT_BITPOS = {2: (2, 4, 6, 8, 10, 12, 14, 0), 4: (0, 4, 8, 12), 8: (0, 8), 16: (0,)}
+SLOT_BITPOS = {2: (0, 2, 8, 10, 4, 6, 12, 14), 4: (0, 4, 8, 12), 8: (0, 8), 16: (0,)}
 
 
 @functools.lru_cache(maxsize=None)

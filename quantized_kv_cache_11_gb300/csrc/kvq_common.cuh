@@ -90,12 +90,12 @@ struct Tile {
 };
 
 // Bit position (within each 16-bit half of a word) of the codes in slot k.  For
-// 2-bit codes slots 0..7 sit at 2,4,6,8,10,12,14,0: slots 0-3 lie in the fp16
-// mantissa field as stored, slots 4-6 after a shift right by 8, slot 7 after a
-// shift left by 8.
+// 2-bit codes slots 0..7 sit at 0,2,8,10,4,6,12,14: the slots of fragment
+// registers 0 and 2 (one row, both k-halves) share a position after a shift
+// right by 8 of the second, as do those of registers 1 and 3.
 template <int BITS>
 __host__ __device__ constexpr int slot_bitpos(int k) {
-  return BITS == 2 ? ((k + 1) & 7) * 2 : BITS * k;
+  return BITS == 2 ? 2 * (k & 1) + 8 * ((k >> 1) & 1) + 4 * (k >> 2) : BITS * k;
 }
 
 // (token, channel) of the FIRST code of key pair P of a lane; the second code is

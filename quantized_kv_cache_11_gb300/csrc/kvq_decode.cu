@@ -15,15 +15,17 @@
 //   multi-stage cp.async ring in shared memory.
 // * Per 32-token group (one warp, the whole GQA group of G query heads):
 //   Q.K^T on tensor cores (mma.m16n8k16, fp16 in, fp32 accumulate).  The A
-//   operand is the codes as exact fp16 integers: one logic op ORs a code pair
-//   into the mantissas of 2^e (e chosen by the codes' bit position) and one
-//   fp16 subtraction removes 2^e.  B = q * scale, split into two fp16 halves
-//   (hi = fp16(q*s), lo = q*s - hi, exact), in separate columns, so the
-//   per-channel scale is applied to q once per group.  The zero points enter
-//   through one more small MMA (rows = zero points).  Online softmax in fp32;
-//   P.V likewise with B = p * scale (hi + lo) per 32-channel value group, the
-//   value zero points and the softmax denominator (a row of ones) from one
-//   small MMA.
+//   operand is the codes themselves: one mask per register leaves a code pair
+//   in the low mantissa bits of two fp16 halves with a zero exponent, which
+//   read as the subnormals c * 2^(p-24) (p = the codes' bit position; the
+//   tensor cores take fp16 subnormals exactly).  p depends only on the
+//   fragment row, so the power of two leaves the fp32 results per row.
+//   B = q * scale, split into two fp16 halves (hi = fp16(q*s), lo = q*s - hi,
+//   exact), in separate columns, so the per-channel scale is applied to q once
+//   per group.  The zero points enter through one more small MMA (rows = zero
+//   points).  Online softmax in fp32; P.V likewise with B = fp16(p * scale)
+//   per 32-channel value group, the value zero points and the softmax
+//   denominator (a row of ones) from one small MMA.
 // * Splits are merged by log-sum-exp; the last CTA to finish a (sequence, KV
 //   head) merges and writes the output, then resets its counter.  No spin-wait.
 #include <cmath>
@@ -37,12 +39,6 @@ constexpr int kTailWeight = 3;  // a 32-token fp16 tail chunk counts as this man
 // Polls of an mbarrier before a wait gives up (each poll may suspend the thread
 // briefly): far longer than any copy takes, short enough to end a stuck kernel.
 constexpr uint32_t kMaxPolls = 1u << 22;
-
-// half2(4), half2(16), half2(256), half2(64): OR-ing a code into the mantissa bits
-// whose unit is 1 (bits 8-9, 6-9, 2-9 and 4-5) gives 4 + c, 16 + c, 256 + c, 64 + c
-// exactly.  Kept in constant memory so the unpack's single logic op takes one
-// operand from there and the mask as an immediate.
-__constant__ uint32_t c_expo[4] = {0x44004400u, 0x4C004C00u, 0x5C005C00u, 0x54005400u};
 
 template <int D, int BITS, int G>
 struct DecodeCfg {
@@ -65,18 +61,17 @@ struct DecodeCfg {
   static constexpr int PSROW = 48;                   // halves per head row of the p~ exchange
   static constexpr int PS = WARPS * G * PSROW * 2;   // p~ exchange, bytes
   static constexpr int ZERO = 4 * D;                 // zero row for lanes without a metadata row
-  static constexpr int ONES = 64;                    // half2(1,1) x 16: the denominator row
   static constexpr int PREFIX = ((KVQ_MAX_BATCH + 1) * 4 + 15) / 16 * 16;
   static constexpr int QS = NT * 4 * (D / 2) * 4;     // q pairs of the segment's heads, lane order
   static constexpr int MBAR = (WARPS * NSTAGE + 1) * 8;  // one mbarrier per stage + the merge's
-  static constexpr int SMEM = RING + PS + ZERO + ONES + PREFIX + QS + MBAR;
+  static constexpr int SMEM = RING + PS + ZERO + PREFIX + QS + MBAR;
   // partials staged per merge batch: they fit the ring, their weights the p~ area
   static constexpr int MERGE_BATCH = RING / (G * PSTRIDE * 4) < PS / (4 * G) ? RING / (G * PSTRIDE * 4)
                                                                               : PS / (4 * G);
   static_assert(MERGE_BATCH >= 1, "a merge batch holds at least one partial");
   static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
   static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
-  static_assert(PS % 16 == 0 && RING % 16 == 0 && ZERO % 16 == 0 && ONES % 16 == 0 && PREFIX % 16 == 0 &&
+  static_assert(PS % 16 == 0 && RING % 16 == 0 && ZERO % 16 == 0 && PREFIX % 16 == 0 &&
                     QS % 16 == 0,
                 "aligned shared regions (the mbarriers need 8 bytes, the copies 16)");
   static_assert(NSTAGE * STAGE >= kGroup * (2 * D + 16), "a staged tail chunk fits a warp's ring");
@@ -163,12 +158,14 @@ template <int D, int BITS, int G>
 struct Decoder {
   using C = DecodeCfg<D, BITS, G>;
   static constexpr int NT = C::NT, KT = C::KT;
-  // fp16 offset carried by an unpacked code, by its register i = 0..3 in an mma
-  // A fragment (rows gid / gid+8 for i even / odd, first / second half of the k
-  // range for i < 2 / i >= 2): 2-bit codes 256, 64, 16, 4; wider codes one offset.
-  static __host__ __device__ constexpr float off(int i) {
-    return BITS == 2 ? (i == 0 ? 256.f : (i == 1 ? 64.f : (i == 2 ? 16.f : 4.f))) : (BITS == 4 ? 16.f : 256.f);
+  // Bit position p of the codes that unpack8 puts in register 4 mt + i (row half
+  // rh = i & 1 of an mma A fragment; never dependent on the k-half i >> 1): the
+  // register holds the fp16 subnormals c * 2^(p - 24).  unit = 2^(24 - p).
+  static __host__ __device__ constexpr int pos(int mt, int rh) {
+    return BITS == 2 ? 4 * mt + 2 * rh : (BITS == 4 ? 4 * rh : 0);
   }
+  static __host__ __device__ constexpr float unit(int mt, int rh) { return (float)(1 << (24 - pos(mt, rh))); }
+  static constexpr uint32_t kSixteenth = 0x2C002C00u;  // half2(1/16, 1/16)
   static constexpr uint32_t kOnes = 0x3C003C00u;  // half2(1, 1)
 
   // Per-warp running state of the online softmax for the G heads.
@@ -177,7 +174,6 @@ struct Decoder {
   float zc[NT][4];     // value-constant MMA: zero points, scale sums, row 12 = sum p~
   const uint32_t* qs;      // q pairs of column 8nt+gid (head 4nt + gid/2) in shared memory
   uint32_t nhl;            // half2(-hl): 0 for the hi column, -1 for the lo column
-  uint32_t hi_only;        // half2(1 - hl)
   uint32_t ones_a;         // the ones row (row 12) of the value-constant MMA: lanes gid 4
   int lane, gid, tig, hl;
 
@@ -188,7 +184,6 @@ struct Decoder {
     tig = lane & 3;
     hl = gid & 1;
     nhl = hl ? 0xBC00BC00u : 0u;
-    hi_only = hl ? 0u : kOnes;
     ones_a = gid == 4 ? kOnes : 0u;
     qs = q_smem + (gid >> 1) * (D / 2) + 4 * tig;
 #pragma unroll
@@ -207,37 +202,31 @@ struct Decoder {
     return *reinterpret_cast<const uint4*>(qs + nt * 4 * (D / 2) + 8 * kt);
   }
 
-  // fp16 pairs (off + c_first, off + c_second) of pairs P0 .. P0+7 of the lane's
-  // words (P0 a multiple of 8): one logic op per pair, plus two shifts per word at
-  // 2 bits.  2-bit slots 0-3 sit at bits 2, 4, 6, 8 (mantissa fields with offsets
-  // 256, 64, 16, 4 as stored), slots 4-6 at 10, 12, 14 (the same fields after a
-  // shift right by 8), slot 7 at 0 (bits 8-9 after a shift left by 8).
+  // Operands of pairs P0 .. P0+7 of the lane's words (P0 a multiple of 8): one
+  // mask per register (plus one shift right by 8 per word at 2 and 4 bits, per
+  // second pair at 8 bits) leaves each code pair in the mantissa bits [p, p+b)
+  // of the two halves, exponent 0.  Bit positions by register: 2 bits
+  // 0,2,0,2 | 4,6,4,6; 4 bits 0,4,0,4; 8 bits 0 (see pos()).
   static __device__ __forceinline__ void unpack8(const uint32_t* w, int P0, uint32_t (&a)[8]) {
     if (BITS == 2) {
-      const uint32_t x = w[P0 / 8];
-      const uint32_t y = x >> 8, z = x << 8;
-      const uint32_t e4 = c_expo[0], e16 = c_expo[1], e256 = c_expo[2], e64 = c_expo[3];
-      a[0] = (x & 0x000C000Cu) | e256;  a[4] = (y & 0x000C000Cu) | e256;
-      a[1] = (x & 0x00300030u) | e64;   a[5] = (y & 0x00300030u) | e64;
-      a[2] = (x & 0x00C000C0u) | e16;   a[6] = (y & 0x00C000C0u) | e16;
-      a[3] = (x & 0x03000300u) | e4;    a[7] = (z & 0x03000300u) | e4;
+      const uint32_t x = w[P0 / 8], y = x >> 8;
+      a[0] = x & 0x00030003u;  a[1] = x & 0x000C000Cu;  a[2] = y & 0x00030003u;  a[3] = y & 0x000C000Cu;
+      a[4] = x & 0x00300030u;  a[5] = x & 0x00C000C0u;  a[6] = y & 0x00300030u;  a[7] = y & 0x00C000C0u;
     } else if (BITS == 4) {
-      const uint32_t e16 = c_expo[1];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t x = w[P0 / 4 + h];
-        a[4 * h + 0] = ((x << 6) & 0x03C003C0u) | e16;
-        a[4 * h + 1] = ((x << 2) & 0x03C003C0u) | e16;
-        a[4 * h + 2] = ((x >> 2) & 0x03C003C0u) | e16;
-        a[4 * h + 3] = ((x >> 6) & 0x03C003C0u) | e16;
+        const uint32_t x = w[P0 / 4 + h], y = x >> 8;
+        a[4 * h + 0] = x & 0x000F000Fu;
+        a[4 * h + 1] = x & 0x00F000F0u;
+        a[4 * h + 2] = y & 0x000F000Fu;
+        a[4 * h + 3] = y & 0x00F000F0u;
       }
     } else {
-      const uint32_t e256 = c_expo[2];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const uint32_t x = w[P0 / 2 + h];
-        a[2 * h + 0] = ((x << 2) & 0x03FC03FCu) | e256;
-        a[2 * h + 1] = ((x >> 6) & 0x03FC03FCu) | e256;
+        a[2 * h + 0] = x & 0x00FF00FFu;
+        a[2 * h + 1] = (x >> 8) & 0x00FF00FFu;
       }
     }
   }
@@ -294,7 +283,7 @@ struct Decoder {
   }
 
   // p~ pairs for the V-side B fragments: column 8nt+gid (head 4nt + gid/2), tokens
-  // 16kt + 2tig + 8r and +1.
+  // 16kt + 2tig + 8r and +1; zero in the lo columns (odd gid), which P.V leaves empty.
   __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -303,14 +292,14 @@ struct Decoder {
       for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          pp[nt][kt][r] = (g < G) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r) : 0u;
+          pp[nt][kt][r] = (g < G && !hl) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r) : 0u;
     }
   }
 
   // One quantized 32-token group staged in shared memory.  zrow: a zero row of
   // at least D/2 words in shared memory.
   __device__ __forceinline__ void quant_group(const uint8_t* stage, __half* ps, const uint32_t* zrow,
-                                              const uint32_t* orow, float scale_log2) {
+                                              float scale_log2) {
     const uint4* s4 = reinterpret_cast<const uint4*>(stage);
     uint32_t kw[C::NWL];
 #pragma unroll
@@ -322,10 +311,8 @@ struct Decoder {
     const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);
     const uint32_t* ks = km + 4 * tig;           // scale pairs
     const uint32_t* kz = km + D / 2 + 4 * tig;   // zero-point pairs
-    // constant-MMA rows: 0 = zero points, 1 = scales of channels 16kt+[0,8),
-    // 2 = scales of channels 16kt+[8,16); a0 reads (kt, r=0) words, a2 (kt, r=1)
-    const uint32_t* rowA = gid == 0 ? kz : (gid == 1 ? ks : zrow);
-    const uint32_t* rowB = gid == 0 ? kz : (gid == 2 ? ks : zrow);
+    // constant-MMA row 0 = the zero points; a0 reads (kt, r=0) words, a2 (kt, r=1)
+    const uint32_t* rowz = gid == 0 ? kz : zrow;
     constexpr int CH = 2;  // two independent accumulation chains over kt (shorter MMA dependency)
     float sacc[CH][2][NT][4];
     float cacc[CH][NT][4];
@@ -342,8 +329,7 @@ struct Decoder {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) qv[nt] = qpairs(nt, kt2);
       const uint4 sv = *reinterpret_cast<const uint4*>(ks + 8 * kt2);
-      const uint4 av = *reinterpret_cast<const uint4*>(rowA + 8 * kt2);
-      const uint4 bv = *reinterpret_cast<const uint4*>(rowB + 8 * kt2);
+      const uint4 zv = *reinterpret_cast<const uint4*>(rowz + 8 * kt2);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int kt = kt2 + h;
@@ -352,7 +338,7 @@ struct Decoder {
         unpack8(kw, kt * 8, a);  // pairs of (kt, mt = 0) then (kt, mt = 1)
         const uint32_t a0[4] = {a[0], a[1], a[2], a[3]};
         const uint32_t a1[4] = {a[4], a[5], a[6], a[7]};
-        const uint32_t ac[4] = {h ? av.z : av.x, 0u, h ? bv.w : bv.y, 0u};
+        const uint32_t ac[4] = {h ? zv.z : zv.x, 0u, h ? zv.w : zv.y, 0u};
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const uint32_t q0 = h ? qv[nt].z : qv[nt].x, q1 = h ? qv[nt].w : qv[nt].y;
@@ -377,22 +363,29 @@ struct Decoder {
     float lg[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      // sum_d q z - sum over the halves of the k range of off * sum q s, head 4nt+tig;
-      // the offsets of token rows gid (r = 0) and gid + 8 (r = 1) differ at 2 bits
-      const float zq = __shfl_sync(0xffffffffu, cacc[0][nt][0], tig);
-      const float s0 = __shfl_sync(0xffffffffu, cacc[0][nt][0], 4 + tig);
-      const float s1 = __shfl_sync(0xffffffffu, cacc[0][nt][0], 8 + tig);
-      const float kc[2] = {zq - off(0) * s0 - off(2) * s1, zq - off(1) * s0 - off(3) * s1};
+      // sum_d q z of head 4nt+tig, plus the code products brought to unit scale
+      // (token row 16mt + gid + 8r holds codes at bit position pos(mt, r))
+      const float zq = __shfl_sync(0xffffffffu, cacc[0][nt][0], tig) * scale_log2;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          lg[nt][mt][r] = (sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + kc[r]) * scale_log2;
+          lg[nt][mt][r] = fmaf(sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1], scale_log2 * unit(mt, r), zq);
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
     load_pp(ps, pp);
-    // ---- P.V
+    // ---- P.V.  At 2 bits the codes of tokens 16..31 sit 4 bits above those of
+    // tokens 0..15 of the same row (pos(1, r) = pos(0, r) + 4): their p~ is
+    // divided by 16 (exactly, a power of two) so that both k-tiles share a unit.
+    uint32_t pv[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        pv[nt][0][r] = pp[nt][0][r];
+        pv[nt][1][r] = BITS == 2 ? h2_as_u32(__hmul2(u32_as_h2(pp[nt][1][r]), u32_as_h2(kSixteenth))) : pp[nt][1][r];
+      }
     uint32_t vw[C::NWL];
 #pragma unroll
     for (int ch = 0; ch < C::NWL / 4; ++ch) {
@@ -412,8 +405,8 @@ struct Decoder {
         uint32_t b[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          b[nt][0] = split_mul(pp[nt][kt][0], vs0);
-          b[nt][1] = split_mul(pp[nt][kt][1], vs1);
+          b[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][0]), u32_as_h2(vs0)));
+          b[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][1]), u32_as_h2(vs1)));
         }
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
@@ -427,17 +420,11 @@ struct Decoder {
       }
     }
     // constant-MMA rows (tokens 16kt + 2tig (+8r)): 0..D/32-1 = zero points of group
-    // j; 4+j = scales of group j, first token halves (a0 only); 8+j (a3) = scales,
-    // second token halves; 12 = ones (the softmax denominator)
-    const uint32_t* r0 = gid < D / 32 ? vzl + 16 * gid : (gid >= 4 && gid < 4 + D / 32 ? vsl + 16 * (gid - 4) : zrow);
-    const uint32_t* r2 = gid < D / 32 ? vzl + 16 * gid : zrow;
-    const uint32_t* r3 = gid < D / 32 ? vsl + 16 * gid : (gid == 4 ? orow + 4 * tig : zrow);
-    const uint4 v0 = *reinterpret_cast<const uint4*>(r0);
-    const uint4 v2 = *reinterpret_cast<const uint4*>(r2);
-    const uint4 v3 = *reinterpret_cast<const uint4*>(r3);
+    // j; 12 = ones (the softmax denominator); B = p~ as rounded
+    const uint4 v0 = *reinterpret_cast<const uint4*>(gid < D / 32 ? vzl + 16 * gid : zrow);
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
-      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v2.w : v2.y, kt ? v3.w : v3.y};
+      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v0.w : v0.y, ones_a};
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
     }
@@ -508,18 +495,12 @@ struct Decoder {
     const int vtok = (lane & 7) + 8 * (lane >> 4), vch = 8 * ((lane >> 3) & 1);
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
-      uint32_t bh[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        bh[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pp[nt][kt][0]), u32_as_h2(hi_only)));
-        bh[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pp[nt][kt][1]), u32_as_h2(hi_only)));
-      }
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
         uint32_t a[4];
         ldmatrix_x4_trans(a, buf + (16 * kt + vtok) * kPitch + (16 * mt + vch) * 2);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, bh[nt][0], bh[nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, pp[nt][kt][0], pp[nt][kt][1]);
       }
       const uint32_t ac[4] = {0u, ones_a, 0u, ones_a};  // denominator row only
 #pragma unroll
@@ -528,28 +509,35 @@ struct Decoder {
     __syncwarp();
   }
 
-  // Write this warp's partial (m, l, unnormalised o) for its G heads.
+  // After the last quantized group of a segment, before any fp16 chunk: bring
+  // the code products in o to unit scale (output rows gid / gid + 8 hold the
+  // codes of row half 0 / 1).
+  __device__ __forceinline__ void quant_done() {
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][nt][i] *= unit(0, i >> 1);
+  }
+
+  // Write this warp's partial (m, l, unnormalised o) for its G heads.  The lo
+  // columns of o are empty; row j of zc holds sum p~ z of value group j.
   __device__ __forceinline__ void write_partial(float* dst) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
       const float lt = __shfl_sync(0xffffffffu, zc[nt][2], 16 + tig);  // row 12: lanes gid 4
-      float vc[2][D / 32];  // output channel rows gid / gid + 8 of each 32-channel group
+      float zs[D / 32];
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        const float zs = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);         // row j
-        const float s0 = __shfl_sync(0xffffffffu, zc[nt][0], 4 * (4 + j) + tig);   // row 4+j
-        const float s1 = __shfl_sync(0xffffffffu, zc[nt][2], 4 * j + tig);         // row 8+j
-        vc[0][j] = zs - off(0) * s0 - off(2) * s1;
-        vc[1][j] = zs - off(1) * s0 - off(3) * s1;
-      }
+      for (int j = 0; j < D / 32; ++j) zs[j] = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);
       if (g < G) {
         float* d = dst + g * C::PSTRIDE;
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
-          d[4 + 16 * mt + gid] = o[mt][nt][0] + o[mt][nt][1] + vc[0][mt / 2];
-          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + o[mt][nt][3] + vc[1][mt / 2];
+          d[4 + 16 * mt + gid] = o[mt][nt][0] + zs[mt / 2];
+          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + zs[mt / 2];
         }
       }
     }
@@ -640,19 +628,17 @@ decode_kernel(const DecodeParams p) {
   uint8_t* ring = smem;
   __half* ps_all = reinterpret_cast<__half*>(smem + C::RING);
   uint32_t* zrow = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS);
-  uint32_t* orow = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS + C::ZERO);
-  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS + C::ZERO + C::ONES);
+  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS + C::ZERO);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t* q_smem = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS + C::ZERO + C::ONES + C::PREFIX);
+  uint32_t* q_smem = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS + C::ZERO + C::PREFIX);
   uint64_t* bars_all =
-      reinterpret_cast<uint64_t*>(smem + C::RING + C::PS + C::ZERO + C::ONES + C::PREFIX + C::QS);
+      reinterpret_cast<uint64_t*>(smem + C::RING + C::PS + C::ZERO + C::PREFIX + C::QS);
   uint64_t* bars = bars_all + warp * C::NSTAGE;
   uint64_t* merge_bar = bars_all + C::WARPS * C::NSTAGE;
   __half* ps = ps_all + warp * G * C::PSROW;
   uint8_t* wring = ring + warp * C::NSTAGE * C::STAGE;
 
   for (int i = threadIdx.x; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
-  if (threadIdx.x < C::ONES / 4) orow[threadIdx.x] = 0x3C003C00u;
   if (lane == 0) {
     for (int st = 0; st < C::NSTAGE; ++st) mbar_init(bars + st, 1);
     if (warp == 0) mbar_init(merge_bar, 1);
@@ -731,7 +717,7 @@ decode_kernel(const DecodeParams p) {
         parity ^= 1u << slotn;
         ++waited;
         if (!ok) { failed = true; break; }
-        dec.quant_group(wring + slotn * C::STAGE, ps, zrow, orow, p.scale_log2);
+        dec.quant_group(wring + slotn * C::STAGE, ps, zrow, p.scale_log2);
       }
       // after a timeout, wait (bounded) for this warp's copies still in flight
       for (; waited < issued; ++waited) {
@@ -740,6 +726,7 @@ decode_kernel(const DecodeParams p) {
         parity ^= 1u << slotn;
       }
       __syncwarp();
+      dec.quant_done();
     }
     if (failed && lane == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
     // fp16 chunks (tail, then sinks) whose first weighted item falls in this warp's range

@@ -17,14 +17,16 @@
 //   into a private byte ring, several copies in flight, completion on mbarriers
 //   with bounded waits.
 // * Per block (one warp, the GQA group's G heads): Q.K^T runs over the three key
-//   classes with the codes turned into exact fp16 operands by one logic op per
-//   pair (2^e OR code), B = q * scale split into fp16 hi + lo, and the zero
-//   points and the 2^e offsets removed through one constant product per k-tile
-//   (rows: zero points, and the scales of each class); masked tokens of a
-//   partial block get -inf.  Online softmax (exp2 domain).  P.V by value class:
-//   codes with B = p~ * scale (hi + lo) and one constant product per class
-//   accumulator (zero points, offset rows, the ones row = the denominator), or
-//   fp16 tiles whose words are the A fragments as stored.
+//   classes with the codes turned into fp16 operands by one mask per register
+//   (the code pair left in the low mantissa bits, exponent 0: the exact
+//   subnormals c * 2^(p-24), p the bit position, which depends only on the
+//   fragment row and the class), B = q * scale split into fp16 hi + lo, one
+//   accumulator per class brought to unit scale per row, and the zero points
+//   through one constant product per k-tile; masked tokens of a partial block
+//   get -inf.  Online softmax (exp2 domain).  P.V by value class: codes with
+//   B = fp16(p~ * scale), the accumulator rescaled by a power of two when the
+//   value width changes, and one constant product (zero points, the ones row =
+//   the denominator); or fp16 tiles whose words are the A fragments as stored.
 // * Splits merge by log-sum-exp; the last CTA of a segment writes the output
 //   and resets the segment's counter.  No spin-wait on other CTAs.
 #include <cmath>
@@ -37,12 +39,21 @@ namespace kvq {
 namespace tz {
 
 constexpr uint32_t kMaxPolls = 1u << 22;
-// half2(4), half2(16), half2(256), half2(64): a code OR-ed into the mantissa bits
-// whose unit is 1 gives 4 + c, 16 + c, 256 + c, 64 + c exactly
-__constant__ uint32_t c_tz_expo[4] = {0x44004400u, 0x4C004C00u, 0x5C005C00u, 0x54005400u};
-// offset of a 2-bit code by its register i = 0..3 in an mma A fragment (2-bit slots
-// 0..7 sit at bits 2,4,6,8,10,12,14,0)
-__host__ __device__ constexpr float off2(int i) { return i == 0 ? 256.f : (i == 1 ? 64.f : (i == 2 ? 16.f : 4.f)); }
+// Bit position of the codes that unpack8<BITS> puts in register 4 mt + i (row
+// half rh = i & 1; the same for both k-halves): the register holds the fp16
+// subnormals c * 2^(p - 24), so unit = 2^(24 - p) brings a product to unit scale.
+__host__ __device__ constexpr int code_pos(int bits, int mt, int rh) {
+  return bits == 2 ? 4 * mt + 2 * rh : (bits == 4 ? 4 * rh : 0);
+}
+__host__ __device__ constexpr float code_unit(int bits, int mt, int rh) {
+  return (float)(1 << (24 - code_pos(bits, mt, rh)));
+}
+// Unit of the P.V accumulator rows of half rh while a warp decodes blocks of value
+// kind k (widths 2, 4, 8: the codes' unit, with the 2-bit tokens 16..31 brought
+// to the unit of tokens 0..15; 16 and fresh: 1).
+__device__ __forceinline__ float value_unit(int k, int rh) {
+  return k == 0 ? code_unit(2, 0, rh) : (k == 1 ? code_unit(4, 0, rh) : (k == 2 ? code_unit(8, 0, rh) : 1.f));
+}
 
 template <int G>
 struct Cfg {
@@ -57,14 +68,13 @@ struct Cfg {
   static constexpr int RINGS = WARPS * RING;
   static constexpr int PS = WARPS * G * PSROW * 2;
   static constexpr int ZERO = 4 * kDim;
-  static constexpr int ONES = 64;
   static constexpr int PREFIX = ((KVQ_TZ_MAX_SEGMENTS + 1) * 8 + 15) / 16 * 16;
   static constexpr int QP = 4 * NT * QPH * 4;
   static constexpr int QN = NT * 4 * (kDim / 2) * 4;
   static constexpr int HDR = 128 + 2 * kSlots;
   static constexpr int FIFO = WARPS * NBAR * 8;
   static constexpr int MBAR = (WARPS * NBAR + 1) * 8;
-  static constexpr int SMEM = RINGS + PS + ZERO + ONES + PREFIX + QP + QN + HDR + FIFO + MBAR;
+  static constexpr int SMEM = RINGS + PS + ZERO + PREFIX + QP + QN + HDR + FIFO + MBAR;
   static constexpr int MERGE_BATCH =
       RINGS / (G * PSTRIDE * 4) < PS / (4 * G) ? RINGS / (G * PSTRIDE * 4) : PS / (4 * G);
   static_assert(RING >= KVQ_TZ_FRESH_BLOCK_BYTES && RING >= KVQ_TZ_MAX_BLOCK_BYTES, "a record fits a ring");
@@ -137,30 +147,30 @@ struct Decoder {
   using C = Cfg<G>;
   static constexpr int NT = C::NT;
   static constexpr uint32_t kOnes = 0x3C003C00u;
+  static constexpr uint32_t kSixteenth = 0x2C002C00u;  // half2(1/16, 1/16)
   float m[NT];
-  float o[8][NT][4];    // P.V: rows = channels (8 tiles of 16), columns (head, hi|lo)
-  float zc[3][NT][4];   // value-constant products per value class (offsets differ)
+  float o[8][NT][4];    // P.V: rows = channels (8 tiles of 16), columns (head, hi|lo); lo stays 0
+  float zc[NT][4];      // value-constant products: rows j = sum p~ z of group j, 12 = sum p~
   const uint32_t* qp;   // slot-ordered q pairs of this lane's column
   const uint32_t* qn;   // natural-order q pairs of this lane's column
-  uint32_t nhl, hi_only, ones_a;
+  uint32_t nhl, ones_a;
   int lane, gid, tig;
+  int ukind;            // o holds value_unit(ukind, rh) times the true sums
 
   __device__ __forceinline__ void init(const uint32_t* qp_smem, const uint32_t* qn_smem) {
     lane = threadIdx.x & 31;
     gid = lane >> 2;
     tig = lane & 3;
     nhl = (gid & 1) ? 0xBC00BC00u : 0u;
-    hi_only = (gid & 1) ? 0u : kOnes;
     ones_a = gid == 4 ? kOnes : 0u;
+    ukind = 3;
     qp = qp_smem + (gid >> 1) * C::QPH + 2 * tig;
     qn = qn_smem + (gid >> 1) * (kDim / 2) + 4 * tig;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt] = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        zc[0][nt][i] = 0.f; zc[1][nt][i] = 0.f; zc[2][nt][i] = 0.f;
-      }
+      for (int i = 0; i < 4; ++i) zc[nt][i] = 0.f;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -175,34 +185,30 @@ struct Decoder {
     return h2_as_u32(__hfma2(x, y, __hmul2_rn(hi, u32_as_h2(nhl))));
   }
 
-  // fp16 pairs (off + first, off + second) of the 8 pairs in w[0 .. C/2).
+  // Operands of the 8 pairs in w[0 .. BITS/2): one mask per register leaves a
+  // code pair in mantissa bits [p, p + BITS) of the two halves, exponent 0 (one
+  // shift right by 8 per word at 2 and 4 bits, per second pair at 8 bits).
   template <int BITS>
   static __device__ __forceinline__ void unpack8(const uint32_t* w, uint32_t (&a)[8]) {
     if (BITS == 2) {
-      const uint32_t x = w[0];
-      const uint32_t y = x >> 8, z = x << 8;
-      const uint32_t e4 = c_tz_expo[0], e16 = c_tz_expo[1], e256 = c_tz_expo[2], e64 = c_tz_expo[3];
-      a[0] = (x & 0x000C000Cu) | e256;  a[4] = (y & 0x000C000Cu) | e256;
-      a[1] = (x & 0x00300030u) | e64;   a[5] = (y & 0x00300030u) | e64;
-      a[2] = (x & 0x00C000C0u) | e16;   a[6] = (y & 0x00C000C0u) | e16;
-      a[3] = (x & 0x03000300u) | e4;    a[7] = (z & 0x03000300u) | e4;
+      const uint32_t x = w[0], y = x >> 8;
+      a[0] = x & 0x00030003u;  a[1] = x & 0x000C000Cu;  a[2] = y & 0x00030003u;  a[3] = y & 0x000C000Cu;
+      a[4] = x & 0x00300030u;  a[5] = x & 0x00C000C0u;  a[6] = y & 0x00300030u;  a[7] = y & 0x00C000C0u;
     } else if (BITS == 4) {
-      const uint32_t e16 = c_tz_expo[1];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t x = w[h];
-        a[4 * h + 0] = ((x << 6) & 0x03C003C0u) | e16;
-        a[4 * h + 1] = ((x << 2) & 0x03C003C0u) | e16;
-        a[4 * h + 2] = ((x >> 2) & 0x03C003C0u) | e16;
-        a[4 * h + 3] = ((x >> 6) & 0x03C003C0u) | e16;
+        const uint32_t x = w[h], y = x >> 8;
+        a[4 * h + 0] = x & 0x000F000Fu;
+        a[4 * h + 1] = x & 0x00F000F0u;
+        a[4 * h + 2] = y & 0x000F000Fu;
+        a[4 * h + 3] = y & 0x00F000F0u;
       }
     } else {
-      const uint32_t e256 = c_tz_expo[2];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const uint32_t x = w[h];
-        a[2 * h + 0] = ((x << 2) & 0x03FC03FCu) | e256;
-        a[2 * h + 1] = ((x >> 6) & 0x03FC03FCu) | e256;
+        a[2 * h + 0] = x & 0x00FF00FFu;
+        a[2 * h + 1] = (x >> 8) & 0x00FF00FFu;
       }
     }
   }
@@ -210,8 +216,8 @@ struct Decoder {
   // One k-tile of key class BITS: codes of sub-tile word row j, global k-tile kt.
   template <int BITS>
   __device__ __forceinline__ void key_tile(const uint32_t* sub, int j, int kt, const uint32_t* ksc,
-                                           const uint32_t* kze, uint32_t mz, uint32_t m0, uint32_t m1,
-                                           float (&s0)[NT][4], float (&s1)[NT][4], float (&cc)[NT][4]) const {
+                                           const uint32_t* kze, uint32_t mz, float (&s0)[NT][4],
+                                           float (&s1)[NT][4], float (&cc)[NT][4]) const {
     uint32_t w[BITS / 2];
 #pragma unroll
     for (int i = 0; i < BITS / 2; ++i) w[i] = sub[(j * (BITS / 2) + i) * 32 + lane];
@@ -221,7 +227,7 @@ struct Decoder {
     const uint2 zv = *reinterpret_cast<const uint2*>(kze + 8 * kt);
     const uint32_t a0[4] = {a[0], a[1], a[2], a[3]};
     const uint32_t a1[4] = {a[4], a[5], a[6], a[7]};
-    const uint32_t ac[4] = {(zv.x & mz) | (sv.x & m0), 0u, (zv.y & mz) | (sv.y & m1), 0u};
+    const uint32_t ac[4] = {zv.x & mz, 0u, zv.y & mz, 0u};  // row 0: the zero points
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const uint2 qv = *reinterpret_cast<const uint2*>(qp + nt * 4 * C::QPH + 8 * kt);
@@ -232,21 +238,34 @@ struct Decoder {
     }
   }
 
-  // All k-tiles of one key class; k-tiles alternate between two accumulation
-  // chains (shorter MMA dependency chains).
+  // All k-tiles of one key class into the class's accumulators; k-tiles
+  // alternate between two accumulation chains (shorter MMA dependency chains).
   template <int BITS>
   __device__ __forceinline__ void key_class(const uint32_t* sub, int ktc, int& kt, const uint32_t* ksc,
-                                            const uint32_t* kze, uint32_t mz, uint32_t m0, uint32_t m1,
-                                            float (&sacc)[2][2][NT][4], float (&cc)[NT][4]) const {
+                                            const uint32_t* kze, uint32_t mz, float (&sacc)[2][2][NT][4],
+                                            float (&cc)[NT][4]) const {
     int j = 0;
     for (; j + 1 < ktc; j += 2, kt += 2) {
-      key_tile<BITS>(sub, j, kt, ksc, kze, mz, m0, m1, sacc[0][0], sacc[0][1], cc);
-      key_tile<BITS>(sub, j + 1, kt + 1, ksc, kze, mz, m0, m1, sacc[1][0], sacc[1][1], cc);
+      key_tile<BITS>(sub, j, kt, ksc, kze, mz, sacc[0][0], sacc[0][1], cc);
+      key_tile<BITS>(sub, j + 1, kt + 1, ksc, kze, mz, sacc[1][0], sacc[1][1], cc);
     }
     if (j < ktc) {
-      key_tile<BITS>(sub, j, kt, ksc, kze, mz, m0, m1, sacc[0][0], sacc[0][1], cc);
+      key_tile<BITS>(sub, j, kt, ksc, kze, mz, sacc[0][0], sacc[0][1], cc);
       ++kt;
     }
+  }
+
+  // Rescale o from the unit of value kind ukind to that of kind k (powers of two).
+  __device__ __forceinline__ void set_units(int k) {
+    if (k == ukind) return;  // warp-uniform
+    const float r0 = value_unit(ukind, 0) / value_unit(k, 0), r1 = value_unit(ukind, 1) / value_unit(k, 1);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        o[mt][nt][0] *= r0; o[mt][nt][1] *= r0; o[mt][nt][2] *= r1; o[mt][nt][3] *= r1;
+      }
+    ukind = k;
   }
 
   // Online softmax over one 32-token block; writes p~ (fp16) to ps[g][t].
@@ -269,9 +288,7 @@ struct Decoder {
         const float alpha = (mnew == m[nt]) ? 1.f : fast_exp2(m[nt] - mnew);
         m[nt] = mnew;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          zc[0][nt][i] *= alpha; zc[1][nt][i] *= alpha; zc[2][nt][i] *= alpha;
-        }
+        for (int i = 0; i < 4; ++i) zc[nt][i] *= alpha;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -293,6 +310,7 @@ struct Decoder {
     __syncwarp();
   }
 
+  // p~ pairs of column 8nt + gid (head 4nt + gid/2); zero in the lo columns (odd gid).
   __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -302,14 +320,14 @@ struct Decoder {
 #pragma unroll
         for (int r = 0; r < 2; ++r)
           pp[nt][kt][r] =
-              (g < G) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r) : 0u;
+              (g < G && !(gid & 1)) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r)
+                                    : 0u;
     }
   }
 
   // P.V over a value tile of codes (class VC: width 2 << VC) and its metadata.
   template <int VC>
-  __device__ __forceinline__ void pv_codes(const uint8_t* vt, const uint32_t (&pp)[NT][2][2], const uint32_t* zrow,
-                                           const uint32_t* orow) {
+  __device__ __forceinline__ void pv_codes(const uint8_t* vt, const uint32_t (&pp)[NT][2][2], const uint32_t* zrow) {
     constexpr int BITS = 2 << VC;
     constexpr int TB = Tile<kDim, BITS>::kBytes;
     constexpr int NWL = Tile<kDim, BITS>::kWordsPerLane;
@@ -323,6 +341,16 @@ struct Decoder {
     const uint32_t* vm = reinterpret_cast<const uint32_t*>(vt + TB);
     const uint32_t* vsl = vm + 4 * tig;             // scale pairs
     const uint32_t* vzl = vm + kDim / 2 + 4 * tig;  // zero-point pairs
+    // 2-bit codes of tokens 16..31 sit 4 bits above those of tokens 0..15 of the
+    // same row: their p~ is divided by 16 (exactly) for a common unit
+    uint32_t pv[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        pv[nt][0][r] = pp[nt][0][r];
+        pv[nt][1][r] = BITS == 2 ? h2_as_u32(__hmul2(u32_as_h2(pp[nt][1][r]), u32_as_h2(kSixteenth))) : pp[nt][1][r];
+      }
 #pragma unroll
     for (int j = 0; j < kDim / 32; ++j) {
       const uint4 sv = *reinterpret_cast<const uint4*>(vsl + 16 * j);
@@ -332,8 +360,8 @@ struct Decoder {
         uint32_t b[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          b[nt][0] = split_mul(pp[nt][kt][0], vs0);
-          b[nt][1] = split_mul(pp[nt][kt][1], vs1);
+          b[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][0]), u32_as_h2(vs0)));
+          b[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][1]), u32_as_h2(vs1)));
         }
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
@@ -346,19 +374,13 @@ struct Decoder {
         }
       }
     }
-    // constant rows (tokens 16kt + 2tig (+8r)): 0..3 zero points of group j,
-    // 4..7 scales (first token halves), 8..11 scales (second halves), 12 ones
-    const uint32_t* r0 = gid < 4 ? vzl + 16 * gid : vsl + 16 * (gid - 4);
-    const uint32_t* r2 = gid < 4 ? vzl + 16 * gid : zrow;
-    const uint32_t* r3 = gid < 4 ? vsl + 16 * gid : (gid == 4 ? orow + 4 * tig : zrow);
-    const uint4 v0 = *reinterpret_cast<const uint4*>(r0);
-    const uint4 v2 = *reinterpret_cast<const uint4*>(r2);
-    const uint4 v3 = *reinterpret_cast<const uint4*>(r3);
+    // constant rows (tokens 16kt + 2tig (+8r)): 0..3 zero points of group j, 12 ones
+    const uint4 v0 = *reinterpret_cast<const uint4*>(gid < 4 ? vzl + 16 * gid : zrow);
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
-      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v2.w : v2.y, kt ? v3.w : v3.y};
+      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v0.w : v0.y, ones_a};
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[VC][nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
+      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
     }
   }
 
@@ -367,81 +389,78 @@ struct Decoder {
     const uint4* s4 = reinterpret_cast<const uint4*>(vt);
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
-      uint32_t bh[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        bh[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pp[nt][kt][0]), u32_as_h2(hi_only)));
-        bh[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pp[nt][kt][1]), u32_as_h2(hi_only)));
-      }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const uint4 v = s4[(2 * mt + kt) * 32 + lane];
         const uint32_t a[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, bh[nt][0], bh[nt][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, pp[nt][kt][0], pp[nt][kt][1]);
       }
       const uint32_t ac[4] = {0u, ones_a, 0u, ones_a};  // the denominator row only
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[0][nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
+      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
     }
   }
 
   // A block of zone A/B: keys quantized in three classes, values by kind.
   __device__ __forceinline__ void quant_block(const uint8_t* rec, int kind, int nvalid, const int* hd, __half* ps,
-                                              const uint32_t* zrow, const uint32_t* orow, float scale_log2) {
+                                              const uint32_t* zrow, float scale_log2) {
     const int kt2 = hd[H_KT], kt4 = hd[H_KT + 1], kt8 = hd[H_KT + 2], KT = kt2 + kt4 + kt8;
     const uint32_t* st = reinterpret_cast<const uint32_t*>(rec);
     const uint32_t* ksc = st + key_code_bytes(kt2, kt4, kt8) / 4 + 2 * tig;
     const uint32_t* kze = ksc + 8 * KT;
-    float sacc[2][2][NT][4];
+    set_units(kind);
+    float sacc[3][2][2][NT][4];  // [key class][chain][mt]
     float cc[NT][4];
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int c = 0; c < 3; ++c)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) { sacc[c][0][nt][i] = 0.f; sacc[c][1][nt][i] = 0.f; cc[nt][i] = 0.f; }
-    // constant-product rows: 0 = zero points; 1, 2 = scales of the 2-bit class
-    // (first / second half of a k-tile; the offsets depend on the token row too:
-    // off2); 3 = 4-bit scales (16); 4 = 8-bit scales (256)
-    const uint32_t mz = gid == 0 ? ~0u : 0u;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) { sacc[c][h][0][nt][i] = 0.f; sacc[c][h][1][nt][i] = 0.f; }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cc[nt][i] = 0.f;
+    const uint32_t mz = gid == 0 ? ~0u : 0u;  // constant-product row 0: the zero points
     int kt = 0;
-    key_class<2>(st, kt2, kt, ksc, kze, mz, gid == 1 ? ~0u : 0u, gid == 2 ? ~0u : 0u, sacc, cc);
-    key_class<4>(st + 32 * kt2, kt4, kt, ksc, kze, mz, gid == 3 ? ~0u : 0u, gid == 3 ? ~0u : 0u, sacc, cc);
-    key_class<8>(st + 32 * kt2 + 64 * kt4, kt8, kt, ksc, kze, mz, gid == 4 ? ~0u : 0u, gid == 4 ? ~0u : 0u, sacc,
-                 cc);
+    key_class<2>(st, kt2, kt, ksc, kze, mz, sacc[0], cc);
+    key_class<4>(st + 32 * kt2, kt4, kt, ksc, kze, mz, sacc[1], cc);
+    key_class<8>(st + 32 * kt2 + 64 * kt4, kt8, kt, ksc, kze, mz, sacc[2], cc);
     float lg[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float zq = __shfl_sync(0xffffffffu, cc[nt][0], tig);
-      const float s1 = __shfl_sync(0xffffffffu, cc[nt][0], 4 + tig);
-      const float s2 = __shfl_sync(0xffffffffu, cc[nt][0], 8 + tig);
-      const float s3 = __shfl_sync(0xffffffffu, cc[nt][0], 12 + tig);
-      const float s4 = __shfl_sync(0xffffffffu, cc[nt][0], 16 + tig);
-      const float kc48 = zq - 16.f * s3 - 256.f * s4;
-      const float kc[2] = {kc48 - off2(0) * s1 - off2(2) * s2, kc48 - off2(1) * s1 - off2(3) * s2};
+      const float zq = __shfl_sync(0xffffffffu, cc[nt][0], tig) * scale_log2;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const float x = sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + sacc[1][mt][nt][2 * r] +
-                          sacc[1][mt][nt][2 * r + 1] + kc[r];
-          lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? x * scale_log2 : -INFINITY;
+          float x = zq;
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            const float sc = sacc[c][0][mt][nt][2 * r] + sacc[c][0][mt][nt][2 * r + 1] +
+                             sacc[c][1][mt][nt][2 * r] + sacc[c][1][mt][nt][2 * r + 1];
+            x = fmaf(sc, scale_log2 * code_unit(2 << c, mt, r), x);
+          }
+          lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? x : -INFINITY;
         }
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
     load_pp(ps, pp);
     const uint8_t* vt = rec + key_bytes(kt2, kt4, kt8);
-    if (kind == 0) pv_codes<0>(vt, pp, zrow, orow);
-    else if (kind == 1) pv_codes<1>(vt, pp, zrow, orow);
-    else if (kind == 2) pv_codes<2>(vt, pp, zrow, orow);
+    if (kind == 0) pv_codes<0>(vt, pp, zrow);
+    else if (kind == 1) pv_codes<1>(vt, pp, zrow);
+    else if (kind == 2) pv_codes<2>(vt, pp, zrow);
     else pv_fp16(vt, pp);
     __syncwarp();
   }
 
   // A fresh block (zone C): fp16 key tile in natural channel order, fp16 values.
   __device__ __forceinline__ void fresh_block(const uint8_t* rec, int nvalid, __half* ps, float scale_log2) {
+    set_units(3);  // fp16 values: unit 1, as zone B
     const uint4* s4 = reinterpret_cast<const uint4*>(rec);
     float sacc[2][NT][4];
 #pragma unroll
@@ -479,37 +498,24 @@ struct Decoder {
     __syncwarp();
   }
 
-  // This warp's partial (m, l, unnormalised o) for its G heads.
-  __device__ __forceinline__ void write_partial(float* dst) const {
-    // offsets of the value classes' codes by A-fragment register i: 2-bit off2(i),
-    // 4-bit 16, 8-bit 256; output rows gid take registers 0 and 2, rows gid + 8
-    // registers 1 and 3
-    constexpr float off[3][4] = {{256.f, 64.f, 16.f, 4.f}, {16.f, 16.f, 16.f, 16.f}, {256.f, 256.f, 256.f, 256.f}};
+  // This warp's partial (m, l, unnormalised o) for its G heads; o is brought to
+  // unit scale first.
+  __device__ __forceinline__ void write_partial(float* dst) {
+    set_units(3);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
-      float lt = 0.f, vc[2][kDim / 32];
+      const float lt = __shfl_sync(0xffffffffu, zc[nt][2], 16 + tig);  // row 12
+      float zs[kDim / 32];
 #pragma unroll
-      for (int j = 0; j < kDim / 32; ++j) { vc[0][j] = 0.f; vc[1][j] = 0.f; }
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        lt += __shfl_sync(0xffffffffu, zc[c][nt][2], 16 + tig);  // row 12
-#pragma unroll
-        for (int j = 0; j < kDim / 32; ++j) {
-          const float zs = __shfl_sync(0xffffffffu, zc[c][nt][0], 4 * j + tig);        // row j
-          const float s0 = __shfl_sync(0xffffffffu, zc[c][nt][0], 4 * (4 + j) + tig);  // row 4+j
-          const float s1 = __shfl_sync(0xffffffffu, zc[c][nt][2], 4 * j + tig);        // row 8+j
-          vc[0][j] += zs - off[c][0] * s0 - off[c][2] * s1;
-          vc[1][j] += zs - off[c][1] * s0 - off[c][3] * s1;
-        }
-      }
+      for (int j = 0; j < kDim / 32; ++j) zs[j] = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);  // row j
       if (g < G) {
         float* d = dst + g * C::PSTRIDE;
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          d[4 + 16 * mt + gid] = o[mt][nt][0] + o[mt][nt][1] + vc[0][mt / 2];
-          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + o[mt][nt][3] + vc[1][mt / 2];
+          d[4 + 16 * mt + gid] = o[mt][nt][0] + zs[mt / 2];
+          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + zs[mt / 2];
         }
       }
     }
@@ -597,8 +603,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
   uint8_t* rings = smem;
   __half* ps_all = reinterpret_cast<__half*>(smem + C::RINGS);
   uint32_t* zrow = reinterpret_cast<uint32_t*>(smem + C::RINGS + C::PS);
-  uint32_t* orow = zrow + C::ZERO / 4;
-  int64_t* s_pref = reinterpret_cast<int64_t*>(smem + C::RINGS + C::PS + C::ZERO + C::ONES);
+  int64_t* s_pref = reinterpret_cast<int64_t*>(smem + C::RINGS + C::PS + C::ZERO);
   uint32_t* qp_smem = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(s_pref) + C::PREFIX);
   uint32_t* qn_smem = qp_smem + C::QP / 4;
   int* s_hdr = reinterpret_cast<int*>(qn_smem + C::QN / 4);
@@ -613,7 +618,6 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
   uint8_t* ring = rings + warp * C::RING;
 
   for (int i = tid; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
-  if (tid < C::ONES / 4) orow[tid] = 0x3C003C00u;
   if (lane == 0) {
     for (int i = 0; i < C::NBAR; ++i) mbar_init(bars + i, 1);
     if (warp == 0) mbar_init(merge_bar, 1);
@@ -756,7 +760,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
         const int k = kb >> 24, blk = kb & 0xFFFFFF;
         const int cnt = k < 4 ? s_hdr[H_NTOK + k] : s_hdr[H_NFRESH];
         const int nvalid = min(kGroup, cnt - kGroup * blk);
-        if (k < 4) dec.quant_block(ring + off, k, nvalid, s_hdr, ps, zrow, orow, p.scale_log2);
+        if (k < 4) dec.quant_block(ring + off, k, nvalid, s_hdr, ps, zrow, p.scale_log2);
         else dec.fresh_block(ring + off, nvalid, ps, p.scale_log2);
         ++done;
         fill();

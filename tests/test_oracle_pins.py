@@ -325,20 +325,21 @@ def test_flushed_group_equals_prefill_quantization():
 # Positions derived by hand from the PTX ISA's mma.m16n8k16 .f16 A-fragment
 # table (a0: row gid, cols 2*tig..+1; a1: row gid+8; a2: cols +8; a3: both) and
 # the tile rules: lane = 4*gid + tig; pair P -> word P // (16/b), slot P % (16/b);
-# first code at bits [b*slot, +b), second at [16 + b*slot, +b); lane word w at
+# first code at bits [p, +b), second at [16 + p, +b) with p the slot's bit position (b*slot at 4
+# and 8 bits; 2-bit slots 0..7 at 0, 2, 8, 10, 4, 6, 12, 14); lane word w at
 # byte ((w // 4) * 32 + lane) * 16 + (w % 4) * 4.
 KPOS_2BIT_D128 = [
     # (token, channel) -> (byte offset of the 32-bit word, bit offset); 2-bit slot
-    # bit positions (2, 4, 6, 8, 10, 12, 14, 0)
-    ((0, 0), (0, 2)), ((0, 1), (0, 18)), ((8, 0), (0, 4)), ((0, 8), (0, 6)),
-    ((8, 9), (0, 24)), ((16, 0), (0, 10)), ((24, 8), (0, 0)), ((1, 0), (64, 2)),
-    ((0, 2), (16, 2)), ((0, 16), (4, 2)), ((0, 64), (512, 2)), ((31, 127), (1020, 16)),
+    # bit positions (0, 2, 8, 10, 4, 6, 12, 14)
+    ((0, 0), (0, 0)), ((0, 1), (0, 16)), ((8, 0), (0, 2)), ((0, 8), (0, 8)),
+    ((8, 9), (0, 26)), ((16, 0), (0, 4)), ((24, 8), (0, 14)), ((1, 0), (64, 0)),
+    ((0, 2), (16, 0)), ((0, 16), (4, 0)), ((0, 64), (512, 0)), ((31, 127), (1020, 30)),
 ]
 KPOS_4BIT_D128 = [((0, 0), (0, 0)), ((16, 0), (4, 0)), ((8, 1), (0, 20)), ((0, 16), (8, 0)),
                   ((0, 32), (512, 0))]
 VPOS_2BIT_D128 = [
-    ((0, 0), (0, 2)), ((1, 0), (0, 18)), ((0, 8), (0, 4)), ((8, 0), (0, 6)),
-    ((16, 0), (0, 10)), ((2, 0), (16, 2)), ((0, 1), (64, 2)), ((0, 16), (4, 2)),
+    ((0, 0), (0, 0)), ((1, 0), (0, 16)), ((0, 8), (0, 2)), ((8, 0), (0, 8)),
+    ((16, 0), (0, 4)), ((2, 0), (16, 0)), ((0, 1), (64, 0)), ((0, 16), (4, 0)),
 ]
 
 
@@ -469,8 +470,8 @@ def test_trizone_channel_order_by_hand():
 # hand from the fragment layout: lane 4 gid + tig; pair P = 8 kt + 4 mt + i covers
 # token 16 mt + gid + 8 (i % 2), channels 16 kt + 2 tig + 8 (i // 2) and +1.
 KSUB_POS = {
-    (1, 2): {(0, 0): (0, 2), (0, 1): (0, 18), (8, 0): (0, 4), (0, 8): (0, 6), (8, 8): (0, 8),
-             (16, 0): (0, 10), (31, 15): (31, 16), (31, 14): (31, 0)},
+    (1, 2): {(0, 0): (0, 0), (0, 1): (0, 16), (8, 0): (0, 2), (0, 8): (0, 8), (8, 8): (0, 10),
+             (16, 0): (0, 4), (31, 15): (31, 30), (31, 14): (31, 14)},
     (3, 4): {(25, 2): (37, 4), (25, 3): (37, 20), (0, 16): (64, 0), (31, 47): (191, 28)},
     (2, 8): {(9, 1): (4, 24), (0, 0): (0, 0), (16, 16): (192, 0)},
 }
