@@ -160,3 +160,19 @@ def random_groups(seed: int, n: int, dist: str = "normal", scale: float = 1.0,
     else:
         raise ValueError(dist)
     return x.clamp(-60000, 60000).half().numpy()
+
+
+def prompt_queries(w: Workload, batches=None) -> np.ndarray:
+    """Query vectors of every prompt position, float16 [B, T, Hq, D], standard
+    normals drawn with their own generator (seed + 1000, one batch row after
+    another) so the draws of ``generate`` are unchanged.  ``batches``: the rows
+    to return (default all); rows are drawn in order, so a subset matches the
+    full draw."""
+    g = torch.Generator().manual_seed(w.seed + 1000)
+    want = range(w.batch) if batches is None else sorted(batches)
+    out = []
+    for b in range(max(want) + 1):
+        x = torch.randn((w.context, w.n_q_heads, w.head_dim), generator=g, dtype=torch.float32).half()
+        if b in want:
+            out.append(x.numpy())
+    return np.stack(out)
