@@ -1,5 +1,5 @@
-"""Thin Python binding of libkvq.so (the C ABI declared in include/kvq.h and
-include/kvq_trizone.h).
+"""Thin Python binding of libkvq.so (the C ABI declared in include/kvq.h,
+include/kvq_trizone.h and include/kvq_rdkv.h).
 
 Argument marshalling only: every step of the quantizer and of the decode runs
 in the library's CUDA kernels.  Tensors are PyTorch CUDA tensors; PyTorch is
@@ -39,12 +39,14 @@ KVQ_TZ_FRESH_BLOCK_BYTES = 16384
 KVQ_TZ_MAX_SEGMENTS = 1024
 KVQ_TZ_NBUF = 3
 KVQ_TZ_BUF_INDEX, KVQ_TZ_BUF_TOKENS, KVQ_TZ_BUF_BLOCKS = range(3)
+KVQ_RDKV_MAX_TOKENS = 1 << 20
 
 # Every entry point of include/*.h.
 EXPORTS = ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
            "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
            "kvq_status_string", "kvq_version", "kvq_trizone_bytes", "kvq_trizone_build",
-           "kvq_trizone_decode_workspace_bytes", "kvq_trizone_decode_attn")
+           "kvq_trizone_decode_workspace_bytes", "kvq_trizone_decode_attn",
+           "kvq_rdkv_workspace_bytes", "kvq_rdkv_token_weights", "kvq_rdkv_allocate")
 KVQ_STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -91,6 +93,14 @@ class kvq_trizone(ctypes.Structure):
     ]
 
 
+class kvq_rdkv(ctypes.Structure):
+    """Mirror of ``struct kvq_rdkv``."""
+
+    _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32)]
+
+
 class KVQError(RuntimeError):
     def __init__(self, fn: str, status: int):
         super().__init__(f"{fn} failed: {status_string(status)} ({status})")
@@ -127,6 +137,14 @@ def load_library() -> ctypes.CDLL:
     lib.kvq_trizone_decode_workspace_bytes.argtypes = [tz_p, ctypes.c_int32, P(c_sz)]
     lib.kvq_trizone_decode_attn.argtypes = [tz_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_sz,
                                             c_vp]
+    rd_p = P(kvq_rdkv)
+    i32p = P(ctypes.c_int32)
+    lib.kvq_rdkv_workspace_bytes.argtypes = [rd_p, P(c_sz)]
+    lib.kvq_rdkv_token_weights.argtypes = [rd_p, c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_i64, c_i64,
+                                           i32p, c_f, c_vp, c_vp, c_sz, c_vp]
+    lib.kvq_rdkv_allocate.argtypes = [rd_p, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp, c_i64, c_i64, c_i64,
+                                      i32p, i32p, c_vp, c_f, c_f, c_vp, ctypes.c_int32, c_vp, c_vp, c_vp,
+                                      c_vp, c_sz, c_vp]
     lib.kvq_status_string.argtypes = [c_int]
     lib.kvq_status_string.restype = ctypes.c_char_p
     lib.kvq_version.argtypes = []
@@ -134,7 +152,8 @@ def load_library() -> ctypes.CDLL:
     for name in ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
                  "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
                  "kvq_trizone_bytes", "kvq_trizone_build", "kvq_trizone_decode_workspace_bytes",
-                 "kvq_trizone_decode_attn"):
+                 "kvq_trizone_decode_attn", "kvq_rdkv_workspace_bytes", "kvq_rdkv_token_weights",
+                 "kvq_rdkv_allocate"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -430,3 +449,112 @@ class TriZoneCache:
 
     def device_errors(self) -> int:
         return int(self.error_flags[0].item())
+
+
+def kvq_rdkv_workspace_bytes(desc: kvq_rdkv) -> int:
+    out = ctypes.c_size_t()
+    _check("kvq_rdkv_workspace_bytes", load_library().kvq_rdkv_workspace_bytes(ctypes.byref(desc),
+                                                                                ctypes.byref(out)))
+    return out.value
+
+
+def _check_prompt(t: torch.Tensor, name: str, heads: int, d: int):
+    _need(t, torch.float16, name)
+    if t.dim() != 4 or t.shape[2] != heads or t.shape[3] != d or t.stride(3) != 1:
+        raise ValueError(f"{name} must be [B, T, {heads}, {d}] with a contiguous last dim")
+
+
+def kvq_rdkv_token_weights(desc: kvq_rdkv, q: torch.Tensor, k: torch.Tensor, n_tokens: Sequence[int],
+                           sm_scale: float, w: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """q: fp16 [B, T, Hq, D]; k: fp16 [B, T, Hkv, D]; w: fp32 [B, Hkv, max_tokens] contiguous."""
+    _check_prompt(q, "q", desc.n_q_heads, desc.head_dim)
+    _check_prompt(k, "k", desc.n_kv_heads, desc.head_dim)
+    _need(w, torch.float32, "w")
+    _need(workspace, torch.uint8, "workspace")
+    if w.shape != (desc.batch, desc.n_kv_heads, desc.max_tokens) or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [B, Hkv, max_tokens] tensor")
+    if len(n_tokens) != desc.batch or any(int(n) > min(q.shape[1], k.shape[1]) for n in n_tokens):
+        raise ValueError("n_tokens needs one entry per sequence, within the prompt tensors")
+    nt = (ctypes.c_int32 * desc.batch)(*[int(x) for x in n_tokens])
+    st = load_library().kvq_rdkv_token_weights(
+        ctypes.byref(desc), _ptr(q), q.stride(0), q.stride(1), q.stride(2), _ptr(k), k.stride(0),
+        k.stride(1), k.stride(2), nt, float(sm_scale), _ptr(w), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check("kvq_rdkv_token_weights", st)
+
+
+def kvq_rdkv_allocate(desc: kvq_rdkv, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                      n_tokens: Sequence[int], t_old: Sequence[int], w: torch.Tensor, v_avg_bits: float,
+                      k_avg_bits: float, v_width: torch.Tensor, k_width: torch.Tensor,
+                      workspace: torch.Tensor, W_t: Optional[torch.Tensor] = None,
+                      W_c: Optional[torch.Tensor] = None, stream=None) -> None:
+    """v_width: uint8 [B, Hkv, max_old] contiguous; k_width: uint8 [B, Hkv, D] contiguous;
+    W_t: fp32 [B, Hkv, max_old] or None; W_c: fp32 [B, Hkv, D] or None."""
+    _check_prompt(q, "q", desc.n_q_heads, desc.head_dim)
+    _check_prompt(k, "k", desc.n_kv_heads, desc.head_dim)
+    _check_prompt(v, "v", desc.n_kv_heads, desc.head_dim)
+    if k.stride() != v.stride() or k.shape != v.shape:
+        raise ValueError("k and v need equal shapes and strides")
+    _need(w, torch.float32, "w")
+    _need(v_width, torch.uint8, "v_width")
+    _need(k_width, torch.uint8, "k_width")
+    _need(workspace, torch.uint8, "workspace")
+    B, H, D = desc.batch, desc.n_kv_heads, desc.head_dim
+    if v_width.dim() != 3 or v_width.shape[:2] != (B, H) or not v_width.is_contiguous():
+        raise ValueError("v_width must be a contiguous [B, Hkv, max_old] tensor")
+    max_old = v_width.shape[2]
+    if k_width.shape != (B, H, D) or not k_width.is_contiguous():
+        raise ValueError("k_width must be a contiguous [B, Hkv, D] tensor")
+    if W_t is not None:
+        _need(W_t, torch.float32, "W_t")
+        if W_t.shape != (B, H, max_old) or not W_t.is_contiguous():
+            raise ValueError("W_t must be a contiguous [B, Hkv, max_old] tensor")
+    if W_c is not None:
+        _need(W_c, torch.float32, "W_c")
+        if W_c.shape != (B, H, D) or not W_c.is_contiguous():
+            raise ValueError("W_c must be a contiguous [B, Hkv, D] tensor")
+    if w.shape != (B, H, desc.max_tokens) or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [B, Hkv, max_tokens] tensor")
+    if len(n_tokens) != B or len(t_old) != B or \
+            any(int(n) > min(q.shape[1], k.shape[1]) for n in n_tokens):
+        raise ValueError("n_tokens and t_old need one entry per sequence, within the prompt tensors")
+    nt = (ctypes.c_int32 * B)(*[int(x) for x in n_tokens])
+    to = (ctypes.c_int32 * B)(*[int(x) for x in t_old])
+    st = load_library().kvq_rdkv_allocate(
+        ctypes.byref(desc), _ptr(q), q.stride(0), q.stride(1), q.stride(2), _ptr(k), _ptr(v),
+        k.stride(0), k.stride(1), k.stride(2), nt, to, _ptr(w), float(v_avg_bits), float(k_avg_bits),
+        _ptr(v_width), max_old, _ptr(k_width), _ptr(W_t), _ptr(W_c), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check("kvq_rdkv_allocate", st)
+
+
+class RDKVAllocator:
+    """Workspace and outputs of the RDKV allocation for one geometry (PyTorch
+    allocations); ``run`` issues the token weights, then the allocation."""
+
+    def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, max_tokens: int, max_old: int,
+                 head_dim: int = 128, device="cuda"):
+        self.desc = kvq_rdkv(batch, n_q_heads, n_kv_heads, head_dim, max_tokens)
+        dev = torch.device(device)
+        self.workspace = torch.zeros(kvq_rdkv_workspace_bytes(self.desc), dtype=torch.uint8, device=dev)
+        self.w = torch.zeros((batch, n_kv_heads, max_tokens), dtype=torch.float32, device=dev)
+        self.v_width = torch.zeros((batch, n_kv_heads, max_old), dtype=torch.uint8, device=dev)
+        self.k_width = torch.zeros((batch, n_kv_heads, head_dim), dtype=torch.uint8, device=dev)
+        self.W_t = torch.zeros((batch, n_kv_heads, max_old), dtype=torch.float32, device=dev)
+        self.W_c = torch.zeros((batch, n_kv_heads, head_dim), dtype=torch.float32, device=dev)
+
+    def token_weights(self, q, k, n_tokens, sm_scale: Optional[float] = None, stream=None):
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.desc.head_dim)
+        kvq_rdkv_token_weights(self.desc, q, k, n_tokens, sm_scale, self.w, self.workspace, stream)
+        return self.w
+
+    def allocate(self, q, k, v, n_tokens, t_old, v_avg_bits: float, k_avg_bits: float, stream=None):
+        kvq_rdkv_allocate(self.desc, q, k, v, n_tokens, t_old, self.w, v_avg_bits, k_avg_bits,
+                          self.v_width, self.k_width, self.workspace, self.W_t, self.W_c, stream)
+        return self.v_width, self.k_width
+
+    def run(self, q, k, v, n_tokens, t_old, v_avg_bits: float, k_avg_bits: float,
+            sm_scale: Optional[float] = None, stream=None):
+        self.token_weights(q, k, n_tokens, sm_scale, stream)
+        return self.allocate(q, k, v, n_tokens, t_old, v_avg_bits, k_avg_bits, stream)

@@ -193,3 +193,62 @@ def test_sink_window_bytes_and_validation(lib):
     st = lib.kvq_quantize_prefill(ctypes.byref(f), 0x100000, 0x101000, 1 << 14, 512, 128,
                                   i32(67, 68), i32(0, 0), None)
     assert st == kvq.KVQ_ERR_INVALID
+
+
+def test_rdkv_workspace_bytes_matches_layout(lib):
+    d = kvq.kvq_rdkv(4, 32, 8, 128, 65536)
+    n = kvq.kvq_rdkv_workspace_bytes(d)
+    lse = 4 * 32 * 65536 * 4                    # per query row, stride rounded up to 64
+    wt = 4 * 8 * 65536 * 4
+    wc = 4 * 8 * 128 * 4
+    part = 4 * 8 * (65536 // 256) * 5 * 128 * 4  # 5 fields per 256-position chunk and channel
+    assert n == lse + wt + wc + part
+    assert kvq.kvq_rdkv_workspace_bytes(kvq.kvq_rdkv(1, 1, 1, 128, 1)) % 256 == 0
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, kvq.KVQ_ERR_UNSUPPORTED), ("n_q_heads", 24, kvq.KVQ_ERR_UNSUPPORTED),
+    ("n_q_heads", 12, kvq.KVQ_ERR_INVALID), ("batch", 0, kvq.KVQ_ERR_INVALID),
+    ("batch", kvq.KVQ_MAX_BATCH + 1, kvq.KVQ_ERR_UNSUPPORTED), ("max_tokens", -1, kvq.KVQ_ERR_INVALID),
+    ("max_tokens", kvq.KVQ_RDKV_MAX_TOKENS + 1, kvq.KVQ_ERR_UNSUPPORTED),
+])
+def test_rdkv_rejects_bad_geometry(lib, field, value, status):
+    d = kvq.kvq_rdkv(2, 8, 8, 128, 1024)
+    setattr(d, field, value)
+    out = ctypes.c_size_t()
+    assert lib.kvq_rdkv_workspace_bytes(ctypes.byref(d), ctypes.byref(out)) == status
+
+
+def test_rdkv_validation_fails_before_launch(lib):
+    # every call below fails host-side validation, so no CUDA call is made
+    d = kvq.kvq_rdkv(2, 8, 2, 128, 1024)
+    ws_n = kvq.kvq_rdkv_workspace_bytes(d)
+    i32 = ctypes.c_int32 * 2
+    q, k, v, w, ws = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000
+    qs, ks = (1024 * 8 * 128, 8 * 128, 128), (1024 * 2 * 128, 2 * 128, 128)
+
+    def tw(**kw):
+        a = dict(q=q, k=k, n=i32(100, 200), scale=0.088, w=w, ws=ws, wsn=ws_n, qs=qs)
+        a.update(kw)
+        return lib.kvq_rdkv_token_weights(ctypes.byref(d), a["q"], *a["qs"], a["k"], *ks, a["n"], a["scale"],
+                                          a["w"], a["ws"], a["wsn"], None)
+    assert tw(q=None) == kvq.KVQ_ERR_INVALID
+    assert tw(q=q + 8) == kvq.KVQ_ERR_INVALID                      # not 16-byte aligned
+    assert tw(qs=(1024 * 8 * 128, 8 * 128 + 4, 128)) == kvq.KVQ_ERR_INVALID  # stride not a multiple of 8
+    assert tw(scale=0.0) == kvq.KVQ_ERR_INVALID
+    assert tw(wsn=ws_n - 1) == kvq.KVQ_ERR_INVALID
+    assert tw(ws=ws + 16) == kvq.KVQ_ERR_INVALID                   # workspace not 256-byte aligned
+    assert tw(n=i32(100, 1025)) == kvq.KVQ_ERR_CAPACITY
+    assert tw(n=i32(-1, 5)) == kvq.KVQ_ERR_INVALID
+
+    def al(**kw):
+        a = dict(n=i32(100, 200), to=i32(90, 150), vb=3.0, kb=4.0, max_old=512, Wt=None, wsn=ws_n)
+        a.update(kw)
+        return lib.kvq_rdkv_allocate(ctypes.byref(d), q, *qs, k, v, *ks, a["n"], a["to"], w, a["vb"], a["kb"],
+                                     0x600000, a["max_old"], 0x700000, a["Wt"], None, ws, a["wsn"], None)
+    assert al(to=i32(101, 150)) == kvq.KVQ_ERR_INVALID             # t_old > n_tokens
+    assert al(max_old=120) == kvq.KVQ_ERR_CAPACITY                 # t_old > max_old
+    assert al(vb=-1.0) == kvq.KVQ_ERR_INVALID
+    assert al(kb=float("inf")) == kvq.KVQ_ERR_INVALID
+    assert al(Wt=0x800002) == kvq.KVQ_ERR_INVALID                  # W_t misaligned
+    assert al(wsn=100) == kvq.KVQ_ERR_INVALID
