@@ -42,11 +42,15 @@ def parse():
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
     ap.add_argument("--sink", type=int, default=0,
                     help="uniform cache: keep the first S tokens fp16 (attention-sink window)")
-    ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone", "serving"],
+    ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone", "serving", "rdkv"],
                     help="uniform: the 128k-token uniform cache (default); trizone: the "
                          "mixed-width cache, 4 sequences x 65,408 old + 128 fresh tokens; "
                          "serving: 16 ragged sequences of 8k-32k tokens, 4-bit, one "
-                         "append + decode per step")
+                         "append + decode per step; rdkv: the bit allocation (token weights "
+                         "+ widths) of the mixed-width workload's 4 x 65,536-token prompts")
+    ap.add_argument("--rdkv-tokens", type=int, default=0,
+                    help="rdkv workload: prompt positions per sequence (default: the workload's 65,536; "
+                         "a smaller prompt is for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -191,6 +195,9 @@ def run_reference(args):
     import torch
     if args.workload == "trizone":
         run_reference_trizone(args)
+        return
+    if args.workload == "rdkv":
+        run_reference_rdkv(args)
         return
     w = workload(args.bits)
     inp = S.generate(w)
@@ -406,6 +413,9 @@ def main():
         return
     if args.workload == "serving":
         main_serving(args)
+        return
+    if args.workload == "rdkv":
+        main_rdkv(args)
         return
     import torch
     import torch.distributed as dist
@@ -806,6 +816,186 @@ def main_serving(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+RDKV_METRIC = "RDKV bit allocation (token weights + V/K widths): ms per prompt batch"
+RDKV_SAMPLE_T = 1536  # prompt positions of the oracle's sample segment
+
+
+def rdkv_flops(w) -> float:
+    """Algorithmic tensor flops of one token-weight pass: the causal score matrix
+    of every (sequence, query head), 2 D flops per (query, key <= query) pair."""
+    T = w.context
+    return float(w.batch * w.n_q_heads) * T * (T + 1) / 2 * 2 * w.head_dim
+
+
+def rdkv_oracle_sample(w, q, inp, T):
+    """The oracle's three phases on the first T prompt positions of one segment;
+    returns (seconds, scale to the full workload by the causal pair count)."""
+    from oracle import rdkv_oracle as R
+    G = w.gqa
+    t0 = time.perf_counter()
+    R.segment_allocation(q[0, :T, 0:G], inp["K"][0, :T, 0], inp["V"][0, :T, 0], T - w.trizone_fresh,
+                         w.sm_scale, 3.0, 4.0)
+    dt = time.perf_counter() - t0
+    scale = w.batch * w.n_kv_heads * (w.context * (w.context + 1)) / (T * (T + 1))
+    return dt, scale
+
+
+def main_rdkv(args):
+    """RDKV allocation of the mixed-width workload's prompts (4 sequences x 65,536
+    positions, 32 query heads over 8 KV heads): a step is kvq_rdkv_token_weights
+    (two tensor-core passes over the causal scores) + kvq_rdkv_allocate (costs,
+    Lagrangian V widths of the 65,408 old tokens, channel statistics, K widths),
+    at 3 bits per old token and 4 bits per channel."""
+    import torch
+    import torch.distributed as dist
+    from quantized_kv_cache_11_gb300 import kvq
+    from quantized_kv_cache_11_gb300 import synthetic as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kvq.load_library()
+    w = S.TRIZONE
+    if args.rdkv_tokens:
+        w = w.scaled(name=f"llama31_8b_trizone_b4_t{args.rdkv_tokens}", context=args.rdkv_tokens)
+    inp = S.generate(w)
+    qn = S.prompt_queries(w)
+    B, H, T, D = w.batch, w.n_kv_heads, w.context, w.head_dim
+    t_old = T - w.trizone_fresh
+    nt, to = [T] * B, [t_old] * B
+    vb, kb = 3.0, 4.0
+    q = torch.from_numpy(qn).to(dev)
+    k = torch.from_numpy(inp["K"]).to(dev)
+    v = torch.from_numpy(inp["V"]).to(dev)
+    a = kvq.RDKVAllocator(B, w.n_q_heads, H, T, t_old, device=dev)
+    warm, steps = min(max(args.warmup, 3), 5), max(1, min(args.steps, 5))
+    for _ in range(warm):
+        a.run(q, k, v, nt, to, vb, kb, w.sm_scale)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for e in ev:
+            e[0].record()
+            a.token_weights(q, k, nt, w.sm_scale)
+            e[1].record()
+            a.allocate(q, k, v, nt, to, vb, kb)
+            e[2].record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    tw_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    al_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms = max_over_ranks(ev[0][0].elapsed_time(ev[-1][2]) / steps, dev)
+    # end to end: prompt tensors from pinned host memory, widths back to the host
+    qh, kh, vh = (torch.from_numpy(x).pin_memory() for x in (qn, inp["K"], inp["V"]))
+    vwh = torch.empty(a.v_width.shape, dtype=torch.uint8).pin_memory()
+    kwh = torch.empty(a.k_width.shape, dtype=torch.uint8).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(2):
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        a.run(q, k, v, nt, to, vb, kb, w.sm_scale)
+        vwh.copy_(a.v_width, non_blocking=True)
+        kwh.copy_(a.k_width, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / 2
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    # parity sample: weights of the last 16 keys of one segment, widths given the costs
+    from oracle import rdkv_oracle as R
+    G = w.gqa
+    kk = inp["K"][0, :, 0].astype(np.float64)
+    tail = np.zeros(16)
+    for tau in range(T - 16, T):
+        for g in range(G):
+            sc = w.sm_scale * (kk[:tau + 1] @ qn[0, tau, g].astype(np.float64))
+            p = np.exp(sc - sc.max())
+            p /= p.sum()
+            tail[:tau + 1 - (T - 16)] += p[T - 16:tau + 1]
+    got = a.w[0, 0, T - 16:].double().cpu().numpy()
+    ref_vw, _ = R.allocate(a.W_t[0, 0, :t_old].cpu().numpy(), R.V_WIDTHS, R.budget_bits(vb, t_old))
+    ref_kw, _ = R.allocate(a.W_c[0, 0].cpu().numpy(), R.K_WIDTHS, R.budget_bits(kb, D))
+    parity = {"segments_checked": 1, "last_keys_weight_max_rel": float(np.abs(got / tail - 1).max()),
+              "v_widths_equal": bool((a.v_width[0, 0, :t_old].cpu().numpy() == ref_vw).all()),
+              "k_widths_equal": bool((a.k_width[0, 0].cpu().numpy() == ref_kw).all())}
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    peak = float(pk.get("bf16_tflops_sustained") or pk["bf16_tflops"])
+    flops = 2 * rdkv_flops(w)  # both passes compute the causal scores
+    achieved = flops / (tw_ms * 1e-3) / 1e12
+    vwd = np.bincount(a.v_width.cpu().numpy().ravel(), minlength=17)[[0, 2, 4, 8, 16]]
+    line = {
+        "metric": RDKV_METRIC, "value": step_ms, "unit": "ms/step", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 in, f32 accumulate", "data": "synthetic",
+        "config": {"workload": "rdkv_" + w.name, "batch": B, "n_q_heads": w.n_q_heads, "n_kv_heads": H,
+                   "head_dim": D, "prompt_tokens": T, "old_tokens": t_old, "v_avg_bits": vb, "k_avg_bits": kb,
+                   "l2": f"inputs larger than L2: {q.numel() * 2 / 1e9:.2f} GB of prompt queries per step"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "rowstats_kernel + colsum_kernel",
+                     "peak_source": "measured bf16_tflops_sustained (fp16 has the bf16 rate)",
+                     "algorithmic_flops": flops},
+        "e2e": {"value": e2e_ms, "unit": "ms/step", "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+                "d2h_bytes_per_step": a.v_width.numel() + a.k_width.numel()},
+        "gpu_launches": steps * 7,
+        "clocks": clk.summary(),
+        "path": {"token_weights_ms": tw_ms, "allocate_ms": al_ms,
+                 "v_width_counts_0_2_4_8_16": vwd.tolist(),
+                 "v_bits_per_old_token": float((vwd * np.array([0, 2, 4, 8, 16])).sum() / (B * H * t_old))},
+        "parity_sample": parity,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import torch as _t
+        dt, scale = rdkv_oracle_sample(w, qn, inp, RDKV_SAMPLE_T)
+        line["cpu_baseline"] = {"value": dt * scale * 1e3, "unit": "ms/step", "cores": _t.get_num_threads(),
+                                "kind": "oracle",
+                                "sample": f"oracle token weights + allocation of 1 of {B * H} segments on its "
+                                          f"first {RDKV_SAMPLE_T} prompt positions, scaled x{scale:.0f} by the "
+                                          f"causal pair count"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference_rdkv(args):
+    """The oracle on the host cores for the RDKV allocation: each step runs the
+    three phases on a sample segment, scaled to the full workload."""
+    from quantized_kv_cache_11_gb300 import synthetic as S
+    import torch
+    w = S.TRIZONE
+    inp = S.generate(w)
+    qn = S.prompt_queries(w, batches=[0])
+    times, scale = [], 1.0
+    for i in range(args.warmup + args.steps):
+        dt, scale = rdkv_oracle_sample(w, qn, inp, 512)
+        if i >= args.warmup:
+            times.append(dt)
+    value = statistics.mean(times) * scale * 1e3
+    sample = (f"oracle token weights + allocation of 1 of {w.batch * w.n_kv_heads} segments on its first 512 "
+              f"prompt positions per step, scaled x{scale:.0f} by the causal pair count")
+    print(json.dumps({
+        "impl": "reference", "metric": RDKV_METRIC, "value": value, "unit": "ms/step", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "rdkv_" + w.name},
+        "cpu_baseline": {"kind": "oracle", "cores": torch.get_num_threads(), "sample": sample,
+                         "value": value, "unit": "ms/step"},
+        "e2e": {"value": value, "unit": "ms/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
 
 
 def _kernel_sha(files=("kvq_decode.cu", "kvq_common.cuh")) -> str:
