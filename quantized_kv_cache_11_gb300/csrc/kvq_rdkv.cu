@@ -79,14 +79,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // 64 rows x 128 fp16 (rows first .. first+63 of a strided matrix) into a staged
-// tile; rows >= n are zero-filled.
+// tile by a CTA of 128 threads: thread i copies 16-byte chunk i % 16 of rows
+// i / 16 + 8 k; rows >= n are zero-filled.
 __device__ __forceinline__ void stage_tile(uint8_t* dst, const __half* base, int64_t row_stride, int first, int n) {
-  for (int e = threadIdx.x; e < kBlk * 16; e += blockDim.x) {
-    const int j = e >> 4, ch = e & 15;
-    const int t = first + j;
-    const bool ok = t < n;
-    const __half* src = base + (int64_t)(ok ? t : 0) * row_stride + ch * 8;
-    cp_async_16_zfill(dst + j * kPitch + ch * 16, src, ok ? 16 : 0);
+  const int ch = threadIdx.x & 15, j0 = threadIdx.x >> 4;
+  const __half* src = base + (int64_t)(first + j0) * row_stride + ch * 8;
+  const int64_t step = 8 * row_stride;
+  uint8_t* d = dst + j0 * kPitch + ch * 16;
+#pragma unroll
+  for (int k = 0; k < kBlk / 8; ++k) {
+    const bool ok = first + j0 + 8 * k < n;
+    cp_async_16_zfill(d + 8 * k * kPitch, ok ? src : base, ok ? 16 : 0);
+    src += step;
   }
 }
 
@@ -119,12 +123,59 @@ __device__ __forceinline__ void tile_scores(float (&s)[8][4], const uint32_t (&a
 #pragma unroll
   for (int kp = 0; kp < 4; ++kp)
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      uint32_t b[4];
+    for (int nt = 0; nt < 8; nt += 2) {  // two n-tiles at a time: no back-to-back MMAs on one accumulator
+      uint32_t b[4], c[4];
       ldmatrix_x4(b, tile + (8 * nt + (lane & 7)) * kPitch + (32 * kp + 8 * (lane >> 3)) * 2);
+      ldmatrix_x4(c, tile + (8 * nt + 8 + (lane & 7)) * kPitch + (32 * kp + 8 * (lane >> 3)) * 2);
       mma_16816(s[nt], a[2 * kp], b[0], b[1]);
+      mma_16816(s[nt + 1], a[2 * kp], c[0], c[1]);
       mma_16816(s[nt], a[2 * kp + 1], b[2], b[3]);
+      mma_16816(s[nt + 1], a[2 * kp + 1], c[2], c[3]);
     }
+}
+
+// Row maxima of the raw scores of rows tau[0], tau[1] (this lane's 16 columns;
+// with EDGE, keys t > tau or t >= n are set to -inf first).
+template <bool EDGE>
+__device__ __forceinline__ void row_max(float (&s)[8][4], float (&mx)[2], const int (&tau)[2], int t0, int n,
+                                        int tig) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float v = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (EDGE) {
+          const int t = t0 + 8 * nt + 2 * tig + c;
+          if (t > tau[r] || t >= n) s[nt][2 * r + c] = -INFINITY;
+        }
+        v = fmaxf(v, s[nt][2 * r + c]);
+      }
+    mx[r] = v;
+  }
+}
+
+// Column sums of exp2(scale * s - lse[tau]) into acc[r] for keys tk[r] (with
+// EDGE, queries tau < tk or tau >= n contribute 0).
+template <bool EDGE>
+__device__ __forceinline__ void col_sums(const float (&s)[8][4], float (&acc)[2], const float* lse, float scale,
+                                         const int (&tk)[2], int q0, int n, int tig) {
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const float2 ls = *reinterpret_cast<const float2*>(lse + 8 * nt + 2 * tig);
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float e = fast_exp2(fmaf(s[nt][2 * r + c], scale, -(c ? ls.y : ls.x)));
+        if (EDGE) {
+          const int tau = q0 + 8 * nt + 2 * tig + c;
+          if (tau < tk[r] || tau >= n) e = 0.f;
+        }
+        acc[r] += e;
+      }
+  }
 }
 
 // Pass 1: lse[b][hq][tau] for the 64 query rows of one CTA (4 warps x 16 rows).
@@ -153,32 +204,21 @@ __global__ void __launch_bounds__(128) rowstats_kernel(const AttnParams p) {
     __syncthreads();
     float s[8][4];
     tile_scores(s, a, smem + (kb & 1) * kTile, lane);
-    const bool edge = kb == qb || (kb + 1) * kBlk > n;
+    float mx[2];
+    if (kb == qb || (kb + 1) * kBlk > n) row_max<true>(s, mx, tau, kb * kBlk, n, tig);
+    else row_max<false>(s, mx, tau, kb * kBlk, n, tig);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float x = s[nt][2 * r + c] * p.scale_log2;
-          if (edge) {
-            const int t = kb * kBlk + 8 * nt + 2 * tig + c;
-            if (t > tau[r] || t >= n) x = -INFINITY;
-          }
-          s[nt][2 * r + c] = x;
-          mx = fmaxf(mx, x);
-        }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float mnew = fmaxf(m[r], mx);
+      float v = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+      const float mnew = fmaxf(m[r], v * p.scale_log2);  // the scale is positive
       if (mnew != -INFINITY) {
         const float alpha = m[r] == -INFINITY ? 0.f : fast_exp2(m[r] - mnew);
         float sum = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-          for (int c = 0; c < 2; ++c) sum += fast_exp2(s[nt][2 * r + c] - mnew);
+          for (int c = 0; c < 2; ++c) sum += fast_exp2(fmaf(s[nt][2 * r + c], p.scale_log2, -mnew));
         l[r] = l[r] * alpha + sum;
         m[r] = mnew;
       }
@@ -241,22 +281,8 @@ __global__ void __launch_bounds__(128) colsum_kernel(const AttnParams p) {
     __syncthreads();
     float s[8][4];
     tile_scores(s, a, smem + buf * kTile, lane);
-    const bool edge = qb == kb || (qb + 1) * kBlk > n;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float2 ls = *reinterpret_cast<const float2*>(s_lse + buf * kBlk + 8 * nt + 2 * tig);
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float e = fast_exp2(fmaf(s[nt][2 * r + c], p.scale_log2, -(c ? ls.y : ls.x)));
-          if (edge) {
-            const int tau = qb * kBlk + 8 * nt + 2 * tig + c;
-            if (tau < tk[r] || tau >= n) e = 0.f;
-          }
-          acc[r] += e;
-        }
-    }
+    if (qb == kb || (qb + 1) * kBlk > n) col_sums<true>(s, acc, s_lse + buf * kBlk, p.scale_log2, tk, qb * kBlk, n, tig);
+    else col_sums<false>(s, acc, s_lse + buf * kBlk, p.scale_log2, tk, qb * kBlk, n, tig);
     __syncthreads();
   }
 #pragma unroll
