@@ -212,6 +212,43 @@ def sequence_attention(q16: np.ndarray, state: dict, sm_scale: float) -> np.ndar
     return decode_attention(q16, keys, values, sm_scale)
 
 
+# ---------------------------------------------------------------------------
+# Pre-RoPE keys ("KV-cache quantization axes", ihal.it, paragraph 9 and the
+# closing paragraph: keys are quantized before the rotary position embedding and
+# the rotation is applied after dequantization).  Readings: RoPE rotates the
+# adjacent channel pairs (2i, 2i+1) of a key at position t by the angle
+# t * theta_i, theta_i = base^(-2i/D); a token's position is its index in the
+# sequence (sinks, then the quantized groups, then the tail); the query is given
+# already rotated to its own position.
+# ---------------------------------------------------------------------------
+def rope_angles(positions: np.ndarray, d: int, base: float) -> np.ndarray:
+    """Angles t * theta_i, float64 [len(positions), d/2]."""
+    i = np.arange(d // 2, dtype=F64)
+    theta = np.power(F64(base), -2.0 * i / d)
+    return np.asarray(positions, dtype=F64)[:, None] * theta[None, :]
+
+
+def rope_rotate(keys: np.ndarray, positions: np.ndarray, base: float) -> np.ndarray:
+    """keys float64 [..., N, D] rotated pair by pair: (k0, k1) ->
+    (k0 cos - k1 sin, k0 sin + k1 cos) with the angle of each token's position."""
+    keys = np.asarray(keys, dtype=F64)
+    ang = rope_angles(positions, keys.shape[-1], base)
+    c, s = np.cos(ang), np.sin(ang)
+    k0, k1 = keys[..., 0::2], keys[..., 1::2]
+    out = np.empty_like(keys)
+    out[..., 0::2] = k0 * c - k1 * s
+    out[..., 1::2] = k0 * s + k1 * c
+    return out
+
+
+def sequence_attention_rope(q16: np.ndarray, state: dict, sm_scale: float, base: float) -> np.ndarray:
+    """Decode attention over a cache of pre-RoPE keys: every key (sinks,
+    dequantized groups, tail) is rotated to its position after dequantization."""
+    keys, values = sequence_kv(state)
+    keys = rope_rotate(keys, np.arange(keys.shape[1]), base)
+    return decode_attention(q16, keys, values, sm_scale)
+
+
 def append_lengths(n_quant: int, n_tail: int, tail_cap: int):
     """Lengths after appending one token (article, paragraph 8): when the tail
     is full, its oldest 32 tokens become the next quantized group first."""

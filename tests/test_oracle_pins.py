@@ -8,6 +8,7 @@ m16n8k16 fragment tables.  A dropped term, a wrong rounding rule, the fp32
 scale in place of the stored fp16 one, a missing clamp or a transposed operand
 each fail at least one test below.
 """
+import math
 from fractions import Fraction
 
 import numpy as np
@@ -642,3 +643,39 @@ def test_append_with_sinks_fills_the_window_then_the_tail():
         if n > S_:
             plain = O.append_lengths(*plain, R)[:2]
         assert state == (min(n, S_),) + plain, n
+
+
+# ------------------------------------------------------------- pre-RoPE keys
+def test_rope_rotation_by_hand():
+    # one pair (D = 2): theta_0 = 1, so the key at position t turns by t radians
+    k = np.array([[1.0, 0.0], [0.0, 2.0], [3.0, 4.0]])
+    got = O.rope_rotate(k, np.array([0, 1, 2]), 10000.0)
+    assert np.allclose(got[0], [1.0, 0.0])
+    assert np.allclose(got[1], [-2.0 * math.sin(1.0), 2.0 * math.cos(1.0)])
+    assert np.allclose(got[2], [3 * math.cos(2.0) - 4 * math.sin(2.0), 3 * math.sin(2.0) + 4 * math.cos(2.0)])
+    # theta_i = base^(-2i/D): D = 4, base 100 -> theta_1 = 0.1
+    assert np.allclose(O.rope_angles(np.array([5]), 4, 100.0), [[5.0, 0.5]])
+
+
+def test_rope_preserves_norms_and_relative_scores():
+    rng = np.random.default_rng(7)
+    k = rng.standard_normal((6, 16))
+    q = rng.standard_normal(16)
+    pos = np.arange(6) + 3
+    rk = O.rope_rotate(k, pos, 500000.0)
+    assert np.allclose(np.linalg.norm(rk, axis=1), np.linalg.norm(k, axis=1))
+    # q at position p against keys at t depends on p - t only: shift both by 11
+    rq = O.rope_rotate(q[None], np.array([9]), 500000.0)[0]
+    rq2 = O.rope_rotate(q[None], np.array([20]), 500000.0)[0]
+    rk2 = O.rope_rotate(k, pos + 11, 500000.0)
+    assert np.allclose(rk @ rq, rk2 @ rq2)
+
+
+def test_rope_attention_position_zero_is_plain():
+    # a single cached token sits at position 0: no rotation, plain attention
+    rng = np.random.default_rng(8)
+    k16 = rng.standard_normal((1, 1, 64)).astype(np.float16)
+    v16 = rng.standard_normal((1, 1, 64)).astype(np.float16)
+    st = O.quantize_sequence(k16, v16, 1, 1, 2)
+    q = rng.standard_normal((2, 64)).astype(np.float16)
+    assert np.allclose(O.sequence_attention_rope(q, st, 0.125, 10000.0), O.sequence_attention(q, st, 0.125))
