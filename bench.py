@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--bits", type=int, default=2, choices=[2, 4])
+    ap.add_argument("--rope", type=float, default=0.0,
+                    help="uniform cache: keys stored before RoPE and rotated in the decode with this "
+                         "rotary base (e.g. 500000); 0 = plain decode")
     ap.add_argument("--sink", type=int, default=0,
                     help="uniform cache: keep the first S tokens fp16 (attention-sink window)")
     ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone", "serving", "rdkv"],
@@ -160,7 +163,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, inp, budget_s=12.0, sink=0):
+def cpu_baseline(w, inp, budget_s=12.0, sink=0, rope=0.0):
     """The oracle as it stands on this host: dequantize + fp64 attention for one
     KV head (its 4 query heads) over the whole context, repeated for ~budget_s,
     scaled by the number of KV heads to one full decode step."""
@@ -173,7 +176,10 @@ def cpu_baseline(w, inp, budget_s=12.0, sink=0):
     t_end = time.perf_counter() + budget_s
     while time.perf_counter() < t_end or len(times) < 2:
         t0 = time.perf_counter()
-        O.sequence_attention(q, st, w.sm_scale)
+        if rope:
+            O.sequence_attention_rope(q, st, w.sm_scale, rope)
+        else:
+            O.sequence_attention(q, st, w.sm_scale)
         times.append(time.perf_counter() - t0)
     per_head = statistics.median(times)
     return {"value": per_head * w.n_kv_heads * 1e6, "unit": UNIT, "kind": "oracle",
@@ -483,26 +489,36 @@ def main():
     # ---- decode: warm up, quick parity sample, graph of launches over the replicas
     outs = [torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev)
             for _ in caches]
+    if args.rope:
+        table = caches[0].rope_table(args.rope)  # one table serves every replica (same geometry)
+
+        def dec(c, qq, out):
+            c.decode_rope(qq, table, w.sm_scale, out=out)
+    else:
+        def dec(c, qq, out):
+            c.decode(qq, w.sm_scale, out=out)
     for i in range(max(args.warmup, 3)):
-        caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep])
+        dec(caches[i % n_rep], q, outs[i % n_rep])
     torch.cuda.synchronize()
     parity = None
     if rank == 0:
         from oracle import kvq_oracle as O
         st = O.quantize_sequence(inp["K"][0][:, :1], inp["V"][0][:, :1], int(inp["seq_len"][0]),
                                  n_tail, w.bits, n_sink_cap=args.sink)
-        ref = O.sequence_attention(inp["q"][0][:w.gqa], st, w.sm_scale)
+        if args.rope:
+            ref = O.sequence_attention_rope(inp["q"][0][:w.gqa], st, w.sm_scale, args.rope)
+        else:
+            ref = O.sequence_attention(inp["q"][0][:w.gqa], st, w.sm_scale)
         got = outs[0][0, :w.gqa].double().cpu().numpy()
         parity = {"kv_heads_checked": 1, "max_abs": float(np.abs(got - ref).max())}
     us_step, steps, clocks = time_graph(
-        lambda i: caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep]),
-        n_rep, args.steps, world, local)
+        lambda i: dec(caches[i % n_rep], q, outs[i % n_rep]), n_rep, args.steps, world, local)
 
     # ---- end to end through the public API: pinned host q in, fp32 output out
     q_host = torch.from_numpy(inp["q"]).pin_memory()
     out_host = torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(q)
-    e2e_us = time_e2e(lambda i, qd: caches[i % n_rep].decode(qd, w.sm_scale, out=outs[i % n_rep]),
+    e2e_us = time_e2e(lambda i, qd: dec(caches[i % n_rep], qd, outs[i % n_rep]),
                       q_host, q_dev, out_host, outs, n_rep, min(steps, 4000))
 
     if rank != 0:
@@ -512,17 +528,19 @@ def main():
     peak, peak_kind = load_peaks()
     nbytes = algorithmic_bytes(w, n_quant, n_tail, n_sink)
     achieved = nbytes / (us_step * 1e-6) / 1e9
-    traffic = None if args.sink else read_traffic("decode_traffic.txt", w.name, _kernel_sha())
+    traffic = None if (args.sink or args.rope) else read_traffic("decode_traffic.txt", w.name, _kernel_sha())
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
+        "config": {"workload": w.name + ("_prerope" if args.rope else ""), "batch": w.batch,
+                   "n_q_heads": w.n_q_heads, "rope_base": args.rope or None,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.context,
                    "n_quant": n_quant, "n_tail": n_tail, "n_sink": n_sink, "bits": w.bits, "group": 32,
                    "l2": f"inputs larger than L2: {n_rep} cache replicas "
                          f"({n_rep * probe.nbytes / 1e6:.0f} MB) rotated every step",
-                   "launch": "CUDA graph of kvq_decode_attn calls"},
+                   "launch": "CUDA graph of " + ("kvq_decode_attn_rope" if args.rope else "kvq_decode_attn") +
+                             " calls"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": nbytes},
@@ -535,7 +553,7 @@ def main():
         "parity_sample": parity,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inp, sink=args.sink)
+        line["cpu_baseline"] = cpu_baseline(w, inp, sink=args.sink, rope=args.rope)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -998,7 +1016,7 @@ def run_reference_rdkv(args):
     }), flush=True)
 
 
-def _kernel_sha(files=("kvq_decode.cu", "kvq_common.cuh")) -> str:
+def _kernel_sha(files=("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_common.cuh")) -> str:
     import hashlib
     h = hashlib.sha256()
     for f in files:

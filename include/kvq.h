@@ -279,6 +279,38 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, int32_t n_q_heads, const void
 kvq_status kvq_decode_attn_static(const kvq_cache* cache, int32_t n_q_heads, const void* q,
                                   float* out, float sm_scale, void* stream);
 
+/*
+ * Pre-RoPE keys ("KV-cache quantization axes", ihal.it, paragraph 9 and the
+ * closing paragraph: the keys are quantized before the rotary position
+ * embedding and rotated after dequantization, so the outlier channels that make
+ * per-channel groups work are not spread over their neighbours).  The cache is
+ * filled as usual (kvq_quantize_prefill / kvq_append_token) with keys taken
+ * BEFORE the rotation; the decode then rotates every key (sinks, quantized
+ * groups, tail) to its position: the adjacent channel pair (2i, 2i+1) of the
+ * token at position t (its index in the sequence: sinks first, then the
+ * quantized tokens, then the tail, oldest first) turns by t * base^(-2i/D):
+ * (k0, k1) -> (k0 cos - k1 sin, k0 sin + k1 cos).  The query is passed already
+ * rotated to its own position, as for kvq_decode_attn.  head_dim 128 only.
+ *
+ * kvq_rope_table_bytes -- bytes of the cos/sin table of a cache geometry: 64 +
+ *   ceil((sink_cap + 32 max_groups + tail_cap) / 32) rows of D/2 float2.
+ * kvq_rope_table -- fills that table on `stream` (float64 angles and sin/cos,
+ *   stored float32): row o < 64 holds (cos, sin)(o theta_i), row 64 + m holds
+ *   (cos, sin)(32 m theta_i), theta_i = base^(-2i/D).  base > 1.  Build it once
+ *   per (geometry, base); table 16-byte aligned, device memory, caller-owned.
+ * kvq_decode_attn_rope -- kvq_decode_attn over a cache of pre-RoPE keys, with
+ *   the table of kvq_rope_table for this cache's geometry.  The K side runs in
+ *   float32 on CUDA cores (the rotation depends on the token, so Q.K^T is no
+ *   longer one matrix product); P.V and the merge are those of kvq_decode_attn.
+ *   workspace: at least kvq_decode_workspace_bytes bytes, zero-filled before
+ *   first use, left zero-filled.  Errors as kvq_decode_attn.
+ */
+kvq_status kvq_rope_table_bytes(const kvq_cache* cache, size_t* bytes);
+kvq_status kvq_rope_table(const kvq_cache* cache, float base, float* table, void* stream);
+kvq_status kvq_decode_attn_rope(const kvq_cache* cache, int32_t n_q_heads, const void* q, float* out,
+                                float sm_scale, const float* table, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code.  Never NULL. */
 const char* kvq_status_string(int status);
 

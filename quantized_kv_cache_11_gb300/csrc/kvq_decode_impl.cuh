@@ -1,0 +1,998 @@
+// Fused-dequant split-K decode attention over the uniform packed cache: the
+// kernel templates, shared by the entry points of kvq_decode.cu and
+// kvq_decode_rope.cu.
+//
+// What it computes ("KV-cache quantization axes", ihal.it, paragraphs 2 and 6;
+// VQKV summary, section 2 "decoding phase"): for every sequence b and query head
+// hq (KV head h = hq / G), out = softmax(sm_scale * q . K_hat^T) . V_hat over the
+// quantized tokens (K_hat = zero + scale * code, dequantized inside the
+// products, never written out) and the fp16 tail tokens.
+//
+// How:
+// * Work partition (stream-K): the work items of every (sequence, KV head) --
+//   its quantized 32-token groups, then its fp16 tail chunks (each weighted as
+//   kTailWeight items) -- are laid end to end, and the list is cut into equal
+//   contiguous ranges, one per resident CTA, so ragged batches stay balanced.
+//   Inside a CTA each warp streams its own sub-range of groups through a private
+//   multi-stage cp.async ring in shared memory.
+// * Per 32-token group (one warp, the whole GQA group of G query heads):
+//   Q.K^T on tensor cores (mma.m16n8k16, fp16 in, fp32 accumulate).  The A
+//   operand is the codes themselves: one mask per register leaves a code pair
+//   in the low mantissa bits of two fp16 halves with a zero exponent, which
+//   read as the subnormals c * 2^(p-24) (p = the codes' bit position; the
+//   tensor cores take fp16 subnormals exactly).  p depends only on the
+//   fragment row, so the power of two leaves the fp32 results per row.
+//   B = q * scale, split into two fp16 halves (hi = fp16(q*s), lo = q*s - hi,
+//   exact), in separate columns, so the per-channel scale is applied to q once
+//   per group.  The zero points enter through one more small MMA (rows = zero
+//   points).  Online softmax in fp32; P.V likewise with B = fp16(p * scale)
+//   per 32-channel value group, the value zero points and the softmax
+//   denominator (a row of ones) from one small MMA.
+// * Splits are merged by log-sum-exp; the last CTA to finish a (sequence, KV
+//   head) merges and writes the output, then resets its counter.  No spin-wait.
+#pragma once
+
+#include <cmath>
+
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr int kTailWeight = 3;  // a 32-token fp16 tail chunk counts as this many groups
+// Polls of an mbarrier before a wait gives up (each poll may suspend the thread
+// briefly): far longer than any copy takes, short enough to end a stuck kernel.
+constexpr uint32_t kMaxPolls = 1u << 22;
+
+// ROPE: the keys are stored before the rotary position embedding and rotated to
+// their positions after dequantization (the K side then runs on CUDA cores).
+template <int D, int BITS, int G, bool ROPE = false>
+struct DecodeCfg {
+  using T = Tile<D, BITS>;
+  static constexpr int TB = T::kBytes;
+  static constexpr int KMETA = 4 * D;  // [2][D] halves
+  static constexpr int VMETA = 4 * D;  // [2][D/32][32] halves
+  static constexpr int BASE = ROPE ? D / 2 * 8 : 0;  // cos/sin of the group's first position block
+  static constexpr int STAGE = 2 * TB + KMETA + VMETA + BASE;
+  static constexpr int NT = (2 * G + 7) / 8;  // 8-column n-tiles: column 2g = hi, 2g+1 = lo
+  static constexpr int KT = D / 16;
+  static constexpr int NWL = T::kWordsPerLane;
+  static constexpr int PPW = T::kPairsPerWord;
+  // one CTA of 16 warps per SM for 2- and 4-bit codes: fewer, larger CTAs leave
+  // fewer split-K partials per (sequence, KV head) for the last CTA to merge
+  // (12 at 4 bits with ROPE: its stage ring, offset table and fp32 q must fit)
+  static constexpr int WARPS = BITS == 8 ? 4 : (ROPE && BITS == 4 ? 12 : 16);
+  static constexpr int NSTAGE = BITS == 2 ? (ROPE ? 3 : 4) : (BITS == 4 ? 2 : 3);
+  static constexpr int MIN_CTAS = 1;
+  static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
+  static constexpr int RING = WARPS * NSTAGE * STAGE;
+  static constexpr int PSROW = 48;                   // halves per head row of the p~ exchange
+  static constexpr int PS = WARPS * G * PSROW * 2;   // p~ exchange, bytes
+  static constexpr int ZERO = 4 * D;                 // zero row for lanes without a metadata row
+  static constexpr int PREFIX = ((KVQ_MAX_BATCH + 1) * 4 + 15) / 16 * 16;
+  static constexpr int QS = NT * 4 * (D / 2) * 4;     // q pairs of the segment's heads, lane order
+  static constexpr int MBAR = (WARPS * NSTAGE + 1) * 8;  // one mbarrier per stage + the merge's
+  static constexpr int INTRA = ROPE ? 64 * (D / 2) * 8 : 0;  // cos/sin of offsets 0..63 within a block
+  static constexpr int QF = ROPE ? NT * 4 * D * 4 : 0;         // fp32 q of the segment's heads
+  static constexpr int SMEM = RING + PS + ZERO + PREFIX + QS + INTRA + QF + MBAR;
+  static_assert(SMEM <= 232448, "fits the shared memory of one CTA");
+  // partials staged per merge batch: they fit the ring, their weights the p~ area
+  static constexpr int MERGE_BATCH = RING / (G * PSTRIDE * 4) < PS / (4 * G) ? RING / (G * PSTRIDE * 4)
+                                                                              : PS / (4 * G);
+  static_assert(MERGE_BATCH >= 1, "a merge batch holds at least one partial");
+  static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
+  static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
+  static_assert(PS % 16 == 0 && RING % 16 == 0 && ZERO % 16 == 0 && PREFIX % 16 == 0 &&
+                    QS % 16 == 0 && INTRA % 16 == 0 && QF % 16 == 0 && STAGE % 16 == 0,
+                "aligned shared regions (the mbarriers need 8 bytes, the copies 16)");
+  static_assert(NSTAGE * STAGE >= kGroup * (2 * D + 16), "a staged tail chunk fits a warp's ring");
+};
+
+struct DecodeParams {
+  const uint8_t* k_codes;
+  const uint8_t* v_codes;
+  const __half* k_meta;
+  const __half* v_meta;
+  const __half* k_tail;
+  const __half* v_tail;
+  const int32_t* n_quant;
+  const int32_t* n_tail;
+  const int32_t* tail_head;
+  const __half* k_sink;
+  const __half* v_sink;
+  const int32_t* n_sink;
+  int32_t* error_flags;
+  const __half* q;
+  const float2* rope;  // ROPE: the table of kvq_rope_table (rows 0..63 offsets, 64 + m position blocks)
+  float* out;
+  int32_t* counters;
+  float* part;
+  float scale_log2;
+  int32_t batch, hkv, max_groups, tail_cap, sink_cap;
+  int32_t n_stream;
+};
+
+// Lengths as the decode sees them; an inconsistent sequence counts as empty.
+struct SeqLen {
+  int nq, nt, th, ns;
+};
+__device__ __forceinline__ SeqLen read_lengths(const DecodeParams& p, int b, bool report) {
+  SeqLen s{p.n_quant[b], p.n_tail[b], p.tail_head[b], p.sink_cap > 0 ? p.n_sink[b] : 0};
+  const bool ok = s.nq >= 0 && s.nq % kGroup == 0 && s.nq / kGroup <= p.max_groups && s.nt >= 0 &&
+                  s.nt <= p.tail_cap && s.th >= 0 && s.th < p.tail_cap && s.th % kGroup == 0 && s.ns >= 0 &&
+                  s.ns <= p.sink_cap && (s.ns == p.sink_cap || (s.nq == 0 && s.nt == 0));
+  if (!ok) {
+    if (report && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_BAD_LENGTHS);
+    s = SeqLen{0, 0, 0, 0};
+  }
+  return s;
+}
+
+// Work items of one (sequence, KV head): its groups, kTailWeight per fp16 chunk
+// (tail chunks, then sink chunks), and at least one (an empty sequence still
+// needs its zero output written).
+__device__ __forceinline__ int seq_items(const SeqLen& s) {
+  const int n = s.nq / kGroup + kTailWeight * ((s.nt + kGroup - 1) / kGroup + (s.ns + kGroup - 1) / kGroup);
+  return n > 0 ? n : 1;
+}
+
+// s_pref[b] = work items of the sequences before b (per KV head).
+__device__ inline void build_prefix(const DecodeParams& p, int* s_pref) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  int run = 0;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int v = (b < p.batch) ? seq_items(read_lengths(p, b, blockIdx.x == 0)) : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += a;
+    }
+    if (b < p.batch) s_pref[b + 1] = run + v;
+    run += __shfl_sync(0xffffffffu, v, 31);
+  }
+  if (lane == 0) s_pref[0] = 0;
+}
+
+// The stream-K CTA that owns global item x (CTA c owns [c*T/N, (c+1)*T/N)).
+__device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
+  return ((x + 1) * n - 1) / total;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D, int BITS, int G, bool ROPE = false>
+struct Decoder {
+  using C = DecodeCfg<D, BITS, G, ROPE>;
+  static constexpr int NT = C::NT, KT = C::KT;
+  // Bit position p of the codes that unpack8 puts in register 4 mt + i (row half
+  // rh = i & 1 of an mma A fragment; never dependent on the k-half i >> 1): the
+  // register holds the fp16 subnormals c * 2^(p - 24).  unit = 2^(24 - p).
+  static __host__ __device__ constexpr int pos(int mt, int rh) {
+    return BITS == 2 ? 4 * mt + 2 * rh : (BITS == 4 ? 4 * rh : 0);
+  }
+  static __host__ __device__ constexpr float unit(int mt, int rh) { return (float)(1 << (24 - pos(mt, rh))); }
+  static constexpr uint32_t kSixteenth = 0x2C002C00u;  // half2(1/16, 1/16)
+  static constexpr uint32_t kOnes = 0x3C003C00u;  // half2(1, 1)
+
+  // Per-warp running state of the online softmax for the G heads.
+  float m[NT];
+  float o[KT][NT][4];  // P.V accumulators: rows = channels, columns (head, hi|lo)
+  float zc[NT][4];     // value-constant MMA: zero points, scale sums, row 12 = sum p~
+  const uint32_t* qs;      // q pairs of column 8nt+gid (head 4nt + gid/2) in shared memory
+  uint32_t nhl;            // half2(-hl): 0 for the hi column, -1 for the lo column
+  uint32_t ones_a;         // the ones row (row 12) of the value-constant MMA: lanes gid 4
+  int lane, gid, tig, hl;
+  const float* qf;         // ROPE: fp32 q [4 NT heads][D] in shared memory
+  const float2* intra;     // ROPE: cos/sin(o theta_i) [64 offsets o][D/2] in shared memory
+
+  // q_smem: the segment's q pairs in lane order ([4 NT heads][D/2] words)
+  __device__ __forceinline__ void init(const uint32_t* q_smem) {
+    lane = threadIdx.x & 31;
+    gid = lane >> 2;
+    tig = lane & 3;
+    hl = gid & 1;
+    nhl = hl ? 0xBC00BC00u : 0u;
+    ones_a = gid == 4 ? kOnes : 0u;
+    qs = q_smem + (gid >> 1) * (D / 2) + 4 * tig;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) zc[nt][i] = 0.f;
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[kt][nt][i] = 0.f;
+    }
+  }
+  // K-side logits with the keys rotated to their positions (adjacent channel
+  // pairs (2i, 2i+1) turned by pos * theta_i) in fp32 on CUDA cores.
+  // keys(kt, h, k) gives the fp32 keys at channels c = 16kt + 2tig + 8h, c + 1 of
+  // this lane's token rows 16(m/2) + gid + 8(m%2), m < 4; the chunk's token j sits
+  // at position 32 m0 + roff + j, base = cos/sin(32 m0 theta_i) [D/2].
+  template <class Keys>
+  __device__ __forceinline__ void rope_logits(Keys keys, const float2* base, int roff, float scale_log2,
+                                              float (&lg)[NT][2][2]) const {
+    constexpr int GP = 4 * NT;
+    float acc[4][GP];
+#pragma unroll
+    for (int m2 = 0; m2 < 4; ++m2)
+#pragma unroll
+      for (int g = 0; g < GP; ++g) acc[m2][g] = 0.f;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = 8 * kt + tig + 4 * h;
+        const float2 bb = base[i];
+        float2 qv[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) qv[g] = *reinterpret_cast<const float2*>(qf + g * D + 2 * i);
+        float2 k[4];
+        keys(kt, h, k);
+#pragma unroll
+        for (int m2 = 0; m2 < 4; ++m2) {
+          const int tau = 16 * (m2 >> 1) + gid + 8 * (m2 & 1);
+          const float2 in = intra[(roff + tau) * (D / 2) + i];
+          const float cs = bb.x * in.x - bb.y * in.y, sn = bb.y * in.x + bb.x * in.y;
+          const float k0 = k[m2].x * cs - k[m2].y * sn, k1 = k[m2].x * sn + k[m2].y * cs;
+#pragma unroll
+          for (int g = 0; g < GP; ++g) acc[m2][g] = fmaf(k0, qv[g].x, fmaf(k1, qv[g].y, acc[m2][g]));
+        }
+      }
+#pragma unroll
+    for (int m2 = 0; m2 < 4; ++m2)
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        acc[m2][g] += __shfl_xor_sync(0xffffffffu, acc[m2][g], 1);
+        acc[m2][g] += __shfl_xor_sync(0xffffffffu, acc[m2][g], 2);
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          // this lane's head 4nt + tig
+          float v = acc[2 * mt + r][0];
+#pragma unroll
+          for (int g = 1; g < GP; ++g) v = (g == 4 * nt + tig) ? acc[2 * mt + r][g] : v;
+          lg[nt][mt][r] = v * scale_log2;
+        }
+  }
+
+  // q pairs (kt, r) and (kt + 1, r) of this lane's column in n-tile nt (kt even)
+  __device__ __forceinline__ uint4 qpairs(int nt, int kt) const {
+    return *reinterpret_cast<const uint4*>(qs + nt * 4 * (D / 2) + 8 * kt);
+  }
+
+  // Operands of pairs P0 .. P0+7 of the lane's words (P0 a multiple of 8): one
+  // mask per register (plus one shift right by 8 per word at 2 and 4 bits, per
+  // second pair at 8 bits) leaves each code pair in the mantissa bits [p, p+b)
+  // of the two halves, exponent 0.  Bit positions by register: 2 bits
+  // 0,2,0,2 | 4,6,4,6; 4 bits 0,4,0,4; 8 bits 0 (see pos()).
+  static __device__ __forceinline__ void unpack8(const uint32_t* w, int P0, uint32_t (&a)[8]) {
+    if (BITS == 2) {
+      const uint32_t x = w[P0 / 8], y = x >> 8;
+      a[0] = x & 0x00030003u;  a[1] = x & 0x000C000Cu;  a[2] = y & 0x00030003u;  a[3] = y & 0x000C000Cu;
+      a[4] = x & 0x00300030u;  a[5] = x & 0x00C000C0u;  a[6] = y & 0x00300030u;  a[7] = y & 0x00C000C0u;
+    } else if (BITS == 4) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t x = w[P0 / 4 + h], y = x >> 8;
+        a[4 * h + 0] = x & 0x000F000Fu;
+        a[4 * h + 1] = x & 0x00F000F0u;
+        a[4 * h + 2] = y & 0x000F000Fu;
+        a[4 * h + 3] = y & 0x00F000F0u;
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t x = w[P0 / 2 + h];
+        a[2 * h + 0] = x & 0x00FF00FFu;
+        a[2 * h + 1] = (x >> 8) & 0x00FF00FFu;
+      }
+    }
+  }
+
+  // hi column: fp16(x*y); lo column: x*y - fp16(x*y) (exact: x*y has <= 22 bits).
+  __device__ __forceinline__ uint32_t split_mul(uint32_t a, uint32_t b) const {
+    const __half2 x = u32_as_h2(a), y = u32_as_h2(b);
+    const __half2 hi = __hmul2_rn(x, y);
+    return h2_as_u32(__hfma2(x, y, __hmul2_rn(hi, u32_as_h2(nhl))));
+  }
+
+  // Online softmax over one 32-token chunk.  lg[nt][mt][r]: log2-domain logits of
+  // token 16mt + gid + 8r for head 4nt + tig.  Writes p~ (fp16) to ps[g][t].
+  __device__ __forceinline__ void softmax(float (&lg)[NT][2][2], __half* ps) {
+    bool need = false;
+    float mloc[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float mx = fmaxf(fmaxf(lg[nt][0][0], lg[nt][0][1]), fmaxf(lg[nt][1][0], lg[nt][1][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      mloc[nt] = mx;
+      need |= mx > m[nt];
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float mnew = fmaxf(m[nt], mloc[nt]);
+        const float alpha = (mnew == m[nt]) ? 1.f : fast_exp2(m[nt] - mnew);
+        m[nt] = mnew;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) zc[nt][i] *= alpha;
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[kt][nt][i] *= alpha;
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = 4 * nt + tig;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const __half2 ph = __floats2half2_rn(fast_exp2(lg[nt][mt][0] - m[nt]),
+                                             fast_exp2(lg[nt][mt][1] - m[nt]));
+        if (g < G) {
+          ps[g * C::PSROW + 16 * mt + gid] = __low2half(ph);
+          ps[g * C::PSROW + 16 * mt + gid + 8] = __high2half(ph);
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  // p~ pairs for the V-side B fragments: column 8nt+gid (head 4nt + gid/2), tokens
+  // 16kt + 2tig + 8r and +1; zero in the lo columns (odd gid), which P.V leaves empty.
+  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) const {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = 4 * nt + (gid >> 1);
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          pp[nt][kt][r] = (g < G && !hl) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r) : 0u;
+    }
+  }
+
+  // One quantized 32-token group staged in shared memory.  zrow: a zero row of
+  // at least D/2 words in shared memory.
+  // roff (ROPE): the group's first position modulo 32.
+  __device__ __forceinline__ void quant_group(const uint8_t* stage, __half* ps, const uint32_t* zrow,
+                                              float scale_log2, int roff = 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(stage);
+    uint32_t kw[C::NWL];
+#pragma unroll
+    for (int ch = 0; ch < C::NWL / 4; ++ch) {
+      const uint4 v = s4[ch * 32 + lane];
+      kw[4 * ch] = v.x; kw[4 * ch + 1] = v.y; kw[4 * ch + 2] = v.z; kw[4 * ch + 3] = v.w;
+    }
+    // key metadata, lane order: pair (kt, r) of this lane at 16(kt/2) + 4tig + 2(kt%2) + r
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);
+    float lg[NT][2][2];
+    if constexpr (ROPE) {
+      // the codes dequantized in fp32: pair P = 8kt + 4mt + (r + 2h) of word P / PPW
+      auto keys = [&](int kt, int h, float2 (&k)[4]) {
+        const int w = 16 * (kt / 2) + 4 * tig + 2 * (kt % 2) + h;
+        const float2 sc = __half22float2(u32_as_h2(km[w])), zp = __half22float2(u32_as_h2(km[D / 2 + w]));
+#pragma unroll
+        for (int m2 = 0; m2 < 4; ++m2) {
+          const int P = 8 * kt + 4 * (m2 >> 1) + (m2 & 1) + 2 * h;
+          const uint32_t word = kw[P / C::PPW];
+          const int bp = slot_bitpos<BITS>(P % C::PPW);
+          constexpr uint32_t kMask = (1u << BITS) - 1u;
+          const float x0 = __uint_as_float(0x4B000000u | ((word >> bp) & kMask)) - 8388608.f;
+          const float x1 = __uint_as_float(0x4B000000u | ((word >> (16 + bp)) & kMask)) - 8388608.f;
+          k[m2] = make_float2(fmaf(sc.x, x0, zp.x), fmaf(sc.y, x1, zp.y));
+        }
+      };
+      rope_logits(keys, reinterpret_cast<const float2*>(stage + 2 * C::TB + C::KMETA + C::VMETA), roff,
+                  scale_log2, lg);
+    } else {
+      const uint32_t* ks = km + 4 * tig;           // scale pairs
+      const uint32_t* kz = km + D / 2 + 4 * tig;   // zero-point pairs
+      // constant-MMA row 0 = the zero points; a0 reads (kt, r=0) words, a2 (kt, r=1)
+      const uint32_t* rowz = gid == 0 ? kz : zrow;
+      constexpr int CH = 2;  // two independent accumulation chains over kt (shorter MMA dependency)
+      float sacc[CH][2][NT][4];
+      float cacc[CH][NT][4];
+  #pragma unroll
+      for (int ch = 0; ch < CH; ++ch)
+  #pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+        for (int i = 0; i < 4; ++i) { sacc[ch][0][nt][i] = 0.f; sacc[ch][1][nt][i] = 0.f; cacc[ch][nt][i] = 0.f; }
+  #pragma unroll
+      for (int kt2 = 0; kt2 < KT; kt2 += 2) {
+        const int ch = (kt2 / 2) % CH;
+        uint4 qv[NT];
+  #pragma unroll
+        for (int nt = 0; nt < NT; ++nt) qv[nt] = qpairs(nt, kt2);
+        const uint4 sv = *reinterpret_cast<const uint4*>(ks + 8 * kt2);
+        const uint4 zv = *reinterpret_cast<const uint4*>(rowz + 8 * kt2);
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int kt = kt2 + h;
+          const uint32_t sp0 = h ? sv.z : sv.x, sp1 = h ? sv.w : sv.y;
+          uint32_t a[8];
+          unpack8(kw, kt * 8, a);  // pairs of (kt, mt = 0) then (kt, mt = 1)
+          const uint32_t a0[4] = {a[0], a[1], a[2], a[3]};
+          const uint32_t a1[4] = {a[4], a[5], a[6], a[7]};
+          const uint32_t ac[4] = {h ? zv.z : zv.x, 0u, h ? zv.w : zv.y, 0u};
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t q0 = h ? qv[nt].z : qv[nt].x, q1 = h ? qv[nt].w : qv[nt].y;
+            const uint32_t b0 = split_mul(q0, sp0);
+            const uint32_t b1 = split_mul(q1, sp1);
+            mma_16816(sacc[ch][0][nt], a0, b0, b1);
+            mma_16816(sacc[ch][1][nt], a1, b0, b1);
+            mma_16816(cacc[ch][nt], ac, q0, q1);
+          }
+        }
+      }
+  #pragma unroll
+      for (int c2 = 1; c2 < CH; ++c2)
+  #pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sacc[0][0][nt][i] += sacc[c2][0][nt][i];
+            sacc[0][1][nt][i] += sacc[c2][1][nt][i];
+            cacc[0][nt][i] += cacc[c2][nt][i];
+          }
+  #pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        // sum_d q z of head 4nt+tig, plus the code products brought to unit scale
+        // (token row 16mt + gid + 8r holds codes at bit position pos(mt, r))
+        const float zq = __shfl_sync(0xffffffffu, cacc[0][nt][0], tig) * scale_log2;
+  #pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+          for (int r = 0; r < 2; ++r)
+            lg[nt][mt][r] = fmaf(sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1], scale_log2 * unit(mt, r), zq);
+      }
+    }
+    softmax(lg, ps);
+    uint32_t pp[NT][2][2];
+    load_pp(ps, pp);
+    // ---- P.V.  At 2 bits the codes of tokens 16..31 sit 4 bits above those of
+    // tokens 0..15 of the same row (pos(1, r) = pos(0, r) + 4): their p~ is
+    // divided by 16 (exactly, a power of two) so that both k-tiles share a unit.
+    uint32_t pv[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        pv[nt][0][r] = pp[nt][0][r];
+        pv[nt][1][r] = BITS == 2 ? h2_as_u32(__hmul2(u32_as_h2(pp[nt][1][r]), u32_as_h2(kSixteenth))) : pp[nt][1][r];
+      }
+    uint32_t vw[C::NWL];
+#pragma unroll
+    for (int ch = 0; ch < C::NWL / 4; ++ch) {
+      const uint4 v = s4[(C::TB / 16) + ch * 32 + lane];
+      vw[4 * ch] = v.x; vw[4 * ch + 1] = v.y; vw[4 * ch + 2] = v.z; vw[4 * ch + 3] = v.w;
+    }
+    // value metadata, lane order: pair (j, kt, r) of this lane at 16j + 4tig + 2kt + r
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB + C::KMETA);
+    const uint32_t* vsl = vm + 4 * tig;          // scale pairs
+    const uint32_t* vzl = vm + D / 2 + 4 * tig;  // zero pairs
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const uint4 sv = *reinterpret_cast<const uint4*>(vsl + 16 * j);
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        const uint32_t vs0 = kt ? sv.z : sv.x, vs1 = kt ? sv.w : sv.y;
+        uint32_t b[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          b[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][0]), u32_as_h2(vs0)));
+          b[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][1]), u32_as_h2(vs1)));
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+          const int mt = 2 * j + mi;
+          uint32_t a8[8];
+          unpack8(vw, mt * 8, a8);  // pairs of (mt, kt = 0) then (mt, kt = 1)
+          const uint32_t a[4] = {a8[4 * kt], a8[4 * kt + 1], a8[4 * kt + 2], a8[4 * kt + 3]};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, b[nt][0], b[nt][1]);
+        }
+      }
+    }
+    // constant-MMA rows (tokens 16kt + 2tig (+8r)): 0..D/32-1 = zero points of group
+    // j; 12 = ones (the softmax denominator); B = p~ as rounded
+    const uint4 v0 = *reinterpret_cast<const uint4*>(gid < D / 32 ? vzl + 16 * gid : zrow);
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v0.w : v0.y, ones_a};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
+    }
+    __syncwarp();
+  }
+
+  // One chunk of up to 32 fp16 tail tokens.  The rows are staged through the
+  // warp's (idle) stage ring: keys first, then values, each as 32 rows of D
+  // halves at a padded pitch (conflict-free fragment loads), missing tokens
+  // zero-filled.  Fragments come from ldmatrix (keys) and ldmatrix.trans
+  // (values, the transposed operand of P.V).
+  static constexpr int kPitch = 2 * D + 16;  // bytes per staged row
+  __device__ __forceinline__ void stage_rows(uint8_t* buf, const __half* base, int first, int count,
+                                             int th, int R) const {
+    constexpr int CPR = 2 * D / 16;  // 16-byte chunks per row
+#pragma unroll 4
+    for (int e = lane; e < kGroup * CPR; e += 32) {
+      const int t = e / CPR, ch = e % CPR;
+      const bool ok = t < count;
+      const __half* src = base + (size_t)(ok ? (th + first + t) % R : 0) * D + ch * 8;
+      cp_async_16_zfill(buf + t * kPitch + ch * 16, src, ok ? 16 : 0);
+    }
+    cp_async_commit();
+  }
+  // rope_base, roff (ROPE): cos/sin of the chunk's position block, its first
+  // position modulo 32.
+  __device__ __forceinline__ void tail_chunk(uint8_t* buf, const __half* kt_base, const __half* vt_base,
+                                             int first, int count, int th, int R, __half* ps,
+                                             float scale_log2, const float2* rope_base = nullptr, int roff = 0) {
+    stage_rows(buf, kt_base, first, count, th, R);
+    cp_async_wait<0>();
+    __syncwarp();
+    float lg[NT][2][2];
+    if constexpr (ROPE) {
+      auto keys = [&](int kt, int h, float2 (&k)[4]) {
+#pragma unroll
+        for (int m2 = 0; m2 < 4; ++m2) {
+          const int row = 16 * (m2 >> 1) + gid + 8 * (m2 & 1), c = 16 * kt + 2 * tig + 8 * h;
+          k[m2] = __half22float2(*reinterpret_cast<const __half2*>(buf + row * kPitch + c * 2));
+        }
+      };
+      rope_logits(keys, rope_base, roff, scale_log2, lg);
+      __syncwarp();
+      stage_rows(buf, vt_base, first, count, th, R);  // overlaps the softmax below
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            if (16 * mt + gid + 8 * r >= count) lg[nt][mt][r] = -INFINITY;
+    } else {
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { sacc[0][nt][i] = 0.f; sacc[1][nt][i] = 0.f; }
+    // lane's ldmatrix row: matrix lane/8 -> (+8 rows if bit 0, +8 columns if bit 1)
+    const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lcol = 8 * (lane >> 4);
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+        ldmatrix_x4(a[mt], buf + (16 * mt + lrow) * kPitch + (16 * kt + lcol) * 2);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 qv = qpairs(nt, kt & ~1);
+        const uint32_t q0 = (kt & 1) ? qv.z : qv.x, q1 = (kt & 1) ? qv.w : qv.y;
+        mma_16816(sacc[0][nt], a[0], q0, q1);
+        mma_16816(sacc[1][nt], a[1], q0, q1);
+      }
+    }
+    __syncwarp();
+    stage_rows(buf, vt_base, first, count, th, R);  // overlaps the softmax below
+    // B = q in both columns of a head: use one of them
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          lg[nt][mt][r] = (16 * mt + gid + 8 * r) < count ? sacc[mt][nt][2 * r] * scale_log2 : -INFINITY;
+    }
+    softmax(lg, ps);
+    uint32_t pp[NT][2][2];
+    load_pp(ps, pp);
+    cp_async_wait<0>();
+    __syncwarp();
+    // value rows: A[d][t] = v[t][d]; matrix lane/8 -> (+8 channels if bit 0, +8 tokens if bit 1)
+    const int vtok = (lane & 7) + 8 * (lane >> 4), vch = 8 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, buf + (16 * kt + vtok) * kPitch + (16 * mt + vch) * 2);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, pp[nt][kt][0], pp[nt][kt][1]);
+      }
+      const uint32_t ac[4] = {0u, ones_a, 0u, ones_a};  // denominator row only
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
+    }
+    __syncwarp();
+  }
+
+  // After the last quantized group of a segment, before any fp16 chunk: bring
+  // the code products in o to unit scale (output rows gid / gid + 8 hold the
+  // codes of row half 0 / 1).
+  __device__ __forceinline__ void quant_done() {
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][nt][i] *= unit(0, i >> 1);
+  }
+
+  // Write this warp's partial (m, l, unnormalised o) for its G heads.  The lo
+  // columns of o are empty; row j of zc holds sum p~ z of value group j.
+  __device__ __forceinline__ void write_partial(float* dst) const {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = 4 * nt + tig;
+      const float lt = __shfl_sync(0xffffffffu, zc[nt][2], 16 + tig);  // row 12: lanes gid 4
+      float zs[D / 32];
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) zs[j] = __shfl_sync(0xffffffffu, zc[nt][0], 4 * j + tig);
+      if (g < G) {
+        float* d = dst + g * C::PSTRIDE;
+        if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          d[4 + 16 * mt + gid] = o[mt][nt][0] + zs[mt / 2];
+          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + zs[mt / 2];
+        }
+      }
+    }
+  }
+};
+
+// Log-sum-exp merge of a segment's nparts consecutive partials into the
+// normalised output [G][D], by the whole CTA.  The partials come from other CTAs:
+// one thread bulk-copies them, MERGE_BATCH at a time, into the (idle) stage ring,
+// so a batch costs one memory round trip; the arithmetic then runs out of shared
+// memory.  Returns false if a bounded wait gave up.
+template <int D, int BITS, int G, bool ROPE>
+__device__ bool final_merge(const float* parts, int nparts, float* out, uint8_t* ring, float* s_w,
+                            uint64_t* bar, uint32_t& parity) {
+  using C = DecodeCfg<D, BITS, G, ROPE>;
+  constexpr int PS = C::PSTRIDE;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  __shared__ float s_M[G], s_L[G], s_scale[G];
+  constexpr int PER = (G * D + C::WARPS * 32 - 1) / (C::WARPS * 32);  // outputs per thread
+  float acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  if (tid < G) { s_M[tid] = -INFINITY; s_L[tid] = 0.f; }
+  bool ok = true;
+  const float* stage = reinterpret_cast<const float*>(ring);
+  for (int first = 0; first < nparts; first += C::MERGE_BATCH) {
+    const int nb = min(C::MERGE_BATCH, nparts - first);
+    __syncthreads();  // the ring (and s_w) are free
+    if (tid == 0) {
+      const uint32_t bytes = (uint32_t)(nb * G * PS * 4);
+      fence_proxy_async();
+      mbar_arrive_expect_tx(bar, bytes);
+      tma_load_1d(ring, parts + (size_t)first * G * PS, bytes, bar);
+    }
+    ok = mbar_wait(bar, parity, kMaxPolls) && ok;
+    parity ^= 1u;
+    // per head (one warp each): batch max, new running max, weights, l
+    for (int g = warp; g < G; g += nthreads / 32) {
+      float mx = -INFINITY;
+      for (int i = lane; i < nb; i += 32) mx = fmaxf(mx, stage[(i * G + g) * PS]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mold = s_M[g], mnew = fmaxf(mold, mx);
+      const float sc = (mnew == -INFINITY || mold == mnew) ? 1.f : exp2f(mold - mnew);
+      float lsum = 0.f;
+      for (int i = lane; i < nb; i += 32) {
+        const float mi = stage[(i * G + g) * PS];
+        const float w = mnew == -INFINITY ? 0.f : exp2f(mi - mnew);
+        s_w[i * G + g] = w;
+        lsum += w * stage[(i * G + g) * PS + 1];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      __syncwarp();
+      if (lane == 0) { s_M[g] = mnew; s_L[g] = s_L[g] * sc + lsum; s_scale[g] = sc; }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = tid + k * nthreads;
+      if (e < G * D) {
+        const int g = e / D, d = e % D;
+        float o = acc[k] * s_scale[g];
+        for (int i = 0; i < nb; ++i) o += s_w[i * G + g] * stage[(i * G + g) * PS + 4 + d];
+        acc[k] = o;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int e = tid + k * nthreads;
+    if (e < G * D) {
+      const float l = s_L[e / D];
+      out[e] = l > 0.f ? acc[k] / l : 0.f;
+    }
+  }
+  return ok;
+}
+
+template <int D, int BITS, int G, bool ROPE = false>
+__global__ void __launch_bounds__(DecodeCfg<D, BITS, G, ROPE>::WARPS * 32, DecodeCfg<D, BITS, G, ROPE>::MIN_CTAS)
+decode_kernel(const DecodeParams p) {
+  using C = DecodeCfg<D, BITS, G, ROPE>;
+  constexpr int NTILES = C::NT;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_last;
+  uint8_t* ring = smem;
+  __half* ps_all = reinterpret_cast<__half*>(smem + C::RING);
+  uint32_t* zrow = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS);
+  int* s_pref = reinterpret_cast<int*>(smem + C::RING + C::PS + C::ZERO);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* q_smem = reinterpret_cast<uint32_t*>(smem + C::RING + C::PS + C::ZERO + C::PREFIX);
+  float2* intra_s = reinterpret_cast<float2*>(smem + C::RING + C::PS + C::ZERO + C::PREFIX + C::QS);
+  float* qf_s = reinterpret_cast<float*>(smem + C::RING + C::PS + C::ZERO + C::PREFIX + C::QS + C::INTRA);
+  uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + C::RING + C::PS + C::ZERO + C::PREFIX + C::QS +
+                                                   C::INTRA + C::QF);
+  uint64_t* bars = bars_all + warp * C::NSTAGE;
+  uint64_t* merge_bar = bars_all + C::WARPS * C::NSTAGE;
+  __half* ps = ps_all + warp * G * C::PSROW;
+  uint8_t* wring = ring + warp * C::NSTAGE * C::STAGE;
+
+  for (int i = threadIdx.x; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
+  if (lane == 0) {
+    for (int st = 0; st < C::NSTAGE; ++st) mbar_init(bars + st, 1);
+    if (warp == 0) mbar_init(merge_bar, 1);
+    mbar_fence_init();
+  }
+  uint32_t parity = 0;  // bit st: parity of the next phase of stage st's mbarrier
+  uint32_t merge_parity = 0;
+  bool failed = false;  // a bounded wait gave up: stop using staged data
+  build_prefix(p, s_pref);
+  __syncthreads();
+  if constexpr (ROPE) {
+    // the cos/sin of the offsets 0..63 of every pair, once per CTA (the merge
+    // barrier's first phase; waited for before any thread may leave)
+    if (threadIdx.x == 0) {
+      fence_proxy_async();
+      mbar_arrive_expect_tx(merge_bar, C::INTRA);
+      tma_load_1d(intra_s, p.rope, C::INTRA, merge_bar);
+    }
+    if (!mbar_wait(merge_bar, 0, kMaxPolls)) failed = true;
+    merge_parity = 1;
+  }
+  const int64_t total = (int64_t)p.hkv * s_pref[p.batch];
+  const int64_t nstream = total < p.n_stream ? total : p.n_stream;
+  const int64_t c = blockIdx.x;
+  if (c >= nstream) return;
+  const int R = p.tail_cap;
+  const int64_t r0 = c * total / nstream, r1 = (c + 1) * total / nstream;
+  for (int64_t x = r0; x < r1;) {
+    // segment containing x: the largest b with hkv * pref[b] <= x
+    int lo = 0, hi = p.batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)p.hkv * s_pref[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int items = s_pref[b + 1] - s_pref[b];
+    const int64_t seg_first = (int64_t)p.hkv * s_pref[b];
+    const int h = (int)((x - seg_first) / items);
+    const int i0 = (int)((x - seg_first) % items);
+    const int64_t xe = min(r1, x + (items - i0));
+    const int n = (int)(xe - x);
+    const int seg = b * p.hkv + h;
+    const SeqLen L = read_lengths(p, b, false);
+    const int ng = L.nq / kGroup;
+    // this warp's contiguous share of items [i0, i0 + n)
+    const int per = (n + C::WARPS - 1) / C::WARPS;
+    const int ia = i0 + min(n, warp * per), ie = i0 + min(n, (warp + 1) * per);
+    Decoder<D, BITS, G, ROPE> dec;
+    {
+      const int ga = ia, cnt = failed ? 0 : max(0, min(ie, ng) - ia);
+      const size_t g0 = (size_t)seg * p.max_groups + ga;
+      // one lane issues four bulk copies per group, completing on the stage's mbarrier
+      auto issue = [&](int idx, int slotn) {
+        if (lane == 0) {
+          const size_t g = g0 + idx;
+          uint8_t* dst = wring + slotn * C::STAGE;
+          fence_proxy_async();
+          mbar_arrive_expect_tx(bars + slotn, C::STAGE);
+          tma_load_1d(dst, p.k_codes + g * C::TB, C::TB, bars + slotn);
+          tma_load_1d(dst + C::TB, p.v_codes + g * C::TB, C::TB, bars + slotn);
+          tma_load_1d(dst + 2 * C::TB, reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA, C::KMETA,
+                      bars + slotn);
+          tma_load_1d(dst + 2 * C::TB + C::KMETA, reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA,
+                      C::VMETA, bars + slotn);
+          if constexpr (ROPE)  // cos/sin of the group's position block: 32 (group + sinks / 32)
+            tma_load_1d(dst + 2 * C::TB + C::KMETA + C::VMETA,
+                        p.rope + (size_t)(64 + ga + idx + (L.ns >> 5)) * (D / 2), C::BASE, bars + slotn);
+        }
+      };
+      // start the first copies, then stage this segment's q (lane order) while they fly
+      int issued = 0, waited = 0;
+#pragma unroll
+      for (int st = 0; st < C::NSTAGE - 1; ++st)
+        if (st < cnt) { issue(st, st); ++issued; }
+      {
+        const __half* qh = p.q + ((size_t)b * p.hkv + h) * G * D;
+        for (int e = threadIdx.x; e < NTILES * 4 * (D / 2); e += blockDim.x) {
+          const int g = e / (D / 2), pr = e % (D / 2);
+          const int kt = 2 * (pr / 16) + (pr % 4) / 2, tg = (pr % 16) / 4, r = pr % 2;
+          const int c = 16 * kt + 2 * tg + 8 * r;
+          q_smem[e] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * D + c) : 0u;
+        }
+        if constexpr (ROPE)
+          for (int e = threadIdx.x; e < NTILES * 4 * D; e += blockDim.x)
+            qf_s[e] = e / D < G ? __half2float(qh[e]) : 0.f;
+      }
+      __syncthreads();
+      dec.init(q_smem);
+      dec.qf = qf_s;
+      dec.intra = intra_s;
+      for (int i = 0; i < cnt; ++i) {
+        if (i + C::NSTAGE - 1 < cnt) { issue(i + C::NSTAGE - 1, (i + C::NSTAGE - 1) % C::NSTAGE); ++issued; }
+        const int slotn = i % C::NSTAGE;
+        const bool ok = mbar_wait(bars + slotn, (parity >> slotn) & 1u, kMaxPolls);
+        parity ^= 1u << slotn;
+        ++waited;
+        if (!ok) { failed = true; break; }
+        dec.quant_group(wring + slotn * C::STAGE, ps, zrow, p.scale_log2, L.ns & 31);
+      }
+      // after a timeout, wait (bounded) for this warp's copies still in flight
+      for (; waited < issued; ++waited) {
+        const int slotn = waited % C::NSTAGE;
+        mbar_wait(bars + slotn, (parity >> slotn) & 1u, kMaxPolls);
+        parity ^= 1u << slotn;
+      }
+      __syncwarp();
+      dec.quant_done();
+    }
+    if (failed && lane == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
+    // fp16 chunks (tail, then sinks) whose first weighted item falls in this warp's range
+    const int ctail = (L.nt + kGroup - 1) / kGroup;
+    for (int t = max(ia, ng); t < (failed ? 0 : ie); ++t) {
+      const int u = t - ng;
+      if (u % kTailWeight != 0) continue;
+      const int ci = u / kTailWeight;
+      if (ci < ctail) {
+        const int first = ci * kGroup;
+        const int t0 = L.ns + L.nq + first;  // position of the chunk's first token
+        dec.tail_chunk(wring, p.k_tail + (size_t)seg * R * D, p.v_tail + (size_t)seg * R * D, first,
+                       min(kGroup, L.nt - first), L.th, R, ps, p.scale_log2,
+                       ROPE ? p.rope + (size_t)(64 + (t0 >> 5)) * (D / 2) : nullptr, t0 & 31);
+      } else {
+        const int first = (ci - ctail) * kGroup;
+        if (first >= L.ns) continue;
+        const int S = p.sink_cap;
+        dec.tail_chunk(wring, p.k_sink + (size_t)seg * S * D, p.v_sink + (size_t)seg * S * D, first,
+                       min(kGroup, L.ns - first), 0, S, ps, p.scale_log2,
+                       ROPE ? p.rope + (size_t)(64 + (first >> 5)) * (D / 2) : nullptr, first & 31);
+      }
+    }
+    // warp partial into the warp's (now idle) ring slice, then the CTA merge
+    dec.write_partial(reinterpret_cast<float*>(wring));
+    __syncthreads();
+    float* slot = p.part + (size_t)(c + seg) * G * C::PSTRIDE;
+    for (int e2 = threadIdx.x; e2 < G * D; e2 += blockDim.x) {
+      const int g = e2 / D, d = e2 % D;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::WARPS; ++w)
+        mx = fmaxf(mx, reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE)[g * C::PSTRIDE]);
+      float lsum = 0.f, osum = 0.f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < C::WARPS; ++w) {
+          const float* src = reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE) + g * C::PSTRIDE;
+          const float wt = exp2f(src[0] - mx);
+          lsum += wt * src[1];
+          osum += wt * src[4 + d];
+        }
+      }
+      slot[g * C::PSTRIDE + 4 + d] = osum;
+      if (d == 0) { slot[g * C::PSTRIDE] = mx; slot[g * C::PSTRIDE + 1] = lsum; }
+    }
+    __threadfence();
+    __syncthreads();
+    const int64_t c0 = cta_of(seg_first + (int64_t)h * items, total, nstream);
+    const int nparts = (int)(cta_of(seg_first + (int64_t)(h + 1) * items - 1, total, nstream) - c0 + 1);
+    if (threadIdx.x == 0) s_last = atomicAdd(&p.counters[seg], 1) == nparts - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      // the stage ring is idle here; the p~ area holds the merge weights
+      const bool ok = final_merge<D, BITS, G, ROPE>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
+                                               p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D, ring,
+                                               reinterpret_cast<float*>(ps_all), merge_bar, merge_parity);
+      if (!ok && threadIdx.x == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
+      if (threadIdx.x == 0) p.counters[seg] = 0;
+    }
+    __syncthreads();
+    x = xe;
+  }
+}
+
+struct DecodeLayout {
+  size_t counters, part, total;
+};
+
+inline DecodeLayout decode_layout(const kvq_cache* c, int G, int n_stream) {
+  DecodeLayout L;
+  const size_t seg = (size_t)c->batch * c->n_kv_heads;
+  const size_t pstride = (size_t)(c->head_dim + 4) * 4 * G;
+  L.counters = 0;
+  L.part = ((seg * 4 + 255) / 256) * 256;
+  // CTA c writes its partial of segment s to slot c + s (distinct for every pair)
+  L.total = L.part + ((size_t)n_stream + seg) * pstride;
+  return L;
+}
+
+template <int D, int BITS, int G, bool ROPE = false>
+struct DecodeLaunch {
+  // resident CTAs on the whole GPU (one wave), computed once per instantiation
+  static int slots(int* err) {
+    static int cached = -1;
+    if (cached < 0) {
+      using C = DecodeCfg<D, BITS, G, ROPE>;
+      int dev = 0, sms = 0, per = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaFuncSetAttribute(decode_kernel<D, BITS, G, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<D, BITS, G, ROPE>, C::WARPS * 32,
+                                                        C::SMEM) != cudaSuccess || per < 1) {
+        *err = 1;
+        return 0;
+      }
+      cached = sms * per;
+    }
+    return cached;
+  }
+  static kvq_status run(DecodeParams p, cudaStream_t s) {
+    using C = DecodeCfg<D, BITS, G, ROPE>;
+    int err = 0;
+    const int n = slots(&err);  // <= RING / (8 G): the final merge keeps 2 floats per partial
+    if (err) return KVQ_ERR_CUDA;
+    p.n_stream = n;
+    decode_kernel<D, BITS, G, ROPE><<<n, C::WARPS * 32, C::SMEM, s>>>(p);
+    return launch_status();
+  }
+};
+
+template <int D, int BITS, bool ROPE = false>
+kvq_status decode_dispatch_g(int G, const DecodeParams& p, cudaStream_t s) {
+  switch (G) {
+    case 1: return DecodeLaunch<D, BITS, 1, ROPE>::run(p, s);
+    case 2: return DecodeLaunch<D, BITS, 2, ROPE>::run(p, s);
+    case 4: return DecodeLaunch<D, BITS, 4, ROPE>::run(p, s);
+    case 8: return DecodeLaunch<D, BITS, 8, ROPE>::run(p, s);
+    default: return KVQ_ERR_UNSUPPORTED;
+  }
+}
+
+inline kvq_status validate_q_heads(const kvq_cache* c, int32_t n_q_heads, int* G) {
+  if (c->batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
+  if (n_q_heads < c->n_kv_heads || n_q_heads % c->n_kv_heads) return KVQ_ERR_INVALID;
+  const int g = n_q_heads / c->n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return KVQ_ERR_UNSUPPORTED;
+  *G = g;
+  return KVQ_OK;
+}
+
+}  // namespace kvq

@@ -1,0 +1,111 @@
+// Decode attention over a cache of pre-RoPE keys ("KV-cache quantization axes",
+// ihal.it, paragraph 9 and the closing paragraph: quantize the keys before the
+// rotary position embedding, rotate them after dequantization).
+//
+// The kernels are the uniform decode's (kvq_decode_impl.cuh) with ROPE set: a
+// lane dequantizes its key code pairs in fp32 (each packed pair is one rotation
+// pair, channels 2i and 2i+1), turns them by the angle of the token's position
+// and forms the dot products with the G query heads on CUDA cores; the angle of
+// position 32 m + o comes from two table rows by the angle-sum formulas: row
+// 64 + m (staged with the group by TMA) and row o (in shared memory, 64 rows).
+#include "kvq_decode_impl.cuh"
+
+namespace kvq {
+
+inline int rope_blocks(const kvq_cache* c) {
+  return (int)(((int64_t)c->sink_cap + (int64_t)kGroup * c->max_groups + c->tail_cap + kGroup - 1) / kGroup);
+}
+
+// table[o][i] = (cos, sin)(o theta_i) for o < 64; table[64 + m][i] = (cos, sin)(32 m theta_i).
+__global__ void rope_table_kernel(float2* table, int half, int rows, double base) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)rows * half) return;
+  const int row = (int)(idx / half), i = (int)(idx % half);
+  const double theta = pow(base, -2.0 * i / (2.0 * half));
+  const double pos = row < 64 ? (double)row : 32.0 * (double)(row - 64);
+  double s, c;
+  sincos(pos * theta, &s, &c);
+  table[idx] = make_float2((float)c, (float)s);
+}
+
+}  // namespace kvq
+
+extern "C" kvq_status kvq_rope_table_bytes(const kvq_cache* c, size_t* bytes) {
+  using namespace kvq;
+  kvq_status s = validate_geometry(c);
+  if (s != KVQ_OK) return s;
+  if (bytes == nullptr) return KVQ_ERR_INVALID;
+  if (c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  *bytes = (size_t)(64 + rope_blocks(c)) * (c->head_dim / 2) * sizeof(float2);
+  return KVQ_OK;
+}
+
+extern "C" kvq_status kvq_rope_table(const kvq_cache* c, float base, float* table, void* stream) {
+  using namespace kvq;
+  kvq_status s = validate_geometry(c);
+  if (s != KVQ_OK) return s;
+  if (c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (table == nullptr || !aligned(table, 16) || !(base > 1.f) || !std::isfinite(base)) return KVQ_ERR_INVALID;
+  const int rows = 64 + rope_blocks(c), half = c->head_dim / 2;
+  const int64_t n = (int64_t)rows * half;
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<float2*>(table), half, rows, (double)base);
+  return launch_status();
+}
+
+extern "C" kvq_status kvq_decode_attn_rope(const kvq_cache* c, int32_t n_q_heads, const void* q, float* out,
+                                           float sm_scale, const float* table, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  using namespace kvq;
+  kvq_status s = validate_cache(c);
+  if (s != KVQ_OK) return s;
+  if (c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  int G = 0;
+  s = validate_q_heads(c, n_q_heads, &G);
+  if (s != KVQ_OK) return s;
+  if (q == nullptr || out == nullptr || workspace == nullptr || table == nullptr) return KVQ_ERR_INVALID;
+  if (!aligned(q, 4) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(table, 16))
+    return KVQ_ERR_INVALID;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID;
+  int err = 0;
+  int n = 0;
+#define KVQ_RSLOTS(B_, G_) \
+  if (c->bits == B_ && G == G_) n = DecodeLaunch<128, B_, G_, true>::slots(&err);
+  KVQ_RSLOTS(2, 1) KVQ_RSLOTS(2, 2) KVQ_RSLOTS(2, 4) KVQ_RSLOTS(2, 8)
+  KVQ_RSLOTS(4, 1) KVQ_RSLOTS(4, 2) KVQ_RSLOTS(4, 4) KVQ_RSLOTS(4, 8)
+  KVQ_RSLOTS(8, 1) KVQ_RSLOTS(8, 2) KVQ_RSLOTS(8, 4) KVQ_RSLOTS(8, 8)
+#undef KVQ_RSLOTS
+  if (err || n == 0) return KVQ_ERR_CUDA;
+  const DecodeLayout L = decode_layout(c, G, n);
+  if (workspace_bytes < L.total) return KVQ_ERR_INVALID;
+  DecodeParams p{};
+  p.k_codes = static_cast<const uint8_t*>(c->k_codes);
+  p.v_codes = static_cast<const uint8_t*>(c->v_codes);
+  p.k_meta = static_cast<const __half*>(c->k_meta);
+  p.v_meta = static_cast<const __half*>(c->v_meta);
+  p.k_tail = static_cast<const __half*>(c->k_tail);
+  p.v_tail = static_cast<const __half*>(c->v_tail);
+  p.n_quant = c->n_quant;
+  p.n_tail = c->n_tail;
+  p.tail_head = c->tail_head;
+  p.k_sink = static_cast<const __half*>(c->k_sink);
+  p.v_sink = static_cast<const __half*>(c->v_sink);
+  p.n_sink = c->n_sink;
+  p.error_flags = c->error_flags;
+  p.q = static_cast<const __half*>(q);
+  p.rope = reinterpret_cast<const float2*>(table);
+  p.out = out;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
+  p.part = reinterpret_cast<float*>(ws + L.part);
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.batch = c->batch;
+  p.hkv = c->n_kv_heads;
+  p.max_groups = c->max_groups;
+  p.tail_cap = c->tail_cap;
+  p.sink_cap = c->sink_cap;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->bits == 2) return decode_dispatch_g<128, 2, true>(G, p, st);
+  if (c->bits == 4) return decode_dispatch_g<128, 4, true>(G, p, st);
+  return decode_dispatch_g<128, 8, true>(G, p, st);
+}

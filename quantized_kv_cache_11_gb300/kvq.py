@@ -46,7 +46,8 @@ EXPORTS = ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
            "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
            "kvq_status_string", "kvq_version", "kvq_trizone_bytes", "kvq_trizone_build",
            "kvq_trizone_decode_workspace_bytes", "kvq_trizone_decode_attn",
-           "kvq_rdkv_workspace_bytes", "kvq_rdkv_token_weights", "kvq_rdkv_allocate")
+           "kvq_rdkv_workspace_bytes", "kvq_rdkv_token_weights", "kvq_rdkv_allocate",
+           "kvq_rope_table_bytes", "kvq_rope_table", "kvq_decode_attn_rope")
 KVQ_STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -130,6 +131,9 @@ def load_library() -> ctypes.CDLL:
     lib.kvq_decode_workspace_bytes.argtypes = [cache_p, ctypes.c_int32, P(c_sz)]
     lib.kvq_decode_attn.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_sz, c_vp]
     lib.kvq_decode_attn_static.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp]
+    lib.kvq_rope_table_bytes.argtypes = [cache_p, P(c_sz)]
+    lib.kvq_rope_table.argtypes = [cache_p, c_f, c_vp, c_vp]
+    lib.kvq_decode_attn_rope.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_vp, c_sz, c_vp]
     tz_p = P(kvq_trizone)
     lib.kvq_trizone_bytes.argtypes = [tz_p, P(c_sz)]
     lib.kvq_trizone_build.argtypes = [tz_p, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp,
@@ -153,7 +157,7 @@ def load_library() -> ctypes.CDLL:
                  "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
                  "kvq_trizone_bytes", "kvq_trizone_build", "kvq_trizone_decode_workspace_bytes",
                  "kvq_trizone_decode_attn", "kvq_rdkv_workspace_bytes", "kvq_rdkv_token_weights",
-                 "kvq_rdkv_allocate"):
+                 "kvq_rdkv_allocate", "kvq_rope_table_bytes", "kvq_rope_table", "kvq_decode_attn_rope"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -254,6 +258,37 @@ def kvq_decode_attn_static(cache: "QuantizedKVCache", q: torch.Tensor, out: torc
     _check("kvq_decode_attn_static", st)
 
 
+def kvq_rope_table_bytes(cache: "QuantizedKVCache") -> int:
+    out = ctypes.c_size_t()
+    _check("kvq_rope_table_bytes", load_library().kvq_rope_table_bytes(ctypes.byref(cache.desc), ctypes.byref(out)))
+    return out.value
+
+
+def kvq_rope_table(cache: "QuantizedKVCache", base: float, table: torch.Tensor, stream=None) -> None:
+    """table: float32 device tensor of kvq_rope_table_bytes bytes."""
+    _need(table, torch.float32, "table")
+    if table.numel() * 4 < kvq_rope_table_bytes(cache) or not table.is_contiguous():
+        raise ValueError("table too small or not contiguous")
+    _check("kvq_rope_table", load_library().kvq_rope_table(ctypes.byref(cache.desc), float(base), _ptr(table),
+                                                           _stream(stream)))
+
+
+def kvq_decode_attn_rope(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.Tensor, sm_scale: float,
+                         table: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Decode over a cache of pre-RoPE keys: q fp16 [B, Hq, D] (rotated to its own
+    position), out fp32 [B, Hq, D], table from kvq_rope_table."""
+    _need(q, torch.float16, "q")
+    _need(out, torch.float32, "out")
+    _need(table, torch.float32, "table")
+    _need(workspace, torch.uint8, "workspace")
+    if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    st = load_library().kvq_decode_attn_rope(ctypes.byref(cache.desc), q.shape[1], _ptr(q), _ptr(out),
+                                             float(sm_scale), _ptr(table), _ptr(workspace), workspace.numel(),
+                                             _stream(stream))
+    _check("kvq_decode_attn_rope", st)
+
+
 class QuantizedKVCache:
     """Owns the device buffers of a uniform cache (allocated with PyTorch)."""
 
@@ -336,6 +371,21 @@ class QuantizedKVCache:
         if sm_scale is None:
             sm_scale = 1.0 / math.sqrt(self.head_dim)
         kvq_decode_attn(self, q, out, sm_scale, self.workspace(q.shape[1]), stream)
+        return out
+
+    def rope_table(self, base: float, stream=None) -> torch.Tensor:
+        """The cos/sin table of this geometry for pre-RoPE keys (kvq_rope_table)."""
+        t = torch.empty(kvq_rope_table_bytes(self) // 4, dtype=torch.float32, device=self.k_codes.device)
+        kvq_rope_table(self, base, t, stream)
+        return t
+
+    def decode_rope(self, q, table, sm_scale: Optional[float] = None, out=None, stream=None):
+        """Decode over pre-RoPE keys rotated to their positions (kvq_decode_attn_rope)."""
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(self.head_dim)
+        kvq_decode_attn_rope(self, q, out, sm_scale, table, self.workspace(q.shape[1]), stream)
         return out
 
     def device_errors(self) -> int:

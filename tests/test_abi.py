@@ -252,3 +252,17 @@ def test_rdkv_validation_fails_before_launch(lib):
     assert al(kb=float("inf")) == kvq.KVQ_ERR_INVALID
     assert al(Wt=0x800002) == kvq.KVQ_ERR_INVALID                  # W_t misaligned
     assert al(wsn=100) == kvq.KVQ_ERR_INVALID
+
+
+def test_rope_table_bytes_and_validation(lib):
+    d = kvq.kvq_cache(1, 8, 128, 2, 131072 // 32, 64)
+    out = ctypes.c_size_t()
+    assert lib.kvq_rope_table_bytes(ctypes.byref(d), ctypes.byref(out)) == kvq.KVQ_OK
+    assert out.value == (64 + (131072 + 64) // 32) * 64 * 8     # 64 offset rows + position blocks
+    d.sink_cap = 5
+    assert lib.kvq_rope_table_bytes(ctypes.byref(d), ctypes.byref(out)) == kvq.KVQ_OK
+    assert out.value == (64 + -(-(5 + 131072 + 64) // 32)) * 64 * 8
+    d64 = kvq.kvq_cache(1, 8, 64, 2, 128, 64)
+    assert lib.kvq_rope_table_bytes(ctypes.byref(d64), ctypes.byref(out)) == kvq.KVQ_ERR_UNSUPPORTED
+    assert lib.kvq_rope_table(ctypes.byref(d), ctypes.c_float(1.0), 0x100000, None) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_rope_table(ctypes.byref(d), ctypes.c_float(10000.0), 0x100008, None) == kvq.KVQ_ERR_INVALID
