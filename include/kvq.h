@@ -242,8 +242,10 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t n_q_heads,
  * Split-K over the sequence: the quantized groups of all sequences and heads
  * are cut into equal ranges on the device from the device-resident lengths
  * (ragged batches stay balanced), and the splits are merged by log-sum-exp.
- * batch <= KVQ_MAX_BATCH.  Precondition: |q[d]| * scale_k(g, d) < 65504 for every key group (fp16
- * operand range of the fused product).
+ * batch <= KVQ_MAX_BATCH.  Preconditions (fp16 operand range of the fused
+ * products): |q[d]| * scale_k(g, d) < 65504 for every key group, and
+ * scale_v(t, j) < 4094 for every value group (the softmax weights are kept
+ * below 16 between rescales).
  */
 kvq_status kvq_decode_attn(const kvq_cache* cache, int32_t n_q_heads, const void* q,
                            float* out, float sm_scale, void* workspace,

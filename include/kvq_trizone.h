@@ -139,8 +139,8 @@ kvq_status kvq_trizone_decode_workspace_bytes(const kvq_trizone* tz, int32_t n_q
  *   q, out, sm_scale   as kvq_decode_attn (out fp32, 16-byte aligned): softmax
  *             over the kept old tokens and the fresh tokens of each sequence
  *   workspace as kvq_decode_attn: zero-filled before first use, left zero-filled
- * batch * n_kv_heads <= KVQ_TZ_MAX_SEGMENTS.  Precondition: |q[d]| * scale < 65504
- * for every key group.
+ * batch * n_kv_heads <= KVQ_TZ_MAX_SEGMENTS.  Preconditions: |q[d]| * scale < 65504
+ * for every key group, value scales < 4094 (as kvq_decode_attn).
  */
 kvq_status kvq_trizone_decode_attn(const kvq_trizone* tz, int32_t n_q_heads, const void* q,
                                    float* out, float sm_scale, void* workspace,

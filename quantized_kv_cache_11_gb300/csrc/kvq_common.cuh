@@ -10,6 +10,11 @@
 namespace kvq {
 
 constexpr int kGroup = KVQ_GROUP;
+// Online softmax: the running maximum (log2 domain) is only moved, and the
+// accumulators rescaled, when a chunk's maximum exceeds it by more than this;
+// the weights p~ = exp2(logit - max) then stay below 2^4 = 16 (exact after the
+// final normalisation, which uses the same reference).
+constexpr float kLazyRescale = 4.f;
 
 // ---------------------------------------------------------------------------
 // Group quantizer ("KV-cache quantization axes", ihal.it, paragraph 3: the

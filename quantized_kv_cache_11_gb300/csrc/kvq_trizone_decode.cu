@@ -279,7 +279,7 @@ struct Decoder {
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       mloc[nt] = mx;
-      need |= mx > m[nt];
+      need |= mx > m[nt] + kLazyRescale;
     }
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
