@@ -82,26 +82,33 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // (kind::f16, fp32 accumulators in tensor memory), both operands in shared
 // memory in the K-major canonical layout without swizzle (core matrices of 8
 // rows x 16 bytes, 128 bytes apart along the channels and 2048 bytes apart
-// along the rows).  A CTA keeps one 128-row operand resident and streams 64-row
-// tiles of the other through a 4-stage ring; warp 5 loads (cp.async, then a
-// proxy fence), warp 4 issues the MMAs into one of two accumulators, warps 0-3
-// each read 32 tensor-memory lanes (one row per thread) and do the softmax
-// arithmetic.  Pass 1: resident query rows of one head, key tiles up to the
+// along the rows).  A CTA keeps 256 rows of one operand resident (two 128-row
+// blocks: every streamed tile serves both, halving the L2 traffic per product)
+// and streams 64-row tiles of the other through a 3-stage ring; warp 9 loads
+// (cp.async, then a proxy fence), warp 8 issues the MMAs into one of two
+// accumulator pairs, warps 0-7 read tensor memory (warp w: block w / 4, lanes
+// 32 (w % 4) .. +31, one row per thread) and do the softmax arithmetic.  Pass 1: resident query rows of one head, key tiles up to the
 // diagonal; pass 2: resident keys of one KV head, the query tiles of the group's
 // heads from the diagonal on.  Every wait is bounded; a CTA that gives up writes
 // NaN so the failure shows in the output.
 namespace tc {
-constexpr int kM = 128;                 // rows of the resident operand
+constexpr int kMB = 128;                // rows of one MMA (one resident block)
+constexpr int kBlocks = 2;              // resident blocks
+constexpr int kM = kMB * kBlocks;       // resident rows of a CTA
 constexpr int kN = 64;                  // rows of a streamed tile
-constexpr int kStages = 4;              // streamed tiles in the ring
-constexpr int kABytes = kM * kD * 2;    // 32 KB
+constexpr int kStages = 3;              // streamed tiles in the ring
+constexpr int kLag = kStages - 2;       // loader: tiles whose copies may still fly while it issues the next
+constexpr int kABytes = kM * kD * 2;    // 64 KB
 constexpr int kBBytes = kN * kD * 2;    // 16 KB
-constexpr int kThreads = 192;
-constexpr uint32_t kCols = 2 * kN;      // two accumulators
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+constexpr int kEpi = 4 * kBlocks;       // epilogue warps
+constexpr int kThreads = (kEpi + 2) * 32;
+constexpr int kMmaWarp = kEpi, kLoadWarp = kEpi + 1;
+constexpr uint32_t kCols = 2 * kBlocks * kN;  // two accumulator sets of kBlocks x kN columns
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kN >> 3) << 17) | ((uint32_t)(kMB >> 4) << 24);
 constexpr int kSmem = kABytes + kStages * kBBytes + kStages * kN * 4 + 16 * 8;
 
-// byte offset of 16-byte chunk c (channels 8c .. 8c+7) of row r
+// byte offset of 16-byte chunk c (channels 8c .. 8c+7) of row r (rows 128 b .. of
+// resident block b follow each other: block b starts at 32 KB b)
 __device__ __forceinline__ int cofs(int r, int c) { return (r >> 3) * 2048 + c * 128 + (r & 7) * 16; }
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(2048 >> 4) << 32) |
@@ -170,12 +177,12 @@ __global__ void __launch_bounds__(tc::kThreads) attn_tc_kernel(const AttnParams 
   const int h = PASS == 1 ? (int)blockIdx.y / p.G : (int)blockIdx.y;
   const int hq = blockIdx.y;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(full + s, 32); mbar_init(freeb + s, 5); }
-    for (int a = 0; a < 2; ++a) { mbar_init(done + a, 1); mbar_init(tfree + a, 4); }
+    for (int s = 0; s < kStages; ++s) { mbar_init(full + s, 32); mbar_init(freeb + s, kEpi + 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(done + a, 1); mbar_init(tfree + a, kEpi); }
     s_fail = 0;
     mbar_fence_init();
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                  "r"(kCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -191,8 +198,8 @@ __global__ void __launch_bounds__(tc::kThreads) attn_tc_kernel(const AttnParams 
   __syncthreads();
   fence_after();
   const uint32_t tmem = s_tmem;
-  if (warp == 5) {
-    // ---- loader: up to 3 tiles in flight; a tile is announced once its copies landed
+  if (warp == kLoadWarp) {
+    // ---- loader: kLag + 1 tiles in flight; a tile is announced once its copies landed
     auto first_of = [&](int i) { return PASS == 1 ? i * kN : (qt0 + i % per_head) * kN; };
     auto head_of = [&](int i) { return h * p.G + i / per_head; };
     auto announce = [&](int i) {
@@ -224,12 +231,12 @@ __global__ void __launch_bounds__(tc::kThreads) attn_tc_kernel(const AttnParams 
         }
       }
       cp_async_commit();
-      if (i >= 2) { cp_async_wait<2>(); announce(i - 2); }
+      if (i >= kLag) { cp_async_wait<kLag>(); announce(i - kLag); }
     }
     cp_async_wait<0>();
-    for (int j = max(0, i - 2); j < i; ++j) announce(j);
+    for (int j = max(0, i - kLag); j < i; ++j) announce(j);
     if (!ok) s_fail = 1;
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ---- MMA issue (one thread)
     if (lane == 0) {
       for (int i = 0; i < steps; ++i) {
@@ -237,17 +244,22 @@ __global__ void __launch_bounds__(tc::kThreads) attn_tc_kernel(const AttnParams 
         if (!mbar_wait(full + s, (i / kStages) & 1, kMaxPolls)) { s_fail = 1; break; }
         if (i >= 2 && !mbar_wait(tfree + a, ((i >> 1) - 1) & 1, kMaxPolls)) { s_fail = 1; break; }
         fence_after();
-        const uint32_t ab = smem_u32(sa), bb = smem_u32(sb + s * kBBytes);
+        const uint32_t bb = smem_u32(sb + s * kBBytes);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) mma(tmem + a * kN, sdesc(ab + kk * 256), sdesc(bb + kk * 256), kk > 0);
+        for (int blk2 = 0; blk2 < kBlocks; ++blk2) {
+          const uint32_t ab = smem_u32(sa + blk2 * (kMB * kD * 2));
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma(tmem + (a * kBlocks + blk2) * kN, sdesc(ab + kk * 256), sdesc(bb + kk * 256), kk > 0);
+        }
         commit(done + a);
         commit(freeb + s);
       }
     }
     __syncwarp();
   } else {
-    // ---- epilogue: thread tid holds row row0 + tid (tensor-memory lane tid)
-    const int r = row0 + tid;
+    // ---- epilogue: thread tid holds row row0 + tid: block tid / 128, tensor-memory lane tid % 128
+    const int r = row0 + tid, blk2 = warp >> 2;
     float m = -INFINITY, l = 0.f, acc = 0.f;
     bool ok = true;
     for (int i = 0; i < steps; ++i) {
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(tc::kThreads) attn_tc_kernel(const AttnParams 
       if (!mbar_wait(done + a, (i >> 1) & 1, kMaxPolls)) { ok = false; break; }
       fence_after();
       float v[kN];
-      const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + a * kN;
+      const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (a * kBlocks + blk2) * kN;
       tc::ld32(ta, v);
       tc::ld32(ta + 32, v + 32);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -308,7 +320,7 @@ __global__ void __launch_bounds__(tc::kThreads) attn_tc_kernel(const AttnParams 
   }
   fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tc::kCols));
   }
