@@ -964,7 +964,7 @@ def main_rdkv(args):
                    "head_dim": D, "prompt_tokens": T, "old_tokens": t_old, "v_avg_bits": vb, "k_avg_bits": kb,
                    "l2": f"inputs larger than L2: {q.numel() * 2 / 1e9:.2f} GB of prompt queries per step"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "rowstats_kernel + colsum_kernel",
+                     "frac": achieved / peak, "traffic": None, "kernel": "attn_tc_kernel<1> + attn_tc_kernel<2> (tcgen05)",
                      "peak_source": "measured bf16_tflops_sustained (fp16 has the bf16 rate)",
                      "algorithmic_flops": flops},
         "e2e": {"value": e2e_ms, "unit": "ms/step", "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,

@@ -149,6 +149,18 @@ __device__ __forceinline__ void ld32(uint32_t addr, float* v) {
         "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
       : "r"(addr));
 }
+// Wait for this thread's tensor-memory loads; v is tied to the wait so no use of
+// the loaded registers can be scheduled before it.
+__device__ __forceinline__ void wait_ld(float* v) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]), "+f"(v[8]),
+        "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]), "+f"(v[16]),
+        "+f"(v[17]), "+f"(v[18]), "+f"(v[19]), "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]),
+        "+f"(v[25]), "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
+      :
+      : "memory");
+}
 }  // namespace tc
 
 template <int PASS>
@@ -270,7 +282,8 @@ __global__ void __launch_bounds__(tc::kThreads) attn_tc_kernel(const AttnParams 
       const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (a * kBlocks + blk2) * kN;
       tc::ld32(ta, v);
       tc::ld32(ta + 32, v + 32);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc::wait_ld(v);       // waits for both loads
+      tc::wait_ld(v + 32);  // (nothing left to wait for: ties the second half's registers)
       fence_before();
       __syncwarp();
       if (lane == 0) tc::arrive(tfree + a);
