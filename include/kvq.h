@@ -81,7 +81,8 @@ typedef enum {
  * s, KV head h, group g (tile = 32 tokens, TB = 32 * D * b / 8 bytes):
  *   k_codes   uint8 [B][Hkv][max_groups][TB]   packed key codes of group g
  *   v_codes   uint8 [B][Hkv][max_groups][TB]   packed value codes of tokens 32g..32g+31
- *   k_meta    fp16  [B][Hkv][max_groups][2][D]   scale plane, zero plane of key group g
+ *   k_meta    fp16  [B][Hkv][max_groups][2D]     zero points and scales of key group g,
+ *                                                interleaved (below)
  *   v_meta    fp16  [B][Hkv][max_groups][2][D]   scale plane, zero plane of the value
  *                                                groups of tokens 32g..32g+31
  *   k_tail    fp16  [B][Hkv][R][D]   ring of fp16 keys; logical tail token i sits
@@ -117,11 +118,13 @@ typedef enum {
  * read as fp16 subnormals, and the two k-halves of a fragment row always share
  * a bit position.)
  *
- * Metadata planes are stored as fp16 pairs (32-bit words) in lane order, D/2
- * pairs per plane:
- *   key plane, pair 16(kt/2) + 4tig + 2(kt%2) + r (tig<4, kt<D/16, r<2):
- *       (x[c], x[c+1]) for channel c = 16kt + 2tig + 8r
- *   value plane, pair 16j + 4tig + 2kt + r (tig<4, j<D/32, kt<2, r<2):
+ * Metadata is stored as fp16 pairs (32-bit words) in lane order:
+ *   key group, D words, word 16kt + 4tig + 2r + f (tig<4, kt<D/16, r<2, f<2):
+ *       (x[c], x[c+1]) for channel c = 16kt + 2tig + 8r, x the zero points
+ *       (f = 0) or the scales (f = 1), so one 16-byte load gives a lane the
+ *       zero points and scales of its channels of k-tile kt
+ *   value groups, a scale plane then a zero plane of D/2 words each, word
+ *       16j + 4tig + 2kt + r (tig<4, j<D/32, kt<2, r<2):
  *       (x[j][t], x[j][t+1]) for channel group j, token t = 16kt + 2tig + 8r
  */
 typedef struct kvq_cache {

@@ -288,9 +288,11 @@ def append_lengths_sink(n_sink: int, n_quant: int, n_tail: int, sink_cap: int, t
 #
 # Metadata, stored as pairs of fp16 values (32-bit words), each block holding a
 # scale plane then a zero-point plane of D/2 pairs:
-#   K, per group:        pair index 16*(kt // 2) + 4*tig + 2*(kt % 2) + r
-#                        (tig < 4, kt < D/16, r < 2)
-#                        = (x[c], x[c + 1]) for channel c = 16*kt + 2*tig + 8*r
+#   K, per group (the two planes interleaved): word 16*kt + 4*tig + 2*r + f
+#                        (kt < D/16, tig < 4, r < 2, f < 2) = (x[c], x[c + 1]) of
+#                        the zero points (f = 0) or the scales (f = 1) for channel
+#                        c = 16*kt + 2*tig + 8*r (one 16-byte load gives a lane
+#                        the zero points and scales of a k-tile)
 #   V, per 32-token tile: pair index 16*j + 4*tig + 2*kt + r
 #                        (tig < 4, j < D/32, kt < 2, r < 2)
 #                        = (x[j][t], x[j][t + 1]) for channel group j and token
@@ -372,15 +374,18 @@ def unpack_tiles(packed: np.ndarray, kind: str, d: int, bits: int) -> np.ndarray
 
 @functools.lru_cache(maxsize=None)
 def key_meta_order(d: int) -> np.ndarray:
-    """Channel of every fp16 slot of a key metadata plane (length D)."""
-    order = np.full(d, -1, dtype=np.int64)
-    for tig in range(4):
-        for kt in range(d // 16):
+    """(field, channel) of every fp16 slot of a key metadata block (2D slots):
+    field 0 = zero point, 1 = scale; int64 [2D, 2]."""
+    order = np.full((2 * d, 2), -1, dtype=np.int64)
+    for kt in range(d // 16):
+        for tig in range(4):
             for r in range(2):
-                pair = 16 * (kt // 2) + 4 * tig + 2 * (kt % 2) + r
-                c = 16 * kt + 2 * tig + 8 * r
-                order[2 * pair], order[2 * pair + 1] = c, c + 1
-    assert sorted(order.tolist()) == list(range(d))
+                for f in range(2):
+                    w = 16 * kt + 4 * tig + 2 * r + f
+                    c = 16 * kt + 2 * tig + 8 * r
+                    order[2 * w] = (f, c)
+                    order[2 * w + 1] = (f, c + 1)
+    assert sorted(map(tuple, order.tolist())) == [(f, c) for f in range(2) for c in range(d)]
     order.setflags(write=False)
     return order
 
@@ -403,9 +408,13 @@ def value_meta_order(d: int) -> np.ndarray:
 
 
 def pack_key_meta(scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
-    """scale/zero float16 [..., D] of key groups -> float16 [..., 2, D] block."""
-    order = key_meta_order(scale.shape[-1])
-    return np.stack([scale[..., order], zero[..., order]], axis=-2)
+    """scale/zero float16 [..., D] of key groups -> float16 [..., 2, D] block (the
+    2D slots in key_meta_order, viewed as two rows of D)."""
+    d = scale.shape[-1]
+    order = key_meta_order(d)
+    both = np.stack([zero, scale], axis=-2)  # field 0 = zero, 1 = scale
+    flat = both[..., order[:, 0], order[:, 1]]
+    return flat.reshape(flat.shape[:-1] + (2, d))
 
 
 def pack_value_meta(scale: np.ndarray, zero: np.ndarray) -> np.ndarray:

@@ -162,15 +162,25 @@ __device__ __forceinline__ void store_meta_lane_order(const __half* nat, __half*
   constexpr int PAIRS = D / 2, PER_LANE = PAIRS / 32;
   const uint16_t* n16 = reinterpret_cast<const uint16_t*>(nat);
   uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+  if (IS_KEY) {
+    // word w = 16 kt + 4 tig + 2 r + f: the zero points (f = 0, nat[D + c]) or the
+    // scales (f = 1, nat[c]) of channels c = 16 kt + 2 tig + 8 r and c + 1
+#pragma unroll
+    for (int e = 0; e < 2 * PER_LANE; ++e) {
+      const int w = lane * 2 * PER_LANE + e;
+      const int kt = w >> 4, tig = (w >> 2) & 3, r = (w >> 1) & 1, f = w & 1;
+      const int c = 16 * kt + 2 * tig + 8 * r, base = f ? 0 : D;
+      d32[w] = (uint32_t)n16[base + c] | ((uint32_t)n16[base + c + 1] << 16);
+    }
+    return;
+  }
 #pragma unroll
   for (int plane = 0; plane < 2; ++plane) {
 #pragma unroll
     for (int e = 0; e < PER_LANE; ++e) {
       const int p = lane * PER_LANE + e;
       const int tig = (p % 16) / 4, w = p % 4, r = w % 2;
-      int idx;
-      if (IS_KEY) idx = 16 * (2 * (p / 16) + w / 2) + 2 * tig + 8 * r;
-      else idx = kGroup * (p / 16) + 16 * (w / 2) + 2 * tig + 8 * r;
+      const int idx = kGroup * (p / 16) + 16 * (w / 2) + 2 * tig + 8 * r;
       const uint32_t lo = n16[plane * D + idx], hi = n16[plane * D + idx + 1];
       d32[plane * PAIRS + p] = lo | (hi << 16);
     }

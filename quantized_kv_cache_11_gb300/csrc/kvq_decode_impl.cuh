@@ -378,14 +378,15 @@ struct Decoder {
       const uint4 v = s4[ch * 32 + lane];
       kw[4 * ch] = v.x; kw[4 * ch + 1] = v.y; kw[4 * ch + 2] = v.z; kw[4 * ch + 3] = v.w;
     }
-    // key metadata, lane order: pair (kt, r) of this lane at 16(kt/2) + 4tig + 2(kt%2) + r
+    // key metadata, lane order: word 16kt + 4tig + 2r + f = the zero points (f = 0) or
+    // scales (f = 1) of channels 16kt + 2tig + 8r and +1
     const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);
     float lg[NT][2][2];
     if constexpr (ROPE) {
       // the codes dequantized in fp32: pair P = 8kt + 4mt + (r + 2h) of word P / PPW
       auto keys = [&](int kt, int h, float2 (&k)[4]) {
-        const int w = 16 * (kt / 2) + 4 * tig + 2 * (kt % 2) + h;
-        const float2 sc = __half22float2(u32_as_h2(km[w])), zp = __half22float2(u32_as_h2(km[D / 2 + w]));
+        const int w = 16 * kt + 4 * tig + 2 * h;
+        const float2 zp = __half22float2(u32_as_h2(km[w])), sc = __half22float2(u32_as_h2(km[w + 1]));
 #pragma unroll
         for (int m2 = 0; m2 < 4; ++m2) {
           const int P = 8 * kt + 4 * (m2 >> 1) + (m2 & 1) + 2 * h;
@@ -400,10 +401,11 @@ struct Decoder {
       rope_logits(keys, reinterpret_cast<const float2*>(stage + 2 * C::TB + C::KMETA + C::VMETA), roff,
                   scale_log2, lg);
     } else {
-      const uint32_t* ks = km + 4 * tig;           // scale pairs
-      const uint32_t* kz = km + D / 2 + 4 * tig;   // zero-point pairs
-      // constant-MMA row 0 = the zero points; a0 reads (kt, r=0) words, a2 (kt, r=1)
-      const uint32_t* rowz = gid == 0 ? kz : zrow;
+      // one 16-byte load per k-tile, (zero r0, scale r0, zero r1, scale r1), is the
+      // constant product's A quad: rows gid hold the zero points (every row alike,
+      // so each lane's own column sum is q.z), rows gid + 8 the scales or zeros,
+      // whose products are not read
+      const uint32_t* kmt = km + 4 * tig;
       constexpr int CH = 2;  // two independent accumulation chains over kt (shorter MMA dependency)
       float sacc[CH][2][NT][4];
       float cacc[CH][NT][4];
@@ -419,17 +421,25 @@ struct Decoder {
         uint4 qv[NT];
   #pragma unroll
         for (int nt = 0; nt < NT; ++nt) qv[nt] = qpairs(nt, kt2);
-        const uint4 sv = *reinterpret_cast<const uint4*>(ks + 8 * kt2);
-        const uint4 zv = *reinterpret_cast<const uint4*>(rowz + 8 * kt2);
+        // (measured: at 2 bits both k-tiles' loads up front and the whole quad as
+        // the operand run fastest; at 4 and 8 bits a load per k-tile with the scale
+        // rows zeroed, which keeps the kernel within 128 registers without spills)
+        constexpr bool kHoist = BITS == 2;
+        uint4 mvp[2];
+        if (kHoist) {
+          mvp[0] = *reinterpret_cast<const uint4*>(kmt + 16 * kt2);
+          mvp[1] = *reinterpret_cast<const uint4*>(kmt + 16 * kt2 + 16);
+        }
   #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int kt = kt2 + h;
-          const uint32_t sp0 = h ? sv.z : sv.x, sp1 = h ? sv.w : sv.y;
+          const uint4 mv = kHoist ? mvp[h] : *reinterpret_cast<const uint4*>(kmt + 16 * kt);
+          const uint32_t sp0 = mv.y, sp1 = mv.w;
           uint32_t a[8];
           unpack8(kw, kt * 8, a);  // pairs of (kt, mt = 0) then (kt, mt = 1)
           const uint32_t a0[4] = {a[0], a[1], a[2], a[3]};
           const uint32_t a1[4] = {a[4], a[5], a[6], a[7]};
-          const uint32_t ac[4] = {h ? zv.z : zv.x, 0u, h ? zv.w : zv.y, 0u};
+          const uint32_t ac[4] = {mv.x, kHoist ? mv.y : 0u, mv.z, kHoist ? mv.w : 0u};
   #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const uint32_t q0 = h ? qv[nt].z : qv[nt].x, q1 = h ? qv[nt].w : qv[nt].y;
@@ -455,7 +465,7 @@ struct Decoder {
       for (int nt = 0; nt < NT; ++nt) {
         // sum_d q z of head 4nt+tig, plus the code products brought to unit scale
         // (token row 16mt + gid + 8r holds codes at bit position pos(mt, r))
-        const float zq = __shfl_sync(0xffffffffu, cacc[0][nt][0], tig) * scale_log2;
+        const float zq = cacc[0][nt][0] * scale_log2;
   #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
   #pragma unroll

@@ -359,13 +359,13 @@ def test_tile_layout_hand_positions(kind, bits, table):
 
 
 def test_metadata_order_hand_positions():
-    # key plane slot -> channel; pair (tig, kt, r) at 16(kt//2) + 4tig + 2(kt%2) + r
-    # holds channels 16kt + 2tig + 8r and +1
+    # key block slot -> (field, channel); word 16kt + 4tig + 2r + f holds field f
+    # (0 zero, 1 scale) of channels 16kt + 2tig + 8r and +1
     ko = O.key_meta_order(128)
-    assert ko[:8].tolist() == [0, 1, 8, 9, 16, 17, 24, 25]  # tig 0: (kt0,r0) (kt0,r1) (kt1,r0) (kt1,r1)
-    assert ko[8:10].tolist() == [2, 3]  # pair 4 = (tig 1, kt 0, r 0)
-    assert ko[32:34].tolist() == [32, 33]  # pair 16 = (tig 0, kt 2, r 0)
-    assert ko[126:128].tolist() == [126, 127]  # pair 63 = (tig 3, kt 7, r 1)
+    assert ko[:8].tolist() == [[0, 0], [0, 1], [1, 0], [1, 1], [0, 8], [0, 9], [1, 8], [1, 9]]
+    assert ko[8:10].tolist() == [[0, 2], [0, 3]]  # word 4 = (kt 0, tig 1, r 0, zero)
+    assert ko[32:34].tolist() == [[0, 16], [0, 17]]  # word 16 = (kt 1, tig 0, r 0, zero)
+    assert ko[254:256].tolist() == [[1, 126], [1, 127]]  # word 127 = (kt 7, tig 3, r 1, scale)
     # value plane slot -> j*32 + token; pair (tig, j, kt, r) at 16j + 4tig + 2kt + r
     vo = O.value_meta_order(128)
     assert vo[:8].tolist() == [0, 1, 8, 9, 16, 17, 24, 25]
@@ -373,8 +373,11 @@ def test_metadata_order_hand_positions():
     assert vo[32:34].tolist() == [32, 33]  # pair 16 = (tig 0, j 1, kt 0, r 0)
     # packing places a planted value where the order says
     sc = np.zeros(128, np.float16)
-    sc[19] = 5  # channel 19 = 16 + 2*1 + 1: (tig 1, kt 1, r 0) second -> pair 4+2 = 6 -> slot 13
-    assert np.nonzero(O.pack_key_meta(sc, np.zeros_like(sc))[0])[0].tolist() == [13]
+    sc[19] = 5  # channel 19 = 16 + 2*1 + 1: (kt 1, tig 1, r 0), scale -> word 16+4+1 = 21, second half -> slot 43
+    assert np.nonzero(O.pack_key_meta(sc, np.zeros_like(sc)).reshape(-1))[0].tolist() == [43]
+    zp = np.zeros(128, np.float16)
+    zp[19] = 5  # the zero point of the same channel: word 20 -> slot 41
+    assert np.nonzero(O.pack_key_meta(np.zeros_like(zp), zp).reshape(-1))[0].tolist() == [41]
     vs = np.zeros((32, 4), np.float16)
     vs[16, 1] = 7  # token 16 of channel group 1 -> pair (tig 0, j 1, kt 1, r 0) = 18 -> slot 36
     assert np.nonzero(O.pack_value_meta(vs, np.zeros_like(vs))[0])[0].tolist() == [36]
