@@ -31,9 +31,9 @@
  *     slots 16kt + 2tig + 8(i/2) and +1; pair P goes to lane word P/(16/c), slot
  *     P%(16/c) at the bit positions of kvq.h; lane word w at byte 4(32w + L) of
  *     the sub-tile (64 kt_c c bytes);
- *   key metadata: scale plane then zero plane, 16 KT halves each; pair
- *     8kt + 2tig + r (kt over all classes' k-tiles in order) holds slots
- *     16kt + 2tig + 8r and +1;
+ *   key metadata: 16 KT fp16 pairs; pair 16kt + 4tig + 2r + f (kt over all
+ *     classes' k-tiles in order) holds the zero points (f = 0) or the scales
+ *     (f = 1) of slots 16kt + 2tig + 8r and +1;
  *   values of width 2/4/8: the value tile of kvq.h at that width (1024, 2048 or
  *     4096 bytes) and its metadata block (512 bytes);
  *   values of width 16: a 16-bit value tile (8192 bytes): the value pair order of

@@ -537,9 +537,10 @@ def trizone_attention(q16: np.ndarray, tz_heads: list, sm_scale: float) -> np.nd
 #     16kt + 2tig + 8(i//2) and +1; pair P -> word P // (16/c), slot P % (16/c)
 #     at bit SLOT_BITPOS[c][slot] (+16 for the second code); lane word w at byte
 #     (w*32 + L)*4 of the sub-tile (64 * kt_c * c bytes).
-#   K metadata: scale plane then zero plane, 16 * KT halves each (KT = sum kt_c,
-#     k-tiles of all classes in order); pair (kt, tig, r) at kt*8 + tig*2 + r holds
-#     permuted slots 16kt + 2tig + 8r and +1.
+#   K metadata: 16 * KT half pairs (KT = sum kt_c, k-tiles of all classes in
+#     order); pair 16kt + 4tig + 2r + f holds the zero points (f = 0) or the
+#     scales (f = 1) of permuted slots 16kt + 2tig + 8r and +1 (the key order of
+#     the uniform cache, over k-tiles of mixed widths).
 #   V: width 2/4/8: the uniform value tile at that width (pack_tiles "V") and its
 #     metadata block (pack_value_meta); width 16: the fp16 values as a 16-bit value
 #     tile (pack_tiles "V" with 16-bit fields: word = half2 of tokens t, t + 1 of
@@ -640,20 +641,20 @@ def trizone_pack_block(blk: dict, slots: np.ndarray, kts, d: int = 128) -> np.nd
             word, bit = trizone_ksub_positions(kt, c)
             parts.append(_pack_words(codes[:, base:base + 16 * kt], word, bit, 16 * kt * c))
         base += 16 * kt
-    # K metadata, lane order over all k-tiles
+    # K metadata, lane order over all k-tiles, zero points and scales interleaved
     kt_all = sum(kts)
-    sc = np.zeros(16 * kt_all, np.float16)
-    ze = np.zeros(16 * kt_all, np.float16)
-    sc[valid] = blk["k_scale"][slots[valid]]
-    ze[valid] = blk["k_zero"][slots[valid]]
-    order = np.empty(16 * kt_all, dtype=np.int64)
+    fields = np.zeros((2, 16 * kt_all), np.float16)  # [zero, scale] per permuted slot
+    fields[0, valid] = blk["k_zero"][slots[valid]]
+    fields[1, valid] = blk["k_scale"][slots[valid]]
+    meta = np.empty(32 * kt_all, np.float16)
     for kt in range(kt_all):
         for tig in range(4):
             for r in range(2):
-                pr = kt * 8 + tig * 2 + r
                 s = 16 * kt + 2 * tig + 8 * r
-                order[2 * pr], order[2 * pr + 1] = s, s + 1
-    parts.append(np.stack([sc[order], ze[order]]).view(np.uint8).ravel())
+                for f in range(2):
+                    pr = 16 * kt + 4 * tig + 2 * r + f
+                    meta[2 * pr], meta[2 * pr + 1] = fields[f, s], fields[f, s + 1]
+    parts.append(meta.view(np.uint8))
     # V
     w = blk["width"]
     if w == 16:

@@ -393,13 +393,14 @@ __global__ void __launch_bounds__(kBlockWarps * 32) block_kernel(const __grid_co
   store_key_subtile<4>(ct, 16 * kt2, kt4, dst + 128 * kt2, lane);
   store_key_subtile<8>(ct, 16 * (kt2 + kt4), kt8, dst + 128 * kt2 + 256 * kt4, lane);
   uint8_t* kmeta = dst + key_code_bytes(kt2, kt4, kt8);
-  for (int pr = lane; pr < 8 * KT; pr += 32) {
-    const int kt = pr >> 3, tg = (pr >> 1) & 3, r = pr & 1;
+  // pair 16kt + 4tig + 2r + f: the zero points (f = 0) or scales (f = 1) of
+  // slots 16kt + 2tig + 8r and +1
+  for (int pr = lane; pr < 16 * KT; pr += 32) {
+    const int kt = pr >> 4, tg = (pr >> 2) & 3, r = (pr >> 1) & 1;
     const int s = 16 * kt + 2 * tg + 8 * r;
-    const uint32_t sw = (uint32_t)__half_as_ushort(ksc[s]) | ((uint32_t)__half_as_ushort(ksc[s + 1]) << 16);
-    const uint32_t zw = (uint32_t)__half_as_ushort(kze[s]) | ((uint32_t)__half_as_ushort(kze[s + 1]) << 16);
-    reinterpret_cast<uint32_t*>(kmeta)[pr] = sw;
-    reinterpret_cast<uint32_t*>(kmeta)[8 * KT + pr] = zw;
+    const __half* src = (pr & 1) ? ksc : kze;
+    reinterpret_cast<uint32_t*>(kmeta)[pr] =
+        (uint32_t)__half_as_ushort(src[s]) | ((uint32_t)__half_as_ushort(src[s + 1]) << 16);
   }
   __syncwarp();
   // ---- values: per token over 32-channel groups at the block's width, or fp16

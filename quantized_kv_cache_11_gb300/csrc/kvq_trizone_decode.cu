@@ -215,23 +215,24 @@ struct Decoder {
 
   // One k-tile of key class BITS: codes of sub-tile word row j, global k-tile kt.
   template <int BITS>
-  __device__ __forceinline__ void key_tile(const uint32_t* sub, int j, int kt, const uint32_t* ksc,
-                                           const uint32_t* kze, uint32_t mz, float (&s0)[NT][4],
-                                           float (&s1)[NT][4], float (&cc)[NT][4]) const {
+  __device__ __forceinline__ void key_tile(const uint32_t* sub, int j, int kt, const uint32_t* kmt,
+                                           float (&s0)[NT][4], float (&s1)[NT][4], float (&cc)[NT][4]) const {
     uint32_t w[BITS / 2];
 #pragma unroll
     for (int i = 0; i < BITS / 2; ++i) w[i] = sub[(j * (BITS / 2) + i) * 32 + lane];
     uint32_t a[8];
     unpack8<BITS>(w, a);
-    const uint2 sv = *reinterpret_cast<const uint2*>(ksc + 8 * kt);
-    const uint2 zv = *reinterpret_cast<const uint2*>(kze + 8 * kt);
+    // (zero r0, scale r0, zero r1, scale r1) of the lane's slots in k-tile kt: the
+    // constant product's A quad as it stands (rows gid: the zero points, every row
+    // alike; rows gid + 8: scales, whose products are not read)
+    const uint4 mv = *reinterpret_cast<const uint4*>(kmt + 16 * kt);
     const uint32_t a0[4] = {a[0], a[1], a[2], a[3]};
     const uint32_t a1[4] = {a[4], a[5], a[6], a[7]};
-    const uint32_t ac[4] = {zv.x & mz, 0u, zv.y & mz, 0u};  // row 0: the zero points
+    const uint32_t ac[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const uint2 qv = *reinterpret_cast<const uint2*>(qp + nt * 4 * C::QPH + 8 * kt);
-      const uint32_t b0 = split_mul(qv.x, sv.x), b1 = split_mul(qv.y, sv.y);
+      const uint32_t b0 = split_mul(qv.x, mv.y), b1 = split_mul(qv.y, mv.w);
       mma_16816(s0[nt], a0, b0, b1);
       mma_16816(s1[nt], a1, b0, b1);
       mma_16816(cc[nt], ac, qv.x, qv.y);
@@ -241,16 +242,15 @@ struct Decoder {
   // All k-tiles of one key class into the class's accumulators; k-tiles
   // alternate between two accumulation chains (shorter MMA dependency chains).
   template <int BITS>
-  __device__ __forceinline__ void key_class(const uint32_t* sub, int ktc, int& kt, const uint32_t* ksc,
-                                            const uint32_t* kze, uint32_t mz, float (&sacc)[2][2][NT][4],
-                                            float (&cc)[NT][4]) const {
+  __device__ __forceinline__ void key_class(const uint32_t* sub, int ktc, int& kt, const uint32_t* kmt,
+                                            float (&sacc)[2][2][NT][4], float (&cc)[NT][4]) const {
     int j = 0;
     for (; j + 1 < ktc; j += 2, kt += 2) {
-      key_tile<BITS>(sub, j, kt, ksc, kze, mz, sacc[0][0], sacc[0][1], cc);
-      key_tile<BITS>(sub, j + 1, kt + 1, ksc, kze, mz, sacc[1][0], sacc[1][1], cc);
+      key_tile<BITS>(sub, j, kt, kmt, sacc[0][0], sacc[0][1], cc);
+      key_tile<BITS>(sub, j + 1, kt + 1, kmt, sacc[1][0], sacc[1][1], cc);
     }
     if (j < ktc) {
-      key_tile<BITS>(sub, j, kt, ksc, kze, mz, sacc[0][0], sacc[0][1], cc);
+      key_tile<BITS>(sub, j, kt, kmt, sacc[0][0], sacc[0][1], cc);
       ++kt;
     }
   }
@@ -407,8 +407,7 @@ struct Decoder {
                                               const uint32_t* zrow, float scale_log2) {
     const int kt2 = hd[H_KT], kt4 = hd[H_KT + 1], kt8 = hd[H_KT + 2], KT = kt2 + kt4 + kt8;
     const uint32_t* st = reinterpret_cast<const uint32_t*>(rec);
-    const uint32_t* ksc = st + key_code_bytes(kt2, kt4, kt8) / 4 + 2 * tig;
-    const uint32_t* kze = ksc + 8 * KT;
+    const uint32_t* kmt = st + key_code_bytes(kt2, kt4, kt8) / 4 + 4 * tig;
     set_units(kind);
     float sacc[3][2][2][NT][4];  // [key class][chain][mt]
     float cc[NT][4];
@@ -424,15 +423,14 @@ struct Decoder {
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) cc[nt][i] = 0.f;
-    const uint32_t mz = gid == 0 ? ~0u : 0u;  // constant-product row 0: the zero points
     int kt = 0;
-    key_class<2>(st, kt2, kt, ksc, kze, mz, sacc[0], cc);
-    key_class<4>(st + 32 * kt2, kt4, kt, ksc, kze, mz, sacc[1], cc);
-    key_class<8>(st + 32 * kt2 + 64 * kt4, kt8, kt, ksc, kze, mz, sacc[2], cc);
+    key_class<2>(st, kt2, kt, kmt, sacc[0], cc);
+    key_class<4>(st + 32 * kt2, kt4, kt, kmt, sacc[1], cc);
+    key_class<8>(st + 32 * kt2 + 64 * kt4, kt8, kt, kmt, sacc[2], cc);
     float lg[NT][2][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float zq = __shfl_sync(0xffffffffu, cc[nt][0], tig) * scale_log2;
+      const float zq = cc[nt][0] * scale_log2;  // q.z (every constant row holds the zero points)
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll

@@ -533,10 +533,17 @@ def test_trizone_pack_block_fields():
         for j, ch in enumerate(cls):
             assert (got[:20, j] == blk["k_codes"][:, ch]).all() and (got[20:, j] == 0).all()
         off += 64 * kt * c
-    meta = rec[off:off + 64 * 8].view(np.float16).reshape(2, 128)
-    # pair (kt=1, tig=2, r=1) = index 13 holds slots 16 + 4 + 8 = 28 and 29
-    assert meta[0, 26].view(np.uint16) == blk["k_scale"][slots[28]].view(np.uint16)
-    assert meta[1, 27].view(np.uint16) == blk["k_zero"][slots[29]].view(np.uint16)
+    meta = rec[off:off + 64 * 8].view(np.float16)
+    # (kt=1, tig=2, r=1) covers slots 16 + 4 + 8 = 28 and 29: its zero-point pair is
+    # pair 16 + 8 + 2 = 26 (halves 52, 53), its scale pair 27 (halves 54, 55)
+    assert meta[54].view(np.uint16) == blk["k_scale"][slots[28]].view(np.uint16)
+    assert meta[53].view(np.uint16) == blk["k_zero"][slots[29]].view(np.uint16)
+    assert meta[52].view(np.uint16) == blk["k_zero"][slots[28]].view(np.uint16)
+    # the first pairs: zero points of slots 0, 1, scales of 0, 1, zero points of 8, 9
+    assert (meta[:6].view(np.uint16) == np.array([blk["k_zero"][slots[0]], blk["k_zero"][slots[1]],
+                                                   blk["k_scale"][slots[0]], blk["k_scale"][slots[1]],
+                                                   blk["k_zero"][slots[8]], blk["k_zero"][slots[9]]],
+                                                  np.float16).view(np.uint16)).all()
     off += 512
     vcodes = O.unpack_tiles(rec[off:off + 1024][None], "V", 128, 2)[0]
     assert (vcodes[:20] == blk["v_codes"]).all() and (vcodes[20:] == 0).all()
