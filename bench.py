@@ -189,6 +189,21 @@ def cpu_baseline(w, inp, budget_s=12.0, sink=0, rope=0.0):
                       f"x{w.n_kv_heads}; numpy fp64 (BLAS threads as the host sets them)"}
 
 
+def uniform_config(w, args, n_quant, n_tail, n_sink) -> dict:
+    """The keys naming a uniform-cache decode workload (both arms print them)."""
+    return {"workload": w.name + ("_prerope" if args.rope else ""), "batch": w.batch,
+            "n_q_heads": w.n_q_heads, "rope_base": args.rope or None,
+            "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.context,
+            "n_quant": n_quant, "n_tail": n_tail, "n_sink": n_sink, "bits": w.bits, "group": 32}
+
+
+def serving_config(w, mean_tokens) -> dict:
+    """The keys naming the ragged serving workload (both arms print them)."""
+    return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "bits": w.bits, "lengths": f"U[{w.ragged[0]}, {w.ragged[1]}]",
+            "mean_tokens": mean_tokens, "step": "one append + one decode"}
+
+
 def run_reference(args):
     """The oracle on the host cores, same metric/config: each step times the
     oracle on a slice of one KV head's context, sized so the run ends in minutes,
@@ -198,6 +213,7 @@ def run_reference(args):
         return
     from oracle import kvq_oracle as O
     from quantized_kv_cache_11_gb300 import synthetic as S
+    import numpy as np
     import torch
     if args.workload == "trizone":
         run_reference_trizone(args)
@@ -205,11 +221,14 @@ def run_reference(args):
     if args.workload == "rdkv":
         run_reference_rdkv(args)
         return
-    w = workload(args.bits)
-    inp = S.generate(w)
+    serving = args.workload == "serving"
+    w = S.SERVING if serving else workload(args.bits)
+    inp = S.generate(w) if serving else with_sink(S.generate(w), args.sink)
     n = int(inp["seq_len"][0])
     nt = int(inp["n_tail"][0])
-    st = O.quantize_sequence(inp["K"][0][:, :1], inp["V"][0][:, :1], n, nt, w.bits)
+    n_sink = 0 if serving else min(args.sink, n)
+    st = O.quantize_sequence(inp["K"][0][:, :1], inp["V"][0][:, :1], n, nt, w.bits, n_sink_cap=n_sink)
+    nq = n - nt - n_sink  # quantized tokens of the sampled sequence
     # per-step budget ~ 150 s / (steps + warmup), slice length a multiple of 32
     per_step = 150.0 / max(1, args.steps + args.warmup)
     t0 = time.perf_counter()
@@ -220,8 +239,8 @@ def run_reference(args):
                        O.dequantize_values(st["v_codes"][:, :sl], st["v_scale"][:, :sl],
                                            st["v_zero"][:, :sl]), w.sm_scale)
     t_blk = max(time.perf_counter() - t0, 1e-5)
-    tokens = int(min(n - nt, max(32, (per_step / t_blk * sl) // 32 * 32)))
-    nblk = (n - nt) // tokens
+    tokens = int(min(nq, max(32, (per_step / t_blk * sl) // 32 * 32)))
+    nblk = nq // tokens
     q = inp["q"][0][:w.gqa]
     times = []
     for i in range(args.warmup + args.steps):
@@ -230,19 +249,30 @@ def run_reference(args):
         t0 = time.perf_counter()
         kk = O.dequantize_keys(st["k_codes"][:, a:e], st["k_scale"][:, a // 32:e // 32],
                                st["k_zero"][:, a // 32:e // 32])
+        if args.rope:  # pre-RoPE keys: rotated to their positions after dequantization
+            kk = O.rope_rotate(kk, np.arange(n_sink + a, n_sink + e), args.rope)
         vv = O.dequantize_values(st["v_codes"][:, a:e], st["v_scale"][:, a:e], st["v_zero"][:, a:e])
         O.decode_attention(q, kk, vv, w.sm_scale)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    scale = w.n_kv_heads * (n - nt) / tokens
+    if serving:  # every (sequence, KV head) segment, scaled by its quantized tokens
+        all_q = int((inp["seq_len"] - inp["n_tail"]).sum()) * w.n_kv_heads
+        scale = all_q / tokens
+        config = serving_config(w, float(inp["seq_len"].mean()))
+        what = f"all {w.batch * w.n_kv_heads} segments ({all_q} quantized tokens; appends not timed)"
+    else:
+        scale = w.n_kv_heads * nq / tokens
+        config = uniform_config(w, args, nq, nt, n_sink)
+        what = "a full step"
+    config.update({"l2": "n/a (host cores)", "launch": "oracle calls on the host"})
     value = statistics.mean(times) * scale * 1e6
-    sample = (f"oracle dequant + fp64 attention on {tokens} of {n - nt} quantized tokens of 1 of "
-              f"{w.n_kv_heads} KV heads per step, scaled x{scale:.1f} to a full step")
+    sample = (f"oracle dequant{' + RoPE' if args.rope else ''} + fp64 attention on {tokens} of {nq} quantized "
+              f"tokens of 1 of {w.n_kv_heads} KV heads per step, scaled x{scale:.1f} to {what}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1000.0,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "bits": w.bits},
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"kind": "oracle", "cores": torch.get_num_threads(), "sample": sample,
                          "value": value, "unit": UNIT},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -533,10 +563,7 @@ def main():
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": w.name + ("_prerope" if args.rope else ""), "batch": w.batch,
-                   "n_q_heads": w.n_q_heads, "rope_base": args.rope or None,
-                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "context": w.context,
-                   "n_quant": n_quant, "n_tail": n_tail, "n_sink": n_sink, "bits": w.bits, "group": 32,
+        "config": {**uniform_config(w, args, n_quant, n_tail, n_sink),
                    "l2": f"inputs larger than L2: {n_rep} cache replicas "
                          f"({n_rep * probe.nbytes / 1e6:.0f} MB) rotated every step",
                    "launch": "CUDA graph of " + ("kvq_decode_attn_rope" if args.rope else "kvq_decode_attn") +
@@ -817,9 +844,7 @@ def main_serving(args):
         "metric": METRIC, "value": step_us, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": step_us / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": w.name, "batch": B, "n_q_heads": w.n_q_heads, "n_kv_heads": H,
-                   "head_dim": D, "bits": w.bits, "lengths": f"U[{w.ragged[0]}, {w.ragged[1]}]",
-                   "mean_tokens": float((nq + ntl).mean()), "step": "one append + one decode",
+        "config": {**serving_config(w, float(inp["seq_len"].mean())),
                    "l2": f"inputs larger than L2: {dbytes / 1e6:.0f} MB read per decode",
                    "launch": "CUDA graph of kvq_append_token + kvq_decode_attn"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -829,7 +854,7 @@ def main_serving(args):
         "clocks": clk.summary(),
         "path": {"step_us": step_us, "decode_us": decode_us, "append_us": step_us - decode_us,
                  "prefill_us": prefill_us, "prefill_gbs": prefill_bytes / (prefill_us * 1e-6) / 1e9,
-                 "prefill_bytes": prefill_bytes},
+                 "prefill_bytes": prefill_bytes, "mean_tokens_at_end": float((nq + ntl).mean())},
     }
     print(json.dumps(line), flush=True)
     if world > 1:
