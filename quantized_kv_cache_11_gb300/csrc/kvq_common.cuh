@@ -151,12 +151,12 @@ __device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst,
   }
 }
 
-// Metadata blocks are stored as fp16 pairs in "lane order" (see kvq.h): pair p
-// of a key plane holds channels 16kt + 2tig + 8r (+1) with kt = 2(p/16) +
-// (p%4)/2, tig = p%16/4, r = p%2; pair p of a value plane holds tokens
-// 16kt + 2tig + 8r (+1) of channel group j = p/16 with tig = p%16/4,
-// kt = (p%4)/2, r = p%2.  The natural-order planes are staged in shared memory
-// (nat[2][D]) and written out permuted.
+// Metadata blocks are stored as fp16 pairs in "lane order" (see kvq.h): key
+// word w = 16kt + 4tig + 2r + f holds the zero points (f = 0) or the scales
+// (f = 1) of channels 16kt + 2tig + 8r and +1; pair p of a value plane holds
+// tokens 16kt + 2tig + 8r (+1) of channel group j = p/16 with tig = p%16/4,
+// kt = (p%4)/2, r = p%2.  The natural-order planes (nat[2][D]: scales, then
+// zero points) are staged in shared memory and written out permuted.
 template <int D, bool IS_KEY>
 __device__ __forceinline__ void store_meta_lane_order(const __half* nat, __half* dst, int lane) {
   constexpr int PAIRS = D / 2, PER_LANE = PAIRS / 32;
