@@ -1,5 +1,6 @@
-"""The grouping-axis effect the pages report for keys ("KV-cache quantization
-axes", ihal.it, paragraphs 3-4): key outliers sit in a few fixed channels and are
+"""The grouping-axis effects the pages report ("KV-cache quantization axes",
+ihal.it, paragraphs 3-6), on the oracle's quantizer at 2 bits, seeded synthetic
+data.  Keys (paragraphs 3-4): key outliers sit in a few fixed channels and are
 stable across tokens, so grouping keys per channel (32 tokens of one channel)
 keeps them from widening the other channels' steps, and both the reconstruction
 error and, more strongly, the error of the attention scores are far lower than
@@ -8,8 +9,19 @@ channel is a large fixed offset plus ordinary noise (the drawn workloads use
 zero-mean N(0, 30) outliers, whose energy dominates and which a per-token group
 captures as its extreme, so they do not show this).  The pages' own figures
 (13.67 -> 4.55 reconstruction, 47.00 -> 9.60 scores, Llama-2-13B) need model
-weights and are not reproduced; checked here with the oracle's quantizer at 2
-bits on seeded synthetic keys."""
+weights and are not reproduced.
+
+Values (paragraphs 5-6): with no fixed outlier channels, per-channel groups can
+look as good or better by reconstruction error, yet the attention output, a
+softmax-weighted sum of value rows, is far worse with them (3.55 per token
+against 49.89 per channel on Llama-2-13B).  The pages trace this to sparse
+attention (84.3% measured): few tokens carry the output, and a per-channel scale
+shared across tokens carries the errors of the others into them.  Reading: value
+rows differ in magnitude from token to token (log-normal row scales), and a
+random 16% of the tokens are relevant, while the rest get weights near zero.  The
+relevance does not depend on the magnitudes.  A per-channel group that holds a
+large row gives the relevant ordinary rows a coarse step.  Per-token errors stay
+in each row, where near-zero weights cancel them."""
 import numpy as np
 import torch
 
@@ -52,3 +64,43 @@ def test_axes_tie_without_outliers():
     q = torch.randn((128,), generator=g).half().numpy().astype(np.float64)
     rec, sc = _errors(k, q)
     assert abs(rec[0] - rec[1]) < 0.1 * rec[1]
+
+
+def _values(seed, T=1024, D=128, sigma=2.0, relevant=0.16):
+    g = torch.Generator().manual_seed(seed)
+    rows = torch.exp(torch.randn((T, 1), generator=g) * sigma)  # per-token magnitude
+    v = (torch.randn((T, D), generator=g) * rows).half().numpy()
+    s = torch.randn((T,), generator=g).double().numpy()          # scores, independent of v
+    s = np.where(torch.rand((T,), generator=g).numpy() < relevant, s, s - 12.0)
+    p = np.exp(s - s.max())
+    return v, p / p.sum()
+
+
+def _value_errors(v, p, bits=2):
+    vf = v.astype(np.float64)
+    c, s, z = O.quantize_keys(v, bits)        # per channel over 32 tokens
+    v_ch = O.dequantize_keys(c, s, z)
+    c, s, z = O.quantize_values(v, bits)      # per token over 32 channels (the library's value grouping)
+    v_tok = O.dequantize_values(c, s, z)
+    rec = [np.linalg.norm(vq - vf) / np.linalg.norm(vf) for vq in (v_ch, v_tok)]
+    ref = p @ vf
+    out = [np.linalg.norm(p @ vq - ref) / np.linalg.norm(ref) for vq in (v_ch, v_tok)]
+    return rec, out
+
+
+def test_values_per_token_win_at_the_attention_output():
+    # averaged over 16 draws, like the pages' averages over layers and heads
+    errs = [_value_errors(*_values(seed)) for seed in range(100, 116)]
+    rec = np.mean([e[0] for e in errs], axis=0)
+    out = np.mean([e[1] for e in errs], axis=0)
+    rec_ratio, out_ratio = rec[0] / rec[1], out[0] / out[1]
+    assert 2 / 3 < rec_ratio < 3 / 2, rec            # reconstruction barely separates the axes
+    assert out_ratio > 2.5, out                        # the attention output does, per token far better
+    assert out_ratio > 2 * rec_ratio
+
+
+def test_value_axes_tie_with_equal_row_scales():
+    errs = [_value_errors(*_values(seed, sigma=0.0)) for seed in range(100, 104)]
+    rec = np.mean([e[0] for e in errs], axis=0)
+    out = np.mean([e[1] for e in errs], axis=0)
+    assert abs(rec[0] / rec[1] - 1) < 0.05 and abs(out[0] / out[1] - 1) < 0.1
