@@ -1042,11 +1042,17 @@ def run_reference_rdkv(args):
 
 
 def _kernel_sha(files=("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_common.cuh")) -> str:
+    """Hash of the kernel's code: the sources with comments and whitespace removed,
+    so that a traffic record stays tied to the code it was measured on."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "quantized_kv_cache_11_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "quantized_kv_cache_11_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                 # line comments
+        h.update(re.sub(r"\s+", "", text).encode())
     return h.hexdigest()[:16]
 
 

@@ -91,7 +91,7 @@ typedef enum {
  *   n_tail    int32 [B]  tokens in the tail, 0..R
  *   tail_head int32 [B]  ring slot of the oldest tail token (multiple of 32)
  *   error_flags int32 [1] or NULL: device error bits (KVQ_DEVERR_*)
- *   sink_cap  S, attention-sink window (same article, paragraph 11: high-precision
+ *   sink_cap  S, attention-sink window (same article, paragraph 9: high-precision
  *             windows for the recent tokens and for the attention sinks): the
  *             first min(S, length) tokens of a sequence stay fp16 and the
  *             quantized groups start after them; 0..256, 0 = no window (the sink
@@ -227,7 +227,7 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t n_q_heads,
 
 /*
  * kvq_decode_attn -- single-query decode attention over the packed cache
- * (ihal.it article, paragraphs 2 and 6: every decode step reads the whole
+ * (ihal.it article, paragraphs 2 and 5: every decode step reads the whole
  * cache, and the output is the softmax-weighted sum of value vectors;
  * VQKV summary, section 2: K/V rebuilt on demand inside the attention kernel).
  *
@@ -285,7 +285,7 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, int32_t n_q_heads, con
                                   float* out, float sm_scale, void* stream);
 
 /*
- * Pre-RoPE keys ("KV-cache quantization axes", ihal.it, paragraph 9 and the
+ * Pre-RoPE keys ("KV-cache quantization axes", ihal.it, paragraph 7 and the
  * closing paragraph: the keys are quantized before the rotary position
  * embedding and rotated after dequantization, so the outlier channels that make
  * per-channel groups work are not spread over their neighbours).  The cache is

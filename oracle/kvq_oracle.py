@@ -16,7 +16,7 @@ the pages by eye:
 * Recent tokens kept in full precision (same article, paragraph 8): tokens that
   do not yet fill a 32-token key group stay in an fp16 tail and are quantized
   in groups once enough have arrived.
-* Decode attention (same article, paragraphs 2 and 6): the output is a
+* Decode attention (same article, paragraphs 2 and 5): the output is a
   softmax-weighted sum of value vectors over every cached token, computed here
   in float64 over the dequantized cache.
 * The mixed-width packed layout (RDKV summary, gist.science 2605.08317,
@@ -135,7 +135,7 @@ def dequantize_values(codes, scale, zero) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
-# Decode attention (article, paragraphs 2 and 6): one query per head attends to
+# Decode attention (article, paragraphs 2 and 5): one query per head attends to
 # every cached token; output = softmax-weighted sum of value vectors.
 # ---------------------------------------------------------------------------
 def decode_attention(q16: np.ndarray, keys: np.ndarray, values: np.ndarray,
@@ -176,7 +176,7 @@ def quantize_sequence(k16: np.ndarray, v16: np.ndarray, seq_len: int, n_tail: in
     """One sequence.  k16/v16: float16 [T, Hkv, D] (T >= seq_len).
     Returns per-head arrays (leading axis Hkv).
 
-    Attention sinks ("KV-cache quantization axes", ihal.it, paragraph 11: high-
+    Attention sinks ("KV-cache quantization axes", ihal.it, paragraph 9: high-
     precision windows for the recent tokens and for the attention sinks): with
     n_sink_cap > 0 the first min(n_sink_cap, seq_len) tokens stay fp16 and the
     quantized groups start after them."""
@@ -213,7 +213,7 @@ def sequence_attention(q16: np.ndarray, state: dict, sm_scale: float) -> np.ndar
 
 
 # ---------------------------------------------------------------------------
-# Pre-RoPE keys ("KV-cache quantization axes", ihal.it, paragraph 9 and the
+# Pre-RoPE keys ("KV-cache quantization axes", ihal.it, paragraph 7 and the
 # closing paragraph: keys are quantized before the rotary position embedding and
 # the rotation is applied after dequantization).  Readings: RoPE rotates the
 # adjacent channel pairs (2i, 2i+1) of a key at position t by the angle

@@ -2,7 +2,7 @@
 // kernel templates, shared by the entry points of kvq_decode.cu and
 // kvq_decode_rope.cu.
 //
-// What it computes ("KV-cache quantization axes", ihal.it, paragraphs 2 and 6;
+// What it computes ("KV-cache quantization axes", ihal.it, paragraphs 2 and 5;
 // VQKV summary, section 2 "decoding phase"): for every sequence b and query head
 // hq (KV head h = hq / G), out = softmax(sm_scale * q . K_hat^T) . V_hat over the
 // quantized tokens (K_hat = zero + scale * code, dequantized inside the

@@ -1,5 +1,5 @@
 // Decode attention over a cache of pre-RoPE keys ("KV-cache quantization axes",
-// ihal.it, paragraph 9 and the closing paragraph: quantize the keys before the
+// ihal.it, paragraph 7 and the closing paragraph: quantize the keys before the
 // rotary position embedding, rotate them after dequantization).
 //
 // The kernels are the uniform decode's (kvq_decode_impl.cuh) with ROPE set: a

@@ -1,5 +1,5 @@
 """GPU parity of the decode over pre-RoPE keys ("KV-cache quantization axes",
-ihal.it, paragraph 9 and the closing paragraph: keys quantized before the rotary
+ihal.it, paragraph 7 and the closing paragraph: keys quantized before the rotary
 position embedding, rotated after dequantization) against the oracle, through
 the C ABI, within 2e-3 max-abs / 1e-3 mean-abs: every code width, GQA group
 sizes 1-8, fp16 tails in the ring, sink windows whose length is not a multiple

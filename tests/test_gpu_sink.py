@@ -1,5 +1,5 @@
 """GPU parity of the attention-sink window ("KV-cache quantization axes",
-ihal.it, paragraph 11: high-precision windows for the recent tokens and the
+ihal.it, paragraph 9: high-precision windows for the recent tokens and the
 attention sinks) against the oracle, through the C ABI: the first S tokens stay
 fp16, the quantized groups start after them (bit-exact), appends fill the window
 first, and decode attends over sinks + groups + tail within 2e-3 / 1e-3."""
