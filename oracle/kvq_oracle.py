@@ -1,8 +1,8 @@
 """CPU oracle for asymmetric low-bit KV-cache quantization and decode attention.
 
-TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
-baseline leg of ``bench.py`` may import this module.  It shares no code with the
-CUDA path and imports nothing from it.
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline and reference legs of ``bench.py`` may import this module.  It
+shares no code with the CUDA path and imports nothing from it.
 
 Everything here is the plain definition, written for a reader to check against
 the pages by eye:
@@ -19,6 +19,11 @@ the pages by eye:
 * Decode attention (same article, paragraphs 2 and 5): the output is a
   softmax-weighted sum of value vectors over every cached token, computed here
   in float64 over the dequantized cache.
+* Attention-sink windows (same article, paragraph 9): the first tokens of a
+  sequence may stay fp16 beside the recent tail.
+* Pre-RoPE keys (same article, paragraph 7 and the closing paragraph): keys are
+  quantized before the rotary position embedding and rotated to their
+  positions after dequantization.
 * The mixed-width packed layout (RDKV summary, gist.science 2605.08317,
   sections 2.1-2.2 and "2.2 TriZone"): widths {0,2,4,8,16} per V token, width
   0 = evicted, 16 = kept in fp16; K channels at {2,4,8} bits for kept tokens
