@@ -195,6 +195,26 @@ def _need(t: torch.Tensor, dtype, name: str):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _check_prefill_args(cache, k_shape, seq_len, n_tail) -> None:
+    """k must cover every sequence's tokens with the cache's heads and head_dim:
+    the library reads k[b, t] for b < B and t < seq_len[b]."""
+    if len(k_shape) != 4 or k_shape[0] < cache.batch or k_shape[2] != cache.n_kv_heads or \
+            k_shape[3] != cache.head_dim:
+        raise ValueError(f"k and v must be [B >= {cache.batch}, T, {cache.n_kv_heads}, {cache.head_dim}]")
+    if len(seq_len) != cache.batch or len(n_tail) != cache.batch:
+        raise ValueError("seq_len and n_tail need one entry per sequence")
+    if any(int(n) > k_shape[1] for n in seq_len):
+        raise ValueError("a sequence is longer than the token axis of k and v")
+
+
+def _check_decode_args(cache, q_shape, out_shape) -> None:
+    """q and out are [B, Hq, D] for the cache's batch and head_dim."""
+    if len(q_shape) != 3 or q_shape[0] != cache.batch or q_shape[2] != cache.head_dim:
+        raise ValueError(f"q must be [{cache.batch}, Hq, {cache.head_dim}]")
+    if tuple(out_shape) != tuple(q_shape):
+        raise ValueError("out must have the shape of q")
+
+
 def kvq_quantize_prefill(cache: "QuantizedKVCache", k: torch.Tensor, v: torch.Tensor,
                          seq_len: Sequence[int], n_tail: Sequence[int], stream=None) -> None:
     """k, v: fp16 CUDA tensors [B, T, Hkv, D] (same strides, D contiguous)."""
@@ -202,6 +222,7 @@ def kvq_quantize_prefill(cache: "QuantizedKVCache", k: torch.Tensor, v: torch.Te
     _need(v, torch.float16, "v")
     if k.shape != v.shape or k.stride() != v.stride() or k.stride(3) != 1:
         raise ValueError("k and v need equal shapes and strides with a contiguous last dim")
+    _check_prefill_args(cache, tuple(k.shape), seq_len, n_tail)
     B = cache.batch
     sl = (ctypes.c_int32 * B)(*[int(x) for x in seq_len])
     nt = (ctypes.c_int32 * B)(*[int(x) for x in n_tail])
@@ -239,6 +260,7 @@ def kvq_decode_attn(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.Tenso
     _need(workspace, torch.uint8, "workspace")
     if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
         raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    _check_decode_args(cache, tuple(q.shape), tuple(out.shape))
     st = load_library().kvq_decode_attn(ctypes.byref(cache.desc), q.shape[1], _ptr(q), _ptr(out),
                                         float(sm_scale), _ptr(workspace), workspace.numel(),
                                         _stream(stream))
@@ -253,6 +275,7 @@ def kvq_decode_attn_static(cache: "QuantizedKVCache", q: torch.Tensor, out: torc
     _need(out, torch.float32, "out")
     if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
         raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    _check_decode_args(cache, tuple(q.shape), tuple(out.shape))
     st = load_library().kvq_decode_attn_static(ctypes.byref(cache.desc), q.shape[1], _ptr(q),
                                                _ptr(out), float(sm_scale), _stream(stream))
     _check("kvq_decode_attn_static", st)
@@ -283,6 +306,7 @@ def kvq_decode_attn_rope(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.
     _need(workspace, torch.uint8, "workspace")
     if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
         raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    _check_decode_args(cache, tuple(q.shape), tuple(out.shape))
     st = load_library().kvq_decode_attn_rope(ctypes.byref(cache.desc), q.shape[1], _ptr(q), _ptr(out),
                                              float(sm_scale), _ptr(table), _ptr(workspace), workspace.numel(),
                                              _stream(stream))
@@ -444,6 +468,7 @@ def kvq_trizone_decode_attn(cache: "TriZoneCache", q: torch.Tensor, out: torch.T
     _need(workspace, torch.uint8, "workspace")
     if not (q.is_contiguous() and out.is_contiguous()) or q.shape != out.shape:
         raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    _check_decode_args(cache, tuple(q.shape), tuple(out.shape))
     st = load_library().kvq_trizone_decode_attn(ctypes.byref(cache.desc), q.shape[1], _ptr(q),
                                                 _ptr(out), float(sm_scale), _ptr(workspace),
                                                 workspace.numel(), _stream(stream))
@@ -508,17 +533,17 @@ def kvq_rdkv_workspace_bytes(desc: kvq_rdkv) -> int:
     return out.value
 
 
-def _check_prompt(t: torch.Tensor, name: str, heads: int, d: int):
+def _check_prompt(t: torch.Tensor, name: str, batch: int, heads: int, d: int):
     _need(t, torch.float16, name)
-    if t.dim() != 4 or t.shape[2] != heads or t.shape[3] != d or t.stride(3) != 1:
-        raise ValueError(f"{name} must be [B, T, {heads}, {d}] with a contiguous last dim")
+    if t.dim() != 4 or t.shape[0] < batch or t.shape[2] != heads or t.shape[3] != d or t.stride(3) != 1:
+        raise ValueError(f"{name} must be [B >= {batch}, T, {heads}, {d}] with a contiguous last dim")
 
 
 def kvq_rdkv_token_weights(desc: kvq_rdkv, q: torch.Tensor, k: torch.Tensor, n_tokens: Sequence[int],
                            sm_scale: float, w: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
     """q: fp16 [B, T, Hq, D]; k: fp16 [B, T, Hkv, D]; w: fp32 [B, Hkv, max_tokens] contiguous."""
-    _check_prompt(q, "q", desc.n_q_heads, desc.head_dim)
-    _check_prompt(k, "k", desc.n_kv_heads, desc.head_dim)
+    _check_prompt(q, "q", desc.batch, desc.n_q_heads, desc.head_dim)
+    _check_prompt(k, "k", desc.batch, desc.n_kv_heads, desc.head_dim)
     _need(w, torch.float32, "w")
     _need(workspace, torch.uint8, "workspace")
     if w.shape != (desc.batch, desc.n_kv_heads, desc.max_tokens) or not w.is_contiguous():
@@ -540,9 +565,9 @@ def kvq_rdkv_allocate(desc: kvq_rdkv, q: torch.Tensor, k: torch.Tensor, v: torch
                       W_c: Optional[torch.Tensor] = None, stream=None) -> None:
     """v_width: uint8 [B, Hkv, max_old] contiguous; k_width: uint8 [B, Hkv, D] contiguous;
     W_t: fp32 [B, Hkv, max_old] or None; W_c: fp32 [B, Hkv, D] or None."""
-    _check_prompt(q, "q", desc.n_q_heads, desc.head_dim)
-    _check_prompt(k, "k", desc.n_kv_heads, desc.head_dim)
-    _check_prompt(v, "v", desc.n_kv_heads, desc.head_dim)
+    _check_prompt(q, "q", desc.batch, desc.n_q_heads, desc.head_dim)
+    _check_prompt(k, "k", desc.batch, desc.n_kv_heads, desc.head_dim)
+    _check_prompt(v, "v", desc.batch, desc.n_kv_heads, desc.head_dim)
     if k.stride() != v.stride() or k.shape != v.shape:
         raise ValueError("k and v need equal shapes and strides")
     _need(w, torch.float32, "w")
