@@ -81,3 +81,16 @@ def test_sink_window_keeps_the_quantized_region():
     # no tail to give: the window cannot be carved out without shrinking the groups
     with pytest.raises(ValueError):
         bench.with_sink({"seq_len": np.array([256], np.int32), "n_tail": np.array([0], np.int32)}, 5)
+
+
+def test_kernel_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = tmp_path / "quantized_kv_cache_11_gb300" / "csrc"
+    src.mkdir(parents=True)
+    body = "// header comment\nint f(int x) {  /* block\n   comment */ return x + 1; }\n"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (src / "k.cu").write_text(body)
+    h0 = bench._kernel_sha(("k.cu",))
+    (src / "k.cu").write_text(body.replace("header comment", "another note").replace("  /*", "\n\n  /*"))
+    assert bench._kernel_sha(("k.cu",)) == h0      # comments and blank lines only
+    (src / "k.cu").write_text(body.replace("x + 1", "x + 2"))
+    assert bench._kernel_sha(("k.cu",)) != h0      # the code itself
