@@ -28,9 +28,14 @@
  * Conventions for every entry point
  * ---------------------------------
  * - Every buffer pointer is a DEVICE pointer owned by the caller, unless a
- *   parameter says "host".  The library allocates nothing, keeps no global
- *   state, never synchronises the stream and is re-entrant.  All work is
- *   enqueued on the given stream.
+ *   parameter says "host".  The library allocates nothing and never
+ *   synchronises the stream; all work is enqueued on the given stream.
+ * - Global state: per device, the library caches each kernel's launch facts
+ *   (shared-memory limit, resident CTAs; computed once under a lock), and
+ *   kvq_decode_attn_static uses one fixed scratch array compiled into the
+ *   library.  Every entry point except kvq_decode_attn_static is re-entrant;
+ *   calls of kvq_decode_attn_static that overlap on one GPU share that array
+ *   and race (see its comment).
  * - Argument errors are detected on the host BEFORE any launch and return
  *   KVQ_ERR_INVALID / KVQ_ERR_UNSUPPORTED / KVQ_ERR_CAPACITY with no side
  *   effect.  A failed launch returns KVQ_ERR_CUDA.  Errors that only the device

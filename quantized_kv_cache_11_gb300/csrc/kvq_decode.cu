@@ -1,6 +1,8 @@
 // C entry points of the uniform-cache decode (kernels in kvq_decode_impl.cuh).
 #include "kvq_decode_impl.cuh"
 
+#include <mutex>
+
 namespace kvq {
 
 inline int decode_slots(const kvq_cache* c, int G, int* err) {
@@ -32,49 +34,27 @@ extern "C" kvq_status kvq_decode_workspace_bytes(const kvq_cache* c, int32_t n_q
   return KVQ_OK;
 }
 
-extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, const void* q, float* out,
-                                      float sm_scale, void* workspace, size_t workspace_bytes,
-                                      void* stream) {
-  using namespace kvq;
+namespace kvq {
+
+// Host-side checks shared by both uniform decode entry points; sets *G and *L
+// (the workspace layout for the current device).
+static kvq_status decode_prepare(const kvq_cache* c, int32_t n_q_heads, const void* q, const float* out,
+                                 float sm_scale, int* G, DecodeLayout* L) {
   kvq_status s = validate_cache(c);
   if (s != KVQ_OK) return s;
-  int G = 0;
-  s = validate_q_heads(c, n_q_heads, &G);
+  s = validate_q_heads(c, n_q_heads, G);
   if (s != KVQ_OK) return s;
-  if (q == nullptr || out == nullptr || workspace == nullptr) return KVQ_ERR_INVALID;
-  if (!aligned(q, 4) || !aligned(out, 16) || !aligned(workspace, 16)) return KVQ_ERR_INVALID;
+  if (q == nullptr || out == nullptr) return KVQ_ERR_INVALID;
+  if (!aligned(q, 4) || !aligned(out, 16)) return KVQ_ERR_INVALID;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID;
   int err = 0;
-  const int n = decode_slots(c, G, &err);
+  const int n = decode_slots(c, *G, &err);
   if (err) return KVQ_ERR_CUDA;
-  const DecodeLayout L = decode_layout(c, G, n);
-  if (workspace_bytes < L.total) return KVQ_ERR_INVALID;
-  DecodeParams p{};
-  p.k_codes = static_cast<const uint8_t*>(c->k_codes);
-  p.v_codes = static_cast<const uint8_t*>(c->v_codes);
-  p.k_meta = static_cast<const __half*>(c->k_meta);
-  p.v_meta = static_cast<const __half*>(c->v_meta);
-  p.k_tail = static_cast<const __half*>(c->k_tail);
-  p.v_tail = static_cast<const __half*>(c->v_tail);
-  p.n_quant = c->n_quant;
-  p.n_tail = c->n_tail;
-  p.tail_head = c->tail_head;
-  p.k_sink = static_cast<const __half*>(c->k_sink);
-  p.v_sink = static_cast<const __half*>(c->v_sink);
-  p.n_sink = c->n_sink;
-  p.error_flags = c->error_flags;
-  p.q = static_cast<const __half*>(q);
-  p.out = out;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
-  p.part = reinterpret_cast<float*>(ws + L.part);
-  p.scale_log2 = sm_scale * 1.4426950408889634f;
-  p.batch = c->batch;
-  p.hkv = c->n_kv_heads;
-  p.max_groups = c->max_groups;
-  p.tail_cap = c->tail_cap;
-  p.sink_cap = c->sink_cap;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  *L = decode_layout(c, *G, n);
+  return KVQ_OK;
+}
+
+static kvq_status decode_launch(const kvq_cache* c, int G, const DecodeParams& p, cudaStream_t st) {
   if (c->head_dim == 128) {
     if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, st);
     if (c->bits == 4) return decode_dispatch_g<128, 4>(G, p, st);
@@ -85,13 +65,27 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, con
   return decode_dispatch_g<64, 8>(G, p, st);
 }
 
+}  // namespace kvq
+
+extern "C" kvq_status kvq_decode_attn(const kvq_cache* c, int32_t n_q_heads, const void* q, float* out,
+                                      float sm_scale, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  using namespace kvq;
+  int G = 0;
+  DecodeLayout L{};
+  if (workspace == nullptr || !aligned(workspace, 16)) return KVQ_ERR_INVALID;
+  kvq_status s = decode_prepare(c, n_q_heads, q, out, sm_scale, &G, &L);
+  if (s != KVQ_OK) return s;
+  if (workspace_bytes < L.total) return KVQ_ERR_INVALID;
+  const DecodeParams p = decode_params(c, q, out, sm_scale, static_cast<uint8_t*>(workspace), L);
+  return decode_launch(c, G, p, static_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------------------
 // Decode without a caller-supplied workspace.  The split-K partials and merge
 // counters live in a fixed array compiled into the library, so the call needs
 // no device allocation at all.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace kvq {
 
 // Every GPU that loads the library holds this array until the process exits.
@@ -124,18 +118,10 @@ static cudaError_t static_scratch_ptr(void** out) {
 extern "C" kvq_status kvq_decode_attn_static(const kvq_cache* c, int32_t n_q_heads, const void* q, float* out,
                                              float sm_scale, void* stream) {
   using namespace kvq;
-  kvq_status s = validate_cache(c);
-  if (s != KVQ_OK) return s;
   int G = 0;
-  s = validate_q_heads(c, n_q_heads, &G);
+  DecodeLayout L{};
+  kvq_status s = decode_prepare(c, n_q_heads, q, out, sm_scale, &G, &L);
   if (s != KVQ_OK) return s;
-  if (q == nullptr || out == nullptr) return KVQ_ERR_INVALID;
-  if (!aligned(q, 4) || !aligned(out, 16)) return KVQ_ERR_INVALID;
-  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID;
-  int err = 0;
-  const int n = decode_slots(c, G, &err);
-  if (err) return KVQ_ERR_CUDA;
-  const DecodeLayout L = decode_layout(c, G, n);
   if (L.total > (size_t)KVQ_STATIC_SCRATCH_BYTES) return KVQ_ERR_CAPACITY;
   void* scratch = nullptr;
   if (static_scratch_ptr(&scratch) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -144,36 +130,6 @@ extern "C" kvq_status kvq_decode_attn_static(const kvq_cache* c, int32_t n_q_hea
   // the merge counters must start at zero; a completed call leaves them zero, an
   // interrupted one might not, so clear them every time (a memset, no allocation)
   if (cudaMemsetAsync(ws + L.counters, 0, L.part - L.counters, st) != cudaSuccess) return KVQ_ERR_CUDA;
-  DecodeParams p{};
-  p.k_codes = static_cast<const uint8_t*>(c->k_codes);
-  p.v_codes = static_cast<const uint8_t*>(c->v_codes);
-  p.k_meta = static_cast<const __half*>(c->k_meta);
-  p.v_meta = static_cast<const __half*>(c->v_meta);
-  p.k_tail = static_cast<const __half*>(c->k_tail);
-  p.v_tail = static_cast<const __half*>(c->v_tail);
-  p.n_quant = c->n_quant;
-  p.n_tail = c->n_tail;
-  p.tail_head = c->tail_head;
-  p.k_sink = static_cast<const __half*>(c->k_sink);
-  p.v_sink = static_cast<const __half*>(c->v_sink);
-  p.n_sink = c->n_sink;
-  p.error_flags = c->error_flags;
-  p.q = static_cast<const __half*>(q);
-  p.out = out;
-  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
-  p.part = reinterpret_cast<float*>(ws + L.part);
-  p.scale_log2 = sm_scale * 1.4426950408889634f;
-  p.batch = c->batch;
-  p.hkv = c->n_kv_heads;
-  p.max_groups = c->max_groups;
-  p.tail_cap = c->tail_cap;
-  p.sink_cap = c->sink_cap;
-  if (c->head_dim == 128) {
-    if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, st);
-    if (c->bits == 4) return decode_dispatch_g<128, 4>(G, p, st);
-    return decode_dispatch_g<128, 8>(G, p, st);
-  }
-  if (c->bits == 2) return decode_dispatch_g<64, 2>(G, p, st);
-  if (c->bits == 4) return decode_dispatch_g<64, 4>(G, p, st);
-  return decode_dispatch_g<64, 8>(G, p, st);
+  const DecodeParams p = decode_params(c, q, out, sm_scale, ws, L);
+  return decode_launch(c, G, p, st);
 }

@@ -955,24 +955,11 @@ inline DecodeLayout decode_layout(const kvq_cache* c, int G, int n_stream) {
 
 template <int D, int BITS, int G, bool ROPE = false>
 struct DecodeLaunch {
-  // resident CTAs on the whole GPU (one wave), computed once per instantiation
+  // resident CTAs on the whole current GPU (one wave), computed once per device
   static int slots(int* err) {
-    static int cached = -1;
-    if (cached < 0) {
-      using C = DecodeCfg<D, BITS, G, ROPE>;
-      int dev = 0, sms = 0, per = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaFuncSetAttribute(decode_kernel<D, BITS, G, ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::SMEM) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<D, BITS, G, ROPE>, C::WARPS * 32,
-                                                        C::SMEM) != cudaSuccess || per < 1) {
-        *err = 1;
-        return 0;
-      }
-      cached = sms * per;
-    }
-    return cached;
+    using C = DecodeCfg<D, BITS, G, ROPE>;
+    return device_slots(reinterpret_cast<const void*>(decode_kernel<D, BITS, G, ROPE>), C::WARPS * 32, C::SMEM,
+                        err);
   }
   static kvq_status run(DecodeParams p, cudaStream_t s) {
     using C = DecodeCfg<D, BITS, G, ROPE>;
@@ -994,6 +981,39 @@ kvq_status decode_dispatch_g(int G, const DecodeParams& p, cudaStream_t s) {
     case 8: return DecodeLaunch<D, BITS, 8, ROPE>::run(p, s);
     default: return KVQ_ERR_UNSUPPORTED;
   }
+}
+
+// The kernel parameters of one decode call: the cache's buffers and lengths, q
+// and out, and the workspace (counters and partials at the offsets of L, from
+// the base ws).  Shared by every decode entry point.
+inline DecodeParams decode_params(const kvq_cache* c, const void* q, float* out, float sm_scale, uint8_t* ws,
+                                  const DecodeLayout& L, const float* rope_table = nullptr) {
+  DecodeParams p{};
+  p.k_codes = static_cast<const uint8_t*>(c->k_codes);
+  p.v_codes = static_cast<const uint8_t*>(c->v_codes);
+  p.k_meta = static_cast<const __half*>(c->k_meta);
+  p.v_meta = static_cast<const __half*>(c->v_meta);
+  p.k_tail = static_cast<const __half*>(c->k_tail);
+  p.v_tail = static_cast<const __half*>(c->v_tail);
+  p.n_quant = c->n_quant;
+  p.n_tail = c->n_tail;
+  p.tail_head = c->tail_head;
+  p.k_sink = static_cast<const __half*>(c->k_sink);
+  p.v_sink = static_cast<const __half*>(c->v_sink);
+  p.n_sink = c->n_sink;
+  p.error_flags = c->error_flags;
+  p.q = static_cast<const __half*>(q);
+  p.rope = reinterpret_cast<const float2*>(rope_table);
+  p.out = out;
+  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
+  p.part = reinterpret_cast<float*>(ws + L.part);
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.batch = c->batch;
+  p.hkv = c->n_kv_heads;
+  p.max_groups = c->max_groups;
+  p.tail_cap = c->tail_cap;
+  p.sink_cap = c->sink_cap;
+  return p;
 }
 
 inline kvq_status validate_q_heads(const kvq_cache* c, int32_t n_q_heads, int* G) {

@@ -78,32 +78,7 @@ extern "C" kvq_status kvq_decode_attn_rope(const kvq_cache* c, int32_t n_q_heads
   if (err || n == 0) return KVQ_ERR_CUDA;
   const DecodeLayout L = decode_layout(c, G, n);
   if (workspace_bytes < L.total) return KVQ_ERR_INVALID;
-  DecodeParams p{};
-  p.k_codes = static_cast<const uint8_t*>(c->k_codes);
-  p.v_codes = static_cast<const uint8_t*>(c->v_codes);
-  p.k_meta = static_cast<const __half*>(c->k_meta);
-  p.v_meta = static_cast<const __half*>(c->v_meta);
-  p.k_tail = static_cast<const __half*>(c->k_tail);
-  p.v_tail = static_cast<const __half*>(c->v_tail);
-  p.n_quant = c->n_quant;
-  p.n_tail = c->n_tail;
-  p.tail_head = c->tail_head;
-  p.k_sink = static_cast<const __half*>(c->k_sink);
-  p.v_sink = static_cast<const __half*>(c->v_sink);
-  p.n_sink = c->n_sink;
-  p.error_flags = c->error_flags;
-  p.q = static_cast<const __half*>(q);
-  p.rope = reinterpret_cast<const float2*>(table);
-  p.out = out;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.counters = reinterpret_cast<int32_t*>(ws + L.counters);
-  p.part = reinterpret_cast<float*>(ws + L.part);
-  p.scale_log2 = sm_scale * 1.4426950408889634f;
-  p.batch = c->batch;
-  p.hkv = c->n_kv_heads;
-  p.max_groups = c->max_groups;
-  p.tail_cap = c->tail_cap;
-  p.sink_cap = c->sink_cap;
+  const DecodeParams p = decode_params(c, q, out, sm_scale, static_cast<uint8_t*>(workspace), L, table);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->bits == 2) return decode_dispatch_g<128, 2, true>(G, p, st);
   if (c->bits == 4) return decode_dispatch_g<128, 4, true>(G, p, st);

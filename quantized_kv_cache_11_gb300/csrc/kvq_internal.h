@@ -5,6 +5,10 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -47,6 +51,51 @@ inline kvq_status validate_cache(const kvq_cache* c) {
     if (c->n_sink == nullptr || !aligned(c->n_sink, 4)) return KVQ_ERR_INVALID;
   }
   return KVQ_OK;
+}
+
+// Launch facts of one kernel on the CURRENT device: its dynamic shared-memory
+// limit raised to `smem` bytes (function attributes are per device) and the
+// number of its CTAs of `threads` threads that fit on the whole GPU at once
+// (SM count x CTAs per SM).  Computed once per (kernel, device) under a lock,
+// so several host threads and several GPUs in one process each get their own.
+// Returns 0 (and sets *err) if a CUDA query fails or no CTA fits.
+inline int device_slots(const void* kernel, int threads, int smem, int* err) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    *err = 1;
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kernel, dev);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int sms = 0, per = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, smem) != cudaSuccess || per < 1) {
+    *err = 1;
+    return 0;
+  }
+  cache[key] = sms * per;
+  return sms * per;
+}
+
+// Raise a kernel's dynamic shared-memory limit to `smem` bytes on the current
+// device, once per (kernel, device) under a lock.  Returns false if a CUDA call
+// fails.
+inline bool device_smem_attr(const void* kernel, int smem) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, bool> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kernel, dev);
+  if (done.count(key)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+  done[key] = true;
+  return true;
 }
 
 inline kvq_status launch_status() {

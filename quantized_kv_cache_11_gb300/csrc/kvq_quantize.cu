@@ -316,13 +316,7 @@ struct PrefillLaunch {
   template <int VEC>
   static kvq_status launch(const PrefillParams& p, dim3 grid, cudaStream_t s) {
     constexpr int smem = kPrefillWarps * StagedTile<D>::BYTES;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(prefill_kernel<D, BITS, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-          cudaSuccess)
-        return KVQ_ERR_CUDA;
-      attr = true;
-    }
+    if (!device_smem_attr(reinterpret_cast<const void*>(prefill_kernel<D, BITS, VEC>), smem)) return KVQ_ERR_CUDA;
     prefill_kernel<D, BITS, VEC><<<grid, kPrefillWarps * 32, smem, s>>>(p);
     return launch_status();
   }
@@ -339,13 +333,7 @@ template <int D, int BITS>
 struct AppendLaunch {
   static kvq_status run(const AppendParams& p, int batch, cudaStream_t s) {
     constexpr int smem = kAppendWarps * StagedTile<D>::BYTES;
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(append_kernel<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-          cudaSuccess)
-        return KVQ_ERR_CUDA;
-      attr = true;
-    }
+    if (!device_smem_attr(reinterpret_cast<const void*>(append_kernel<D, BITS>), smem)) return KVQ_ERR_CUDA;
     append_kernel<D, BITS><<<batch, kAppendWarps * 32, smem, s>>>(p);
     return launch_status();
   }

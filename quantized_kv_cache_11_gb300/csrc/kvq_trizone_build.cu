@@ -484,12 +484,7 @@ extern "C" kvq_status kvq_trizone_build(const kvq_trizone* tz, const void* k, co
   index_kernel<<<dim3(tz->n_kv_heads, tz->batch), kIndexThreads, 0, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
   constexpr int smem = kBlockWarps * kWarpScratch;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr = true;
-  }
+  if (!device_smem_attr(reinterpret_cast<const void*>(block_kernel), smem)) return KVQ_ERR_CUDA;
   const int gx = (max_items + kBlockWarps - 1) / kBlockWarps;
   block_kernel<<<dim3(gx, tz->n_kv_heads, tz->batch), kBlockWarps * 32, smem, st>>>(p);
   return launch_status();

@@ -824,24 +824,10 @@ inline Layout layout(const kvq_trizone* t, int G, int n_stream) {
 
 template <int G>
 struct Launch {
+  // resident CTAs on the whole current GPU, computed once per device
   static int slots(int* err) {
-    static int cached = -1;
-    if (cached < 0) {
-      using C = Cfg<G>;
-      int dev = 0, sms = 0, per = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-              cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel<G>, C::WARPS * 32, C::SMEM) !=
-              cudaSuccess ||
-          per < 1) {
-        *err = 1;
-        return 0;
-      }
-      cached = sms * per;
-    }
-    return cached;
+    using C = Cfg<G>;
+    return device_slots(reinterpret_cast<const void*>(decode_kernel<G>), C::WARPS * 32, C::SMEM, err);
   }
   static kvq_status run(Params p, cudaStream_t st) {
     int err = 0;
