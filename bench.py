@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused-dequant decode attn: µs/step, achieved HBM GB/s vs peak (Llama-3.1-8B, 128k)"
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6800.0
+MIN_TIMED_S = 0.5  # shortest timed region (clock samples under load)
 
 
 def parse():
@@ -45,8 +46,11 @@ def parse():
                          "rotary base (e.g. 500000); 0 = plain decode")
     ap.add_argument("--sink", type=int, default=0,
                     help="uniform cache: keep the first S tokens fp16 (attention-sink window)")
-    ap.add_argument("--workload", default="uniform", choices=["uniform", "trizone", "serving", "rdkv"],
-                    help="uniform: the 128k-token uniform cache (default); trizone: the "
+    ap.add_argument("--workload", default="uniform",
+                    choices=["uniform", "llama2_13b", "trizone", "serving", "rdkv"],
+                    help="uniform: the Llama-3.1-8B 128k-token uniform cache (default); llama2_13b: "
+                         "the Llama-2-13B MHA cache (8 sequences x 40 heads x 4,096 tokens, "
+                         "4,064 quantized + 32 fp16); trizone: the "
                          "mixed-width cache, 4 sequences x 65,408 old + 128 fresh tokens; "
                          "serving: 16 ragged sequences of 8k-32k tokens, 4-bit, one "
                          "append + decode per step; rdkv: the bit allocation (token weights "
@@ -58,9 +62,17 @@ def parse():
     return ap.parse_args()
 
 
-def workload(bits):
+def workload(bits, name="uniform"):
     from quantized_kv_cache_11_gb300 import synthetic as S
+    if name == "llama2_13b":
+        w = S.LLAMA2_13B
+        return w if bits == 2 else w.scaled(name=w.name.replace("2bit", f"{bits}bit"), bits=bits)
     return S.LLAMA31_8B_128K if bits == 2 else S.LLAMA31_8B_128K_4BIT
+
+
+def dtype_label(bits) -> str:
+    """The arithmetic the decode path computes in."""
+    return f"int{bits} codes x fp16 operands on tensor cores, fp32 accumulate and softmax"
 
 
 def algorithmic_bytes(w, n_quant, n_tail, n_sink=0) -> int:
@@ -163,30 +175,158 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, inp, budget_s=12.0, sink=0, rope=0.0):
-    """The oracle as it stands on this host: dequantize + fp64 attention for one
-    KV head (its 4 query heads) over the whole context, repeated for ~budget_s,
-    scaled by the number of KV heads to one full decode step."""
+# ---- the oracle on the host cores: one code path for the GPU arm's cpu_baseline
+# and the reference arm.  Each (sequence, KV head) segment of the cache is one
+# unit of work; worker processes (spawned, one per core, single-threaded BLAS)
+# each hold a round-robin share of the sampled segments, quantize them once, and
+# then run the oracle's fp64 decode attention over them on every step.
+
+def _oracle_worker(conn, bits, sm_scale, rope):
     from oracle import kvq_oracle as O
-    import torch
-    st = O.quantize_sequence(inp["K"][0][:, :1], inp["V"][0][:, :1], int(inp["seq_len"][0]),
-                             int(inp["n_tail"][0]), w.bits, n_sink_cap=sink)
-    q = inp["q"][0][:w.gqa]
-    times = []
-    t_end = time.perf_counter() + budget_s
-    while time.perf_counter() < t_end or len(times) < 2:
+    held, states = [], []
+    while True:
+        msg = conn.recv()
+        if msg[0] == "stop":
+            conn.close()
+            return
+        if msg[0] == "load":
+            held.append(msg[1:])
+            conn.send(("ok",))
+        elif msg[0] == "quantize":
+            t0 = time.perf_counter()
+            states = [(qh, O.quantize_sequence(k, v, n, nt, bits, n_sink_cap=ns))
+                      for (k, v, qh, n, nt, ns) in held]
+            conn.send((time.perf_counter() - t0,))
+        elif msg[0] == "attend":
+            t0 = time.perf_counter()
+            for qh, st in states:
+                if rope:
+                    O.sequence_attention_rope(qh, st, sm_scale, rope)
+                else:
+                    O.sequence_attention(qh, st, sm_scale)
+            conn.send((time.perf_counter() - t0,))
+
+
+class OraclePool:
+    """n spawned worker processes with single-threaded BLAS (spawn: safe after
+    CUDA has been initialised in this process)."""
+
+    def __init__(self, n, bits, sm_scale, rope):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            self.conns, self.procs = [], []
+            for _ in range(n):
+                a, b = ctx.Pipe()
+                pr = ctx.Process(target=_oracle_worker, args=(b, bits, sm_scale, rope), daemon=True)
+                pr.start()
+                self.conns.append(a)
+                self.procs.append(pr)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def load(self, segs):
+        for i, sg in enumerate(segs):
+            self.conns[i % len(self.conns)].send(("load", *sg))
+        for i, _ in enumerate(segs):
+            self.conns[i % len(self.conns)].recv()
+
+    def phase(self, cmd) -> float:
+        """Wall seconds of one phase run by every worker at once."""
         t0 = time.perf_counter()
-        if rope:
-            O.sequence_attention_rope(q, st, w.sm_scale, rope)
-        else:
-            O.sequence_attention(q, st, w.sm_scale)
-        times.append(time.perf_counter() - t0)
-    per_head = statistics.median(times)
-    return {"value": per_head * w.n_kv_heads * 1e6, "unit": UNIT, "kind": "oracle",
-            "cores": torch.get_num_threads(),
-            "sample": f"1 of {w.n_kv_heads} KV heads ({w.gqa} query heads) over all "
-                      f"{int(inp['seq_len'][0])} tokens, median of {len(times)} runs, "
-                      f"x{w.n_kv_heads}; numpy fp64 (BLAS threads as the host sets them)"}
+        for c in self.conns:
+            c.send((cmd,))
+        for c in self.conns:
+            c.recv()
+        return time.perf_counter() - t0
+
+    def close(self):
+        for c in self.conns:
+            c.send(("stop",))
+        for pr in self.procs:
+            pr.join(timeout=30)
+
+
+def oracle_segments(w, inp, n_sink_cap=0, limit=None):
+    """(K, V, q of the GQA group, length, tail, sink window) of the first `limit`
+    (sequence, KV head) segments, in batch-major order."""
+    out = []
+    G = w.gqa
+    for b in range(w.batch):
+        for h in range(w.n_kv_heads):
+            if limit is not None and len(out) >= limit:
+                return out
+            n = int(inp["seq_len"][b])
+            out.append((np.ascontiguousarray(inp["K"][b, :, h:h + 1]), np.ascontiguousarray(inp["V"][b, :, h:h + 1]),
+                        np.ascontiguousarray(inp["q"][b][h * G:(h + 1) * G]), n, int(inp["n_tail"][b]),
+                        min(n_sink_cap, n)))
+    return out
+
+
+class OracleStep:
+    """The oracle's decode step on this host's cores.  A single-threaded probe of
+    one segment sizes the sample: every segment when a whole step fits the
+    budget, else whole rounds of one segment per core (the time is then scaled
+    to all segments and flagged as extrapolated)."""
+
+    def __init__(self, w, inp, sink=0, rope=0.0, step_budget_s=2.0):
+        self.w, self.rope = w, rope
+        self.S = w.batch * w.n_kv_heads
+        self.cores = os.cpu_count() or 1
+        probe = OraclePool(1, w.bits, w.sm_scale, rope)
+        probe.load(oracle_segments(w, inp, sink, limit=1))
+        self.t_quant1 = probe.phase("quantize")
+        self.t_attn1 = min(probe.phase("attend") for _ in range(2))
+        probe.close()
+        rounds = max(1, int(step_budget_s / max(self.t_attn1, 1e-6)))
+        self.m = min(self.S, self.cores * rounds)
+        self.pool = OraclePool(min(self.cores, self.m), w.bits, w.sm_scale, rope)
+        self.pool.load(oracle_segments(w, inp, sink, limit=self.m))
+        self.t_quant = self.pool.phase("quantize")
+
+    def step_us(self) -> float:
+        """One decode step (attention over the sampled segments on every core),
+        scaled to all segments; microseconds."""
+        return self.pool.phase("attend") * self.S / self.m * 1e6
+
+    def describe(self, values) -> dict:
+        S, m = self.S, self.m
+        what = "all" if m == S else f"{m} of"
+        return {
+            "value": statistics.mean(values), "unit": UNIT, "kind": "oracle", "cores": self.cores,
+            "nproc": self.cores, "threads_per_process": 1,
+            "extrapolated": m < S, "sampled_fraction": m / S,
+            "all_cores": {"attention_us_per_step": statistics.mean(values),
+                          "quantize_ms_per_cache": self.t_quant * S / m * 1e3},
+            "single_thread": {"attention_us_per_step": self.t_attn1 * S * 1e6,
+                              "quantize_ms_per_cache": self.t_quant1 * S * 1e3,
+                              "from": "one segment timed alone, x segments"},
+            "sample": f"oracle fp64 decode attention{' with RoPE' if self.rope else ''} over {what} {S} "
+                      f"(sequence, KV head) segments per step on {min(self.cores, m)} worker processes "
+                      f"(os.cpu_count() = {self.cores}, one BLAS thread each), mean of {len(values)} steps"
+                      + ("" if m == S else f", scaled x{S / m:.2f} to the full step") +
+                      "; quantizer timed once per segment (the prefill of the cache)",
+        }
+
+    def close(self):
+        self.pool.close()
+
+
+def cpu_baseline(w, inp, sink=0, rope=0.0, n_steps=3):
+    """The GPU arm's CPU figure: the same oracle step as the reference arm."""
+    ost = OracleStep(w, inp, sink=sink, rope=rope)
+    try:
+        vals = [ost.step_us() for _ in range(n_steps)]
+        return ost.describe(vals)
+    finally:
+        ost.close()
 
 
 def uniform_config(w, args, n_quant, n_tail, n_sink) -> dict:
@@ -211,10 +351,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from oracle import kvq_oracle as O
     from quantized_kv_cache_11_gb300 import synthetic as S
-    import numpy as np
-    import torch
     if args.workload == "trizone":
         run_reference_trizone(args)
         return
@@ -222,59 +359,34 @@ def run_reference(args):
         run_reference_rdkv(args)
         return
     serving = args.workload == "serving"
-    w = S.SERVING if serving else workload(args.bits)
+    w = S.SERVING if serving else workload(args.bits, args.workload)
     inp = S.generate(w) if serving else with_sink(S.generate(w), args.sink)
     n = int(inp["seq_len"][0])
     nt = int(inp["n_tail"][0])
     n_sink = 0 if serving else min(args.sink, n)
-    st = O.quantize_sequence(inp["K"][0][:, :1], inp["V"][0][:, :1], n, nt, w.bits, n_sink_cap=n_sink)
-    nq = n - nt - n_sink  # quantized tokens of the sampled sequence
-    # per-step budget ~ 150 s / (steps + warmup), slice length a multiple of 32
-    per_step = 150.0 / max(1, args.steps + args.warmup)
-    t0 = time.perf_counter()
-    sl = 1024
-    O.decode_attention(inp["q"][0][:w.gqa],
-                       O.dequantize_keys(st["k_codes"][:, :sl], st["k_scale"][:, :sl // 32],
-                                         st["k_zero"][:, :sl // 32]),
-                       O.dequantize_values(st["v_codes"][:, :sl], st["v_scale"][:, :sl],
-                                           st["v_zero"][:, :sl]), w.sm_scale)
-    t_blk = max(time.perf_counter() - t0, 1e-5)
-    tokens = int(min(nq, max(32, (per_step / t_blk * sl) // 32 * 32)))
-    nblk = nq // tokens
-    q = inp["q"][0][:w.gqa]
+    nq = n - nt - n_sink
+    # per-step budget so the whole run ends in a few minutes
+    ost = OracleStep(w, inp, sink=n_sink, rope=args.rope,
+                     step_budget_s=min(4.0, 150.0 / max(1, args.steps + args.warmup)))
     times = []
     for i in range(args.warmup + args.steps):
-        j = i % max(1, nblk)
-        a, e = j * tokens, (j + 1) * tokens
-        t0 = time.perf_counter()
-        kk = O.dequantize_keys(st["k_codes"][:, a:e], st["k_scale"][:, a // 32:e // 32],
-                               st["k_zero"][:, a // 32:e // 32])
-        if args.rope:  # pre-RoPE keys: rotated to their positions after dequantization
-            kk = O.rope_rotate(kk, np.arange(n_sink + a, n_sink + e), args.rope)
-        vv = O.dequantize_values(st["v_codes"][:, a:e], st["v_scale"][:, a:e], st["v_zero"][:, a:e])
-        O.decode_attention(q, kk, vv, w.sm_scale)
+        t = ost.step_us()
         if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
-    if serving:  # every (sequence, KV head) segment, scaled by its quantized tokens
-        all_q = int((inp["seq_len"] - inp["n_tail"]).sum()) * w.n_kv_heads
-        scale = all_q / tokens
+            times.append(t)
+    cb = ost.describe(times)
+    ost.close()
+    if serving:
         config = serving_config(w, float(inp["seq_len"].mean()))
-        what = f"all {w.batch * w.n_kv_heads} segments ({all_q} quantized tokens; appends not timed)"
     else:
-        scale = w.n_kv_heads * nq / tokens
         config = uniform_config(w, args, nq, nt, n_sink)
-        what = "a full step"
     config.update({"l2": "n/a (host cores)", "launch": "oracle calls on the host"})
-    value = statistics.mean(times) * scale * 1e6
-    sample = (f"oracle dequant{' + RoPE' if args.rope else ''} + fp64 attention on {tokens} of {nq} quantized "
-              f"tokens of 1 of {w.n_kv_heads} KV heads per step, scaled x{scale:.1f} to {what}")
+    value = cb["value"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1000.0,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config,
-        "cpu_baseline": {"kind": "oracle", "cores": torch.get_num_threads(), "sample": sample,
-                         "value": value, "unit": UNIT},
+        "data": "synthetic", "config": config, "extrapolated": cb["extrapolated"],
+        "cpu_baseline": cb,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -327,7 +439,13 @@ def time_graph(launch, n_rep, steps_wanted, world, local):
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
-    reps = max(1, math.ceil(steps_wanted / per_graph))
+    t0 = time.perf_counter()
+    g.replay()
+    torch.cuda.synchronize()
+    t_replay = time.perf_counter() - t0
+    # at least the requested launches, and at least MIN_TIMED_S of timed work so
+    # that the clock sampler sees the GPU under load
+    reps = max(1, math.ceil(steps_wanted / per_graph), math.ceil(MIN_TIMED_S / max(t_replay, 1e-6)))
     steps = reps * per_graph
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -467,7 +585,7 @@ def main():
     dev = torch.device("cuda", local)
     kvq.load_library()
 
-    w = workload(args.bits)
+    w = workload(args.bits, args.workload)
     inp = with_sink(S.generate(w), args.sink)
     n_sink = min(args.sink, int(inp["seq_len"][0]))
     n_quant = int(inp["seq_len"][0] - inp["n_tail"][0]) - n_sink
@@ -562,7 +680,7 @@ def main():
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(w.bits), "data": "synthetic",
         "config": {**uniform_config(w, args, n_quant, n_tail, n_sink),
                    "l2": f"inputs larger than L2: {n_rep} cache replicas "
                          f"({n_rep * probe.nbytes / 1e6:.0f} MB) rotated every step",
@@ -716,7 +834,9 @@ def main_trizone(args):
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int2/int4/int8 codes and fp16 rows x fp16 operands on tensor cores, fp32 accumulate and softmax",
+        "data": "synthetic",
         "config": {"workload": w.name, "batch": B, "n_q_heads": w.n_q_heads, "n_kv_heads": H,
                    "head_dim": w.head_dim, "old_tokens": t_old, "fresh_tokens": nf,
                    "kept_tokens_mean": nb["kept"] / (B * H),
@@ -843,7 +963,7 @@ def main_serving(args):
     line = {
         "metric": METRIC, "value": step_us, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": step_us / 1000.0, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(w.bits), "data": "synthetic",
         "config": {**serving_config(w, float(inp["seq_len"].mean())),
                    "l2": f"inputs larger than L2: {dbytes / 1e6:.0f} MB read per decode",
                    "launch": "CUDA graph of kvq_append_token + kvq_decode_attn"},
@@ -856,6 +976,8 @@ def main_serving(args):
                  "prefill_us": prefill_us, "prefill_gbs": prefill_bytes / (prefill_us * 1e-6) / 1e9,
                  "prefill_bytes": prefill_bytes, "mean_tokens_at_end": float((nq + ntl).mean())},
     }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)  # the decode over the caches as prefilled
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
