@@ -153,3 +153,68 @@ def test_allocation_monotone_in_budget():
 def test_budget_floor():
     assert R.budget_bits(3.0, 65408) == 196224
     assert R.budget_bits(2.5, 3) == 7
+
+
+# ------------------------------------------------------------- the three phases together
+SEGMENT = os.path.join(os.path.dirname(__file__), "golden", "rdkv_segment_example.txt")
+
+
+def _segment_example():
+    rec = {}
+    for line in open(SEGMENT):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, val = (f.strip() for f in line.split("|"))
+        rows = [[float(x) if not x.startswith("0x") else int(x, 16) for x in r.split()] for r in val.split(";")]
+        rec[key] = rows if len(rows) > 1 else rows[0]
+    return rec
+
+
+def test_segment_allocation_hand_example():
+    # phase 2 evicts two tokens; phase 3 must take its statistics over the two
+    # kept tokens only (over all four, the key widths would come out reversed)
+    ex = _segment_example()
+    q = np.array(ex["q_rows"])[:, None, :]        # [T, G = 1, D]
+    k, v = np.array(ex["k_rows"]), np.array(ex["v_rows"])
+    out = R.segment_allocation(q, k, v, 4, 1.0, ex["v_avg_bits"][0], ex["k_avg_bits"][0],
+                               w_tokens=np.array(ex["w_t"]))
+    assert out["sigma_t"].tolist() == ex["sigma_t"]
+    assert out["v_width"].tolist() == [int(x) for x in ex["v_width"]]
+    assert out["kept"].tolist() == [True, True, False, False]
+    np.testing.assert_allclose(out["w_c"], ex["w_c"], rtol=1e-15, atol=1e-15)
+    assert out["sigma_c"].tolist() == ex["sigma_c"]
+    assert out["k_width"].tolist() == [int(x) for x in ex["k_width"]]
+    # the multipliers of the hand derivation
+    assert R.allocate(out["W_t"], R.V_WIDTHS, 4)[1] == ex["v_lam_bits"][0]
+    assert R.allocate(out["W_c"], R.K_WIDTHS, 10)[1] == ex["k_lam_bits"][0]
+    # the statistics over all tokens give the reversed key widths (the example
+    # separates the two readings)
+    W_all = (R.channel_weights(q, k) * R.variance(k, axis=0)).astype(np.float32)
+    assert R.allocate(W_all, R.K_WIDTHS, 10)[0].tolist() == [int(x) for x in ex["k_width_all_tokens"]]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_segment_allocation_is_the_phases_in_order(seed):
+    # phase 1 (token weights over the prompt) -> phase 2 (value widths of the old
+    # tokens within floor(v_bits * t_old)) -> phase 3 (channel weights and
+    # variances over the kept old tokens, key widths within floor(k_bits * D)),
+    # each step called separately
+    rng = np.random.default_rng(100 + seed)
+    T, G, D, t_old = 48, 2, 8, 40
+    q = rng.standard_normal((T, G, D))
+    k = rng.standard_normal((T, D)) * np.array([1, 1, 6, 1, 1, 1, 3, 1])
+    v = rng.standard_normal((T, D)) * np.exp(rng.standard_normal((T, 1)))
+    vb, kb = 2.5, 4.0
+    out = R.segment_allocation(q, k, v, t_old, 0.35, vb, kb)
+    w = R.token_weights(q, k, 0.35)[:t_old]
+    Wt = (w * R.variance(v[:t_old], axis=1)).astype(np.float32)
+    vw, _ = R.allocate(Wt, R.V_WIDTHS, R.budget_bits(vb, t_old))
+    kept = k[:t_old][vw != 0]
+    Wc = (R.channel_weights(q, kept) * R.variance(kept, axis=0)).astype(np.float32)
+    kw, _ = R.allocate(Wc, R.K_WIDTHS, R.budget_bits(kb, D))
+    assert out["v_width"].tolist() == vw.tolist() and out["k_width"].tolist() == kw.tolist()
+    # budgets: the value bits fit floor(2.5 * 40) = 100; the key bits fit floor(4 * 8) = 32
+    assert int(out["v_width"].astype(int).sum()) <= 100
+    assert int(out["k_width"].astype(int).sum()) <= 32
+    assert 0 < out["kept"].sum() < t_old  # the budget evicts some tokens and keeps others
