@@ -321,6 +321,19 @@ kvq_status kvq_decode_attn_rope(const kvq_cache* cache, int32_t n_q_heads, const
                                 float sm_scale, const float* table, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/*
+ * kvq_selftest_bounded_wait -- checks, on the current device, the bounded wait
+ * that the kernels use for staged data.  One CTA of two warps waits on a
+ * shared-memory mbarrier that expects one arrival, polling at most max_polls
+ * times.  With arrive != 0 a thread arrives first and the wait completes; with
+ * arrive == 0 nothing arrives, the wait gives up, KVQ_DEVERR_TIMEOUT is OR-ed
+ * into *error_flags (device int32) and the kernel returns normally (no copy is
+ * in flight, the context stays usable).  There is no counterpart in the pages:
+ * it is a diagnostic of the library's own failure path.  KVQ_ERR_INVALID for a
+ * NULL or misaligned error_flags or max_polls == 0.
+ */
+kvq_status kvq_selftest_bounded_wait(int32_t* error_flags, uint32_t max_polls, int32_t arrive, void* stream);
+
 /* Human-readable name of a status code.  Never NULL. */
 const char* kvq_status_string(int status);
 

@@ -53,7 +53,17 @@ struct DecodeCfg {
   static constexpr int KMETA = 4 * D;  // [2][D] halves
   static constexpr int VMETA = 4 * D;  // [2][D/32][32] halves
   static constexpr int BASE = ROPE ? D / 2 * 8 : 0;  // cos/sin of the group's first position block
-  static constexpr int STAGE = 2 * TB + KMETA + VMETA + BASE;
+  // groups per stage: two consecutive groups of a segment are staged and decoded
+  // together at 2 bits (one wait, one set of copies and one softmax maximum per
+  // 64 tokens, and one zero-point product serves both groups)
+  static constexpr int GPI = (BITS == 2 && !ROPE) ? 2 : 1;
+  // stage layout: the key codes of its GPI groups, their value codes, their key
+  // metadata, their value metadata (each array as consecutive groups, as in the
+  // cache, so that one bulk copy per array fills it), then (ROPE) the cos/sin row
+  static constexpr int STAGE1 = 2 * TB + KMETA + VMETA + BASE;  // bytes of one group
+  static constexpr int STAGE = GPI * (2 * TB + KMETA + VMETA) + BASE;
+  static constexpr int OFF_VC = GPI * TB, OFF_KM = 2 * GPI * TB, OFF_VM = 2 * GPI * TB + GPI * KMETA,
+                       OFF_BASE = GPI * (2 * TB + KMETA + VMETA);
   static constexpr int NT = (2 * G + 7) / 8;  // 8-column n-tiles: column 2g = hi, 2g+1 = lo
   static constexpr int KT = D / 16;
   static constexpr int NWL = T::kWordsPerLane;
@@ -61,8 +71,10 @@ struct DecodeCfg {
   // one CTA of 16 warps per SM for 2- and 4-bit codes: fewer, larger CTAs leave
   // fewer split-K partials per (sequence, KV head) for the last CTA to merge
   // (12 at 4 bits with ROPE: its stage ring, offset table and fp32 q must fit)
-  static constexpr int WARPS = BITS == 8 ? 4 : (ROPE && BITS == 4 ? 12 : 16);
-  static constexpr int NSTAGE = BITS == 2 ? (ROPE ? 3 : 4) : (BITS == 4 ? 2 : 3);
+  static constexpr int WARPS = BITS == 8 ? 4 : ((ROPE && BITS == 4) || GPI == 2 ? 12 : 16);
+  static constexpr int NSTAGE = BITS == 2 ? (ROPE ? 3 : 2) : (BITS == 4 ? 2 : 3);
+  // q pairs held in registers (one n-tile) instead of re-read from shared memory
+  static constexpr bool QREG = NT == 1 && GPI == 2;
   static constexpr int MIN_CTAS = 1;
   static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
   static constexpr int RING = WARPS * NSTAGE * STAGE;
@@ -185,6 +197,7 @@ struct Decoder {
   float o[KT][NT][4];  // P.V accumulators: rows = channels, columns (head, hi|lo)
   float zc[NT][4];     // value-constant MMA: zero points, scale sums, row 12 = sum p~
   const uint32_t* qs;      // q pairs of column 8nt+gid (head 4nt + gid/2) in shared memory
+  uint4 qr[C::QREG ? KT / 2 : 1];  // QREG: the same pairs in registers, k-tiles (kt, kt + 1) per entry
   uint32_t nhl;            // half2(-hl): 0 for the hi column, -1 for the lo column
   uint32_t ones_a;         // the ones row (row 12) of the value-constant MMA: lanes gid 4
   int lane, gid, tig, hl;
@@ -200,6 +213,10 @@ struct Decoder {
     nhl = hl ? 0xBC00BC00u : 0u;
     ones_a = gid == 4 ? kOnes : 0u;
     qs = q_smem + (gid >> 1) * (D / 2) + 4 * tig;
+    if constexpr (C::QREG) {
+#pragma unroll
+      for (int k2 = 0; k2 < KT / 2; ++k2) qr[k2] = *reinterpret_cast<const uint4*>(qs + 16 * k2);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m[nt] = -INFINITY;
@@ -269,6 +286,7 @@ struct Decoder {
 
   // q pairs (kt, r) and (kt + 1, r) of this lane's column in n-tile nt (kt even)
   __device__ __forceinline__ uint4 qpairs(int nt, int kt) const {
+    if constexpr (C::QREG) return qr[kt / 2];
     return *reinterpret_cast<const uint4*>(qs + nt * 4 * (D / 2) + 8 * kt);
   }
 
@@ -308,6 +326,24 @@ struct Decoder {
     return h2_as_u32(__hfma2(x, y, __hmul2_rn(hi, u32_as_h2(nhl))));
   }
 
+  // Move the running maximum of every head to max(m, mloc) and rescale the
+  // accumulators to it (called only when some head's chunk maximum passed its
+  // running maximum by more than kLazyRescale).
+  __device__ __forceinline__ void rescale(const float (&mloc)[NT]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float mnew = fmaxf(m[nt], mloc[nt]);
+      const float alpha = (mnew == m[nt]) ? 1.f : fast_exp2(m[nt] - mnew);
+      m[nt] = mnew;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) zc[nt][i] *= alpha;
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[kt][nt][i] *= alpha;
+    }
+  }
+
   // Online softmax over one 32-token chunk.  lg[nt][mt][r]: log2-domain logits of
   // token 16mt + gid + 8r for head 4nt + tig.  Writes p~ (fp16) to ps[g][t].
   __device__ __forceinline__ void softmax(float (&lg)[NT][2][2], __half* ps) {
@@ -322,20 +358,7 @@ struct Decoder {
       mloc[nt] = mx;
       need |= mx > m[nt] + kLazyRescale;
     }
-    if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float mnew = fmaxf(m[nt], mloc[nt]);
-        const float alpha = (mnew == m[nt]) ? 1.f : fast_exp2(m[nt] - mnew);
-        m[nt] = mnew;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) zc[nt][i] *= alpha;
-#pragma unroll
-        for (int kt = 0; kt < KT; ++kt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) o[kt][nt][i] *= alpha;
-      }
-    }
+    if (__any_sync(0xffffffffu, need)) rescale(mloc);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + tig;
@@ -366,12 +389,74 @@ struct Decoder {
     }
   }
 
-  // One quantized 32-token group staged in shared memory.  zrow: a zero row of
-  // at least D/2 words in shared memory.
-  // roff (ROPE): the group's first position modulo 32.
-  __device__ __forceinline__ void quant_group(const uint8_t* stage, __half* ps, const uint32_t* zrow,
-                                              float scale_log2, int roff = 0) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(stage);
+  // P.V of one staged group (value codes vc, value metadata vm) with the B
+  // fragments pp of its p~ (column 8nt+gid, tokens 16kt + 2tig + 8r, +1), into o
+  // and zc.  At 2 bits the codes of tokens 16..31 sit 4 bits above those of
+  // tokens 0..15 of the same row (pos(1, r) = pos(0, r) + 4): their p~ is divided
+  // by 16 (exactly, a power of two) so that both k-tiles share a unit.
+  __device__ __forceinline__ void pv_group(const uint8_t* vc, const uint8_t* vm8, const uint32_t (&pp)[NT][2][2],
+                                           const uint32_t* zrow) {
+    uint32_t pv[NT][2][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        pv[nt][0][r] = pp[nt][0][r];
+        pv[nt][1][r] = BITS == 2 ? h2_as_u32(__hmul2(u32_as_h2(pp[nt][1][r]), u32_as_h2(kSixteenth))) : pp[nt][1][r];
+      }
+    const uint4* v4 = reinterpret_cast<const uint4*>(vc);
+    uint32_t vw[C::NWL];
+#pragma unroll
+    for (int ch = 0; ch < C::NWL / 4; ++ch) {
+      const uint4 v = v4[ch * 32 + lane];
+      vw[4 * ch] = v.x; vw[4 * ch + 1] = v.y; vw[4 * ch + 2] = v.z; vw[4 * ch + 3] = v.w;
+    }
+    // value metadata, lane order: pair (j, kt, r) of this lane at 16j + 4tig + 2kt + r
+    const uint32_t* vm = reinterpret_cast<const uint32_t*>(vm8);
+    const uint32_t* vsl = vm + 4 * tig;          // scale pairs
+    const uint32_t* vzl = vm + D / 2 + 4 * tig;  // zero pairs
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const uint4 sv = *reinterpret_cast<const uint4*>(vsl + 16 * j);
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        const uint32_t vs0 = kt ? sv.z : sv.x, vs1 = kt ? sv.w : sv.y;
+        uint32_t b[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          b[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][0]), u32_as_h2(vs0)));
+          b[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][1]), u32_as_h2(vs1)));
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+          const int mt = 2 * j + mi;
+          uint32_t a8[8];
+          unpack8(vw, mt * 8, a8);  // pairs of (mt, kt = 0) then (mt, kt = 1)
+          const uint32_t a[4] = {a8[4 * kt], a8[4 * kt + 1], a8[4 * kt + 2], a8[4 * kt + 3]};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, b[nt][0], b[nt][1]);
+        }
+      }
+    }
+    // constant-MMA rows (tokens 16kt + 2tig (+8r)): 0..D/32-1 = zero points of group
+    // j; 12 = ones (the softmax denominator); B = p~ as rounded
+    const uint4 v0 = *reinterpret_cast<const uint4*>(gid < D / 32 ? vzl + 16 * gid : zrow);
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v0.w : v0.y, ones_a};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
+    }
+  }
+
+  // One quantized 32-token group staged in shared memory: key codes kc, value
+  // codes vc, key metadata km8, value metadata vm8 (and, ROPE, the cos/sin row
+  // base of its position block).  zrow: a zero row of at least D/2 words in
+  // shared memory.  roff (ROPE): the group's first position modulo 32.
+  __device__ __forceinline__ void quant_group(const uint8_t* kc, const uint8_t* vc, const uint8_t* km8,
+                                              const uint8_t* vm8, const uint8_t* base, __half* ps,
+                                              const uint32_t* zrow, float scale_log2, int roff = 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(kc);
     uint32_t kw[C::NWL];
 #pragma unroll
     for (int ch = 0; ch < C::NWL / 4; ++ch) {
@@ -380,7 +465,7 @@ struct Decoder {
     }
     // key metadata, lane order: word 16kt + 4tig + 2r + f = the zero points (f = 0) or
     // scales (f = 1) of channels 16kt + 2tig + 8r and +1
-    const uint32_t* km = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB);
+    const uint32_t* km = reinterpret_cast<const uint32_t*>(km8);
     float lg[NT][2][2];
     if constexpr (ROPE) {
       // the codes dequantized in fp32: pair P = 8kt + 4mt + (r + 2h) of word P / PPW
@@ -398,8 +483,7 @@ struct Decoder {
           k[m2] = make_float2(fmaf(sc.x, x0, zp.x), fmaf(sc.y, x1, zp.y));
         }
       };
-      rope_logits(keys, reinterpret_cast<const float2*>(stage + 2 * C::TB + C::KMETA + C::VMETA), roff,
-                  scale_log2, lg);
+      rope_logits(keys, reinterpret_cast<const float2*>(base), roff, scale_log2, lg);
     } else {
       // one 16-byte load per k-tile, (zero r0, scale r0, zero r1, scale r1), is the
       // constant product's A quad: rows gid hold the zero points (every row alike,
@@ -476,59 +560,115 @@ struct Decoder {
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
     load_pp(ps, pp);
-    // ---- P.V.  At 2 bits the codes of tokens 16..31 sit 4 bits above those of
-    // tokens 0..15 of the same row (pos(1, r) = pos(0, r) + 4): their p~ is
-    // divided by 16 (exactly, a power of two) so that both k-tiles share a unit.
-    uint32_t pv[NT][2][2];
+    pv_group(vc, vm8, pp, zrow);
+    __syncwarp();
+  }
+
+  // Two consecutive quantized groups staged together (stage layout of DecodeCfg:
+  // GPI = 2), decoded as one 64-token chunk: one softmax maximum, one zero-point
+  // product per k-tile for both groups (rows gid: the first group's zero points,
+  // rows gid + 8: the second's), and the p~ of both turned into P.V operands in
+  // registers (movmatrix), without a shared-memory round trip.
+  __device__ __forceinline__ void quant_pair(const uint8_t* stage, const uint32_t* zrow, float scale_log2) {
+    static_assert(C::GPI == 2 && !ROPE, "two-group stages");
+    float lg[2][NT][2][2];
+    {
+      float sacc[2][2][NT][4];  // [group][mt]
+      float cacc[NT][4];        // rows gid: q.z of the first group, rows gid + 8: of the second
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        pv[nt][0][r] = pp[nt][0][r];
-        pv[nt][1][r] = BITS == 2 ? h2_as_u32(__hmul2(u32_as_h2(pp[nt][1][r]), u32_as_h2(kSixteenth))) : pp[nt][1][r];
-      }
-    uint32_t vw[C::NWL];
-#pragma unroll
-    for (int ch = 0; ch < C::NWL / 4; ++ch) {
-      const uint4 v = s4[(C::TB / 16) + ch * 32 + lane];
-      vw[4 * ch] = v.x; vw[4 * ch + 1] = v.y; vw[4 * ch + 2] = v.z; vw[4 * ch + 3] = v.w;
-    }
-    // value metadata, lane order: pair (j, kt, r) of this lane at 16j + 4tig + 2kt + r
-    const uint32_t* vm = reinterpret_cast<const uint32_t*>(stage + 2 * C::TB + C::KMETA);
-    const uint32_t* vsl = vm + 4 * tig;          // scale pairs
-    const uint32_t* vzl = vm + D / 2 + 4 * tig;  // zero pairs
-#pragma unroll
-    for (int j = 0; j < D / 32; ++j) {
-      const uint4 sv = *reinterpret_cast<const uint4*>(vsl + 16 * j);
-#pragma unroll
-      for (int kt = 0; kt < 2; ++kt) {
-        const uint32_t vs0 = kt ? sv.z : sv.x, vs1 = kt ? sv.w : sv.y;
-        uint32_t b[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          b[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][0]), u32_as_h2(vs0)));
-          b[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][1]), u32_as_h2(vs1)));
+        for (int i = 0; i < 4; ++i) {
+          sacc[0][0][nt][i] = sacc[0][1][nt][i] = sacc[1][0][nt][i] = sacc[1][1][nt][i] = 0.f;
+          cacc[nt][i] = 0.f;
         }
+      // the key side of each group in turn (fewer live registers than both at
+      // once); the zero-point product of both groups runs with the second
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-          const int mt = 2 * j + mi;
-          uint32_t a8[8];
-          unpack8(vw, mt * 8, a8);  // pairs of (mt, kt = 0) then (mt, kt = 1)
-          const uint32_t a[4] = {a8[4 * kt], a8[4 * kt + 1], a8[4 * kt + 2], a8[4 * kt + 3]};
+      for (int x = 0; x < 2; ++x) {
+        const uint4* k4 = reinterpret_cast<const uint4*>(stage + x * C::TB);
+        const uint32_t* kmt = reinterpret_cast<const uint32_t*>(stage + C::OFF_KM + x * C::KMETA) + 4 * tig;
+        const uint32_t* kmo = reinterpret_cast<const uint32_t*>(stage + C::OFF_KM) + 4 * tig;  // first group's
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816(o[mt][nt], a, b[nt][0], b[nt][1]);
+        for (int kt4 = 0; kt4 < KT; kt4 += 4) {
+          // the lane's code words of k-tiles kt4 .. kt4 + 3 (one word per k-tile at 2 bits)
+          const uint4 v = k4[(kt4 / 4) * 32 + lane];
+          const uint32_t kw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int kt = kt4 + kk;
+            const uint4 mv = *reinterpret_cast<const uint4*>(kmt + 16 * kt);
+            uint32_t a[8];
+            unpack8(kw, kk * 8, a);
+            const uint32_t a0[4] = {a[0], a[1], a[2], a[3]};
+            const uint32_t a1[4] = {a[4], a[5], a[6], a[7]};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint4 qv = qpairs(nt, kt & ~1);
+              const uint32_t q0 = (kt & 1) ? qv.z : qv.x, q1 = (kt & 1) ? qv.w : qv.y;
+              const uint32_t b0 = split_mul(q0, mv.y);
+              const uint32_t b1 = split_mul(q1, mv.w);
+              mma_16816(sacc[x][0][nt], a0, b0, b1);
+              mma_16816(sacc[x][1][nt], a1, b0, b1);
+              if (x == 1) {
+                const uint2 z0 = make_uint2(kmo[16 * kt], kmo[16 * kt + 2]);
+                const uint32_t ac[4] = {z0.x, mv.x, z0.y, mv.z};
+                mma_16816(cacc[nt], ac, q0, q1);
+              }
+            }
+          }
         }
       }
-    }
-    // constant-MMA rows (tokens 16kt + 2tig (+8r)): 0..D/32-1 = zero points of group
-    // j; 12 = ones (the softmax denominator); B = p~ as rounded
-    const uint4 v0 = *reinterpret_cast<const uint4*>(gid < D / 32 ? vzl + 16 * gid : zrow);
 #pragma unroll
-    for (int kt = 0; kt < 2; ++kt) {
-      const uint32_t ac[4] = {kt ? v0.z : v0.x, ones_a, kt ? v0.w : v0.y, ones_a};
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_16816(zc[nt], ac, pp[nt][kt][0], pp[nt][kt][1]);
+        for (int x = 0; x < 2; ++x) {
+          const float zq = cacc[nt][2 * x] * scale_log2;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+              lg[x][nt][mt][r] =
+                  fmaf(sacc[x][mt][nt][2 * r] + sacc[x][mt][nt][2 * r + 1], scale_log2 * unit(mt, r), zq);
+        }
     }
+    // online softmax over the 64 tokens
+    bool need = false;
+    float mloc[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        mx = fmaxf(mx, fmaxf(fmaxf(lg[x][nt][0][0], lg[x][nt][0][1]), fmaxf(lg[x][nt][1][0], lg[x][nt][1][1])));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      mloc[nt] = mx;
+      need |= mx > m[nt] + kLazyRescale;
+    }
+    if (__any_sync(0xffffffffu, need)) rescale(mloc);
+    // p~ to the P.V B fragments: lane (gid, tig) holds p~ of head 4nt + tig at
+    // tokens 16mt + gid + 8r, i.e. the pair of columns (2tig, 2tig + 1) = (p~, 0)
+    // of row gid of the 8 x 8 matrices [tokens 16mt + 8r + (0..7)] x [columns];
+    // transposed in registers, lane (gid, tig) holds column gid (head gid/2's p~,
+    // or zeros for odd gid) at tokens 2tig, 2tig + 1: the B fragment of P.V.
+    uint32_t pp[2][NT][2][2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            float pf = fast_exp2(lg[x][nt][mt][r] - m[nt]);
+            if (G % 4 != 0 && 4 * nt + tig >= G) pf = 0.f;
+            pp[x][nt][mt][r] = movmatrix_trans(h2_as_u32(__floats2half2_rn(pf, 0.f)));
+          }
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      pv_group(stage + C::OFF_VC + x * C::TB, stage + C::OFF_VM + x * C::VMETA, pp[x], zrow);
     __syncwarp();
   }
 
@@ -693,6 +833,7 @@ __device__ bool final_merge(const float* parts, int nparts, float* out, uint8_t*
     __syncthreads();  // the ring (and s_w) are free
     if (tid == 0) {
       const uint32_t bytes = (uint32_t)(nb * G * PS * 4);
+      fence_proxy_async_global();  // the partials were written by other CTAs' ordinary stores
       fence_proxy_async();
       mbar_arrive_expect_tx(bar, bytes);
       tma_load_1d(ring, parts + (size_t)first * G * PS, bytes, bar);
@@ -816,29 +957,33 @@ decode_kernel(const DecodeParams p) {
     {
       const int ga = ia, cnt = failed ? 0 : max(0, min(ie, ng) - ia);
       const size_t g0 = (size_t)seg * p.max_groups + ga;
-      // one lane issues four bulk copies per group, completing on the stage's mbarrier
-      auto issue = [&](int idx, int slotn) {
+      const int nst = (cnt + C::GPI - 1) / C::GPI;  // stages of up to GPI consecutive groups
+      // one lane issues four bulk copies per stage (codes, values, key and value
+      // metadata of its groups, each contiguous in the cache), completing on the
+      // stage's mbarrier
+      auto issue = [&](int si, int slotn) {
         if (lane == 0) {
-          const size_t g = g0 + idx;
+          const int gi = si * C::GPI, n_in = min(C::GPI, cnt - gi);
+          const size_t g = g0 + gi;
           uint8_t* dst = wring + slotn * C::STAGE;
           fence_proxy_async();
-          mbar_arrive_expect_tx(bars + slotn, C::STAGE);
-          tma_load_1d(dst, p.k_codes + g * C::TB, C::TB, bars + slotn);
-          tma_load_1d(dst + C::TB, p.v_codes + g * C::TB, C::TB, bars + slotn);
-          tma_load_1d(dst + 2 * C::TB, reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA, C::KMETA,
-                      bars + slotn);
-          tma_load_1d(dst + 2 * C::TB + C::KMETA, reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA,
-                      C::VMETA, bars + slotn);
+          mbar_arrive_expect_tx(bars + slotn, n_in * C::STAGE1);
+          tma_load_1d(dst, p.k_codes + g * C::TB, n_in * C::TB, bars + slotn);
+          tma_load_1d(dst + C::OFF_VC, p.v_codes + g * C::TB, n_in * C::TB, bars + slotn);
+          tma_load_1d(dst + C::OFF_KM, reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA,
+                      n_in * C::KMETA, bars + slotn);
+          tma_load_1d(dst + C::OFF_VM, reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA,
+                      n_in * C::VMETA, bars + slotn);
           if constexpr (ROPE)  // cos/sin of the group's position block: 32 (group + sinks / 32)
-            tma_load_1d(dst + 2 * C::TB + C::KMETA + C::VMETA,
-                        p.rope + (size_t)(64 + ga + idx + (L.ns >> 5)) * (D / 2), C::BASE, bars + slotn);
+            tma_load_1d(dst + C::OFF_BASE, p.rope + (size_t)(64 + ga + gi + (L.ns >> 5)) * (D / 2), C::BASE,
+                        bars + slotn);
         }
       };
       // start the first copies, then stage this segment's q (lane order) while they fly
       int issued = 0, waited = 0;
 #pragma unroll
       for (int st = 0; st < C::NSTAGE - 1; ++st)
-        if (st < cnt) { issue(st, st); ++issued; }
+        if (st < nst) { issue(st, st); ++issued; }
       {
         const __half* qh = p.q + ((size_t)b * p.hkv + h) * G * D;
         for (int e = threadIdx.x; e < NTILES * 4 * (D / 2); e += blockDim.x) {
@@ -855,14 +1000,22 @@ decode_kernel(const DecodeParams p) {
       dec.init(q_smem);
       dec.qf = qf_s;
       dec.intra = intra_s;
-      for (int i = 0; i < cnt; ++i) {
-        if (i + C::NSTAGE - 1 < cnt) { issue(i + C::NSTAGE - 1, (i + C::NSTAGE - 1) % C::NSTAGE); ++issued; }
+      for (int i = 0; i < nst; ++i) {
+        if (i + C::NSTAGE - 1 < nst) { issue(i + C::NSTAGE - 1, (i + C::NSTAGE - 1) % C::NSTAGE); ++issued; }
         const int slotn = i % C::NSTAGE;
         const bool ok = mbar_wait(bars + slotn, (parity >> slotn) & 1u, kMaxPolls);
         parity ^= 1u << slotn;
         ++waited;
         if (!ok) { failed = true; break; }
-        dec.quant_group(wring + slotn * C::STAGE, ps, zrow, p.scale_log2, L.ns & 31);
+        const uint8_t* st = wring + slotn * C::STAGE;
+        if constexpr (C::GPI == 2) {
+          if (cnt - i * C::GPI >= 2) {
+            dec.quant_pair(st, zrow, p.scale_log2);
+            continue;
+          }
+        }
+        dec.quant_group(st, st + C::OFF_VC, st + C::OFF_KM, st + C::OFF_VM, st + C::OFF_BASE, ps, zrow,
+                        p.scale_log2, L.ns & 31);
       }
       // after a timeout, wait (bounded) for this warp's copies still in flight
       for (; waited < issued; ++waited) {
@@ -918,14 +1071,15 @@ decode_kernel(const DecodeParams p) {
       slot[g * C::PSTRIDE + 4 + d] = osum;
       if (d == 0) { slot[g * C::PSTRIDE] = mx; slot[g * C::PSTRIDE + 1] = lsum; }
     }
-    __threadfence();
     __syncthreads();
     const int64_t c0 = cta_of(seg_first + (int64_t)h * items, total, nstream);
     const int nparts = (int)(cta_of(seg_first + (int64_t)(h + 1) * items - 1, total, nstream) - c0 + 1);
-    if (threadIdx.x == 0) s_last = atomicAdd(&p.counters[seg], 1) == nparts - 1;
+    // one acquire-release add publishes the CTA's partial (the barrier above
+    // orders every thread's writes before it) and, for the last arrival, makes
+    // the other CTAs' partials visible (the barrier below passes that on)
+    if (threadIdx.x == 0) s_last = atomic_add_acq_rel(&p.counters[seg], 1) == nparts - 1;
     __syncthreads();
     if (s_last) {
-      __threadfence();
       // the stage ring is idle here; the p~ area holds the merge weights
       const bool ok = final_merge<D, BITS, G, ROPE>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
                                                p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D, ring,

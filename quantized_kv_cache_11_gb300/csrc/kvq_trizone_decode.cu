@@ -542,6 +542,7 @@ __device__ bool final_merge(const float* parts, int nparts, float* out, uint8_t*
     __syncthreads();
     if (tid == 0) {
       const uint32_t bytes = (uint32_t)(nb * G * PS * 4);
+      fence_proxy_async_global();  // the partials were written by other CTAs' ordinary stores
       fence_proxy_async();
       mbar_arrive_expect_tx(bar, bytes);
       tma_load_1d(ring, parts + (size_t)first * G * PS, bytes, bar);
@@ -791,14 +792,15 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
       slotp[g * C::PSTRIDE + 4 + d] = osum;
       if (d == 0) { slotp[g * C::PSTRIDE] = mx; slotp[g * C::PSTRIDE + 1] = lsum; }
     }
-    __threadfence();
     __syncthreads();
     const int64_t c0 = cta_of(S, total, nstream);
     const int nparts = (int)(cta_of(S + W - 1, total, nstream) - c0 + 1);
-    if (tid == 0) s_last = atomicAdd(&p.counters[s], 1) == nparts - 1;
+    // one acquire-release add publishes the CTA's partial (the barrier above
+    // orders every thread's writes before it) and, for the last arrival, makes
+    // the other CTAs' partials visible (the barrier below passes that on)
+    if (tid == 0) s_last = atomic_add_acq_rel(&p.counters[s], 1) == nparts - 1;
     __syncthreads();
     if (s_last) {
-      __threadfence();
       const bool ok = final_merge<G>(p.part + (size_t)(c0 + s) * G * C::PSTRIDE, nparts, p.out + (size_t)s * G * kDim,
                                      rings, reinterpret_cast<float*>(ps_all), merge_bar, merge_parity, s_M, s_L,
                                      s_scale);

@@ -47,7 +47,7 @@ EXPORTS = ("kvq_cache_bytes", "kvq_quantize_prefill", "kvq_append_token",
            "kvq_status_string", "kvq_version", "kvq_trizone_bytes", "kvq_trizone_build",
            "kvq_trizone_decode_workspace_bytes", "kvq_trizone_decode_attn",
            "kvq_rdkv_workspace_bytes", "kvq_rdkv_token_weights", "kvq_rdkv_allocate",
-           "kvq_rope_table_bytes", "kvq_rope_table", "kvq_decode_attn_rope")
+           "kvq_rope_table_bytes", "kvq_rope_table", "kvq_decode_attn_rope", "kvq_selftest_bounded_wait")
 KVQ_STATIC_SCRATCH_BYTES = 4 << 20
 
 
@@ -134,6 +134,7 @@ def load_library() -> ctypes.CDLL:
     lib.kvq_rope_table_bytes.argtypes = [cache_p, P(c_sz)]
     lib.kvq_rope_table.argtypes = [cache_p, c_f, c_vp, c_vp]
     lib.kvq_decode_attn_rope.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_vp, c_sz, c_vp]
+    lib.kvq_selftest_bounded_wait.argtypes = [c_vp, ctypes.c_uint32, ctypes.c_int32, c_vp]
     tz_p = P(kvq_trizone)
     lib.kvq_trizone_bytes.argtypes = [tz_p, P(c_sz)]
     lib.kvq_trizone_build.argtypes = [tz_p, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_vp,
@@ -157,7 +158,8 @@ def load_library() -> ctypes.CDLL:
                  "kvq_decode_workspace_bytes", "kvq_decode_attn", "kvq_decode_attn_static",
                  "kvq_trizone_bytes", "kvq_trizone_build", "kvq_trizone_decode_workspace_bytes",
                  "kvq_trizone_decode_attn", "kvq_rdkv_workspace_bytes", "kvq_rdkv_token_weights",
-                 "kvq_rdkv_allocate", "kvq_rope_table_bytes", "kvq_rope_table", "kvq_decode_attn_rope"):
+                 "kvq_rdkv_allocate", "kvq_rope_table_bytes", "kvq_rope_table", "kvq_decode_attn_rope",
+                 "kvq_selftest_bounded_wait"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -311,6 +313,13 @@ def kvq_decode_attn_rope(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.
                                              float(sm_scale), _ptr(table), _ptr(workspace), workspace.numel(),
                                              _stream(stream))
     _check("kvq_decode_attn_rope", st)
+
+
+def kvq_selftest_bounded_wait(error_flags: torch.Tensor, max_polls: int, arrive: bool, stream=None) -> None:
+    """error_flags: int32 device tensor (one element used)."""
+    _need(error_flags, torch.int32, "error_flags")
+    _check("kvq_selftest_bounded_wait", load_library().kvq_selftest_bounded_wait(
+        _ptr(error_flags), int(max_polls), int(bool(arrive)), _stream(stream)))
 
 
 class QuantizedKVCache:

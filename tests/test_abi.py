@@ -266,3 +266,9 @@ def test_rope_table_bytes_and_validation(lib):
     assert lib.kvq_rope_table_bytes(ctypes.byref(d64), ctypes.byref(out)) == kvq.KVQ_ERR_UNSUPPORTED
     assert lib.kvq_rope_table(ctypes.byref(d), ctypes.c_float(1.0), 0x100000, None) == kvq.KVQ_ERR_INVALID
     assert lib.kvq_rope_table(ctypes.byref(d), ctypes.c_float(10000.0), 0x100008, None) == kvq.KVQ_ERR_INVALID
+
+
+def test_selftest_validation_fails_before_launch(lib):
+    assert lib.kvq_selftest_bounded_wait(None, 16, 0, None) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_selftest_bounded_wait(0x1002, 16, 0, None) == kvq.KVQ_ERR_INVALID  # misaligned
+    assert lib.kvq_selftest_bounded_wait(0x1000, 0, 0, None) == kvq.KVQ_ERR_INVALID   # no polls

@@ -190,3 +190,21 @@ def test_decode_reports_bad_device_lengths():
     out = cache.decode(q, w.sm_scale)
     assert cache.device_errors() & kvq.KVQ_DEVERR_BAD_LENGTHS
     assert torch.isfinite(out).all()
+
+
+def test_bounded_wait_gives_up_and_reports():
+    # the mbarrier wait of every staging loop: with nothing arriving it must end
+    # after its poll limit, set KVQ_DEVERR_TIMEOUT and leave the context usable
+    import time
+    flags = torch.zeros(4, dtype=torch.int32, device="cuda")
+    kvq.kvq_selftest_bounded_wait(flags, 1 << 20, arrive=True)
+    torch.cuda.synchronize()
+    assert int(flags[0]) == 0  # satisfied wait: no error
+    t0 = time.perf_counter()
+    kvq.kvq_selftest_bounded_wait(flags, 4096, arrive=False)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 5.0
+    assert int(flags[0]) == kvq.KVQ_DEVERR_TIMEOUT
+    # the context still works
+    x = torch.arange(8, device="cuda", dtype=torch.float32)
+    assert float(x.sum()) == 28.0
