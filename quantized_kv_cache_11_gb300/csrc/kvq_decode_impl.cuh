@@ -71,10 +71,10 @@ struct DecodeCfg {
   // one CTA of 16 warps per SM for 2- and 4-bit codes: fewer, larger CTAs leave
   // fewer split-K partials per (sequence, KV head) for the last CTA to merge
   // (12 at 4 bits with ROPE: its stage ring, offset table and fp32 q must fit)
-  static constexpr int WARPS = BITS == 8 ? 4 : ((ROPE && BITS == 4) || GPI == 2 ? 12 : 16);
+  static constexpr int WARPS = BITS == 8 ? 4 : (ROPE && BITS == 4 ? 12 : 16);
   static constexpr int NSTAGE = BITS == 2 ? (ROPE ? 3 : 2) : (BITS == 4 ? 2 : 3);
   // q pairs held in registers (one n-tile) instead of re-read from shared memory
-  static constexpr bool QREG = NT == 1 && GPI == 2;
+  static constexpr bool QREG = false;
   static constexpr int MIN_CTAS = 1;
   static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
   static constexpr int RING = WARPS * NSTAGE * STAGE;
@@ -574,13 +574,13 @@ struct Decoder {
     float lg[2][NT][2][2];
     {
       float sacc[2][2][NT][4];  // [group][mt]
-      float cacc[NT][4];        // rows gid: q.z of the first group, rows gid + 8: of the second
+      float cacc[2][NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           sacc[0][0][nt][i] = sacc[0][1][nt][i] = sacc[1][0][nt][i] = sacc[1][1][nt][i] = 0.f;
-          cacc[nt][i] = 0.f;
+          cacc[0][nt][i] = cacc[1][nt][i] = 0.f;
         }
       // the key side of each group in turn (fewer live registers than both at
       // once); the zero-point product of both groups runs with the second
@@ -610,11 +610,8 @@ struct Decoder {
               const uint32_t b1 = split_mul(q1, mv.w);
               mma_16816(sacc[x][0][nt], a0, b0, b1);
               mma_16816(sacc[x][1][nt], a1, b0, b1);
-              if (x == 1) {
-                const uint2 z0 = make_uint2(kmo[16 * kt], kmo[16 * kt + 2]);
-                const uint32_t ac[4] = {z0.x, mv.x, z0.y, mv.z};
-                mma_16816(cacc[nt], ac, q0, q1);
-              }
+              const uint32_t ac[4] = {mv.x, mv.y, mv.z, mv.w};
+              mma_16816(cacc[x][nt], ac, q0, q1);
             }
           }
         }
@@ -623,7 +620,7 @@ struct Decoder {
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          const float zq = cacc[nt][2 * x] * scale_log2;
+          const float zq = cacc[x][nt][0] * scale_log2;
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
