@@ -88,10 +88,9 @@ struct DecodeCfg {
   static constexpr int QF = ROPE ? NT * 4 * D * 4 : 0;         // fp32 q of the segment's heads
   static constexpr int SMEM = RING + PS + ZERO + PREFIX + QS + INTRA + QF + MBAR;
   static_assert(SMEM <= 232448, "fits the shared memory of one CTA");
-  // partials staged per merge batch: they fit the ring, their weights the p~ area
-  static constexpr int MERGE_BATCH = RING / (G * PSTRIDE * 4) < PS / (4 * G) ? RING / (G * PSTRIDE * 4)
-                                                                              : PS / (4 * G);
-  static_assert(MERGE_BATCH >= 1, "a merge batch holds at least one partial");
+  // the final merge's weights ([partials][G] + G floats) fit the ring for any
+  // partial count up to the CTA count of one wave
+  static_assert(RING >= (1024 + 1) * G * 4, "merge weights fit the stage ring");
   static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
   static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
   static_assert(PS % 16 == 0 && RING % 16 == 0 && ZERO % 16 == 0 && PREFIX % 16 == 0 &&
@@ -170,12 +169,6 @@ __device__ inline void build_prefix(const DecodeParams& p, int* s_pref) {
 // The stream-K CTA that owns global item x (CTA c owns [c*T/N, (c+1)*T/N)).
 __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
   return ((x + 1) * n - 1) / total;
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 template <int D, int BITS, int G, bool ROPE = false>
@@ -806,78 +799,69 @@ struct Decoder {
 };
 
 // Log-sum-exp merge of a segment's nparts consecutive partials into the
-// normalised output [G][D], by the whole CTA.  The partials come from other CTAs:
-// one thread bulk-copies them, MERGE_BATCH at a time, into the (idle) stage ring,
-// so a batch costs one memory round trip; the arithmetic then runs out of shared
-// memory.  Returns false if a bounded wait gave up.
+// normalised output [G][D], by the whole CTA.  The partials come from other CTAs
+// (visible after the acquire of the split-K counter) and are read from L2 with
+// ordinary loads: one warp per head finds the maximum over the non-empty partials
+// and their weights (s_w [nparts][G] in shared memory, then the G sums of weights
+// times denominators), then every thread sums its output elements.
 template <int D, int BITS, int G, bool ROPE>
-__device__ bool final_merge(const float* parts, int nparts, float* out, uint8_t* ring, float* s_w,
-                            uint64_t* bar, uint32_t& parity) {
+__device__ void final_merge(const float* parts, int nparts, float* out, float* s_w) {
   using C = DecodeCfg<D, BITS, G, ROPE>;
   constexpr int PS = C::PSTRIDE;
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
-  __shared__ float s_M[G], s_L[G], s_scale[G];
-  constexpr int PER = (G * D + C::WARPS * 32 - 1) / (C::WARPS * 32);  // outputs per thread
-  float acc[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  if (tid < G) { s_M[tid] = -INFINITY; s_L[tid] = 0.f; }
-  bool ok = true;
-  const float* stage = reinterpret_cast<const float*>(ring);
-  for (int first = 0; first < nparts; first += C::MERGE_BATCH) {
-    const int nb = min(C::MERGE_BATCH, nparts - first);
-    __syncthreads();  // the ring (and s_w) are free
-    if (tid == 0) {
-      const uint32_t bytes = (uint32_t)(nb * G * PS * 4);
-      fence_proxy_async_global();  // the partials were written by other CTAs' ordinary stores
-      fence_proxy_async();
-      mbar_arrive_expect_tx(bar, bytes);
-      tma_load_1d(ring, parts + (size_t)first * G * PS, bytes, bar);
+  float* s_l = s_w + (size_t)nparts * G;
+  for (int g = warp; g < G; g += nthreads / 32) {
+    // (m, l) of partials lane, lane + 32, ...: the first 32 held in registers
+    float m0 = -INFINITY, l0 = 0.f;
+    if (lane < nparts) {
+      m0 = __ldcg(parts + (size_t)(lane * G + g) * PS);
+      l0 = __ldcg(parts + (size_t)(lane * G + g) * PS + 1);
     }
-    ok = mbar_wait(bar, parity, kMaxPolls) && ok;
-    parity ^= 1u;
-    // per head (one warp each): batch max, new running max, weights, l
-    for (int g = warp; g < G; g += nthreads / 32) {
-      float mx = -INFINITY;
-      for (int i = lane; i < nb; i += 32) mx = fmaxf(mx, stage[(i * G + g) * PS]);
+    float mx = l0 > 0.f ? m0 : -INFINITY;
+    for (int i = lane + 32; i < nparts; i += 32)
+      if (__ldcg(parts + (size_t)(i * G + g) * PS + 1) > 0.f) mx = fmaxf(mx, __ldcg(parts + (size_t)(i * G + g) * PS));
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mold = s_M[g], mnew = fmaxf(mold, mx);
-      const float sc = (mnew == -INFINITY || mold == mnew) ? 1.f : exp2f(mold - mnew);
-      float lsum = 0.f;
-      for (int i = lane; i < nb; i += 32) {
-        const float mi = stage[(i * G + g) * PS];
-        const float w = mnew == -INFINITY ? 0.f : exp2f(mi - mnew);
-        s_w[i * G + g] = w;
-        lsum += w * stage[(i * G + g) * PS + 1];
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-      __syncwarp();
-      if (lane == 0) { s_M[g] = mnew; s_L[g] = s_L[g] * sc + lsum; s_scale[g] = sc; }
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float lsum = 0.f;
+    if (lane < nparts) {
+      const float w = l0 > 0.f ? fast_exp2(m0 - mx) : 0.f;
+      s_w[lane * G + g] = w;
+      lsum = w * l0;
     }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int e = tid + k * nthreads;
-      if (e < G * D) {
-        const int g = e / D, d = e % D;
-        float o = acc[k] * s_scale[g];
-        for (int i = 0; i < nb; ++i) o += s_w[i * G + g] * stage[(i * G + g) * PS + 4 + d];
-        acc[k] = o;
-      }
+    for (int i = lane + 32; i < nparts; i += 32) {
+      const float li = __ldcg(parts + (size_t)(i * G + g) * PS + 1);
+      const float w = li > 0.f ? fast_exp2(__ldcg(parts + (size_t)(i * G + g) * PS) - mx) : 0.f;
+      s_w[i * G + g] = w;
+      lsum = fmaf(w, li, lsum);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if (lane == 0) s_l[g] = lsum;
   }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += nthreads) {
+    const int g = e / D, d = e % D;
+    // eight independent loads in flight per round (one L2 round trip per round)
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int i = 0;
+    for (; i + 8 <= nparts; i += 8) {
+      float v[8];
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int e = tid + k * nthreads;
-    if (e < G * D) {
-      const float l = s_L[e / D];
-      out[e] = l > 0.f ? acc[k] / l : 0.f;
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(parts + (size_t)((i + k) * G + g) * PS + 4 + d);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) o[k] = fmaf(s_w[(i + k) * G + g], v[k], o[k]);
     }
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = i + k < nparts ? __ldcg(parts + (size_t)((i + k) * G + g) * PS + 4 + d) : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (i + k < nparts) o[k] = fmaf(s_w[(i + k) * G + g], v[k], o[k]);
+    const float osum = ((o[0] + o[1]) + (o[2] + o[3])) + ((o[4] + o[5]) + (o[6] + o[7]));
+    const float l = s_l[g];
+    out[e] = l > 0.f ? osum / l : 0.f;
   }
-  return ok;
 }
 
 template <int D, int BITS, int G, bool ROPE = false>
@@ -902,6 +886,9 @@ decode_kernel(const DecodeParams p) {
   __half* ps = ps_all + warp * G * C::PSROW;
   uint8_t* wring = ring + warp * C::NSTAGE * C::STAGE;
 
+  // the lengths first (warp 0: their loads are the kernel's first memory round
+  // trip), the shared-memory set-up of the other warps meanwhile
+  build_prefix(p, s_pref);
   for (int i = threadIdx.x; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
   if (lane == 0) {
     for (int st = 0; st < C::NSTAGE; ++st) mbar_init(bars + st, 1);
@@ -911,7 +898,6 @@ decode_kernel(const DecodeParams p) {
   uint32_t parity = 0;  // bit st: parity of the next phase of stage st's mbarrier
   uint32_t merge_parity = 0;
   bool failed = false;  // a bounded wait gave up: stop using staged data
-  build_prefix(p, s_pref);
   __syncthreads();
   if constexpr (ROPE) {
     // the cos/sin of the offsets 0..63 of every pair, once per CTA (the merge
@@ -965,12 +951,13 @@ decode_kernel(const DecodeParams p) {
           uint8_t* dst = wring + slotn * C::STAGE;
           fence_proxy_async();
           mbar_arrive_expect_tx(bars + slotn, n_in * C::STAGE1);
-          tma_load_1d(dst, p.k_codes + g * C::TB, n_in * C::TB, bars + slotn);
-          tma_load_1d(dst + C::OFF_VC, p.v_codes + g * C::TB, n_in * C::TB, bars + slotn);
-          tma_load_1d(dst + C::OFF_KM, reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA,
-                      n_in * C::KMETA, bars + slotn);
-          tma_load_1d(dst + C::OFF_VM, reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA,
-                      n_in * C::VMETA, bars + slotn);
+          const uint64_t pol = l2_evict_first_policy();
+          tma_load_1d_hint(dst, p.k_codes + g * C::TB, n_in * C::TB, bars + slotn, pol);
+          tma_load_1d_hint(dst + C::OFF_VC, p.v_codes + g * C::TB, n_in * C::TB, bars + slotn, pol);
+          tma_load_1d_hint(dst + C::OFF_KM, reinterpret_cast<const uint8_t*>(p.k_meta) + g * C::KMETA,
+                           n_in * C::KMETA, bars + slotn, pol);
+          tma_load_1d_hint(dst + C::OFF_VM, reinterpret_cast<const uint8_t*>(p.v_meta) + g * C::VMETA,
+                           n_in * C::VMETA, bars + slotn, pol);
           if constexpr (ROPE)  // cos/sin of the group's position block: 32 (group + sinks / 32)
             tma_load_1d(dst + C::OFF_BASE, p.rope + (size_t)(64 + ga + gi + (L.ns >> 5)) * (D / 2), C::BASE,
                         bars + slotn);
@@ -1060,7 +1047,7 @@ decode_kernel(const DecodeParams p) {
 #pragma unroll
         for (int w = 0; w < C::WARPS; ++w) {
           const float* src = reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE) + g * C::PSTRIDE;
-          const float wt = exp2f(src[0] - mx);
+          const float wt = fast_exp2(src[0] - mx);
           lsum += wt * src[1];
           osum += wt * src[4 + d];
         }
@@ -1077,11 +1064,10 @@ decode_kernel(const DecodeParams p) {
     if (threadIdx.x == 0) s_last = atomic_add_acq_rel(&p.counters[seg], 1) == nparts - 1;
     __syncthreads();
     if (s_last) {
-      // the stage ring is idle here; the p~ area holds the merge weights
-      const bool ok = final_merge<D, BITS, G, ROPE>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
-                                               p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D, ring,
-                                               reinterpret_cast<float*>(ps_all), merge_bar, merge_parity);
-      if (!ok && threadIdx.x == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
+      // the stage ring (idle here) holds the merge weights
+      final_merge<D, BITS, G, ROPE>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
+                                    p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D,
+                                    reinterpret_cast<float*>(ring));
       if (threadIdx.x == 0) p.counters[seg] = 0;
     }
     __syncthreads();

@@ -71,12 +71,6 @@ struct AttnParams {
   int32_t n[KVQ_MAX_BATCH];
 };
 
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // ------------------------------------------------------- tcgen05 passes
 // The same two passes on the 5th-generation tensor cores: tcgen05.mma
 // (kind::f16, fp32 accumulators in tensor memory), both operands in shared

@@ -99,12 +99,6 @@ struct Params {
   int32_t n_stream;
 };
 
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
   return ((x + 1) * n - 1) / total;
 }
@@ -555,11 +549,11 @@ __device__ bool final_merge(const float* parts, int nparts, float* out, uint8_t*
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       const float mold = s_M[g], mnew = fmaxf(mold, mx);
-      const float sc = (mnew == -INFINITY || mold == mnew) ? 1.f : exp2f(mold - mnew);
+      const float sc = (mnew == -INFINITY || mold == mnew) ? 1.f : fast_exp2(mold - mnew);
       float lsum = 0.f;
       for (int i = lane; i < nb; i += 32) {
         const float mi = stage[(i * G + g) * PS];
-        const float w = mnew == -INFINITY ? 0.f : exp2f(mi - mnew);
+        const float w = mnew == -INFINITY ? 0.f : fast_exp2(mi - mnew);
         s_w[i * G + g] = w;
         lsum += w * stage[(i * G + g) * PS + 1];
       }
@@ -784,7 +778,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
 #pragma unroll
         for (int w = 0; w < C::WARPS; ++w) {
           const float* src = reinterpret_cast<const float*>(rings + w * C::RING) + g * C::PSTRIDE;
-          const float wt = exp2f(src[0] - mx);
+          const float wt = fast_exp2(src[0] - mx);
           lsum += wt * src[1];
           osum += wt * src[4 + d];
         }
