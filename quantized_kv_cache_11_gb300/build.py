@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_quantize.cu", "kvq_decode.cu", "kvq_trizone_build.cu",
-           "kvq_trizone_decode.cu", "kvq_rdkv.cu", "kvq_decode_rope.cu", "kvq_selftest.cu"]
+           "kvq_trizone_decode.cu", "kvq_rdkv.cu", "kvq_decode_rope.cu", "kvq_selftest.cu",
+           "kvq_decode_cps2.cu", "kvq_decode_cps4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE-exact fp32 division and no flush-to-zero: the quantizer must match the
 # oracle bit for bit.  Never --use_fast_math.

@@ -6,15 +6,11 @@
 namespace kvq {
 
 inline int decode_slots(const kvq_cache* c, int G, int* err) {
-#define KVQ_SLOTS(D_, B_, G_) \
-  if (c->head_dim == D_ && c->bits == B_ && G == G_) return DecodeLaunch<D_, B_, G_>::slots(err);
-#define KVQ_SLOTS_G(D_, B_) KVQ_SLOTS(D_, B_, 1) KVQ_SLOTS(D_, B_, 2) KVQ_SLOTS(D_, B_, 4) KVQ_SLOTS(D_, B_, 8)
-  KVQ_SLOTS_G(128, 2) KVQ_SLOTS_G(128, 4) KVQ_SLOTS_G(128, 8)
-  KVQ_SLOTS_G(64, 2) KVQ_SLOTS_G(64, 4) KVQ_SLOTS_G(64, 8)
-#undef KVQ_SLOTS_G
-#undef KVQ_SLOTS
-  *err = 2;
-  return 0;
+  const int cps = decode_shape(c, err);
+  if (*err) return 0;
+  if (cps == 2) return decode_slots_cps2(c, G, err);
+  if (cps == 4) return decode_slots_cps4(c, G, err);
+  return decode_slots_shape<1>(c, G, err);
 }
 
 }  // namespace kvq
@@ -55,14 +51,12 @@ static kvq_status decode_prepare(const kvq_cache* c, int32_t n_q_heads, const vo
 }
 
 static kvq_status decode_launch(const kvq_cache* c, int G, const DecodeParams& p, cudaStream_t st) {
-  if (c->head_dim == 128) {
-    if (c->bits == 2) return decode_dispatch_g<128, 2>(G, p, st);
-    if (c->bits == 4) return decode_dispatch_g<128, 4>(G, p, st);
-    return decode_dispatch_g<128, 8>(G, p, st);
-  }
-  if (c->bits == 2) return decode_dispatch_g<64, 2>(G, p, st);
-  if (c->bits == 4) return decode_dispatch_g<64, 4>(G, p, st);
-  return decode_dispatch_g<64, 8>(G, p, st);
+  int err = 0;
+  const int cps = decode_shape(c, &err);
+  if (err) return KVQ_ERR_CUDA;
+  if (cps == 2) return decode_run_cps2(c, G, p, st);
+  if (cps == 4) return decode_run_cps4(c, G, p, st);
+  return decode_run_shape<1>(c, G, p, st);
 }
 
 }  // namespace kvq

@@ -46,7 +46,11 @@ constexpr uint32_t kMaxPolls = 1u << 22;
 
 // ROPE: the keys are stored before the rotary position embedding and rotated to
 // their positions after dequantization (the K side then runs on CUDA cores).
-template <int D, int BITS, int G, bool ROPE = false>
+// CPS: CTAs per SM (1, 2 or 4; the 2- and 4-bit decode without RoPE only).
+// Several smaller CTAs per SM suit caches of many short (sequence, KV head)
+// segments: each CTA then holds about one segment piece, and the pieces' set-up
+// and merges overlap on the SM instead of running one after another.
+template <int D, int BITS, int G, bool ROPE = false, int CPS = 1>
 struct DecodeCfg {
   using T = Tile<D, BITS>;
   static constexpr int TB = T::kBytes;
@@ -68,14 +72,15 @@ struct DecodeCfg {
   static constexpr int KT = D / 16;
   static constexpr int NWL = T::kWordsPerLane;
   static constexpr int PPW = T::kPairsPerWord;
-  // one CTA of 16 warps per SM for 2- and 4-bit codes: fewer, larger CTAs leave
-  // fewer split-K partials per (sequence, KV head) for the last CTA to merge
-  // (12 at 4 bits with ROPE: its stage ring, offset table and fp32 q must fit)
-  static constexpr int WARPS = BITS == 8 ? 4 : (ROPE && BITS == 4 ? 12 : 16);
+  // 16 warps per SM for 2- and 4-bit codes, as one CTA (fewer split-K partials
+  // per segment) or as CPS CTAs of 16 / CPS warps (12 warps at 4 bits with ROPE:
+  // its stage ring, offset table and fp32 q must fit)
+  static_assert(CPS == 1 || (!ROPE && BITS != 8), "several CTAs per SM only without RoPE, at 2 and 4 bits");
+  static constexpr int WARPS = BITS == 8 ? 4 : (ROPE && BITS == 4 ? 12 : 16 / CPS);
   static constexpr int NSTAGE = BITS == 2 ? (ROPE ? 3 : 2) : (BITS == 4 ? 2 : 3);
   // q pairs held in registers (one n-tile) instead of re-read from shared memory
   static constexpr bool QREG = false;
-  static constexpr int MIN_CTAS = 1;
+  static constexpr int MIN_CTAS = CPS;
   static constexpr int PSTRIDE = D + 4;  // floats per head in a partial: m, l, pad, pad, o[D]
   static constexpr int RING = WARPS * NSTAGE * STAGE;
   static constexpr int PSROW = 48;                   // halves per head row of the p~ exchange
@@ -88,9 +93,9 @@ struct DecodeCfg {
   static constexpr int QF = ROPE ? NT * 4 * D * 4 : 0;         // fp32 q of the segment's heads
   static constexpr int SMEM = RING + PS + ZERO + PREFIX + QS + INTRA + QF + MBAR;
   static_assert(SMEM <= 232448, "fits the shared memory of one CTA");
-  // the final merge's weights ([partials][G] + G floats) fit the ring for any
-  // partial count up to the CTA count of one wave
-  static_assert(RING >= (1024 + 1) * G * 4, "merge weights fit the stage ring");
+  // the final merge keeps its weights ([partials][G] + G floats) in the ring:
+  // up to RING / (4 G) - 1 partials per segment (checked at launch)
+  static constexpr int MAX_PARTS = RING / (4 * G) - 1;
   static_assert(WARPS * G * PSTRIDE * 4 <= RING, "warp partials reuse the stage ring");
   static_assert(NSTAGE * STAGE >= G * PSTRIDE * 4, "a warp's partial fits its ring slice");
   static_assert(PS % 16 == 0 && RING % 16 == 0 && ZERO % 16 == 0 && PREFIX % 16 == 0 &&
@@ -171,9 +176,9 @@ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
   return ((x + 1) * n - 1) / total;
 }
 
-template <int D, int BITS, int G, bool ROPE = false>
+template <int D, int BITS, int G, bool ROPE = false, int CPS = 1>
 struct Decoder {
-  using C = DecodeCfg<D, BITS, G, ROPE>;
+  using C = DecodeCfg<D, BITS, G, ROPE, CPS>;
   static constexpr int NT = C::NT, KT = C::KT;
   // Bit position p of the codes that unpack8 puts in register 4 mt + i (row half
   // rh = i & 1 of an mma A fragment; never dependent on the k-half i >> 1): the
@@ -804,9 +809,9 @@ struct Decoder {
 // ordinary loads: one warp per head finds the maximum over the non-empty partials
 // and their weights (s_w [nparts][G] in shared memory, then the G sums of weights
 // times denominators), then every thread sums its output elements.
-template <int D, int BITS, int G, bool ROPE>
+template <int D, int BITS, int G, bool ROPE, int CPS>
 __device__ void final_merge(const float* parts, int nparts, float* out, float* s_w) {
-  using C = DecodeCfg<D, BITS, G, ROPE>;
+  using C = DecodeCfg<D, BITS, G, ROPE, CPS>;
   constexpr int PS = C::PSTRIDE;
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -864,10 +869,11 @@ __device__ void final_merge(const float* parts, int nparts, float* out, float* s
   }
 }
 
-template <int D, int BITS, int G, bool ROPE = false>
-__global__ void __launch_bounds__(DecodeCfg<D, BITS, G, ROPE>::WARPS * 32, DecodeCfg<D, BITS, G, ROPE>::MIN_CTAS)
+template <int D, int BITS, int G, bool ROPE = false, int CPS = 1>
+__global__ void __launch_bounds__(DecodeCfg<D, BITS, G, ROPE, CPS>::WARPS * 32,
+                                  DecodeCfg<D, BITS, G, ROPE, CPS>::MIN_CTAS)
 decode_kernel(const DecodeParams p) {
-  using C = DecodeCfg<D, BITS, G, ROPE>;
+  using C = DecodeCfg<D, BITS, G, ROPE, CPS>;
   constexpr int NTILES = C::NT;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
@@ -936,7 +942,7 @@ decode_kernel(const DecodeParams p) {
     // this warp's contiguous share of items [i0, i0 + n)
     const int per = (n + C::WARPS - 1) / C::WARPS;
     const int ia = i0 + min(n, warp * per), ie = i0 + min(n, (warp + 1) * per);
-    Decoder<D, BITS, G, ROPE> dec;
+    Decoder<D, BITS, G, ROPE, CPS> dec;
     {
       const int ga = ia, cnt = failed ? 0 : max(0, min(ie, ng) - ia);
       const size_t g0 = (size_t)seg * p.max_groups + ga;
@@ -1065,7 +1071,7 @@ decode_kernel(const DecodeParams p) {
     __syncthreads();
     if (s_last) {
       // the stage ring (idle here) holds the merge weights
-      final_merge<D, BITS, G, ROPE>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
+      final_merge<D, BITS, G, ROPE, CPS>(p.part + (size_t)(c0 + seg) * G * C::PSTRIDE, nparts,
                                     p.out + ((size_t)b * p.hkv * G + (size_t)h * G) * D,
                                     reinterpret_cast<float*>(ring));
       if (threadIdx.x == 0) p.counters[seg] = 0;
@@ -1090,34 +1096,89 @@ inline DecodeLayout decode_layout(const kvq_cache* c, int G, int n_stream) {
   return L;
 }
 
-template <int D, int BITS, int G, bool ROPE = false>
+template <int D, int BITS, int G, bool ROPE = false, int CPS = 1>
 struct DecodeLaunch {
   // resident CTAs on the whole current GPU (one wave), computed once per device
   static int slots(int* err) {
-    using C = DecodeCfg<D, BITS, G, ROPE>;
-    return device_slots(reinterpret_cast<const void*>(decode_kernel<D, BITS, G, ROPE>), C::WARPS * 32, C::SMEM,
-                        err);
+    using C = DecodeCfg<D, BITS, G, ROPE, CPS>;
+    return device_slots(reinterpret_cast<const void*>(decode_kernel<D, BITS, G, ROPE, CPS>), C::WARPS * 32,
+                        C::SMEM, err);
   }
   static kvq_status run(DecodeParams p, cudaStream_t s) {
-    using C = DecodeCfg<D, BITS, G, ROPE>;
+    using C = DecodeCfg<D, BITS, G, ROPE, CPS>;
     int err = 0;
-    const int n = slots(&err);  // <= RING / (8 G): the final merge keeps 2 floats per partial
+    const int n = slots(&err);
     if (err) return KVQ_ERR_CUDA;
+    // a segment's partials come from at most n CTAs (+ one spare slot)
+    if (n + 1 > C::MAX_PARTS) return KVQ_ERR_UNSUPPORTED;
     p.n_stream = n;
-    decode_kernel<D, BITS, G, ROPE><<<n, C::WARPS * 32, C::SMEM, s>>>(p);
+    decode_kernel<D, BITS, G, ROPE, CPS><<<n, C::WARPS * 32, C::SMEM, s>>>(p);
     return launch_status();
   }
 };
 
-template <int D, int BITS, bool ROPE = false>
+template <int D, int BITS, bool ROPE = false, int CPS = 1>
 kvq_status decode_dispatch_g(int G, const DecodeParams& p, cudaStream_t s) {
   switch (G) {
-    case 1: return DecodeLaunch<D, BITS, 1, ROPE>::run(p, s);
-    case 2: return DecodeLaunch<D, BITS, 2, ROPE>::run(p, s);
-    case 4: return DecodeLaunch<D, BITS, 4, ROPE>::run(p, s);
-    case 8: return DecodeLaunch<D, BITS, 8, ROPE>::run(p, s);
+    case 1: return DecodeLaunch<D, BITS, 1, ROPE, CPS>::run(p, s);
+    case 2: return DecodeLaunch<D, BITS, 2, ROPE, CPS>::run(p, s);
+    case 4: return DecodeLaunch<D, BITS, 4, ROPE, CPS>::run(p, s);
+    case 8: return DecodeLaunch<D, BITS, 8, ROPE, CPS>::run(p, s);
     default: return KVQ_ERR_UNSUPPORTED;
   }
+}
+
+// The uniform decode (no RoPE) of one CTA shape: resident CTAs and launch, by
+// head_dim, bits and G.  Instantiated for CPS 1 in kvq_decode.cu and for CPS 2
+// and 4 in their own translation units.
+template <int CPS>
+int decode_slots_shape(const kvq_cache* c, int G, int* err) {
+#define KVQ_SLOTS(D_, B_, G_) \
+  if (c->head_dim == D_ && c->bits == B_ && G == G_) return DecodeLaunch<D_, B_, G_, false, CPS>::slots(err);
+#define KVQ_SLOTS_G(D_, B_) KVQ_SLOTS(D_, B_, 1) KVQ_SLOTS(D_, B_, 2) KVQ_SLOTS(D_, B_, 4) KVQ_SLOTS(D_, B_, 8)
+  KVQ_SLOTS_G(128, 2) KVQ_SLOTS_G(128, 4) KVQ_SLOTS_G(64, 2) KVQ_SLOTS_G(64, 4)
+  if constexpr (CPS == 1) { KVQ_SLOTS_G(128, 8) KVQ_SLOTS_G(64, 8) }
+#undef KVQ_SLOTS_G
+#undef KVQ_SLOTS
+  *err = 2;
+  return 0;
+}
+
+template <int CPS>
+kvq_status decode_run_shape(const kvq_cache* c, int G, const DecodeParams& p, cudaStream_t st) {
+  if (c->head_dim == 128) {
+    if (c->bits == 2) return decode_dispatch_g<128, 2, false, CPS>(G, p, st);
+    if (c->bits == 4) return decode_dispatch_g<128, 4, false, CPS>(G, p, st);
+    if constexpr (CPS == 1) return decode_dispatch_g<128, 8, false, 1>(G, p, st);
+    return KVQ_ERR_UNSUPPORTED;
+  }
+  if (c->bits == 2) return decode_dispatch_g<64, 2, false, CPS>(G, p, st);
+  if (c->bits == 4) return decode_dispatch_g<64, 4, false, CPS>(G, p, st);
+  if constexpr (CPS == 1) return decode_dispatch_g<64, 8, false, 1>(G, p, st);
+  return KVQ_ERR_UNSUPPORTED;
+}
+
+// Defined in the CPS 2 and CPS 4 translation units.
+int decode_slots_cps2(const kvq_cache* c, int G, int* err);
+int decode_slots_cps4(const kvq_cache* c, int G, int* err);
+kvq_status decode_run_cps2(const kvq_cache* c, int G, const DecodeParams& p, cudaStream_t st);
+kvq_status decode_run_cps4(const kvq_cache* c, int G, const DecodeParams& p, cudaStream_t st);
+
+// CTAs per SM for a uniform decode without RoPE: the smallest of 1, 2, 4 whose
+// grid (one wave) has at least one CTA per (sequence, KV head) segment, so that a
+// CTA rarely spans two segments; 1 at 8 bits.
+inline int decode_shape(const kvq_cache* c, int* err) {
+  if (c->bits == 8) return 1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess) {
+    *err = 1;
+    return 1;
+  }
+  const int64_t seg = (int64_t)c->batch * c->n_kv_heads;
+  if (seg <= sms) return 1;
+  if (seg <= 2 * (int64_t)sms) return 2;
+  return 4;
 }
 
 // The kernel parameters of one decode call: the cache's buffers and lengths, q

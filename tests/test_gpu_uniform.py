@@ -208,3 +208,36 @@ def test_bounded_wait_gives_up_and_reports():
     # the context still works
     x = torch.arange(8, device="cuda", dtype=torch.float32)
     assert float(x.sum()) == 28.0
+
+
+# Geometries with many (sequence, KV head) segments: on a 152-SM GPU the decode
+# runs them as 1, 2 and 4 CTAs per SM (the launch picks the smallest grid with a
+# CTA per segment); ragged lengths and fp16 tails put several segment pieces and
+# chunk items in one CTA.  Every sequence is checked against the oracle.
+SHAPES = {
+    "seg_100_d128_2bit_gqa4": (S.SERVING.scaled(batch=25, n_kv_heads=4, n_q_heads=16, context=300,
+                                                ragged=(1, 300), bits=2), 2),
+    "seg_200_d128_2bit_mha": (S.LLAMA2_13B.scaled(batch=25, n_q_heads=8, n_kv_heads=8, context=200,
+                                                  n_tail=8), 2),
+    "seg_400_d64_4bit_gqa2": (S.SERVING.scaled(batch=50, n_kv_heads=8, n_q_heads=16, head_dim=64, context=260,
+                                               ragged=(0, 260), bits=4), 4),
+    "seg_320_d128_2bit_gqa8": (S.SERVING.scaled(batch=40, n_kv_heads=8, n_q_heads=64, context=160,
+                                                ragged=(30, 160), bits=2), 2),
+}
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_many_segments_match_oracle(name):
+    w, bits = SHAPES[name]
+    inp = S.generate(w)
+    if w.ragged is not None:
+        inp["n_tail"] = (inp["seq_len"] % 32).astype(np.int32)
+    cache = H.device_cache(w, inp, bits)
+    q = torch.from_numpy(inp["q"]).cuda()
+    out = cache.decode(q, w.sm_scale).cpu().numpy()
+    assert cache.device_errors() == 0
+    ref = H.oracle_decode(inp["q"], H.oracle_states(inp, bits), w.sm_scale)
+    H.assert_close(out, ref)
+    # a second call gives identical bits (the merge counters were left at zero)
+    out2 = cache.decode(q, w.sm_scale).cpu().numpy()
+    assert (out2 == out).all()
