@@ -25,9 +25,10 @@
 //   B = q * scale, split into two fp16 halves (hi = fp16(q*s), lo = q*s - hi,
 //   exact), in separate columns, so the per-channel scale is applied to q once
 //   per group.  The zero points enter through one more small MMA (rows = zero
-//   points).  Online softmax in fp32; P.V likewise with B = fp16(p * scale)
-//   per 32-channel value group, the value zero points and the softmax
-//   denominator (a row of ones) from one small MMA.
+//   points).  Online softmax in fp32; P.V likewise with B = p * scale per
+//   32-channel value group, split into hi and lo fp16 columns (exact: the
+//   columns of the other heads' lo halves are otherwise empty), the value zero
+//   points and the softmax denominator (a row of ones) from one small MMA.
 // * Splits are merged by log-sum-exp; the last CTA to finish a (sequence, KV
 //   head) merges and writes the output, then resets its counter.  No spin-wait.
 #pragma once
@@ -183,8 +184,12 @@ struct Decoder {
   // Bit position p of the codes that unpack8 puts in register 4 mt + i (row half
   // rh = i & 1 of an mma A fragment; never dependent on the k-half i >> 1): the
   // register holds the fp16 subnormals c * 2^(p - 24).  unit = 2^(24 - p).
+  // p is at least 2: measured on GB300, a tensor-core dot product over such
+  // subnormal operands keeps about 17 + p significant bits (relative error near
+  // 2^-(17 + p) of the summed magnitudes; fp32-like from p = 6 on), so codes at
+  // p = 0 would lose 7 bits against the fp32 accumulation.
   static __host__ __device__ constexpr int pos(int mt, int rh) {
-    return BITS == 2 ? 4 * mt + 2 * rh : (BITS == 4 ? 4 * rh : 0);
+    return 2 + (BITS == 2 ? 4 * mt + 2 * rh : (BITS == 4 ? 4 * rh : 0));
   }
   static __host__ __device__ constexpr float unit(int mt, int rh) { return (float)(1 << (24 - pos(mt, rh))); }
   static constexpr uint32_t kSixteenth = 0x2C002C00u;  // half2(1/16, 1/16)
@@ -289,30 +294,30 @@ struct Decoder {
   }
 
   // Operands of pairs P0 .. P0+7 of the lane's words (P0 a multiple of 8): one
-  // mask per register (plus one shift right by 8 per word at 2 and 4 bits, per
-  // second pair at 8 bits) leaves each code pair in the mantissa bits [p, p+b)
-  // of the two halves, exponent 0.  Bit positions by register: 2 bits
-  // 0,2,0,2 | 4,6,4,6; 4 bits 0,4,0,4; 8 bits 0 (see pos()).
+  // mask per register, on the word shifted left by 2 or right by 6, leaves each
+  // code pair in the mantissa bits [p, p+b) of the two halves, exponent 0.  Bit
+  // positions by register: 2 bits 2,4,2,4 | 6,8,6,8; 4 bits 2,6,2,6; 8 bits 2
+  // (see pos()).
   static __device__ __forceinline__ void unpack8(const uint32_t* w, int P0, uint32_t (&a)[8]) {
     if (BITS == 2) {
-      const uint32_t x = w[P0 / 8], y = x >> 8;
-      a[0] = x & 0x00030003u;  a[1] = x & 0x000C000Cu;  a[2] = y & 0x00030003u;  a[3] = y & 0x000C000Cu;
-      a[4] = x & 0x00300030u;  a[5] = x & 0x00C000C0u;  a[6] = y & 0x00300030u;  a[7] = y & 0x00C000C0u;
+      const uint32_t w0 = w[P0 / 8], x = w0 << 2, y = w0 >> 6;
+      a[0] = x & 0x000C000Cu;  a[1] = x & 0x00300030u;  a[2] = y & 0x000C000Cu;  a[3] = y & 0x00300030u;
+      a[4] = x & 0x00C000C0u;  a[5] = x & 0x03000300u;  a[6] = y & 0x00C000C0u;  a[7] = y & 0x03000300u;
     } else if (BITS == 4) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t x = w[P0 / 4 + h], y = x >> 8;
-        a[4 * h + 0] = x & 0x000F000Fu;
-        a[4 * h + 1] = x & 0x00F000F0u;
-        a[4 * h + 2] = y & 0x000F000Fu;
-        a[4 * h + 3] = y & 0x00F000F0u;
+        const uint32_t w0 = w[P0 / 4 + h], x = w0 << 2, y = w0 >> 6;
+        a[4 * h + 0] = x & 0x003C003Cu;
+        a[4 * h + 1] = x & 0x03C003C0u;
+        a[4 * h + 2] = y & 0x003C003Cu;
+        a[4 * h + 3] = y & 0x03C003C0u;
       }
     } else {
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const uint32_t x = w[P0 / 2 + h];
-        a[2 * h + 0] = x & 0x00FF00FFu;
-        a[2 * h + 1] = (x >> 8) & 0x00FF00FFu;
+        a[2 * h + 0] = (x << 2) & 0x03FC03FCu;
+        a[2 * h + 1] = (x >> 6) & 0x03FC03FCu;
       }
     }
   }
@@ -374,8 +379,10 @@ struct Decoder {
   }
 
   // p~ pairs for the V-side B fragments: column 8nt+gid (head 4nt + gid/2), tokens
-  // 16kt + 2tig + 8r and +1; zero in the lo columns (odd gid), which P.V leaves empty.
-  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) const {
+  // 16kt + 2tig + 8r and +1.  with_lo: the lo columns (odd gid) hold p~ too (the
+  // quantized groups split p~ * scale into hi and lo columns); otherwise zero
+  // (the fp16 chunks multiply p~ itself, exact in one column).
+  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2], bool with_lo) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + (gid >> 1);
@@ -383,7 +390,9 @@ struct Decoder {
       for (int kt = 0; kt < 2; ++kt)
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-          pp[nt][kt][r] = (g < G && !hl) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r) : 0u;
+          pp[nt][kt][r] = (g < G && (with_lo || !hl))
+                              ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r)
+                              : 0u;
     }
   }
 
@@ -422,8 +431,8 @@ struct Decoder {
         uint32_t b[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          b[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][0]), u32_as_h2(vs0)));
-          b[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][1]), u32_as_h2(vs1)));
+          b[nt][0] = split_mul(pv[nt][kt][0], vs0);
+          b[nt][1] = split_mul(pv[nt][kt][1], vs1);
         }
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
@@ -557,7 +566,7 @@ struct Decoder {
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
-    load_pp(ps, pp);
+    load_pp(ps, pp, true);
     pv_group(vc, vm8, pp, zrow);
     __syncwarp();
   }
@@ -644,10 +653,11 @@ struct Decoder {
     }
     if (__any_sync(0xffffffffu, need)) rescale(mloc);
     // p~ to the P.V B fragments: lane (gid, tig) holds p~ of head 4nt + tig at
-    // tokens 16mt + gid + 8r, i.e. the pair of columns (2tig, 2tig + 1) = (p~, 0)
+    // tokens 16mt + gid + 8r, i.e. the pair of columns (2tig, 2tig + 1) = (p~, p~)
     // of row gid of the 8 x 8 matrices [tokens 16mt + 8r + (0..7)] x [columns];
     // transposed in registers, lane (gid, tig) holds column gid (head gid/2's p~,
-    // or zeros for odd gid) at tokens 2tig, 2tig + 1: the B fragment of P.V.
+    // the hi column for even gid, the lo column for odd) at tokens 2tig, 2tig + 1:
+    // the B fragment of P.V.
     uint32_t pp[2][NT][2][2];
 #pragma unroll
     for (int x = 0; x < 2; ++x)
@@ -659,7 +669,7 @@ struct Decoder {
           for (int r = 0; r < 2; ++r) {
             float pf = fast_exp2(lg[x][nt][mt][r] - m[nt]);
             if (G % 4 != 0 && 4 * nt + tig >= G) pf = 0.f;
-            pp[x][nt][mt][r] = movmatrix_trans(h2_as_u32(__floats2half2_rn(pf, 0.f)));
+            pp[x][nt][mt][r] = movmatrix_trans(h2_as_u32(__floats2half2_rn(pf, pf)));
           }
 #pragma unroll
     for (int x = 0; x < 2; ++x)
@@ -747,7 +757,7 @@ struct Decoder {
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
-    load_pp(ps, pp);
+    load_pp(ps, pp, false);
     cp_async_wait<0>();
     __syncwarp();
     // value rows: A[d][t] = v[t][d]; matrix lane/8 -> (+8 channels if bit 0, +8 tokens if bit 1)
@@ -780,8 +790,9 @@ struct Decoder {
         for (int i = 0; i < 4; ++i) o[mt][nt][i] *= unit(0, i >> 1);
   }
 
-  // Write this warp's partial (m, l, unnormalised o) for its G heads.  The lo
-  // columns of o are empty; row j of zc holds sum p~ z of value group j.
+  // Write this warp's partial (m, l, unnormalised o) for its G heads: o is the sum
+  // of its hi and lo columns; row j of zc (hi column) holds sum p~ z of value
+  // group j, row 12 the sum of p~.
   __device__ __forceinline__ void write_partial(float* dst) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -795,8 +806,8 @@ struct Decoder {
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
-          d[4 + 16 * mt + gid] = o[mt][nt][0] + zs[mt / 2];
-          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + zs[mt / 2];
+          d[4 + 16 * mt + gid] = (o[mt][nt][0] + o[mt][nt][1]) + zs[mt / 2];
+          d[4 + 16 * mt + gid + 8] = (o[mt][nt][2] + o[mt][nt][3]) + zs[mt / 2];
         }
       }
     }
@@ -847,23 +858,17 @@ __device__ void final_merge(const float* parts, int nparts, float* out, float* s
   __syncthreads();
   for (int e = tid; e < G * D; e += nthreads) {
     const int g = e / D, d = e % D;
-    // eight independent loads in flight per round (one L2 round trip per round)
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int i = 0;
-    for (; i + 8 <= nparts; i += 8) {
-      float v[8];
+    // up to 32 independent loads in flight per round (one L2 round trip each)
+    float osum = 0.f;
+    for (int i = 0; i < nparts; i += 32) {
+      float v[32];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(parts + (size_t)((i + k) * G + g) * PS + 4 + d);
+      for (int k = 0; k < 32; ++k)
+        v[k] = i + k < nparts ? __ldcg(parts + (size_t)((i + k) * G + g) * PS + 4 + d) : 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) o[k] = fmaf(s_w[(i + k) * G + g], v[k], o[k]);
+      for (int k = 0; k < 32; ++k)
+        if (i + k < nparts) osum = fmaf(s_w[(i + k) * G + g], v[k], osum);
     }
-    float v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) v[k] = i + k < nparts ? __ldcg(parts + (size_t)((i + k) * G + g) * PS + 4 + d) : 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (i + k < nparts) o[k] = fmaf(s_w[(i + k) * G + g], v[k], o[k]);
-    const float osum = ((o[0] + o[1]) + (o[2] + o[3])) + ((o[4] + o[5]) + (o[6] + o[7]));
     const float l = s_l[g];
     out[e] = l > 0.f ? osum / l : 0.f;
   }
@@ -1041,25 +1046,37 @@ decode_kernel(const DecodeParams p) {
     // warp partial into the warp's (now idle) ring slice, then the CTA merge
     dec.write_partial(reinterpret_cast<float*>(wring));
     __syncthreads();
+    // the warps' weights once per (warp, head), then the output elements
+    float* wts = reinterpret_cast<float*>(ps_all);  // [WARPS][G] weights, [WARPS][G] weight x l
+    if (threadIdx.x < C::WARPS * G) {
+      const int w = threadIdx.x / G, g = threadIdx.x % G;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w2 = 0; w2 < C::WARPS; ++w2)
+        mx = fmaxf(mx, reinterpret_cast<const float*>(ring + w2 * C::NSTAGE * C::STAGE)[g * C::PSTRIDE]);
+      const float* src = reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE) + g * C::PSTRIDE;
+      const float wt = mx == -INFINITY ? 0.f : fast_exp2(src[0] - mx);
+      wts[w * G + g] = wt;
+      wts[C::WARPS * G + w * G + g] = wt * src[1];
+      if (w == 0) wts[2 * C::WARPS * G + g] = mx;
+    }
+    __syncthreads();
     float* slot = p.part + (size_t)(c + seg) * G * C::PSTRIDE;
     for (int e2 = threadIdx.x; e2 < G * D; e2 += blockDim.x) {
       const int g = e2 / D, d = e2 % D;
-      float mx = -INFINITY;
+      float osum = 0.f;
 #pragma unroll
       for (int w = 0; w < C::WARPS; ++w)
-        mx = fmaxf(mx, reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE)[g * C::PSTRIDE]);
-      float lsum = 0.f, osum = 0.f;
-      if (mx != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < C::WARPS; ++w) {
-          const float* src = reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE) + g * C::PSTRIDE;
-          const float wt = fast_exp2(src[0] - mx);
-          lsum += wt * src[1];
-          osum += wt * src[4 + d];
-        }
-      }
+        osum = fmaf(wts[w * G + g],
+                    reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE)[g * C::PSTRIDE + 4 + d], osum);
       slot[g * C::PSTRIDE + 4 + d] = osum;
-      if (d == 0) { slot[g * C::PSTRIDE] = mx; slot[g * C::PSTRIDE + 1] = lsum; }
+      if (d == 0) {
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::WARPS; ++w) lsum += wts[C::WARPS * G + w * G + g];
+        slot[g * C::PSTRIDE] = wts[2 * C::WARPS * G + g];
+        slot[g * C::PSTRIDE + 1] = lsum;
+      }
     }
     __syncthreads();
     const int64_t c0 = cta_of(seg_first + (int64_t)h * items, total, nstream);

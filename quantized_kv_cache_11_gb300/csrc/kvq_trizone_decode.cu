@@ -24,9 +24,10 @@
 //   accumulator per class brought to unit scale per row, and the zero points
 //   through one constant product per k-tile; masked tokens of a partial block
 //   get -inf.  Online softmax (exp2 domain).  P.V by value class: codes with
-//   B = fp16(p~ * scale), the accumulator rescaled by a power of two when the
-//   value width changes, and one constant product (zero points, the ones row =
-//   the denominator); or fp16 tiles whose words are the A fragments as stored.
+//   B = p~ * scale split into hi and lo fp16 columns (exact), the accumulator
+//   rescaled by a power of two when the value width changes, and one constant
+//   product (zero points, the ones row = the denominator); or fp16 tiles whose
+//   words are the A fragments as stored.
 // * Splits merge by log-sum-exp; the last CTA of a segment writes the output
 //   and resets the segment's counter.  No spin-wait on other CTAs.
 #include <cmath>
@@ -42,8 +43,10 @@ constexpr uint32_t kMaxPolls = 1u << 22;
 // Bit position of the codes that unpack8<BITS> puts in register 4 mt + i (row
 // half rh = i & 1; the same for both k-halves): the register holds the fp16
 // subnormals c * 2^(p - 24), so unit = 2^(24 - p) brings a product to unit scale.
+// p >= 2: a tensor-core dot product over subnormal operands at position p keeps
+// about 17 + p significant bits (measured on GB300), so p = 0 is avoided.
 __host__ __device__ constexpr int code_pos(int bits, int mt, int rh) {
-  return bits == 2 ? 4 * mt + 2 * rh : (bits == 4 ? 4 * rh : 0);
+  return 2 + (bits == 2 ? 4 * mt + 2 * rh : (bits == 4 ? 4 * rh : 0));
 }
 __host__ __device__ constexpr float code_unit(int bits, int mt, int rh) {
   return (float)(1 << (24 - code_pos(bits, mt, rh)));
@@ -179,30 +182,30 @@ struct Decoder {
     return h2_as_u32(__hfma2(x, y, __hmul2_rn(hi, u32_as_h2(nhl))));
   }
 
-  // Operands of the 8 pairs in w[0 .. BITS/2): one mask per register leaves a
-  // code pair in mantissa bits [p, p + BITS) of the two halves, exponent 0 (one
-  // shift right by 8 per word at 2 and 4 bits, per second pair at 8 bits).
+  // Operands of the 8 pairs in w[0 .. BITS/2): one mask per register, on the
+  // word shifted left by 2 or right by 6, leaves a code pair in mantissa bits
+  // [p, p + BITS) of the two halves, exponent 0.
   template <int BITS>
   static __device__ __forceinline__ void unpack8(const uint32_t* w, uint32_t (&a)[8]) {
     if (BITS == 2) {
-      const uint32_t x = w[0], y = x >> 8;
-      a[0] = x & 0x00030003u;  a[1] = x & 0x000C000Cu;  a[2] = y & 0x00030003u;  a[3] = y & 0x000C000Cu;
-      a[4] = x & 0x00300030u;  a[5] = x & 0x00C000C0u;  a[6] = y & 0x00300030u;  a[7] = y & 0x00C000C0u;
+      const uint32_t w0 = w[0], x = w0 << 2, y = w0 >> 6;
+      a[0] = x & 0x000C000Cu;  a[1] = x & 0x00300030u;  a[2] = y & 0x000C000Cu;  a[3] = y & 0x00300030u;
+      a[4] = x & 0x00C000C0u;  a[5] = x & 0x03000300u;  a[6] = y & 0x00C000C0u;  a[7] = y & 0x03000300u;
     } else if (BITS == 4) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t x = w[h], y = x >> 8;
-        a[4 * h + 0] = x & 0x000F000Fu;
-        a[4 * h + 1] = x & 0x00F000F0u;
-        a[4 * h + 2] = y & 0x000F000Fu;
-        a[4 * h + 3] = y & 0x00F000F0u;
+        const uint32_t w0 = w[h], x = w0 << 2, y = w0 >> 6;
+        a[4 * h + 0] = x & 0x003C003Cu;
+        a[4 * h + 1] = x & 0x03C003C0u;
+        a[4 * h + 2] = y & 0x003C003Cu;
+        a[4 * h + 3] = y & 0x03C003C0u;
       }
     } else {
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const uint32_t x = w[h];
-        a[2 * h + 0] = x & 0x00FF00FFu;
-        a[2 * h + 1] = (x >> 8) & 0x00FF00FFu;
+        a[2 * h + 0] = (x << 2) & 0x03FC03FCu;
+        a[2 * h + 1] = (x >> 6) & 0x03FC03FCu;
       }
     }
   }
@@ -304,8 +307,10 @@ struct Decoder {
     __syncwarp();
   }
 
-  // p~ pairs of column 8nt + gid (head 4nt + gid/2); zero in the lo columns (odd gid).
-  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2]) const {
+  // p~ pairs of column 8nt + gid (head 4nt + gid/2).  with_lo: the lo columns
+  // (odd gid) hold p~ too (code blocks split p~ * scale into hi and lo columns);
+  // otherwise zero (fp16 values multiply p~ itself, exact in one column).
+  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2], bool with_lo) const {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int g = 4 * nt + (gid >> 1);
@@ -314,8 +319,9 @@ struct Decoder {
 #pragma unroll
         for (int r = 0; r < 2; ++r)
           pp[nt][kt][r] =
-              (g < G && !(gid & 1)) ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r)
-                                    : 0u;
+              (g < G && (with_lo || !(gid & 1)))
+                  ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r)
+                  : 0u;
     }
   }
 
@@ -354,8 +360,8 @@ struct Decoder {
         uint32_t b[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          b[nt][0] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][0]), u32_as_h2(vs0)));
-          b[nt][1] = h2_as_u32(__hmul2(u32_as_h2(pv[nt][kt][1]), u32_as_h2(vs1)));
+          b[nt][0] = split_mul(pv[nt][kt][0], vs0);
+          b[nt][1] = split_mul(pv[nt][kt][1], vs1);
         }
 #pragma unroll
         for (int mi = 0; mi < 2; ++mi) {
@@ -441,7 +447,7 @@ struct Decoder {
     }
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
-    load_pp(ps, pp);
+    load_pp(ps, pp, kind < 3);
     const uint8_t* vt = rec + key_bytes(kt2, kt4, kt8);
     if (kind == 0) pv_codes<0>(vt, pp, zrow);
     else if (kind == 1) pv_codes<1>(vt, pp, zrow);
@@ -485,7 +491,7 @@ struct Decoder {
           lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? sacc[mt][nt][2 * r] * scale_log2 : -INFINITY;
     softmax(lg, ps);
     uint32_t pp[NT][2][2];
-    load_pp(ps, pp);
+    load_pp(ps, pp, false);
     pv_fp16(rec + kFp16TileBytes, pp);
     __syncwarp();
   }
@@ -506,8 +512,8 @@ struct Decoder {
         if (gid == 0) { d[0] = m[nt]; d[1] = lt; }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          d[4 + 16 * mt + gid] = o[mt][nt][0] + zs[mt / 2];
-          d[4 + 16 * mt + gid + 8] = o[mt][nt][2] + zs[mt / 2];
+          d[4 + 16 * mt + gid] = (o[mt][nt][0] + o[mt][nt][1]) + zs[mt / 2];
+          d[4 + 16 * mt + gid + 8] = (o[mt][nt][2] + o[mt][nt][3]) + zs[mt / 2];
         }
       }
     }
@@ -736,8 +742,8 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
             fifo[slot * 2 + 1] = (k << 24) | blk;
             fence_proxy_async();
             mbar_arrive_expect_tx(bars + slot, (uint32_t)size);
-            tma_load_1d(ring + off, p.blocks + (size_t)s * p.region + s_hdr[H_OFF + k] + (size_t)blk * size,
-                        (uint32_t)size, bars + slot);
+            tma_load_1d_hint(ring + off, p.blocks + (size_t)s * p.region + s_hdr[H_OFF + k] + (size_t)blk * size,
+                             (uint32_t)size, bars + slot, l2_evict_first_policy());
           }
           __syncwarp();
           wr = off + size;
