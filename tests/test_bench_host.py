@@ -53,10 +53,11 @@ def test_rdkv_flops_by_hand():
 
 def test_traffic_record_requires_the_measured_source():
     sha = bench._kernel_sha()
-    rec = bench.read_traffic("decode_traffic.txt", S.LLAMA31_8B_128K.name, sha)
+    name = f"decode_traffic_{S.LLAMA31_8B_128K.name}.txt"
+    rec = bench.read_traffic(name, S.LLAMA31_8B_128K.name, sha)
     assert rec is None or rec > bench.algorithmic_bytes(S.LLAMA31_8B_128K, 131008, 64)
-    assert bench.read_traffic("decode_traffic.txt", S.LLAMA31_8B_128K.name, "0" * 16) is None
-    assert bench.read_traffic("decode_traffic.txt", "another_workload", sha) is None
+    assert bench.read_traffic(name, S.LLAMA31_8B_128K.name, "0" * 16) is None
+    assert bench.read_traffic(name, "another_workload", sha) is None
     assert bench.read_traffic("no_such_record.txt", S.LLAMA31_8B_128K.name, sha) is None
 
 
