@@ -62,18 +62,30 @@ __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
 // and its low mantissa bits are that number.
 constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
 constexpr uint32_t kRoundMagicBits = 0x4B400000u;
-// The code clamped to [0, cmax] (cmax = 2^b - 1).
-__device__ __forceinline__ uint32_t quant_code_levels(float x, const GroupParams& p, uint32_t cmax) {
-  if (p.scale == 0.f) return 0u;
+// The code clamped to [0, cmax] (cmax = 2^b - 1) from y = fl(d * inv), and
+// whether y lies in the window near a half-integer where the exact quotient must
+// decide.  No branch: a zero scale has inv = 0, so y = 0 and the code is 0.
+__device__ __forceinline__ uint32_t quant_code_fast(float x, const GroupParams& p, uint32_t cmax, bool& near_tie) {
   const float d = __fsub_rn(x, p.zero);  // >= 0
-  float q = __fmul_rn(d, p.inv);
-  float t = __fadd_rn(q, kRoundMagic);
-  if (fabsf(__fsub_rn(q, __fsub_rn(t, kRoundMagic))) > 0.5f - 0x1p-11f) {
-    q = __fdiv_rn(d, p.scale);  // near a tie: the exact quotient decides
-    t = __fadd_rn(q, kRoundMagic);
-  }
+  const float q = __fmul_rn(d, p.inv);
+  const float t = __fadd_rn(q, kRoundMagic);
+  near_tie = fabsf(__fsub_rn(q, __fsub_rn(t, kRoundMagic))) > 0.5f - 0x1p-11f;
   const uint32_t c = __float_as_uint(t) - kRoundMagicBits;
   return c > cmax ? cmax : c;
+}
+
+// The code from the exactly rounded quotient fl(d / scale).
+__device__ __forceinline__ uint32_t quant_code_exact(float x, float scale, float zero, uint32_t cmax) {
+  if (scale == 0.f) return 0u;
+  const float q = __fdiv_rn(__fsub_rn(x, zero), scale);
+  const uint32_t c = __float_as_uint(__fadd_rn(q, kRoundMagic)) - kRoundMagicBits;
+  return c > cmax ? cmax : c;
+}
+
+__device__ __forceinline__ uint32_t quant_code_levels(float x, const GroupParams& p, uint32_t cmax) {
+  bool near_tie;
+  const uint32_t c = quant_code_fast(x, p, cmax, near_tie);
+  return near_tie ? quant_code_exact(x, p.scale, p.zero, cmax) : c;
 }
 
 template <int BITS>

@@ -95,17 +95,34 @@ __device__ __forceinline__ void quantize_tile_staged(const __half* ksrc, const _
       km[c0 + j] = gp[j].scale_h;
       km[D + c0 + j] = gp[j].zero_h;
     }
+    constexpr uint32_t cmax = (1u << BITS) - 1u;
+    // codes without a branch; bit t of `redo`: a code of token t lies near a
+    // rounding tie, and the token's codes are redone with the exact quotient
+    uint32_t redo = 0u;
 #pragma unroll 4
     for (int t = 0; t < kGroup; ++t) {
       uint32_t w = 0u;
+      bool near = false;
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
         const __half2 x = *reinterpret_cast<const __half2*>(kr + t * S::PH + c0 + 2 * j);
-        w |= quant_code<BITS>(__low2float(x), gp[2 * j]) << (16 * j);
-        w |= quant_code<BITS>(__high2float(x), gp[2 * j + 1]) << (16 * j + 8);
+        bool n0, n1;
+        w |= quant_code_fast(__low2float(x), gp[2 * j], cmax, n0) << (16 * j);
+        w |= quant_code_fast(__high2float(x), gp[2 * j + 1], cmax, n1) << (16 * j + 8);
+        near = near || n0 || n1;
       }
+      redo |= (uint32_t)near << t;
       if (CPL == 4) *reinterpret_cast<uint32_t*>(ct + t * S::PC + c0) = w;
       else *reinterpret_cast<uint16_t*>(ct + t * S::PC + c0) = (uint16_t)w;
+    }
+#pragma unroll 1
+    while (redo != 0u) {
+      const int t = __ffs(redo) - 1;
+      redo &= redo - 1u;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j)
+        ct[t * S::PC + c0 + j] = (uint8_t)quant_code_exact(__half2float(kr[t * S::PH + c0 + j]), gp[j].scale,
+                                                           gp[j].zero, cmax);
     }
   }
   __syncwarp();
@@ -133,13 +150,28 @@ __device__ __forceinline__ void quantize_tile_staged(const __half* ksrc, const _
                                                 fmaxf(__low2float(mx), __high2float(mx)));
       vm[j * kGroup + t] = gp.scale_h;
       vm[D + j * kGroup + t] = gp.zero_h;
+      constexpr uint32_t cmax = (1u << BITS) - 1u;
+      // bit w4 of `redo`: one of the four codes of word w4 lies near a rounding
+      // tie; those words are redone with the exact quotient
+      uint32_t redo = 0u;
 #pragma unroll
       for (int w4 = 0; w4 < 8; ++w4) {
-        const uint32_t c0 = quant_code<BITS>(__low2float(h[2 * w4]), gp);
-        const uint32_t c1 = quant_code<BITS>(__high2float(h[2 * w4]), gp);
-        const uint32_t c2 = quant_code<BITS>(__low2float(h[2 * w4 + 1]), gp);
-        const uint32_t c3 = quant_code<BITS>(__high2float(h[2 * w4 + 1]), gp);
+        bool n0, n1, n2, n3;
+        const uint32_t c0 = quant_code_fast(__low2float(h[2 * w4]), gp, cmax, n0);
+        const uint32_t c1 = quant_code_fast(__high2float(h[2 * w4]), gp, cmax, n1);
+        const uint32_t c2 = quant_code_fast(__low2float(h[2 * w4 + 1]), gp, cmax, n2);
+        const uint32_t c3 = quant_code_fast(__high2float(h[2 * w4 + 1]), gp, cmax, n3);
+        redo |= (uint32_t)(n0 || n1 || n2 || n3) << w4;
         *reinterpret_cast<uint32_t*>(ct + t * S::PC + 32 * j + 4 * w4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      }
+#pragma unroll 1
+      while (redo != 0u) {
+        const int w4 = __ffs(redo) - 1;
+        redo &= redo - 1u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          ct[t * S::PC + 32 * j + 4 * w4 + e] =
+              (uint8_t)quant_code_exact(__half2float(vr[t * S::PH + 32 * j + 4 * w4 + e]), gp.scale, gp.zero, cmax);
       }
     }
   }
