@@ -303,15 +303,24 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, int32_t n_q_heads, con
  * rotated to its own position, as for kvq_decode_attn.  head_dim 128 only.
  *
  * kvq_rope_table_bytes -- bytes of the cos/sin table of a cache geometry: 64 +
- *   ceil((sink_cap + 32 max_groups + tail_cap) / 32) rows of D/2 float2.
- * kvq_rope_table -- fills that table on `stream` (float64 angles and sin/cos,
- *   stored float32): row o < 64 holds (cos, sin)(o theta_i), row 64 + m holds
- *   (cos, sin)(32 m theta_i), theta_i = base^(-2i/D).  base > 1.  Build it once
- *   per (geometry, base); table 16-byte aligned, device memory, caller-owned.
+ *   ceil((sink_cap + 32 max_groups + tail_cap) / 32) rows of D/2 float2, then
+ *   58,240 bytes of fp16 pieces (56 rows of 1,040 bytes).
+ * kvq_rope_table -- fills that table on `stream` (float64 angles and sin/cos):
+ *   row o < 64 holds float32 (cos, sin)(o theta_i), row 64 + m holds float32
+ *   (cos, sin)(32 m theta_i), theta_i = base^(-2i/D); the piece part holds
+ *   cos/sin(o theta_i), o < 64, split into an fp16 hi piece of at most
+ *   11 - bits significant bits and the fp16 of the rest, in the order the
+ *   decode loads them (it depends on the cache's bits).  base > 1.  Build it
+ *   once per (geometry, bits, base); table 16-byte aligned, device memory,
+ *   caller-owned.
  * kvq_decode_attn_rope -- kvq_decode_attn over a cache of pre-RoPE keys, with
- *   the table of kvq_rope_table for this cache's geometry.  The K side runs in
- *   float32 on CUDA cores (the rotation depends on the token, so Q.K^T is no
- *   longer one matrix product); P.V and the merge are those of kvq_decode_attn.
+ *   the table of kvq_rope_table for this cache.  The rotation depends on the
+ *   token, so Q.K^T is no longer one matrix product.  At 2 and 4 bits the query
+ *   is turned back by the angle of each 32-position block and every code is
+ *   multiplied, exactly in fp16, by the hi and lo pieces of the cos and sin of
+ *   its offset inside the block before the tensor-core products; at 8 bits the
+ *   keys are rotated in float32 on CUDA cores.  P.V and the merge are those of
+ *   kvq_decode_attn.
  *   workspace: at least kvq_decode_workspace_bytes bytes, zero-filled before
  *   first use, left zero-filled.  Errors as kvq_decode_attn.
  */

@@ -51,6 +51,18 @@ constexpr uint32_t kMaxPolls = 1u << 22;
 // Several smaller CTAs per SM suit caches of many short (sequence, KV head)
 // segments: each CTA then holds about one segment piece, and the pieces' set-up
 // and merges overlap on the SM instead of running one after another.
+// Pre-RoPE decode at 2 and 4 bits: the part of the kvq_rope_table table that
+// holds the cos/sin of the offsets o within a 32-token block as fp16 pieces
+// (hi: at most 11 - b significant bits, so that a b-bit code times it is exact
+// in fp16; lo: the fp16 of the rest), in the order the tensor-core K side loads
+// them.  Row o (< 56) holds, for k-tile kt, lane column tig and piece (hi, lo),
+// 16 bytes: half2 (cos, sin) at (o, pair 8kt+tig), (o+8, that pair), (o, pair
+// 8kt+tig+4), (o+8, that pair): the mma A quad of token rows o, o+8.  Rows are
+// padded by 16 bytes (conflict-free 16-byte loads across a warp's 8 rows).
+constexpr int kRopeTrigRows = 56;
+constexpr int kRopeTrigRow = 8 * 4 * 2 * 16 + 16;
+constexpr int kRopeTrigBytes = kRopeTrigRows * kRopeTrigRow;
+
 template <int D, int BITS, int G, bool ROPE = false, int CPS = 1>
 struct DecodeCfg {
   using T = Tile<D, BITS>;
@@ -74,11 +86,14 @@ struct DecodeCfg {
   static constexpr int NWL = T::kWordsPerLane;
   static constexpr int PPW = T::kPairsPerWord;
   // 16 warps per SM for 2- and 4-bit codes, as one CTA (fewer split-K partials
-  // per segment) or as CPS CTAs of 16 / CPS warps (12 warps at 4 bits with ROPE:
-  // its stage ring, offset table and fp32 q must fit)
+  // per segment) or as CPS CTAs of 16 / CPS warps (12 warps with ROPE: its stage
+  // ring, offset piece table and fp32 q must fit)
   static_assert(CPS == 1 || (!ROPE && BITS != 8), "several CTAs per SM only without RoPE, at 2 and 4 bits");
-  static constexpr int WARPS = BITS == 8 ? 4 : (ROPE && BITS == 4 ? 12 : 16 / CPS);
-  static constexpr int NSTAGE = BITS == 2 ? (ROPE ? 3 : 2) : (BITS == 4 ? 2 : 3);
+  static constexpr int WARPS = BITS == 8 ? 4 : (ROPE ? 12 : 16 / CPS);
+  static constexpr int NSTAGE = BITS == 8 || (ROPE && BITS == 2) ? 3 : 2;
+  // ROPE at 2 and 4 bits: the rotated keys' products on tensor cores (pieces of
+  // the offsets' cos/sin in shared memory); at 8 bits on CUDA cores
+  static constexpr bool RTC = ROPE && BITS != 8;
   // q pairs held in registers (one n-tile) instead of re-read from shared memory
   static constexpr bool QREG = false;
   static constexpr int MIN_CTAS = CPS;
@@ -90,7 +105,8 @@ struct DecodeCfg {
   static constexpr int PREFIX = ((KVQ_MAX_BATCH + 1) * 4 + 15) / 16 * 16;
   static constexpr int QS = NT * 4 * (D / 2) * 4;     // q pairs of the segment's heads, lane order
   static constexpr int MBAR = (WARPS * NSTAGE + 1) * 8;  // one mbarrier per stage + the merge's
-  static constexpr int INTRA = ROPE ? 64 * (D / 2) * 8 : 0;  // cos/sin of offsets 0..63 within a block
+  // cos/sin of the offsets 0..63 within a block: fp16 pieces (RTC) or fp32
+  static constexpr int INTRA = ROPE ? (RTC ? kRopeTrigBytes : 64 * (D / 2) * 8) : 0;
   static constexpr int QF = ROPE ? NT * 4 * D * 4 : 0;         // fp32 q of the segment's heads
   static constexpr int SMEM = RING + PS + ZERO + PREFIX + QS + INTRA + QF + MBAR;
   static_assert(SMEM <= 232448, "fits the shared memory of one CTA");
@@ -121,6 +137,7 @@ struct DecodeParams {
   int32_t* error_flags;
   const __half* q;
   const float2* rope;  // ROPE: the table of kvq_rope_table (rows 0..63 offsets, 64 + m position blocks)
+  const uint8_t* rope_trig;  // ROPE at 2 and 4 bits: its fp16 piece part (kRopeTrigBytes)
   float* out;
   int32_t* counters;
   float* part;
@@ -205,7 +222,8 @@ struct Decoder {
   uint32_t ones_a;         // the ones row (row 12) of the value-constant MMA: lanes gid 4
   int lane, gid, tig, hl;
   const float* qf;         // ROPE: fp32 q [4 NT heads][D] in shared memory
-  const float2* intra;     // ROPE: cos/sin(o theta_i) [64 offsets o][D/2] in shared memory
+  const float2* intra;     // ROPE: cos/sin(o theta_i) [64 offsets o][D/2] (fp32)
+  const uint8_t* trig;     // RTC: the fp16 pieces of the offsets' cos/sin in shared memory
 
   // q_smem: the segment's q pairs in lane order ([4 NT heads][D/2] words)
   __device__ __forceinline__ void init(const uint32_t* q_smem) {
@@ -285,6 +303,105 @@ struct Decoder {
           for (int g = 1; g < GP; ++g) v = (g == 4 * nt + tig) ? acc[2 * mt + r][g] : v;
           lg[nt][mt][r] = v * scale_log2;
         }
+  }
+
+  // The lane's B value of a head from the fp32 pair (v0, v1): fp16(v) in the hi
+  // column, fp16(v - fp16(v)) in the lo column (hlf = 0 or 1).
+  static __device__ __forceinline__ uint32_t piece(float v0, float v1, float hlf) {
+    const __half2 h = __floats2half2_rn(v0, v1);
+    const float2 hf = __half22float2(h);
+    return h2_as_u32(__floats2half2_rn(fmaf(-hlf, hf.x, v0), fmaf(-hlf, hf.y, v1)));
+  }
+
+  // K-side logits of one pre-RoPE group on tensor cores (RTC).  The group's
+  // tokens sit at positions 32 m + o, o = roff + row; with beta_i = 32 m theta_i
+  // and alpha_i = o theta_i, the rotated key pair (R(alpha + beta) k).q equals
+  // (R(alpha) k).q~ with q~ = R(-beta) q, that is
+  //   cos(alpha) (k0 q~0 + k1 q~1) + sin(alpha) (k0 q~1 - k1 q~0),  k = s c + z.
+  // Codes: registers c 2^p (normal fp16) times the hi and lo pieces of cos and
+  // sin(alpha) from the piece table (hi products exact: the hi piece has at most
+  // 11 - BITS bits), against B = (s0 q~0, s1 q~1) and (s0 q~1, -s1 q~0); zero
+  // points: the pieces themselves as the A quad, against (z.q~, z x q~).  B
+  // values in hi/lo columns as elsewhere.  kw: the lane's code words; km: the
+  // group's key metadata (lane order); base: cos/sin(beta_i) [D/2].
+  __device__ __forceinline__ void rope_tc_logits(const uint32_t* kw, const uint32_t* km, const float2* base,
+                                                 int roff, float scale_log2, float (&lg)[NT][2][2]) const {
+    float acc[2][NT][4], zac[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][nt][i] = zac[mt][nt][i] = 0.f;
+    const float hlf = hl ? 1.f : 0.f;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      const int i0 = 8 * kt + tig, i1 = i0 + 4;
+      // (zero, scale) of channels 2 i0, 2 i0 + 1, then of 2 i1, 2 i1 + 1
+      const uint4 mv = *reinterpret_cast<const uint4*>(km + 16 * kt + 4 * tig);
+      const float2 z0 = __half22float2(u32_as_h2(mv.x)), s0 = __half22float2(u32_as_h2(mv.y));
+      const float2 z1 = __half22float2(u32_as_h2(mv.z)), s1 = __half22float2(u32_as_h2(mv.w));
+      const float2 b0 = base[i0], b1 = base[i1];
+      uint32_t bc[NT][2], bs[NT][2], bz[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int g = 4 * nt + (gid >> 1);
+        if (G % 4 == 0 || g < G) {
+          const float2 qa = *reinterpret_cast<const float2*>(qf + g * D + 2 * i0);
+          const float2 qb = *reinterpret_cast<const float2*>(qf + g * D + 2 * i1);
+          const float ta0 = fmaf(b0.x, qa.x, b0.y * qa.y), ta1 = fmaf(b0.x, qa.y, -b0.y * qa.x);
+          const float tb0 = fmaf(b1.x, qb.x, b1.y * qb.y), tb1 = fmaf(b1.x, qb.y, -b1.y * qb.x);
+          bc[nt][0] = piece(s0.x * ta0, s0.y * ta1, hlf);
+          bc[nt][1] = piece(s1.x * tb0, s1.y * tb1, hlf);
+          bs[nt][0] = piece(s0.x * ta1, -s0.y * ta0, hlf);
+          bs[nt][1] = piece(s1.x * tb1, -s1.y * tb0, hlf);
+          bz[nt][0] = piece(fmaf(z0.x, ta0, z0.y * ta1), fmaf(z0.x, ta1, -z0.y * ta0), hlf);
+          bz[nt][1] = piece(fmaf(z1.x, tb0, z1.y * tb1), fmaf(z1.x, tb1, -z1.y * tb0), hlf);
+        } else {
+          bc[nt][0] = bc[nt][1] = bs[nt][0] = bs[nt][1] = bz[nt][0] = bz[nt][1] = 0u;
+        }
+      }
+      // the codes as normal fp16 values c 2^p: exponent field of 1024 OR-ed in, 1024 taken off
+      uint32_t a[8];
+      unpack8(kw, 8 * kt, a);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        a[e] = h2_as_u32(__hsub2(u32_as_h2(a[e] | 0x64006400u), u32_as_h2(0x64006400u)));
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint8_t* row = trig + (roff + 16 * mt + gid) * kRopeTrigRow + (kt * 4 + tig) * 32;
+        const uint4 th = *reinterpret_cast<const uint4*>(row);
+        const uint4 tl = *reinterpret_cast<const uint4*>(row + 16);
+        const uint32_t x[4] = {a[4 * mt], a[4 * mt + 1], a[4 * mt + 2], a[4 * mt + 3]};
+        const uint32_t thv[4] = {th.x, th.y, th.z, th.w}, tlv[4] = {tl.x, tl.y, tl.z, tl.w};
+        uint32_t ach[4], acl[4], ash[4], asl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half2 xe = u32_as_h2(x[e]), h = u32_as_h2(thv[e]), l = u32_as_h2(tlv[e]);
+          ach[e] = h2_as_u32(__hmul2(xe, __low2half2(h)));
+          ash[e] = h2_as_u32(__hmul2(xe, __high2half2(h)));
+          acl[e] = h2_as_u32(__hmul2(xe, __low2half2(l)));
+          asl[e] = h2_as_u32(__hmul2(xe, __high2half2(l)));
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_16816(acc[mt][nt], ach, bc[nt][0], bc[nt][1]);
+          mma_16816(acc[mt][nt], acl, bc[nt][0], bc[nt][1]);
+          mma_16816(acc[mt][nt], ash, bs[nt][0], bs[nt][1]);
+          mma_16816(acc[mt][nt], asl, bs[nt][0], bs[nt][1]);
+          mma_16816(zac[mt][nt], thv, bz[nt][0], bz[nt][1]);
+          mma_16816(zac[mt][nt], tlv, bz[nt][0], bz[nt][1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          lg[nt][mt][r] = scale_log2 * fmaf(acc[mt][nt][2 * r] + acc[mt][nt][2 * r + 1],
+                                            1.f / (float)(1 << pos(mt, r)), zac[mt][nt][2 * r] + zac[mt][nt][2 * r + 1]);
   }
 
   // q pairs (kt, r) and (kt + 1, r) of this lane's column in n-tile nt (kt even)
@@ -474,7 +591,9 @@ struct Decoder {
     // scales (f = 1) of channels 16kt + 2tig + 8r and +1
     const uint32_t* km = reinterpret_cast<const uint32_t*>(km8);
     float lg[NT][2][2];
-    if constexpr (ROPE) {
+    if constexpr (C::RTC) {
+      rope_tc_logits(kw, km, reinterpret_cast<const float2*>(base), roff, scale_log2, lg);
+    } else if constexpr (ROPE) {
       // the codes dequantized in fp32: pair P = 8kt + 4mt + (r + 2h) of word P / PPW
       auto keys = [&](int kt, int h, float2 (&k)[4]) {
         const int w = 16 * kt + 4 * tig + 2 * h;
@@ -916,7 +1035,8 @@ decode_kernel(const DecodeParams p) {
     if (threadIdx.x == 0) {
       fence_proxy_async();
       mbar_arrive_expect_tx(merge_bar, C::INTRA);
-      tma_load_1d(intra_s, p.rope, C::INTRA, merge_bar);
+      tma_load_1d(intra_s, C::RTC ? static_cast<const void*>(p.rope_trig) : static_cast<const void*>(p.rope),
+                  C::INTRA, merge_bar);
     }
     if (!mbar_wait(merge_bar, 0, kMaxPolls)) failed = true;
     merge_parity = 1;
@@ -994,7 +1114,10 @@ decode_kernel(const DecodeParams p) {
       __syncthreads();
       dec.init(q_smem);
       dec.qf = qf_s;
-      dec.intra = intra_s;
+      // RTC: the fp16 pieces in shared memory; the fp32 rows (tail and sink
+      // chunks) read from the table in global memory
+      dec.intra = C::RTC ? p.rope : intra_s;
+      dec.trig = reinterpret_cast<const uint8_t*>(intra_s);
       for (int i = 0; i < nst; ++i) {
         if (i + C::NSTAGE - 1 < nst) { issue(i + C::NSTAGE - 1, (i + C::NSTAGE - 1) % C::NSTAGE); ++issued; }
         const int slotn = i % C::NSTAGE;

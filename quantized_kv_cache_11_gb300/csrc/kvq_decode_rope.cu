@@ -2,12 +2,15 @@
 // ihal.it, paragraph 7 and the closing paragraph: quantize the keys before the
 // rotary position embedding, rotate them after dequantization).
 //
-// The kernels are the uniform decode's (kvq_decode_impl.cuh) with ROPE set: a
-// lane dequantizes its key code pairs in fp32 (each packed pair is one rotation
-// pair, channels 2i and 2i+1), turns them by the angle of the token's position
-// and forms the dot products with the G query heads on CUDA cores; the angle of
-// position 32 m + o comes from two table rows by the angle-sum formulas: row
-// 64 + m (staged with the group by TMA) and row o (in shared memory, 64 rows).
+// The kernels are the uniform decode's (kvq_decode_impl.cuh) with ROPE set.  At
+// 2 and 4 bits the rotated keys' products run on tensor cores: the query is
+// turned back by the angle of the group's 32-position block (table row 64 + m,
+// staged with the group by TMA) and each code is multiplied, exactly in fp16, by
+// pieces of the cos/sin of its offset inside the block (the fp16 piece part of
+// the table, in shared memory).  At 8 bits, and for the fp16 tail and sink
+// chunks, a lane rotates its key pairs in fp32 and forms the dot products on
+// CUDA cores, the angle of position 32 m + o from rows 64 + m and o by the
+// angle-sum formulas.
 #include "kvq_decode_impl.cuh"
 
 namespace kvq {
@@ -28,6 +31,35 @@ __global__ void rope_table_kernel(float2* table, int half, int rows, double base
   table[idx] = make_float2((float)c, (float)s);
 }
 
+// x rounded to nearest with at most hb significant bits (float64).
+__device__ inline double round_bits(double x, int hb) {
+  if (x == 0.0) return 0.0;
+  int e;
+  const double m = frexp(x, &e);  // x = m 2^e, 0.5 <= |m| < 1
+  return ldexp(rint(ldexp(m, hb)), e - hb);
+}
+
+// The fp16 piece part (layout of kRopeTrigRow): one thread per half2 slot.
+__global__ void rope_trig_kernel(uint8_t* trig, int half, double base, int hb) {
+  constexpr int kSlots = kRopeTrigRows * 8 * 4 * 2 * 4;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= kSlots) return;
+  const int e = idx & 3, pc = (idx >> 2) & 1, tig = (idx >> 3) & 3, kt = (idx >> 5) & 7, o = idx >> 8;
+  const int i = 8 * kt + tig + 4 * (e >> 1);  // pair
+  const int row = o + 8 * (e & 1);            // offset
+  const double theta = pow(base, -2.0 * i / (2.0 * half));
+  double sn, cs;
+  sincos((double)row * theta, &sn, &cs);
+  const double ch = (double)__double2half(round_bits(cs, hb)), sh = (double)__double2half(round_bits(sn, hb));
+  const __half2 v = pc == 0 ? __halves2half2(__double2half(ch), __double2half(sh))
+                            : __halves2half2(__double2half(cs - ch), __double2half(sn - sh));
+  *reinterpret_cast<__half2*>(trig + o * kRopeTrigRow + ((kt * 4 + tig) * 2 + pc) * 16 + 4 * e) = v;
+}
+
+inline size_t rope_trig_offset(const kvq_cache* c) {
+  return (size_t)(64 + rope_blocks(c)) * (c->head_dim / 2) * sizeof(float2);
+}
+
 }  // namespace kvq
 
 extern "C" kvq_status kvq_rope_table_bytes(const kvq_cache* c, size_t* bytes) {
@@ -36,7 +68,7 @@ extern "C" kvq_status kvq_rope_table_bytes(const kvq_cache* c, size_t* bytes) {
   if (s != KVQ_OK) return s;
   if (bytes == nullptr) return KVQ_ERR_INVALID;
   if (c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
-  *bytes = (size_t)(64 + rope_blocks(c)) * (c->head_dim / 2) * sizeof(float2);
+  *bytes = rope_trig_offset(c) + kRopeTrigBytes;
   return KVQ_OK;
 }
 
@@ -48,8 +80,13 @@ extern "C" kvq_status kvq_rope_table(const kvq_cache* c, float base, float* tabl
   if (table == nullptr || !aligned(table, 16) || !(base > 1.f) || !std::isfinite(base)) return KVQ_ERR_INVALID;
   const int rows = 64 + rope_blocks(c), half = c->head_dim / 2;
   const int64_t n = (int64_t)rows * half;
-  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<float2*>(table), half, rows, (double)base);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(reinterpret_cast<float2*>(table), half, rows,
+                                                                (double)base);
+  uint8_t* trig = reinterpret_cast<uint8_t*>(table) + rope_trig_offset(c);
+  if (cudaMemsetAsync(trig, 0, kRopeTrigBytes, st) != cudaSuccess) return KVQ_ERR_CUDA;  // row padding
+  constexpr int kSlots = kRopeTrigRows * 8 * 4 * 2 * 4;
+  rope_trig_kernel<<<(kSlots + 255) / 256, 256, 0, st>>>(trig, half, (double)base, 11 - c->bits);
   return launch_status();
 }
 
@@ -78,7 +115,8 @@ extern "C" kvq_status kvq_decode_attn_rope(const kvq_cache* c, int32_t n_q_heads
   if (err || n == 0) return KVQ_ERR_CUDA;
   const DecodeLayout L = decode_layout(c, G, n);
   if (workspace_bytes < L.total) return KVQ_ERR_INVALID;
-  const DecodeParams p = decode_params(c, q, out, sm_scale, static_cast<uint8_t*>(workspace), L, table);
+  DecodeParams p = decode_params(c, q, out, sm_scale, static_cast<uint8_t*>(workspace), L, table);
+  p.rope_trig = reinterpret_cast<const uint8_t*>(table) + rope_trig_offset(c);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->bits == 2) return decode_dispatch_g<128, 2, true>(G, p, st);
   if (c->bits == 4) return decode_dispatch_g<128, 4, true>(G, p, st);

@@ -258,10 +258,13 @@ def test_rope_table_bytes_and_validation(lib):
     d = kvq.kvq_cache(1, 8, 128, 2, 131072 // 32, 64)
     out = ctypes.c_size_t()
     assert lib.kvq_rope_table_bytes(ctypes.byref(d), ctypes.byref(out)) == kvq.KVQ_OK
-    assert out.value == (64 + (131072 + 64) // 32) * 64 * 8     # 64 offset rows + position blocks
+    # 64 fp32 offset rows + position blocks, then the fp16 piece part: 56 offset
+    # rows of 8 k-tiles x 4 lane columns x 2 pieces x 16 bytes, + 16 bytes of padding
+    pieces = 56 * (8 * 4 * 2 * 16 + 16)
+    assert out.value == (64 + (131072 + 64) // 32) * 64 * 8 + pieces
     d.sink_cap = 5
     assert lib.kvq_rope_table_bytes(ctypes.byref(d), ctypes.byref(out)) == kvq.KVQ_OK
-    assert out.value == (64 + -(-(5 + 131072 + 64) // 32)) * 64 * 8
+    assert out.value == (64 + -(-(5 + 131072 + 64) // 32)) * 64 * 8 + pieces
     d64 = kvq.kvq_cache(1, 8, 64, 2, 128, 64)
     assert lib.kvq_rope_table_bytes(ctypes.byref(d64), ctypes.byref(out)) == kvq.KVQ_ERR_UNSUPPORTED
     assert lib.kvq_rope_table(ctypes.byref(d), ctypes.c_float(1.0), 0x100000, None) == kvq.KVQ_ERR_INVALID
