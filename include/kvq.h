@@ -308,7 +308,7 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, int32_t n_q_heads, con
  * kvq_rope_table -- fills that table on `stream` (float64 angles and sin/cos):
  *   row o < 64 holds float32 (cos, sin)(o theta_i), row 64 + m holds float32
  *   (cos, sin)(32 m theta_i), theta_i = base^(-2i/D); the piece part holds
- *   cos/sin(o theta_i), o < 64, split into an fp16 hi piece of at most
+ *   2^14 cos/sin(o theta_i), o < 64, split into an fp16 hi piece of at most
  *   11 - bits significant bits and the fp16 of the rest, in the order the
  *   decode loads them (it depends on the cache's bits).  base > 1.  Build it
  *   once per (geometry, bits, base); table 16-byte aligned, device memory,

@@ -53,9 +53,9 @@ constexpr uint32_t kMaxPolls = 1u << 22;
 // and merges overlap on the SM instead of running one after another.
 // Pre-RoPE decode at 2 and 4 bits: the part of the kvq_rope_table table that
 // holds the cos/sin of the offsets o within a 32-token block as fp16 pieces
-// (hi: at most 11 - b significant bits, so that a b-bit code times it is exact
-// in fp16; lo: the fp16 of the rest), in the order the tensor-core K side loads
-// them.  Row o (< 56) holds, for k-tile kt, lane column tig and piece (hi, lo),
+// times 2^14 (hi: at most 11 - b significant bits, so that a b-bit code times it
+// is exact in fp16; lo: the fp16 of the rest), in the order the tensor-core K
+// side loads them.  Row o (< 56) holds, for k-tile kt, lane column tig and piece (hi, lo),
 // 16 bytes: half2 (cos, sin) at (o, pair 8kt+tig), (o+8, that pair), (o, pair
 // 8kt+tig+4), (o+8, that pair): the mma A quad of token rows o, o+8.  Rows are
 // padded by 16 bytes (conflict-free 16-byte loads across a warp's 8 rows).
@@ -318,10 +318,10 @@ struct Decoder {
   // and alpha_i = o theta_i, the rotated key pair (R(alpha + beta) k).q equals
   // (R(alpha) k).q~ with q~ = R(-beta) q, that is
   //   cos(alpha) (k0 q~0 + k1 q~1) + sin(alpha) (k0 q~1 - k1 q~0),  k = s c + z.
-  // Codes: registers c 2^p (normal fp16) times the hi and lo pieces of cos and
-  // sin(alpha) from the piece table (hi products exact: the hi piece has at most
-  // 11 - BITS bits), against B = (s0 q~0, s1 q~1) and (s0 q~1, -s1 q~0); zero
-  // points: the pieces themselves as the A quad, against (z.q~, z x q~).  B
+  // Codes: registers c 2^(p - 24) times the hi and lo pieces (times 2^14) of cos
+  // and sin(alpha) from the piece table (hi products exact: the hi piece has at
+  // most 11 - BITS bits), against B = (s0 q~0, s1 q~1) and (s0 q~1, -s1 q~0);
+  // zero points: the pieces themselves as the A quad, against (z.q~, z x q~).  B
   // values in hi/lo columns as elsewhere.  kw: the lane's code words; km: the
   // group's key metadata (lane order); base: cos/sin(beta_i) [D/2].
   __device__ __forceinline__ void rope_tc_logits(const uint32_t* kw, const uint32_t* km, const float2* base,
@@ -361,12 +361,12 @@ struct Decoder {
           bc[nt][0] = bc[nt][1] = bs[nt][0] = bs[nt][1] = bz[nt][0] = bz[nt][1] = 0u;
         }
       }
-      // the codes as normal fp16 values c 2^p: exponent field of 1024 OR-ed in, 1024 taken off
+      // the codes as in the plain decode, fp16 subnormals c 2^(p - 24); the pieces
+      // are stored times 2^14, so the products c t 2^(p - 10) are normal fp16 and
+      // exact (except for |c t| < 2^-4, where the subnormal grid of 2^-24 bounds
+      // the absolute error by 2^-25 in those units)
       uint32_t a[8];
       unpack8(kw, 8 * kt, a);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        a[e] = h2_as_u32(__hsub2(u32_as_h2(a[e] | 0x64006400u), u32_as_h2(0x64006400u)));
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const uint8_t* row = trig + (roff + 16 * mt + gid) * kRopeTrigRow + (kt * 4 + tig) * 32;
@@ -401,7 +401,8 @@ struct Decoder {
 #pragma unroll
         for (int r = 0; r < 2; ++r)
           lg[nt][mt][r] = scale_log2 * fmaf(acc[mt][nt][2 * r] + acc[mt][nt][2 * r + 1],
-                                            1.f / (float)(1 << pos(mt, r)), zac[mt][nt][2 * r] + zac[mt][nt][2 * r + 1]);
+                                            (float)(1 << 10) / (float)(1 << pos(mt, r)),
+                                            (zac[mt][nt][2 * r] + zac[mt][nt][2 * r + 1]) * 0x1p-14f);
   }
 
   // q pairs (kt, r) and (kt + 1, r) of this lane's column in n-tile nt (kt even)

@@ -50,9 +50,11 @@ __global__ void rope_trig_kernel(uint8_t* trig, int half, double base, int hb) {
   const double theta = pow(base, -2.0 * i / (2.0 * half));
   double sn, cs;
   sincos((double)row * theta, &sn, &cs);
-  const double ch = (double)__double2half(round_bits(cs, hb)), sh = (double)__double2half(round_bits(sn, hb));
+  // pieces times 2^14 (exact power-of-two scaling; |hi| <= 2^14)
+  const double ch = (double)__double2half(ldexp(round_bits(cs, hb), 14));
+  const double sh = (double)__double2half(ldexp(round_bits(sn, hb), 14));
   const __half2 v = pc == 0 ? __halves2half2(__double2half(ch), __double2half(sh))
-                            : __halves2half2(__double2half(cs - ch), __double2half(sn - sh));
+                            : __halves2half2(__double2half(ldexp(cs, 14) - ch), __double2half(ldexp(sn, 14) - sh));
   *reinterpret_cast<__half2*>(trig + o * kRopeTrigRow + ((kt * 4 + tig) * 2 + pc) * 16 + 4 * e) = v;
 }
 
