@@ -305,12 +305,19 @@ struct Decoder {
         }
   }
 
-  // The lane's B value of a head from the fp32 pair (v0, v1): fp16(v) in the hi
-  // column, fp16(v - fp16(v)) in the lo column (hlf = 0 or 1).
-  static __device__ __forceinline__ uint32_t piece(float v0, float v1, float hlf) {
+  // B registers of pairs i0 (r0) and i1 = i0 + 4 (r1) from the fp32 pair (v0, v1)
+  // of this lane's own pair (i0 in the hi column's lane, i1 in the lo column's):
+  // the hi column takes fp16(v), the lo column fp16(v - fp16(v)); each lane keeps
+  // the piece of its own column and passes the other to its partner (lane ^ 4,
+  // the other column of the same head).  hlf = 0 (hi) or 1 (lo).
+  __device__ __forceinline__ void exchange(float v0, float v1, float hlf, uint32_t& r0, uint32_t& r1) const {
     const __half2 h = __floats2half2_rn(v0, v1);
     const float2 hf = __half22float2(h);
-    return h2_as_u32(__floats2half2_rn(fmaf(-hlf, hf.x, v0), fmaf(-hlf, hf.y, v1)));
+    const uint32_t mine = h2_as_u32(__floats2half2_rn(fmaf(-hlf, hf.x, v0), fmaf(-hlf, hf.y, v1)));
+    const uint32_t send = h2_as_u32(__floats2half2_rn(fmaf(hlf - 1.f, hf.x, v0), fmaf(hlf - 1.f, hf.y, v1)));
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 4);
+    r0 = hl ? recv : mine;
+    r1 = hl ? mine : recv;
   }
 
   // K-side logits of one pre-RoPE group on tensor cores (RTC).  The group's
@@ -336,30 +343,22 @@ struct Decoder {
     const float hlf = hl ? 1.f : 0.f;
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt) {
-      const int i0 = 8 * kt + tig, i1 = i0 + 4;
-      // (zero, scale) of channels 2 i0, 2 i0 + 1, then of 2 i1, 2 i1 + 1
-      const uint4 mv = *reinterpret_cast<const uint4*>(km + 16 * kt + 4 * tig);
-      const float2 z0 = __half22float2(u32_as_h2(mv.x)), s0 = __half22float2(u32_as_h2(mv.y));
-      const float2 z1 = __half22float2(u32_as_h2(mv.z)), s1 = __half22float2(u32_as_h2(mv.w));
-      const float2 b0 = base[i0], b1 = base[i1];
+      // this lane's own pair: 8kt + tig in the hi column's lane, + 4 in the lo one's
+      const int ip = 8 * kt + tig + 4 * hl;
+      // (zero, scale) of channels 2 ip, 2 ip + 1 (the lane-order metadata quad holds
+      // those of pair 8kt + tig, then of pair 8kt + tig + 4)
+      const uint2 mv = *reinterpret_cast<const uint2*>(km + 16 * kt + 4 * tig + 2 * hl);
+      const float2 zz = __half22float2(u32_as_h2(mv.x)), ss = __half22float2(u32_as_h2(mv.y));
+      const float2 bb = base[ip];
       uint32_t bc[NT][2], bs[NT][2], bz[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const int g = 4 * nt + (gid >> 1);
-        if (G % 4 == 0 || g < G) {
-          const float2 qa = *reinterpret_cast<const float2*>(qf + g * D + 2 * i0);
-          const float2 qb = *reinterpret_cast<const float2*>(qf + g * D + 2 * i1);
-          const float ta0 = fmaf(b0.x, qa.x, b0.y * qa.y), ta1 = fmaf(b0.x, qa.y, -b0.y * qa.x);
-          const float tb0 = fmaf(b1.x, qb.x, b1.y * qb.y), tb1 = fmaf(b1.x, qb.y, -b1.y * qb.x);
-          bc[nt][0] = piece(s0.x * ta0, s0.y * ta1, hlf);
-          bc[nt][1] = piece(s1.x * tb0, s1.y * tb1, hlf);
-          bs[nt][0] = piece(s0.x * ta1, -s0.y * ta0, hlf);
-          bs[nt][1] = piece(s1.x * tb1, -s1.y * tb0, hlf);
-          bz[nt][0] = piece(fmaf(z0.x, ta0, z0.y * ta1), fmaf(z0.x, ta1, -z0.y * ta0), hlf);
-          bz[nt][1] = piece(fmaf(z1.x, tb0, z1.y * tb1), fmaf(z1.x, tb1, -z1.y * tb0), hlf);
-        } else {
-          bc[nt][0] = bc[nt][1] = bs[nt][0] = bs[nt][1] = bz[nt][0] = bz[nt][1] = 0u;
-        }
+        // head 4nt + gid/2 (heads past G have q = 0 in shared memory)
+        const float2 qa = *reinterpret_cast<const float2*>(qf + (4 * nt + (gid >> 1)) * D + 2 * ip);
+        const float t0 = fmaf(bb.x, qa.x, bb.y * qa.y), t1 = fmaf(bb.x, qa.y, -bb.y * qa.x);
+        exchange(ss.x * t0, ss.y * t1, hlf, bc[nt][0], bc[nt][1]);
+        exchange(ss.x * t1, -ss.y * t0, hlf, bs[nt][0], bs[nt][1]);
+        exchange(fmaf(zz.x, t0, zz.y * t1), fmaf(zz.x, t1, -zz.y * t0), hlf, bz[nt][0], bz[nt][1]);
       }
       // the codes as in the plain decode, fp16 subnormals c 2^(p - 24); the pieces
       // are stored times 2^14, so the products c t 2^(p - 10) are normal fp16 and
