@@ -676,8 +676,13 @@ def main():
     peak, peak_kind = load_peaks()
     nbytes = algorithmic_bytes(w, n_quant, n_tail, n_sink)
     achieved = nbytes / (us_step * 1e-6) / 1e9
-    traffic = None if (args.sink or args.rope) else read_traffic(f"decode_traffic_{w.name}.txt", w.name,
-                                                                  _kernel_sha())
+    if args.sink:
+        traffic = None
+    elif args.rope:
+        traffic = read_traffic(f"decode_traffic_{w.name}_prerope.txt", w.name + "_prerope",
+                               _kernel_sha(ROPE_FILES))
+    else:
+        traffic = read_traffic(f"decode_traffic_{w.name}.txt", w.name, _kernel_sha())
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False,
@@ -1164,8 +1169,11 @@ def run_reference_rdkv(args):
     }), flush=True)
 
 
-def _kernel_sha(files=("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_decode_cps2.cu", "kvq_decode_cps4.cu",
-                        "kvq_common.cuh")) -> str:
+DECODE_FILES = ("kvq_decode_impl.cuh", "kvq_decode.cu", "kvq_decode_cps2.cu", "kvq_decode_cps4.cu", "kvq_common.cuh")
+ROPE_FILES = ("kvq_decode_impl.cuh", "kvq_decode_rope.cu", "kvq_common.cuh")
+
+
+def _kernel_sha(files=DECODE_FILES) -> str:
     """Hash of the kernel's code: the sources with comments and whitespace removed,
     so that a traffic record stays tied to the code it was measured on."""
     import hashlib
