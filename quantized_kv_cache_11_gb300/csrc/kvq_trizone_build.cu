@@ -286,8 +286,23 @@ __device__ __forceinline__ void quantize_values(const __half* rows, int n, uint8
     g.scale = __half2float(vm[j * kGroup + t]);
     g.zero = __half2float(vm[kDim + j * kGroup + t]);
     g.inv = vinv[j * kGroup + t];
+    // the four codes without a branch, then the exact quotient for all four in the
+    // rare case that one of them lies near a rounding tie
+    constexpr uint32_t cmax = (1u << C) - 1u;
+    uint32_t c[4];
+    bool near = false;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ct[t * kDim + c0 + i] = t < n ? (uint8_t)quant_code<C>(x[i], g) : (uint8_t)0;
+    for (int i = 0; i < 4; ++i) {
+      bool ni;
+      c[i] = quant_code_fast(x[i], g, cmax, ni);
+      near = near || ni;
+    }
+    if (near) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = quant_code_exact(x[i], g.scale, g.zero, cmax);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ct[t * kDim + c0 + i] = t < n ? (uint8_t)c[i] : (uint8_t)0;
   }
   __syncwarp();
 }
@@ -322,8 +337,20 @@ __device__ __forceinline__ void key_channels(const __half* rows, int n, int d0, 
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + d0);
     const float x[4] = {__low2float(u32_as_h2(raw.x)), __high2float(u32_as_h2(raw.x)), __low2float(u32_as_h2(raw.y)),
                         __high2float(u32_as_h2(raw.y))};
+    uint32_t c[4];
+    bool near = false;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ct[t * kSlots + slot[i]] = (uint8_t)quant_code_levels(x[i], g[i], cmax[i]);
+    for (int i = 0; i < 4; ++i) {
+      bool ni;
+      c[i] = quant_code_fast(x[i], g[i], cmax[i], ni);
+      near = near || ni;
+    }
+    if (near) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = quant_code_exact(x[i], g[i].scale, g[i].zero, cmax[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ct[t * kSlots + slot[i]] = (uint8_t)c[i];
   }
 }
 
