@@ -1192,35 +1192,34 @@ decode_kernel(const DecodeParams p) {
     // warp partial into the warp's (now idle) ring slice, then the CTA merge
     dec.write_partial(reinterpret_cast<float*>(wring));
     __syncthreads();
-    // the warps' weights once per (warp, head), then the output elements
-    float* wts = reinterpret_cast<float*>(ps_all);  // [WARPS][G] weights, [WARPS][G] weight x l
-    if (threadIdx.x < C::WARPS * G) {
-      const int w = threadIdx.x / G, g = threadIdx.x % G;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int w2 = 0; w2 < C::WARPS; ++w2)
-        mx = fmaxf(mx, reinterpret_cast<const float*>(ring + w2 * C::NSTAGE * C::STAGE)[g * C::PSTRIDE]);
-      const float* src = reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE) + g * C::PSTRIDE;
-      const float wt = mx == -INFINITY ? 0.f : fast_exp2(src[0] - mx);
-      wts[w * G + g] = wt;
-      wts[C::WARPS * G + w * G + g] = wt * src[1];
-      if (w == 0) wts[2 * C::WARPS * G + g] = mx;
-    }
-    __syncthreads();
+    // the CTA merge: each warp takes chunks of 32 output elements (one head each);
+    // lanes w < WARPS load warp w's (m, l) of that head, the weights are formed in
+    // registers and broadcast by shuffles (no shared-memory round trip, one barrier)
     float* slot = p.part + (size_t)(c + seg) * G * C::PSTRIDE;
-    for (int e2 = threadIdx.x; e2 < G * D; e2 += blockDim.x) {
-      const int g = e2 / D, d = e2 % D;
+    static_assert(C::WARPS <= 32 && D % 32 == 0, "a warp's lanes hold the warps' weights");
+    for (int ch = warp; ch < G * D / 32; ch += C::WARPS) {
+      const int g = ch * 32 / D, d = ch * 32 % D + lane;
+      float mw = -INFINITY, lw = 0.f;
+      if (lane < C::WARPS) {
+        const float* src = reinterpret_cast<const float*>(ring + lane * C::NSTAGE * C::STAGE) + g * C::PSTRIDE;
+        mw = src[0];
+        lw = src[1];
+      }
+      float mx = mw;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float wt = (lane < C::WARPS && mx != -INFINITY) ? fast_exp2(mw - mx) : 0.f;
+      float lsum = wt * lw;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
       float osum = 0.f;
 #pragma unroll
       for (int w = 0; w < C::WARPS; ++w)
-        osum = fmaf(wts[w * G + g],
+        osum = fmaf(__shfl_sync(0xffffffffu, wt, w),
                     reinterpret_cast<const float*>(ring + w * C::NSTAGE * C::STAGE)[g * C::PSTRIDE + 4 + d], osum);
       slot[g * C::PSTRIDE + 4 + d] = osum;
       if (d == 0) {
-        float lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::WARPS; ++w) lsum += wts[C::WARPS * G + w * G + g];
-        slot[g * C::PSTRIDE] = wts[2 * C::WARPS * G + g];
+        slot[g * C::PSTRIDE] = mx;
         slot[g * C::PSTRIDE + 1] = lsum;
       }
     }
