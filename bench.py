@@ -463,6 +463,25 @@ def time_graph(launch, n_rep, steps_wanted, world, local):
     return elapsed_ms * 1000.0 / steps, steps, clk.summary()
 
 
+def time_single(launch, n_rep, n=64):
+    """Median (and 10th / 90th percentile) of n separately timed launches, each
+    bracketed by its own CUDA events on the current stream, eager (no graph),
+    rotating the replicas; microseconds."""
+    import torch
+    for i in range(3):
+        launch(i)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(ev):
+        a.record()
+        launch(i)
+        b.record()
+    torch.cuda.synchronize()
+    t = np.array([a.elapsed_time(b) * 1000.0 for a, b in ev])
+    return {"median_us": float(np.median(t)), "p10_us": float(np.percentile(t, 10)),
+            "p90_us": float(np.percentile(t, 90)), "launches": n}
+
+
 def max_over_ranks(value: float, device) -> float:
     """The largest of the ranks' values (every rank gets it); the value itself
     when there is one rank.  Each rank runs its own replica of the workload, so
@@ -661,6 +680,7 @@ def main():
         parity = {"kv_heads_checked": 1, "max_abs": float(np.abs(got - ref).max())}
     us_step, steps, clocks = time_graph(
         lambda i: dec(caches[i % n_rep], q, outs[i % n_rep]), n_rep, args.steps, world, local)
+    single = time_single(lambda i: dec(caches[i % n_rep], q, outs[i % n_rep]), n_rep)
 
     # ---- end to end through the public API: pinned host q in, fp32 output out
     q_host = torch.from_numpy(inp["q"]).pin_memory()
@@ -699,7 +719,7 @@ def main():
                 "d2h_bytes_per_step": out_host.numel() * 4},
         "gpu_launches": steps,
         "clocks": clocks,
-        "path": {"decode_us": us_step, "prefill_us": prefill_us,
+        "path": {"decode_us": us_step, "decode_per_launch": single, "prefill_us": prefill_us,
                  "prefill_gbs": prefill_bytes / (prefill_us * 1e-6) / 1e9, "append_us": append_us},
         "parity_sample": parity,
     }
@@ -826,6 +846,7 @@ def main_trizone(args):
     us_step, steps, clocks = time_graph(
         lambda i: caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep]),
         n_rep, args.steps, world, local)
+    single = time_single(lambda i: caches[i % n_rep].decode(q, w.sm_scale, out=outs[i % n_rep]), n_rep)
     q_host = torch.from_numpy(inp["q"]).pin_memory()
     out_host = torch.empty(B, w.n_q_heads, w.head_dim, dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(q)
@@ -859,7 +880,7 @@ def main_trizone(args):
                 "d2h_bytes_per_step": out_host.numel() * 4},
         "gpu_launches": steps,
         "clocks": clocks,
-        "path": {"decode_us": us_step, "build_us": build_us,
+        "path": {"decode_us": us_step, "decode_per_launch": single, "build_us": build_us,
                  "build_gbs": build_bytes / (build_us * 1e-6) / 1e9},
         "parity_sample": parity,
     }
