@@ -82,17 +82,6 @@ __device__ __forceinline__ uint32_t quant_code_exact(float x, float scale, float
   return c > cmax ? cmax : c;
 }
 
-__device__ __forceinline__ uint32_t quant_code_levels(float x, const GroupParams& p, uint32_t cmax) {
-  bool near_tie;
-  const uint32_t c = quant_code_fast(x, p, cmax, near_tie);
-  return near_tie ? quant_code_exact(x, p.scale, p.zero, cmax) : c;
-}
-
-template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float x, const GroupParams& p) {
-  return quant_code_levels(x, p, (1u << BITS) - 1);
-}
-
 // ---------------------------------------------------------------------------
 // Packed tile layout (see kvq.h).  Lane L (gid = L/4, tig = L%4) owns D/2 code
 // pairs; pair P lives in the lane's word P/(16/BITS), slot P%(16/BITS).

@@ -72,7 +72,7 @@ struct DecodeCfg {
   static constexpr int BASE = ROPE ? D / 2 * 8 : 0;  // cos/sin of the group's first position block
   // groups per stage: two consecutive groups of a segment are staged and decoded
   // together at 2 bits (one wait, one set of copies and one softmax maximum per
-  // 64 tokens, and one zero-point product serves both groups)
+  // 64 tokens)
   static constexpr int GPI = (BITS == 2 && !ROPE) ? 2 : 1;
   // stage layout: the key codes of its GPI groups, their value codes, their key
   // metadata, their value metadata (each array as consecutive groups, as in the
@@ -691,10 +691,10 @@ struct Decoder {
   }
 
   // Two consecutive quantized groups staged together (stage layout of DecodeCfg:
-  // GPI = 2), decoded as one 64-token chunk: one softmax maximum, one zero-point
-  // product per k-tile for both groups (rows gid: the first group's zero points,
-  // rows gid + 8: the second's), and the p~ of both turned into P.V operands in
-  // registers (movmatrix), without a shared-memory round trip.
+  // GPI = 2), decoded as one 64-token chunk: one softmax maximum, each group's
+  // zero-point product from its own 16-byte metadata load as it stands, and the
+  // p~ of both turned into P.V operands in registers (movmatrix), without a
+  // shared-memory round trip.
   __device__ __forceinline__ void quant_pair(const uint8_t* stage, const uint32_t* zrow, float scale_log2) {
     static_assert(C::GPI == 2 && !ROPE, "two-group stages");
     float lg[2][NT][2][2];
