@@ -119,17 +119,17 @@ __device__ __forceinline__ void value_pair_pos(int P, int gid, int tig, int& t, 
   t = 16 * kt + 2 * tig + 8 * (i >> 1);
 }
 
-// Pack a 32 x D tile of codes held in shared memory (ct[t * PITCH + c]) and store
-// it to global memory with one 16-byte store per lane per chunk (coalesced).
+// Pack chunk ch (the lane's words 4ch .. 4ch + 3) of a 32 x D tile of codes held
+// in shared memory (ct[t * PITCH + c]) and store it to global memory with one
+// 16-byte store (a warp's 32 lanes write 512 contiguous bytes).
 template <int D, int BITS, bool IS_KEY, int PITCH = D>
-__device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst, int lane) {
+__device__ __forceinline__ void pack_store_chunk(const uint8_t* ct, uint8_t* dst, int lane, int ch) {
   using T = Tile<D, BITS>;
   const int gid = lane >> 2, tig = lane & 3;
-  uint32_t w[T::kWordsPerLane];
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int i = 0; i < T::kWordsPerLane; ++i) w[i] = 0u;
-#pragma unroll
-  for (int P = 0; P < D / 2; ++P) {
+  for (int k4 = 0; k4 < 4 * T::kPairsPerWord; ++k4) {
+    const int P = ch * 4 * T::kPairsPerWord + k4;
     int t, c;
     uint32_t first, second;
     if (IS_KEY) {
@@ -142,14 +142,17 @@ __device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst,
       first = ct[t * PITCH + c];
       second = ct[(t + 1) * PITCH + c];
     }
-    const int wi = P / T::kPairsPerWord, k = P % T::kPairsPerWord;
-    w[wi] |= (first << slot_bitpos<BITS>(k)) | (second << (16 + slot_bitpos<BITS>(k)));
+    const int k = k4 % T::kPairsPerWord;
+    w[k4 / T::kPairsPerWord] |= (first << slot_bitpos<BITS>(k)) | (second << (16 + slot_bitpos<BITS>(k)));
   }
+  *reinterpret_cast<uint4*>(dst + (size_t)(ch * 32 + lane) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Pack a whole 32 x D tile (every chunk of the lane).
+template <int D, int BITS, bool IS_KEY, int PITCH = D>
+__device__ __forceinline__ void pack_store_tile(const uint8_t* ct, uint8_t* dst, int lane) {
 #pragma unroll
-  for (int ch = 0; ch < T::kChunksPerLane; ++ch) {
-    uint4 v = make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-    *reinterpret_cast<uint4*>(dst + (size_t)(ch * 32 + lane) * 16) = v;
-  }
+  for (int ch = 0; ch < Tile<D, BITS>::kChunksPerLane; ++ch) pack_store_chunk<D, BITS, IS_KEY, PITCH>(ct, dst, lane, ch);
 }
 
 // Metadata blocks are stored as fp16 pairs in "lane order" (see kvq.h): key

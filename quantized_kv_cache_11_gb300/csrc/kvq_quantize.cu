@@ -8,7 +8,9 @@
 namespace kvq {
 
 constexpr int kPrefillWarps = 4;
-constexpr int kAppendWarps = 8;
+// append: tile groups per block; a group of D/32 warps flushes one head's oldest
+// 32 tail tokens together (the flush is on the decode step's critical path)
+constexpr int kAppendGroups = 8;
 
 struct PrefillParams {
   const __half* k;
@@ -239,6 +241,111 @@ prefill_kernel(const __grid_constant__ PrefillParams p) {
   }
 }
 
+// The tile of quantize_tile_staged quantized by the D/32 warps of a group
+// together (wi: the warp's index in the group, bar: the group's named barrier):
+// keys one channel per thread; values the 32-channel group wi, one token per
+// lane; the packing split by 16-byte chunk.  The arithmetic is the same, so the
+// bytes are identical.  Every staged row has been read when it returns.
+template <int D, int BITS>
+__device__ __forceinline__ void quantize_tile_coop(const __half* ksrc, const __half* vsrc, int64_t tstride,
+                                                   uint8_t* kcodes_dst, __half* kmeta_dst, uint8_t* vcodes_dst,
+                                                   __half* vmeta_dst, uint8_t* ws, int wi, int lane, int bar) {
+  using S = StagedTile<D>;
+  using T = Tile<D, BITS>;
+  constexpr int W = D / 32, NTH = W * 32;
+  constexpr uint32_t cmax = (1u << BITS) - 1u;
+  __half* rows = reinterpret_cast<__half*>(ws);  // key rows, then value rows
+  uint8_t* ct = ws + S::ROWS;
+  __half* km = reinterpret_cast<__half*>(ws + S::ROWS + kGroup * S::PC);
+  __half* vm = km + 2 * D;
+  const int tid = wi * 32 + lane;
+  auto sync = [&]() { asm volatile("bar.sync %0, %1;\n" ::"r"(bar), "r"(NTH) : "memory"); };
+  auto stage = [&](const __half* src) {
+    constexpr int CPR = 2 * D / 16;  // 16-byte copies per row
+    for (int e = tid; e < kGroup * CPR; e += NTH) {
+      const int t = e / CPR, ch = e % CPR;
+      cp_async_16(rows + t * S::PH + ch * 8, src + (int64_t)t * tstride + ch * 8);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    sync();
+  };
+  stage(ksrc);
+  {  // keys: channel tid over the 32 tokens
+    const int c = tid;
+    __half mn = rows[c], mx = mn;
+#pragma unroll 8
+    for (int t = 1; t < kGroup; ++t) {
+      const __half x = rows[t * S::PH + c];
+      mn = __hmin(mn, x);
+      mx = __hmax(mx, x);
+    }
+    const GroupParams gp = group_params<BITS>(__half2float(mn), __half2float(mx));
+    km[c] = gp.scale_h;
+    km[D + c] = gp.zero_h;
+    uint32_t redo = 0u;  // bit t: the code of token t lies near a rounding tie
+#pragma unroll 8
+    for (int t = 0; t < kGroup; ++t) {
+      bool near;
+      ct[t * S::PC + c] = (uint8_t)quant_code_fast(__half2float(rows[t * S::PH + c]), gp, cmax, near);
+      redo |= (uint32_t)near << t;
+    }
+#pragma unroll 1
+    while (redo != 0u) {
+      const int t = __ffs(redo) - 1;
+      redo &= redo - 1u;
+      ct[t * S::PC + c] = (uint8_t)quant_code_exact(__half2float(rows[t * S::PH + c]), gp.scale, gp.zero, cmax);
+    }
+  }
+  sync();
+  for (int ch = wi; ch < T::kChunksPerLane; ch += W) pack_store_chunk<D, BITS, true, S::PC>(ct, kcodes_dst, lane, ch);
+  if (wi == W - 1) store_meta_lane_order<D, true>(km, kmeta_dst, lane);
+  sync();  // the rows and codes buffers are free again
+  stage(vsrc);
+  {  // values: group j = wi of token t = lane
+    const int t = lane, j = wi;
+    const uint4* row = reinterpret_cast<const uint4*>(rows + t * S::PH + 32 * j);
+    uint4 x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = row[i];
+    const __half2* h = reinterpret_cast<const __half2*>(x);
+    __half2 mn = h[0], mx = h[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+      mn = __hmin2(mn, h[i]);
+      mx = __hmax2(mx, h[i]);
+    }
+    const GroupParams gp = group_params<BITS>(fminf(__low2float(mn), __high2float(mn)),
+                                              fmaxf(__low2float(mx), __high2float(mx)));
+    vm[j * kGroup + t] = gp.scale_h;
+    vm[D + j * kGroup + t] = gp.zero_h;
+    uint32_t redo = 0u;  // bit w4: a code of word w4 lies near a rounding tie
+#pragma unroll
+    for (int w4 = 0; w4 < 8; ++w4) {
+      bool n0, n1, n2, n3;
+      const uint32_t c0 = quant_code_fast(__low2float(h[2 * w4]), gp, cmax, n0);
+      const uint32_t c1 = quant_code_fast(__high2float(h[2 * w4]), gp, cmax, n1);
+      const uint32_t c2 = quant_code_fast(__low2float(h[2 * w4 + 1]), gp, cmax, n2);
+      const uint32_t c3 = quant_code_fast(__high2float(h[2 * w4 + 1]), gp, cmax, n3);
+      redo |= (uint32_t)(n0 || n1 || n2 || n3) << w4;
+      *reinterpret_cast<uint32_t*>(ct + t * S::PC + 32 * j + 4 * w4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+    }
+#pragma unroll 1
+    while (redo != 0u) {
+      const int w4 = __ffs(redo) - 1;
+      redo &= redo - 1u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        ct[t * S::PC + 32 * j + 4 * w4 + e] =
+            (uint8_t)quant_code_exact(__half2float(rows[t * S::PH + 32 * j + 4 * w4 + e]), gp.scale, gp.zero, cmax);
+    }
+  }
+  sync();
+  for (int ch = wi; ch < T::kChunksPerLane; ch += W) pack_store_chunk<D, BITS, false, S::PC>(ct, vcodes_dst, lane, ch);
+  if (wi == W - 1) store_meta_lane_order<D, false>(vm, vmeta_dst, lane);
+  sync();  // the group's buffers may be reused
+}
+
 struct AppendParams {
   const __half* k_new;
   const __half* v_new;
@@ -259,10 +366,13 @@ struct AppendParams {
 };
 
 // grid (B); each block owns one sequence so the length update is race-free.
+// kAppendGroups groups of D/32 warps; group g handles heads g, g + kAppendGroups, ...
 template <int D, int BITS>
-__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendParams p) {
-  extern __shared__ __align__(16) uint8_t s_stage[];  // StagedTile<D>::BYTES per warp
+__global__ void __launch_bounds__(kAppendGroups * D) append_kernel(const AppendParams p) {
+  extern __shared__ __align__(16) uint8_t s_stage[];  // StagedTile<D>::BYTES per group
+  constexpr int W = D / 32, NWARPS = kAppendGroups * W;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / W, wi = warp % W;
   const int b = blockIdx.x;
   const int R = p.tail_cap;
   const int nq = p.n_quant[b], nt = p.n_tail[b], hd = p.tail_head[b];
@@ -275,7 +385,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
       return;
     }
     constexpr int CPL = D / 32;
-    for (int h = warp; h < p.hkv; h += kAppendWarps) {
+    for (int h = warp; h < p.hkv; h += NWARPS) {
       const size_t bh = (size_t)b * p.hkv + h;
       const size_t src = bh * D + lane * CPL, dst = (bh * p.sink_cap + ns) * D + lane * CPL;
       for (int i = 0; i < CPL; ++i) {
@@ -300,7 +410,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
   const int nt2 = flush ? nt - kGroup : nt;
   const int slot = (hd2 + nt2) % R;
   constexpr int CPL = D / 32;
-  for (int h = warp; h < p.hkv; h += kAppendWarps) {
+  for (int h = grp; h < p.hkv; h += kAppendGroups) {
     const size_t bh = (size_t)b * p.hkv + h;
     __half* kt = p.k_tail + bh * R * D;
     __half* vt = p.v_tail + bh * R * D;
@@ -309,10 +419,12 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(const AppendP
       // multiples of 32): contiguous, 16-byte aligned rows
       using T = Tile<D, BITS>;
       const size_t gi = bh * p.max_groups + nq / kGroup;
-      quantize_tile_staged<D, BITS, 16>(kt + (size_t)hd * D, vt + (size_t)hd * D, D, p.k_codes + gi * T::kBytes,
-                                        p.k_meta + gi * 2 * D, p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D,
-                                        s_stage + warp * StagedTile<D>::BYTES, lane);
+      quantize_tile_coop<D, BITS>(kt + (size_t)hd * D, vt + (size_t)hd * D, D, p.k_codes + gi * T::kBytes,
+                                  p.k_meta + gi * 2 * D, p.v_codes + gi * T::kBytes, p.v_meta + gi * 2 * D,
+                                  s_stage + grp * StagedTile<D>::BYTES, wi, lane, 1 + grp);
     }
+    // the new token (after a flush into slot hd, whose row the flush has read)
+    if (wi != 0) continue;
     const size_t src = bh * D + lane * CPL;
     const size_t dst = (size_t)slot * D + lane * CPL;
     if (CPL == 4) {
@@ -366,9 +478,9 @@ struct PrefillLaunch {
 template <int D, int BITS>
 struct AppendLaunch {
   static kvq_status run(const AppendParams& p, int batch, cudaStream_t s) {
-    constexpr int smem = kAppendWarps * StagedTile<D>::BYTES;
+    constexpr int smem = kAppendGroups * StagedTile<D>::BYTES;
     if (!device_smem_attr(reinterpret_cast<const void*>(append_kernel<D, BITS>), smem)) return KVQ_ERR_CUDA;
-    append_kernel<D, BITS><<<batch, kAppendWarps * 32, smem, s>>>(p);
+    append_kernel<D, BITS><<<batch, kAppendGroups * D, smem, s>>>(p);
     return launch_status();
   }
 };
