@@ -66,6 +66,7 @@ typedef enum {
 #define KVQ_DEVERR_APPEND_CAPACITY 1 /* append needed a flush but the quantized region was full */
 #define KVQ_DEVERR_BAD_LENGTHS 2     /* decode saw n_tail > tail_cap or n_quant beyond capacity */
 #define KVQ_DEVERR_TIMEOUT 4         /* a bounded wait for staged data gave up; output invalid */
+#define KVQ_DEVERR_BAD_TABLE 16      /* pre-RoPE decode: the table was built for another cache; output invalid */
 
 #define KVQ_GROUP 32
 #define KVQ_MAX_BATCH 512 /* sequences per prefill call */
@@ -320,14 +321,17 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, int32_t n_q_heads, con
  *   multiplied, exactly in fp16, by the hi and lo pieces of the cos and sin of
  *   its offset inside the block before the tensor-core products; at 8 bits the
  *   keys are rotated in float32 on CUDA cores.  P.V and the merge are those of
- *   kvq_decode_attn.
+ *   kvq_decode_attn.  table_bytes: the size of the table buffer, at least
+ *   kvq_rope_table_bytes for this cache (else KVQ_ERR_INVALID, before any
+ *   launch); a table built for a cache of another width (or geometry) sets
+ *   KVQ_DEVERR_BAD_TABLE in error_flags and the output is invalid.
  *   workspace: at least kvq_decode_workspace_bytes bytes, zero-filled before
  *   first use, left zero-filled.  Errors as kvq_decode_attn.
  */
 kvq_status kvq_rope_table_bytes(const kvq_cache* cache, size_t* bytes);
 kvq_status kvq_rope_table(const kvq_cache* cache, float base, float* table, void* stream);
 kvq_status kvq_decode_attn_rope(const kvq_cache* cache, int32_t n_q_heads, const void* q, float* out,
-                                float sm_scale, const float* table, void* workspace,
+                                float sm_scale, const float* table, size_t table_bytes, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
 /*

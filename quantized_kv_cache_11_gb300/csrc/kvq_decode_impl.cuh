@@ -62,6 +62,9 @@ constexpr uint32_t kMaxPolls = 1u << 22;
 constexpr int kRopeTrigRows = 56;
 constexpr int kRopeTrigRow = 8 * 4 * 2 * 16 + 16;
 constexpr int kRopeTrigBytes = kRopeTrigRows * kRopeTrigRow;
+// row 0's padding: a tag and the code width the pieces were cut for
+constexpr int kRopeTrigTagOffset = 8 * 4 * 2 * 16;
+constexpr uint32_t kRopeTrigTag = 0x5251564Bu;
 
 template <int D, int BITS, int G, bool ROPE = false, int CPS = 1>
 struct DecodeCfg {
@@ -1063,6 +1066,13 @@ decode_kernel(const DecodeParams p) {
     }
     if (!mbar_wait(merge_bar, 0, kMaxPolls)) failed = true;
     merge_parity = 1;
+    if constexpr (C::RTC) {
+      const uint32_t* tag = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(intra_s) +
+                                                              kRopeTrigTagOffset);
+      if (!failed && threadIdx.x == 0 && (tag[0] != kRopeTrigTag || tag[1] != (uint32_t)BITS) &&
+          p.error_flags != nullptr)
+        atomicOr(p.error_flags, KVQ_DEVERR_BAD_TABLE);
+    }
   }
   const int64_t total = (int64_t)p.hkv * s_pref[p.batch];
   const int64_t nstream = total < p.n_stream ? total : p.n_stream;

@@ -56,6 +56,11 @@ __global__ void rope_trig_kernel(uint8_t* trig, int half, double base, int hb) {
   const __half2 v = pc == 0 ? __halves2half2(__double2half(ch), __double2half(sh))
                             : __halves2half2(__double2half(ldexp(cs, 14) - ch), __double2half(ldexp(sn, 14) - sh));
   *reinterpret_cast<__half2*>(trig + o * kRopeTrigRow + ((kt * 4 + tig) * 2 + pc) * 16 + 4 * e) = v;
+  if (idx == 0) {  // the tag in row 0's padding: which code width the pieces were cut for
+    uint32_t* tag = reinterpret_cast<uint32_t*>(trig + kRopeTrigTagOffset);
+    tag[0] = kRopeTrigTag;
+    tag[1] = (uint32_t)(11 - hb);
+  }
 }
 
 inline size_t rope_trig_offset(const kvq_cache* c) {
@@ -93,8 +98,8 @@ extern "C" kvq_status kvq_rope_table(const kvq_cache* c, float base, float* tabl
 }
 
 extern "C" kvq_status kvq_decode_attn_rope(const kvq_cache* c, int32_t n_q_heads, const void* q, float* out,
-                                           float sm_scale, const float* table, void* workspace,
-                                           size_t workspace_bytes, void* stream) {
+                                           float sm_scale, const float* table, size_t table_bytes,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
   using namespace kvq;
   kvq_status s = validate_cache(c);
   if (s != KVQ_OK) return s;
@@ -106,6 +111,7 @@ extern "C" kvq_status kvq_decode_attn_rope(const kvq_cache* c, int32_t n_q_heads
   if (!aligned(q, 4) || !aligned(out, 16) || !aligned(workspace, 16) || !aligned(table, 16))
     return KVQ_ERR_INVALID;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return KVQ_ERR_INVALID;
+  if (table_bytes < rope_trig_offset(c) + kRopeTrigBytes) return KVQ_ERR_INVALID;
   int err = 0;
   int n = 0;
 #define KVQ_RSLOTS(B_, G_) \

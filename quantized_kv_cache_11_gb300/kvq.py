@@ -26,6 +26,7 @@ KVQ_ERR_CUDA = -4
 KVQ_DEVERR_APPEND_CAPACITY = 1
 KVQ_DEVERR_BAD_LENGTHS = 2
 KVQ_DEVERR_TIMEOUT = 4
+KVQ_DEVERR_BAD_TABLE = 16
 KVQ_GROUP = 32
 KVQ_MAX_BATCH = 512
 KVQ_NBUF = 9
@@ -133,7 +134,7 @@ def load_library() -> ctypes.CDLL:
     lib.kvq_decode_attn_static.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp]
     lib.kvq_rope_table_bytes.argtypes = [cache_p, P(c_sz)]
     lib.kvq_rope_table.argtypes = [cache_p, c_f, c_vp, c_vp]
-    lib.kvq_decode_attn_rope.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_vp, c_sz, c_vp]
+    lib.kvq_decode_attn_rope.argtypes = [cache_p, ctypes.c_int32, c_vp, c_vp, c_f, c_vp, c_sz, c_vp, c_sz, c_vp]
     lib.kvq_selftest_bounded_wait.argtypes = [c_vp, ctypes.c_uint32, ctypes.c_int32, c_vp]
     tz_p = P(kvq_trizone)
     lib.kvq_trizone_bytes.argtypes = [tz_p, P(c_sz)]
@@ -310,8 +311,8 @@ def kvq_decode_attn_rope(cache: "QuantizedKVCache", q: torch.Tensor, out: torch.
         raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
     _check_decode_args(cache, tuple(q.shape), tuple(out.shape))
     st = load_library().kvq_decode_attn_rope(ctypes.byref(cache.desc), q.shape[1], _ptr(q), _ptr(out),
-                                             float(sm_scale), _ptr(table), _ptr(workspace), workspace.numel(),
-                                             _stream(stream))
+                                             float(sm_scale), _ptr(table), table.numel() * 4, _ptr(workspace),
+                                             workspace.numel(), _stream(stream))
     _check("kvq_decode_attn_rope", st)
 
 

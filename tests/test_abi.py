@@ -271,6 +271,19 @@ def test_rope_table_bytes_and_validation(lib):
     assert lib.kvq_rope_table(ctypes.byref(d), ctypes.c_float(10000.0), 0x100008, None) == kvq.KVQ_ERR_INVALID
 
 
+def test_rope_decode_validation_fails_before_launch(lib):
+    d = _fake_cache()
+    need = ctypes.c_size_t()
+    assert lib.kvq_rope_table_bytes(ctypes.byref(d), ctypes.byref(need)) == kvq.KVQ_OK
+    dec = lambda tb, table=0x600000, hq=16: lib.kvq_decode_attn_rope(
+        ctypes.byref(d), hq, 0x200000, 0x300000, ctypes.c_float(0.088), table, tb, 0x400000, 1 << 30, None)
+    assert dec(need.value - 16) == kvq.KVQ_ERR_INVALID   # the table is too small for this cache
+    assert dec(0) == kvq.KVQ_ERR_INVALID
+    assert dec(need.value, table=0) == kvq.KVQ_ERR_INVALID
+    assert dec(need.value, table=0x600008) == kvq.KVQ_ERR_INVALID  # 16-byte aligned
+    assert dec(need.value, hq=6) == kvq.KVQ_ERR_INVALID
+
+
 def test_selftest_validation_fails_before_launch(lib):
     assert lib.kvq_selftest_bounded_wait(None, 16, 0, None) == kvq.KVQ_ERR_INVALID
     assert lib.kvq_selftest_bounded_wait(0x1002, 16, 0, None) == kvq.KVQ_ERR_INVALID  # misaligned

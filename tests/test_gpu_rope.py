@@ -9,6 +9,7 @@ import pytest
 import torch
 
 from oracle import kvq_oracle as O
+from quantized_kv_cache_11_gb300 import kvq
 from quantized_kv_cache_11_gb300 import synthetic as S
 from tests import helpers as H
 
@@ -80,3 +81,19 @@ def test_rope_after_appends():
     assert nq == 224 and nt == 46
     st = O.quantize_sequence(kk, vv, 270, nt, 2)
     _check(cache, inp, w, 2, 0, states=[st])
+
+
+def test_table_of_another_width_is_reported():
+    # the fp16 pieces are cut for the cache's code width: a table built for a
+    # 4-bit cache of the same geometry, used on a 2-bit cache, sets the device
+    # error bit (both tables have the same size, so every read stays in bounds)
+    w, bits, sink, inp = _inp("gqa4_2bit")
+    c2 = H.device_cache(w, inp, 2)
+    c4 = H.device_cache(w, inp, 4)
+    q = torch.from_numpy(inp["q"]).cuda()
+    c2.decode_rope(q, c2.rope_table(BASE), w.sm_scale)
+    assert c2.device_errors() == 0
+    t4 = c4.rope_table(BASE)
+    assert t4.numel() == c2.rope_table(BASE).numel()
+    c2.decode_rope(q, t4, w.sm_scale)
+    assert c2.device_errors() & kvq.KVQ_DEVERR_BAD_TABLE
