@@ -516,6 +516,35 @@ struct Decoder {
     }
   }
 
+  // Online softmax over one 32-token chunk, straight into the P.V B fragments
+  // (both columns of a head hold p~, as load_pp(.., true) gives): the p~ pairs of a
+  // lane's C-layout rows are transposed in registers (movmatrix), as for two-group
+  // stages, instead of a round trip through shared memory.
+  __device__ __forceinline__ void softmax_pp(const float (&lg)[NT][2][2], uint32_t (&pp)[NT][2][2]) {
+    bool need = false;
+    float mloc[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float mx = fmaxf(fmaxf(lg[nt][0][0], lg[nt][0][1]), fmaxf(lg[nt][1][0], lg[nt][1][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      mloc[nt] = mx;
+      need |= mx > m[nt] + kLazyRescale;
+    }
+    if (__any_sync(0xffffffffu, need)) rescale(mloc);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float pf = fast_exp2(lg[nt][mt][r] - m[nt]);
+          if (G % 4 != 0 && 4 * nt + tig >= G) pf = 0.f;
+          pp[nt][mt][r] = movmatrix_trans(h2_as_u32(__floats2half2_rn(pf, pf)));
+        }
+  }
+
   // P.V of one staged group (value codes vc, value metadata vm) with the B
   // fragments pp of its p~ (column 8nt+gid, tokens 16kt + 2tig + 8r, +1), into o
   // and zc.  At 2 bits the codes of tokens 16..31 sit 4 bits above those of
@@ -686,9 +715,8 @@ struct Decoder {
             lg[nt][mt][r] = fmaf(sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1], scale_log2 * unit(mt, r), zq);
       }
     }
-    softmax(lg, ps);
     uint32_t pp[NT][2][2];
-    load_pp(ps, pp, true);
+    softmax_pp(lg, pp);
     pv_group(vc, vm8, pp, zrow);
     __syncwarp();
   }
