@@ -663,10 +663,11 @@ struct Decoder {
         uint4 qv[NT];
   #pragma unroll
         for (int nt = 0; nt < NT; ++nt) qv[nt] = qpairs(nt, kt2);
-        // (measured: at 2 bits both k-tiles' loads up front and the whole quad as
-        // the operand run fastest; at 4 and 8 bits a load per k-tile with the scale
-        // rows zeroed, which keeps the kernel within 128 registers without spills)
-        constexpr bool kHoist = BITS == 2;
+        // (measured: at 2 and 4 bits both k-tiles' loads up front and the whole quad
+        // as the operand run fastest (4-bit 128k step 35.5 -> 35.0 us once p~ no
+        // longer went through shared memory); at 8 bits, with 4 warps per CTA and
+        // more registers per code word, a load per k-tile with the scale rows zeroed)
+        constexpr bool kHoist = BITS != 8;
         uint4 mvp[2];
         if (kHoist) {
           mvp[0] = *reinterpret_cast<const uint4*>(kmt + 16 * kt2);
