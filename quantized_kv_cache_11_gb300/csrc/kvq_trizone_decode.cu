@@ -66,10 +66,9 @@ struct Cfg {
   static constexpr int RING = 16384;  // bytes of a warp's byte ring (>= the largest record)
   static constexpr int NBAR = 4;      // copies in flight per warp, at most
   static constexpr int PSTRIDE = kDim + 4;
-  static constexpr int PSROW = 48;
   static constexpr int QPH = 88;  // words per head of the slot-ordered q (10 k-tiles x 8, + 8 pad)
   static constexpr int RINGS = WARPS * RING;
-  static constexpr int PS = WARPS * G * PSROW * 2;
+  static constexpr int PS = WARPS * G * 96;  // the final merge's weights, [MERGE_BATCH][G] floats
   static constexpr int ZERO = 4 * kDim;
   static constexpr int PREFIX = ((KVQ_TZ_MAX_SEGMENTS + 1) * 8 + 15) / 16 * 16;
   static constexpr int QP = 4 * NT * QPH * 4;
@@ -265,8 +264,12 @@ struct Decoder {
     ukind = k;
   }
 
-  // Online softmax over one 32-token block; writes p~ (fp16) to ps[g][t].
-  __device__ __forceinline__ void softmax(float (&lg)[NT][2][2], __half* ps) {
+  // Online softmax over one 32-token block, straight into the P.V B fragments of
+  // column 8nt + gid (head 4nt + gid/2): the p~ pairs of a lane's C-layout rows are
+  // transposed in registers (movmatrix).  with_lo: the lo columns (odd gid) hold p~
+  // too (code blocks split p~ * scale into hi and lo columns); otherwise zero (fp16
+  // values multiply p~ itself, exact in one column).
+  __device__ __forceinline__ void softmax_pp(const float (&lg)[NT][2][2], uint32_t (&pp)[NT][2][2], bool with_lo) {
     bool need = false;
     float mloc[NT];
 #pragma unroll
@@ -292,37 +295,18 @@ struct Decoder {
           for (int i = 0; i < 4; ++i) o[mt][nt][i] *= alpha;
       }
     }
+    const bool zero_lo = !with_lo && (gid & 1);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int g = 4 * nt + tig;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const __half2 ph = __floats2half2_rn(fast_exp2(lg[nt][mt][0] - m[nt]), fast_exp2(lg[nt][mt][1] - m[nt]));
-        if (g < G) {
-          ps[g * C::PSROW + 16 * mt + gid] = __low2half(ph);
-          ps[g * C::PSROW + 16 * mt + gid + 8] = __high2half(ph);
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float pf = fast_exp2(lg[nt][mt][r] - m[nt]);
+          if (G % 4 != 0 && 4 * nt + tig >= G) pf = 0.f;
+          const uint32_t t = movmatrix_trans(h2_as_u32(__floats2half2_rn(pf, pf)));
+          pp[nt][mt][r] = zero_lo ? 0u : t;
         }
-      }
-    }
-    __syncwarp();
-  }
-
-  // p~ pairs of column 8nt + gid (head 4nt + gid/2).  with_lo: the lo columns
-  // (odd gid) hold p~ too (code blocks split p~ * scale into hi and lo columns);
-  // otherwise zero (fp16 values multiply p~ itself, exact in one column).
-  __device__ __forceinline__ void load_pp(const __half* ps, uint32_t (&pp)[NT][2][2], bool with_lo) const {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int g = 4 * nt + (gid >> 1);
-#pragma unroll
-      for (int kt = 0; kt < 2; ++kt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-          pp[nt][kt][r] =
-              (g < G && (with_lo || !(gid & 1)))
-                  ? *reinterpret_cast<const uint32_t*>(ps + g * C::PSROW + 16 * kt + 2 * tig + 8 * r)
-                  : 0u;
-    }
   }
 
   // P.V over a value tile of codes (class VC: width 2 << VC) and its metadata.
@@ -403,7 +387,7 @@ struct Decoder {
   }
 
   // A block of zone A/B: keys quantized in three classes, values by kind.
-  __device__ __forceinline__ void quant_block(const uint8_t* rec, int kind, int nvalid, const int* hd, __half* ps,
+  __device__ __forceinline__ void quant_block(const uint8_t* rec, int kind, int nvalid, const int* hd,
                                               const uint32_t* zrow, float scale_log2) {
     const int kt2 = hd[H_KT], kt4 = hd[H_KT + 1], kt8 = hd[H_KT + 2], KT = kt2 + kt4 + kt8;
     const uint32_t* st = reinterpret_cast<const uint32_t*>(rec);
@@ -445,9 +429,8 @@ struct Decoder {
           lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? x : -INFINITY;
         }
     }
-    softmax(lg, ps);
     uint32_t pp[NT][2][2];
-    load_pp(ps, pp, kind < 3);
+    softmax_pp(lg, pp, kind < 3);
     const uint8_t* vt = rec + key_bytes(kt2, kt4, kt8);
     if (kind == 0) pv_codes<0>(vt, pp, zrow);
     else if (kind == 1) pv_codes<1>(vt, pp, zrow);
@@ -457,7 +440,7 @@ struct Decoder {
   }
 
   // A fresh block (zone C): fp16 key tile in natural channel order, fp16 values.
-  __device__ __forceinline__ void fresh_block(const uint8_t* rec, int nvalid, __half* ps, float scale_log2) {
+  __device__ __forceinline__ void fresh_block(const uint8_t* rec, int nvalid, float scale_log2) {
     set_units(3);  // fp16 values: unit 1, as zone B
     const uint4* s4 = reinterpret_cast<const uint4*>(rec);
     float sacc[2][NT][4];
@@ -489,9 +472,8 @@ struct Decoder {
 #pragma unroll
         for (int r = 0; r < 2; ++r)
           lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? sacc[mt][nt][2 * r] * scale_log2 : -INFINITY;
-    softmax(lg, ps);
     uint32_t pp[NT][2][2];
-    load_pp(ps, pp, false);
+    softmax_pp(lg, pp, false);
     pv_fp16(rec + kFp16TileBytes, pp);
     __syncwarp();
   }
@@ -600,7 +582,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
   __shared__ int s_lo[kKinds], s_cum[kKinds + 1];
   __shared__ float s_M[G], s_L[G], s_scale[G];
   uint8_t* rings = smem;
-  __half* ps_all = reinterpret_cast<__half*>(smem + C::RINGS);
+  float* s_wts = reinterpret_cast<float*>(smem + C::RINGS);  // the final merge's weights
   uint32_t* zrow = reinterpret_cast<uint32_t*>(smem + C::RINGS + C::PS);
   int64_t* s_pref = reinterpret_cast<int64_t*>(smem + C::RINGS + C::PS + C::ZERO);
   uint32_t* qp_smem = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(s_pref) + C::PREFIX);
@@ -613,7 +595,6 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
   uint64_t* bars = bars_all + warp * C::NBAR;
   uint64_t* merge_bar = bars_all + C::WARPS * C::NBAR;
   int* fifo = fifo_all + warp * C::NBAR * 2;  // per entry: ring offset, kind << 24 | block
-  __half* ps = ps_all + warp * G * C::PSROW;
   uint8_t* ring = rings + warp * C::RING;
 
   for (int i = tid; i < C::ZERO / 4; i += blockDim.x) zrow[i] = 0u;
@@ -759,8 +740,8 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
         const int k = kb >> 24, blk = kb & 0xFFFFFF;
         const int cnt = k < 4 ? s_hdr[H_NTOK + k] : s_hdr[H_NFRESH];
         const int nvalid = min(kGroup, cnt - kGroup * blk);
-        if (k < 4) dec.quant_block(ring + off, k, nvalid, s_hdr, ps, zrow, p.scale_log2);
-        else dec.fresh_block(ring + off, nvalid, ps, p.scale_log2);
+        if (k < 4) dec.quant_block(ring + off, k, nvalid, s_hdr, zrow, p.scale_log2);
+        else dec.fresh_block(ring + off, nvalid, p.scale_log2);
         ++done;
         fill();
       }
@@ -802,7 +783,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
     __syncthreads();
     if (s_last) {
       const bool ok = final_merge<G>(p.part + (size_t)(c0 + s) * G * C::PSTRIDE, nparts, p.out + (size_t)s * G * kDim,
-                                     rings, reinterpret_cast<float*>(ps_all), merge_bar, merge_parity, s_M, s_L,
+                                     rings, s_wts, merge_bar, merge_parity, s_M, s_L,
                                      s_scale);
       if (!ok && tid == 0 && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_TIMEOUT);
       if (tid == 0) p.counters[s] = 0;
