@@ -393,41 +393,59 @@ struct Decoder {
     const uint32_t* st = reinterpret_cast<const uint32_t*>(rec);
     const uint32_t* kmt = st + key_code_bytes(kt2, kt4, kt8) / 4 + 4 * tig;
     set_units(kind);
-    float sacc[3][2][2][NT][4];  // [key class][chain][mt]
+    // one accumulator set (two chains), reused by the three key classes: each class
+    // is folded into the logits at its own unit before the next one starts
+    float sacc[2][2][NT][4];  // [chain][mt]
     float cc[NT][4];
+    float lg[NT][2][2];
 #pragma unroll
-    for (int c = 0; c < 3; ++c)
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cc[nt][i] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) lg[nt][mt][r] = 0.f;
+    auto fold = [&](int c) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float sc = sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + sacc[1][mt][nt][2 * r] +
+                             sacc[1][mt][nt][2 * r + 1];
+            lg[nt][mt][r] = fmaf(sc, code_unit(2 << c, mt, r), lg[nt][mt][r]);
+          }
+    };
+    auto zero = [&]() {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) { sacc[c][h][0][nt][i] = 0.f; sacc[c][h][1][nt][i] = 0.f; }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) cc[nt][i] = 0.f;
+          for (int i = 0; i < 4; ++i) { sacc[h][0][nt][i] = 0.f; sacc[h][1][nt][i] = 0.f; }
+    };
     int kt = 0;
-    key_class<2>(st, kt2, kt, kmt, sacc[0], cc);
-    key_class<4>(st + 32 * kt2, kt4, kt, kmt, sacc[1], cc);
-    key_class<8>(st + 32 * kt2 + 64 * kt4, kt8, kt, kmt, sacc[2], cc);
-    float lg[NT][2][2];
+    zero();
+    key_class<2>(st, kt2, kt, kmt, sacc, cc);
+    fold(0);
+    zero();
+    key_class<4>(st + 32 * kt2, kt4, kt, kmt, sacc, cc);
+    fold(1);
+    zero();
+    key_class<8>(st + 32 * kt2 + 64 * kt4, kt8, kt, kmt, sacc, cc);
+    fold(2);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float zq = cc[nt][0] * scale_log2;  // q.z (every constant row holds the zero points)
+      const float zq = cc[nt][0];  // q.z (every constant row holds the zero points)
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float x = zq;
-#pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            const float sc = sacc[c][0][mt][nt][2 * r] + sacc[c][0][mt][nt][2 * r + 1] +
-                             sacc[c][1][mt][nt][2 * r] + sacc[c][1][mt][nt][2 * r + 1];
-            x = fmaf(sc, scale_log2 * code_unit(2 << c, mt, r), x);
-          }
-          lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? x : -INFINITY;
-        }
+        for (int r = 0; r < 2; ++r)
+          lg[nt][mt][r] = (16 * mt + gid + 8 * r) < nvalid ? (lg[nt][mt][r] + zq) * scale_log2 : -INFINITY;
     }
     uint32_t pp[NT][2][2];
     softmax_pp(lg, pp, kind < 3);
