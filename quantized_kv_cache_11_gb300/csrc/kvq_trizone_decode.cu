@@ -235,20 +235,11 @@ struct Decoder {
     }
   }
 
-  // All k-tiles of one key class into the class's accumulators; k-tiles
-  // alternate between two accumulation chains (shorter MMA dependency chains).
+  // All k-tiles of one key class into the accumulators (rows of m-tiles 0 and 1).
   template <int BITS>
   __device__ __forceinline__ void key_class(const uint32_t* sub, int ktc, int& kt, const uint32_t* kmt,
-                                            float (&sacc)[2][2][NT][4], float (&cc)[NT][4]) const {
-    int j = 0;
-    for (; j + 1 < ktc; j += 2, kt += 2) {
-      key_tile<BITS>(sub, j, kt, kmt, sacc[0][0], sacc[0][1], cc);
-      key_tile<BITS>(sub, j + 1, kt + 1, kmt, sacc[1][0], sacc[1][1], cc);
-    }
-    if (j < ktc) {
-      key_tile<BITS>(sub, j, kt, kmt, sacc[0][0], sacc[0][1], cc);
-      ++kt;
-    }
+                                            float (&sacc)[2][NT][4], float (&cc)[NT][4]) const {
+    for (int j = 0; j < ktc; ++j, ++kt) key_tile<BITS>(sub, j, kt, kmt, sacc[0], sacc[1], cc);
   }
 
   // Rescale o from the unit of value kind ukind to that of kind k (powers of two).
@@ -393,9 +384,9 @@ struct Decoder {
     const uint32_t* st = reinterpret_cast<const uint32_t*>(rec);
     const uint32_t* kmt = st + key_code_bytes(kt2, kt4, kt8) / 4 + 4 * tig;
     set_units(kind);
-    // one accumulator set (two chains), reused by the three key classes: each class
-    // is folded into the logits at its own unit before the next one starts
-    float sacc[2][2][NT][4];  // [chain][mt]
+    // one accumulator set, reused by the three key classes: each class is folded
+    // into the logits at its own unit before the next one starts
+    float sacc[2][NT][4];  // [mt]
     float cc[NT][4];
     float lg[NT][2][2];
 #pragma unroll
@@ -414,19 +405,15 @@ struct Decoder {
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float sc = sacc[0][mt][nt][2 * r] + sacc[0][mt][nt][2 * r + 1] + sacc[1][mt][nt][2 * r] +
-                             sacc[1][mt][nt][2 * r + 1];
-            lg[nt][mt][r] = fmaf(sc, code_unit(2 << c, mt, r), lg[nt][mt][r]);
-          }
+          for (int r = 0; r < 2; ++r)
+            lg[nt][mt][r] = fmaf(sacc[mt][nt][2 * r] + sacc[mt][nt][2 * r + 1], code_unit(2 << c, mt, r),
+                                 lg[nt][mt][r]);
     };
     auto zero = [&]() {
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) { sacc[h][0][nt][i] = 0.f; sacc[h][1][nt][i] = 0.f; }
+        for (int i = 0; i < 4; ++i) { sacc[0][nt][i] = 0.f; sacc[1][nt][i] = 0.f; }
     };
     int kt = 0;
     zero();
