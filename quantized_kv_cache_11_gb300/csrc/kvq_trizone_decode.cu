@@ -239,6 +239,7 @@ struct Decoder {
   template <int BITS>
   __device__ __forceinline__ void key_class(const uint32_t* sub, int ktc, int& kt, const uint32_t* kmt,
                                             float (&sacc)[2][NT][4], float (&cc)[NT][4]) const {
+#pragma unroll 4
     for (int j = 0; j < ktc; ++j, ++kt) key_tile<BITS>(sub, j, kt, kmt, sacc[0], sacc[1], cc);
   }
 
