@@ -51,25 +51,25 @@ __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
 }
 
 // code = clamp(rint(fl(d / scale))), d = fl(x - zero), every op round-to-nearest.
-// Fast path: y = fl(d * fl(1/scale)).  With Q = d / scale exact, y and the rounded
-// quotient fl(Q) each lie within 2^-23 |Q| of Q, and 0 <= Q < 2^9 here (d <= max -
-// min and scale is that range over 2^b - 1, up to fp16 rounding of the scale), so
-// |y - fl(Q)| < 2^-13: y rounds to the same integer as fl(Q) unless y is within
-// 2^-13 of a half-integer.  Those rare y (window 2^-11, four times the bound) take
-// the exact IEEE division, so the code is bit-identical to the division.
-// Rounding to an integer, ties to even: for 0 <= y < 2^22, y + 1.5 * 2^23 is
-// rounded to a whole number by the fp32 addition itself (the sum's ulp is 1),
-// and its low mantissa bits are that number.
+// Fast path: y = d * fl(1/scale), the exact product inside an FMA.  With Q = d /
+// scale exact, y and the rounded quotient fl(Q) each lie within 2^-24 |Q| (1 + e)
+// of Q, and 0 <= Q < 2^9 here (d <= max - min and scale is that range over 2^b - 1,
+// up to fp16 rounding of the scale), so |y - fl(Q)| < 2^-14: y rounds to the same
+// integer as fl(Q) unless y is within 2^-14 of a half-integer.  Those rare y (window
+// 2^-11, eight times the bound) take the exact IEEE division, so the code is
+// bit-identical to the division.
+// Rounding to an integer, ties to even: for 0 <= y < 2^22, fma(d, inv, 1.5 * 2^23)
+// rounds y + 1.5 * 2^23 once to a whole number (the sum's ulp is 1), and its low
+// mantissa bits are that number; fma(d, inv, -that number) is y's distance to it.
 constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23
 constexpr uint32_t kRoundMagicBits = 0x4B400000u;
-// The code clamped to [0, cmax] (cmax = 2^b - 1) from y = fl(d * inv), and
-// whether y lies in the window near a half-integer where the exact quotient must
-// decide.  No branch: a zero scale has inv = 0, so y = 0 and the code is 0.
+// The code clamped to [0, cmax] (cmax = 2^b - 1) from y = d * inv, and whether y
+// lies in the window near a half-integer where the exact quotient must decide.
+// No branch: a zero scale has inv = 0, so y = 0 and the code is 0.
 __device__ __forceinline__ uint32_t quant_code_fast(float x, const GroupParams& p, uint32_t cmax, bool& near_tie) {
   const float d = __fsub_rn(x, p.zero);  // >= 0
-  const float q = __fmul_rn(d, p.inv);
-  const float t = __fadd_rn(q, kRoundMagic);
-  near_tie = fabsf(__fsub_rn(q, __fsub_rn(t, kRoundMagic))) > 0.5f - 0x1p-11f;
+  const float t = __fmaf_rn(d, p.inv, kRoundMagic);
+  near_tie = fabsf(__fmaf_rn(d, p.inv, -__fsub_rn(t, kRoundMagic))) > 0.5f - 0x1p-11f;
   const uint32_t c = __float_as_uint(t) - kRoundMagicBits;
   return c > cmax ? cmax : c;
 }
