@@ -168,6 +168,37 @@ def test_append_flush_matches_oracle(bits, R):
     assert cache.device_errors() == 0
 
 
+def test_append_flush_at_max_batch():
+    # KVQ_MAX_BATCH sequences of ragged lengths, each appended 40 tokens: every
+    # sequence crosses at least one flush (tail ring of 32)
+    B = kvq.KVQ_MAX_BATCH
+    w = S.SERVING.scaled(batch=B, n_kv_heads=1, n_q_heads=4, context=120, tail_cap=32,
+                         ragged=(1, 60), bits=2)
+    inp = S.generate(w)
+    inp["n_tail"] = (inp["seq_len"] % 32).astype(np.int32)
+    cache = H.device_cache(w, inp, 2, max_tokens=120, tail_cap=32)
+    K = torch.from_numpy(inp["K"]).cuda()
+    V = torch.from_numpy(inp["V"]).cuda()
+    seq = inp["seq_len"].astype(int).copy()
+    nq = (inp["seq_len"] - inp["n_tail"]).astype(int)
+    ntl = inp["n_tail"].astype(int).copy()
+    rows = torch.arange(B, device="cuda")
+    for step in range(40):
+        idx = torch.tensor(seq, device="cuda")
+        cache.append(K[rows, idx].contiguous(), V[rows, idx].contiguous())
+        for b in range(B):
+            nq[b], ntl[b], _ = O.append_lengths(nq[b], ntl[b], 32)
+        seq += 1
+    torch.cuda.synchronize()
+    assert cache.device_errors() == 0
+    st_inp = dict(inp, seq_len=seq.astype(np.int32), n_tail=ntl.astype(np.int32))
+    states = H.oracle_states(st_inp, 2)
+    H.assert_buffers_equal(cache, states)
+    q = torch.from_numpy(inp["q"]).cuda()
+    out = cache.decode(q, w.sm_scale).cpu().numpy()
+    H.assert_close(out, H.oracle_decode(inp["q"], states, w.sm_scale))
+
+
 def test_append_past_capacity_sets_error_and_leaves_sequence():
     w = S.LLAMA31_8B_128K.scaled(batch=1, context=64, n_tail=32, tail_cap=32)
     inp = S.generate(w)
@@ -223,6 +254,12 @@ SHAPES = {
                                                ragged=(0, 260), bits=4), 4),
     "seg_320_d128_2bit_gqa8": (S.SERVING.scaled(batch=40, n_kv_heads=8, n_q_heads=64, context=160,
                                                 ragged=(30, 160), bits=2), 2),
+    # the largest batch one call takes (KVQ_MAX_BATCH sequences): the prefill's
+    # per-sequence tables and the decode's shared-memory prefix sums at their limit
+    "seg_512_d128_2bit_maxbatch": (S.SERVING.scaled(batch=kvq.KVQ_MAX_BATCH, n_kv_heads=1, n_q_heads=4,
+                                                    context=70, ragged=(1, 70), bits=2), 2),
+    "seg_1024_d64_4bit_maxbatch": (S.SERVING.scaled(batch=kvq.KVQ_MAX_BATCH, n_kv_heads=2, n_q_heads=4,
+                                                    head_dim=64, context=40, ragged=(0, 40), bits=4), 4),
 }
 
 
@@ -233,10 +270,12 @@ def test_many_segments_match_oracle(name):
     if w.ragged is not None:
         inp["n_tail"] = (inp["seq_len"] % 32).astype(np.int32)
     cache = H.device_cache(w, inp, bits)
+    states = H.oracle_states(inp, bits)
+    H.assert_buffers_equal(cache, states)
     q = torch.from_numpy(inp["q"]).cuda()
     out = cache.decode(q, w.sm_scale).cpu().numpy()
     assert cache.device_errors() == 0
-    ref = H.oracle_decode(inp["q"], H.oracle_states(inp, bits), w.sm_scale)
+    ref = H.oracle_decode(inp["q"], states, w.sm_scale)
     H.assert_close(out, ref)
     # a second call gives identical bits (the merge counters were left at zero)
     out2 = cache.decode(q, w.sm_scale).cpu().numpy()
