@@ -150,6 +150,26 @@ def test_ragged_lengths_and_empty_sequences():
     H.assert_close(out, oracle_out(w, inp, t_old, n_fresh))
 
 
+@pytest.mark.parametrize("case", ["aligned_ragged", "stream_k_many_segments"])
+def test_decode_partitions(case):
+    # the two partitions of the decode's CTAs: a few segments of unequal length
+    # (each gets CTAs of its own, in proportion to its work) and more segments
+    # than CTAs (a CTA's range crosses segment boundaries, merged by the split-K
+    # counters); every segment against the oracle
+    if case == "aligned_ragged":
+        w = W.scaled(batch=6, n_kv_heads=2, n_q_heads=8, context=3000, trizone_fresh=20)
+        t_old, n_fresh = [2980, 2500, 1200, 400, 2900, 60], [20, 3, 0, 20, 11, 1]
+    else:
+        w = W.scaled(batch=40, n_kv_heads=8, n_q_heads=32, context=200, trizone_fresh=8)
+        t_old, n_fresh = None, None
+    inp, t_old, n_fresh, cache = run_case(w, t_old, n_fresh)
+    q = torch.from_numpy(inp["q"]).cuda()
+    out = cache.decode(q, w.sm_scale).cpu().numpy()
+    assert cache.device_errors() == 0
+    H.assert_close(out, oracle_out(w, inp, t_old, n_fresh))
+    assert torch.equal(torch.from_numpy(out), cache.decode(q, w.sm_scale).cpu())
+
+
 def test_decode_repeatable_and_workspace_reset():
     # the blocks are dealt to warps the same way on every call: identical results
     w, inp, t_old, n_fresh, cache = run_named("mix")
