@@ -5,11 +5,14 @@
 // (fp16 values) and zone C (fp16 fresh tokens), so the cache is never expanded.
 //
 // How:
-// * Work partition (stream-K): every block of every (sequence, KV head) weighs
-//   a few units by kind (the decode of a block costs about the same for every
-//   value width: the arithmetic, not the record's bytes, sets its time); the
-//   units of all segments are laid end to end and cut into equal ranges, one
-//   per resident CTA.  A CTA owns the blocks whose first unit falls in its range.
+// * Work partition: every block of every (sequence, KV head) weighs a few units
+//   by kind (the decode of a block costs about the same for every value width:
+//   the arithmetic, not the record's bytes, sets its time).  When each segment's
+//   share of the resident CTAs rounds down to a whole number within 15%, every
+//   segment gets that many CTAs of its own, each an equal range of its units;
+//   otherwise (stream-K) the units of all segments are laid end to end and cut
+//   into equal ranges, one per resident CTA.  A CTA owns the blocks whose first
+//   unit falls in its range.
 // * Inside a CTA the warps deal the CTA's blocks of the current segment round
 //   robin (blocks are stored by kind, so every warp gets a similar mix of sizes,
 //   and the assignment -- hence the summation order -- is the same on every
