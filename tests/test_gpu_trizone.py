@@ -150,7 +150,7 @@ def test_ragged_lengths_and_empty_sequences():
     H.assert_close(out, oracle_out(w, inp, t_old, n_fresh))
 
 
-@pytest.mark.parametrize("case", ["aligned_ragged", "stream_k_many_segments"])
+@pytest.mark.parametrize("case", ["aligned_ragged", "stream_k_many_segments", "max_segments"])
 def test_decode_partitions(case):
     # the two partitions of the decode's CTAs: a few segments of unequal length
     # (each gets CTAs of its own, in proportion to its work) and more segments
@@ -159,8 +159,12 @@ def test_decode_partitions(case):
     if case == "aligned_ragged":
         w = W.scaled(batch=6, n_kv_heads=2, n_q_heads=8, context=3000, trizone_fresh=20)
         t_old, n_fresh = [2980, 2500, 1200, 400, 2900, 60], [20, 3, 0, 20, 11, 1]
-    else:
+    elif case == "stream_k_many_segments":
         w = W.scaled(batch=40, n_kv_heads=8, n_q_heads=32, context=200, trizone_fresh=8)
+        t_old, n_fresh = None, None
+    else:  # KVQ_TZ_MAX_SEGMENTS (sequence, KV head) segments
+        w = W.scaled(batch=kvq.KVQ_TZ_MAX_SEGMENTS // 8, n_kv_heads=8, n_q_heads=32, context=100,
+                     trizone_fresh=4)
         t_old, n_fresh = None, None
     inp, t_old, n_fresh, cache = run_case(w, t_old, n_fresh)
     q = torch.from_numpy(inp["q"]).cuda()
