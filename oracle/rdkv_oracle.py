@@ -111,10 +111,6 @@ def budget_bits(avg_bits: float, n_units: int) -> int:
     return int(math.floor(float(avg_bits) * float(n_units)))
 
 
-def _f32(x) -> np.float32:
-    return np.float32(x)
-
-
 def choose(W: np.ndarray, lam_bits: int, widths) -> np.ndarray:
     """Per unit, the width minimising fl32(fl32(W 2^-b) + fl32(lam b)); ties go to
     the smaller width (widths ascending).  W float32 [N]."""
