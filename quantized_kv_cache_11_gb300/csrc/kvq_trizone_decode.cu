@@ -117,9 +117,18 @@ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
 // end of a ~58 us launch, against 5.6% more work per CTA when aligned.
 constexpr int kAlignSlack = 115;
 
-// Work units of one block of each kind (value width 2, 4, 8, 16, fresh):
-// measured decode time per block, in steps of about a tenth.
-__constant__ int c_kind_units[kKinds] = {10, 10, 11, 12, 12};
+// Work units of one block of each kind (value width 2, 4, 8, 16, fresh) with
+// 9 key k-tiles: measured decode time per block, in steps of about a hundredth;
+// each key k-tile more or fewer adds or takes kKtUnits to a quantized block
+// (measured: segments of 10 k-tiles took 7% longer than those of 9).
+__constant__ int c_kind_units[kKinds] = {100, 100, 110, 120, 120};
+constexpr int kKtUnits = 7;
+
+__device__ __forceinline__ int kind_units(int k, const int32_t* hd) {
+  int kt = hd[H_KT] + hd[H_KT + 1] + hd[H_KT + 2];
+  kt = kt < 0 ? 0 : (kt > kKtMax ? kKtMax : kt);  // clamped: the index is checked later
+  return k < 4 ? c_kind_units[k] + kKtUnits * (kt - 9) : c_kind_units[k];
+}
 
 // Work units of a segment as the partition sees it: its blocks by kind (block
 // counts clamped so that a corrupt index cannot overflow the prefix), at least 1.
@@ -129,7 +138,7 @@ __device__ __forceinline__ int64_t seg_weight(const Params& p, int s) {
 #pragma unroll
   for (int k = 0; k < kKinds; ++k) {
     const int n = hd[H_NBLK + k];
-    w += (int64_t)(n < 0 ? 0 : (n > (1 << 24) ? (1 << 24) : n)) * c_kind_units[k];
+    w += (int64_t)(n < 0 ? 0 : (n > (1 << 24) ? (1 << 24) : n)) * kind_units(k, hd);
   }
   return w > 0 ? w : 1;
 }
@@ -638,9 +647,24 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
     }
     if (lane == 0) s_pref[0] = 0;
     __syncwarp();
-    // the segment-aligned plan (kAlignSlack): c_s per segment, an inclusive scan
-    // of them, and this CTA's segment, index among its c_s and first CTA
+    // the segment-aligned plan (kAlignSlack): c_s per segment, rounded to the
+    // nearest when those fit the slots (the heavier segments take the spare CTAs),
+    // else rounded down; an inclusive scan of them gives this CTA's segment, its
+    // index among the c_s and the segment's first CTA
     const int64_t ns = run < p.n_stream ? run : p.n_stream;
+    int64_t nround = 0;
+    for (int s0 = 0; s0 < p.n_seg; s0 += 32) {
+      const int s = s0 + lane;
+      int64_t cs = 0;
+      if (s < p.n_seg) {
+        cs = (2 * ns * (s_pref[s + 1] - s_pref[s]) + run) / (2 * run);
+        if (cs < 1) cs = 1;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, off);
+      nround += cs;
+    }
+    const bool nearest = nround <= ns;
     bool fits = true;
     int64_t cbase = 0;
     if (lane == 0) s_aseg = -1;
@@ -650,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
       int64_t cs = 0;
       if (s < p.n_seg) {
         const int64_t ws = s_pref[s + 1] - s_pref[s];
-        cs = ns * ws / run;
+        cs = nearest ? (2 * ns * ws + run) / (2 * run) : ns * ws / run;
         if (cs < 1) cs = 1;
         if (ws * ns * 100 > (int64_t)kAlignSlack * run * cs) fits = false;
       }
@@ -733,7 +757,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
       int cum = 0;
       for (int k = 0; k < kKinds; ++k) {
         const int n = ok ? s_hdr[H_NBLK + k] : 0;
-        const int wg = c_kind_units[k];
+        const int wg = kind_units(k, s_hdr);
         const int64_t lo64 = a <= cw ? 0 : (a - cw + wg - 1) / wg;
         const int lo = (int)(lo64 < n ? lo64 : n);
         const int64_t hi64 = e <= cw ? 0 : (e - cw + wg - 1) / wg;
