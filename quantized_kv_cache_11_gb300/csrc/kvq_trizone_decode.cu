@@ -7,9 +7,10 @@
 // How:
 // * Work partition: every block of every (sequence, KV head) weighs a few units
 //   by kind (the decode of a block costs about the same for every value width:
-//   the arithmetic, not the record's bytes, sets its time).  When each segment's
-//   share of the resident CTAs rounds down to a whole number within 15%, every
-//   segment gets that many CTAs of its own, each an equal range of its units;
+//   the arithmetic, not the record's bytes, sets its time; a key k-tile more
+//   costs a few units more).  When each segment's share of the resident CTAs
+//   rounds to a whole number within 15%, every segment gets that many CTAs of
+//   its own, each an equal range of its units;
 //   otherwise (stream-K) the units of all segments are laid end to end and cut
 //   into equal ranges, one per resident CTA.  A CTA owns the blocks whose first
 //   unit falls in its range.
@@ -108,9 +109,10 @@ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
   return ((x + 1) * n - 1) / total;
 }
 
-// Segment-aligned partition: segment s gets c_s = max(1, floor(n * w_s / W))
-// CTAs of its own, each an equal share of its units, when no segment's share is
-// more than this many percent of the mean W / n (and the c_s fit in n).  A CTA
+// Segment-aligned partition: segment s gets c_s = max(1, round(n * w_s / W))
+// CTAs of its own (rounded down instead when the rounded shares do not fit in
+// n), each an equal share of its units, when no segment's share is more than
+// this many percent of the mean W / n (and the c_s fit in n).  A CTA
 // whose range spans two segments (the stream-K cut) pays a second set-up and a
 // second merge, and, as the last arrival of the next segment, its final merge:
 // measured on 32 segments of 65,536 tokens over 304 CTAs that was ~8 us at the
