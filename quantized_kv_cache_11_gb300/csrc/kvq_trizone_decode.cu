@@ -118,6 +118,7 @@ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t total, int64_t n) {
 // measured on 32 segments of 65,536 tokens over 304 CTAs that was ~8 us at the
 // end of a ~58 us launch, against 5.6% more work per CTA when aligned.
 constexpr int kAlignSlack = 115;
+constexpr int kHdrVecBytes = 112;  // header bytes the plan stages (words 0..27)
 
 // Work units of one block of each kind (value width 2, 4, 8, 16, fresh) with
 // 9 key k-tiles: measured decode time per block, in steps of about a hundredth;
@@ -609,6 +610,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last, s_total;
   __shared__ int s_aligned, s_aseg, s_aj, s_acs, s_ac0;  // the segment-aligned plan
+  __shared__ int s_hpre;  // the first 112 header bytes of the CTA's segment already staged
   __shared__ int s_lo[kKinds], s_cum[kKinds + 1];
   __shared__ float s_M[G], s_L[G], s_scale[G];
   uint8_t* rings = smem;
@@ -635,6 +637,17 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
   }
   // weighted prefix over the segments
   if (warp == 0) {
+    // at most 32 segments: lane s also loads the first 112 bytes of segment s's
+    // index record (every field the partition and the copies use), kept for the
+    // segment-aligned plan, which then needs no second round trip for them
+    constexpr int kHdrVec = kHdrVecBytes / 16;
+    const bool few = p.n_seg <= 32;
+    uint4 hw[kHdrVec];
+    if (few && lane < p.n_seg) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.index + (size_t)lane * KVQ_TZ_INDEX_BYTES);
+#pragma unroll
+      for (int i = 0; i < kHdrVec; ++i) hw[i] = src[i];
+    }
     int64_t run = 0;
     for (int s0 = 0; s0 < p.n_seg; s0 += 32) {
       const int s = s0 + lane;
@@ -654,6 +667,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
     // else rounded down; an inclusive scan of them gives this CTA's segment, its
     // index among the c_s and the segment's first CTA
     const int64_t ns = run < p.n_stream ? run : p.n_stream;
+    bool mine = false;  // this lane's segment is the CTA's
     int64_t nround = 0;
     for (int s0 = 0; s0 < p.n_seg; s0 += 32) {
       const int s = s0 + lane;
@@ -688,6 +702,7 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
       }
       const int64_t first = cbase + v - cs;
       if (cs > 0 && (int64_t)blockIdx.x >= first && (int64_t)blockIdx.x < first + cs) {
+        mine = true;
         s_aseg = s;
         s_aj = (int)(blockIdx.x - first);
         s_acs = (int)cs;
@@ -697,6 +712,11 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
     }
     fits = __all_sync(0xffffffffu, fits) && cbase <= ns;
     if (lane == 0) s_aligned = fits ? 1 : 0;
+    if (fits && few && mine) {
+#pragma unroll
+      for (int i = 0; i < kHdrVec; ++i) reinterpret_cast<uint4*>(s_hdr)[i] = hw[i];
+    }
+    if (lane == 0) s_hpre = fits && few ? 1 : 0;
   }
   __syncthreads();
   const int64_t total = s_pref[p.n_seg];
@@ -728,30 +748,27 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
   for (; s < p.n_seg && s_pref[s] < r1; ++s) {
     const int64_t S = s_pref[s], W = s_pref[s + 1] - S;
     const int64_t a = r0 > S ? r0 - S : 0, e = (r1 - S) < W ? r1 - S : W;
-    // ---- segment header, slots, q (slot order and natural order)
-    const uint8_t* idx = p.index + (size_t)s * KVQ_TZ_INDEX_BYTES;
-    if (tid < (128 + 2 * kSlots) / 4) reinterpret_cast<uint32_t*>(s_hdr)[tid] = reinterpret_cast<const uint32_t*>(idx)[tid];
-    __syncthreads();
-    const __half* qh = p.q + (size_t)s * G * kDim;
-    for (int i = tid; i < 4 * NT * C::QPH; i += blockDim.x) {
-      const int g = i / C::QPH, w = i % C::QPH;
-      uint32_t val = 0u;
-      if (g < G && w < 8 * kKtMax) {
-        const int kt = w >> 3, tg = (w >> 1) & 3, r = w & 1;
-        const int sl = 16 * kt + 2 * tg + 8 * r;
-        const int c0 = s_slots[sl], c1 = s_slots[sl + 1];
-        const uint32_t lo16 = c0 >= 0 && c0 < kDim ? (uint32_t)__half_as_ushort(qh[g * kDim + c0]) : 0u;
-        const uint32_t hi16 = c1 >= 0 && c1 < kDim ? (uint32_t)__half_as_ushort(qh[g * kDim + c1]) : 0u;
-        val = lo16 | (hi16 << 16);
+    // ---- segment header (with the slots) and q in natural channel order, in the
+    // pair order of the fragments; with the header's first 112 bytes staged by
+    // the plan, warp 0 cuts this CTA's blocks while the other warps load the rest
+    const bool pre = s_hpre != 0;
+    {
+      const uint8_t* idx = p.index + (size_t)s * KVQ_TZ_INDEX_BYTES;
+      const int lt = pre ? tid - 32 : tid, nth = pre ? (int)blockDim.x - 32 : (int)blockDim.x;
+      if (lt >= 0) {
+        const int w0 = pre ? kHdrVecBytes / 4 : 0;
+        for (int w = w0 + lt; w < (128 + 2 * kSlots) / 4; w += nth)
+          reinterpret_cast<uint32_t*>(s_hdr)[w] = reinterpret_cast<const uint32_t*>(idx)[w];
+        const __half* qh = p.q + (size_t)s * G * kDim;
+        for (int i = lt; i < NT * 4 * (kDim / 2); i += nth) {
+          const int g = i / (kDim / 2), pr = i % (kDim / 2);
+          const int kt = 2 * (pr / 16) + (pr % 4) / 2, tg = (pr % 16) / 4, r = pr % 2;
+          const int ch = 16 * kt + 2 * tg + 8 * r;
+          qn_smem[i] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * kDim + ch) : 0u;
+        }
       }
-      qp_smem[i] = val;
     }
-    for (int i = tid; i < NT * 4 * (kDim / 2); i += blockDim.x) {
-      const int g = i / (kDim / 2), pr = i % (kDim / 2);
-      const int kt = 2 * (pr / 16) + (pr % 4) / 2, tg = (pr % 16) / 4, r = pr % 2;
-      const int ch = 16 * kt + 2 * tg + 8 * r;
-      qn_smem[i] = g < G ? *reinterpret_cast<const uint32_t*>(qh + g * kDim + ch) : 0u;
-    }
+    if (!pre) __syncthreads();
     if (tid == 0) {
       const bool ok = header_ok(s_hdr, p.region);
       if (!ok && p.error_flags != nullptr) atomicOr(p.error_flags, KVQ_DEVERR_BAD_LENGTHS);
@@ -774,7 +791,6 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
     }
     __syncthreads();
     Decoder<G> dec;
-    dec.init(qp_smem, qn_smem);
     // ---- this warp's blocks (round robin), streamed through the ring
     {
       const int ntot = failed ? 0 : s_total;
@@ -821,6 +837,32 @@ __global__ void __launch_bounds__(Cfg<G>::WARPS * 32, Cfg<G>::MIN_CTAS) decode_k
         }
       };
       fill();
+      // q in slot order, gathered from the staged natural copy (channel c sits in
+      // pair 16 (kt / 2) + 4 tg + 2 (kt % 2) + r, c = 16 kt + 2 tg + 8 r + (c & 1)),
+      // while the first copies fly
+      {
+        const __half* qn_h = reinterpret_cast<const __half*>(qn_smem);
+        auto q_at = [&](int g, int ch) -> uint32_t {
+          const int kt = ch >> 4, w16 = ch & 15, r = w16 >> 3, tg = (w16 & 7) >> 1;
+          const int pr = 16 * (kt >> 1) + 4 * tg + 2 * (kt & 1) + r;
+          return (uint32_t)__half_as_ushort(qn_h[2 * (g * (kDim / 2) + pr) + (ch & 1)]);
+        };
+        for (int i = tid; i < 4 * NT * C::QPH; i += blockDim.x) {
+          const int g = i / C::QPH, w = i % C::QPH;
+          uint32_t val = 0u;
+          if (g < G && w < 8 * kKtMax) {
+            const int kt = w >> 3, tg = (w >> 1) & 3, r = w & 1;
+            const int sl = 16 * kt + 2 * tg + 8 * r;
+            const int c0 = s_slots[sl], c1 = s_slots[sl + 1];
+            const uint32_t lo16 = c0 >= 0 && c0 < kDim ? q_at(g, c0) : 0u;
+            const uint32_t hi16 = c1 >= 0 && c1 < kDim ? q_at(g, c1) : 0u;
+            val = lo16 | (hi16 << 16);
+          }
+          qp_smem[i] = val;
+        }
+      }
+      __syncthreads();
+      dec.init(qp_smem, qn_smem);
       while (done < issued) {
         const int slot = done % C::NBAR;
         if (!mbar_wait(bars + slot, (done / C::NBAR) & 1u, kMaxPolls)) { failed = true; break; }
