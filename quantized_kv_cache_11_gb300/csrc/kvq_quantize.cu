@@ -33,6 +33,11 @@ struct PrefillParams {
   int32_t ntail[KVQ_MAX_BATCH];
 };
 
+// Four values <= 255 as the bytes of one word (a in byte 0), by byte permutes.
+__device__ __forceinline__ uint32_t pack4_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
 // One warp quantizes one 32-token tile of keys and values whose rows it stages in
 // shared memory (cp.async, VEC bytes per copy; keys first, then the values in the
 // same buffer, so that twice as many warps fit an SM).  Keys: each lane owns
@@ -103,16 +108,20 @@ __device__ __forceinline__ void quantize_tile_staged(const __half* ksrc, const _
     uint32_t redo = 0u;
 #pragma unroll 4
     for (int t = 0; t < kGroup; ++t) {
-      uint32_t w = 0u;
+      // the codes (each <= 255) gathered into bytes by byte permutes: three per
+      // four codes, against three shifts and two ORs
+      uint32_t h16[NH];  // codes of channel pair j in bytes 0 and 1
       bool near = false;
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
         const __half2 x = *reinterpret_cast<const __half2*>(kr + t * S::PH + c0 + 2 * j);
         bool n0, n1;
-        w |= quant_code_fast(__low2float(x), gp[2 * j], cmax, n0) << (16 * j);
-        w |= quant_code_fast(__high2float(x), gp[2 * j + 1], cmax, n1) << (16 * j + 8);
+        const uint32_t a = quant_code_fast(__low2float(x), gp[2 * j], cmax, n0);
+        const uint32_t b = quant_code_fast(__high2float(x), gp[2 * j + 1], cmax, n1);
+        h16[j] = __byte_perm(a, b, 0x0040);
         near = near || n0 || n1;
       }
+      const uint32_t w = NH == 2 ? __byte_perm(h16[0], h16[NH - 1], 0x5410) : h16[0];
       redo |= (uint32_t)near << t;
       if (CPL == 4) *reinterpret_cast<uint32_t*>(ct + t * S::PC + c0) = w;
       else *reinterpret_cast<uint16_t*>(ct + t * S::PC + c0) = (uint16_t)w;
@@ -166,7 +175,7 @@ __device__ __forceinline__ void quantize_tile_staged(const __half* ksrc, const _
         const uint32_t c2 = quant_code_fast(__low2float(h[2 * w4 + 1]), gp, cmax, n2);
         const uint32_t c3 = quant_code_fast(__high2float(h[2 * w4 + 1]), gp, cmax, n3);
         redo |= (uint32_t)(n0 || n1 || n2 || n3) << w4;
-        *reinterpret_cast<uint32_t*>(ct + t * S::PC + 32 * j + 4 * w4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+        *reinterpret_cast<uint32_t*>(ct + t * S::PC + 32 * j + 4 * w4) = pack4_bytes(c0, c1, c2, c3);
       }
 #pragma unroll 1
       while (redo != 0u) {
@@ -328,7 +337,7 @@ __device__ __forceinline__ void quantize_tile_coop(const __half* ksrc, const __h
       const uint32_t c2 = quant_code_fast(__low2float(h[2 * w4 + 1]), gp, cmax, n2);
       const uint32_t c3 = quant_code_fast(__high2float(h[2 * w4 + 1]), gp, cmax, n3);
       redo |= (uint32_t)(n0 || n1 || n2 || n3) << w4;
-      *reinterpret_cast<uint32_t*>(ct + t * S::PC + 32 * j + 4 * w4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      *reinterpret_cast<uint32_t*>(ct + t * S::PC + 32 * j + 4 * w4) = pack4_bytes(c0, c1, c2, c3);
     }
 #pragma unroll 1
     while (redo != 0u) {
