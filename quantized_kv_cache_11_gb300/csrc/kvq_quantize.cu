@@ -33,11 +33,6 @@ struct PrefillParams {
   int32_t ntail[KVQ_MAX_BATCH];
 };
 
-// Four values <= 255 as the bytes of one word (a in byte 0), by byte permutes.
-__device__ __forceinline__ uint32_t pack4_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
-}
-
 // One warp quantizes one 32-token tile of keys and values whose rows it stages in
 // shared memory (cp.async, VEC bytes per copy; keys first, then the values in the
 // same buffer, so that twice as many warps fit an SM).  Keys: each lane owns

@@ -173,11 +173,13 @@ __global__ void __launch_bounds__(kIndexThreads) index_kernel(const __grid_const
 // every row, then waits for all of them.
 template <typename TokOf>
 __device__ __forceinline__ void stage_rows(__half* rows, const __half* base, int64_t st, int n, TokOf tok_of,
-                                           int lane) {
+                                           int lane, bool replicate = false) {
+  const int tok0 = tok_of(0);
 #pragma unroll 8
   for (int t = 0; t < kGroup; ++t) {
     const int tok = tok_of(t);
     if (t < n) cp_async_8(rows + t * kDim + 4 * lane, base + (int64_t)tok * st + 4 * lane);
+    else if (replicate && n > 0) cp_async_8(rows + t * kDim + 4 * lane, base + (int64_t)tok0 * st + 4 * lane);
     else *reinterpret_cast<uint2*>(rows + t * kDim + 4 * lane) = make_uint2(0u, 0u);
   }
   cp_async_commit();
@@ -254,67 +256,87 @@ template <int C>
 __device__ __forceinline__ void quantize_values(const __half* rows, int n, uint8_t* ct, __half* vm, float* vinv,
                                                 int lane) {
   const int c0 = 4 * lane, j = lane / 8;
+  constexpr uint32_t cmax = (1u << C) - 1u;
+  // min/max of group j of every token: reduced over the group's 8 lanes; lane
+  // t % 8 keeps token t's (slot t / 8)
+  float rmn[4], rmx[4];
+#pragma unroll
   for (int t = 0; t < kGroup; ++t) {
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + c0);
     const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
-    float mn = fminf(fminf(__low2float(lo), __high2float(lo)), fminf(__low2float(hi), __high2float(hi)));
-    float mx = fmaxf(fmaxf(__low2float(lo), __high2float(lo)), fmaxf(__low2float(hi), __high2float(hi)));
+    const __half2 m2 = __hmin2(lo, hi), x2 = __hmax2(lo, hi);
+    float mn = fminf(__low2float(m2), __high2float(m2));
+    float mx = fmaxf(__low2float(x2), __high2float(x2));
 #pragma unroll
     for (int off = 1; off < 8; off <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     }
     if ((lane & 7) == (t & 7)) {
-      if (t < n) {
-        const GroupParams g = group_params<C>(mn, mx);
-        vm[j * kGroup + t] = g.scale_h;
-        vm[kDim + j * kGroup + t] = g.zero_h;
-        vinv[j * kGroup + t] = g.inv;
-      } else {
-        vm[j * kGroup + t] = __float2half_rn(0.f);
-        vm[kDim + j * kGroup + t] = __float2half_rn(0.f);
-        vinv[j * kGroup + t] = 0.f;
-      }
+      rmn[t >> 3] = mn;
+      rmx[t >> 3] = mx;
     }
   }
+  // the parameters of tokens lane % 8 + 8k of group j, every lane busy
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int t = (lane & 7) + 8 * k;
+    GroupParams g = group_params<C>(rmn[k], rmx[k]);
+    if (t >= n) {
+      g.scale_h = __float2half_rn(0.f);
+      g.zero_h = __float2half_rn(0.f);
+      g.inv = 0.f;
+    }
+    vm[j * kGroup + t] = g.scale_h;
+    vm[kDim + j * kGroup + t] = g.zero_h;
+    vinv[j * kGroup + t] = g.inv;
+  }
   __syncwarp();
+  // the codes without a branch; bit t of `redo`: one of the lane's four codes of
+  // token t lies near a rounding tie, and those four are redone with the exact
+  // quotient afterwards
+  uint32_t redo = 0u;
+#pragma unroll 4
   for (int t = 0; t < kGroup; ++t) {
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + c0);
     const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
-    const float x[4] = {__low2float(lo), __high2float(lo), __low2float(hi), __high2float(hi)};
     GroupParams g;
     g.scale = __half2float(vm[j * kGroup + t]);
     g.zero = __half2float(vm[kDim + j * kGroup + t]);
     g.inv = vinv[j * kGroup + t];
-    // the four codes without a branch, then the exact quotient for all four in the
-    // rare case that one of them lies near a rounding tie
-    constexpr uint32_t cmax = (1u << C) - 1u;
-    uint32_t c[4];
-    bool near = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      bool ni;
-      c[i] = quant_code_fast(x[i], g, cmax, ni);
-      near = near || ni;
-    }
-    if (near) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] = quant_code_exact(x[i], g.scale, g.zero, cmax);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ct[t * kDim + c0 + i] = t < n ? (uint8_t)c[i] : (uint8_t)0;
+    bool n0, n1, n2, n3;
+    const uint32_t q0 = quant_code_fast(__low2float(lo), g, cmax, n0);
+    const uint32_t q1 = quant_code_fast(__high2float(lo), g, cmax, n1);
+    const uint32_t q2 = quant_code_fast(__low2float(hi), g, cmax, n2);
+    const uint32_t q3 = quant_code_fast(__high2float(hi), g, cmax, n3);
+    redo |= (uint32_t)((n0 || n1 || n2 || n3) && t < n) << t;
+    *reinterpret_cast<uint32_t*>(ct + t * kDim + c0) = t < n ? pack4_bytes(q0, q1, q2, q3) : 0u;
+  }
+#pragma unroll 1
+  while (redo != 0u) {
+    const int t = __ffs(redo) - 1;
+    redo &= redo - 1u;
+    const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + c0);
+    const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
+    const float sc = __half2float(vm[j * kGroup + t]), ze = __half2float(vm[kDim + j * kGroup + t]);
+    *reinterpret_cast<uint32_t*>(ct + t * kDim + c0) =
+        pack4_bytes(quant_code_exact(__low2float(lo), sc, ze, cmax), quant_code_exact(__high2float(lo), sc, ze, cmax),
+                    quant_code_exact(__low2float(hi), sc, ze, cmax), quant_code_exact(__high2float(hi), sc, ze, cmax));
   }
   __syncwarp();
 }
 
 // The lane's 4 key channels d0..d0+3 over the block's n tokens, each at its own
 // width: fp16 min/max on half2, then the parameters and the codes (to ct at the
-// channels' slots).
+// channels' slots).  The rows past n hold copies of row 0 (stage_rows with
+// replicate), so the min/max over all 32 rows is that over the n tokens; their
+// codes are stored as 0.
 __device__ __forceinline__ void key_channels(const __half* rows, int n, int d0, const uint8_t* slot_of,
                                              const uint8_t* kw, uint8_t* ct, __half* ksc, __half* kze) {
   __half2 mn0 = *reinterpret_cast<const __half2*>(rows + d0), mn1 = *reinterpret_cast<const __half2*>(rows + d0 + 2);
   __half2 mx0 = mn0, mx1 = mn1;
-  for (int t = 1; t < n; ++t) {
+#pragma unroll 8
+  for (int t = 1; t < kGroup; ++t) {
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + d0);
     const __half2 a = u32_as_h2(raw.x), b = u32_as_h2(raw.y);
     mn0 = __hmin2(mn0, a); mx0 = __hmax2(mx0, a);
@@ -333,24 +355,33 @@ __device__ __forceinline__ void key_channels(const __half* rows, int n, int d0, 
     ksc[slot[i]] = g[i].scale_h;
     kze[slot[i]] = g[i].zero_h;
   }
-  for (int t = 0; t < n; ++t) {
+  // the codes without a branch; bit t of `redo`: one of the lane's four codes of
+  // token t lies near a rounding tie (those four are redone with the exact
+  // quotient afterwards)
+  uint32_t redo = 0u;
+#pragma unroll 4
+  for (int t = 0; t < kGroup; ++t) {
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + d0);
     const float x[4] = {__low2float(u32_as_h2(raw.x)), __high2float(u32_as_h2(raw.x)), __low2float(u32_as_h2(raw.y)),
                         __high2float(u32_as_h2(raw.y))};
-    uint32_t c[4];
     bool near = false;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       bool ni;
-      c[i] = quant_code_fast(x[i], g[i], cmax[i], ni);
+      const uint32_t c = quant_code_fast(x[i], g[i], cmax[i], ni);
       near = near || ni;
+      ct[t * kSlots + slot[i]] = t < n ? (uint8_t)c : (uint8_t)0;
     }
-    if (near) {
+    redo |= (uint32_t)(near && t < n) << t;
+  }
+#pragma unroll 1
+  while (redo != 0u) {
+    const int t = __ffs(redo) - 1;
+    redo &= redo - 1u;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] = quant_code_exact(x[i], g[i].scale, g[i].zero, cmax[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ct[t * kSlots + slot[i]] = (uint8_t)c[i];
+    for (int i = 0; i < 4; ++i)
+      ct[t * kSlots + slot[i]] =
+          (uint8_t)quant_code_exact(__half2float(rows[t * kDim + d0 + i]), g[i].scale, g[i].zero, cmax[i]);
   }
 }
 
@@ -412,7 +443,7 @@ __global__ void __launch_bounds__(kBlockWarps * 32) block_kernel(const __grid_co
     ksc[i] = __float2half_rn(0.f);
     kze[i] = __float2half_rn(0.f);
   }
-  stage_rows(rows, kseq, p.st, n, tok, lane);
+  stage_rows(rows, kseq, p.st, n, tok, lane, true);
   key_channels(rows, n, 4 * lane, s_slot_of, s_kw, ct, ksc, kze);
   __syncwarp();
   const int kt2 = s_hdr[H_KT], kt4 = s_hdr[H_KT + 1], kt8 = s_hdr[H_KT + 2], KT = kt2 + kt4 + kt8;
