@@ -79,16 +79,30 @@ __global__ void __launch_bounds__(kIndexThreads) index_kernel(const __grid_const
   int32_t* toks = p.tokens + seg * p.max_old;
   bool bad = false;
 
-  // ---- kept old tokens, grouped by value width (stable)
-  const int chunk = (t_old + kIndexThreads - 1) / kIndexThreads;
+  // ---- kept old tokens, grouped by value width (stable).  Each thread takes a
+  // contiguous chunk (a multiple of 16 tokens), read 16 widths per load when the
+  // width row is 16-byte aligned
+  const int chunk = ((t_old + kIndexThreads - 1) / kIndexThreads + 15) & ~15;
   const int t0 = min(t_old, tid * chunk), t1 = min(t_old, t0 + chunk);
+  const bool v16 = (reinterpret_cast<uintptr_t>(vw) & 15) == 0;
+  auto each_width = [&](auto&& f) {
+    int t = t0;
+    if (v16)
+      for (; t + 16 <= t1; t += 16) {
+        const uint4 q = *reinterpret_cast<const uint4*>(vw + t);
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) f(t + k, (int)((w4[k >> 2] >> (8 * (k & 3))) & 0xFFu));
+      }
+    for (; t < t1; ++t) f(t, (int)vw[t]);
+  };
   int cnt[4] = {0, 0, 0, 0};
-  for (int t = t0; t < t1; ++t) {
-    const int c = v_class(vw[t]);
+  each_width([&](int, int w) {
+    const int c = v_class(w);
     bad |= c == -2;
 #pragma unroll
     for (int i = 0; i < 4; ++i) cnt[i] += c == i;
-  }
+  });
   int start[4], ntok[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) start[i] = block_excl_scan(cnt[i], s_warp, ntok[i]);
@@ -98,12 +112,12 @@ __global__ void __launch_bounds__(kIndexThreads) index_kernel(const __grid_const
     start[i] += cls_first;
     cls_first += ntok[i];
   }
-  for (int t = t0; t < t1; ++t) {
-    const int c = v_class(vw[t]);
+  each_width([&](int t, int w) {
+    const int c = v_class(w);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       if (c == i) toks[start[i]++] = t;
-  }
+  });
 
   // ---- channel slots by key width (2, 4, 8), each class padded to 16
   for (int i = tid; i < kSlots; i += blockDim.x) s_slots[i] = -1;
