@@ -15,7 +15,7 @@
 namespace kvq {
 namespace tz {
 
-constexpr int kIndexThreads = 256;
+constexpr int kIndexThreads = 1024;
 constexpr int kBlockWarps = 4;
 // per-warp scratch of the block kernel: 32 staged fp16 rows, codes by slot,
 // key scale/zero by slot, value metadata, value reciprocal scales
@@ -67,7 +67,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& total) {
 }
 
 // grid (Hkv, B), kIndexThreads threads.
-__global__ void __launch_bounds__(kIndexThreads) index_kernel(const __grid_constant__ BuildParams p) {
+__global__ void __launch_bounds__(kIndexThreads, 1) index_kernel(const __grid_constant__ BuildParams p) {
   __shared__ int16_t s_slots[kSlots];
   __shared__ int s_warp[kIndexThreads / 32];
   __shared__ int s_hdr[32];
