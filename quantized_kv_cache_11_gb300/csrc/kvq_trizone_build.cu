@@ -16,7 +16,7 @@ namespace kvq {
 namespace tz {
 
 constexpr int kIndexThreads = 1024;
-constexpr int kBlockWarps = 4;
+constexpr int kBlockWarps = 5;
 // per-warp scratch of the block kernel: 32 staged fp16 rows, codes by slot,
 // key scale/zero by slot, value metadata, value reciprocal scales
 constexpr int kRowsBytes = kGroup * kDim * 2;
