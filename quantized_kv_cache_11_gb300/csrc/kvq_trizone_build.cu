@@ -272,30 +272,43 @@ __device__ __forceinline__ void quantize_values(const __half* rows, int n, uint8
   const int c0 = 4 * lane, j = lane / 8;
   constexpr uint32_t cmax = (1u << C) - 1u;
   // min/max of group j of every token: reduced over the group's 8 lanes; lane
-  // t % 8 keeps token t's (slot t / 8)
-  float rmn[4], rmx[4];
+  // t % 8 keeps token t's.  Eight tokens per pass, the kept pair shifted into
+  // rmn / rmx (after the four passes slot 3 - k holds token lane % 8 + 8k), so
+  // the pass loop stays rolled without indexing registers
+  float rmn[4] = {0.f, 0.f, 0.f, 0.f}, rmx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int t8 = 0; t8 < kGroup; t8 += 8) {
+    float kmn = 0.f, kmx = 0.f;
 #pragma unroll
-  for (int t = 0; t < kGroup; ++t) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + c0);
-    const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
-    const __half2 m2 = __hmin2(lo, hi), x2 = __hmax2(lo, hi);
-    float mn = fminf(__low2float(m2), __high2float(m2));
-    float mx = fmaxf(__low2float(x2), __high2float(x2));
+    for (int u = 0; u < 8; ++u) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(rows + (t8 + u) * kDim + c0);
+      const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
+      const __half2 m2 = __hmin2(lo, hi), x2 = __hmax2(lo, hi);
+      float mn = fminf(__low2float(m2), __high2float(m2));
+      float mx = fmaxf(__low2float(x2), __high2float(x2));
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      for (int off = 1; off < 8; off <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      }
+      if ((lane & 7) == u) {
+        kmn = mn;
+        kmx = mx;
+      }
     }
-    if ((lane & 7) == (t & 7)) {
-      rmn[t >> 3] = mn;
-      rmx[t >> 3] = mx;
+#pragma unroll
+    for (int k = 3; k > 0; --k) {
+      rmn[k] = rmn[k - 1];
+      rmx[k] = rmx[k - 1];
     }
+    rmn[0] = kmn;
+    rmx[0] = kmx;
   }
   // the parameters of tokens lane % 8 + 8k of group j, every lane busy
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int t = (lane & 7) + 8 * k;
-    GroupParams g = group_params<C>(rmn[k], rmx[k]);
+    GroupParams g = group_params<C>(rmn[3 - k], rmx[3 - k]);
     if (t >= n) {
       g.scale_h = __float2half_rn(0.f);
       g.zero_h = __float2half_rn(0.f);
