@@ -323,7 +323,7 @@ __device__ __forceinline__ void quantize_values(const __half* rows, int n, uint8
   // token t lies near a rounding tie, and those four are redone with the exact
   // quotient afterwards
   uint32_t redo = 0u;
-#pragma unroll 4
+#pragma unroll 2
   for (int t = 0; t < kGroup; ++t) {
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + c0);
     const __half2 lo = u32_as_h2(raw.x), hi = u32_as_h2(raw.y);
@@ -386,7 +386,7 @@ __device__ __forceinline__ void key_channels(const __half* rows, int n, int d0, 
   // token t lies near a rounding tie (those four are redone with the exact
   // quotient afterwards)
   uint32_t redo = 0u;
-#pragma unroll 4
+#pragma unroll 2
   for (int t = 0; t < kGroup; ++t) {
     const uint2 raw = *reinterpret_cast<const uint2*>(rows + t * kDim + d0);
     const float x[4] = {__low2float(u32_as_h2(raw.x)), __high2float(u32_as_h2(raw.x)), __low2float(u32_as_h2(raw.y)),
